@@ -1,0 +1,284 @@
+/*
+ * oracle.c -- plain, slow CPU reference of the Q4_K mixture-of-experts FFN.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * CPU-baseline leg of bench.py load this library.  It shares no code,
+ * header, table or constant with the CUDA path in
+ * quantized_moe_expert_gemv_gb300/csrc/, and neither side includes the other.
+ *
+ * What it computes (the method, as the sparkinfer pages describe it):
+ *   sparkinfer README (luciferlive112116), "Layout" table: the kernels
+ *   directory holds a "fused quantized MoE expert FFN", a "decode GEMV" and
+ *   "GGUF dequant"; the moe directory holds a "sync-free MoE router + expert
+ *   dispatch (on-device counts)".  Its opening section keeps experts
+ *   "quantized-resident, dequantized on-read" for greedy bs=1 decode of a
+ *   Q4_K_M GGUF Qwen3-30B-A3B.  The SP-RKINFER README (gittensor-ai-lab),
+ *   "Benchmark - Qwen3.8-27B" prefill note, has the grouped/prefill variant
+ *   dequantize "Q4_K into the GEMM operand on every pass".
+ *
+ * Per token the MoE FFN is
+ *   z      = W_r x (+ bias)                       router logits, E values
+ *   ids    = the k largest z (descending; equal z -> lower expert index)
+ *   w_i    = softmax(z)[ids_i] / sum_j softmax(z)[ids_j]   (renormalised)
+ *   g, u   = W_gate[e] x, W_up[e] x               (I values each)
+ *   h      = silu(g) * u,  silu(g) = g / (1 + exp(-g))
+ *   y      = W_down[e] h                          (H values)
+ *   out    = sum_i w_i y_i
+ * with every expert matrix stored as GGUF Q4_K super-blocks and read as
+ * the fp32 weights the Q4_K decode defines.
+ *
+ * Precision: all products and sums are fp64 over the exact fp32 weights and
+ * the exact fp32 value of each bf16 activation; results are rounded to
+ * fp32 once at the end.  The top-k choice is taken on the logits rounded
+ * to fp32 (the precision the GPU path decides in).
+ *
+ * Q4_K (GGUF) super-block, 144 bytes per 256 weights, byte order:
+ *   bytes 0-1   d     (IEEE binary16, little-endian)
+ *   bytes 2-3   dmin  (IEEE binary16, little-endian)
+ *   bytes 4-15  scales[12]: eight 6-bit scales sc_j and eight 6-bit mins m_j
+ *   bytes 16-143 qs[128]: 4-bit codes q
+ *   sub-block j (j = 0..7) covers weights 32j .. 32j+31 of the block;
+ *   qs[32i + l] holds weight l of sub-block 2i in its low nibble and
+ *   weight l of sub-block 2i+1 in its high nibble;
+ *   j < 4 : sc_j = scales[j] & 63,  m_j = scales[j+4] & 63
+ *   j >= 4: sc_j = (scales[j+4] & 15) | ((scales[j-4] >> 6) << 4)
+ *           m_j  = (scales[j+4] >> 4) | ((scales[j]   >> 6) << 4)
+ *   weight = d * sc_j * q - dmin * m_j
+ *
+ * No function here is tuned: loops follow the definitions one term at a time.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_QK 256
+#define OR_BLOCK_BYTES 144
+
+int or_version(void) { return 1; }
+
+/* IEEE 754 binary16 -> exact double.  1 sign bit, 5 exponent bits (bias 15),
+ * 10 fraction bits; exponent 0 is subnormal (fraction * 2^-24), exponent 31
+ * is inf/nan. */
+double or_half_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int f = h & 1023;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);
+    } else if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + f), e - 25);
+    }
+    return sign ? -v : v;
+}
+
+/* bf16 bit pattern -> exact double (bf16 is the top half of an fp32). */
+double or_bf16_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* The 6-bit scale and min of sub-block j, as the Q4_K format packs them. */
+void or_q4k_scale_min(const uint8_t *scales, int j, int *sc, int *m) {
+    if (j < 4) {
+        *sc = scales[j] & 63;
+        *m = scales[j + 4] & 63;
+    } else {
+        *sc = (scales[j + 4] & 15) | ((scales[j - 4] >> 6) << 4);
+        *m = (scales[j + 4] >> 4) | ((scales[j] >> 6) << 4);
+    }
+}
+
+/* Decode one super-block into 256 fp32 weights.  The value d*sc*q - dmin*m
+ * is formed exactly in fp64 (each product has at most 21 significant bits)
+ * and rounded to fp32 once. */
+static void or_q4k_block(const uint8_t *blk, float *out) {
+    double d = or_half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+    double dmin = or_half_to_double((uint16_t)(blk[2] | (blk[3] << 8)));
+    const uint8_t *scales = blk + 4;
+    const uint8_t *qs = blk + 16;
+    for (int j = 0; j < 8; ++j) {
+        int sc, m;
+        or_q4k_scale_min(scales, j, &sc, &m);
+        int i = j / 2;
+        for (int l = 0; l < 32; ++l) {
+            int byte = qs[32 * i + l];
+            int q = (j % 2 == 0) ? (byte & 15) : (byte >> 4);
+            double w = d * (double)sc * (double)q - dmin * (double)m;
+            out[32 * j + l] = (float)w;
+        }
+    }
+}
+
+void or_q4k_dequant(const uint8_t *blocks, int64_t n_blocks, float *out) {
+    for (int64_t b = 0; b < n_blocks; ++b)
+        or_q4k_block(blocks + b * OR_BLOCK_BYTES, out + b * OR_QK);
+}
+
+/* One row of a Q4_K matrix with `cols` input columns, as fp32 weights. */
+static void or_q4k_row(const uint8_t *row_blocks, int cols, float *out) {
+    or_q4k_dequant(row_blocks, cols / OR_QK, out);
+}
+
+/* Router logits in fp64: z_e = sum_c W_r[e][c] * x_c (+ bias_e). */
+void or_router_logits(const float *router_w, const float *bias, const uint16_t *x_bf16,
+                      int E, int H, double *z) {
+    for (int e = 0; e < E; ++e) {
+        double s = 0.0;
+        for (int c = 0; c < H; ++c)
+            s += (double)router_w[(int64_t)e * H + c] * or_bf16_to_double(x_bf16[c]);
+        if (bias) s += (double)bias[e];
+        z[e] = s;
+    }
+}
+
+/* The k largest of z32, in descending order; equal values -> lower index
+ * first.  Selection by repeated scan: pick the best not yet taken. */
+void or_topk(const float *z32, int E, int k, int32_t *ids) {
+    unsigned char *taken = (unsigned char *)calloc((size_t)E, 1);
+    for (int i = 0; i < k; ++i) {
+        int best = -1;
+        for (int e = 0; e < E; ++e) {
+            if (taken[e]) continue;
+            if (best < 0 || z32[e] > z32[best]) best = e;
+        }
+        taken[best] = 1;
+        ids[i] = best;
+    }
+    free(taken);
+}
+
+/* Renormalised softmax weights of the selected experts: the softmax over
+ * all E logits, divided by its sum over the selected ones. */
+void or_renorm_weights(const double *z, int E, const int32_t *ids, int k, double *w) {
+    double zmax = z[0];
+    for (int e = 1; e < E; ++e)
+        if (z[e] > zmax) zmax = z[e];
+    double total = 0.0;
+    for (int e = 0; e < E; ++e) total += exp(z[e] - zmax);
+    double sel = 0.0;
+    for (int i = 0; i < k; ++i) sel += exp(z[ids[i]] - zmax) / total;
+    for (int i = 0; i < k; ++i) w[i] = (exp(z[ids[i]] - zmax) / total) / sel;
+}
+
+/* Route T tokens: ids [T][k], weights [T][k]; optionally the fp64 logits
+ * [T][E] and each token's margin z_(k) - z_(k+1) (sorted fp64 logits;
+ * +inf when k == E). */
+void or_route_tokens(const float *router_w, const float *bias, const uint16_t *x_bf16,
+                     int T, int E, int H, int k, int32_t *ids, double *w,
+                     double *z_out, double *margin) {
+    double *z = (double *)malloc(sizeof(double) * (size_t)E);
+    float *z32 = (float *)malloc(sizeof(float) * (size_t)E);
+    for (int t = 0; t < T; ++t) {
+        or_router_logits(router_w, bias, x_bf16 + (int64_t)t * H, E, H, z);
+        for (int e = 0; e < E; ++e) z32[e] = (float)z[e];
+        or_topk(z32, E, k, ids + (int64_t)t * k);
+        or_renorm_weights(z, E, ids + (int64_t)t * k, k, w + (int64_t)t * k);
+        if (z_out)
+            for (int e = 0; e < E; ++e) z_out[(int64_t)t * E + e] = z[e];
+        if (margin) {
+            if (k >= E) {
+                margin[t] = INFINITY;
+            } else {
+                /* k-th and (k+1)-th largest fp64 logits by repeated scan */
+                unsigned char *taken = (unsigned char *)calloc((size_t)E, 1);
+                double kth = 0.0, next = 0.0;
+                for (int i = 0; i <= k; ++i) {
+                    int best = -1;
+                    for (int e = 0; e < E; ++e)
+                        if (!taken[e] && (best < 0 || z[e] > z[best])) best = e;
+                    taken[best] = 1;
+                    if (i == k - 1) kth = z[best];
+                    if (i == k) next = z[best];
+                }
+                free(taken);
+                margin[t] = kth - next;
+            }
+        }
+    }
+    free(z);
+    free(z32);
+}
+
+static double or_silu(double g) { return g / (1.0 + exp(-g)); }
+
+/* One expert's SwiGLU FFN in fp64:
+ *   g_r = sum_c Wg[r][c] x_c,  u_r = sum_c Wu[r][c] x_c,  h_r = silu(g_r) u_r,
+ *   y_c = sum_r Wd[c][r] h_r.
+ * wg, wu: this expert's [I][H/256] blocks; wd: its [H][I/256] blocks. */
+void or_expert_ffn(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd,
+                   int H, int I, const double *x, double *h_out, double *y) {
+    float *row = (float *)malloc(sizeof(float) * (size_t)(H > I ? H : I));
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    int64_t gate_row_bytes = (int64_t)(H / OR_QK) * OR_BLOCK_BYTES;
+    int64_t down_row_bytes = (int64_t)(I / OR_QK) * OR_BLOCK_BYTES;
+    for (int r = 0; r < I; ++r) {
+        double g = 0.0, u = 0.0;
+        or_q4k_row(wg + r * gate_row_bytes, H, row);
+        for (int c = 0; c < H; ++c) g += (double)row[c] * x[c];
+        or_q4k_row(wu + r * gate_row_bytes, H, row);
+        for (int c = 0; c < H; ++c) u += (double)row[c] * x[c];
+        h[r] = or_silu(g) * u;
+        if (h_out) h_out[r] = h[r];
+    }
+    for (int c = 0; c < H; ++c) {
+        double s = 0.0;
+        or_q4k_row(wd + c * down_row_bytes, I, row);
+        for (int r = 0; r < I; ++r) s += (double)row[r] * h[r];
+        y[c] = s;
+    }
+    free(row);
+    free(h);
+}
+
+/* The whole MoE FFN for one token.  Outputs: ids [k], w [k], out32 [H]
+ * (fp32-rounded), and optionally out64 [H] and h [k][I] (fp64). */
+void or_moe_token(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down,
+                  const float *router_w, const float *bias, int H, int I, int E, int k,
+                  const uint16_t *x_bf16, int32_t *ids, double *w, float *out32,
+                  double *out64, double *h_out) {
+    double *x = (double *)malloc(sizeof(double) * (size_t)H);
+    double *y = (double *)malloc(sizeof(double) * (size_t)H);
+    double *acc = (double *)calloc((size_t)H, sizeof(double));
+    for (int c = 0; c < H; ++c) x[c] = or_bf16_to_double(x_bf16[c]);
+    or_route_tokens(router_w, bias, x_bf16, 1, E, H, k, ids, w, NULL, NULL);
+    int64_t gate_expert_bytes = (int64_t)I * (H / OR_QK) * OR_BLOCK_BYTES;
+    int64_t down_expert_bytes = (int64_t)H * (I / OR_QK) * OR_BLOCK_BYTES;
+    for (int i = 0; i < k; ++i) {
+        int e = ids[i];
+        or_expert_ffn(w_gate + e * gate_expert_bytes, w_up + e * gate_expert_bytes,
+                      w_down + e * down_expert_bytes, H, I, x,
+                      h_out ? h_out + (int64_t)i * I : NULL, y);
+        for (int c = 0; c < H; ++c) acc[c] += w[i] * y[c];
+    }
+    for (int c = 0; c < H; ++c) {
+        out32[c] = (float)acc[c];
+        if (out64) out64[c] = acc[c];
+    }
+    free(x);
+    free(y);
+    free(acc);
+}
+
+/* Grouped-prefill bookkeeping for T tokens routed top-k (ids [T][k]):
+ *   counts[e]   = number of (token, slot) pairs routed to e
+ *   offsets[e]  = sum of counts[0..e-1]  (exclusive scan; offsets[E] = T*k)
+ *   perm[j]     = pair id p = t*k + slot at position j, ordered by expert
+ *                 and, within one expert, by increasing pair id. */
+void or_counts_offsets_perm(const int32_t *ids, int T, int k, int E,
+                            int32_t *counts, int32_t *offsets, int32_t *perm) {
+    int64_t P = (int64_t)T * k;
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t p = 0; p < P; ++p) counts[ids[p]] += 1;
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int64_t pos = 0;
+    for (int e = 0; e < E; ++e)
+        for (int64_t p = 0; p < P; ++p)
+            if (ids[p] == e) perm[pos++] = (int32_t)p;
+}

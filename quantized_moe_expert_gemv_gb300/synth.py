@@ -1,0 +1,169 @@
+"""Seeded synthetic inputs for a Q4_K-resident mixture-of-experts FFN layer.
+
+This module only draws random bytes and numbers. It holds none of the
+method's arithmetic (no dequantization, routing, FFN or combine), so both
+the CUDA path (tests, bench) and the CPU oracle (tests) may take their
+inputs from it.
+
+Value recipe (the sparkinfer pages name Q4_K_M experts, the Qwen3-30B-A3B
+shape and greedy bs=1 decode, but print no weights; the recipe is the
+plainest synthetic stand-in with the shapes of those workloads):
+  * Q4_K super-block, 144 bytes per 256 weights, in GGUF byte order
+    {fp16 d, fp16 dmin, u8 scales[12], u8 qs[128]}:
+      d    ~ U[1e-4, 2e-3] rounded to fp16 (round-to-nearest-even),
+      dmin ~ U[0, 1e-3]    rounded to fp16,
+      scales[12], qs[128]: uniform random bytes.
+  * router weights fp32 ~ N(0, 0.02); activations x ~ N(0, 1) rounded to
+    bf16 (round-to-nearest-even), carried as uint16 bit patterns.
+
+Weight tensors are expert-major and blocked along each matrix's input
+(column) dimension, GGUF's own row layout:
+  gate, up : [E][I rows][H/256 blocks][144 B]
+  down     : [E][H rows][I/256 blocks][144 B]
+
+Every draw comes from numpy's PCG64 seeded through SeedSequence with an
+explicit key, which gives the same bytes on x86-64 and aarch64.
+"""
+from __future__ import annotations
+
+import json
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+Q4K_BLOCK_BYTES = 144
+Q4K_BLOCK_WEIGHTS = 256
+
+_DIR = os.path.dirname(os.path.abspath(__file__))
+
+
+@dataclass(frozen=True)
+class MoeShape:
+    hidden: int          # H: model dimension (input of gate/up, output of down)
+    intermediate: int    # I: expert FFN width
+    n_experts: int       # E
+    top_k: int           # k
+
+    @property
+    def blocks_per_gate_row(self) -> int:
+        return self.hidden // Q4K_BLOCK_WEIGHTS
+
+    @property
+    def blocks_per_down_row(self) -> int:
+        return self.intermediate // Q4K_BLOCK_WEIGHTS
+
+    @property
+    def expert_bytes(self) -> int:
+        """Q4_K bytes of one expert's gate + up + down matrices."""
+        return 3 * self.hidden * self.intermediate // Q4K_BLOCK_WEIGHTS * Q4K_BLOCK_BYTES
+
+
+# Tiny layer: hidden 256, 8 experts, top-2, intermediate 256, seed 0.
+TINY = MoeShape(hidden=256, intermediate=256, n_experts=8, top_k=2)
+# Qwen3-30B-A3B MoE layer: hidden 2048, 128 experts, top-8, intermediate 768.
+QWEN3_30B_A3B = MoeShape(hidden=2048, intermediate=768, n_experts=128, top_k=8)
+
+
+def rng(*key: int | str) -> np.random.Generator:
+    """A PCG64 generator keyed by a tuple of ints/strings."""
+    ints = []
+    for k in key:
+        if isinstance(k, str):
+            ints.extend(k.encode())
+        else:
+            ints.append(int(k))
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(ints)))
+
+
+def q4k_random_blocks(g: np.random.Generator, n_blocks: int) -> np.ndarray:
+    """n_blocks random Q4_K super-blocks, uint8 [n_blocks, 144]."""
+    raw = np.frombuffer(g.bytes(n_blocks * Q4K_BLOCK_BYTES), dtype=np.uint8)
+    raw = raw.reshape(n_blocks, Q4K_BLOCK_BYTES).copy()
+    d = g.uniform(1e-4, 2e-3, n_blocks).astype(np.float16)
+    dmin = g.uniform(0.0, 1e-3, n_blocks).astype(np.float16)
+    raw[:, 0:2] = d.astype("<f2").view(np.uint8).reshape(n_blocks, 2)
+    raw[:, 2:4] = dmin.astype("<f2").view(np.uint8).reshape(n_blocks, 2)
+    return raw
+
+
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (nearest-even); return the uint16 bit patterns."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to fp32 (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+@dataclass
+class MoeLayer:
+    shape: MoeShape
+    w_gate: np.ndarray        # uint8 [E, I, H/256, 144]
+    w_up: np.ndarray          # uint8 [E, I, H/256, 144]
+    w_down: np.ndarray        # uint8 [E, H, I/256, 144]
+    router_w: np.ndarray      # float32 [E, H]
+    router_bias: np.ndarray | None = None   # float32 [E] or None
+
+
+def make_router_w(shape: MoeShape, seed: int, layer: int = 0) -> np.ndarray:
+    """Router weights fp32 N(0, 0.02), [E, H]."""
+    g = rng(seed, layer, "router")
+    return g.normal(0.0, 0.02, size=(shape.n_experts, shape.hidden)).astype(np.float32)
+
+
+def make_layer(shape: MoeShape, seed: int, layer: int = 0,
+               router_bias: np.ndarray | None = None) -> MoeLayer:
+    E, H, I = shape.n_experts, shape.hidden, shape.intermediate
+    nbh, nbi = shape.blocks_per_gate_row, shape.blocks_per_down_row
+    wg = q4k_random_blocks(rng(seed, layer, "gate"), E * I * nbh).reshape(E, I, nbh, Q4K_BLOCK_BYTES)
+    wu = q4k_random_blocks(rng(seed, layer, "up"), E * I * nbh).reshape(E, I, nbh, Q4K_BLOCK_BYTES)
+    wd = q4k_random_blocks(rng(seed, layer, "down"), E * H * nbi).reshape(E, H, nbi, Q4K_BLOCK_BYTES)
+    rw = make_router_w(shape, seed, layer)
+    bias = None if router_bias is None else np.asarray(router_bias, dtype=np.float32).copy()
+    return MoeLayer(shape, wg, wu, wd, rw, bias)
+
+
+def make_tokens(shape: MoeShape, seed: int, n_tokens: int, stream: int | str = "x") -> np.ndarray:
+    """bf16 activations N(0,1) as uint16 bits, [n_tokens, H]."""
+    g = rng(seed, "tokens", stream)
+    return bf16_bits(g.standard_normal((n_tokens, shape.hidden), dtype=np.float32))
+
+
+# ---------------------------------------------------------------------------
+# Biased routing for the small-batch dedup workload: a hot set of 32 of the
+# 128 experts receives a constant logit offset beta.  The hot set is the first
+# 32 entries of a seeded permutation; beta itself is a stored number, found
+# once with the CPU oracle so that the hot set carries 60% of the
+# renormalised top-k routing mass on the workload's 512 x 4 tokens (the
+# script that wrote it lives under tests/golden/).
+# ---------------------------------------------------------------------------
+DEDUP_BIAS_FILE = os.path.join(os.path.dirname(_DIR), "tests", "golden", "dedup_bias.json")
+
+
+def dedup_hot_set(seed: int, n_experts: int = 128, n_hot: int = 32) -> np.ndarray:
+    return np.sort(rng(seed, "hot-set").permutation(n_experts)[:n_hot]).astype(np.int32)
+
+
+def dedup_router_bias(seed: int, beta: float, n_experts: int = 128, n_hot: int = 32) -> np.ndarray:
+    b = np.zeros(n_experts, dtype=np.float32)
+    b[dedup_hot_set(seed, n_experts, n_hot)] = np.float32(beta)
+    return b
+
+
+def load_dedup_beta() -> float:
+    with open(DEDUP_BIAS_FILE) as f:
+        return float(json.load(f)["beta"])
+
+
+# Workload descriptions (sizes and seeds); "seed" follows the workload's index.
+WORKLOADS = {
+    "tiny": dict(shape=TINY, seed=0, n_tokens=1),
+    "layer": dict(shape=QWEN3_30B_A3B, seed=1, n_tokens=1024),
+    "stack48": dict(shape=QWEN3_30B_A3B, seed=2, n_layers=48, n_steps=256),
+    "dedup4": dict(shape=QWEN3_30B_A3B, seed=3, tokens_per_step=4, n_steps=512),
+    "prefill": dict(shape=QWEN3_30B_A3B, seed=4, n_tokens=4096),
+}

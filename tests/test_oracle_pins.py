@@ -1,0 +1,371 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Each test ties one oracle function to the Q4_K definition through hand
+arithmetic, a closed form, an invariant, a library routine or a brute-force
+dense restatement, so that a dropped term, a wrong sign or index, or a
+transposed operand anywhere in the oracle fails at least one test.
+"""
+from __future__ import annotations
+
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from quantized_moe_expert_gemv_gb300 import synth
+from tests.q4k_fixtures import make_block, pack_scales
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- fp16 / bf16
+def test_half_to_double_matches_numpy_for_every_bit_pattern(oracle_lib):
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(int(b)) for b in bits])
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(np.isinf(got) & (got > 0), np.isinf(ref) & (ref > 0))
+
+
+def test_bf16_generator_matches_torch_rounding():
+    torch = pytest.importorskip("torch")
+    g = np.random.default_rng(7)
+    a = np.concatenate([g.standard_normal(100000).astype(np.float32),
+                        np.array([0.0, -0.0, 1.0, 3.0e38, 1.0e-39], dtype=np.float32)])
+    ours = synth.bf16_bits(a)
+    ref = torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    assert oracle.bf16_to_double(int(ours[0])) == float(torch.from_numpy(a[:1]).to(torch.bfloat16).float())
+
+
+# ------------------------------------------------------------ scale/min unpack
+def _bits(v: int) -> str:
+    return format(v, "08b")
+
+
+def _expected_sc_m(s: np.ndarray, j: int) -> tuple[int, int]:
+    """The 6-bit fields read as bit strings (most significant bit first)."""
+    if j < 4:
+        return int(_bits(s[j])[2:], 2), int(_bits(s[j + 4])[2:], 2)
+    sc = _bits(s[j - 4])[:2] + _bits(s[j + 4])[4:]
+    m = _bits(s[j])[:2] + _bits(s[j + 4])[:4]
+    return int(sc, 2), int(m, 2)
+
+
+def test_scale_min_exhaustive_over_every_byte_read(oracle_lib):
+    g = np.random.default_rng(1)
+    for j in range(8):
+        s = g.integers(0, 256, 12, dtype=np.uint8)
+        if j < 4:
+            for a in range(256):
+                s[j] = a
+                s[j + 4] = 255 - a
+                assert oracle.q4k_scale_min(s, j) == _expected_sc_m(s, j)
+        else:
+            for a in range(256):
+                for b in range(256):
+                    s[j + 4] = a
+                    s[j - 4] = b
+                    s[j] = (a * 7 + b * 13) & 255
+                    assert oracle.q4k_scale_min(s, j) == _expected_sc_m(s, j)
+
+
+def test_scale_min_is_a_bijection_on_the_12_scale_bytes(oracle_lib):
+    """16 six-bit fields fill exactly 96 bits: decoding then re-packing any 12
+    bytes returns them unchanged, and packing then decoding returns the fields."""
+    g = np.random.default_rng(2)
+    for _ in range(2000):
+        s = g.integers(0, 256, 12, dtype=np.uint8)
+        sc, m = zip(*[oracle.q4k_scale_min(s, j) for j in range(8)])
+        assert np.array_equal(pack_scales(list(sc), list(m)), s)
+        sc2 = list(g.integers(0, 64, 8))
+        m2 = list(g.integers(0, 64, 8))
+        packed = pack_scales(sc2, m2)
+        assert [oracle.q4k_scale_min(packed, j) for j in range(8)] == list(zip(sc2, m2))
+
+
+# --------------------------------------------------------- hand-derived blocks
+def _hand_block(spec) -> np.ndarray:
+    blk = np.zeros(144, dtype=np.uint8)
+    blk[0:2] = np.frombuffer(bytes.fromhex(spec["d_hex"])[::-1], dtype=np.uint8)
+    blk[2:4] = np.frombuffer(bytes.fromhex(spec["dmin_hex"])[::-1], dtype=np.uint8)
+    blk[4:16] = np.frombuffer(bytes.fromhex(spec["scales_hex"]), dtype=np.uint8)
+    rule = spec["qs_rule"]
+    if rule.startswith("qs[32i+l] = ((15 - l%16) << 4)"):
+        for i in range(4):
+            for l in range(32):
+                blk[16 + 32 * i + l] = ((15 - l % 16) << 4) | (l % 16)
+    elif rule.startswith("qs[0] = 0x01"):
+        blk[16] = 0x01
+    elif rule.startswith("all qs bytes 0xFF"):
+        blk[16:] = 0xFF
+    else:
+        raise AssertionError(rule)
+    return blk
+
+
+def test_hand_derived_blocks(oracle_lib):
+    with open(os.path.join(GOLDEN, "q4k_hand_blocks.json")) as f:
+        fixture = json.load(f)
+    n_checked = 0
+    for spec in fixture["blocks"]:
+        w = oracle.q4k_dequant(_hand_block(spec))
+        for e in spec["expected"]:
+            assert w[32 * e["j"] + e["l"]] == np.float32(e["w"]), (spec["name"], e)
+            n_checked += 1
+    assert n_checked >= 15
+
+
+# --------------------------------------------------------- closed-form blocks
+@pytest.mark.parametrize("j", range(8))
+def test_single_nonzero_scale_closed_form(oracle_lib, j):
+    d = 0.0013
+    d16 = float(np.float16(d))
+    for sc_val in (1, 17, 33, 48, 63):          # 17..63 set the high two bits for j >= 4
+        for c in (1, 7, 15):
+            sc = [0] * 8
+            sc[j] = sc_val
+            blk = make_block(d, 0.0, sc, [0] * 8, np.full((8, 32), c))
+            w = oracle.q4k_dequant(blk).reshape(8, 32)
+            expect = np.float32(d16 * sc_val * c)
+            assert np.all(w[j] == expect)
+            others = np.delete(w, j, axis=0)
+            assert np.all(others == 0.0)
+
+
+@pytest.mark.parametrize("j", range(8))
+def test_min_only_closed_form(oracle_lib, j):
+    dmin16 = float(np.float16(0.00071))
+    for m_val in (1, 20, 47, 63):
+        m = [0] * 8
+        m[j] = m_val
+        blk = make_block(0.002, 0.00071, [0] * 8, m, np.full((8, 32), 9))
+        w = oracle.q4k_dequant(blk).reshape(8, 32)
+        assert np.all(w[j] == np.float32(-dmin16 * m_val))
+        assert np.all(np.delete(w, j, axis=0) == 0.0)
+
+
+def test_nibble_order_and_position(oracle_lib):
+    """Weight l of sub-block 2i is the low nibble of qs[32i+l]; of 2i+1 the high nibble."""
+    codes = np.zeros((8, 32), dtype=np.uint8)
+    for j in range(8):
+        for l in range(32):
+            codes[j, l] = (3 * j + 5 * l) % 16
+    blk = make_block(1.0, 0.0, [1] * 8, [0] * 8, codes)
+    w = oracle.q4k_dequant(blk).reshape(8, 32)
+    assert np.array_equal(w, codes.astype(np.float32))
+    # and directly from the bytes
+    qs = blk[16:]
+    for i in range(4):
+        for l in range(32):
+            assert w[2 * i, l] == qs[32 * i + l] & 15
+            assert w[2 * i + 1, l] == qs[32 * i + l] >> 4
+
+
+def test_dequant_is_the_exactly_rounded_value(oracle_lib):
+    """Random blocks: each weight equals the exact rational d*sc*q - dmin*m
+    rounded once to fp32."""
+    g = synth.rng(11)
+    blocks = synth.q4k_random_blocks(g, 40)
+    w = oracle.q4k_dequant(blocks).reshape(40, 8, 32)
+    for b in range(40):
+        blk = blocks[b]
+        d = Fraction(float(blk[0:2].view("<f2")[0]))
+        dmin = Fraction(float(blk[2:4].view("<f2")[0]))
+        s = blk[4:16]
+        for j in range(8):
+            sc, m = _expected_sc_m(s, j)
+            for l in range(0, 32, 5):
+                byte = int(blk[16 + 32 * (j // 2) + l])
+                q = (byte & 15) if j % 2 == 0 else (byte >> 4)
+                exact = d * sc * q - dmin * m
+                assert w[b, j, l] == np.float32(float(exact))
+
+
+# --------------------------------------------------------------------- routing
+def test_router_logits_match_numpy(oracle_lib):
+    g = np.random.default_rng(3)
+    E, H = 16, 512
+    W = g.normal(0, 0.02, (E, H)).astype(np.float32)
+    xb = synth.bf16_bits(g.standard_normal(H).astype(np.float32))
+    bias = g.normal(0, 0.5, E).astype(np.float32)
+    xf = synth.bf16_to_f32(xb).astype(np.float64)
+    z = oracle.router_logits(W, xb, bias)
+    ref = W.astype(np.float64) @ xf + bias.astype(np.float64)
+    np.testing.assert_allclose(z, ref, rtol=1e-13, atol=1e-15)
+    z0 = oracle.router_logits(W, xb)
+    np.testing.assert_allclose(z0, W.astype(np.float64) @ xf, rtol=1e-13, atol=1e-15)
+
+
+def test_topk_matches_stable_sort_with_ties(oracle_lib):
+    g = np.random.default_rng(4)
+    for E, k in ((8, 2), (128, 8), (256, 8), (16, 16), (5, 1)):
+        for _ in range(50):
+            z = g.integers(-6, 6, E).astype(np.float32) * np.float32(0.25)   # many exact ties
+            ids = oracle.topk(z, k)
+            ref = np.lexsort((np.arange(E), -z))[:k]     # descending value, then lower index
+            assert np.array_equal(ids, ref)
+
+
+def test_renormalised_weights(oracle_lib):
+    g = np.random.default_rng(5)
+    for E, k in ((8, 2), (128, 8), (32, 32)):
+        z = g.normal(0, 1, E)
+        ids = oracle.topk(z.astype(np.float32), k)
+        w = oracle.renorm_weights(z, ids)
+        assert abs(w.sum() - 1.0) < 1e-12
+        # renormalising the full softmax = softmax over the selected logits
+        np.testing.assert_allclose(w, scipy.special.softmax(z[ids]), rtol=1e-12)
+        if k == E:
+            np.testing.assert_allclose(w, scipy.special.softmax(z)[ids], rtol=1e-12)
+        assert np.all(np.diff(w) <= 0)                 # descending logits -> descending weights
+
+
+def test_route_tokens_margin_and_consistency(oracle_lib):
+    g = np.random.default_rng(6)
+    E, H, k, T = 32, 256, 4, 20
+    W = g.normal(0, 0.02, (E, H)).astype(np.float32)
+    xb = synth.bf16_bits(g.standard_normal((T, H)).astype(np.float32))
+    ids, w, z, margin = oracle.route_tokens(W, xb, k, want_logits=True)
+    for t in range(T):
+        zs = np.sort(z[t])[::-1]
+        assert margin[t] == zs[k - 1] - zs[k]
+        assert np.array_equal(ids[t], oracle.topk(z[t].astype(np.float32), k))
+        np.testing.assert_allclose(w[t], scipy.special.softmax(z[t][ids[t]]), rtol=1e-12)
+        assert len(set(ids[t].tolist())) == k and ids[t].min() >= 0 and ids[t].max() < E
+
+
+# ---------------------------------------------------------------- expert FFN
+def _const_matrix(rows, cols, d, sc_j, j, code):
+    """Q4_K matrix whose every block has one nonzero sub-block j (scale sc_j, code)."""
+    sc = [0] * 8
+    sc[j] = sc_j
+    blk = make_block(d, 0.0, sc, [0] * 8, np.full((8, 32), code))
+    return np.tile(blk, (rows, cols // 256, 1)).reshape(rows, cols // 256, 144)
+
+
+@pytest.mark.parametrize("sign_case", ["positive", "negative_gate"])
+def test_expert_ffn_closed_form(oracle_lib, sign_case):
+    """x = ones: g = (H/256)*32*d*sc*c, u = (H/256)*32*d_u, h = silu(g)*u,
+    y_c = (I/256)*32*d_d*sc_d*h for every output c."""
+    H, I = 512, 256
+    d16 = float(np.float16(0.0011))
+    du16 = float(np.float16(0.03125))
+    dd16 = float(np.float16(0.0019))
+    wg = _const_matrix(I, H, 0.0011, 33, 5, 7)
+    if sign_case == "negative_gate":
+        # dmin*m dominates: every gate weight is -dmin*m (sc = 0)
+        blk = make_block(0.001, 0.0005, [0] * 8, [40] * 8, np.full((8, 32), 3))
+        wg = np.tile(blk, (I, H // 256, 1)).reshape(I, H // 256, 144)
+        w_gate_val = -float(np.float16(0.0005)) * 40
+        g_val = H * w_gate_val
+    else:
+        g_val = (H // 256) * 32 * d16 * 33 * 7
+    wu = _const_matrix(I, H, 0.03125, 1, 0, 1)
+    wd = _const_matrix(H, I, 0.0019, 9, 3, 2)
+    x = np.ones(H)
+    h, y = oracle.expert_ffn(wg, wu, wd, x, H, I)
+    u_val = (H // 256) * 32 * du16
+    h_val = g_val * scipy.special.expit(g_val) * u_val
+    y_val = (I // 256) * 32 * dd16 * 9 * 2 * h_val
+    np.testing.assert_allclose(h, h_val, rtol=1e-13)
+    np.testing.assert_allclose(y, y_val, rtol=1e-13)
+    # silu identity: silu(g) - silu(-g) = g
+    assert abs(g_val * scipy.special.expit(g_val) - (-g_val) * scipy.special.expit(-g_val) - g_val) < 1e-9
+
+
+def _dense_reference(layer, xb):
+    """Brute force: every expert's FFN densely with numpy, then mask to the
+    top-k and weight by the renormalised softmax."""
+    s = layer.shape
+    E, H, I, k = s.n_experts, s.hidden, s.intermediate, s.top_k
+    x = synth.bf16_to_f32(xb).astype(np.float64)
+    z = layer.router_w.astype(np.float64) @ x
+    if layer.router_bias is not None:
+        z = z + layer.router_bias.astype(np.float64)
+    order = np.lexsort((np.arange(E), -z.astype(np.float32)))
+    sel = order[:k]
+    p = scipy.special.softmax(z)
+    wsel = p[sel] / p[sel].sum()
+    out = np.zeros(H)
+    for e in range(E):
+        Wg = oracle.q4k_dequant(layer.w_gate[e]).reshape(I, H).astype(np.float64)
+        Wu = oracle.q4k_dequant(layer.w_up[e]).reshape(I, H).astype(np.float64)
+        Wd = oracle.q4k_dequant(layer.w_down[e]).reshape(H, I).astype(np.float64)
+        g = Wg @ x
+        hh = g * scipy.special.expit(g) * (Wu @ x)
+        y = Wd @ hh
+        mask = np.isin(e, sel)
+        if mask:
+            out += wsel[list(sel).index(e)] * y
+    return sel, wsel, out
+
+
+@pytest.mark.parametrize("shape", [synth.MoeShape(256, 256, 4, 2), synth.MoeShape(512, 256, 4, 4),
+                                   synth.MoeShape(256, 512, 6, 3)])
+def test_moe_token_matches_dense_brute_force(oracle_lib, shape):
+    layer = synth.make_layer(shape, seed=21)
+    xs = synth.make_tokens(shape, seed=21, n_tokens=3)
+    for t in range(3):
+        res = oracle.moe_token(layer, xs[t])
+        sel, wsel, out = _dense_reference(layer, xs[t])
+        assert np.array_equal(res.ids, sel)
+        np.testing.assert_allclose(res.w, wsel, rtol=1e-12)
+        np.testing.assert_allclose(res.out64, out, rtol=1e-10, atol=1e-12 * np.abs(out).max())
+        assert np.array_equal(res.out32, res.out64.astype(np.float32))
+
+
+def test_identical_experts_reduce_to_one_expert(oracle_lib):
+    shape = synth.MoeShape(256, 256, 6, 3)
+    layer = synth.make_layer(shape, seed=22)
+    for name in ("w_gate", "w_up", "w_down"):
+        arr = getattr(layer, name)
+        arr[:] = arr[0]
+    xs = synth.make_tokens(shape, seed=22, n_tokens=4)
+    for t in range(4):
+        res = oracle.moe_token(layer, xs[t])
+        x = synth.bf16_to_f32(xs[t]).astype(np.float64)
+        _, y = oracle.expert_ffn(layer.w_gate[0], layer.w_up[0], layer.w_down[0], x, 256, 256)
+        np.testing.assert_allclose(res.out64, y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
+
+
+def test_router_bias_shifts_selection(oracle_lib):
+    shape = synth.MoeShape(256, 256, 8, 2)
+    layer = synth.make_layer(shape, seed=23, router_bias=np.array([0, 0, 0, 0, 0, 50.0, 0, 40.0]))
+    xs = synth.make_tokens(shape, seed=23, n_tokens=5)
+    for t in range(5):
+        res = oracle.moe_token(layer, xs[t])
+        assert list(res.ids) == [5, 7]
+
+
+# --------------------------------------------------------- prefill bookkeeping
+def test_counts_offsets_perm_match_numpy(oracle_lib):
+    g = np.random.default_rng(8)
+    for T, k, E in ((1, 1, 1), (7, 2, 8), (300, 8, 128), (64, 4, 5)):
+        ids = np.stack([g.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+        counts, offsets, perm = oracle.counts_offsets_perm(ids, E)
+        flat = ids.reshape(-1)
+        assert np.array_equal(counts, np.bincount(flat, minlength=E))
+        assert offsets[0] == 0 and np.array_equal(offsets[1:], np.cumsum(counts))
+        assert np.array_equal(perm, np.argsort(flat, kind="stable"))
+        assert np.array_equal(np.sort(perm), np.arange(T * k))
+
+
+# ------------------------------------------------------ dedup workload recipe
+def test_stored_dedup_beta_gives_sixty_percent_hot_mass(oracle_lib):
+    wl = synth.WORKLOADS["dedup4"]
+    shape, seed = wl["shape"], wl["seed"]
+    beta = synth.load_dedup_beta()
+    bias = synth.dedup_router_bias(seed, beta)
+    rw = synth.make_router_w(shape, seed)
+    xs = synth.make_tokens(shape, seed, wl["tokens_per_step"] * wl["n_steps"])
+    ids, w, _, _ = oracle.route_tokens(rw, xs, shape.top_k, bias=bias)
+    hot = np.isin(ids, synth.dedup_hot_set(seed))
+    share = float((w * hot).sum() / w.sum())
+    assert abs(share - 0.60) <= 0.005, share
