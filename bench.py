@@ -1,0 +1,468 @@
+#!/usr/bin/env python
+"""Benchmark of the Q4_K MoE FFN decode path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline workload: one Qwen3-30B-A3B-shaped MoE layer (hidden 2048, 128
+experts, top-8, intermediate 768, Q4_K experts resident in HBM), 1024
+independent tokens decoded one at a time (bs=1).  One step = the 1024
+sequential single-token forwards (router GEMV, softmax/top-k, gate/up
+dequant-GEMV + SwiGLU, down dequant-GEMV + weighted combine), replayed as one
+CUDA graph.  The layer's 339.7 MB of experts exceed the 129 MB L2, so no
+flush is inserted between steps.
+
+Printed: one JSON line with value = tokens/s over all ranks, the dominant
+kernel's HBM roofline (its CUDA-event time on its own stream), the whole
+chain's achieved bandwidth, nvidia-smi clocks sampled during the timed
+region, an end-to-end figure with host<->device copies in the timed
+region, the CPU oracle's throughput on a bounded sample, and (unless
+--no-extras) the 48-layer stack and the 4-token deduplicated workloads.
+
+--impl reference times the CPU oracle (the reference implementation of the
+method) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode tok/s at bs=1 (Qwen3-30B-A3B shape, Q4_K); HBM GB/s vs peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-extras", action="store_true", help="skip the stack/dedup workloads")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--tokens", type=int, default=0,
+                   help="tokens per step of the headline layer (default 1024; small values for ncu)")
+    p.add_argument("--cpu-sample-tokens", type=int, default=0,
+                   help="tokens of the CPU oracle sample (default: 4 per host core, at least 16)")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    return FALLBACK_HBM_GBS, "fallback (6.8 TB/s)"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.file.read())) if len(r) >= 9]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        power = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+class Dist:
+    def __init__(self, n_gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl" if n_gpus > 0 else "gloo")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t)
+        return float(t.item())
+
+
+# --------------------------------------------------------- CPU oracle timing
+_ORACLE_INPUTS = {}
+
+
+def oracle_tokens_per_s(n_tokens: int, threads: int):
+    """The CPU oracle, unchanged, on n_tokens of the headline layer (one token
+    per task, `threads` tasks at a time).  Returns (tok/s, seconds, threads)."""
+    import oracle
+    from quantized_moe_expert_gemv_gb300 import synth
+    wl = synth.WORKLOADS["layer"]
+    if "layer" not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS["layer"] = synth.make_layer(wl["shape"], seed=wl["seed"])
+    layer = _ORACLE_INPUTS["layer"]
+    x = synth.make_tokens(wl["shape"], seed=wl["seed"], n_tokens=n_tokens)
+    oracle.build()
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda t: oracle.moe_token(layer, x[t]), range(n_tokens)))
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, dist):
+    """--impl reference: the CPU oracle, timed per step on a bounded sample."""
+    if dist.rank != 0:
+        return
+    cores = cpu_cores()
+    sample = max(cores, 8)
+    steps_t = []
+    for i in range(args.warmup + args.steps):
+        tps, dt = oracle_tokens_per_s(sample, cores)
+        if i >= args.warmup:
+            steps_t.append(dt)
+    total = sum(steps_t)
+    value = sample * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded Q4_K experts, bf16 N(0,1) tokens)",
+        "config": {"workload": "qwen3-30b-a3b-moe-layer-decode-bs1", "hidden": 2048,
+                   "intermediate": 768, "experts": 128, "top_k": 8,
+                   "tokens_per_step": sample, "l2_policy": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample} tokens of the headline layer per step, one per thread"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- GPU workloads
+def build_layer_graph(binding, plan, L, x_rows, out_rows, scratch, stream, n_tok=1, route=None,
+                      events=None):
+    """Capture one CUDA graph of len(x_rows) sequential decode calls."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for t in range(len(x_rows)):
+                ro = route[t] if route is not None else None
+                if events is not None:
+                    binding.si_debug_decode_events(plan, L, x_rows[t], n_tok, out_rows[t], ro, scratch,
+                                                   events[t], stream=stream)
+                else:
+                    binding.si_moe_forward_decode(plan, L, x_rows[t], n_tok, out_rows[t], ro, scratch,
+                                                  stream=stream)
+    return g
+
+
+def time_graph(g, stream, steps, warmup, dist, sampler=None):
+    import torch
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            g.replay()
+        end.record(stream)
+    end.synchronize()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    dist.barrier()
+    ms = start.elapsed_time(end)
+    return dist.max(ms), clocks
+
+
+def bench_layer(args, dist, binding, device, synth, torch, hbm_peak):
+    wl = synth.WORKLOADS["layer"]
+    shape, seed, T = wl["shape"], wl["seed"], (args.tokens or wl["n_tokens"])
+    layer = synth.make_layer(shape, seed=seed)
+    dl = device.to_device(layer)
+    plan = binding.si_moe_plan(device.desc_for(shape), torch.cuda.current_device())
+    scratch = device.alloc_scratch(plan, binding.SI_MODE_DECODE, 1)
+    x_host = synth.make_tokens(shape, seed=seed, n_tokens=T)
+    x = device.tokens_to_device(x_host)
+    out = torch.empty((T, shape.hidden), dtype=torch.float32, device="cuda")
+    L = dl.struct()
+    stream = torch.cuda.Stream()
+    g = build_layer_graph(binding, plan, L, [x[t] for t in range(T)], [out[t] for t in range(T)],
+                          scratch, stream)
+    sampler = ClockSampler(torch.cuda.current_device())
+    ms, clocks = time_graph(g, stream, args.steps, args.warmup, dist, sampler)
+    st = binding.si_moe_read_status(plan, scratch, stream)
+    assert st == binding.SI_OK, binding.si_status_string(st)
+    ms_step = ms / args.steps
+    total_tokens = dist.sum(T * args.steps)
+    value = total_tokens / (ms / 1e3)
+
+    # Per-kernel CUDA-event timing of the same 1024-token step (events around
+    # each of the three kernels, recorded on the launch stream inside a graph).
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(T)]
+    with torch.cuda.stream(stream):
+        for row in ev:          # torch creates the CUDA event on its first record
+            for e in row:
+                e.record(stream)
+    torch.cuda.synchronize()
+    gi = build_layer_graph(binding, plan, L, [x[t] for t in range(T)], [out[t] for t in range(T)],
+                           scratch, stream, events=ev)
+    for _ in range(2):
+        gi.replay()
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 10))
+    sums = [0.0, 0.0, 0.0]
+    for _ in range(reps):
+        with torch.cuda.stream(stream):
+            gi.replay()
+        torch.cuda.synchronize()
+        for t in range(T):
+            for k in range(3):
+                sums[k] += ev[t][k].elapsed_time(ev[t][k + 1])
+    per_launch_ms = [s / (reps * T) for s in sums]
+    nbh, nbi = shape.blocks_per_gate_row, shape.blocks_per_down_row
+    gateup_bytes = shape.top_k * 2 * shape.intermediate * nbh * 144
+    down_bytes = shape.top_k * shape.hidden * nbi * 144
+    router_bytes = shape.n_experts * shape.hidden * 4 + shape.hidden * 2
+    expert_bytes = gateup_bytes + down_bytes
+    gu_gbs = gateup_bytes / (per_launch_ms[1] * 1e-3) / 1e9
+
+    # End to end: pinned host tokens in, pinned host outputs back, every step.
+    x_pin = torch.from_numpy(x_host.view("int16")).pin_memory()
+    out_pin = torch.empty((T, shape.hidden), dtype=torch.float32).pin_memory()
+    x16 = x.view(torch.int16)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            x16.copy_(x_pin, non_blocking=True)
+            g.replay()
+            out_pin.copy_(out, non_blocking=True)
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = dist.max(e0.elapsed_time(e1))
+    e2e_value = total_tokens / (e2e_ms / 1e3)
+
+    tok_per_s_rank = T * args.steps / (ms / 1e3)
+    chain_gbs = expert_bytes * tok_per_s_rank / 1e9
+    result = {
+        "value": value, "unit": "tok/s", "ms_per_step": ms_step,
+        "config": {"workload": "qwen3-30b-a3b-moe-layer-decode-bs1", "hidden": shape.hidden,
+                   "intermediate": shape.intermediate, "experts": shape.n_experts, "top_k": shape.top_k,
+                   "weights": "Q4_K (GGUF, 144 B / 256 weights)", "tokens_per_step": T, "seed": seed,
+                   "global_batch": 1, "parallelism": f"replicas x{dist.world}",
+                   "l2_policy": "inputs larger than L2: 339.7 MB of resident experts per layer vs "
+                                "129 MB L2; no flush between steps",
+                   "graph": "one CUDA graph per step (1024 x 3 kernels)"},
+        "roofline": {"bound": "hbm", "kernel": "k_gateup (gate/up dequant-GEMV + SwiGLU)",
+                     "achieved": gu_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gu_gbs / hbm_peak,
+                     "traffic": None,
+                     "algorithmic_bytes_per_launch": gateup_bytes,
+                     "launch_ms": per_launch_ms[1]},
+        "kernels_ms_per_token": {"router_topk": per_launch_ms[0], "gateup": per_launch_ms[1],
+                                 "down": per_launch_ms[2]},
+        "chain": {"expert_bytes_per_token": expert_bytes, "router_bytes_per_token": router_bytes,
+                  "achieved_gbs": chain_gbs, "frac_of_peak": chain_gbs / hbm_peak,
+                  "us_per_token": 1e3 * ms_step / T},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": T * shape.hidden * 2,
+                "d2h_bytes_per_step": T * shape.hidden * 4},
+        "gpu_launches": 3 * T * args.steps,
+    }
+    del g, gi
+    return result
+
+
+def bench_stack48(args, dist, binding, device, synth, torch, hbm_peak):
+    wl = synth.WORKLOADS["stack48"]
+    shape, seed, NL, S = wl["shape"], wl["seed"], wl["n_layers"], wl["n_steps"]
+    plan = binding.si_moe_plan(device.desc_for(shape), torch.cuda.current_device())
+    scratch = device.alloc_scratch(plan, binding.SI_MODE_DECODE, 1)
+    layers = []
+    for l in range(NL):
+        wg, wu, wd, rw = synth.make_layer_torch(shape, seed, l)
+        layers.append((binding.layer_struct(wg, wu, wd, rw), (wg, wu, wd, rw)))
+    x = synth.make_tokens_torch(S * NL, shape.hidden, (seed, "stack-x")).view(S, NL, shape.hidden)
+    out = torch.empty((S, NL, shape.hidden), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(S):
+                for l in range(NL):
+                    binding.si_moe_forward_decode(plan, layers[l][0], x[s, l], 1, out[s, l], None, scratch,
+                                                  stream=stream)
+    steps = max(1, args.steps // 4)
+    ms, clocks = time_graph(g, stream, steps, min(args.warmup, 2), dist, ClockSampler(torch.cuda.current_device()))
+    st = binding.si_moe_read_status(plan, scratch, stream)
+    assert st == binding.SI_OK
+    tok_s = S * steps / (ms / 1e3)
+    step_bytes = NL * shape.top_k * shape.expert_bytes
+    gbs = step_bytes * tok_s / 1e9
+    del g
+    return {"workload": "48-layer stack, 256 decode steps (16.3 GB Q4_K resident)",
+            "tok_per_s": dist.sum(tok_s), "layer_tok_per_s": dist.sum(tok_s) * NL,
+            "us_per_step": 1e6 / tok_s, "expert_bytes_per_step": step_bytes,
+            "achieved_gbs": gbs, "frac_of_peak": gbs / hbm_peak, "clocks": clocks,
+            "gpu_launches": 3 * NL * S * steps}
+
+
+def bench_dedup4(args, dist, binding, device, synth, torch, hbm_peak):
+    wl = synth.WORKLOADS["dedup4"]
+    shape, seed, n, S = wl["shape"], wl["seed"], wl["tokens_per_step"], wl["n_steps"]
+    bias = synth.dedup_router_bias(seed, synth.load_dedup_beta())
+    layer = synth.make_layer(shape, seed=seed, router_bias=bias)
+    dl = device.to_device(layer)
+    plan = binding.si_moe_plan(device.desc_for(shape), torch.cuda.current_device())
+    scratch = device.alloc_scratch(plan, binding.SI_MODE_DECODE, n)
+    x = device.tokens_to_device(synth.make_tokens(shape, seed, n * S)).view(S, n, shape.hidden)
+    out = torch.empty((S, n, shape.hidden), dtype=torch.float32, device="cuda")
+    counts = torch.zeros((S, shape.n_experts), dtype=torch.int32, device="cuda")
+    routes = [binding.route_struct(expert_counts=counts[s]) for s in range(S)]
+    stream = torch.cuda.Stream()
+    g = build_layer_graph(binding, plan, dl.struct(), [x[s] for s in range(S)], [out[s] for s in range(S)],
+                          scratch, stream, n_tok=n, route=routes)
+    steps = max(1, args.steps // 2)
+    ms, clocks = time_graph(g, stream, steps, args.warmup, dist, ClockSampler(torch.cuda.current_device()))
+    U = (counts > 0).sum(dim=1).double()
+    u_mean = float(U.mean())
+    tok_s = n * S * steps / (ms / 1e3)
+    step_s = S * steps / (ms / 1e3)
+    bytes_per_step = u_mean * shape.expert_bytes
+    gbs = bytes_per_step * step_s / 1e9
+    del g
+    return {"workload": "4 tokens/step deduplicated decode, 512 steps, biased routing (32 hot experts, 60% mass)",
+            "tok_per_s": dist.sum(tok_s), "us_per_step": 1e6 / step_s, "mean_unique_experts": u_mean,
+            "expert_bytes_per_step": bytes_per_step,
+            "non_dedup_bytes_per_step": n * shape.top_k * shape.expert_bytes,
+            "achieved_gbs": gbs, "frac_of_peak": gbs / hbm_peak, "clocks": clocks,
+            "gpu_launches": 3 * S * steps}
+
+
+def run_ours(args, dist):
+    import torch
+    from quantized_moe_expert_gemv_gb300 import binding, build, device, synth
+    build.build()
+    binding.load_library()
+    torch.cuda.set_device(dist.local)
+    hbm_peak, peak_src = peaks()
+    res = bench_layer(args, dist, binding, device, synth, torch, hbm_peak)
+    res["roofline"]["peak_source"] = peak_src
+    line = {"metric": METRIC, "value": res["value"], "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded Q4_K experts, bf16 N(0,1) tokens)"}
+    for k in ("config", "roofline", "kernels_ms_per_token", "chain", "clocks", "e2e", "gpu_launches"):
+        line[k] = res[k]
+    if not args.no_extras:
+        torch.cuda.empty_cache()
+        try:
+            line["stack48"] = bench_stack48(args, dist, binding, device, synth, torch, hbm_peak)
+        except Exception as exc:  # report, do not hide the headline
+            line["stack48"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+        try:
+            line["dedup4"] = bench_dedup4(args, dist, binding, device, synth, torch, hbm_peak)
+        except Exception as exc:
+            line["dedup4"] = {"error": repr(exc)}
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        cores = cpu_cores()
+        n = args.cpu_sample_tokens or max(16, 4 * cores)
+        tps, dt = oracle_tokens_per_s(n, cores)
+        line["cpu_baseline"] = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{n} tokens of the headline layer, one per thread, {dt:.1f} s"}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, dist)
+    else:
+        run_ours(args, dist)
+    if dist.pg:
+        dist.pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

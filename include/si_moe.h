@@ -1,0 +1,171 @@
+/*
+ * si_moe.h -- C ABI of libsimoe: a Q4_K-resident mixture-of-experts FFN
+ * (router, top-k, dequant-on-read expert GEMVs, SwiGLU, weighted combine)
+ * for single-stream decode and grouped prefill on one GB300 (sm_103a).
+ *
+ * What the library computes, per token x (H values):
+ *   z = W_r x (+ bias); ids = k largest z (descending, equal z -> lower
+ *   index); w_i = softmax(z)[ids_i] / sum_j softmax(z)[ids_j];
+ *   h_i = silu(W_gate[ids_i] x) * (W_up[ids_i] x);  out = sum_i w_i W_down[ids_i] h_i.
+ * Sources: sparkinfer README (luciferlive112116), opening section (experts
+ * "quantized-resident, dequantized on-read", greedy bs=1 decode of a Q4_K_M
+ * GGUF Qwen3-30B-A3B) and "Layout" table (kernels: "decode GEMV", "fused
+ * quantized MoE expert FFN", "GGUF dequant"; moe: "sync-free MoE router +
+ * expert dispatch (on-device counts, CUDA-graph-ready)"); SP-RKINFER README
+ * (gittensor-ai-lab), "Benchmark - Qwen3.8-27B" prefill note (Q4_K is
+ * dequantized into the GEMM operand on every prefill pass); the CuTe-DSL
+ * sparkinfer README (local-inference-lab), "Using it" (host plan, views-only
+ * bind, capture-safe run) for the shape of this interface.
+ *
+ * Conventions for every call:
+ *  - Ownership: the caller owns every device buffer and the stream.  The
+ *    library never allocates or frees device memory, never synchronises
+ *    inside a forward call, and its forward calls can be captured in a CUDA
+ *    graph.  A plan owns host memory only.
+ *  - Device pointers must be 16-byte aligned (SI_ERR_MISALIGNED otherwise).
+ *  - Errors: no call throws.  Argument errors are reported before any
+ *    launch.  A failed launch returns SI_ERR_CUDA.  Faults found on the
+ *    device (a bounded wait that ran out) are recorded in the scratch status
+ *    word and returned by si_moe_read_status.
+ *  - Threading: calls on one plan are thread-safe when each thread uses its
+ *    own scratch buffer.
+ *
+ * Q4_K weights (GGUF's block format, unmodified): 144-byte super-blocks of
+ * 256 weights {fp16 d, fp16 dmin, u8 scales[12], u8 qs[128]}, blocked along
+ * each matrix's input dimension, expert-major:
+ *   w_gate, w_up: [E][I rows][H/256 blocks]   (row r of expert e at byte
+ *                 ((e*I + r) * H/256) * 144)
+ *   w_down:       [E][H rows][I/256 blocks]
+ */
+#ifndef SI_MOE_H
+#define SI_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *si_stream_t;
+
+typedef enum si_status {
+    SI_OK = 0,
+    SI_ERR_INVALID_ARG = 1,       /* null pointer, bad size, bad mode */
+    SI_ERR_UNSUPPORTED = 2,       /* a shape this build has no kernel for */
+    SI_ERR_MISALIGNED = 3,        /* a device pointer not 16-byte aligned */
+    SI_ERR_SCRATCH_TOO_SMALL = 4, /* scratch_bytes below si_moe_scratch_bytes() */
+    SI_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */
+    SI_ERR_TIMEOUT = 6,           /* a bounded device-side wait ran out */
+    SI_ERR_DEVICE = 7             /* another device-side check failed */
+} si_status;
+
+#define SI_WTYPE_Q4_K 12          /* GGUF's type id of Q4_K */
+#define SI_MODE_DECODE 0
+#define SI_MODE_PREFILL 1
+#define SI_MAX_EXPERTS 256
+#define SI_MAX_TOPK 16
+#define SI_MAX_DECODE_TOKENS 4
+
+/* Layer shape.  hidden and intermediate are multiples of 256 (one Q4_K
+ * super-block); 1 <= top_k <= min(n_experts, SI_MAX_TOPK);
+ * n_experts <= SI_MAX_EXPERTS; max_tokens bounds the prefill token count.
+ * wtype must be SI_WTYPE_Q4_K; flags must be 0. */
+typedef struct si_moe_desc {
+    int32_t hidden;
+    int32_t intermediate;
+    int32_t n_experts;
+    int32_t top_k;
+    int32_t max_tokens;
+    int32_t wtype;
+    uint32_t flags;
+} si_moe_desc;
+
+typedef struct si_moe_plan_s *si_moe_plan_t;
+
+/* Validate desc for device cuda_device and choose launch shapes from its
+ * properties (SM count, shared memory, L2).  Host memory only; no device
+ * allocation.  *out receives a plan to free with si_moe_plan_destroy. */
+si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *out);
+void si_moe_plan_destroy(si_moe_plan_t plan);
+
+/* Bytes of caller-allocated device scratch one forward call of `mode`
+ * needs for n_tokens tokens (decode: 1..SI_MAX_DECODE_TOKENS; prefill:
+ * 1..max_tokens).  A buffer sized for n tokens serves any smaller count. */
+si_status si_moe_scratch_bytes(si_moe_plan_t plan, int mode, int32_t n_tokens, size_t *bytes);
+
+/* Zero the scratch control block (status word and arrival counters),
+ * stream-ordered.  Call once after allocating a scratch buffer, before its
+ * first forward call. */
+si_status si_moe_scratch_init(si_moe_plan_t plan, void *scratch, size_t scratch_bytes,
+                              si_stream_t stream);
+
+/* One layer's weights (device pointers, read only). */
+typedef struct si_moe_layer {
+    const void *w_gate;        /* Q4_K [E][I][H/256] */
+    const void *w_up;          /* Q4_K [E][I][H/256] */
+    const void *w_down;        /* Q4_K [E][H][I/256] */
+    const float *router_w;     /* fp32 [E][H], row-major */
+    const float *router_bias;  /* fp32 [E] added to the logits, or NULL */
+} si_moe_layer;
+
+/* Optional routing outputs (device pointers; each may be NULL). */
+typedef struct si_moe_route_out {
+    int32_t *topk_ids;         /* [n][k] selected experts, descending logit */
+    float *topk_w;             /* [n][k] renormalised softmax weights */
+    int32_t *expert_counts;    /* [E] tokens (decode) or pairs (prefill) per expert */
+    int32_t *expert_offsets;   /* [E+1] exclusive scan of counts (prefill only) */
+    int32_t *perm;             /* [n*k] pair ids t*k+slot ordered by expert, then pair id (prefill only) */
+    float *logits;             /* [n][E] fp32 router logits */
+} si_moe_route_out;
+
+/* Decode: n_tokens (1..SI_MAX_DECODE_TOKENS) independent tokens through one
+ * layer.  x_bf16: [n][H] bf16; out: [n][H] fp32 (written, not accumulated).
+ * With n_tokens > 1 each selected expert is read once per call and applied
+ * to every token that chose it.  Stream-ordered, no host synchronisation. */
+si_status si_moe_forward_decode(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
+                                int32_t n_tokens, float *out, si_moe_route_out *route_out,
+                                void *scratch, size_t scratch_bytes, si_stream_t stream);
+
+/* Grouped prefill: T tokens (1..max_tokens) routed top-k, permuted by
+ * expert with on-device counts/offsets, Q4_K tiles dequantized into bf16
+ * tensor-core operands (fp32 accumulation), SwiGLU, down GEMM, and the
+ * weighted combine back to token order (slot order, deterministic).
+ * x_bf16: [T][H] bf16; out: [T][H] fp32. */
+si_status si_moe_forward_prefill(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
+                                 int32_t n_tokens, float *out, si_moe_route_out *route_out,
+                                 void *scratch, size_t scratch_bytes, si_stream_t stream);
+
+/* Synchronise `stream`, return the device status recorded in `scratch`
+ * since the last read (SI_OK if none) and clear it. */
+si_status si_moe_read_status(si_moe_plan_t plan, const void *scratch, si_stream_t stream);
+
+const char *si_status_string(si_status status);
+
+/* Test exports.  si_debug_q4k_dequant decodes n_blocks Q4_K blocks into
+ * out_f32 [n_blocks*256] and/or out_bf16 [n_blocks*256] (either may be
+ * NULL): w = d*sc*q - dmin*m rounded once to fp32 (bf16: round-to-nearest-
+ * even of that fp32 value).  si_debug_topk runs the decode top-k on given
+ * fp32 logits [n][E] (n <= SI_MAX_DECODE_TOKENS) and fills route_out's
+ * topk_ids, topk_w and expert_counts. */
+si_status si_debug_q4k_dequant(const void *blocks, int64_t n_blocks, float *out_f32,
+                               uint16_t *out_bf16, si_stream_t stream);
+si_status si_debug_topk(const float *logits, int32_t n, const si_moe_desc *desc,
+                        si_moe_route_out *route_out, si_stream_t stream);
+
+/* Timing export: si_moe_forward_decode that also records caller-created
+ * cudaEvent_t handles on `stream` -- events[0] before the router kernel,
+ * events[1] before the gate/up kernel, events[2] before the down kernel,
+ * events[3] after it (any may be NULL).  Recorded as external events, so a
+ * CUDA-graph capture keeps them as event-record nodes.  Same arguments,
+ * errors and results as si_moe_forward_decode. */
+si_status si_debug_decode_events(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
+                                 int32_t n_tokens, float *out, si_moe_route_out *route_out,
+                                 void *scratch, size_t scratch_bytes, void *const *events,
+                                 si_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SI_MOE_H */

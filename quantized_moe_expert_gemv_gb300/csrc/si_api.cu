@@ -1,0 +1,252 @@
+// si_api.cu -- the C ABI (include/si_moe.h): plans, validation, scratch
+// layout and stream-ordered launches.  Nothing here allocates device memory
+// or synchronises, except si_moe_read_status (which is documented to).
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "si_internal.h"
+
+using si::DecodeArgs;
+using si::DecodeLayout;
+using si::Plan;
+
+struct si_moe_plan_s {
+    Plan p;
+};
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+si_status validate_desc(const si_moe_desc *d) {
+    if (!d) return SI_ERR_INVALID_ARG;
+    if (d->wtype != SI_WTYPE_Q4_K || d->flags != 0) return SI_ERR_UNSUPPORTED;
+    if (d->hidden <= 0 || d->intermediate <= 0 || d->hidden % 256 || d->intermediate % 256)
+        return SI_ERR_INVALID_ARG;
+    if (d->n_experts < 1 || d->n_experts > SI_MAX_EXPERTS) return SI_ERR_INVALID_ARG;
+    if (d->top_k < 1 || d->top_k > d->n_experts || d->top_k > SI_MAX_TOPK) return SI_ERR_INVALID_ARG;
+    if (d->max_tokens < 1) return SI_ERR_INVALID_ARG;
+    // decode keeps n tokens of activations (fp32) in shared memory
+    if ((size_t)SI_MAX_DECODE_TOKENS * d->hidden * 4 * 33 / 32 > 200 * 1024) return SI_ERR_UNSUPPORTED;
+    return SI_OK;
+}
+
+}  // namespace
+
+namespace si {
+
+DecodeLayout decode_layout(const si_moe_desc &d, int n) {
+    DecodeLayout L{};
+    size_t o = 0;
+    auto take = [&o](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.ctrl = take(kCtrlBytes);
+    L.logits = take((size_t)n * d.n_experts * sizeof(float));
+    L.ids = take((size_t)n * d.top_k * sizeof(int32_t));
+    L.wts = take((size_t)n * d.top_k * sizeof(float));
+    L.counts = take((size_t)d.n_experts * sizeof(int32_t));
+    L.uniq = take(sizeof(UniqTable));
+    L.h = take((size_t)n * d.top_k * d.intermediate * sizeof(float));
+    L.total = o;
+    return L;
+}
+
+}  // namespace si
+
+extern "C" {
+
+const char *si_status_string(si_status s) {
+    switch (s) {
+        case SI_OK: return "ok";
+        case SI_ERR_INVALID_ARG: return "invalid argument";
+        case SI_ERR_UNSUPPORTED: return "unsupported shape or mode";
+        case SI_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+        case SI_ERR_SCRATCH_TOO_SMALL: return "scratch buffer too small";
+        case SI_ERR_CUDA: return "CUDA error";
+        case SI_ERR_TIMEOUT: return "device-side wait timed out";
+        case SI_ERR_DEVICE: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *out) {
+    if (!out) return SI_ERR_INVALID_ARG;
+    *out = nullptr;
+    const si_status v = validate_desc(desc);
+    if (v != SI_OK) return v;
+    Plan p{};
+    p.desc = *desc;
+    p.device = cuda_device;
+    if (cudaDeviceGetAttribute(&p.sm_count, cudaDevAttrMultiProcessorCount, cuda_device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p.l2_bytes, cudaDevAttrL2CacheSize, cuda_device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, cuda_device) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return SI_ERR_CUDA;
+    }
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, cuda_device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, cuda_device);
+    if (major != 10 || minor != 3) return SI_ERR_UNSUPPORTED;  // built for sm_103a only
+    p.dec = si::decode_layout(*desc, SI_MAX_DECODE_TOKENS);
+    si_moe_plan_s *h = new (std::nothrow) si_moe_plan_s;
+    if (!h) return SI_ERR_INVALID_ARG;
+    h->p = p;
+    *out = h;
+    return SI_OK;
+}
+
+void si_moe_plan_destroy(si_moe_plan_t plan) { delete plan; }
+
+si_status si_moe_scratch_bytes(si_moe_plan_t plan, int mode, int32_t n_tokens, size_t *bytes) {
+    if (!plan || !bytes) return SI_ERR_INVALID_ARG;
+    const si_moe_desc &d = plan->p.desc;
+    if (mode == SI_MODE_DECODE) {
+        if (n_tokens < 1 || n_tokens > SI_MAX_DECODE_TOKENS) return SI_ERR_INVALID_ARG;
+        *bytes = si::decode_layout(d, n_tokens).total;
+        return SI_OK;
+    }
+    if (mode == SI_MODE_PREFILL) return SI_ERR_UNSUPPORTED;
+    return SI_ERR_INVALID_ARG;
+}
+
+si_status si_moe_scratch_init(si_moe_plan_t plan, void *scratch, size_t scratch_bytes,
+                              si_stream_t stream) {
+    if (!plan || !scratch) return SI_ERR_INVALID_ARG;
+    if (!aligned(scratch, 16)) return SI_ERR_MISALIGNED;
+    if (scratch_bytes < si::kCtrlBytes) return SI_ERR_SCRATCH_TOO_SMALL;
+    if (cudaMemsetAsync(scratch, 0, si::kCtrlBytes, (cudaStream_t)stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SI_ERR_CUDA;
+    }
+    return SI_OK;
+}
+
+static si_status forward_decode_impl(si_moe_plan_t plan, const si_moe_layer *layer,
+                                     const void *x_bf16, int32_t n_tokens, float *out,
+                                     si_moe_route_out *ro, void *scratch, size_t scratch_bytes,
+                                     cudaEvent_t const *events, si_stream_t stream) {
+    if (!plan || !layer || !x_bf16 || !out || !scratch) return SI_ERR_INVALID_ARG;
+    if (!layer->w_gate || !layer->w_up || !layer->w_down || !layer->router_w) return SI_ERR_INVALID_ARG;
+    if (n_tokens < 1 || n_tokens > SI_MAX_DECODE_TOKENS) return SI_ERR_INVALID_ARG;
+    if (!aligned(layer->w_gate, 16) || !aligned(layer->w_up, 16) || !aligned(layer->w_down, 16) ||
+        !aligned(layer->router_w, 16) || !aligned(x_bf16, 16) || !aligned(out, 16) ||
+        !aligned(scratch, 16) || (layer->router_bias && !aligned(layer->router_bias, 4)))
+        return SI_ERR_MISALIGNED;
+    if (ro && ((ro->topk_ids && !aligned(ro->topk_ids, 4)) || (ro->topk_w && !aligned(ro->topk_w, 4)) ||
+               (ro->expert_counts && !aligned(ro->expert_counts, 4)) ||
+               (ro->logits && !aligned(ro->logits, 4))))
+        return SI_ERR_MISALIGNED;
+    const si_moe_desc &d = plan->p.desc;
+    const DecodeLayout L = si::decode_layout(d, n_tokens);
+    if (scratch_bytes < L.total) return SI_ERR_SCRATCH_TOO_SMALL;
+    uint8_t *sb = static_cast<uint8_t *>(scratch);
+    DecodeArgs a{};
+    a.wg = static_cast<const uint8_t *>(layer->w_gate);
+    a.wu = static_cast<const uint8_t *>(layer->w_up);
+    a.wd = static_cast<const uint8_t *>(layer->w_down);
+    a.router_w = layer->router_w;
+    a.router_bias = layer->router_bias;
+    a.x = static_cast<const uint16_t *>(x_bf16);
+    a.out = out;
+    a.H = d.hidden;
+    a.I = d.intermediate;
+    a.E = d.n_experts;
+    a.k = d.top_k;
+    a.n = n_tokens;
+    a.ctrl = reinterpret_cast<int32_t *>(sb + L.ctrl);
+    a.logits = reinterpret_cast<float *>(sb + L.logits);
+    a.ids = reinterpret_cast<int32_t *>(sb + L.ids);
+    a.wts = reinterpret_cast<float *>(sb + L.wts);
+    a.counts = reinterpret_cast<int32_t *>(sb + L.counts);
+    a.uniq = reinterpret_cast<si::UniqTable *>(sb + L.uniq);
+    a.h = reinterpret_cast<float *>(sb + L.h);
+    if (ro) {
+        a.o_ids = ro->topk_ids;
+        a.o_w = ro->topk_w;
+        a.o_counts = ro->expert_counts;
+        a.o_logits = ro->logits;
+    }
+    if (si::launch_decode(plan->p, a, (cudaStream_t)stream, events) != cudaSuccess) {
+        cudaGetLastError();
+        return SI_ERR_CUDA;
+    }
+    return SI_OK;
+}
+
+si_status si_moe_forward_decode(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
+                                int32_t n_tokens, float *out, si_moe_route_out *ro, void *scratch,
+                                size_t scratch_bytes, si_stream_t stream) {
+    return forward_decode_impl(plan, layer, x_bf16, n_tokens, out, ro, scratch, scratch_bytes,
+                               nullptr, stream);
+}
+
+si_status si_debug_decode_events(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
+                                 int32_t n_tokens, float *out, si_moe_route_out *ro, void *scratch,
+                                 size_t scratch_bytes, void *const *events, si_stream_t stream) {
+    return forward_decode_impl(plan, layer, x_bf16, n_tokens, out, ro, scratch, scratch_bytes,
+                               reinterpret_cast<cudaEvent_t const *>(events), stream);
+}
+
+si_status si_moe_forward_prefill(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
+                                 int32_t n_tokens, float *out, si_moe_route_out *route_out,
+                                 void *scratch, size_t scratch_bytes, si_stream_t stream) {
+    (void)layer; (void)x_bf16; (void)n_tokens; (void)out; (void)route_out; (void)scratch;
+    (void)scratch_bytes; (void)stream;
+    if (!plan) return SI_ERR_INVALID_ARG;
+    return SI_ERR_UNSUPPORTED;
+}
+
+si_status si_moe_read_status(si_moe_plan_t plan, const void *scratch, si_stream_t stream) {
+    if (!plan || !scratch) return SI_ERR_INVALID_ARG;
+    if (!aligned(scratch, 16)) return SI_ERR_MISALIGNED;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SI_ERR_CUDA;
+    }
+    int32_t word = 0;
+    if (cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return SI_ERR_CUDA;
+    }
+    if (word != 0) {
+        if (cudaMemset(const_cast<void *>(scratch), 0, sizeof(word)) != cudaSuccess) {
+            cudaGetLastError();
+            return SI_ERR_CUDA;
+        }
+        return (si_status)word;
+    }
+    return SI_OK;
+}
+
+si_status si_debug_q4k_dequant(const void *blocks, int64_t n_blocks, float *out_f32,
+                               uint16_t *out_bf16, si_stream_t stream) {
+    if (!blocks || n_blocks < 0 || (!out_f32 && !out_bf16)) return SI_ERR_INVALID_ARG;
+    if (!aligned(blocks, 16) || (out_f32 && !aligned(out_f32, 16)) || (out_bf16 && !aligned(out_bf16, 16)))
+        return SI_ERR_MISALIGNED;
+    if (si::launch_debug_dequant(static_cast<const uint8_t *>(blocks), n_blocks, out_f32, out_bf16,
+                                 (cudaStream_t)stream) != cudaSuccess)
+        return SI_ERR_CUDA;
+    return SI_OK;
+}
+
+si_status si_debug_topk(const float *logits, int32_t n, const si_moe_desc *desc,
+                        si_moe_route_out *ro, si_stream_t stream) {
+    if (!logits || !desc || !ro) return SI_ERR_INVALID_ARG;
+    if (n < 1 || n > SI_MAX_DECODE_TOKENS) return SI_ERR_INVALID_ARG;
+    if (desc->n_experts < 1 || desc->n_experts > SI_MAX_EXPERTS || desc->top_k < 1 ||
+        desc->top_k > desc->n_experts || desc->top_k > SI_MAX_TOPK)
+        return SI_ERR_INVALID_ARG;
+    if (!aligned(logits, 4)) return SI_ERR_MISALIGNED;
+    if (si::launch_debug_topk(logits, n, desc->n_experts, desc->top_k, ro->topk_ids, ro->topk_w,
+                              ro->expert_counts, (cudaStream_t)stream) != cudaSuccess)
+        return SI_ERR_CUDA;
+    return SI_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,344 @@
+// si_decode.cu -- bs=1 (and n<=4 deduplicated) decode through a Q4_K MoE FFN.
+//
+// Three stream-ordered kernels per layer, no host synchronisation
+// (sparkinfer README, "Layout": moe/ "sync-free MoE router + expert dispatch
+// (on-device counts, CUDA-graph-ready)"; kernels/ "decode GEMV", "fused
+// quantized MoE expert FFN"):
+//   1. k_router_topk : router GEMV z = W_r x (+bias); the last CTA to arrive
+//                      takes softmax, top-k, renormalised weights, per-expert
+//                      counts and the table of distinct experts.
+//   2. k_gateup      : for every (distinct expert, intermediate row) the gate
+//                      and up rows are dequantized on read and dotted with x of
+//                      each token that chose the expert; h = silu(g) * u.
+//   3. k_down        : every output row c dots the down rows of the selected
+//                      experts with their h and sums them weighted by the
+//                      routing weights (fixed order, no atomics).
+#include <cstdint>
+
+#include "si_device.cuh"
+#include "si_internal.h"
+
+namespace si {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// --------------------------------------------------------------- router
+__global__ void __launch_bounds__(kThreads) k_router_topk(DecodeArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kWarps + warp;
+    if (e < a.E) {
+        float acc[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
+        const float *wrow = a.router_w + (size_t)e * a.H;
+        for (int c = 8 * lane; c < a.H; c += 256) {
+            const float4 w0 = __ldg(reinterpret_cast<const float4 *>(wrow + c));
+            const float4 w1 = __ldg(reinterpret_cast<const float4 *>(wrow + c + 4));
+#pragma unroll
+            for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
+                if (t < a.n) {
+                    const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + c));
+                    float s = acc[t];
+                    s = fmaf(w0.x, __uint_as_float(xv.x << 16), s);
+                    s = fmaf(w0.y, __uint_as_float(xv.x & 0xffff0000u), s);
+                    s = fmaf(w0.z, __uint_as_float(xv.y << 16), s);
+                    s = fmaf(w0.w, __uint_as_float(xv.y & 0xffff0000u), s);
+                    s = fmaf(w1.x, __uint_as_float(xv.z << 16), s);
+                    s = fmaf(w1.y, __uint_as_float(xv.z & 0xffff0000u), s);
+                    s = fmaf(w1.z, __uint_as_float(xv.w << 16), s);
+                    s = fmaf(w1.w, __uint_as_float(xv.w & 0xffff0000u), s);
+                    acc[t] = s;
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
+            if (t < a.n) {
+                float z = warp_sum(acc[t]);
+                if (a.router_bias) z += __ldg(a.router_bias + e);
+                if (lane == 0) {
+                    a.logits[t * a.E + e] = z;
+                    if (a.o_logits) a.o_logits[t * a.E + e] = z;
+                }
+            }
+        }
+    }
+
+    // Last CTA to arrive routes every token.  Every writer fences its logits
+    // before the barrier; thread 0 then takes the arrival ticket.
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int ticket = atomicAdd(a.ctrl + kCtrlRouterTicket, 1);
+        s_last = (ticket == (int)gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    __shared__ float s_z[SI_MAX_DECODE_TOKENS][SI_MAX_EXPERTS];
+    __shared__ int s_ids[SI_MAX_DECODE_TOKENS][SI_MAX_TOPK];
+    __shared__ float s_w[SI_MAX_DECODE_TOKENS][SI_MAX_TOPK];
+    __shared__ int s_counts[SI_MAX_EXPERTS];
+    for (int i = threadIdx.x; i < a.n * a.E; i += kThreads)
+        s_z[i / a.E][i % a.E] = __ldcg(a.logits + i);
+    for (int i = threadIdx.x; i < a.E; i += kThreads) s_counts[i] = 0;
+    __syncthreads();
+    if (warp < a.n) {
+        warp_topk(s_z[warp], a.E, a.k, s_ids[warp], s_w[warp]);
+        __syncwarp();
+        for (int i = lane; i < a.k; i += 32) {
+            a.ids[warp * a.k + i] = s_ids[warp][i];
+            a.wts[warp * a.k + i] = s_w[warp][i];
+            if (a.o_ids) a.o_ids[warp * a.k + i] = s_ids[warp][i];
+            if (a.o_w) a.o_w[warp * a.k + i] = s_w[warp][i];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // Distinct experts in ascending order, with the tokens/slots that chose them.
+        UniqTable *u = a.uniq;
+        int U = 0;
+        int ex[kMaxSlots];
+        for (int t = 0; t < a.n; ++t) {
+            for (int i = 0; i < a.k; ++i) {
+                const int e2 = s_ids[t][i];
+                s_counts[e2] += 1;
+                int pos = 0;
+                while (pos < U && ex[pos] < e2) ++pos;
+                if (pos == U || ex[pos] != e2) {
+                    for (int q = U; q > pos; --q) ex[q] = ex[q - 1];
+                    ex[pos] = e2;
+                    ++U;
+                }
+            }
+        }
+        int fill[kMaxSlots];
+        for (int s = 0; s < U; ++s) {
+            u->expert[s] = ex[s];
+            fill[s] = 0;
+        }
+        for (int t = 0; t < a.n; ++t) {
+            for (int i = 0; i < a.k; ++i) {
+                const int e2 = s_ids[t][i];
+                int s = 0;
+                while (ex[s] != e2) ++s;
+                u->tok[s][fill[s]] = t;
+                u->slot[s][fill[s]] = i;
+                ++fill[s];
+            }
+        }
+        for (int s = 0; s < U; ++s) u->ntok[s] = fill[s];
+        a.ctrl[kCtrlNumUnique] = U;
+        a.ctrl[kCtrlRouterTicket] = 0;  // ready for the next call
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.E; i += kThreads) {
+        a.counts[i] = s_counts[i];
+        if (a.o_counts) a.o_counts[i] = s_counts[i];
+    }
+}
+
+// ---------------------------------------------------------------- gate/up
+template <int NT>
+__device__ __forceinline__ void gateup_rowpair(const DecodeArgs &a, const float *xs,
+                                               const float *Xs, const UniqTable *u, int s, int r,
+                                               int lane) {
+    const int e = u->expert[s];
+    const int nbH = a.H / kQK;
+    const size_t row_bytes = (size_t)nbH * kBlockBytes;
+    const uint8_t *gbase = a.wg + ((size_t)e * a.I + r) * row_bytes;
+    const uint8_t *ubase = a.wu + ((size_t)e * a.I + r) * row_bytes;
+    int tok[NT], slot[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        tok[t] = u->tok[s][t];
+        slot[t] = u->slot[s][t];
+    }
+    float g[NT], uu[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) g[t] = uu[t] = 0.f;
+    for (int it = lane; it < 4 * nbH; it += 32) {
+        const int b = it >> 2, i = it & 3;
+        const uint8_t *bg = gbase + b * kBlockBytes;
+        const uint8_t *bu = ubase + b * kBlockBytes;
+        const uint4 hg = ldg_nc_v4(bg), qg0 = ldg_nc_v4(bg + 16 + 32 * i),
+                    qg1 = ldg_nc_v4(bg + 32 + 32 * i);
+        const uint4 hu = ldg_nc_v4(bu), qu0 = ldg_nc_v4(bu + 16 + 32 * i),
+                    qu1 = ldg_nc_v4(bu + 32 + 32 * i);
+        const SubScales sg = chunk_scales(hg, i), su = chunk_scales(hu, i);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const float *xa = xs + (size_t)tok[t] * a.H + kQK * b + 64 * i;
+            const f32x2 *pa = reinterpret_cast<const f32x2 *>(xa);
+            const f32x2 *pb = reinterpret_cast<const f32x2 *>(xa + 32);
+            auto xa2 = [pa](int p) { return pa[p]; };
+            auto xb2 = [pb](int p) { return pb[p]; };
+            const float Xa = Xs[tok[t] * (a.H / 32) + 8 * b + 2 * i];
+            const float Xb = Xs[tok[t] * (a.H / 32) + 8 * b + 2 * i + 1];
+            g[t] += chunk_contrib(sg, chunk_code_sums(qg0, qg1, xa2, xb2), Xa, Xb);
+            uu[t] += chunk_contrib(su, chunk_code_sums(qu0, qu1, xa2, xb2), Xa, Xb);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const float gs = warp_sum(g[t]);
+        const float us = warp_sum(uu[t]);
+        if (lane == 0) a.h[((size_t)tok[t] * a.k + slot[t]) * a.I + r] = silu(gs) * us;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_gateup(DecodeArgs a) {
+    extern __shared__ __align__(16) float smem[];
+    float *xs = smem;               // [n][H]
+    float *Xs = smem + a.n * a.H;   // [n][H/32] sub-block sums
+    const int nH = a.n * a.H;
+    for (int i = threadIdx.x; i < nH; i += kThreads) xs[i] = bf16_bits_to_f32(a.x[i]);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nH / 32; i += kThreads) {
+        float s = 0.f;
+        for (int l = 0; l < 32; ++l) s += xs[32 * i + l];
+        Xs[i] = s;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const UniqTable *u = a.uniq;
+    const int U = a.ctrl[kCtrlNumUnique];
+    const int total = U * a.I;
+    for (int p = blockIdx.x * kWarps + warp; p < total; p += gridDim.x * kWarps) {
+        const int s = p / a.I, r = p - s * a.I;
+        switch (u->ntok[s]) {
+            case 1: gateup_rowpair<1>(a, xs, Xs, u, s, r, lane); break;
+            case 2: gateup_rowpair<2>(a, xs, Xs, u, s, r, lane); break;
+            case 3: gateup_rowpair<3>(a, xs, Xs, u, s, r, lane); break;
+            default: gateup_rowpair<4>(a, xs, Xs, u, s, r, lane); break;
+        }
+    }
+}
+
+// ------------------------------------------------------------------- down
+template <int GS>
+__global__ void __launch_bounds__(kThreads) k_down(DecodeArgs a) {
+    extern __shared__ __align__(16) float smem[];
+    float *Hs = smem;  // [n*k][I/32] sub-block sums of h
+    const int nIs = a.I / 32;
+    for (int i = threadIdx.x; i < a.n * a.k * nIs; i += kThreads) {
+        const float4 *hp = reinterpret_cast<const float4 *>(a.h + (size_t)32 * i);
+        float s = 0.f;
+#pragma unroll
+        for (int l = 0; l < 8; ++l) {
+            const float4 v = __ldg(hp + l);
+            s += v.x + v.y + v.z + v.w;
+        }
+        Hs[i] = s;
+    }
+    __syncthreads();
+    constexpr int kGroups = 32 / GS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gl = lane % GS;
+    const int c = (blockIdx.x * kWarps + warp) * kGroups + lane / GS;
+    if ((blockIdx.x * kWarps + warp) * kGroups >= a.H) return;  // whole warp idle
+    const int nbI = a.I / kQK;
+    const size_t row_bytes = (size_t)nbI * kBlockBytes;
+    const UniqTable *u = a.uniq;
+    const int U = a.ctrl[kCtrlNumUnique];
+    float acc[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < U; ++s) {
+        const int e = u->expert[s];
+        const int nt = u->ntok[s];
+        const uint8_t *row = a.wd + ((size_t)e * a.H + c) * row_bytes;
+        int sl[SI_MAX_DECODE_TOKENS];
+#pragma unroll
+        for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t)
+            sl[t] = (t < nt) ? u->tok[s][t] * a.k + u->slot[s][t] : 0;
+        float y[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
+        for (int it = gl; it < 4 * nbI; it += GS) {
+            const int b = it >> 2, i = it & 3;
+            const uint8_t *blk = row + b * kBlockBytes;
+            const uint4 hd = ldg_nc_v4(blk), q0 = ldg_nc_v4(blk + 16 + 32 * i),
+                        q1 = ldg_nc_v4(blk + 32 + 32 * i);
+            const SubScales sc = chunk_scales(hd, i);
+#pragma unroll
+            for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
+                if (t < nt) {
+                    const float *ha = a.h + (size_t)sl[t] * a.I + kQK * b + 64 * i;
+                    const f32x2 *pa = reinterpret_cast<const f32x2 *>(ha);
+                    const f32x2 *pb = reinterpret_cast<const f32x2 *>(ha + 32);
+                    auto xa2 = [pa](int p) { return __ldg(pa + p); };
+                    auto xb2 = [pb](int p) { return __ldg(pb + p); };
+                    const float Xa = Hs[sl[t] * nIs + 8 * b + 2 * i];
+                    const float Xb = Hs[sl[t] * nIs + 8 * b + 2 * i + 1];
+                    y[t] += chunk_contrib(sc, chunk_code_sums(q0, q1, xa2, xb2), Xa, Xb);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
+            if (t < nt) {
+                const float ys = group_sum<GS>(y[t]);
+                const int tk = u->tok[s][t];
+                const float w = a.wts[sl[t]];
+#pragma unroll
+                for (int q = 0; q < SI_MAX_DECODE_TOKENS; ++q)
+                    if (q == tk) acc[q] = fmaf(w, ys, acc[q]);
+            }
+        }
+    }
+    if (gl == 0 && c < a.H) {
+#pragma unroll
+        for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t)
+            if (t < a.n) a.out[(size_t)t * a.H + c] = acc[t];
+    }
+}
+
+// --------------------------------------------------------------- launcher
+static int pow2_at_least(int v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+static cudaError_t mark(cudaEvent_t const *events, int i, cudaStream_t s) {
+    if (!events || !events[i]) return cudaSuccess;
+    return cudaEventRecordWithFlags(events[i], s, cudaEventRecordExternal);
+}
+
+cudaError_t launch_decode(const Plan &p, const DecodeArgs &a, cudaStream_t s,
+                          cudaEvent_t const *events) {
+    (void)p;
+    cudaError_t err = mark(events, 0, s);
+    if (err != cudaSuccess) return err;
+    const int router_blocks = (a.E + kWarps - 1) / kWarps;
+    k_router_topk<<<router_blocks, kThreads, 0, s>>>(a);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    if ((err = mark(events, 1, s)) != cudaSuccess) return err;
+
+    const size_t gu_smem = (size_t)a.n * a.H * sizeof(float) + (size_t)a.n * (a.H / 32) * sizeof(float);
+    if (gu_smem > 48 * 1024) {
+        err = cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gu_smem);
+        if (err != cudaSuccess) return err;
+    }
+    const int slots = a.n * a.k;
+    const int gu_blocks = (slots * a.I + kWarps - 1) / kWarps;
+    k_gateup<<<gu_blocks, kThreads, gu_smem, s>>>(a);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    if ((err = mark(events, 2, s)) != cudaSuccess) return err;
+
+    const size_t dn_smem = (size_t)slots * (a.I / 32) * sizeof(float);
+    const int gs = pow2_at_least(4 * (a.I / kQK) < 32 ? 4 * (a.I / kQK) : 32);
+    const int rows_per_block = kWarps * (32 / gs);
+    const int dn_blocks = (a.H + rows_per_block - 1) / rows_per_block;
+    switch (gs) {
+        case 4: k_down<4><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
+        case 8: k_down<8><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
+        case 16: k_down<16><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
+        default: k_down<32><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    return mark(events, 3, s);
+}
+
+}  // namespace si

@@ -1,0 +1,71 @@
+// si_internal.h -- host-side plan, scratch layout and kernel launchers.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/si_moe.h"
+
+namespace si {
+
+// Scratch control block (int32 words at the start of every scratch buffer).
+enum CtrlWord : int {
+    kCtrlStatus = 0,        // first device-side error code (si_status), 0 = none
+    kCtrlRouterTicket = 1,  // arrival counter of the router CTAs (self-resetting)
+    kCtrlNumUnique = 2,     // distinct experts selected by this decode call
+    kCtrlWords = 64,
+};
+constexpr size_t kCtrlBytes = kCtrlWords * sizeof(int32_t);
+constexpr int kMaxSlots = SI_MAX_DECODE_TOKENS * SI_MAX_TOPK;  // 64
+
+// Table of the distinct experts of one decode call (all int32).
+struct UniqTable {
+    int32_t expert[kMaxSlots];                        // ascending expert ids
+    int32_t ntok[kMaxSlots];                          // tokens that chose it
+    int32_t tok[kMaxSlots][SI_MAX_DECODE_TOKENS];     // which tokens
+    int32_t slot[kMaxSlots][SI_MAX_DECODE_TOKENS];    // at which top-k slot
+};
+
+struct DecodeLayout {
+    size_t ctrl, logits, ids, wts, counts, uniq, h, total;
+};
+
+struct Plan {
+    si_moe_desc desc;
+    int device;
+    int sm_count;
+    int l2_bytes;
+    int smem_optin;
+    DecodeLayout dec;  // sized for SI_MAX_DECODE_TOKENS tokens
+};
+
+DecodeLayout decode_layout(const si_moe_desc &d, int n_tokens);
+
+// Arguments of the decode kernels (device pointers + sizes).
+struct DecodeArgs {
+    const uint8_t *wg, *wu, *wd;
+    const float *router_w, *router_bias;
+    const uint16_t *x;  // [n][H] bf16 bits
+    float *out;         // [n][H]
+    int H, I, E, k, n;
+    int32_t *ctrl;
+    float *logits;  // [n][E]
+    int32_t *ids;   // [n][k]
+    float *wts;     // [n][k]
+    int32_t *counts;
+    UniqTable *uniq;
+    float *h;  // [n][k][I]
+    int32_t *o_ids;
+    float *o_w;
+    int32_t *o_counts;
+    float *o_logits;
+};
+
+cudaError_t launch_decode(const Plan &p, const DecodeArgs &a, cudaStream_t s,
+                          cudaEvent_t const *events = nullptr);
+cudaError_t launch_debug_dequant(const uint8_t *blocks, int64_t n_blocks, float *out_f32,
+                                 uint16_t *out_bf16, cudaStream_t s);
+cudaError_t launch_debug_topk(const float *logits, int n, int E, int k, int32_t *ids, float *w,
+                              int32_t *counts, cudaStream_t s);
+
+}  // namespace si

@@ -1,0 +1,60 @@
+"""Device residency for layers and tokens (torch owns the memory).
+
+Weights stay in GGUF Q4_K form in HBM, exactly the bytes the generator (or
+a GGUF file) holds; nothing is repacked or dequantized ahead of time.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import binding
+from .synth import MoeLayer, MoeShape
+
+
+@dataclass
+class DeviceLayer:
+    shape: MoeShape
+    w_gate: torch.Tensor      # uint8 [E, I, H/256, 144]
+    w_up: torch.Tensor
+    w_down: torch.Tensor      # uint8 [E, H, I/256, 144]
+    router_w: torch.Tensor    # float32 [E, H]
+    router_bias: Optional[torch.Tensor] = None
+
+    def struct(self) -> binding.si_moe_layer:
+        return binding.layer_struct(self.w_gate, self.w_up, self.w_down, self.router_w,
+                                    self.router_bias)
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.w_gate, self.w_up, self.w_down,
+                                                            self.router_w))
+
+
+def to_device(layer: MoeLayer, device="cuda") -> DeviceLayer:
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    bias = None if layer.router_bias is None else up(layer.router_bias)
+    return DeviceLayer(layer.shape, up(layer.w_gate), up(layer.w_up), up(layer.w_down),
+                       up(layer.router_w), bias)
+
+
+def tokens_to_device(x_bits: np.ndarray, device="cuda") -> torch.Tensor:
+    """bf16 bit patterns (uint16 numpy) -> torch.bfloat16 device tensor."""
+    t = torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def desc_for(shape: MoeShape, max_tokens: int = 1) -> binding.si_moe_desc:
+    return binding.make_desc(shape.hidden, shape.intermediate, shape.n_experts, shape.top_k, max_tokens)
+
+
+def alloc_scratch(plan: binding.Plan, mode: int, n_tokens: int, device="cuda",
+                  stream=None) -> torch.Tensor:
+    nbytes = binding.si_moe_scratch_bytes(plan, mode, n_tokens)
+    t = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    binding.si_moe_scratch_init(plan, t, stream)
+    return t

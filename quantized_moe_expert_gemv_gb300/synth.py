@@ -167,3 +167,50 @@ WORKLOADS = {
     "dedup4": dict(shape=QWEN3_30B_A3B, seed=3, tokens_per_step=4, n_steps=512),
     "prefill": dict(shape=QWEN3_30B_A3B, seed=4, n_tokens=4096),
 }
+
+
+# ---------------------------------------------------------------------------
+# Device-side drawing for the 48-layer stack (16 GB of Q4_K bytes): the same
+# distributions as q4k_random_blocks, drawn by torch's CUDA generator so the
+# stack is resident in seconds.  The oracle never reads these layers; parity
+# of the per-layer kernels is established on numpy-drawn layers of the same
+# shape.
+# ---------------------------------------------------------------------------
+def _torch_seed(*key) -> int:
+    return int(rng(*key).integers(0, 2**62))
+
+
+def q4k_random_blocks_torch(n_blocks: int, seed_key: tuple, device="cuda"):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(_torch_seed(*seed_key))
+    raw = torch.randint(0, 256, (n_blocks, Q4K_BLOCK_BYTES), dtype=torch.uint8, device=device,
+                        generator=g)
+    d = (torch.rand(n_blocks, generator=g, device=device, dtype=torch.float32) * (2e-3 - 1e-4)
+         + 1e-4).to(torch.float16)
+    dmin = (torch.rand(n_blocks, generator=g, device=device, dtype=torch.float32) * 1e-3).to(torch.float16)
+    raw[:, 0:2] = d.view(torch.uint8).view(n_blocks, 2)
+    raw[:, 2:4] = dmin.view(torch.uint8).view(n_blocks, 2)
+    return raw
+
+
+def make_layer_torch(shape: MoeShape, seed: int, layer: int, device="cuda"):
+    """(w_gate, w_up, w_down, router_w) as device tensors for one layer."""
+    import torch
+    E, H, I = shape.n_experts, shape.hidden, shape.intermediate
+    nbh, nbi = shape.blocks_per_gate_row, shape.blocks_per_down_row
+    wg = q4k_random_blocks_torch(E * I * nbh, (seed, layer, "gate-dev"), device).view(E, I, nbh, 144)
+    wu = q4k_random_blocks_torch(E * I * nbh, (seed, layer, "up-dev"), device).view(E, I, nbh, 144)
+    wd = q4k_random_blocks_torch(E * H * nbi, (seed, layer, "down-dev"), device).view(E, H, nbi, 144)
+    g = torch.Generator(device=device)
+    g.manual_seed(_torch_seed(seed, layer, "router-dev"))
+    rw = torch.randn((E, H), generator=g, device=device, dtype=torch.float32) * 0.02
+    return wg, wu, wd, rw
+
+
+def make_tokens_torch(n: int, hidden: int, seed_key: tuple, device="cuda"):
+    """bf16 N(0,1) activations [n, hidden] drawn on the device."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(_torch_seed(*seed_key))
+    return torch.randn((n, hidden), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)

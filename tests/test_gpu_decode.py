@@ -1,0 +1,275 @@
+"""GPU parity of the decode path (router, top-k, gate/up GEMV + SwiGLU,
+down GEMV + weighted combine, deduplicated small batches) against the CPU
+oracle, through the C ABI."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from quantized_moe_expert_gemv_gb300 import binding, build, device, synth
+from tests import parity
+from tests.q4k_fixtures import make_block
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    binding.load_library()
+    oracle.build()
+
+
+class Runner:
+    """Plan + scratch + device layer for one shape; decode calls through the ABI."""
+
+    def __init__(self, layer: synth.MoeLayer, max_n=binding.SI_MAX_DECODE_TOKENS):
+        self.layer = layer
+        self.shape = layer.shape
+        self.dl = device.to_device(layer)
+        self.plan = binding.si_moe_plan(device.desc_for(self.shape))
+        self.scratch = device.alloc_scratch(self.plan, binding.SI_MODE_DECODE, max_n)
+
+    def decode(self, x_bits: np.ndarray):
+        s = self.shape
+        n = x_bits.shape[0]
+        x = device.tokens_to_device(x_bits)
+        out = torch.empty((n, s.hidden), dtype=torch.float32, device="cuda")
+        ids = torch.full((n, s.top_k), -1, dtype=torch.int32, device="cuda")
+        w = torch.empty((n, s.top_k), dtype=torch.float32, device="cuda")
+        counts = torch.full((s.n_experts,), -1, dtype=torch.int32, device="cuda")
+        logits = torch.empty((n, s.n_experts), dtype=torch.float32, device="cuda")
+        ro = binding.route_struct(topk_ids=ids, topk_w=w, expert_counts=counts, logits=logits)
+        binding.si_moe_forward_decode(self.plan, self.dl.struct(), x, n, out, ro, self.scratch)
+        assert binding.si_moe_read_status(self.plan, self.scratch) == binding.SI_OK
+        return (out.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy(), counts.cpu().numpy(),
+                logits.cpu().numpy())
+
+
+def check_tokens(layer, x_bits, out, ids, w, sample=None):
+    """Compare per-token GPU results with the oracle; return #near-tie tokens."""
+    s = layer.shape
+    rows = range(x_bits.shape[0]) if sample is None else sample
+    o_ids, o_w, z64, margin = oracle.route_tokens(layer.router_w, x_bits, s.top_k,
+                                                  bias=layer.router_bias, want_logits=True)
+    near = 0
+    for t in range(x_bits.shape[0]):
+        if not parity.routing_ok(ids[t], o_ids[t], z64[t], margin[t], s.top_k):
+            near += 1
+            continue
+        np.testing.assert_allclose(w[t], o_w[t], rtol=0, atol=2e-6)
+        assert abs(float(w[t].sum()) - 1.0) < 1e-5
+    for t in rows:
+        if not np.array_equal(ids[t], o_ids[t]):
+            continue
+        ref = oracle.moe_token(layer, x_bits[t])
+        parity.assert_close(out[t], ref.out64, f"token {t}")
+    return near
+
+
+# ------------------------------------------------------------------ dequant
+def test_debug_dequant_bit_exact_against_oracle():
+    g = synth.rng(100)
+    tiny = synth.make_layer(synth.TINY, seed=0)
+    parts = [tiny.w_gate.reshape(-1, 144), tiny.w_down.reshape(-1, 144),
+             synth.q4k_random_blocks(g, 5000)]
+    # closed-form blocks: every sub-block alone, scales with the high bits set
+    for j in range(8):
+        sc = [0] * 8
+        sc[j] = 63 - j
+        m = [0] * 8
+        m[(j + 3) % 8] = 40 + j
+        parts.append(make_block(0.0017, 0.0009, sc, m, np.full((8, 32), j + 3))[None])
+    # special fp16 values of d and dmin: subnormals, zero, largest finite
+    spec = synth.q4k_random_blocks(g, 6)
+    for i, (dh, mh) in enumerate([(0x0001, 0x03ff), (0x0000, 0x0400), (0x7bff, 0x0000),
+                                  (0x3c00, 0x3c00), (0x8001, 0x0002), (0x1234, 0xb800)]):
+        spec[i, 0:2] = np.array([dh & 255, dh >> 8], dtype=np.uint8)
+        spec[i, 2:4] = np.array([mh & 255, mh >> 8], dtype=np.uint8)
+    parts.append(spec)
+    blocks = np.ascontiguousarray(np.concatenate(parts, axis=0))
+    n = blocks.shape[0]
+    ref = oracle.q4k_dequant(blocks)
+    dev_blocks = torch.from_numpy(blocks).cuda()
+    f32 = torch.empty(n * 256, dtype=torch.float32, device="cuda")
+    bf = torch.empty(n * 256, dtype=torch.int16, device="cuda")
+    binding.si_debug_q4k_dequant(dev_blocks, n, f32, bf)
+    torch.cuda.synchronize()
+    got = f32.cpu().numpy()
+    finite = np.isfinite(ref)
+    assert np.array_equal(got.view(np.uint32)[finite], ref.view(np.uint32)[finite])
+    ref_bf = torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(bf.cpu().numpy()[finite], ref_bf[finite])
+
+
+def test_debug_dequant_qwen_layer_sample_bit_exact():
+    layer_blocks = synth.q4k_random_blocks(synth.rng(1, 0, "gate"), 200_000)
+    ref = oracle.q4k_dequant(layer_blocks)
+    dev = torch.from_numpy(layer_blocks).cuda()
+    f32 = torch.empty(ref.size, dtype=torch.float32, device="cuda")
+    binding.si_debug_q4k_dequant(dev, layer_blocks.shape[0], f32, None)
+    assert np.array_equal(f32.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+# -------------------------------------------------------------------- top-k
+@pytest.mark.parametrize("E,k", [(8, 2), (128, 8), (256, 16), (16, 16), (5, 1), (33, 7)])
+def test_debug_topk_bit_exact(E, k):
+    g = np.random.default_rng(E * 100 + k)
+    for trial in range(20):
+        n = 1 + trial % 4
+        if trial % 2:
+            z = (g.integers(-4, 4, (n, E)) * 0.5).astype(np.float32)     # many exact ties
+        else:
+            z = g.normal(0, 1, (n, E)).astype(np.float32)
+        desc = binding.make_desc(256, 256, E, k)
+        ids = torch.full((n, k), -1, dtype=torch.int32, device="cuda")
+        w = torch.empty((n, k), dtype=torch.float32, device="cuda")
+        counts = torch.empty(E, dtype=torch.int32, device="cuda")
+        binding.si_debug_topk(torch.from_numpy(z).cuda(), n, desc,
+                              binding.route_struct(topk_ids=ids, topk_w=w, expert_counts=counts))
+        ids_h, w_h = ids.cpu().numpy(), w.cpu().numpy()
+        ref_counts = np.zeros(E, dtype=np.int64)
+        for t in range(n):
+            o = oracle.topk(z[t], k)
+            assert np.array_equal(ids_h[t], o)
+            np.testing.assert_allclose(w_h[t], oracle.renorm_weights(z[t].astype(np.float64), o),
+                                       rtol=0, atol=2e-6)
+            ref_counts[o] += 1
+        assert np.array_equal(counts.cpu().numpy(), ref_counts)
+
+
+# ------------------------------------------------------------ decode paths
+def test_decode_tiny_layer_seed0():
+    wl = synth.WORKLOADS["tiny"]
+    layer = synth.make_layer(wl["shape"], seed=wl["seed"])
+    x = synth.make_tokens(wl["shape"], seed=wl["seed"], n_tokens=33)
+    r = Runner(layer)
+    outs, idss, ws = [], [], []
+    for t in range(x.shape[0]):
+        out, ids, w, counts, logits = r.decode(x[t:t + 1])
+        ref_counts = np.bincount(ids[0], minlength=layer.shape.n_experts)
+        assert np.array_equal(counts, ref_counts)
+        z_ref = oracle.router_logits(layer.router_w, x[t])
+        np.testing.assert_allclose(logits[0], z_ref, rtol=0, atol=1e-5)
+        outs.append(out[0]), idss.append(ids[0]), ws.append(w[0])
+    near = check_tokens(layer, x, np.array(outs), np.array(idss), np.array(ws))
+    assert near <= 1
+
+
+def test_decode_qwen3_layer_routing_all_tokens_outputs_sampled():
+    wl = synth.WORKLOADS["layer"]
+    shape = wl["shape"]
+    layer = synth.make_layer(shape, seed=wl["seed"])
+    x = synth.make_tokens(shape, seed=wl["seed"], n_tokens=wl["n_tokens"])
+    r = Runner(layer)
+    outs = np.empty((x.shape[0], shape.hidden), np.float32)
+    ids = np.empty((x.shape[0], shape.top_k), np.int32)
+    ws = np.empty((x.shape[0], shape.top_k), np.float32)
+    for t in range(x.shape[0]):
+        o, i, w, c, _ = r.decode(x[t:t + 1])
+        outs[t], ids[t], ws[t] = o[0], i[0], w[0]
+        assert c.sum() == shape.top_k
+    sample = list(range(0, x.shape[0], 97)) + [x.shape[0] - 1]
+    near = check_tokens(layer, x, outs, ids, ws, sample=sample)
+    assert near <= 3
+
+
+@pytest.mark.parametrize("n", [2, 3, 4])
+def test_decode_dedup_batches_match_per_token_oracle(n):
+    wl = synth.WORKLOADS["dedup4"]
+    shape, seed = wl["shape"], wl["seed"]
+    bias = synth.dedup_router_bias(seed, synth.load_dedup_beta())
+    layer = synth.make_layer(shape, seed=seed, router_bias=bias)
+    x_all = synth.make_tokens(shape, seed, 4 * 6)
+    r = Runner(layer)
+    for step in range(3):
+        x = x_all[4 * step: 4 * step + n]
+        out, ids, w, counts, _ = r.decode(x)
+        assert np.array_equal(counts, np.bincount(ids.reshape(-1), minlength=shape.n_experts))
+        check_tokens(layer, x, out, ids, w)
+        # one decode of n tokens == n decodes of one token
+        for t in range(n):
+            o1, i1, _, _, _ = r.decode(x[t:t + 1])
+            assert np.array_equal(i1[0], ids[t])
+            parity.assert_close(out[t], o1[0], "batched vs single")
+
+
+@pytest.mark.parametrize("H,I,E,k,n", [
+    (256, 256, 8, 2, 1), (512, 768, 16, 4, 3), (768, 512, 4, 4, 2), (1024, 256, 32, 1, 4),
+    (256, 1280, 6, 3, 1), (4096, 256, 8, 8, 2), (256, 256, 1, 1, 1), (2048, 768, 256, 16, 4),
+])
+def test_decode_shapes(H, I, E, k, n):
+    shape = synth.MoeShape(H, I, E, k)
+    layer = synth.make_layer(shape, seed=H + I + E + k)
+    x = synth.make_tokens(shape, seed=7, n_tokens=n)
+    out, ids, w, counts, _ = Runner(layer).decode(x)
+    near = check_tokens(layer, x, out, ids, w)
+    assert near == 0
+
+
+def test_decode_identical_experts_any_routing():
+    shape = synth.MoeShape(512, 512, 16, 4)
+    layer = synth.make_layer(shape, seed=31)
+    for name in ("w_gate", "w_up", "w_down"):
+        arr = getattr(layer, name)
+        arr[:] = arr[0]
+    x = synth.make_tokens(shape, seed=31, n_tokens=4)
+    out, _, _, _, _ = Runner(layer).decode(x)
+    for t in range(4):
+        xf = synth.bf16_to_f32(x[t]).astype(np.float64)
+        _, y = oracle.expert_ffn(layer.w_gate[0], layer.w_up[0], layer.w_down[0], xf, 512, 512)
+        parity.assert_close(out[t], y, "identical experts")
+
+
+def test_decode_argument_errors():
+    shape = synth.TINY
+    layer = synth.make_layer(shape, seed=0)
+    r = Runner(layer)
+    x = device.tokens_to_device(synth.make_tokens(shape, 0, 2))
+    out = torch.empty((2, shape.hidden), dtype=torch.float32, device="cuda")
+    L = r.dl.struct()
+
+    def call(xp, n, outp, scratch, nbytes=None):
+        lib = binding.load_library()
+        nb = nbytes if nbytes is not None else scratch.numel()
+        import ctypes
+        return lib.si_moe_forward_decode(r.plan.handle, ctypes.byref(L), xp, n, outp, None,
+                                         scratch.data_ptr(), nb, torch.cuda.current_stream().cuda_stream)
+
+    assert call(x.data_ptr() + 2, 1, out.data_ptr(), r.scratch) == binding.SI_ERR_MISALIGNED
+    assert call(x.data_ptr(), 1, out.data_ptr() + 4, r.scratch) == binding.SI_ERR_MISALIGNED
+    assert call(x.data_ptr(), 0, out.data_ptr(), r.scratch) == binding.SI_ERR_INVALID_ARG
+    assert call(x.data_ptr(), 5, out.data_ptr(), r.scratch) == binding.SI_ERR_INVALID_ARG
+    need = binding.si_moe_scratch_bytes(r.plan, binding.SI_MODE_DECODE, 2)
+    assert call(x.data_ptr(), 2, out.data_ptr(), r.scratch, need - 1) == binding.SI_ERR_SCRATCH_TOO_SMALL
+    assert call(x.data_ptr(), 2, out.data_ptr(), r.scratch, need) == binding.SI_OK
+    assert binding.si_moe_read_status(r.plan, r.scratch) == binding.SI_OK
+
+
+def test_decode_in_cuda_graph_matches_eager():
+    wl = synth.WORKLOADS["layer"]
+    shape = wl["shape"]
+    layer = synth.make_layer(shape, seed=wl["seed"])
+    r = Runner(layer)
+    xb = synth.make_tokens(shape, seed=wl["seed"], n_tokens=8)
+    x = device.tokens_to_device(xb)
+    out = torch.zeros((8, shape.hidden), dtype=torch.float32, device="cuda")
+    L = r.dl.struct()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for t in range(8):   # warm-up outside capture
+            binding.si_moe_forward_decode(r.plan, L, x[t], 1, out[t], None, r.scratch, stream=s)
+    s.synchronize()
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for t in range(8):
+            binding.si_moe_forward_decode(r.plan, L, x[t], 1, out[t], None, r.scratch, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
