@@ -53,7 +53,7 @@ def parse_args():
     p.add_argument("--tokens", type=int, default=0,
                    help="tokens per step of the headline layer (default 1024; small values for ncu)")
     p.add_argument("--cpu-sample-tokens", type=int, default=0,
-                   help="tokens of the CPU oracle sample (default: 4 per host core, at least 16)")
+                   help="tokens of the CPU oracle sample (default: 16 per host core, at least 64)")
     return p.parse_args()
 
 
@@ -445,7 +445,7 @@ def run_ours(args, dist):
             line["dedup4"] = {"error": repr(exc)}
     if dist.rank == 0 and not args.no_cpu_baseline:
         cores = cpu_cores()
-        n = args.cpu_sample_tokens or max(16, 4 * cores)
+        n = args.cpu_sample_tokens or max(64, 16 * cores)
         tps, dt = oracle_tokens_per_s(n, cores)
         line["cpu_baseline"] = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{n} tokens of the headline layer, one per thread, {dt:.1f} s"}
