@@ -143,6 +143,30 @@ si_status si_moe_read_status(si_moe_plan_t plan, const void *scratch, si_stream_
 
 const char *si_status_string(si_status status);
 
+/* Decode without a caller scratch buffer, for callers that cannot allocate
+ * device memory: for example a plug-in inside a host framework whose memory
+ * pool owns all device memory and gives it no allocator, or a latency-
+ * critical decode loop where cudaMalloc would synchronise the device.  (The
+ * sparkinfer pages have no counterpart of this entry point.)
+ * Same arguments, results and errors as si_moe_forward_decode, minus the
+ * scratch pointer and size.  The scratch is one fixed device array of
+ * SI_STATIC_SCRATCH_BYTES per GPU, part of the library's module image: every
+ * GPU that loads the library holds it until the process exits.  A call whose
+ * shape needs more scratch (si_moe_scratch_bytes) is rejected with
+ * SI_ERR_SCRATCH_TOO_SMALL before any launch.  The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).  The first call on
+ * a device looks up the array's device address with that device current; make
+ * that first call before any stream capture.  Every call on a device shares
+ * the one array, which keeps the previous call's contents; each call clears
+ * the words that must start at zero (stream-ordered).  Calls that may overlap
+ * on the GPU (different streams, or unordered host threads) race on the array:
+ * order them.  Device-side status of these calls is not readable through
+ * si_moe_read_status. */
+#define SI_STATIC_SCRATCH_BYTES (1u << 20)
+si_status si_moe_forward_decode_noalloc(si_moe_plan_t plan, const si_moe_layer *layer,
+                                        const void *x_bf16, int32_t n_tokens, float *out,
+                                        si_moe_route_out *route_out, si_stream_t stream);
+
 /* Test exports.  si_debug_q4k_dequant decodes n_blocks Q4_K blocks into
  * out_f32 [n_blocks*256] and/or out_bf16 [n_blocks*256] (either may be
  * NULL): w = d*sc*q - dmin*m rounded once to fp32 (bf16: round-to-nearest-

@@ -32,6 +32,7 @@ SI_MODE_PREFILL = 1
 SI_MAX_EXPERTS = 256
 SI_MAX_TOPK = 16
 SI_MAX_DECODE_TOKENS = 4
+SI_STATIC_SCRATCH_BYTES = 1 << 20
 
 
 class SiError(RuntimeError):
@@ -95,6 +96,9 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.si_debug_decode_events.argtypes = [vp, ctypes.POINTER(si_moe_layer), vp, i32, vp,
                                            ctypes.POINTER(si_moe_route_out), vp, sz,
                                            ctypes.POINTER(vp), vp]
+    lib.si_moe_forward_decode_noalloc.restype = ctypes.c_int
+    lib.si_moe_forward_decode_noalloc.argtypes = [vp, ctypes.POINTER(si_moe_layer), vp, i32, vp,
+                                                  ctypes.POINTER(si_moe_route_out), vp]
     lib.si_moe_read_status.restype = ctypes.c_int
     lib.si_moe_read_status.argtypes = [vp, vp, vp]
     lib.si_debug_q4k_dequant.restype = ctypes.c_int
@@ -220,6 +224,18 @@ def si_moe_forward_prefill(plan, layer: si_moe_layer, x, n_tokens, out, route_ou
                            stream=None, raw_status=False):
     return _forward("si_moe_forward_prefill", plan, layer, x, n_tokens, out, route_out, scratch, stream,
                     raw_status)
+
+
+def si_moe_forward_decode_noalloc(plan, layer: si_moe_layer, x, n_tokens, out, route_out=None,
+                                  stream=None, raw_status=False):
+    """Decode with the library's built-in device scratch (no caller buffer,
+    no allocation); see include/si_moe.h for its limits."""
+    ro = ctypes.byref(route_out) if route_out is not None else None
+    st = load_library().si_moe_forward_decode_noalloc(plan.handle, ctypes.byref(layer), _ptr(x),
+                                                      int(n_tokens), _ptr(out), ro, _stream(stream))
+    if not raw_status:
+        _check(st, "si_moe_forward_decode_noalloc")
+    return st
 
 
 def si_debug_decode_events(plan, layer: si_moe_layer, x, n_tokens, out, route_out=None, scratch=None,
