@@ -167,6 +167,12 @@ si_status si_moe_forward_decode_noalloc(si_moe_plan_t plan, const si_moe_layer *
                                         const void *x_bf16, int32_t n_tokens, float *out,
                                         si_moe_route_out *route_out, si_stream_t stream);
 
+/* Test/bench export: 1 if decode of n_tokens tokens runs the fused expert
+ * kernel (one launch for gate/up, SwiGLU, down and combine after the router
+ * launch), 0 if it runs the generic gate/up + down kernels, -1 on a bad
+ * argument. */
+int si_debug_decode_fused(si_moe_plan_t plan, int32_t n_tokens);
+
 /* Test exports.  si_debug_q4k_dequant decodes n_blocks Q4_K blocks into
  * out_f32 [n_blocks*256] and/or out_bf16 [n_blocks*256] (either may be
  * NULL): w = d*sc*q - dmin*m rounded once to fp32 (bf16: round-to-nearest-

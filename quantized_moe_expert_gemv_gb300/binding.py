@@ -99,6 +99,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.si_moe_forward_decode_noalloc.restype = ctypes.c_int
     lib.si_moe_forward_decode_noalloc.argtypes = [vp, ctypes.POINTER(si_moe_layer), vp, i32, vp,
                                                   ctypes.POINTER(si_moe_route_out), vp]
+    lib.si_debug_decode_fused.restype = ctypes.c_int
+    lib.si_debug_decode_fused.argtypes = [vp, i32]
     lib.si_moe_read_status.restype = ctypes.c_int
     lib.si_moe_read_status.argtypes = [vp, vp, vp]
     lib.si_debug_q4k_dequant.restype = ctypes.c_int
@@ -115,7 +117,7 @@ def declared_symbols() -> list[str]:
     """Names of the functions include/si_moe.h declares."""
     with open(HEADER_PATH) as f:
         text = f.read()
-    return sorted(set(re.findall(r"^\s*(?:si_status|void|const char \*)\s*\*?\s*(si_\w+)\s*\(",
+    return sorted(set(re.findall(r"^\s*(?:si_status|void|int|const char \*)\s*\*?\s*(si_\w+)\s*\(",
                                  text, flags=re.M)))
 
 
@@ -249,6 +251,10 @@ def si_debug_decode_events(plan, layer: si_moe_layer, x, n_tokens, out, route_ou
     _check(lib.si_debug_decode_events(plan.handle, ctypes.byref(layer), _ptr(x), int(n_tokens), _ptr(out),
                                       ro, _ptr(scratch), nbytes, ev, _stream(stream)),
            "si_debug_decode_events")
+
+
+def si_debug_decode_fused(plan: Plan, n_tokens: int) -> int:
+    return load_library().si_debug_decode_fused(plan.handle, int(n_tokens))
 
 
 def si_moe_read_status(plan: Plan, scratch, stream=None) -> int:

@@ -2,6 +2,7 @@
 // layout and stream-ordered launches.  Nothing here allocates device memory
 // or synchronises, except si_moe_read_status (which is documented to).
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -94,6 +95,29 @@ si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *o
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, cuda_device);
     if (major != 10 || minor != 3) return SI_ERR_UNSUPPORTED;  // built for sm_103a only
     p.dec = si::decode_layout(*desc, SI_MAX_DECODE_TOKENS);
+    // Bounded device-side waits: about one second at GB300 clocks.  A test may
+    // shorten the budget through SI_FAULT_WAIT_BUDGET (a non-negative decimal
+    // cycle count); unset or malformed leaves the default.
+    p.wait_budget = 2000000000LL;
+    if (const char *env = std::getenv("SI_FAULT_WAIT_BUDGET")) {
+        char *end = nullptr;
+        const long long v = std::strtoll(env, &end, 10);
+        if (end && end != env && *end == '\0' && v >= 0) p.wait_budget = v;
+    }
+    const int cur_dev = [] { int d = 0; cudaGetDevice(&d); return d; }();
+    if (cur_dev != cuda_device) cudaSetDevice(cuda_device);
+    for (int n = 1; n <= SI_MAX_DECODE_TOKENS; ++n) {
+        si::DecodeArgs tmp{};
+        p.fused_ok[n] = false;
+        if (si::expert_fused_layout(*desc, n, p.sm_count, p.smem_optin, tmp)) {
+            int per_sm = 0;
+            if (si::expert_fused_occupancy(desc->hidden / 256, n > 1, tmp.fz_smem, p.smem_optin, &per_sm) == cudaSuccess &&
+                per_sm >= 1)
+                p.fused_ok[n] = true;
+            cudaGetLastError();
+        }
+    }
+    if (cur_dev != cuda_device) cudaSetDevice(cur_dev);
     si_moe_plan_s *h = new (std::nothrow) si_moe_plan_s;
     if (!h) return SI_ERR_INVALID_ARG;
     h->p = p;
@@ -200,6 +224,11 @@ si_status si_moe_forward_prefill(si_moe_plan_t plan, const si_moe_layer *layer, 
     (void)scratch_bytes; (void)stream;
     if (!plan) return SI_ERR_INVALID_ARG;
     return SI_ERR_UNSUPPORTED;
+}
+
+int si_debug_decode_fused(si_moe_plan_t plan, int32_t n_tokens) {
+    if (!plan || n_tokens < 1 || n_tokens > SI_MAX_DECODE_TOKENS) return -1;
+    return plan->p.fused_ok[n_tokens] ? 1 : 0;
 }
 
 si_status si_moe_read_status(si_moe_plan_t plan, const void *scratch, si_stream_t stream) {

@@ -24,29 +24,60 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
 // --------------------------------------------------------------- router
+__device__ __forceinline__ float dot8_bf16(const float4 &w0, const float4 &w1, const uint4 &xv, float s) {
+    s = fmaf(w0.x, __uint_as_float(xv.x << 16), s);
+    s = fmaf(w0.y, __uint_as_float(xv.x & 0xffff0000u), s);
+    s = fmaf(w0.z, __uint_as_float(xv.y << 16), s);
+    s = fmaf(w0.w, __uint_as_float(xv.y & 0xffff0000u), s);
+    s = fmaf(w1.x, __uint_as_float(xv.z << 16), s);
+    s = fmaf(w1.y, __uint_as_float(xv.z & 0xffff0000u), s);
+    s = fmaf(w1.z, __uint_as_float(xv.w << 16), s);
+    s = fmaf(w1.w, __uint_as_float(xv.w & 0xffff0000u), s);
+    return s;
+}
+
+// NJ > 0: H == 256*NJ and the router row is loaded into registers before the
+// programmatic-dependent-launch wait (router weights do not depend on the
+// token, so this overlaps the previous kernel's tail).  NJ == 0: any H.
+template <int NJ>
 __global__ void __launch_bounds__(kThreads) k_router_topk(DecodeArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kWarps + warp;
+    const float *wrow = a.router_w + (size_t)min(e, a.E - 1) * a.H;
+    float4 wr[2 * (NJ > 0 ? NJ : 1)];
+    if (NJ > 0) {
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            wr[2 * j] = __ldg(reinterpret_cast<const float4 *>(wrow + 256 * j + 8 * lane));
+            wr[2 * j + 1] = __ldg(reinterpret_cast<const float4 *>(wrow + 256 * j + 8 * lane + 4));
+        }
+    }
+    pdl_launch_dependents();  // the expert kernel may become resident now
+    pdl_wait();               // x and the scratch are ready (previous kernels complete)
     if (e < a.E) {
         float acc[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
-        const float *wrow = a.router_w + (size_t)e * a.H;
-        for (int c = 8 * lane; c < a.H; c += 256) {
-            const float4 w0 = __ldg(reinterpret_cast<const float4 *>(wrow + c));
-            const float4 w1 = __ldg(reinterpret_cast<const float4 *>(wrow + c + 4));
+        if (NJ > 0) {
 #pragma unroll
-            for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
-                if (t < a.n) {
-                    const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + c));
-                    float s = acc[t];
-                    s = fmaf(w0.x, __uint_as_float(xv.x << 16), s);
-                    s = fmaf(w0.y, __uint_as_float(xv.x & 0xffff0000u), s);
-                    s = fmaf(w0.z, __uint_as_float(xv.y << 16), s);
-                    s = fmaf(w0.w, __uint_as_float(xv.y & 0xffff0000u), s);
-                    s = fmaf(w1.x, __uint_as_float(xv.z << 16), s);
-                    s = fmaf(w1.y, __uint_as_float(xv.z & 0xffff0000u), s);
-                    s = fmaf(w1.z, __uint_as_float(xv.w << 16), s);
-                    s = fmaf(w1.w, __uint_as_float(xv.w & 0xffff0000u), s);
-                    acc[t] = s;
+            for (int j = 0; j < NJ; ++j) {
+#pragma unroll
+                for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
+                    if (t < a.n) {
+                        const uint4 xv = __ldg(
+                            reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + 256 * j + 8 * lane));
+                        acc[t] = dot8_bf16(wr[2 * j], wr[2 * j + 1], xv, acc[t]);
+                    }
+                }
+            }
+        } else {
+            for (int c = 8 * lane; c < a.H; c += 256) {
+                const float4 w0 = __ldg(reinterpret_cast<const float4 *>(wrow + c));
+                const float4 w1 = __ldg(reinterpret_cast<const float4 *>(wrow + c + 4));
+#pragma unroll
+                for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
+                    if (t < a.n) {
+                        const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + c));
+                        acc[t] = dot8_bf16(w0, w1, xv, acc[t]);
+                    }
                 }
             }
         }
@@ -189,7 +220,7 @@ __device__ __forceinline__ void gateup_rowpair(const DecodeArgs &a, const float 
     }
 }
 
-__global__ void __launch_bounds__(kThreads) k_gateup(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads) k_gateup_generic(DecodeArgs a) {
     extern __shared__ __align__(16) float smem[];
     float *xs = smem;               // [n][H]
     float *Xs = smem + a.n * a.H;   // [n][H/32] sub-block sums
@@ -219,7 +250,7 @@ __global__ void __launch_bounds__(kThreads) k_gateup(DecodeArgs a) {
 
 // ------------------------------------------------------------------- down
 template <int GS>
-__global__ void __launch_bounds__(kThreads) k_down(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads) k_down_generic(DecodeArgs a) {
     extern __shared__ __align__(16) float smem[];
     float *Hs = smem;  // [n*k][I/32] sub-block sums of h
     const int nIs = a.I / 32;
@@ -304,25 +335,60 @@ static cudaError_t mark(cudaEvent_t const *events, int i, cudaStream_t s) {
     return cudaEventRecordWithFlags(events[i], s, cudaEventRecordExternal);
 }
 
-cudaError_t launch_decode(const Plan &p, const DecodeArgs &a, cudaStream_t s,
+template <int NJ>
+static cudaError_t launch_router_t(const DecodeArgs &a, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.E + kWarps - 1) / kWarps);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_router_topk<NJ>, a);
+}
+
+static cudaError_t launch_router(const DecodeArgs &a, cudaStream_t s) {
+    switch (a.H / kQK) {
+        case 1: return launch_router_t<1>(a, s);
+        case 2: return launch_router_t<2>(a, s);
+        case 3: return launch_router_t<3>(a, s);
+        case 4: return launch_router_t<4>(a, s);
+        case 5: return launch_router_t<5>(a, s);
+        case 6: return launch_router_t<6>(a, s);
+        case 7: return launch_router_t<7>(a, s);
+        case 8: return launch_router_t<8>(a, s);
+        default: return launch_router_t<0>(a, s);
+    }
+}
+
+cudaError_t launch_decode(const Plan &p, const DecodeArgs &a_in, cudaStream_t s,
                           cudaEvent_t const *events) {
-    (void)p;
+    DecodeArgs a = a_in;
+    a.wait_budget = p.wait_budget;
     cudaError_t err = mark(events, 0, s);
     if (err != cudaSuccess) return err;
-    const int router_blocks = (a.E + kWarps - 1) / kWarps;
-    k_router_topk<<<router_blocks, kThreads, 0, s>>>(a);
-    err = cudaGetLastError();
+    err = launch_router(a, s);
     if (err != cudaSuccess) return err;
     if ((err = mark(events, 1, s)) != cudaSuccess) return err;
 
+    if (p.fused_ok[a.n] && expert_fused_layout(p.desc, a.n, p.sm_count, p.smem_optin, a)) {
+        err = launch_expert_fused(a, p.sm_count, s);
+        if (err != cudaSuccess) return err;
+        if ((err = mark(events, 2, s)) != cudaSuccess) return err;
+        return mark(events, 3, s);
+    }
+
     const size_t gu_smem = (size_t)a.n * a.H * sizeof(float) + (size_t)a.n * (a.H / 32) * sizeof(float);
     if (gu_smem > 48 * 1024) {
-        err = cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gu_smem);
+        err = cudaFuncSetAttribute(k_gateup_generic, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gu_smem);
         if (err != cudaSuccess) return err;
     }
     const int slots = a.n * a.k;
     const int gu_blocks = (slots * a.I + kWarps - 1) / kWarps;
-    k_gateup<<<gu_blocks, kThreads, gu_smem, s>>>(a);
+    k_gateup_generic<<<gu_blocks, kThreads, gu_smem, s>>>(a);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     if ((err = mark(events, 2, s)) != cudaSuccess) return err;
@@ -332,10 +398,10 @@ cudaError_t launch_decode(const Plan &p, const DecodeArgs &a, cudaStream_t s,
     const int rows_per_block = kWarps * (32 / gs);
     const int dn_blocks = (a.H + rows_per_block - 1) / rows_per_block;
     switch (gs) {
-        case 4: k_down<4><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
-        case 8: k_down<8><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
-        case 16: k_down<16><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
-        default: k_down<32><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
+        case 4: k_down_generic<4><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
+        case 8: k_down_generic<8><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
+        case 16: k_down_generic<16><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
+        default: k_down_generic<32><<<dn_blocks, kThreads, dn_smem, s>>>(a); break;
     }
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     return mark(events, 3, s);

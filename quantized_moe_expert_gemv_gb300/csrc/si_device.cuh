@@ -201,3 +201,121 @@ __device__ __forceinline__ void warp_topk(const float *z, int E, int k, int *ids
 }
 
 }  // namespace si
+
+// =====================================================================
+// Asynchronous copies, mbarriers, programmatic dependent launch, bounded
+// waits (sm_90+ PTX, used on sm_103a).
+// =====================================================================
+namespace si {
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+// Make mbarrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// L2 policy for streamed expert weights: evict first, so one token's
+// experts do not displace activations/router weights (and do not make a
+// later token's reads look like HBM reads when they are L2 hits).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Bulk global -> shared copy (TMA, non-tensor); completes `bytes` of the
+// transaction count of mbarrier `bar`.  dst/src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Record the first device-side error of a call (0 = none).
+__device__ __forceinline__ void set_status(int32_t *status, int code) { atomicCAS(status, 0, code); }
+
+// Wait for phase `parity` of an mbarrier for at most `budget` SM cycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long budget) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > budget) return false;
+        __nanosleep(20);
+    }
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid-wide barrier over all CTAs of a launch whose CTAs are all resident
+// (grid <= resident capacity).  ctr/gen are two words of the scratch control
+// block: the last arriver resets the counter and bumps the generation.
+// Called by every thread of the CTA; returns false (and records
+// SI_ERR_TIMEOUT) if the other CTAs did not arrive within `budget` cycles.
+__device__ __forceinline__ bool grid_barrier(int32_t *ctr, int32_t *gen, int32_t *status,
+                                             long long budget) {
+    __shared__ int s_ok;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int g0 = ld_acquire_gpu(gen);
+        int ok = 1;
+        if (atomicAdd(ctr, 1) == (int)gridDim.x - 1) {
+            *ctr = 0;
+            __threadfence();
+            atomicAdd(gen, 1);
+        } else {
+            const long long t0 = clock64();
+            while (ld_acquire_gpu(gen) == g0) {
+                if (clock64() - t0 > budget) {
+                    ok = 0;
+                    set_status(status, 6 /* SI_ERR_TIMEOUT */);
+                    break;
+                }
+                __nanosleep(32);
+            }
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+}  // namespace si

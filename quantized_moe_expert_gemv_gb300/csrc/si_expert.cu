@@ -1,0 +1,545 @@
+// si_expert.cu -- fused expert kernel of the decode path: for the experts the
+// router selected, dequant-on-read gate/up GEMV + SwiGLU, then the down GEMV
+// and the weighted top-k combine, in one launch.
+//
+// sparkinfer README (luciferlive112116), "Layout": kernels/ "fused quantized MoE
+// expert FFN", "decode GEMV"; opening section: experts "quantized-resident,
+// dequantized on-read, minimizing bytes-per-token"; "Milestone 1": "split-K
+// occupancy" (here: every SM streams a slice of every selected expert).
+//
+// Launch: one CTA per SM (grid = SM count, all CTAs resident), 8 consumer
+// warps + 1 producer warp.  Programmatic dependent launch: the CTAs become
+// resident while the router kernel runs and wait on griddepcontrol.wait.
+//
+//  * Work split.  The U*I (expert, intermediate-row) pairs are cut into G equal
+//    contiguous ranges, one per CTA; the H output rows likewise.
+//  * Producer warp.  As soon as the routing is known it issues TMA bulk copies
+//    (cp.async.bulk, L2 evict-first) of every gate/up row pair of its range
+//    into a ring of NSA stages (8 row pairs per stage) and of its down rows of
+//    every selected expert into a ring of NSB stages, so the whole slice of
+//    the token's expert bytes is in flight at once.
+//  * Phase A (consumers).  Lane (block b, chunk i) of a row keeps the 64
+//    activations of its columns in registers; each row is a 32-lane dot with
+//    the Q4_K chunk code sums of si_device.cuh; h = silu(g) * u goes to the
+//    scratch buffer.
+//  * Grid barrier (bounded).  All of h exists.
+//  * Phase B.  Warp w takes experts w, w+8, ...; its h is staged in shared
+//    memory; lane (row r, chunk i) dots the prefetched down rows; results are
+//    weighted by the routing weight and summed over the top-k slots in slot
+//    order (deterministic, no atomics).
+#include <cstdint>
+
+#include "si_device.cuh"
+#include "si_internal.h"
+
+namespace si {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kExpertThreads = (kConsumerWarps + 1) * 32;
+constexpr long long kDrainBudget = 4000000000LL;  // cycles to wait for in-flight copies after an error
+constexpr int kMaxDownRowsPerLane = 4;            // rows per CTA <= 32
+
+// ------------------------------------------------------------------ helpers
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+// Code sums of one chunk against NT token activations read from shared memory
+// (xa[t] points at the chunk's first column for token t; sub-block b is +32).
+template <int NT>
+__device__ __forceinline__ void chunk_code_sums_smem(const uint4 &q0, const uint4 &q1,
+                                                     const float *const (&xa)[NT], ChunkSums (&out)[NT]) {
+    f32x2 acc_a[NT], acc_b[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc_a[t] = acc_b[t] = 0ull;
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const uint32_t lo = w[p] & 0x0f0f0f0fu;
+        const uint32_t hi = (w[p] >> 4) & 0x0f0f0f0fu;
+        const f32x2 l01 = pack2(code_plus_128<0>(lo), code_plus_128<1>(lo));
+        const f32x2 l23 = pack2(code_plus_128<2>(lo), code_plus_128<3>(lo));
+        const f32x2 h01 = pack2(code_plus_128<0>(hi), code_plus_128<1>(hi));
+        const f32x2 h23 = pack2(code_plus_128<2>(hi), code_plus_128<3>(hi));
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const f32x2 *pa = reinterpret_cast<const f32x2 *>(xa[t]);
+            ffma2(acc_a[t], l01, pa[2 * p]);
+            ffma2(acc_a[t], l23, pa[2 * p + 1]);
+            ffma2(acc_b[t], h01, pa[16 + 2 * p]);
+            ffma2(acc_b[t], h23, pa[16 + 2 * p + 1]);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const float2 fa = unpack2(acc_a[t]), fb = unpack2(acc_b[t]);
+        out[t].Fa = fa.x + fa.y;
+        out[t].Fb = fb.x + fb.y;
+    }
+}
+
+// Sum of two per-lane partials (g, u) over a group of GS lanes.  Returns the
+// g total in the group's lane 0 (first) and the u total (second).
+template <int GS>
+__device__ __forceinline__ float2 group_sum_pair(float g, float u, int li) {
+    const bool upper = (li & (GS / 2)) != 0;
+    float v = upper ? u : g;
+    const float o = upper ? g : u;
+    v += __shfl_xor_sync(0xffffffffu, o, GS / 2);
+#pragma unroll
+    for (int off = GS / 4; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    const float other = __shfl_xor_sync(0xffffffffu, v, GS / 2);
+    return make_float2(upper ? other : v, upper ? v : other);
+}
+
+struct ExpertWork {
+    int p0, p1;  // row pairs [p0, p1) of the flattened (slot, intermediate row) space
+    int c0, nrows;
+    int nA, nB;
+};
+
+// ---------------------------------------------------------------- producer
+template <int NBH>
+__device__ void produce_A(const DecodeArgs &a, const ExpertWork &wk, int j, uint8_t *stA, uint32_t fullA,
+                          uint32_t emptyA, int *lastA, volatile int *s_err, uint64_t pol, bool &ok) {
+    constexpr int CH = kConsumerWarps * (32 / (4 * NBH));
+    constexpr int rowg = NBH * kBlockBytes;
+    constexpr int stage_bytes = 2 * CH * rowg;
+    const int NSA = a.fz_nsa;
+    const int st = j % NSA;
+    if (j >= NSA) {
+        const uint32_t parity = ((j / NSA) - 1) & 1;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(emptyA + 8 * st, parity)) {
+            if (*s_err || clock64() - t0 > a.wait_budget) {
+                if (!*s_err) set_status(a.ctrl + kCtrlStatus, SI_ERR_TIMEOUT);
+                *s_err = 1;
+                ok = false;
+                return;
+            }
+            __nanosleep(20);
+        }
+    }
+    const int qa = wk.p0 + CH * j;
+    const int qb = min(qa + CH, wk.p1);
+    const uint32_t full = fullA + 8 * st;
+    mbar_arrive_expect_tx(full, (uint32_t)(2 * (qb - qa) * rowg));
+    const uint32_t dst_g = smem_addr(stA + (size_t)st * stage_bytes);
+    const uint32_t dst_u = dst_g + CH * rowg;
+    const UniqTable *u = a.uniq;
+    for (int p = qa; p < qb;) {
+        const int s = p / a.I;
+        const int r = p - s * a.I;
+        const int run_end = min(qb, (s + 1) * a.I);
+        const int n = run_end - p;
+        const size_t src_off = ((size_t)u->expert[s] * a.I + r) * rowg;
+        const uint32_t off = (uint32_t)((p - qa) * rowg);
+        bulk_g2s(dst_g + off, a.wg + src_off, (uint32_t)(n * rowg), full, pol);
+        bulk_g2s(dst_u + off, a.wu + src_off, (uint32_t)(n * rowg), full, pol);
+        p = run_end;
+    }
+    lastA[st] = (j / NSA) & 1;
+}
+
+__device__ void produce_B(const DecodeArgs &a, const ExpertWork &wk, int s, uint8_t *stB, uint32_t fullB,
+                          uint32_t emptyB, int *lastB, volatile int *s_err, uint64_t pol, bool &ok) {
+    const int NSB = a.fz_nsb;
+    const int st = s % NSB;
+    if (s >= NSB) {
+        const uint32_t parity = ((s / NSB) - 1) & 1;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(emptyB + 8 * st, parity)) {
+            if (*s_err || clock64() - t0 > a.wait_budget) {
+                if (!*s_err) set_status(a.ctrl + kCtrlStatus, SI_ERR_TIMEOUT);
+                *s_err = 1;
+                ok = false;
+                return;
+            }
+            __nanosleep(20);
+        }
+    }
+    const int rowd = (a.I / kQK) * kBlockBytes;
+    const uint32_t bytes = (uint32_t)(wk.nrows * rowd);
+    const uint32_t full = fullB + 8 * st;
+    mbar_arrive_expect_tx(full, bytes);
+    const size_t src_off = ((size_t)a.uniq->expert[s] * a.H + wk.c0) * rowd;
+    bulk_g2s(smem_addr(stB + (size_t)st * a.fz_stage_b), a.wd + src_off, bytes, full, pol);
+    lastB[st] = (s / NSB) & 1;
+}
+
+// ------------------------------------------------------------------ kernel
+template <int NBH, bool DEDUP>
+__global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    constexpr int GS = 4 * NBH;   // lanes per gate/up row
+    constexpr int RPW = 32 / GS;  // rows per warp pass
+    constexpr int CH = kConsumerWarps * RPW;
+    constexpr int rowg = NBH * kBlockBytes;
+    constexpr int stageA_bytes = 2 * CH * rowg;
+    __shared__ int s_err;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NSA = a.fz_nsa, NSB = a.fz_nsb;
+    uint8_t *stA = sm + a.fz_off_a;
+    uint8_t *stB = sm + a.fz_off_b;
+    const uint32_t fullA = smem_addr(sm + a.fz_off_bar);
+    const uint32_t emptyA = fullA + 8 * NSA;
+    const uint32_t fullB = emptyA + 8 * NSA;
+    const uint32_t emptyB = fullB + 8 * NSB;
+    int *lastA = reinterpret_cast<int *>(sm + a.fz_off_bar + 16 * (NSA + NSB));
+    int *lastB = lastA + NSA;
+    int32_t *status = a.ctrl + kCtrlStatus;
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < NSA; ++st) {
+            mbar_init(fullA + 8 * st, 1);
+            mbar_init(emptyA + 8 * st, kConsumerWarps);
+            lastA[st] = -1;
+        }
+        for (int st = 0; st < NSB; ++st) {
+            mbar_init(fullB + 8 * st, 1);
+            mbar_init(emptyB + 8 * st, 1);
+            lastB[st] = -1;
+        }
+        s_err = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();  // the router kernel (and everything before it) is complete
+
+    const UniqTable *u = a.uniq;
+    const int U = a.ctrl[kCtrlNumUnique];
+    ExpertWork wk;
+    {
+        const long long P = (long long)U * a.I;
+        const int G = gridDim.x, bid = blockIdx.x;
+        wk.p0 = (int)(P * bid / G);
+        wk.p1 = (int)(P * (bid + 1) / G);
+        wk.c0 = (int)((long long)a.H * bid / G);
+        wk.nrows = (int)((long long)a.H * (bid + 1) / G) - wk.c0;
+        wk.nA = (wk.p1 - wk.p0 + CH - 1) / CH;
+        wk.nB = wk.nrows > 0 ? U : 0;
+    }
+    bool ok = true;
+    volatile int *verr = &s_err;
+
+    // ------------------------------------------------ issue (producer warp)
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            const int first = min(wk.nA, NSA);
+            for (int j = 0; j < first; ++j) produce_A<NBH>(a, wk, j, stA, fullA, emptyA, lastA, verr, pol, ok);
+            for (int s = 0; s < min(wk.nB, NSB); ++s) produce_B(a, wk, s, stB, fullB, emptyB, lastB, verr, pol, ok);
+            for (int j = first; j < wk.nA && ok; ++j)
+                produce_A<NBH>(a, wk, j, stA, fullA, emptyA, lastA, verr, pol, ok);
+        }
+        __syncwarp();
+    }
+
+    // ------------------------------------------------ phase A (consumers)
+    if (warp < kConsumerWarps) {
+        const int g = lane / GS, li = lane % GS, b = li >> 2, i = li & 3;
+        float *xs = reinterpret_cast<float *>(sm + a.fz_off_x);  // DEDUP: [n][H] fp32
+        float *Xs = xs + a.n * a.H;                               // DEDUP: [n][H/32]
+        f32x2 xr[32];
+        float Xa = 0.f, Xb = 0.f;
+        if (!DEDUP) {
+            const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + kQK * b + 64 * i);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint4 v = __ldg(xp + q);
+                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const float lo = __uint_as_float(wv[e2] << 16);
+                    const float hi = __uint_as_float(wv[e2] & 0xffff0000u);
+                    xr[4 * q + e2] = pack2(lo, hi);
+                    if (q < 4) Xa += lo + hi;
+                    else Xb += lo + hi;
+                }
+            }
+        } else {
+            for (int t = threadIdx.x; t < a.n * a.H; t += kConsumerWarps * 32)
+                xs[t] = bf16_bits_to_f32(a.x[t]);
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+            for (int t = threadIdx.x; t < a.n * a.H / 32; t += kConsumerWarps * 32) {
+                float sacc = 0.f;
+                for (int l = 0; l < 32; ++l) sacc += xs[32 * t + l];
+                Xs[t] = sacc;
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        }
+
+        for (int j = 0; j < wk.nA; ++j) {
+            const int st = j % NSA;
+            const bool landed = mbar_wait_bounded(fullA + 8 * st, (j / NSA) & 1, a.wait_budget);
+            if (!__all_sync(0xffffffffu, landed)) {  // one decision per warp
+                set_status(status, SI_ERR_TIMEOUT);
+                *verr = 1;
+                break;
+            }
+            const int q = CH * j + warp * RPW + g;  // local row-pair index
+            const bool active = q < wk.p1 - wk.p0;
+            const uint8_t *grow = stA + (size_t)st * stageA_bytes + (warp * RPW + g) * rowg + b * kBlockBytes;
+            const uint8_t *urow = grow + CH * rowg;
+            const uint4 hg = lds128(grow), qg0 = lds128(grow + 16 + 32 * i), qg1 = lds128(grow + 32 + 32 * i);
+            const uint4 hu = lds128(urow), qu0 = lds128(urow + 16 + 32 * i), qu1 = lds128(urow + 32 + 32 * i);
+            const SubScales sg = chunk_scales(hg, i), su = chunk_scales(hu, i);
+            const int p = wk.p0 + (active ? q : 0);
+            const int s = p / a.I, r = p - s * a.I;
+            if (!DEDUP) {
+                auto xa2 = [&xr](int t) { return xr[t]; };
+                auto xb2 = [&xr](int t) { return xr[16 + t]; };
+                const float gp = chunk_contrib(sg, chunk_code_sums(qg0, qg1, xa2, xb2), Xa, Xb);
+                const float up = chunk_contrib(su, chunk_code_sums(qu0, qu1, xa2, xb2), Xa, Xb);
+                const float2 gu = group_sum_pair<GS>(gp, up, li);
+                if (active && li == 0) {
+                    const int slot = u->slot[s][0];
+                    a.h[(size_t)slot * a.I + r] = silu(gu.x) * gu.y;
+                }
+            } else {
+                const int nt = active ? u->ntok[s] : 1;
+                // groups of one warp may hold rows of different experts: reduce to the warp's
+                // largest token count so every lane takes part in every shuffle
+                const int nt_warp = __reduce_max_sync(0xffffffffu, nt);
+                float gp[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
+                float up[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
+#define SI_DEDUP_CASE(NT)                                                                        \
+    {                                                                                            \
+        const float *xa[NT];                                                                     \
+        ChunkSums fg[NT], fu[NT];                                                                \
+        _Pragma("unroll") for (int t = 0; t < NT; ++t) xa[t] =                                   \
+            xs + (size_t)u->tok[s][t] * a.H + kQK * b + 64 * i;                                  \
+        chunk_code_sums_smem<NT>(qg0, qg1, xa, fg);                                              \
+        chunk_code_sums_smem<NT>(qu0, qu1, xa, fu);                                              \
+        _Pragma("unroll") for (int t = 0; t < NT; ++t) {                                         \
+            const int xo = u->tok[s][t] * (a.H / 32) + 8 * b + 2 * i;                            \
+            gp[t] = chunk_contrib(sg, fg[t], Xs[xo], Xs[xo + 1]);                                \
+            up[t] = chunk_contrib(su, fu[t], Xs[xo], Xs[xo + 1]);                                \
+        }                                                                                        \
+    }
+                switch (nt) {
+                    case 1: SI_DEDUP_CASE(1) break;
+                    case 2: SI_DEDUP_CASE(2) break;
+                    case 3: SI_DEDUP_CASE(3) break;
+                    default: SI_DEDUP_CASE(4) break;
+                }
+#undef SI_DEDUP_CASE
+#pragma unroll
+                for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
+                    if (t >= nt_warp) break;
+                    const float2 gu = group_sum_pair<GS>(gp[t], up[t], li);
+                    if (active && li == 0 && t < nt) {
+                        const int pair = u->tok[s][t] * a.k + u->slot[s][t];
+                        a.h[(size_t)pair * a.I + r] = silu(gu.x) * gu.y;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(emptyA + 8 * st);
+        }
+    }
+
+    // ------------------------------------------------ all of h exists
+    const bool bar_ok = grid_barrier(a.ctrl + kCtrlBarCount, a.ctrl + kCtrlBarGen, status, a.wait_budget);
+    pdl_launch_dependents();
+    if (!bar_ok) s_err = 1;
+
+    if (warp == kConsumerWarps) {
+        if (lane == 0 && !*verr) {
+            const uint64_t pol = l2_evict_first_policy();
+            for (int s = NSB; s < wk.nB && ok; ++s)
+                produce_B(a, wk, s, stB, fullB, emptyB, lastB, verr, pol, ok);
+        }
+        __syncwarp();
+    }
+
+    // ------------------------------------------------ phase B (down + combine)
+    float *yw = reinterpret_cast<float *>(sm + a.fz_off_yw);  // [n*k][RB]
+    const int RB = a.fz_rb;
+    const bool skip_b = __any_sync(0xffffffffu, *verr != 0);  // read once per warp
+    if (warp < kConsumerWarps && !skip_b) {
+        const int nbI = a.I / kQK;
+        const int rowd = nbI * kBlockBytes;
+        float *hb = reinterpret_cast<float *>(sm + a.fz_off_h) + (size_t)warp * a.I;
+        float *hs = reinterpret_cast<float *>(sm + a.fz_off_hs) + (size_t)warp * (a.I / 32);
+        const int r8 = lane >> 2, i = lane & 3;
+        for (int s = warp; s < wk.nB; s += kConsumerWarps) {
+            const int st = s % NSB;
+            const bool landed = mbar_wait_bounded(fullB + 8 * st, (s / NSB) & 1, a.wait_budget);
+            if (!__all_sync(0xffffffffu, landed)) {
+                set_status(status, SI_ERR_TIMEOUT);
+                *verr = 1;
+                break;
+            }
+            const uint8_t *rows = stB + (size_t)st * a.fz_stage_b;
+            const int nt = u->ntok[s];
+            for (int jt = 0; jt < nt; ++jt) {
+                const int pair = u->tok[s][jt] * a.k + u->slot[s][jt];
+                const float wgt = a.wts[pair];
+                const float4 *hsrc = reinterpret_cast<const float4 *>(a.h + (size_t)pair * a.I);
+                for (int q = lane; q < a.I / 4; q += 32) reinterpret_cast<float4 *>(hb)[q] = __ldcg(hsrc + q);
+                __syncwarp();
+                for (int q = lane; q < a.I / 32; q += 32) {
+                    const float4 *hp = reinterpret_cast<const float4 *>(hb + 32 * q);
+                    float sacc = 0.f;
+#pragma unroll
+                    for (int l = 0; l < 8; ++l) {
+                        const float4 v = hp[l];
+                        sacc += (v.x + v.y) + (v.z + v.w);
+                    }
+                    hs[q] = sacc;
+                }
+                __syncwarp();
+                float acc[kMaxDownRowsPerLane] = {0.f, 0.f, 0.f, 0.f};
+                for (int bb = 0; bb < nbI; ++bb) {
+                    const f32x2 *hx = reinterpret_cast<const f32x2 *>(hb + kQK * bb + 64 * i);
+                    f32x2 hr[32];
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) hr[t] = hx[t];
+                    const float Ha = hs[8 * bb + 2 * i], Hb = hs[8 * bb + 2 * i + 1];
+                    auto xa2 = [&hr](int t) { return hr[t]; };
+                    auto xb2 = [&hr](int t) { return hr[16 + t]; };
+#pragma unroll
+                    for (int m = 0; m < kMaxDownRowsPerLane; ++m) {
+                        const int lr = r8 + 8 * m;
+                        if (lr < wk.nrows) {
+                            const uint8_t *blk = rows + (size_t)lr * rowd + bb * kBlockBytes;
+                            const uint4 hd = lds128(blk), q0 = lds128(blk + 16 + 32 * i),
+                                        q1 = lds128(blk + 32 + 32 * i);
+                            acc[m] += chunk_contrib(chunk_scales(hd, i), chunk_code_sums(q0, q1, xa2, xb2),
+                                                    Ha, Hb);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < kMaxDownRowsPerLane; ++m) {
+                    float v = acc[m];
+                    v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    v += __shfl_xor_sync(0xffffffffu, v, 2);
+                    const int lr = r8 + 8 * m;
+                    if (i == 0 && lr < wk.nrows) yw[(size_t)pair * RB + lr] = wgt * v;
+                }
+                __syncwarp();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(emptyB + 8 * st);
+        }
+    }
+    __syncthreads();
+
+    if (!*verr) {
+        for (int idx = threadIdx.x; idx < a.n * wk.nrows; idx += blockDim.x) {
+            const int t = idx / wk.nrows, lr = idx - t * wk.nrows;
+            float sacc = 0.f;
+            for (int slot = 0; slot < a.k; ++slot) sacc += yw[(size_t)(t * a.k + slot) * RB + lr];
+            a.out[(size_t)t * a.H + wk.c0 + lr] = sacc;
+        }
+    } else if (threadIdx.x == 0) {
+        // An error stopped this CTA early: let its copies in flight land before it exits.
+        for (int st = 0; st < NSA; ++st)
+            if (lastA[st] >= 0) mbar_wait_bounded(fullA + 8 * st, lastA[st], kDrainBudget);
+        for (int st = 0; st < NSB; ++st)
+            if (lastB[st] >= 0) mbar_wait_bounded(fullB + 8 * st, lastB[st], kDrainBudget);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+// Shared-memory plan of the fused kernel for n tokens on `grid` CTAs; returns
+// false if this shape needs the generic kernels.
+bool expert_fused_layout(const si_moe_desc &d, int n, int grid, int smem_max, DecodeArgs &a) {
+    const int nbh = d.hidden / kQK;
+    if (nbh != 1 && nbh != 2 && nbh != 4 && nbh != 8) return false;
+    const int nbi = d.intermediate / kQK;
+    const int RB = (d.hidden + grid - 1) / grid;
+    if (RB > 8 * kMaxDownRowsPerLane) return false;
+    const int umax = n * d.top_k;
+    const int CH = kConsumerWarps * (32 / (4 * nbh));
+    const size_t stageA = (size_t)2 * CH * nbh * kBlockBytes;
+    const size_t stageB = (size_t)RB * nbi * kBlockBytes;
+    const long long P = (long long)umax * d.intermediate;
+    const int nA_max = (int)(((P + grid - 1) / grid + CH - 1) / CH);
+    const bool dedup = n > 1;
+    auto al = [](size_t v) { return (v + 127) / 128 * 128; };
+    const size_t x_bytes = dedup ? al((size_t)n * d.hidden * 4 + (size_t)n * (d.hidden / 32) * 4) : 0;
+    const size_t h_bytes = al((size_t)kConsumerWarps * d.intermediate * 4);
+    const size_t hs_bytes = al((size_t)kConsumerWarps * (d.intermediate / 32) * 4);
+    const size_t yw_bytes = al((size_t)umax * RB * 4);
+    int NSA = nA_max < 6 ? (nA_max < 1 ? 1 : nA_max) : 6;
+    const size_t fixed = x_bytes + h_bytes + hs_bytes + yw_bytes;
+    auto bar_bytes = [](int nsa, int nsb) { return (size_t)16 * (nsa + nsb) + (size_t)4 * (nsa + nsb) + 64; };
+    const long long sA = (long long)stageA, sB = (long long)stageB;
+    auto fits = [&](int nsa, int nsb) {
+        const long long need = 256 + (long long)fixed + (long long)nsa * sA + (long long)nsb * sB +
+                               (long long)bar_bytes(nsa, nsb) + 128;
+        return need <= (long long)smem_max;
+    };
+    int NSB = 0;
+    while (NSB < umax && fits(NSA, NSB + 1)) ++NSB;
+    if (NSB < 1) {
+        NSA = 2;
+        while (NSB < umax && fits(NSA, NSB + 1)) ++NSB;
+        if (NSB < 1) return false;
+    }
+    size_t off = 0;
+    a.fz_off_a = (int)off;
+    off += NSA * stageA;
+    a.fz_off_b = (int)off;
+    off += al(NSB * stageB);
+    a.fz_off_x = (int)off;
+    off += x_bytes;
+    a.fz_off_h = (int)off;
+    off += h_bytes;
+    a.fz_off_hs = (int)off;
+    off += hs_bytes;
+    a.fz_off_yw = (int)off;
+    off += yw_bytes;
+    a.fz_off_bar = (int)off;
+    off += bar_bytes(NSA, NSB);
+    a.fz_nsa = NSA;
+    a.fz_nsb = NSB;
+    a.fz_rb = RB;
+    a.fz_stage_b = (int)stageB;
+    a.fz_smem = (int)off;
+    return off <= (size_t)smem_max;
+}
+
+template <int NBH, bool DEDUP>
+static cudaError_t launch_expert_t(const DecodeArgs &a, int grid, cudaStream_t s) {
+    auto kern = k_expert<NBH, DEDUP>;  // dynamic smem limit raised at plan time
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kExpertThreads);
+    cfg.dynamicSmemBytes = a.fz_smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+cudaError_t launch_expert_fused(const DecodeArgs &a, int grid, cudaStream_t s) {
+    const int nbh = a.H / kQK;
+    const bool dedup = a.n > 1;
+    switch (nbh) {
+        case 1: return dedup ? launch_expert_t<1, true>(a, grid, s) : launch_expert_t<1, false>(a, grid, s);
+        case 2: return dedup ? launch_expert_t<2, true>(a, grid, s) : launch_expert_t<2, false>(a, grid, s);
+        case 4: return dedup ? launch_expert_t<4, true>(a, grid, s) : launch_expert_t<4, false>(a, grid, s);
+        default: return dedup ? launch_expert_t<8, true>(a, grid, s) : launch_expert_t<8, false>(a, grid, s);
+    }
+}
+
+cudaError_t expert_fused_occupancy(int nbh, bool dedup, int smem, int smem_max, int *blocks_per_sm) {
+    const void *f = nullptr;
+    switch (nbh) {
+        case 1: f = dedup ? (const void *)k_expert<1, true> : (const void *)k_expert<1, false>; break;
+        case 2: f = dedup ? (const void *)k_expert<2, true> : (const void *)k_expert<2, false>; break;
+        case 4: f = dedup ? (const void *)k_expert<4, true> : (const void *)k_expert<4, false>; break;
+        default: f = dedup ? (const void *)k_expert<8, true> : (const void *)k_expert<8, false>; break;
+    }
+    cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    if (err != cudaSuccess) return err;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, f, kExpertThreads, smem);
+}
+
+}  // namespace si

@@ -13,6 +13,8 @@ enum CtrlWord : int {
     kCtrlStatus = 0,        // first device-side error code (si_status), 0 = none
     kCtrlRouterTicket = 1,  // arrival counter of the router CTAs (self-resetting)
     kCtrlNumUnique = 2,     // distinct experts selected by this decode call
+    kCtrlBarCount = 3,      // grid-barrier arrival counter of the fused expert kernel
+    kCtrlBarGen = 4,        // grid-barrier generation
     kCtrlWords = 64,
 };
 constexpr size_t kCtrlBytes = kCtrlWords * sizeof(int32_t);
@@ -36,6 +38,8 @@ struct Plan {
     int sm_count;
     int l2_bytes;
     int smem_optin;
+    long long wait_budget;  // SM cycles a device-side wait may spin before reporting SI_ERR_TIMEOUT
+    bool fused_ok[SI_MAX_DECODE_TOKENS + 1];  // fused expert kernel usable for n tokens
     DecodeLayout dec;  // sized for SI_MAX_DECODE_TOKENS tokens
 };
 
@@ -59,10 +63,17 @@ struct DecodeArgs {
     float *o_w;
     int32_t *o_counts;
     float *o_logits;
+    long long wait_budget;
+    // shared-memory plan of the fused expert kernel (set by expert_fused_layout)
+    int fz_off_a, fz_off_b, fz_off_x, fz_off_h, fz_off_hs, fz_off_yw, fz_off_bar;
+    int fz_nsa, fz_nsb, fz_rb, fz_stage_b, fz_smem;
 };
 
 cudaError_t launch_decode(const Plan &p, const DecodeArgs &a, cudaStream_t s,
                           cudaEvent_t const *events = nullptr);
+bool expert_fused_layout(const si_moe_desc &d, int n, int grid, int smem_max, DecodeArgs &a);
+cudaError_t launch_expert_fused(const DecodeArgs &a, int grid, cudaStream_t s);
+cudaError_t expert_fused_occupancy(int nbh, bool dedup, int smem, int smem_max, int *blocks_per_sm);
 cudaError_t launch_debug_dequant(const uint8_t *blocks, int64_t n_blocks, float *out_f32,
                                  uint16_t *out_bf16, cudaStream_t s);
 cudaError_t launch_debug_topk(const float *logits, int n, int E, int k, int32_t *ids, float *w,
