@@ -537,7 +537,13 @@ cudaError_t expert_fused_occupancy(int nbh, bool dedup, int smem, int smem_max, 
         case 4: f = dedup ? (const void *)k_expert<4, true> : (const void *)k_expert<4, false>; break;
         default: f = dedup ? (const void *)k_expert<8, true> : (const void *)k_expert<8, false>; break;
     }
-    cudaError_t err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, f);
+    if (err != cudaSuccess) return err;
+    // the opt-in limit covers static + dynamic shared memory
+    const int dyn_max = smem_max - (int)fa.sharedSizeBytes;
+    if (smem > dyn_max) return cudaErrorInvalidValue;
+    err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
     if (err != cudaSuccess) return err;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, f, kExpertThreads, smem);
 }
