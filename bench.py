@@ -296,9 +296,12 @@ def bench_layer(args, dist, binding, device, synth, torch, hbm_peak):
     down_bytes = shape.top_k * shape.hidden * nbi * 144
     router_bytes = shape.n_experts * shape.hidden * 4 + shape.hidden * 2
     expert_bytes = gateup_bytes + down_bytes
-    fused = binding.si_debug_decode_fused(plan, 1) == 1
+    path = binding.si_debug_decode_fused(plan, 1)
+    plan_info = binding.si_debug_plan_info(plan)
+    fused = path >= 1
     if fused:   # one expert launch: gate/up + SwiGLU + down + combine
-        dom_name = "k_expert (fused gate/up dequant-GEMV + SwiGLU + down dequant-GEMV + combine)"
+        dom_name = ("k_expert_cluster" if path == 2 else "k_expert") + \
+            " (fused gate/up dequant-GEMV + SwiGLU + down dequant-GEMV + combine)"
         dom_bytes, dom_ms = expert_bytes, per_launch_ms[1] + per_launch_ms[2]
     else:
         dom_name = "k_gateup_generic (gate/up dequant-GEMV + SwiGLU)"
@@ -338,7 +341,8 @@ def bench_layer(args, dist, binding, device, synth, torch, hbm_peak):
                    "global_batch": 1, "parallelism": f"replicas x{dist.world}",
                    "l2_policy": "inputs larger than L2: 339.7 MB of resident experts per layer vs "
                                 "129 MB L2; no flush between steps",
-                   "graph": "one CUDA graph per step (1024 sequential decode calls)"},
+                   "graph": "one CUDA graph per step (1024 sequential decode calls)",
+                   "plan": plan_info},
         "roofline": {"bound": "hbm", "kernel": dom_name,
                      "achieved": dom_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": dom_gbs / hbm_peak,
                      "traffic": None,
@@ -392,7 +396,7 @@ def bench_stack48(args, dist, binding, device, synth, torch, hbm_peak):
             "tok_per_s": dist.sum(tok_s), "layer_tok_per_s": dist.sum(tok_s) * NL,
             "us_per_step": 1e6 / tok_s, "expert_bytes_per_step": step_bytes,
             "achieved_gbs": gbs, "frac_of_peak": gbs / hbm_peak, "clocks": clocks,
-            "gpu_launches": (2 if binding.si_debug_decode_fused(plan, 1) == 1 else 3) * NL * S * steps}
+            "gpu_launches": (2 if binding.si_debug_decode_fused(plan, 1) >= 1 else 3) * NL * S * steps}
 
 
 def bench_dedup4(args, dist, binding, device, synth, torch, hbm_peak):
@@ -424,7 +428,7 @@ def bench_dedup4(args, dist, binding, device, synth, torch, hbm_peak):
             "expert_bytes_per_step": bytes_per_step,
             "non_dedup_bytes_per_step": n * shape.top_k * shape.expert_bytes,
             "achieved_gbs": gbs, "frac_of_peak": gbs / hbm_peak, "clocks": clocks,
-            "gpu_launches": (2 if binding.si_debug_decode_fused(plan, n) == 1 else 3) * S * steps}
+            "gpu_launches": (2 if binding.si_debug_decode_fused(plan, n) >= 1 else 3) * S * steps}
 
 
 def run_ours(args, dist):

@@ -29,6 +29,13 @@
  *    word and returned by si_moe_read_status.
  *  - Threading: calls on one plan are thread-safe when each thread uses its
  *    own scratch buffer.
+ *  - Bounded waits: every device-side wait gives up after about one second
+ *    and records SI_ERR_TIMEOUT.  Test mode: when the environment variable
+ *    SI_FAULT_WAIT_BUDGET holds a decimal cycle count at si_moe_plan time,
+ *    that plan's waits use it as their budget and its expert kernels first
+ *    wait on a scratch word nothing writes, so the error path (record the
+ *    status, skip the rest, let in-flight copies land, return) runs for
+ *    certain.  After SI_ERR_TIMEOUT call si_moe_scratch_init again.
  *
  * Q4_K weights (GGUF's block format, unmodified): 144-byte super-blocks of
  * 256 weights {fp16 d, fp16 dmin, u8 scales[12], u8 qs[128]}, blocked along
@@ -167,11 +174,17 @@ si_status si_moe_forward_decode_noalloc(si_moe_plan_t plan, const si_moe_layer *
                                         const void *x_bf16, int32_t n_tokens, float *out,
                                         si_moe_route_out *route_out, si_stream_t stream);
 
-/* Test/bench export: 1 if decode of n_tokens tokens runs the fused expert
- * kernel (one launch for gate/up, SwiGLU, down and combine after the router
- * launch), 0 if it runs the generic gate/up + down kernels, -1 on a bad
- * argument. */
+/* Test/bench export: which expert kernels decode of n_tokens tokens runs
+ * after the router launch: 2 = the cluster kernel (one launch, n_tokens == 1),
+ * 1 = the grid-synchronised fused kernel (one launch), 0 = the generic
+ * gate/up + down kernels (two launches); -1 on a bad argument. */
 int si_debug_decode_fused(si_moe_plan_t plan, int32_t n_tokens);
+
+/* Test/bench export: up to n plan facts into info[]: SM count, cluster path
+ * usable (0/1), CTAs per cluster, clusters of that size resident at once,
+ * clusters one token needs (top_k * intermediate/256), shared memory per CTA
+ * (opt-in bytes).  Returns the number written, -1 on a bad argument. */
+int si_debug_plan_info(si_moe_plan_t plan, int32_t *info, int32_t n);
 
 /* Test exports.  si_debug_q4k_dequant decodes n_blocks Q4_K blocks into
  * out_f32 [n_blocks*256] and/or out_bf16 [n_blocks*256] (either may be

@@ -99,6 +99,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.si_moe_forward_decode_noalloc.restype = ctypes.c_int
     lib.si_moe_forward_decode_noalloc.argtypes = [vp, ctypes.POINTER(si_moe_layer), vp, i32, vp,
                                                   ctypes.POINTER(si_moe_route_out), vp]
+    lib.si_debug_plan_info.restype = ctypes.c_int
+    lib.si_debug_plan_info.argtypes = [vp, ctypes.POINTER(i32), i32]
     lib.si_debug_decode_fused.restype = ctypes.c_int
     lib.si_debug_decode_fused.argtypes = [vp, i32]
     lib.si_moe_read_status.restype = ctypes.c_int
@@ -251,6 +253,13 @@ def si_debug_decode_events(plan, layer: si_moe_layer, x, n_tokens, out, route_ou
     _check(lib.si_debug_decode_events(plan.handle, ctypes.byref(layer), _ptr(x), int(n_tokens), _ptr(out),
                                       ro, _ptr(scratch), nbytes, ev, _stream(stream)),
            "si_debug_decode_events")
+
+
+def si_debug_plan_info(plan: Plan) -> dict:
+    buf = (ctypes.c_int32 * 6)()
+    load_library().si_debug_plan_info(plan.handle, buf, 6)
+    keys = ("sm_count", "cluster_ok", "cluster_size", "clusters_resident", "clusters_needed", "smem_optin")
+    return dict(zip(keys, list(buf)))
 
 
 def si_debug_decode_fused(plan: Plan, n_tokens: int) -> int:

@@ -99,10 +99,14 @@ si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *o
     // shorten the budget through SI_FAULT_WAIT_BUDGET (a non-negative decimal
     // cycle count); unset or malformed leaves the default.
     p.wait_budget = 2000000000LL;
+    p.fault_wait = false;
     if (const char *env = std::getenv("SI_FAULT_WAIT_BUDGET")) {
         char *end = nullptr;
         const long long v = std::strtoll(env, &end, 10);
-        if (end && end != env && *end == '\0' && v >= 0) p.wait_budget = v;
+        if (end && end != env && *end == '\0' && v >= 0) {
+            p.wait_budget = v;
+            p.fault_wait = true;  // and make a wait run out for certain: see kCtrlFaultFlag
+        }
     }
     const int cur_dev = [] { int d = 0; cudaGetDevice(&d); return d; }();
     if (cur_dev != cuda_device) cudaSetDevice(cuda_device);
@@ -114,6 +118,28 @@ si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *o
             if (si::expert_fused_occupancy(desc->hidden / 256, n > 1, tmp.fz_smem, p.smem_optin, &per_sm) == cudaSuccess &&
                 per_sm >= 1)
                 p.fused_ok[n] = true;
+            cudaGetLastError();
+        }
+    }
+    {
+        // Largest cluster size whose clusters (one per selected expert and 256-wide
+        // block of the intermediate dimension) are all resident at once.
+        p.cluster_ok = false;
+        p.cluster_size = 0;
+        p.cluster_active = 0;
+        const int units = desc->top_k * (desc->intermediate / 256);
+        for (int C = 8; C >= 2 && !p.cluster_ok; --C) {
+            si::DecodeArgs tmp{};
+            if (units * C > p.sm_count) continue;
+            if (!si::expert_cluster_layout(*desc, C, p.smem_optin, tmp)) continue;
+            int clusters = 0;
+            if (si::expert_cluster_prepare(desc->hidden / 256, p.smem_optin, tmp.cl_smem, C, &clusters) ==
+                    cudaSuccess &&
+                clusters >= units) {
+                p.cluster_ok = true;
+                p.cluster_size = C;
+                p.cluster_active = clusters;
+            }
             cudaGetLastError();
         }
     }
@@ -226,8 +252,18 @@ si_status si_moe_forward_prefill(si_moe_plan_t plan, const si_moe_layer *layer, 
     return SI_ERR_UNSUPPORTED;
 }
 
+int si_debug_plan_info(si_moe_plan_t plan, int32_t *info, int32_t n) {
+    if (!plan || !info || n < 1) return -1;
+    const int32_t v[6] = {plan->p.sm_count, plan->p.cluster_ok ? 1 : 0, plan->p.cluster_size,
+                          plan->p.cluster_active, plan->p.desc.top_k * (plan->p.desc.intermediate / 256),
+                          plan->p.smem_optin};
+    for (int q = 0; q < n && q < 6; ++q) info[q] = v[q];
+    return n < 6 ? n : 6;
+}
+
 int si_debug_decode_fused(si_moe_plan_t plan, int32_t n_tokens) {
     if (!plan || n_tokens < 1 || n_tokens > SI_MAX_DECODE_TOKENS) return -1;
+    if (n_tokens == 1 && plan->p.cluster_ok) return 2;
     return plan->p.fused_ok[n_tokens] ? 1 : 0;
 }
 

@@ -56,9 +56,10 @@ __global__ void __launch_bounds__(128) k_debug_topk(const float *logits, int n, 
     for (int i = threadIdx.x; i < n * E; i += blockDim.x) s_z[i / E][i % E] = logits[i];
     for (int i = threadIdx.x; i < E; i += blockDim.x) s_counts[i] = 0;
     __syncthreads();
+    cta_topk_ranks(s_z, n, E, k, s_ids, s_w);
+    __syncthreads();
     if (warp < n) {
-        warp_topk(s_z[warp], E, k, s_ids[warp], s_w[warp]);
-        __syncwarp();
+        warp_renorm(s_w[warp], k);
         for (int i = lane; i < k; i += 32) {
             if (ids) ids[warp * k + i] = s_ids[warp][i];
             if (w) w[warp * k + i] = s_w[warp][i];

@@ -36,13 +36,26 @@ __device__ __forceinline__ float dot8_bf16(const float4 &w0, const float4 &w1, c
     return s;
 }
 
-// NJ > 0: H == 256*NJ and the router row is loaded into registers before the
-// programmatic-dependent-launch wait (router weights do not depend on the
-// token, so this overlaps the previous kernel's tail).  NJ == 0: any H.
+// Router + top-k, one thread-block cluster (or one CTA for small E).  Warp
+// w of CTA c owns expert e = c*WPC + w.  NJ > 0: H == 256*NJ and the
+// expert's router row is loaded into registers before the programmatic-
+// dependent-launch wait (router weights do not depend on the token, so this
+// overlaps the previous kernel's tail).  NJ == 0: any H, loaded after the wait.
+// Logits are gathered into CTA 0 through distributed shared memory; CTA 0
+// takes softmax, top-k, renormalised weights, per-expert counts and the
+// table of distinct experts (deterministic: ascending expert id, tokens in
+// pair order).
 template <int NJ>
-__global__ void __launch_bounds__(kThreads) k_router_topk(DecodeArgs a) {
+__global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs a) {
+    __shared__ float s_z[SI_MAX_DECODE_TOKENS][SI_MAX_EXPERTS];
+    __shared__ int s_ids[SI_MAX_DECODE_TOKENS][SI_MAX_TOPK];
+    __shared__ float s_w[SI_MAX_DECODE_TOKENS][SI_MAX_TOPK];
+    __shared__ int s_counts[SI_MAX_EXPERTS];
+    __shared__ int s_pos[SI_MAX_EXPERTS];
+    __shared__ int s_U;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * kWarps + warp;
+    const int wpc = blockDim.x >> 5;
+    const int e = blockIdx.x * wpc + warp;
     const float *wrow = a.router_w + (size_t)min(e, a.E - 1) * a.H;
     float4 wr[2 * (NJ > 0 ? NJ : 1)];
     if (NJ > 0) {
@@ -52,8 +65,15 @@ __global__ void __launch_bounds__(kThreads) k_router_topk(DecodeArgs a) {
             wr[2 * j + 1] = __ldg(reinterpret_cast<const float4 *>(wrow + 256 * j + 8 * lane + 4));
         }
     }
-    pdl_launch_dependents();  // the expert kernel may become resident now
+    // Warm L2 with x (a prefetch returns no data: if an earlier kernel is still
+    // writing x, L2 stays coherent and the loads below happen after the wait).
+    if (blockIdx.x == 0 && threadIdx.x < (a.n * a.H * 2) / 128) prefetch_l2(reinterpret_cast<const uint8_t *>(a.x) + 128 * threadIdx.x);
     pdl_wait();               // x and the scratch are ready (previous kernels complete)
+    pdl_launch_dependents();  // the expert kernel may become resident now (x is final)
+    if (a.zero_out) {         // the cluster expert kernel accumulates the top-k combine into out
+        const int nthr = gridDim.x * blockDim.x;
+        for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < a.n * a.H; q += nthr) a.out[q] = 0.f;
+    }
     if (e < a.E) {
         float acc[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
         if (NJ > 0) {
@@ -87,38 +107,27 @@ __global__ void __launch_bounds__(kThreads) k_router_topk(DecodeArgs a) {
                 float z = warp_sum(acc[t]);
                 if (a.router_bias) z += __ldg(a.router_bias + e);
                 if (lane == 0) {
-                    a.logits[t * a.E + e] = z;
+                    if (gridDim.x > 1) st_cluster_f32(&s_z[t][e], 0, z);
+                    else s_z[t][e] = z;
                     if (a.o_logits) a.o_logits[t * a.E + e] = z;
                 }
             }
         }
     }
-
-    // Last CTA to arrive routes every token.  Every writer fences its logits
-    // before the barrier; thread 0 then takes the arrival ticket.
-    __shared__ int s_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const int ticket = atomicAdd(a.ctrl + kCtrlRouterTicket, 1);
-        s_last = (ticket == (int)gridDim.x - 1);
+    if (gridDim.x > 1) {
+        cluster_sync();
+        if (cluster_ctarank() != 0) return;
+    } else {
+        __syncthreads();
     }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
 
-    __shared__ float s_z[SI_MAX_DECODE_TOKENS][SI_MAX_EXPERTS];
-    __shared__ int s_ids[SI_MAX_DECODE_TOKENS][SI_MAX_TOPK];
-    __shared__ float s_w[SI_MAX_DECODE_TOKENS][SI_MAX_TOPK];
-    __shared__ int s_counts[SI_MAX_EXPERTS];
-    for (int i = threadIdx.x; i < a.n * a.E; i += kThreads)
-        s_z[i / a.E][i % a.E] = __ldcg(a.logits + i);
-    for (int i = threadIdx.x; i < a.E; i += kThreads) s_counts[i] = 0;
+    // ---- CTA 0: top-k of every token, then counts and the distinct-expert table
+    const int nk = a.n * a.k;
+    for (int i = threadIdx.x; i < a.E; i += blockDim.x) s_counts[i] = 0;
+    cta_topk_ranks(s_z, a.n, a.E, a.k, s_ids, s_w);
     __syncthreads();
     if (warp < a.n) {
-        warp_topk(s_z[warp], a.E, a.k, s_ids[warp], s_w[warp]);
-        __syncwarp();
+        warp_renorm(s_w[warp], a.k);
         for (int i = lane; i < a.k; i += 32) {
             a.ids[warp * a.k + i] = s_ids[warp][i];
             a.wts[warp * a.k + i] = s_w[warp][i];
@@ -127,48 +136,61 @@ __global__ void __launch_bounds__(kThreads) k_router_topk(DecodeArgs a) {
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        // Distinct experts in ascending order, with the tokens/slots that chose them.
-        UniqTable *u = a.uniq;
-        int U = 0;
-        int ex[kMaxSlots];
-        for (int t = 0; t < a.n; ++t) {
-            for (int i = 0; i < a.k; ++i) {
-                const int e2 = s_ids[t][i];
-                s_counts[e2] += 1;
-                int pos = 0;
-                while (pos < U && ex[pos] < e2) ++pos;
-                if (pos == U || ex[pos] != e2) {
-                    for (int q = U; q > pos; --q) ex[q] = ex[q - 1];
-                    ex[pos] = e2;
-                    ++U;
-                }
-            }
+    if (a.no_table) {  // one token: counts are 0/1 membership of the k distinct ids
+        for (int ex = threadIdx.x; ex < a.E; ex += blockDim.x) {
+            int c = 0;
+            for (int i = 0; i < a.k; ++i) c += (s_ids[0][i] == ex);
+            a.counts[ex] = c;
+            if (a.o_counts) a.o_counts[ex] = c;
         }
-        int fill[kMaxSlots];
-        for (int s = 0; s < U; ++s) {
-            u->expert[s] = ex[s];
-            fill[s] = 0;
+        return;
+    }
+    for (int p = threadIdx.x; p < nk; p += blockDim.x) atomicAdd(&s_counts[s_ids[p / a.k][p % a.k]], 1);
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scan of "selected" flags over the E experts (8 per lane)
+        int flag[8], run = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int ex = 8 * lane + q;
+            flag[q] = (ex < a.E && s_counts[ex] > 0) ? 1 : 0;
+            run += flag[q];
         }
-        for (int t = 0; t < a.n; ++t) {
-            for (int i = 0; i < a.k; ++i) {
-                const int e2 = s_ids[t][i];
-                int s = 0;
-                while (ex[s] != e2) ++s;
-                u->tok[s][fill[s]] = t;
-                u->slot[s][fill[s]] = i;
-                ++fill[s];
-            }
+        int incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
         }
-        for (int s = 0; s < U; ++s) u->ntok[s] = fill[s];
-        a.ctrl[kCtrlNumUnique] = U;
-        a.ctrl[kCtrlRouterTicket] = 0;  // ready for the next call
+        int pos = incl - run;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int ex = 8 * lane + q;
+            if (ex < a.E) s_pos[ex] = pos;
+            pos += flag[q];
+        }
+        if (lane == 31) s_U = incl;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < a.E; i += kThreads) {
-        a.counts[i] = s_counts[i];
-        if (a.o_counts) a.o_counts[i] = s_counts[i];
+    UniqTable *u = a.uniq;
+    for (int ex = threadIdx.x; ex < a.E; ex += blockDim.x) {
+        const int c = s_counts[ex];
+        if (c > 0) {
+            u->expert[s_pos[ex]] = ex;
+            u->ntok[s_pos[ex]] = c;
+        }
+        a.counts[ex] = c;
+        if (a.o_counts) a.o_counts[ex] = c;
     }
+    for (int p = threadIdx.x; p < nk; p += blockDim.x) {
+        const int t = p / a.k, i = p - t * a.k;
+        const int ex = s_ids[t][i];
+        int j = 0;  // rank among the pairs that chose ex (pair-id order)
+        for (int q = 0; q < p; ++q) j += (s_ids[q / a.k][q % a.k] == ex);
+        u->tok[s_pos[ex]][j] = t;
+        u->slot[s_pos[ex]][j] = i;
+    }
+    if (threadIdx.x == 0) a.ctrl[kCtrlNumUnique] = s_U;
 }
 
 // ---------------------------------------------------------------- gate/up
@@ -335,22 +357,34 @@ static cudaError_t mark(cudaEvent_t const *events, int i, cudaStream_t s) {
     return cudaEventRecordWithFlags(events[i], s, cudaEventRecordExternal);
 }
 
+// One CTA for up to 32 experts, else an 8-CTA cluster (portable size).
+static int router_cluster_size(int E) { return E <= 32 ? 1 : 8; }
+
 template <int NJ>
 static cudaError_t launch_router_t(const DecodeArgs &a, cudaStream_t s) {
+    const int C = router_cluster_size(a.E);
+    const int wpc = (a.E + C - 1) / C;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((a.E + kWarps - 1) / kWarps);
-    cfg.blockDim = dim3(kThreads);
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(32 * wpc);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k_router_topk<NJ>, a);
 }
 
 static cudaError_t launch_router(const DecodeArgs &a, cudaStream_t s) {
+    // register prefetch of the router rows: 2*NJ float4 per lane; with 1024
+    // threads per CTA (E > 128) keep the register footprint small instead
+    if ((a.E + router_cluster_size(a.E) - 1) / router_cluster_size(a.E) > 16) return launch_router_t<0>(a, s);
     switch (a.H / kQK) {
         case 1: return launch_router_t<1>(a, s);
         case 2: return launch_router_t<2>(a, s);
@@ -368,12 +402,23 @@ cudaError_t launch_decode(const Plan &p, const DecodeArgs &a_in, cudaStream_t s,
                           cudaEvent_t const *events) {
     DecodeArgs a = a_in;
     a.wait_budget = p.wait_budget;
+    a.fault_wait = p.fault_wait ? 1 : 0;
+    const bool cluster =
+        a.n == 1 && p.cluster_ok && expert_cluster_layout(p.desc, p.cluster_size, p.smem_optin, a);
+    a.zero_out = cluster ? 1 : 0;
+    a.no_table = cluster ? 1 : 0;
     cudaError_t err = mark(events, 0, s);
     if (err != cudaSuccess) return err;
     err = launch_router(a, s);
     if (err != cudaSuccess) return err;
     if ((err = mark(events, 1, s)) != cudaSuccess) return err;
 
+    if (cluster) {
+        err = launch_expert_cluster(a, s);
+        if (err != cudaSuccess) return err;
+        if ((err = mark(events, 2, s)) != cudaSuccess) return err;
+        return mark(events, 3, s);
+    }
     if (p.fused_ok[a.n] && expert_fused_layout(p.desc, a.n, p.sm_count, p.smem_optin, a)) {
         err = launch_expert_fused(a, p.sm_count, s);
         if (err != cudaSuccess) return err;

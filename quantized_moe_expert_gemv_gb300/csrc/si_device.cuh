@@ -150,56 +150,6 @@ __device__ __forceinline__ float group_sum(float v) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
-// ------------------------------------------------------------------ top-k
-// One warp selects the k largest of z[0..E) (E <= 256, k <= 16), descending,
-// equal values -> lower index first, and the renormalised softmax weights
-// w_i = exp(z_i - z_0) / sum_j exp(z_j - z_0) over the selected logits
-// (equal to the full softmax renormalised over the selection).  All lanes
-// return the same ids/weights.
-__device__ __forceinline__ void warp_topk(const float *z, int E, int k, int *ids, float *wts) {
-    const int lane = threadIdx.x & 31;
-    float v[8];
-    bool live[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int idx = lane + 32 * j;
-        live[j] = idx < E;
-        v[j] = live[j] ? z[idx] : 0.0f;
-    }
-    float zsel[16];
-    for (int i = 0; i < k; ++i) {
-        float bv = 0.0f;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int idx = lane + 32 * j;
-            if (live[j] && (bi == 0x7fffffff || v[j] > bv)) {
-                bv = v[j];
-                bi = idx;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            const bool take = (oi != 0x7fffffff) &&
-                              (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-            if (take) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (lane + 32 * j == bi) live[j] = false;
-        ids[i] = bi;
-        zsel[i] = bv;
-    }
-    float denom = 0.0f;
-    for (int i = 0; i < k; ++i) denom += expf(zsel[i] - zsel[0]);
-    for (int i = 0; i < k; ++i) wts[i] = expf(zsel[i] - zsel[0]) / denom;
-}
-
 }  // namespace si
 
 // =====================================================================
@@ -283,6 +233,18 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
     return v;
 }
 
+// Fault-injection wait (test mode only): wait for `*flag != 0` -- a word
+// nothing writes -- for at most `budget` cycles; returns false when the wait
+// runs out, which it always does.
+__device__ __forceinline__ bool wait_flag_bounded(const int32_t *flag, long long budget) {
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(flag) == 0) {
+        if (clock64() - t0 > budget) return false;
+        __nanosleep(32);
+    }
+    return true;
+}
+
 // Grid-wide barrier over all CTAs of a launch whose CTAs are all resident
 // (grid <= resident capacity).  ctr/gen are two words of the scratch control
 // block: the last arriver resets the counter and bumps the generation.
@@ -316,6 +278,250 @@ __device__ __forceinline__ bool grid_barrier(int32_t *ctr, int32_t *gen, int32_t
     }
     __syncthreads();
     return s_ok != 0;
+}
+
+}  // namespace si
+
+// =====================================================================
+// Thread-block clusters: distributed shared memory and the cluster barrier.
+// =====================================================================
+namespace si {
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Store v into shared memory of CTA `rank` of this cluster, at the address that
+// `local` has in this CTA.
+__device__ __forceinline__ void st_cluster_f32(const void *local, uint32_t rank, float v) {
+    uint32_t raddr;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(raddr), "f"(v) : "memory");
+}
+// All threads of all CTAs of the cluster; release/acquire orders DSMEM stores.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+}  // namespace si
+
+// =====================================================================
+// int16-activation chunk dot products (dp2a).
+//
+// A chunk is 64 consecutive input columns: sub-blocks 2i (a) and 2i+1 (b) of
+// one Q4_K block.  Its activations are held as 32 words of signed 16-bit
+// pairs (word p = columns 2p | 2p+1 << 16), xq = rint(x / s) with
+// s = max|x| / 32767 over the chunk, so |xq| <= 32767 and the quantisation
+// error is at most s/2 per column (relative ~1.5e-5 of the chunk's largest
+// activation).  Dot products with the 4-bit codes are then exact int32 sums
+// (dp2a: two 16x8-bit products per instruction); the sub-block sums of the
+// unquantised activations, X_a and X_b, carry the min term exactly:
+//   sum_l w_l x_l ~= d*s*(sc_a*I_a + sc_b*I_b) - dmin*(m_a*X_a + m_b*X_b)
+// with I = sum q*xq.  Bounds: |I| <= 32*15*32767 < 2^24 and
+// |sc_a*I_a + sc_b*I_b| <= 2*63*15728160 < 2^31.
+// (The pages' decode kernels use "on-read dp4a MMVQ" with 8-bit
+// activations; 16-bit activations keep the error far below the tolerance.)
+// =====================================================================
+namespace si {
+
+__device__ __forceinline__ int dp2a_lo(uint32_t xpair, uint32_t bytes, int acc) {
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(acc) : "r"(xpair), "r"(bytes));
+    return acc;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t xpair, uint32_t bytes, int acc) {
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(acc) : "r"(xpair), "r"(bytes));
+    return acc;
+}
+
+// round(a*inv) and round(b*inv) (|.| <= 32767) as one word of int16 pairs:
+// adding 1.5*2^23 puts the rounded integer in the low mantissa bits
+// (round-to-nearest-even by the addition), two's complement included.
+__device__ __forceinline__ uint32_t pack_q16(float a, float b, float inv) {
+    const uint32_t ua = __float_as_uint(fmaf(a, inv, 12582912.0f));
+    const uint32_t ub = __float_as_uint(fmaf(b, inv, 12582912.0f));
+    return __byte_perm(ua, ub, 0x5410);
+}
+
+// Quantise 64 activations (pairs) into 32 int16-pair words; returns the scale.
+__device__ __forceinline__ float quantize64(const float (&x)[64], uint32_t (&w)[32], float &Xa, float &Xb) {
+    // max |x| and the two sub-block sums as balanced trees (short dependency chains)
+    float m[32], sa[16], sb[16];
+#pragma unroll
+    for (int l = 0; l < 32; ++l) m[l] = fmaxf(fabsf(x[2 * l]), fabsf(x[2 * l + 1]));
+#pragma unroll
+    for (int l = 0; l < 16; ++l) {
+        sa[l] = x[2 * l] + x[2 * l + 1];
+        sb[l] = x[32 + 2 * l] + x[32 + 2 * l + 1];
+    }
+#pragma unroll
+    for (int w2 = 16; w2 >= 1; w2 >>= 1) {
+#pragma unroll
+        for (int l = 0; l < w2; ++l) m[l] = fmaxf(m[l], m[l + w2]);
+    }
+#pragma unroll
+    for (int w2 = 8; w2 >= 1; w2 >>= 1) {
+#pragma unroll
+        for (int l = 0; l < w2; ++l) {
+            sa[l] += sa[l + w2];
+            sb[l] += sb[l + w2];
+        }
+    }
+    const float mx = m[0];
+    Xa = sa[0];
+    Xb = sb[0];
+    const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
+#pragma unroll
+    for (int p = 0; p < 32; ++p) w[p] = pack_q16(x[2 * p], x[2 * p + 1], inv);
+    return mx * (1.0f / 32767.0f);
+}
+
+// I_a = sum_l q_lo(l)*xq[l], I_b = sum_l q_hi(l)*xq[32+l] over one 32-byte
+// chunk (q0, q1); xw(p) returns activation word p (p < 32).
+template <typename XW>
+__device__ __forceinline__ int2 chunk_isums(const uint4 &q0, const uint4 &q1, XW xw) {
+    int a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t lo = w[t] & 0x0f0f0f0fu;  // codes of sub-block a, weights 4t..4t+3
+        const uint32_t hi = w[t] & 0xf0f0f0f0u;  // 16 x codes of sub-block b
+        a0 = dp2a_lo(xw(2 * t), lo, a0);
+        a1 = dp2a_hi(xw(2 * t + 1), lo, a1);
+        b0 = dp2a_lo(xw(16 + 2 * t), hi, b0);
+        b1 = dp2a_hi(xw(16 + 2 * t + 1), hi, b1);
+    }
+    return make_int2(a0 + a1, (b0 + b1) >> 4);  // b sums are exact multiples of 16
+}
+
+struct ChunkScalesI {
+    float d, dmin;
+    int sca, scb, ma, mb;
+};
+
+// Scales and mins of sub-blocks 2i and 2i+1 without branching on i (i varies
+// across the lanes of a warp).  The pair's bytes sit at bit offset 16*(i&1):
+//   i < 2 : sc = bytes of scales[0..3] & 63,  m = bytes of scales[4..7] & 63
+//   i >= 2: sc = (scales[8..11] & 15) | (top 2 bits of scales[0..3]) << 4
+//           m  = (scales[8..11] >> 4) | (top 2 bits of scales[4..7]) << 4
+__device__ __forceinline__ ChunkScalesI chunk_scales_i(const uint4 &hdr, int i) {
+    ChunkScalesI s;
+    s.d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffffu)));
+    s.dmin = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+    const int sh = 16 * (i & 1);
+    const bool low = i < 2;
+    const uint32_t Y = hdr.y >> sh, Z = hdr.z >> sh, W = hdr.w >> sh;
+    const uint32_t hiY = (Y >> 2) & 0x3030u, hiZ = (Z >> 2) & 0x3030u;
+    const uint32_t scp = low ? (Y & 0x3f3fu) : ((W & 0x0f0fu) | hiY);
+    const uint32_t mp = low ? (Z & 0x3f3fu) : (((W >> 4) & 0x0f0fu) | hiZ);
+    s.sca = scp & 0xffu;
+    s.scb = (scp >> 8) & 0xffu;
+    s.ma = mp & 0xffu;
+    s.mb = (mp >> 8) & 0xffu;
+    return s;
+}
+
+__device__ __forceinline__ float chunk_contrib_i(const ChunkScalesI &c, int2 I, float xs, float Xa, float Xb) {
+    const int sc = c.sca * I.x + c.scb * I.y;
+    const float mm = fmaf((float)c.ma, Xa, (float)c.mb * Xb);
+    return fmaf(c.d * xs, (float)sc, -c.dmin * mm);
+}
+
+// Top-k of n rows of logits z[t][0..E) by ranks, using all threads of a CTA:
+// the rank of z[t][e] is the number of logits that beat it (greater, or equal
+// with a lower index); the experts of rank < k are the selection, stored at
+// their rank (descending order, ties -> lower index).  ids/zsel are
+// [n][SI_MAX_TOPK] in shared memory; zsel receives the selected logits.
+// When the CTA has spare threads, tpi threads share one logit's comparisons
+// and add their counts with shuffles.  Needs a __syncthreads before (z
+// complete) and after (results complete).
+__device__ __forceinline__ int rank_part(const float *zr, int E, int e, float ze, int j0, int step) {
+    int rank = 0;
+#pragma unroll 4
+    for (int j = j0; j < E; j += step) {
+        const float zj = zr[j];
+        rank += (zj > ze) | ((zj == ze) & (j < e));
+    }
+    return rank;
+}
+
+__device__ __forceinline__ void cta_topk_ranks(const float (*z)[256], int n, int E, int k, int (*ids)[16],
+                                               float (*zsel)[16]) {
+    const int items = n * E;
+    int tpi = 1;
+    while (tpi < 32 && items * tpi * 2 <= (int)blockDim.x) tpi <<= 1;
+    if (tpi == 1) {
+        for (int q = threadIdx.x; q < items; q += blockDim.x) {
+            const int t = q / E, e = q - t * E;
+            const float ze = z[t][e];
+            const int rank = rank_part(z[t], E, e, ze, 0, 1);
+            if (rank < k) {
+                ids[t][rank] = e;
+                zsel[t][rank] = ze;
+            }
+        }
+    } else {
+        // one pass; every thread takes part in the shuffles (items * tpi <= blockDim)
+        const int q = threadIdx.x;
+        const int item = min(q / tpi, items - 1), part = q & (tpi - 1);
+        const int t = item / E, e = item - t * E;
+        const float ze = z[t][e];
+        int rank = rank_part(z[t], E, e, ze, part, tpi);
+        for (int o = tpi >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        if (q / tpi < items && part == 0 && rank < k) {
+            ids[t][rank] = e;
+            zsel[t][rank] = ze;
+        }
+    }
+}
+
+// Renormalised softmax weights of one token's selected logits (one warp):
+// w_i = exp(z_i - z_0) / sum_j exp(z_j - z_0), z_0 the largest.  In place.
+__device__ __forceinline__ void warp_renorm(float *zw, int k) {
+    const int lane = threadIdx.x & 31;
+    const float z0 = zw[0];
+    const float ex = lane < k ? expf(zw[lane] - z0) : 0.f;
+    float den = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    __syncwarp();
+    if (lane < k) zw[lane] = ex / den;
+    __syncwarp();
+}
+
+}  // namespace si
+
+// =====================================================================
+// Tiled TMA (tensor-map) loads and float reductions into global memory.
+// =====================================================================
+namespace si {
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// 2-D tiled tensor load of one box into shared memory (dst 128-byte aligned),
+// completing bytes on mbarrier `bar`; x = innermost coordinate (elements).
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void red_add_f32(float *p, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 }  // namespace si

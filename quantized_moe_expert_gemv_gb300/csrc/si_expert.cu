@@ -38,46 +38,31 @@ constexpr int kConsumerWarps = 8;
 constexpr int kExpertThreads = (kConsumerWarps + 1) * 32;
 constexpr long long kDrainBudget = 4000000000LL;  // cycles to wait for in-flight copies after an error
 constexpr int kMaxDownRowsPerLane = 4;            // rows per CTA <= 32
+constexpr int kStaticSmemReserve = 4096;
+constexpr int kPairsPerWarp = 2;                  // gate/up row pairs per warp per stage          // static shared memory of k_expert (routing table, flags)
 
 // ------------------------------------------------------------------ helpers
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
-// Code sums of one chunk against NT token activations read from shared memory
-// (xa[t] points at the chunk's first column for token t; sub-block b is +32).
-template <int NT>
-__device__ __forceinline__ void chunk_code_sums_smem(const uint4 &q0, const uint4 &q1,
-                                                     const float *const (&xa)[NT], ChunkSums (&out)[NT]) {
-    f32x2 acc_a[NT], acc_b[NT];
+// Sum of four per-lane partials (v0..v3) over a group of GS lanes.  On
+// return, lane 0 of the group holds the total of v0, lane GS/4 of v1, lane
+// GS/2 of v2, lane 3GS/4 of v3.
+template <int GS>
+__device__ __forceinline__ float group_sum_quad(float v0, float v1, float v2, float v3, int li) {
+    const bool up2 = (li & (GS / 2)) != 0;
+    float a = up2 ? v2 : v0, b = up2 ? v3 : v1;
+    a += __shfl_xor_sync(0xffffffffu, up2 ? v0 : v2, GS / 2);
+    b += __shfl_xor_sync(0xffffffffu, up2 ? v1 : v3, GS / 2);
+    const bool up1 = (li & (GS / 4)) != 0;
+    float v = up1 ? b : a;
+    v += __shfl_xor_sync(0xffffffffu, up1 ? a : b, GS / 4);
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc_a[t] = acc_b[t] = 0ull;
-    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const uint32_t lo = w[p] & 0x0f0f0f0fu;
-        const uint32_t hi = (w[p] >> 4) & 0x0f0f0f0fu;
-        const f32x2 l01 = pack2(code_plus_128<0>(lo), code_plus_128<1>(lo));
-        const f32x2 l23 = pack2(code_plus_128<2>(lo), code_plus_128<3>(lo));
-        const f32x2 h01 = pack2(code_plus_128<0>(hi), code_plus_128<1>(hi));
-        const f32x2 h23 = pack2(code_plus_128<2>(hi), code_plus_128<3>(hi));
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const f32x2 *pa = reinterpret_cast<const f32x2 *>(xa[t]);
-            ffma2(acc_a[t], l01, pa[2 * p]);
-            ffma2(acc_a[t], l23, pa[2 * p + 1]);
-            ffma2(acc_b[t], h01, pa[16 + 2 * p]);
-            ffma2(acc_b[t], h23, pa[16 + 2 * p + 1]);
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        const float2 fa = unpack2(acc_a[t]), fb = unpack2(acc_b[t]);
-        out[t].Fa = fa.x + fa.y;
-        out[t].Fb = fb.x + fb.y;
-    }
+    for (int off = GS / 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
 }
 
 // Sum of two per-lane partials (g, u) over a group of GS lanes.  Returns the
-// g total in the group's lane 0 (first) and the u total (second).
+// g total (first) and the u total (second) in every lane of the group.
 template <int GS>
 __device__ __forceinline__ float2 group_sum_pair(float g, float u, int li) {
     const bool upper = (li & (GS / 2)) != 0;
@@ -90,6 +75,27 @@ __device__ __forceinline__ float2 group_sum_pair(float g, float u, int li) {
     return make_float2(upper ? other : v, upper ? v : other);
 }
 
+// Per-token quantised activations in shared memory (deduplicated batches):
+// words [n][H/2], scales [n][H/64], sub-block sums [n][H/32].
+struct XQ {
+    const uint32_t *w;
+    const float *sc;
+    const float *sum;
+};
+
+// The call's routing (distinct experts, their tokens/slots, the weights),
+// copied once into shared memory: the producer and the consumers read it for
+// every copy and row, and a global-memory round trip each time would
+// serialise the whole kernel.
+struct SmemRoute {
+    int U;
+    int expert[kMaxSlots];
+    int ntok[kMaxSlots];
+    int tok[kMaxSlots][SI_MAX_DECODE_TOKENS];
+    int slot[kMaxSlots][SI_MAX_DECODE_TOKENS];
+    float wts[kMaxSlots];  // [n*k] routing weights by pair id
+};
+
 struct ExpertWork {
     int p0, p1;  // row pairs [p0, p1) of the flattened (slot, intermediate row) space
     int c0, nrows;
@@ -98,9 +104,10 @@ struct ExpertWork {
 
 // ---------------------------------------------------------------- producer
 template <int NBH>
-__device__ void produce_A(const DecodeArgs &a, const ExpertWork &wk, int j, uint8_t *stA, uint32_t fullA,
-                          uint32_t emptyA, int *lastA, volatile int *s_err, uint64_t pol, bool &ok) {
-    constexpr int CH = kConsumerWarps * (32 / (4 * NBH));
+__device__ void produce_A(const DecodeArgs &a, const SmemRoute &rt, const ExpertWork &wk, int j, uint8_t *stA,
+                          uint32_t fullA, uint32_t emptyA, int *lastA, volatile int *s_err, uint64_t pol,
+                          bool &ok) {
+    constexpr int CH = kConsumerWarps * (32 / (4 * NBH)) * kPairsPerWarp;
     constexpr int rowg = NBH * kBlockBytes;
     constexpr int stage_bytes = 2 * CH * rowg;
     const int NSA = a.fz_nsa;
@@ -124,13 +131,12 @@ __device__ void produce_A(const DecodeArgs &a, const ExpertWork &wk, int j, uint
     mbar_arrive_expect_tx(full, (uint32_t)(2 * (qb - qa) * rowg));
     const uint32_t dst_g = smem_addr(stA + (size_t)st * stage_bytes);
     const uint32_t dst_u = dst_g + CH * rowg;
-    const UniqTable *u = a.uniq;
     for (int p = qa; p < qb;) {
         const int s = p / a.I;
         const int r = p - s * a.I;
         const int run_end = min(qb, (s + 1) * a.I);
         const int n = run_end - p;
-        const size_t src_off = ((size_t)u->expert[s] * a.I + r) * rowg;
+        const size_t src_off = ((size_t)rt.expert[s] * a.I + r) * rowg;
         const uint32_t off = (uint32_t)((p - qa) * rowg);
         bulk_g2s(dst_g + off, a.wg + src_off, (uint32_t)(n * rowg), full, pol);
         bulk_g2s(dst_u + off, a.wu + src_off, (uint32_t)(n * rowg), full, pol);
@@ -139,8 +145,9 @@ __device__ void produce_A(const DecodeArgs &a, const ExpertWork &wk, int j, uint
     lastA[st] = (j / NSA) & 1;
 }
 
-__device__ void produce_B(const DecodeArgs &a, const ExpertWork &wk, int s, uint8_t *stB, uint32_t fullB,
-                          uint32_t emptyB, int *lastB, volatile int *s_err, uint64_t pol, bool &ok) {
+__device__ void produce_B(const DecodeArgs &a, const SmemRoute &rt, const ExpertWork &wk, int s, uint8_t *stB,
+                          uint32_t fullB, uint32_t emptyB, int *lastB, volatile int *s_err, uint64_t pol,
+                          bool &ok) {
     const int NSB = a.fz_nsb;
     const int st = s % NSB;
     if (s >= NSB) {
@@ -160,7 +167,7 @@ __device__ void produce_B(const DecodeArgs &a, const ExpertWork &wk, int s, uint
     const uint32_t bytes = (uint32_t)(wk.nrows * rowd);
     const uint32_t full = fullB + 8 * st;
     mbar_arrive_expect_tx(full, bytes);
-    const size_t src_off = ((size_t)a.uniq->expert[s] * a.H + wk.c0) * rowd;
+    const size_t src_off = ((size_t)rt.expert[s] * a.H + wk.c0) * rowd;
     bulk_g2s(smem_addr(stB + (size_t)st * a.fz_stage_b), a.wd + src_off, bytes, full, pol);
     lastB[st] = (s / NSB) & 1;
 }
@@ -171,10 +178,11 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t sm[];
     constexpr int GS = 4 * NBH;   // lanes per gate/up row
     constexpr int RPW = 32 / GS;  // rows per warp pass
-    constexpr int CH = kConsumerWarps * RPW;
+    constexpr int CH = kConsumerWarps * RPW * kPairsPerWarp;  // row pairs per stage
     constexpr int rowg = NBH * kBlockBytes;
     constexpr int stageA_bytes = 2 * CH * rowg;
     __shared__ int s_err;
+    __shared__ SmemRoute rt;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NSA = a.fz_nsa, NSB = a.fz_nsb;
@@ -205,8 +213,23 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
     __syncthreads();
     pdl_wait();  // the router kernel (and everything before it) is complete
 
-    const UniqTable *u = a.uniq;
-    const int U = a.ctrl[kCtrlNumUnique];
+    {
+        const int *src = reinterpret_cast<const int *>(a.uniq);  // UniqTable: expert, ntok, tok, slot
+        for (int q = threadIdx.x; q < kMaxSlots * (2 + 2 * SI_MAX_DECODE_TOKENS); q += blockDim.x) {
+            const int v = src[q];
+            if (q < kMaxSlots) rt.expert[q] = v;
+            else if (q < 2 * kMaxSlots) rt.ntok[q - kMaxSlots] = v;
+            else if (q < 2 * kMaxSlots + kMaxSlots * SI_MAX_DECODE_TOKENS)
+                (&rt.tok[0][0])[q - 2 * kMaxSlots] = v;
+            else
+                (&rt.slot[0][0])[q - 2 * kMaxSlots - kMaxSlots * SI_MAX_DECODE_TOKENS] = v;
+        }
+        for (int q = threadIdx.x; q < a.n * a.k; q += blockDim.x) rt.wts[q] = a.wts[q];
+        if (threadIdx.x == 0) rt.U = a.ctrl[kCtrlNumUnique];
+    }
+    __syncthreads();
+    const SmemRoute *u = &rt;
+    const int U = rt.U;
     ExpertWork wk;
     {
         const long long P = (long long)U * a.I;
@@ -226,10 +249,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();
             const int first = min(wk.nA, NSA);
-            for (int j = 0; j < first; ++j) produce_A<NBH>(a, wk, j, stA, fullA, emptyA, lastA, verr, pol, ok);
-            for (int s = 0; s < min(wk.nB, NSB); ++s) produce_B(a, wk, s, stB, fullB, emptyB, lastB, verr, pol, ok);
+            for (int j = 0; j < first; ++j)
+                produce_A<NBH>(a, rt, wk, j, stA, fullA, emptyA, lastA, verr, pol, ok);
+            for (int s = 0; s < min(wk.nB, NSB); ++s)
+                produce_B(a, rt, wk, s, stB, fullB, emptyB, lastB, verr, pol, ok);
             for (int j = first; j < wk.nA && ok; ++j)
-                produce_A<NBH>(a, wk, j, stA, fullA, emptyA, lastA, verr, pol, ok);
+                produce_A<NBH>(a, rt, wk, j, stA, fullA, emptyA, lastA, verr, pol, ok);
         }
         __syncwarp();
     }
@@ -237,38 +262,62 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
     // ------------------------------------------------ phase A (consumers)
     if (warp < kConsumerWarps) {
         const int g = lane / GS, li = lane % GS, b = li >> 2, i = li & 3;
-        float *xs = reinterpret_cast<float *>(sm + a.fz_off_x);  // DEDUP: [n][H] fp32
-        float *Xs = xs + a.n * a.H;                               // DEDUP: [n][H/32]
-        f32x2 xr[32];
-        float Xa = 0.f, Xb = 0.f;
+        const int chunk = 4 * b + i;  // this lane's 64-column chunk of a gate/up row
+        uint32_t xw[32];
+        float xs = 0.f, Xa = 0.f, Xb = 0.f;
+        XQ xq{};
         if (!DEDUP) {
-            const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + kQK * b + 64 * i);
+            float xf[64];
+            const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + 64 * chunk);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const uint4 v = __ldg(xp + q);
                 const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int e2 = 0; e2 < 4; ++e2) {
-                    const float lo = __uint_as_float(wv[e2] << 16);
-                    const float hi = __uint_as_float(wv[e2] & 0xffff0000u);
-                    xr[4 * q + e2] = pack2(lo, hi);
-                    if (q < 4) Xa += lo + hi;
-                    else Xb += lo + hi;
+                    xf[8 * q + 2 * e2] = __uint_as_float(wv[e2] << 16);
+                    xf[8 * q + 2 * e2 + 1] = __uint_as_float(wv[e2] & 0xffff0000u);
                 }
             }
+            xs = quantize64(xf, xw, Xa, Xb);
         } else {
-            for (int t = threadIdx.x; t < a.n * a.H; t += kConsumerWarps * 32)
-                xs[t] = bf16_bits_to_f32(a.x[t]);
-            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-            for (int t = threadIdx.x; t < a.n * a.H / 32; t += kConsumerWarps * 32) {
-                float sacc = 0.f;
-                for (int l = 0; l < 32; ++l) sacc += xs[32 * t + l];
-                Xs[t] = sacc;
+            uint32_t *xqw = reinterpret_cast<uint32_t *>(sm + a.fz_off_x);  // [n][H/2]
+            float *xqs = reinterpret_cast<float *>(xqw + (size_t)a.n * a.H / 2);  // [n][H/64]
+            float *xqx = xqs + (size_t)a.n * a.H / 64;                          // [n][H/32]
+            for (int c = threadIdx.x; c < a.n * a.H / 64; c += kConsumerWarps * 32) {
+                const int t = c / (a.H / 64), cc = c - t * (a.H / 64);
+                float xf[64];
+                uint32_t wq[32];
+                const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + 64 * cc);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 v = __ldg(xp + q);
+                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        xf[8 * q + 2 * e2] = __uint_as_float(wv[e2] << 16);
+                        xf[8 * q + 2 * e2 + 1] = __uint_as_float(wv[e2] & 0xffff0000u);
+                    }
+                }
+                float sa, sb;
+                xqs[c] = quantize64(xf, wq, sa, sb);
+                xqx[2 * c] = sa;
+                xqx[2 * c + 1] = sb;
+#pragma unroll
+                for (int p = 0; p < 32; ++p) xqw[(size_t)c * 32 + p] = wq[p];
             }
             asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+            xq = XQ{xqw, xqs, xqx};
         }
 
-        for (int j = 0; j < wk.nA; ++j) {
+        if (a.fault_wait) {
+            const bool got = wait_flag_bounded(a.ctrl + kCtrlFaultFlag, a.wait_budget);
+            if (!__all_sync(0xffffffffu, got)) {
+                set_status(status, SI_ERR_TIMEOUT);
+                *verr = 1;
+            }
+        }
+        for (int j = 0; j < wk.nA && !__any_sync(0xffffffffu, *verr != 0); ++j) {
             const int st = j % NSA;
             const bool landed = mbar_wait_bounded(fullA + 8 * st, (j / NSA) & 1, a.wait_budget);
             if (!__all_sync(0xffffffffu, landed)) {  // one decision per warp
@@ -276,61 +325,57 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
                 *verr = 1;
                 break;
             }
-            const int q = CH * j + warp * RPW + g;  // local row-pair index
-            const bool active = q < wk.p1 - wk.p0;
-            const uint8_t *grow = stA + (size_t)st * stageA_bytes + (warp * RPW + g) * rowg + b * kBlockBytes;
-            const uint8_t *urow = grow + CH * rowg;
-            const uint4 hg = lds128(grow), qg0 = lds128(grow + 16 + 32 * i), qg1 = lds128(grow + 32 + 32 * i);
-            const uint4 hu = lds128(urow), qu0 = lds128(urow + 16 + 32 * i), qu1 = lds128(urow + 32 + 32 * i);
-            const SubScales sg = chunk_scales(hg, i), su = chunk_scales(hu, i);
-            const int p = wk.p0 + (active ? q : 0);
-            const int s = p / a.I, r = p - s * a.I;
-            if (!DEDUP) {
-                auto xa2 = [&xr](int t) { return xr[t]; };
-                auto xb2 = [&xr](int t) { return xr[16 + t]; };
-                const float gp = chunk_contrib(sg, chunk_code_sums(qg0, qg1, xa2, xb2), Xa, Xb);
-                const float up = chunk_contrib(su, chunk_code_sums(qu0, qu1, xa2, xb2), Xa, Xb);
-                const float2 gu = group_sum_pair<GS>(gp, up, li);
-                if (active && li == 0) {
-                    const int slot = u->slot[s][0];
-                    a.h[(size_t)slot * a.I + r] = silu(gu.x) * gu.y;
-                }
-            } else {
-                const int nt = active ? u->ntok[s] : 1;
-                // groups of one warp may hold rows of different experts: reduce to the warp's
-                // largest token count so every lane takes part in every shuffle
-                const int nt_warp = __reduce_max_sync(0xffffffffu, nt);
-                float gp[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
-                float up[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
-#define SI_DEDUP_CASE(NT)                                                                        \
-    {                                                                                            \
-        const float *xa[NT];                                                                     \
-        ChunkSums fg[NT], fu[NT];                                                                \
-        _Pragma("unroll") for (int t = 0; t < NT; ++t) xa[t] =                                   \
-            xs + (size_t)u->tok[s][t] * a.H + kQK * b + 64 * i;                                  \
-        chunk_code_sums_smem<NT>(qg0, qg1, xa, fg);                                              \
-        chunk_code_sums_smem<NT>(qu0, qu1, xa, fu);                                              \
-        _Pragma("unroll") for (int t = 0; t < NT; ++t) {                                         \
-            const int xo = u->tok[s][t] * (a.H / 32) + 8 * b + 2 * i;                            \
-            gp[t] = chunk_contrib(sg, fg[t], Xs[xo], Xs[xo + 1]);                                \
-            up[t] = chunk_contrib(su, fu[t], Xs[xo], Xs[xo + 1]);                                \
-        }                                                                                        \
-    }
-                switch (nt) {
-                    case 1: SI_DEDUP_CASE(1) break;
-                    case 2: SI_DEDUP_CASE(2) break;
-                    case 3: SI_DEDUP_CASE(3) break;
-                    default: SI_DEDUP_CASE(4) break;
-                }
-#undef SI_DEDUP_CASE
+            const uint8_t *stage = stA + (size_t)st * stageA_bytes;
+            float part[2 * kPairsPerWarp];   // g, u of each of this warp's row pairs
+            int rows[kPairsPerWarp];
+            bool act[kPairsPerWarp];
 #pragma unroll
-                for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
-                    if (t >= nt_warp) break;
-                    const float2 gu = group_sum_pair<GS>(gp[t], up[t], li);
-                    if (active && li == 0 && t < nt) {
-                        const int pair = u->tok[s][t] * a.k + u->slot[s][t];
-                        a.h[(size_t)pair * a.I + r] = silu(gu.x) * gu.y;
+            for (int m = 0; m < kPairsPerWarp; ++m) {
+                const int ql = (warp * RPW + g) * kPairsPerWarp + m;  // row pair within the stage
+                const int q = CH * j + ql;
+                act[m] = q < wk.p1 - wk.p0;
+                rows[m] = wk.p0 + (act[m] ? q : 0);
+                const uint8_t *grow = stage + ql * rowg + b * kBlockBytes;
+                const uint8_t *urow = grow + CH * rowg;
+                const uint4 hg = lds128(grow), qg0 = lds128(grow + 16 + 32 * i), qg1 = lds128(grow + 32 + 32 * i);
+                const uint4 hu = lds128(urow), qu0 = lds128(urow + 16 + 32 * i), qu1 = lds128(urow + 32 + 32 * i);
+                const ChunkScalesI cg = chunk_scales_i(hg, i), cu = chunk_scales_i(hu, i);
+                if (!DEDUP) {
+                    auto xwf = [&xw](int p) { return xw[p]; };
+                    part[2 * m] = chunk_contrib_i(cg, chunk_isums(qg0, qg1, xwf), xs, Xa, Xb);
+                    part[2 * m + 1] = chunk_contrib_i(cu, chunk_isums(qu0, qu1, xwf), xs, Xa, Xb);
+                } else {
+                    // every token that chose this row's expert; h lands per (token, slot) pair
+                    const int p = rows[m];
+                    const int s = p / a.I, r = p - s * a.I;
+                    const int nt = act[m] ? u->ntok[s] : 0;
+                    const int nt_warp = __reduce_max_sync(0xffffffffu, nt);
+                    for (int t = 0; t < nt_warp; ++t) {
+                        const int tok = t < nt ? u->tok[s][t] : 0;
+                        const uint32_t *wrow = xq.w + (size_t)tok * a.H / 2 + 32 * chunk;
+                        auto xwf = [wrow](int pp) { return wrow[pp]; };
+                        const float sc = xq.sc[tok * (a.H / 64) + chunk];
+                        const float xa = xq.sum[tok * (a.H / 32) + 2 * chunk];
+                        const float xb = xq.sum[tok * (a.H / 32) + 2 * chunk + 1];
+                        const float gp = chunk_contrib_i(cg, chunk_isums(qg0, qg1, xwf), sc, xa, xb);
+                        const float up = chunk_contrib_i(cu, chunk_isums(qu0, qu1, xwf), sc, xa, xb);
+                        const float2 gu = group_sum_pair<GS>(gp, up, li);
+                        if (t < nt && li == 0) {
+                            const int pair = u->tok[s][t] * a.k + u->slot[s][t];
+                            a.h[(size_t)pair * a.I + r] = silu(gu.x) * gu.y;
+                        }
                     }
+                }
+            }
+            if (!DEDUP) {
+                static_assert(kPairsPerWarp == 2, "reduction below is written for two row pairs");
+                const float tot = group_sum_quad<GS>(part[0], part[1], part[2], part[3], li);
+                const float other = __shfl_down_sync(0xffffffffu, tot, GS / 4);  // u of the same pair
+                const int m = (li == 0) ? 0 : 1;
+                if ((li == 0 || li == GS / 2) && act[m]) {
+                    const int p = rows[m];
+                    const int s = p / a.I, r = p - s * a.I;
+                    a.h[(size_t)u->slot[s][0] * a.I + r] = silu(tot) * other;
                 }
             }
             __syncwarp();
@@ -347,7 +392,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
         if (lane == 0 && !*verr) {
             const uint64_t pol = l2_evict_first_policy();
             for (int s = NSB; s < wk.nB && ok; ++s)
-                produce_B(a, wk, s, stB, fullB, emptyB, lastB, verr, pol, ok);
+                produce_B(a, rt, wk, s, stB, fullB, emptyB, lastB, verr, pol, ok);
         }
         __syncwarp();
     }
@@ -359,11 +404,18 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
     if (warp < kConsumerWarps && !skip_b) {
         const int nbI = a.I / kQK;
         const int rowd = nbI * kBlockBytes;
-        float *hb = reinterpret_cast<float *>(sm + a.fz_off_h) + (size_t)warp * a.I;
-        float *hs = reinterpret_cast<float *>(sm + a.fz_off_hs) + (size_t)warp * (a.I / 32);
+        const int nsub = a.I / 32;
+        // this warp's quantised copy of one h vector: words [I/2], scales [I/64], sums [I/32]
+        uint32_t *hq = reinterpret_cast<uint32_t *>(sm + a.fz_off_h) + (size_t)warp * (a.I / 2 + a.I / 64 + a.I / 32);
+        float *hsc = reinterpret_cast<float *>(hq + a.I / 2);
+        float *hsum = hsc + a.I / 64;
         const int r8 = lane >> 2, i = lane & 3;
-        for (int s = warp; s < wk.nB; s += kConsumerWarps) {
+        // Chunk s lives in stage s % NSB.  Every stage is owned by one warp, which takes that
+        // stage's chunks in issue order, so no warp ever waits on a stage phase that is more
+        // than one use ahead of the barrier (mbarrier phases are told apart by parity only).
+        for (int s = 0; s < wk.nB; ++s) {
             const int st = s % NSB;
+            if (st % kConsumerWarps != warp) continue;
             const bool landed = mbar_wait_bounded(fullB + 8 * st, (s / NSB) & 1, a.wait_budget);
             if (!__all_sync(0xffffffffu, landed)) {
                 set_status(status, SI_ERR_TIMEOUT);
@@ -374,30 +426,51 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
             const int nt = u->ntok[s];
             for (int jt = 0; jt < nt; ++jt) {
                 const int pair = u->tok[s][jt] * a.k + u->slot[s][jt];
-                const float wgt = a.wts[pair];
-                const float4 *hsrc = reinterpret_cast<const float4 *>(a.h + (size_t)pair * a.I);
-                for (int q = lane; q < a.I / 4; q += 32) reinterpret_cast<float4 *>(hb)[q] = __ldcg(hsrc + q);
-                __syncwarp();
-                for (int q = lane; q < a.I / 32; q += 32) {
-                    const float4 *hp = reinterpret_cast<const float4 *>(hb + 32 * q);
-                    float sacc = 0.f;
+                const float wgt = rt.wts[pair];
+                // quantise h of this (token, slot): lane = sub-block, partner lane^1 shares the chunk
+                for (int sb0 = 0; sb0 < nsub; sb0 += 32) {
+                    const int sb = sb0 + lane;
+                    float hv[32];
+                    float mx = 0.f, sum = 0.f;
+                    if (sb < nsub) {
+                        const float4 *hp = reinterpret_cast<const float4 *>(a.h + (size_t)pair * a.I + 32 * sb);
 #pragma unroll
-                    for (int l = 0; l < 8; ++l) {
-                        const float4 v = hp[l];
-                        sacc += (v.x + v.y) + (v.z + v.w);
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 v = __ldcg(hp + q);
+                            hv[4 * q] = v.x, hv[4 * q + 1] = v.y, hv[4 * q + 2] = v.z, hv[4 * q + 3] = v.w;
+                        }
+#pragma unroll
+                        for (int l = 0; l < 32; ++l) {
+                            mx = fmaxf(mx, fabsf(hv[l]));
+                            sum += hv[l];
+                        }
                     }
-                    hs[q] = sacc;
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    if (sb < nsub) {
+                        const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
+#pragma unroll
+                        for (int pp = 0; pp < 16; ++pp) {
+                            const int lo = __float2int_rn(hv[2 * pp] * inv);
+                            const int hi = __float2int_rn(hv[2 * pp + 1] * inv);
+                            hq[16 * sb + pp] = (uint32_t)(lo & 0xffff) | ((uint32_t)hi << 16);
+                        }
+                        hsum[sb] = sum;
+                        if ((sb & 1) == 0) hsc[sb >> 1] = mx * (1.0f / 32767.0f);
+                    }
                 }
                 __syncwarp();
                 float acc[kMaxDownRowsPerLane] = {0.f, 0.f, 0.f, 0.f};
                 for (int bb = 0; bb < nbI; ++bb) {
-                    const f32x2 *hx = reinterpret_cast<const f32x2 *>(hb + kQK * bb + 64 * i);
-                    f32x2 hr[32];
+                    const int c = 4 * bb + i;
+                    uint32_t hw[32];
+                    const uint4 *hqp = reinterpret_cast<const uint4 *>(hq + 32 * c);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) hr[t] = hx[t];
-                    const float Ha = hs[8 * bb + 2 * i], Hb = hs[8 * bb + 2 * i + 1];
-                    auto xa2 = [&hr](int t) { return hr[t]; };
-                    auto xb2 = [&hr](int t) { return hr[16 + t]; };
+                    for (int q = 0; q < 8; ++q) {
+                        const uint4 v = hqp[q];
+                        hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
+                    }
+                    const float xs = hsc[c], Ha = hsum[2 * c], Hb = hsum[2 * c + 1];
+                    auto xwf = [&hw](int p) { return hw[p]; };
 #pragma unroll
                     for (int m = 0; m < kMaxDownRowsPerLane; ++m) {
                         const int lr = r8 + 8 * m;
@@ -405,8 +478,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
                             const uint8_t *blk = rows + (size_t)lr * rowd + bb * kBlockBytes;
                             const uint4 hd = lds128(blk), q0 = lds128(blk + 16 + 32 * i),
                                         q1 = lds128(blk + 32 + 32 * i);
-                            acc[m] += chunk_contrib(chunk_scales(hd, i), chunk_code_sums(q0, q1, xa2, xb2),
-                                                    Ha, Hb);
+                            acc[m] += chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums(q0, q1, xwf), xs, Ha, Hb);
                         }
                     }
                 }
@@ -452,23 +524,25 @@ bool expert_fused_layout(const si_moe_desc &d, int n, int grid, int smem_max, De
     const int RB = (d.hidden + grid - 1) / grid;
     if (RB > 8 * kMaxDownRowsPerLane) return false;
     const int umax = n * d.top_k;
-    const int CH = kConsumerWarps * (32 / (4 * nbh));
+    const int CH = kConsumerWarps * (32 / (4 * nbh)) * kPairsPerWarp;
     const size_t stageA = (size_t)2 * CH * nbh * kBlockBytes;
     const size_t stageB = (size_t)RB * nbi * kBlockBytes;
     const long long P = (long long)umax * d.intermediate;
     const int nA_max = (int)(((P + grid - 1) / grid + CH - 1) / CH);
     const bool dedup = n > 1;
     auto al = [](size_t v) { return (v + 127) / 128 * 128; };
-    const size_t x_bytes = dedup ? al((size_t)n * d.hidden * 4 + (size_t)n * (d.hidden / 32) * 4) : 0;
-    const size_t h_bytes = al((size_t)kConsumerWarps * d.intermediate * 4);
-    const size_t hs_bytes = al((size_t)kConsumerWarps * (d.intermediate / 32) * 4);
+    const size_t x_bytes =
+        dedup ? al((size_t)n * (d.hidden / 2 + d.hidden / 64 + d.hidden / 32) * 4) : 0;
+    const size_t h_bytes =
+        al((size_t)kConsumerWarps * (d.intermediate / 2 + d.intermediate / 64 + d.intermediate / 32) * 4);
+    const size_t hs_bytes = 0;
     const size_t yw_bytes = al((size_t)umax * RB * 4);
-    int NSA = nA_max < 6 ? (nA_max < 1 ? 1 : nA_max) : 6;
+    int NSA = nA_max < 4 ? (nA_max < 1 ? 1 : nA_max) : 4;
     const size_t fixed = x_bytes + h_bytes + hs_bytes + yw_bytes;
     auto bar_bytes = [](int nsa, int nsb) { return (size_t)16 * (nsa + nsb) + (size_t)4 * (nsa + nsb) + 64; };
     const long long sA = (long long)stageA, sB = (long long)stageB;
     auto fits = [&](int nsa, int nsb) {
-        const long long need = 256 + (long long)fixed + (long long)nsa * sA + (long long)nsb * sB +
+        const long long need = kStaticSmemReserve + (long long)fixed + (long long)nsa * sA + (long long)nsb * sB +
                                (long long)bar_bytes(nsa, nsb) + 128;
         return need <= (long long)smem_max;
     };

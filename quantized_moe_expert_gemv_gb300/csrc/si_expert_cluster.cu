@@ -1,0 +1,466 @@
+// si_expert_cluster.cu -- single-token decode: the selected experts' FFN on
+// thread-block clusters, with no grid-wide synchronisation.
+//
+// sparkinfer README (luciferlive112116), "Layout": kernels/ "fused quantized MoE
+// expert FFN", "decode GEMV"; opening section: experts "quantized-resident,
+// dequantized on-read, minimizing bytes-per-token"; "Milestone 1": "split-K
+// occupancy".
+//
+// Work unit = (selected expert e = ids[s], 256-wide block column b of its
+// intermediate dimension).  One cluster of C CTAs owns a unit:
+//   * gate/up: the cluster's CTAs split the unit's 256 intermediate rows; each
+//     computes h_r = silu(g_r) * u_r for its rows (activations quantised to
+//     int16 per 64-column chunk, dp2a on the 4-bit codes) and writes h_r into
+//     the shared memory of every CTA of the cluster (distributed shared memory);
+//   * one hardware cluster barrier makes the unit's 256 h values visible;
+//   * down: CTA rank c applies Q4_K block b of the down rows
+//     [H*c/C, H*(c+1)/C) of expert e to that h slice and adds w_s * y into the
+//     output with float reductions (the top-k combine: every output row sums
+//     one partial per (slot, block column)).
+// The router kernel zeroes the output first.  Weight bytes: gate/up rows by
+// 1-D bulk copies; down blocks, 144-byte pieces with a 432-byte row stride,
+// by a 2-D tensor map (box = 144 bytes x BR rows).  All copies are issued
+// by one producer thread as soon as the routing is known (L2 evict-first).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+
+#include "si_device.cuh"
+#include "si_internal.h"
+
+namespace si {
+
+namespace {
+constexpr int kCW = 16;                     // consumer warps (four per SM sub-partition)
+constexpr int kClThreads = (kCW + 1) * 32;  // + one producer warp
+constexpr int kPairs = 2;                   // gate/up row pairs per warp per stage
+constexpr long long kDrain = 4000000000LL;
+constexpr int kMaxDownLanes = 8;            // row groups per warp in the down phase: RPC <= 8*kCW*8
+
+__device__ __forceinline__ uint4 ld_s128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+// Sum of four per-lane partials over a group of GS lanes: on return lane 0 of
+// the group holds the total of v0, lane GS/4 of v1, lane GS/2 of v2 and lane
+// 3GS/4 of v3.
+template <int GS>
+__device__ __forceinline__ float quad_sum(float v0, float v1, float v2, float v3, int li) {
+    const bool up2 = (li & (GS / 2)) != 0;
+    float x = up2 ? v2 : v0, y = up2 ? v3 : v1;
+    x += __shfl_xor_sync(0xffffffffu, up2 ? v0 : v2, GS / 2);
+    y += __shfl_xor_sync(0xffffffffu, up2 ? v1 : v3, GS / 2);
+    const bool up1 = (li & (GS / 4)) != 0;
+    float v = up1 ? y : x;
+    v += __shfl_xor_sync(0xffffffffu, up1 ? x : y, GS / 4);
+#pragma unroll
+    for (int off = GS / 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// Sum of (g, u) over a group of GS lanes; lane 0 of the group gets the g total,
+// lane GS/2 the u total.
+template <int GS>
+__device__ __forceinline__ float pair_sum(float g, float u, int li) {
+    const bool up = (li & (GS / 2)) != 0;
+    float v = up ? u : g;
+    v += __shfl_xor_sync(0xffffffffu, up ? g : u, GS / 2);
+#pragma unroll
+    for (int off = GS / 4; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+}  // namespace
+
+template <int NBH>
+__global__ void __launch_bounds__(kClThreads, 1)
+    k_expert_cluster(const __grid_constant__ CUtensorMap tmap_down, DecodeArgs a) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    constexpr int GS = 4 * NBH;
+    constexpr int RPW = 32 / GS;
+    constexpr int CH = kCW * RPW * kPairs;  // row pairs per stage
+    constexpr int rowg = NBH * kBlockBytes;
+    constexpr int stageA = 2 * CH * rowg;
+    __shared__ int s_err;
+    __shared__ int s_expert, s_slot;
+    __shared__ float s_w;
+    __shared__ int s_lastA[8];
+    __shared__ int s_lastB;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = (int)cluster_nctarank();
+    const int rank = (int)cluster_ctarank();
+    const int nbI = a.I / kQK;
+    const int unit = blockIdx.x / C;
+    const int slot = unit / nbI, bcol = unit - slot * nbI;
+    const int r_lo = kQK * bcol + (kQK * rank) / C;
+    const int n_rp = kQK * bcol + (kQK * (rank + 1)) / C - r_lo;
+    const int c_lo = (a.H * rank) / C;
+    const int n_rows = (a.H * (rank + 1)) / C - c_lo;
+    const int nA = (n_rp + CH - 1) / CH;
+    const int NSA = a.cl_nsa;
+    const int BR = a.cl_box_rows, box_stride = a.cl_box_stride, nbox = a.cl_nbox;
+
+    uint8_t *stA = sm + a.cl_off_a;
+    uint8_t *stB = sm + a.cl_off_b;
+    float *hslice = reinterpret_cast<float *>(sm + a.cl_off_h);  // [256] h of the unit
+    float *ybuf = reinterpret_cast<float *>(sm + a.cl_off_y);    // [rows] down partials
+    const uint32_t fullA = smem_addr(sm + a.cl_off_bar);
+    const uint32_t emptyA = fullA + 8 * NSA;
+    const uint32_t fullB = emptyA + 8 * NSA;
+    int32_t *status = a.ctrl + kCtrlStatus;
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tmap_down);  // descriptor fetch off the critical path
+        for (int st = 0; st < NSA; ++st) {
+            mbar_init(fullA + 8 * st, 1);
+            mbar_init(emptyA + 8 * st, kCW);
+            s_lastA[st] = -1;
+        }
+        mbar_init(fullB, 1);
+        s_lastB = -1;
+        s_err = 0;
+        fence_mbar_init();
+    }
+    // The token's H/64 activation chunks, quantised once (warp 0) into shared memory
+    // before the dependency wait: the router launches this kernel only after its
+    // own wait on the producers of x, so x is final here.
+    if (warp == 0 && lane < a.H / 64) {
+        uint32_t *xq = reinterpret_cast<uint32_t *>(sm + a.cl_off_x);  // [H/64][32] words
+        float *xqf = reinterpret_cast<float *>(xq + a.H / 2);          // [H/64][3]: scale, Xa, Xb
+        float xf[64];
+        uint32_t wq[32];
+        float sa, sb;
+        const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + 64 * lane);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint4 v = __ldg(xp + q);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+                xf[8 * q + 2 * e2] = __uint_as_float(wv[e2] << 16);
+                xf[8 * q + 2 * e2 + 1] = __uint_as_float(wv[e2] & 0xffff0000u);
+            }
+        }
+        const float sc = quantize64(xf, wq, sa, sb);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            reinterpret_cast<uint4 *>(xq + 32 * lane)[q] = make_uint4(wq[4 * q], wq[4 * q + 1], wq[4 * q + 2], wq[4 * q + 3]);
+        xqf[3 * lane] = sc;
+        xqf[3 * lane + 1] = sa;
+        xqf[3 * lane + 2] = sb;
+    }
+    __syncthreads();
+    pdl_wait();  // routing of this token is complete
+    if (threadIdx.x == 0) {
+        s_slot = slot;
+        s_expert = a.ids[slot];
+        s_w = a.wts[slot];
+    }
+    __syncthreads();
+    const int e = s_expert;
+    volatile int *verr = &s_err;
+
+    // --------------------------------------------------------- producer
+    if (warp == kCW) {
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            auto issueA = [&](int j) -> bool {
+                const int st = j % NSA;
+                if (j >= NSA) {
+                    const uint32_t par = ((j / NSA) - 1) & 1;
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(emptyA + 8 * st, par)) {
+                        if (*verr || clock64() - t0 > a.wait_budget) {
+                            if (!*verr) set_status(status, SI_ERR_TIMEOUT);
+                            *verr = 1;
+                            return false;
+                        }
+                        __nanosleep(20);
+                    }
+                }
+                const int q0 = CH * j, q1 = min(q0 + CH, n_rp);
+                const uint32_t bytes = (uint32_t)((q1 - q0) * rowg);
+                mbar_arrive_expect_tx(fullA + 8 * st, 2 * bytes);
+                const size_t src = ((size_t)e * a.I + r_lo + q0) * rowg;
+                const uint32_t dst = smem_addr(stA + (size_t)st * stageA);
+                bulk_g2s(dst, a.wg + src, bytes, fullA + 8 * st, pol);
+                bulk_g2s(dst + CH * rowg, a.wu + src, bytes, fullA + 8 * st, pol);
+                s_lastA[st] = (j / NSA) & 1;
+                return true;
+            };
+            const int first = min(nA, NSA);
+            for (int j = 0; j < first; ++j) issueA(j);
+            // down blocks of this CTA's rows: nbox tensor boxes of BR rows x 144 bytes
+            mbar_arrive_expect_tx(fullB, (uint32_t)(nbox * BR * kBlockBytes));
+            for (int bx = 0; bx < nbox; ++bx)
+                tma_load_2d(smem_addr(stB + (size_t)bx * box_stride), &tmap_down, kBlockBytes * bcol,
+                            e * a.H + c_lo + bx * BR, fullB, pol);
+            s_lastB = 0;
+            for (int j = first; j < nA; ++j)
+                if (!issueA(j)) break;
+        }
+        __syncwarp();
+    }
+
+    // --------------------------------------------------------- gate/up
+    if (warp < kCW) {
+        const int g = lane / GS, li = lane % GS, b = li >> 2, i = li & 3;
+        const int chunk = 4 * b + i;
+        const uint32_t *xq = reinterpret_cast<const uint32_t *>(sm + a.cl_off_x);  // quantised in the prologue
+        const float *xqf = reinterpret_cast<const float *>(xq + a.H / 2);
+        uint32_t xw[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint4 v = reinterpret_cast<const uint4 *>(xq + 32 * chunk)[q];
+            xw[4 * q] = v.x, xw[4 * q + 1] = v.y, xw[4 * q + 2] = v.z, xw[4 * q + 3] = v.w;
+        }
+        const float xs = xqf[3 * chunk], Xa = xqf[3 * chunk + 1], Xb = xqf[3 * chunk + 2];
+        auto xwf = [&xw](int p) { return xw[p]; };
+        if (a.fault_wait) {
+            const bool got = wait_flag_bounded(a.ctrl + kCtrlFaultFlag, a.wait_budget);
+            if (!__all_sync(0xffffffffu, got)) {
+                set_status(status, SI_ERR_TIMEOUT);
+                *verr = 1;
+            }
+        }
+        for (int j = 0; j < nA && !__any_sync(0xffffffffu, *verr != 0); ++j) {
+            const int st = j % NSA;
+            const bool landed = mbar_wait_bounded(fullA + 8 * st, (j / NSA) & 1, a.wait_budget);
+            if (!__all_sync(0xffffffffu, landed)) {
+                set_status(status, SI_ERR_TIMEOUT);
+                *verr = 1;
+                break;
+            }
+            const uint8_t *stage = stA + (size_t)st * stageA;
+            float part[2 * kPairs];
+#pragma unroll
+            for (int m = 0; m < kPairs; ++m) {
+                const int ql = (warp * RPW + g) * kPairs + m;  // row pair within the stage
+                const uint8_t *grow = stage + ql * rowg + b * kBlockBytes;
+                const uint8_t *urow = grow + CH * rowg;
+                const uint4 hg = ld_s128(grow), qg0 = ld_s128(grow + 16 + 32 * i), qg1 = ld_s128(grow + 32 + 32 * i);
+                const uint4 hu = ld_s128(urow), qu0 = ld_s128(urow + 16 + 32 * i), qu1 = ld_s128(urow + 32 + 32 * i);
+                part[2 * m] = chunk_contrib_i(chunk_scales_i(hg, i), chunk_isums(qg0, qg1, xwf), xs, Xa, Xb);
+                part[2 * m + 1] = chunk_contrib_i(chunk_scales_i(hu, i), chunk_isums(qu0, qu1, xwf), xs, Xa, Xb);
+            }
+            // totals: g0 at group lane 0, u0 at GS/4, g1 at GS/2, u1 at 3GS/4
+            const float tot = quad_sum<GS>(part[0], part[1], part[2], part[3], li);
+            const float uu = __shfl_down_sync(0xffffffffu, tot, GS / 4);
+            float hv = silu(tot) * uu;  // meaningful in group lanes 0 (pair 0) and GS/2 (pair 1)
+            // lanes 0..C-1 of the group each store one pair's h into one peer (parallel pushes)
+#pragma unroll
+            for (int m = 0; m < kPairs; ++m) {
+                const float hm = __shfl_sync(0xffffffffu, hv, (lane - li) + m * (GS / 2));
+                const int q = CH * j + (warp * RPW + g) * kPairs + m;
+                if (q < n_rp)
+                    for (int peer = li; peer < C; peer += GS)  // GS may be smaller than C
+                        st_cluster_f32(hslice + (r_lo + q - kQK * bcol), (uint32_t)peer, hm);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(emptyA + 8 * st);
+        }
+    }
+
+    // every CTA of the cluster has written its h rows into every peer
+    cluster_sync();
+
+    // --------------------------------------------------------- down + combine
+    const bool skip = __any_sync(0xffffffffu, *verr != 0);
+    uint32_t *hq = reinterpret_cast<uint32_t *>(sm + a.cl_off_x);  // reuse: [4][32] words + [4][3]
+    float *hqf = reinterpret_cast<float *>(hq + 128);
+    if (warp < kCW && !skip) {
+        if (warp < 4) {  // the unit's four 64-column chunks of h: warp c quantises chunk c
+            const float2 v = reinterpret_cast<const float2 *>(hslice + 64 * warp)[lane];  // columns 2l, 2l+1
+            float mx = fmaxf(fabsf(v.x), fabsf(v.y));
+            float sum = v.x + v.y;  // lanes 0..15: sub-block a, 16..31: sub-block b
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
+            hq[32 * warp + lane] = pack_q16(v.x, v.y, inv);
+            if (lane == 0) {
+                hqf[3 * warp] = mx * (1.0f / 32767.0f);
+                hqf[3 * warp + 1] = sum;
+            }
+            if (lane == 16) hqf[3 * warp + 2] = sum;
+        }
+    }
+    if (warp < kCW) asm volatile("bar.sync 1, %0;" ::"r"(kCW * 32) : "memory");  // consumer warps only
+    if (warp < kCW && !skip) {
+        const int r8 = lane >> 2, i = lane & 3;
+        uint32_t hw[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint4 v = reinterpret_cast<const uint4 *>(hq + 32 * i)[q];
+            hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
+        }
+        const float hs = hqf[3 * i], Ha = hqf[3 * i + 1], Hb = hqf[3 * i + 2];
+        auto hwf = [&hw](int p) { return hw[p]; };
+        const bool landed = mbar_wait_bounded(fullB, 0, a.wait_budget);
+        if (!__all_sync(0xffffffffu, landed)) {
+            set_status(status, SI_ERR_TIMEOUT);
+            *verr = 1;
+        } else {
+#pragma unroll 1
+            for (int m = 0; m < kMaxDownLanes; ++m) {
+                const int lr0 = 8 * kCW * m + 8 * warp;  // first row of this warp's 8-row group
+                if (lr0 >= n_rows) break;           // uniform across the warp
+                const int lr = lr0 + r8;
+                float v = 0.f;
+                if (lr < n_rows) {
+                    const int bx = lr / BR;
+                    const uint8_t *blk = stB + (size_t)bx * box_stride + (size_t)(lr - bx * BR) * kBlockBytes;
+                    const uint4 hd = ld_s128(blk), q0 = ld_s128(blk + 16 + 32 * i), q1 = ld_s128(blk + 32 + 32 * i);
+                    v = chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums(q0, q1, hwf), hs, Ha, Hb);
+                }
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                if (i == 0 && lr < n_rows) ybuf[lr] = v;
+            }
+        }
+    }
+    __syncthreads();
+    if (!*verr) {
+        const float w = s_w;
+        float *out = a.out + c_lo;
+        for (int lr = threadIdx.x; lr < n_rows; lr += blockDim.x) red_add_f32(out + lr, w * ybuf[lr]);
+    } else if (threadIdx.x == 0) {
+        for (int st = 0; st < NSA; ++st)
+            if (s_lastA[st] >= 0) mbar_wait_bounded(fullA + 8 * st, s_lastA[st], kDrain);
+        if (s_lastB >= 0) mbar_wait_bounded(fullB, 0, kDrain);
+    }
+}
+
+// ------------------------------------------------------------------ host
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// Cluster size and shared-memory plan for n = 1; false if this shape needs
+// the other expert kernel.
+bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs &a) {
+    const int nbh = d.hidden / kQK;
+    if (nbh != 1 && nbh != 2 && nbh != 4 && nbh != 8) return false;
+    if (C < 2 || C > 8) return false;
+    const int CH = kCW * (32 / (4 * nbh)) * kPairs;
+    const int rowg = nbh * kBlockBytes;
+    const int stageA = 2 * CH * rowg;
+    const int rp_max = (kQK + C - 1) / C;
+    const int nA_max = (rp_max + CH - 1) / CH;
+    const int rpc = (d.hidden + C - 1) / C;  // down rows per CTA (max)
+    if (rpc > 8 * kCW * kMaxDownLanes) return false;
+    const int nbox = (rpc + 255) / 256;
+    const int BR = (rpc + nbox - 1) / nbox;
+    const int box_stride = (BR * kBlockBytes + 127) / 128 * 128;
+    auto al = [](int v) { return (v + 127) / 128 * 128; };
+    int NSA = nA_max < 3 ? nA_max : 3;
+    int off = 0;
+    a.cl_off_a = off;
+    off += NSA * stageA;
+    a.cl_off_b = off;
+    off += nbox * box_stride;
+    a.cl_off_h = off;
+    off += al(kQK * 4);
+    a.cl_off_x = off;  // quantised x: [H/64][32] words + [H/64][3] floats (later: quantised h)
+    off += al(d.hidden / 2 * 4 + d.hidden / 64 * 3 * 4);
+    a.cl_off_y = off;
+    off += al(rpc * 4);
+    a.cl_off_bar = off;
+    off += 8 * (2 * NSA + 1) + 64;
+    if (off + 1024 > smem_max) return false;  // + static shared memory
+    a.cl_nsa = NSA;
+    a.cl_C = C;
+    a.cl_box_rows = BR;
+    a.cl_nbox = nbox;
+    a.cl_box_stride = box_stride;
+    a.cl_smem = off;
+    return true;
+}
+
+static bool make_down_tensor_map(const DecodeArgs &a, CUtensorMap *tm) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int nbi = a.I / kQK;
+    cuuint64_t dims[2] = {(cuuint64_t)nbi * kBlockBytes, (cuuint64_t)a.E * a.H};
+    cuuint64_t strides[1] = {(cuuint64_t)nbi * kBlockBytes};
+    cuuint32_t box[2] = {(cuuint32_t)kBlockBytes, (cuuint32_t)a.cl_box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.wd), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NBH>
+static cudaError_t launch_cluster_t(const DecodeArgs &a, const CUtensorMap &tm, cudaStream_t s) {
+    const int units = a.k * (a.I / kQK);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(units * a.cl_C);
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = a.cl_smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = a.cl_C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH>, tm, a);
+}
+
+cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s) {
+    CUtensorMap tm;
+    if (!make_down_tensor_map(a, &tm)) return cudaErrorInvalidValue;
+    switch (a.H / kQK) {
+        case 1: return launch_cluster_t<1>(a, tm, s);
+        case 2: return launch_cluster_t<2>(a, tm, s);
+        case 4: return launch_cluster_t<4>(a, tm, s);
+        default: return launch_cluster_t<8>(a, tm, s);
+    }
+}
+
+cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters) {
+    *active_clusters = 0;
+    if (!tensor_map_encoder()) return cudaErrorNotSupported;  // down blocks are fetched by a tensor map
+    const void *f = nullptr;
+    switch (nbh) {
+        case 1: f = (const void *)k_expert_cluster<1>; break;
+        case 2: f = (const void *)k_expert_cluster<2>; break;
+        case 4: f = (const void *)k_expert_cluster<4>; break;
+        default: f = (const void *)k_expert_cluster<8>; break;
+    }
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, f);
+    if (err != cudaSuccess) return err;
+    const int dyn_max = smem_max - (int)fa.sharedSizeBytes;
+    if (smem > dyn_max) return cudaErrorInvalidValue;
+    if ((err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max)) != cudaSuccess)
+        return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(active_clusters, f, &cfg);
+}
+
+}  // namespace si

@@ -15,6 +15,7 @@ enum CtrlWord : int {
     kCtrlNumUnique = 2,     // distinct experts selected by this decode call
     kCtrlBarCount = 3,      // grid-barrier arrival counter of the fused expert kernel
     kCtrlBarGen = 4,        // grid-barrier generation
+    kCtrlFaultFlag = 5,     // never written: the fault-injection wait of the expert kernels waits on it
     kCtrlWords = 64,
 };
 constexpr size_t kCtrlBytes = kCtrlWords * sizeof(int32_t);
@@ -39,7 +40,11 @@ struct Plan {
     int l2_bytes;
     int smem_optin;
     long long wait_budget;  // SM cycles a device-side wait may spin before reporting SI_ERR_TIMEOUT
+    bool fault_wait;        // test mode: expert kernels first wait on a flag nothing sets
     bool fused_ok[SI_MAX_DECODE_TOKENS + 1];  // fused expert kernel usable for n tokens
+    bool cluster_ok;                          // cluster expert kernel usable for n = 1
+    int cluster_size;                         // CTAs per cluster (all clusters co-resident)
+    int cluster_active;                       // clusters of that size the device holds at once
     DecodeLayout dec;  // sized for SI_MAX_DECODE_TOKENS tokens
 };
 
@@ -64,9 +69,15 @@ struct DecodeArgs {
     int32_t *o_counts;
     float *o_logits;
     long long wait_budget;
+    int fault_wait;  // test mode (SI_FAULT_WAIT_BUDGET set): wait on kCtrlFaultFlag first
     // shared-memory plan of the fused expert kernel (set by expert_fused_layout)
     int fz_off_a, fz_off_b, fz_off_x, fz_off_h, fz_off_hs, fz_off_yw, fz_off_bar;
     int fz_nsa, fz_nsb, fz_rb, fz_stage_b, fz_smem;
+    // shared-memory plan of the cluster expert kernel (set by expert_cluster_layout)
+    int cl_off_a, cl_off_b, cl_off_h, cl_off_x, cl_off_y, cl_off_bar;
+    int cl_nsa, cl_C, cl_box_rows, cl_nbox, cl_box_stride, cl_smem;
+    int zero_out;  // router zeroes out[n][H] (the expert kernel accumulates into it)
+    int no_table;  // router skips the distinct-expert table (single-token cluster path)
 };
 
 cudaError_t launch_decode(const Plan &p, const DecodeArgs &a, cudaStream_t s,
@@ -74,6 +85,9 @@ cudaError_t launch_decode(const Plan &p, const DecodeArgs &a, cudaStream_t s,
 bool expert_fused_layout(const si_moe_desc &d, int n, int grid, int smem_max, DecodeArgs &a);
 cudaError_t launch_expert_fused(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t expert_fused_occupancy(int nbh, bool dedup, int smem, int smem_max, int *blocks_per_sm);
+bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs &a);
+cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s);
+cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters);
 cudaError_t launch_debug_dequant(const uint8_t *blocks, int64_t n_blocks, float *out_f32,
                                  uint16_t *out_bf16, cudaStream_t s);
 cudaError_t launch_debug_topk(const float *logits, int n, int E, int k, int32_t *ids, float *w,
