@@ -42,6 +42,37 @@ METRIC = "MoE-layer decode tok/s at bs=1 (Qwen3-30B-A3B shape, Q4_K); HBM GB/s v
 FALLBACK_HBM_GBS = 6800.0
 
 
+# DRAM bytes per launch of the dominant kernel from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the
+# kernel's sources are the ones that were profiled (sha256 over the files).
+PROFILED_TRAFFIC = {
+    "k_expert_cluster": {
+        "bytes": 21289472,
+        "profile": "profiles/k_expert_cluster_qwen3_bs1.md",
+        "sources": ["quantized_moe_expert_gemv_gb300/csrc/si_expert_cluster.cu",
+                    "quantized_moe_expert_gemv_gb300/csrc/si_device.cuh",
+                    "quantized_moe_expert_gemv_gb300/csrc/si_internal.h"],
+        "sha256": "00b40ab683079ef1d0b54849da3b6cad91973d2338b0ce7a94f0508fd6f18f1d",
+    },
+}
+
+
+def profiled_traffic(kernel: str):
+    """(bytes per launch, note) from the stored ncu capture, or (None, why not)."""
+    import hashlib
+    ent = PROFILED_TRAFFIC.get(kernel)
+    if ent is None:
+        return None, "no ncu capture for this kernel"
+    root = os.path.dirname(os.path.abspath(__file__))
+    h = hashlib.sha256()
+    for f in ent["sources"]:
+        with open(os.path.join(root, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != ent["sha256"]:
+        return None, "kernel sources changed since the ncu capture"
+    return ent["bytes"], "ncu dram__bytes_read.sum + dram__bytes_write.sum, " + ent["profile"]
+
+
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -307,6 +338,8 @@ def bench_layer(args, dist, binding, device, synth, torch, hbm_peak):
         dom_name = "k_gateup_generic (gate/up dequant-GEMV + SwiGLU)"
         dom_bytes, dom_ms = gateup_bytes, per_launch_ms[1]
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic, traffic_note = profiled_traffic("k_expert_cluster") if path == 2 else \
+        (None, "no ncu capture for this kernel")
 
     # End to end: pinned host tokens in, pinned host outputs back, every step.
     x_pin = torch.from_numpy(x_host.view("int16")).pin_memory()
@@ -345,7 +378,7 @@ def bench_layer(args, dist, binding, device, synth, torch, hbm_peak):
                    "plan": plan_info},
         "roofline": {"bound": "hbm", "kernel": dom_name,
                      "achieved": dom_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": dom_gbs / hbm_peak,
-                     "traffic": None,
+                     "traffic": traffic, "traffic_source": traffic_note,
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "launch_ms": dom_ms,
                      "timing": "CUDA events recorded on the launch stream around each launch "
