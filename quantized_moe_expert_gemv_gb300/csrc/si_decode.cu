@@ -44,7 +44,9 @@ __device__ __forceinline__ float dot8_bf16(const float4 &w0, const float4 &w1, c
 // Logits are gathered into CTA 0 through distributed shared memory; CTA 0
 // takes softmax, top-k, renormalised weights, per-expert counts and the
 // table of distinct experts (deterministic: ascending expert id, tokens in
-// pair order).
+// pair order).  One token feeding the cluster expert kernel (sel_logits):
+// every CTA receives every logit, each warp ranks its own expert and stores
+// the selected ones at their rank; the expert kernel forms the weights.
 template <int NJ>
 __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs a) {
     __shared__ float s_z[SI_MAX_DECODE_TOKENS][SI_MAX_EXPERTS];
@@ -53,10 +55,24 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
     __shared__ int s_counts[SI_MAX_EXPERTS];
     __shared__ int s_pos[SI_MAX_EXPERTS];
     __shared__ int s_U;
+    __shared__ uint4 s_x[NJ > 0 ? SI_MAX_DECODE_TOKENS * 32 * NJ : 1];  // x [n][H] bf16 (NJ > 0)
+    // parameters used after the dependency wait, read now
+    const uint16_t *const xg_p = pin_ptr(a.x);
+    float *const out_p = pin_ptr(a.out);
+    const float *const bias_p = pin_ptr(a.router_bias);
+    float *const ologits_p = pin_ptr(a.o_logits);
+    int32_t *const ids_p = pin_ptr(a.ids);
+    float *const wts_p = pin_ptr(a.wts);
+    int32_t *const oids_p = pin_ptr(a.o_ids);
+    float *const ow_p = pin_ptr(a.o_w);
+    int32_t *const counts_p = pin_ptr(a.counts);
+    int32_t *const ocounts_p = pin_ptr(a.o_counts);
+    const int n = pin_i32(a.n), H = pin_i32(a.H), E = pin_i32(a.E), k = pin_i32(a.k);
+    const int zero_out = pin_i32(a.zero_out), sel_logits = pin_i32(a.sel_logits);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wpc = blockDim.x >> 5;
     const int e = blockIdx.x * wpc + warp;
-    const float *wrow = a.router_w + (size_t)min(e, a.E - 1) * a.H;
+    const float *wrow = a.router_w + (size_t)min(e, E - 1) * H;
     float4 wr[2 * (NJ > 0 ? NJ : 1)];
     if (NJ > 0) {
 #pragma unroll
@@ -65,37 +81,43 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
             wr[2 * j + 1] = __ldg(reinterpret_cast<const float4 *>(wrow + 256 * j + 8 * lane + 4));
         }
     }
+    if (NJ > 0) {  // the router rows must be in registers before the wait, not fetched after it
+#pragma unroll
+        for (int j = 0; j < 2 * NJ; ++j)
+            asm volatile("" ::"f"(wr[j].x), "f"(wr[j].y), "f"(wr[j].z), "f"(wr[j].w));
+    }
     // Warm L2 with x (a prefetch returns no data: if an earlier kernel is still
     // writing x, L2 stays coherent and the loads below happen after the wait).
-    if (blockIdx.x == 0 && threadIdx.x < (a.n * a.H * 2) / 128) prefetch_l2(reinterpret_cast<const uint8_t *>(a.x) + 128 * threadIdx.x);
+    if (blockIdx.x == 0 && threadIdx.x < (n * H * 2) / 128) prefetch_l2(reinterpret_cast<const uint8_t *>(xg_p) + 128 * threadIdx.x);
     pdl_wait();               // x and the scratch are ready (previous kernels complete)
     pdl_launch_dependents();  // the expert kernel may become resident now (x is final)
-    if (a.zero_out) {         // the cluster expert kernel accumulates the top-k combine into out
-        const int nthr = gridDim.x * blockDim.x;
-        for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < a.n * a.H; q += nthr) a.out[q] = 0.f;
+    if (NJ > 0) {             // x once per CTA into shared memory (every warp reads all of it)
+        const uint4 *xg = reinterpret_cast<const uint4 *>(xg_p);
+        for (int q = threadIdx.x; q < n * 32 * NJ; q += blockDim.x) s_x[q] = __ldg(xg + q);
     }
-    if (e < a.E) {
+    if (zero_out) {         // the cluster expert kernel accumulates the top-k combine into out
+        const int nthr = gridDim.x * blockDim.x;
+        for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n * H; q += nthr) out_p[q] = 0.f;
+    }
+    if (NJ > 0) __syncthreads();
+    if (e < E) {
         float acc[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
         if (NJ > 0) {
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
 #pragma unroll
                 for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
-                    if (t < a.n) {
-                        const uint4 xv = __ldg(
-                            reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + 256 * j + 8 * lane));
-                        acc[t] = dot8_bf16(wr[2 * j], wr[2 * j + 1], xv, acc[t]);
-                    }
+                    if (t < n) acc[t] = dot8_bf16(wr[2 * j], wr[2 * j + 1], s_x[32 * (NJ * t + j) + lane], acc[t]);
                 }
             }
         } else {
-            for (int c = 8 * lane; c < a.H; c += 256) {
+            for (int c = 8 * lane; c < H; c += 256) {
                 const float4 w0 = __ldg(reinterpret_cast<const float4 *>(wrow + c));
                 const float4 w1 = __ldg(reinterpret_cast<const float4 *>(wrow + c + 4));
 #pragma unroll
                 for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
-                    if (t < a.n) {
-                        const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + c));
+                    if (t < n) {
+                        const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(xg_p + (size_t)t * H + c));
                         acc[t] = dot8_bf16(w0, w1, xv, acc[t]);
                     }
                 }
@@ -103,49 +125,72 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
         }
 #pragma unroll
         for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
-            if (t < a.n) {
+            if (t < n) {
                 float z = warp_sum(acc[t]);
-                if (a.router_bias) z += __ldg(a.router_bias + e);
-                if (lane == 0) {
+                if (bias_p) z += __ldg(bias_p + e);
+                if (sel_logits) {  // every CTA of the cluster gets every logit (lane c -> CTA c)
+                    if (lane < (int)gridDim.x) {
+                        if (gridDim.x > 1) st_cluster_f32(&s_z[t][e], (uint32_t)lane, z);
+                        else s_z[t][e] = z;
+                    }
+                } else if (lane == 0) {
                     if (gridDim.x > 1) st_cluster_f32(&s_z[t][e], 0, z);
                     else s_z[t][e] = z;
-                    if (a.o_logits) a.o_logits[t * a.E + e] = z;
                 }
+                if (lane == 0 && ologits_p) ologits_p[t * E + e] = z;
             }
         }
     }
-    if (gridDim.x > 1) {
-        cluster_sync();
-        if (cluster_ctarank() != 0) return;
-    } else {
-        __syncthreads();
-    }
+    if (gridDim.x > 1) cluster_sync();
+    else __syncthreads();
 
-    // ---- CTA 0: top-k of every token, then counts and the distinct-expert table
-    const int nk = a.n * a.k;
-    for (int i = threadIdx.x; i < a.E; i += blockDim.x) s_counts[i] = 0;
-    cta_topk_ranks(s_z, a.n, a.E, a.k, s_ids, s_w);
-    __syncthreads();
-    if (warp < a.n) {
-        warp_renorm(s_w[warp], a.k);
-        for (int i = lane; i < a.k; i += 32) {
-            a.ids[warp * a.k + i] = s_ids[warp][i];
-            a.wts[warp * a.k + i] = s_w[warp][i];
-            if (a.o_ids) a.o_ids[warp * a.k + i] = s_ids[warp][i];
-            if (a.o_w) a.o_w[warp * a.k + i] = s_w[warp][i];
-        }
-    }
-    __syncthreads();
-    if (a.no_table) {  // one token: counts are 0/1 membership of the k distinct ids
-        for (int ex = threadIdx.x; ex < a.E; ex += blockDim.x) {
+    // ---- one token feeding the cluster expert kernel: every warp ranks its own
+    // expert against all E logits (the number of logits that beat it: greater,
+    // or equal with a lower index -- descending order, ties to the lower index)
+    // and, if selected, stores it at its rank with its logit.
+    if (sel_logits) {
+        if (e < E) {
+            const float ze = s_z[0][e];
             int c = 0;
-            for (int i = 0; i < a.k; ++i) c += (s_ids[0][i] == ex);
-            a.counts[ex] = c;
-            if (a.o_counts) a.o_counts[ex] = c;
+#pragma unroll
+            for (int q = 0; q < SI_MAX_EXPERTS / 32; ++q) {
+                const int j = lane + 32 * q;
+                if (j < E) {
+                    const float zj = s_z[0][j];
+                    c += (zj > ze) | ((zj == ze) & (j < e));
+                }
+            }
+            const int r = __reduce_add_sync(0xffffffffu, c);
+            if (lane == 0) {
+                if (r < k) {
+                    ids_p[r] = e;
+                    wts_p[r] = ze;  // the expert kernel turns these into renormalised weights
+                    if (oids_p) oids_p[r] = e;
+                }
+                counts_p[e] = r < k ? 1 : 0;
+                if (ocounts_p) ocounts_p[e] = r < k ? 1 : 0;
+            }
         }
         return;
     }
-    for (int p = threadIdx.x; p < nk; p += blockDim.x) atomicAdd(&s_counts[s_ids[p / a.k][p % a.k]], 1);
+    if (gridDim.x > 1 && cluster_ctarank() != 0) return;
+
+    // ---- CTA 0: top-k of every token, then counts and the distinct-expert table
+    const int nk = n * k;
+    for (int i = threadIdx.x; i < E; i += blockDim.x) s_counts[i] = 0;
+    cta_topk_ranks(s_z, n, E, k, s_ids, s_w);
+    __syncthreads();
+    if (warp < n) {
+        warp_renorm(s_w[warp], k);
+        for (int i = lane; i < k; i += 32) {
+            ids_p[warp * k + i] = s_ids[warp][i];
+            wts_p[warp * k + i] = s_w[warp][i];
+            if (oids_p) oids_p[warp * k + i] = s_ids[warp][i];
+            if (ow_p) ow_p[warp * k + i] = s_w[warp][i];
+        }
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < nk; p += blockDim.x) atomicAdd(&s_counts[s_ids[p / k][p % k]], 1);
     __syncthreads();
     if (warp == 0) {
         // exclusive scan of "selected" flags over the E experts (8 per lane)
@@ -153,7 +198,7 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const int ex = 8 * lane + q;
-            flag[q] = (ex < a.E && s_counts[ex] > 0) ? 1 : 0;
+            flag[q] = (ex < E && s_counts[ex] > 0) ? 1 : 0;
             run += flag[q];
         }
         int incl = run;
@@ -166,27 +211,27 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const int ex = 8 * lane + q;
-            if (ex < a.E) s_pos[ex] = pos;
+            if (ex < E) s_pos[ex] = pos;
             pos += flag[q];
         }
         if (lane == 31) s_U = incl;
     }
     __syncthreads();
     UniqTable *u = a.uniq;
-    for (int ex = threadIdx.x; ex < a.E; ex += blockDim.x) {
+    for (int ex = threadIdx.x; ex < E; ex += blockDim.x) {
         const int c = s_counts[ex];
         if (c > 0) {
             u->expert[s_pos[ex]] = ex;
             u->ntok[s_pos[ex]] = c;
         }
-        a.counts[ex] = c;
-        if (a.o_counts) a.o_counts[ex] = c;
+        counts_p[ex] = c;
+        if (ocounts_p) ocounts_p[ex] = c;
     }
     for (int p = threadIdx.x; p < nk; p += blockDim.x) {
-        const int t = p / a.k, i = p - t * a.k;
+        const int t = p / k, i = p - t * k;
         const int ex = s_ids[t][i];
         int j = 0;  // rank among the pairs that chose ex (pair-id order)
-        for (int q = 0; q < p; ++q) j += (s_ids[q / a.k][q % a.k] == ex);
+        for (int q = 0; q < p; ++q) j += (s_ids[q / k][q % k] == ex);
         u->tok[s_pos[ex]][j] = t;
         u->slot[s_pos[ex]][j] = i;
     }
@@ -406,7 +451,7 @@ cudaError_t launch_decode(const Plan &p, const DecodeArgs &a_in, cudaStream_t s,
     const bool cluster =
         a.n == 1 && p.cluster_ok && expert_cluster_layout(p.desc, p.cluster_size, p.smem_optin, a);
     a.zero_out = cluster ? 1 : 0;
-    a.no_table = cluster ? 1 : 0;
+    a.sel_logits = cluster ? 1 : 0;
     cudaError_t err = mark(events, 0, s);
     if (err != cudaSuccess) return err;
     err = launch_router(a, s);

@@ -208,6 +208,26 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// A value passed through a register move the compiler may neither move nor
+// re-derive: pins a kernel-parameter read to this point of the program.  A
+// graph launch's parameter buffer is not in the constant caches when the
+// kernel starts, so parameters needed after the dependency wait are read
+// before it, where the miss overlaps the wait.
+__device__ __forceinline__ uint64_t pin_u64(uint64_t v) {
+    uint64_t r;
+    asm volatile("mov.b64 %0, %1;" : "=l"(r) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ int pin_i32(int v) {
+    int r;
+    asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+    return r;
+}
+template <typename T>
+__device__ __forceinline__ T *pin_ptr(T *p) {
+    return reinterpret_cast<T *>(pin_u64(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -225,6 +245,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
         if (clock64() - t0 > budget) return false;
         __nanosleep(20);
     }
+}
+
+// The same wait for a whole warp with one polling lane: lane 0 spins, and
+// once it has seen the phase complete every lane takes one try_wait of its
+// own (which then succeeds at once) for the acquire of the copied bytes.
+// Polling from one lane keeps the barrier word free for the producer's and
+// the copy engine's updates.  Warp-uniform result.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, long long budget) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, budget);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) ok = mbar_wait_bounded(bar, parity, budget);
+    return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {

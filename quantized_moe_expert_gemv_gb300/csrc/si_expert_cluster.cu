@@ -19,8 +19,13 @@
 //     one partial per (slot, block column)).
 // The router kernel zeroes the output first.  Weight bytes: gate/up rows by
 // 1-D bulk copies; down blocks, 144-byte pieces with a 432-byte row stride,
-// by a 2-D tensor map (box = 144 bytes x BR rows).  All copies are issued
-// by one producer thread as soon as the routing is known (L2 evict-first).
+// by 2-D tensor maps (boxes of 144 bytes x 128 rows, one mbarrier per box, so
+// the down phase starts on the first box while the later ones land; the last
+// box of a CTA uses a second map whose box height is the remainder).  The
+// barriers' transaction counts are posted before the dependency wait, and one
+// producer thread issues every copy as soon as the expert id is known (L2
+// evict-first).  The kernel lets the next kernel of the stream launch at once:
+// that kernel's own dependency wait still covers all of this kernel's work.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -37,6 +42,7 @@ constexpr int kClThreads = (kCW + 1) * 32;  // + one producer warp
 constexpr int kPairs = 2;                   // gate/up row pairs per warp per stage
 constexpr long long kDrain = 4000000000LL;
 constexpr int kMaxDownLanes = 8;            // row groups per warp in the down phase: RPC <= 8*kCW*8
+constexpr int kBoxRows = 8 * kCW;           // down rows per tensor box = rows of one down iteration
 
 __device__ __forceinline__ uint4 ld_s128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
@@ -72,7 +78,8 @@ __device__ __forceinline__ float pair_sum(float g, float u, int li) {
 
 template <int NBH>
 __global__ void __launch_bounds__(kClThreads, 1)
-    k_expert_cluster(const __grid_constant__ CUtensorMap tmap_down, DecodeArgs a) {
+    k_expert_cluster(const __grid_constant__ CUtensorMap tmap_down, const __grid_constant__ CUtensorMap tmap_tail,
+                     DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t sm[];
     constexpr int GS = 4 * NBH;
     constexpr int RPW = 32 / GS;
@@ -84,48 +91,69 @@ __global__ void __launch_bounds__(kClThreads, 1)
     __shared__ float s_w;
     __shared__ int s_lastA[8];
     __shared__ int s_lastB;
+    pdl_launch_dependents();  // the next kernel's dependency wait still covers this whole grid
+
+    // parameters used after the dependency wait, read now
+    const uint8_t *const wg = pin_ptr(a.wg), *const wu = pin_ptr(a.wu);
+    const int32_t *const ids = pin_ptr(a.ids);
+    const float *const zsel = pin_ptr(a.wts);  // the selected logits in rank order (see below)
+    float *const o_w = pin_ptr(a.o_w);
+    const int k = pin_i32(a.k);
+    float *const out_g = pin_ptr(a.out);
+    int32_t *const ctrl = pin_ptr(a.ctrl);
+    const long long budget = (long long)pin_u64((uint64_t)a.wait_budget);
+    const int fault_wait = pin_i32(a.fault_wait);
+    const int I = pin_i32(a.I), H = pin_i32(a.H);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = (int)cluster_nctarank();
     const int rank = (int)cluster_ctarank();
-    const int nbI = a.I / kQK;
+    const int nbI = I / kQK;
     const int unit = blockIdx.x / C;
     const int slot = unit / nbI, bcol = unit - slot * nbI;
     const int r_lo = kQK * bcol + (kQK * rank) / C;
     const int n_rp = kQK * bcol + (kQK * (rank + 1)) / C - r_lo;
-    const int c_lo = (a.H * rank) / C;
-    const int n_rows = (a.H * (rank + 1)) / C - c_lo;
+    const int c_lo = (H * rank) / C;
+    const int n_rows = (H * (rank + 1)) / C - c_lo;
     const int nA = (n_rp + CH - 1) / CH;
-    const int NSA = a.cl_nsa;
-    const int BR = a.cl_box_rows, box_stride = a.cl_box_stride, nbox = a.cl_nbox;
+    const int NSA = pin_i32(a.cl_nsa);
+    const int box_stride = pin_i32(a.cl_box_stride), nbox = pin_i32(a.cl_nbox), tail_rows = pin_i32(a.cl_tail_rows);
 
-    uint8_t *stA = sm + a.cl_off_a;
-    uint8_t *stB = sm + a.cl_off_b;
-    float *hslice = reinterpret_cast<float *>(sm + a.cl_off_h);  // [256] h of the unit
-    float *ybuf = reinterpret_cast<float *>(sm + a.cl_off_y);    // [rows] down partials
-    const uint32_t fullA = smem_addr(sm + a.cl_off_bar);
+    uint8_t *stA = sm + pin_i32(a.cl_off_a);
+    uint8_t *stB = sm + pin_i32(a.cl_off_b);
+    float *hslice = reinterpret_cast<float *>(sm + pin_i32(a.cl_off_h));  // [256] h of the unit
+    float *ybuf = reinterpret_cast<float *>(sm + pin_i32(a.cl_off_y));    // [rows] down partials
+    uint32_t *const xq_s = reinterpret_cast<uint32_t *>(sm + pin_i32(a.cl_off_x));  // quantised x, later h
+    const uint32_t fullA = smem_addr(sm + pin_i32(a.cl_off_bar));
     const uint32_t emptyA = fullA + 8 * NSA;
-    const uint32_t fullB = emptyA + 8 * NSA;
-    int32_t *status = a.ctrl + kCtrlStatus;
+    const uint32_t fullB = emptyA + 8 * NSA;  // [nbox]
+    int32_t *status = ctrl + kCtrlStatus;
+    auto stage_bytes = [&](int j) { return (uint32_t)((min(CH * (j + 1), n_rp) - CH * j) * rowg); };
+    auto box_bytes = [&](int bx) { return (uint32_t)((bx == nbox - 1 ? tail_rows : kBoxRows) * kBlockBytes); };
 
     if (threadIdx.x == 0) {
-        prefetch_tensormap(&tmap_down);  // descriptor fetch off the critical path
+        prefetch_tensormap(&tmap_down);  // descriptor fetches off the critical path
+        prefetch_tensormap(&tmap_tail);
         for (int st = 0; st < NSA; ++st) {
             mbar_init(fullA + 8 * st, 1);
             mbar_init(emptyA + 8 * st, kCW);
             s_lastA[st] = -1;
         }
-        mbar_init(fullB, 1);
+        for (int bx = 0; bx < nbox; ++bx) mbar_init(fullB + 8 * bx, 1);
         s_lastB = -1;
         s_err = 0;
         fence_mbar_init();
+        // the byte counts of the first ring pass and of every down box do not
+        // depend on the routing: post them now (the producer's arrival)
+        for (int j = 0; j < min(nA, NSA); ++j) mbar_arrive_expect_tx(fullA + 8 * j, 2 * stage_bytes(j));
+        for (int bx = 0; bx < nbox; ++bx) mbar_arrive_expect_tx(fullB + 8 * bx, box_bytes(bx));
     }
     // The token's H/64 activation chunks, quantised once (warp 0) into shared memory
     // before the dependency wait: the router launches this kernel only after its
     // own wait on the producers of x, so x is final here.
-    if (warp == 0 && lane < a.H / 64) {
-        uint32_t *xq = reinterpret_cast<uint32_t *>(sm + a.cl_off_x);  // [H/64][32] words
-        float *xqf = reinterpret_cast<float *>(xq + a.H / 2);          // [H/64][3]: scale, Xa, Xb
+    if (warp == 0 && lane < H / 64) {
+        uint32_t *xq = xq_s;                                   // [H/64][32] words
+        float *xqf = reinterpret_cast<float *>(xq + H / 2);   // [H/64][3]: scale, Xa, Xb
         float xf[64];
         uint32_t wq[32];
         float sa, sb;
@@ -150,10 +178,24 @@ __global__ void __launch_bounds__(kClThreads, 1)
     }
     __syncthreads();
     pdl_wait();  // routing of this token is complete
-    if (threadIdx.x == 0) {
-        s_slot = slot;
-        s_expert = a.ids[slot];
-        s_w = a.wts[slot];
+    // The router left the k selected experts in rank order with their logits;
+    // the renormalised weight of rank r is exp(z_r - z_0) / sum_j exp(z_j - z_0)
+    // (z_0 is the largest).  Warp 0 forms all k; CTA 0 reports them.
+    if (warp == 0) {
+        const int id = lane < k ? ids[lane] : 0;
+        const float zr = lane < k ? zsel[lane] : 0.f;
+        const float z0 = __shfl_sync(0xffffffffu, zr, 0);
+        const float ex = lane < k ? expf(zr - z0) : 0.f;
+        float den = ex;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        const float w = ex / den;
+        if (lane == slot) {
+            s_slot = slot;
+            s_expert = id;
+            s_w = w;
+        }
+        if (blockIdx.x == 0 && o_w && lane < k) o_w[lane] = w;
     }
     __syncthreads();
     const int e = s_expert;
@@ -165,35 +207,35 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const uint64_t pol = l2_evict_first_policy();
             auto issueA = [&](int j) -> bool {
                 const int st = j % NSA;
+                const uint32_t bytes = stage_bytes(j);
                 if (j >= NSA) {
                     const uint32_t par = ((j / NSA) - 1) & 1;
                     const long long t0 = clock64();
                     while (!mbar_try_wait(emptyA + 8 * st, par)) {
-                        if (*verr || clock64() - t0 > a.wait_budget) {
+                        if (*verr || clock64() - t0 > budget) {
                             if (!*verr) set_status(status, SI_ERR_TIMEOUT);
                             *verr = 1;
                             return false;
                         }
                         __nanosleep(20);
                     }
+                    mbar_arrive_expect_tx(fullA + 8 * st, 2 * bytes);  // later passes: posted here
                 }
-                const int q0 = CH * j, q1 = min(q0 + CH, n_rp);
-                const uint32_t bytes = (uint32_t)((q1 - q0) * rowg);
-                mbar_arrive_expect_tx(fullA + 8 * st, 2 * bytes);
-                const size_t src = ((size_t)e * a.I + r_lo + q0) * rowg;
+                const int q0 = CH * j;
+                const size_t src = ((size_t)e * I + r_lo + q0) * rowg;
                 const uint32_t dst = smem_addr(stA + (size_t)st * stageA);
-                bulk_g2s(dst, a.wg + src, bytes, fullA + 8 * st, pol);
-                bulk_g2s(dst + CH * rowg, a.wu + src, bytes, fullA + 8 * st, pol);
+                bulk_g2s(dst, wg + src, bytes, fullA + 8 * st, pol);
+                bulk_g2s(dst + CH * rowg, wu + src, bytes, fullA + 8 * st, pol);
                 s_lastA[st] = (j / NSA) & 1;
                 return true;
             };
             const int first = min(nA, NSA);
             for (int j = 0; j < first; ++j) issueA(j);
-            // down blocks of this CTA's rows: nbox tensor boxes of BR rows x 144 bytes
-            mbar_arrive_expect_tx(fullB, (uint32_t)(nbox * BR * kBlockBytes));
+            // down blocks of this CTA's rows: boxes of 128 rows x 144 bytes, the last one
+            // tail_rows high (its own map); each box completes its own barrier
             for (int bx = 0; bx < nbox; ++bx)
-                tma_load_2d(smem_addr(stB + (size_t)bx * box_stride), &tmap_down, kBlockBytes * bcol,
-                            e * a.H + c_lo + bx * BR, fullB, pol);
+                tma_load_2d(smem_addr(stB + (size_t)bx * box_stride), bx == nbox - 1 ? &tmap_tail : &tmap_down,
+                            kBlockBytes * bcol, e * H + c_lo + bx * kBoxRows, fullB + 8 * bx, pol);
             s_lastB = 0;
             for (int j = first; j < nA; ++j)
                 if (!issueA(j)) break;
@@ -205,8 +247,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
     if (warp < kCW) {
         const int g = lane / GS, li = lane % GS, b = li >> 2, i = li & 3;
         const int chunk = 4 * b + i;
-        const uint32_t *xq = reinterpret_cast<const uint32_t *>(sm + a.cl_off_x);  // quantised in the prologue
-        const float *xqf = reinterpret_cast<const float *>(xq + a.H / 2);
+        const uint32_t *xq = xq_s;  // quantised in the prologue
+        const float *xqf = reinterpret_cast<const float *>(xq + H / 2);
         uint32_t xw[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -215,8 +257,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
         const float xs = xqf[3 * chunk], Xa = xqf[3 * chunk + 1], Xb = xqf[3 * chunk + 2];
         auto xwf = [&xw](int p) { return xw[p]; };
-        if (a.fault_wait) {
-            const bool got = wait_flag_bounded(a.ctrl + kCtrlFaultFlag, a.wait_budget);
+        if (fault_wait) {
+            const bool got = wait_flag_bounded(ctrl + kCtrlFaultFlag, budget);
             if (!__all_sync(0xffffffffu, got)) {
                 set_status(status, SI_ERR_TIMEOUT);
                 *verr = 1;
@@ -224,8 +266,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
         for (int j = 0; j < nA && !__any_sync(0xffffffffu, *verr != 0); ++j) {
             const int st = j % NSA;
-            const bool landed = mbar_wait_bounded(fullA + 8 * st, (j / NSA) & 1, a.wait_budget);
-            if (!__all_sync(0xffffffffu, landed)) {
+            if (!mbar_wait_warp(fullA + 8 * st, (j / NSA) & 1, budget)) {
                 set_status(status, SI_ERR_TIMEOUT);
                 *verr = 1;
                 break;
@@ -265,7 +306,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
 
     // --------------------------------------------------------- down + combine
     const bool skip = __any_sync(0xffffffffu, *verr != 0);
-    uint32_t *hq = reinterpret_cast<uint32_t *>(sm + a.cl_off_x);  // reuse: [4][32] words + [4][3]
+    uint32_t *hq = xq_s;  // reuse: [4][32] words + [4][3]
     float *hqf = reinterpret_cast<float *>(hq + 128);
     if (warp < kCW && !skip) {
         if (warp < 4) {  // the unit's four 64-column chunks of h: warp c quantises chunk c
@@ -296,38 +337,37 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
         const float hs = hqf[3 * i], Ha = hqf[3 * i + 1], Hb = hqf[3 * i + 2];
         auto hwf = [&hw](int p) { return hw[p]; };
-        const bool landed = mbar_wait_bounded(fullB, 0, a.wait_budget);
-        if (!__all_sync(0xffffffffu, landed)) {
-            set_status(status, SI_ERR_TIMEOUT);
-            *verr = 1;
-        } else {
+        // box m holds rows [128m, 128m + 128) = the rows of iteration m; every warp
+        // waits for every box (so none is left in flight), rows past n_rows are skipped
 #pragma unroll 1
-            for (int m = 0; m < kMaxDownLanes; ++m) {
-                const int lr0 = 8 * kCW * m + 8 * warp;  // first row of this warp's 8-row group
-                if (lr0 >= n_rows) break;           // uniform across the warp
-                const int lr = lr0 + r8;
-                float v = 0.f;
-                if (lr < n_rows) {
-                    const int bx = lr / BR;
-                    const uint8_t *blk = stB + (size_t)bx * box_stride + (size_t)(lr - bx * BR) * kBlockBytes;
-                    const uint4 hd = ld_s128(blk), q0 = ld_s128(blk + 16 + 32 * i), q1 = ld_s128(blk + 32 + 32 * i);
-                    v = chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums(q0, q1, hwf), hs, Ha, Hb);
-                }
-                v += __shfl_xor_sync(0xffffffffu, v, 1);
-                v += __shfl_xor_sync(0xffffffffu, v, 2);
-                if (i == 0 && lr < n_rows) ybuf[lr] = v;
+        for (int m = 0; m < nbox; ++m) {
+            if (!mbar_wait_warp(fullB + 8 * m, 0, budget)) {
+                set_status(status, SI_ERR_TIMEOUT);
+                *verr = 1;
+                break;
             }
+            const int lr = kBoxRows * m + 8 * warp + r8;
+            float v = 0.f;
+            if (lr < n_rows) {
+                const uint8_t *blk = stB + (size_t)m * box_stride + (size_t)(8 * warp + r8) * kBlockBytes;
+                const uint4 hd = ld_s128(blk), q0 = ld_s128(blk + 16 + 32 * i), q1 = ld_s128(blk + 32 + 32 * i);
+                v = chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums(q0, q1, hwf), hs, Ha, Hb);
+            }
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            if (i == 0 && lr < n_rows) ybuf[lr] = v;
         }
     }
     __syncthreads();
     if (!*verr) {
         const float w = s_w;
-        float *out = a.out + c_lo;
+        float *out = out_g + c_lo;
         for (int lr = threadIdx.x; lr < n_rows; lr += blockDim.x) red_add_f32(out + lr, w * ybuf[lr]);
-    } else if (threadIdx.x == 0) {
+    } else if (threadIdx.x == 0) {  // no copy may still be writing this CTA's shared memory at exit
         for (int st = 0; st < NSA; ++st)
             if (s_lastA[st] >= 0) mbar_wait_bounded(fullA + 8 * st, s_lastA[st], kDrain);
-        if (s_lastB >= 0) mbar_wait_bounded(fullB, 0, kDrain);
+        if (s_lastB >= 0)
+            for (int bx = 0; bx < nbox; ++bx) mbar_wait_bounded(fullB + 8 * bx, 0, kDrain);
     }
 }
 
@@ -359,17 +399,17 @@ bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs
     const int rp_max = (kQK + C - 1) / C;
     const int nA_max = (rp_max + CH - 1) / CH;
     const int rpc = (d.hidden + C - 1) / C;  // down rows per CTA (max)
-    if (rpc > 8 * kCW * kMaxDownLanes) return false;
-    const int nbox = (rpc + 255) / 256;
-    const int BR = (rpc + nbox - 1) / nbox;
-    const int box_stride = (BR * kBlockBytes + 127) / 128 * 128;
+    if (rpc > kBoxRows * kMaxDownLanes) return false;
+    const int nbox = (rpc + kBoxRows - 1) / kBoxRows;
+    const int tail = rpc - (nbox - 1) * kBoxRows;  // 1..128 rows in the last box
+    const int box_stride = kBoxRows * kBlockBytes;  // 18432 = 144 * 128
     auto al = [](int v) { return (v + 127) / 128 * 128; };
     int NSA = nA_max < 3 ? nA_max : 3;
     int off = 0;
     a.cl_off_a = off;
     off += NSA * stageA;
     a.cl_off_b = off;
-    off += nbox * box_stride;
+    off += (nbox - 1) * box_stride + al(tail * kBlockBytes);
     a.cl_off_h = off;
     off += al(kQK * 4);
     a.cl_off_x = off;  // quantised x: [H/64][32] words + [H/64][3] floats (later: quantised h)
@@ -377,24 +417,26 @@ bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs
     a.cl_off_y = off;
     off += al(rpc * 4);
     a.cl_off_bar = off;
-    off += 8 * (2 * NSA + 1) + 64;
+    off += 8 * (2 * NSA + nbox) + 64;
     if (off + 1024 > smem_max) return false;  // + static shared memory
     a.cl_nsa = NSA;
     a.cl_C = C;
-    a.cl_box_rows = BR;
+    a.cl_tail_rows = tail;
     a.cl_nbox = nbox;
     a.cl_box_stride = box_stride;
     a.cl_smem = off;
     return true;
 }
 
-static bool make_down_tensor_map(const DecodeArgs &a, CUtensorMap *tm) {
+// Down rows of all experts as a 2-D byte tensor [E*H rows][I/256*144 bytes];
+// a box is one 144-byte block column of `rows` consecutive rows.
+static bool make_down_tensor_map(const DecodeArgs &a, int rows, CUtensorMap *tm) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const int nbi = a.I / kQK;
     cuuint64_t dims[2] = {(cuuint64_t)nbi * kBlockBytes, (cuuint64_t)a.E * a.H};
     cuuint64_t strides[1] = {(cuuint64_t)nbi * kBlockBytes};
-    cuuint32_t box[2] = {(cuuint32_t)kBlockBytes, (cuuint32_t)a.cl_box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)kBlockBytes, (cuuint32_t)rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.wd), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -402,7 +444,8 @@ static bool make_down_tensor_map(const DecodeArgs &a, CUtensorMap *tm) {
 }
 
 template <int NBH>
-static cudaError_t launch_cluster_t(const DecodeArgs &a, const CUtensorMap &tm, cudaStream_t s) {
+static cudaError_t launch_cluster_t(const DecodeArgs &a, const CUtensorMap &tm, const CUtensorMap &tt,
+                                    cudaStream_t s) {
     const int units = a.k * (a.I / kQK);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(units * a.cl_C);
@@ -418,17 +461,18 @@ static cudaError_t launch_cluster_t(const DecodeArgs &a, const CUtensorMap &tm, 
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH>, tm, a);
+    return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH>, tm, tt, a);
 }
 
 cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s) {
-    CUtensorMap tm;
-    if (!make_down_tensor_map(a, &tm)) return cudaErrorInvalidValue;
+    CUtensorMap tm, tt;
+    if (!make_down_tensor_map(a, kBoxRows, &tm) || !make_down_tensor_map(a, a.cl_tail_rows, &tt))
+        return cudaErrorInvalidValue;
     switch (a.H / kQK) {
-        case 1: return launch_cluster_t<1>(a, tm, s);
-        case 2: return launch_cluster_t<2>(a, tm, s);
-        case 4: return launch_cluster_t<4>(a, tm, s);
-        default: return launch_cluster_t<8>(a, tm, s);
+        case 1: return launch_cluster_t<1>(a, tm, tt, s);
+        case 2: return launch_cluster_t<2>(a, tm, tt, s);
+        case 4: return launch_cluster_t<4>(a, tm, tt, s);
+        default: return launch_cluster_t<8>(a, tm, tt, s);
     }
 }
 

@@ -75,9 +75,10 @@ struct DecodeArgs {
     int fz_nsa, fz_nsb, fz_rb, fz_stage_b, fz_smem;
     // shared-memory plan of the cluster expert kernel (set by expert_cluster_layout)
     int cl_off_a, cl_off_b, cl_off_h, cl_off_x, cl_off_y, cl_off_bar;
-    int cl_nsa, cl_C, cl_box_rows, cl_nbox, cl_box_stride, cl_smem;
+    int cl_nsa, cl_C, cl_tail_rows, cl_nbox, cl_box_stride, cl_smem;
     int zero_out;  // router zeroes out[n][H] (the expert kernel accumulates into it)
-    int no_table;  // router skips the distinct-expert table (single-token cluster path)
+    int sel_logits;  // single token, cluster expert kernel: the router writes ids in rank order, the
+                     // selected logits (not weights) and 0/1 counts; the expert kernel forms the weights
 };
 
 cudaError_t launch_decode(const Plan &p, const DecodeArgs &a, cudaStream_t s,

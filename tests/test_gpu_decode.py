@@ -143,6 +143,47 @@ def test_debug_topk_bit_exact(E, k):
 
 
 # ------------------------------------------------------------ decode paths
+@pytest.mark.parametrize("H,I,E,k", [(2048, 768, 128, 8), (256, 256, 8, 2), (2048, 768, 256, 16)])
+def test_decode_single_token_router_ties_and_zero_rows(H, I, E, k):
+    """Single-token routing with exact ties: identical router rows give
+    bit-identical logits, and zero rows (of +0.0 or -0.0 weights) give zero
+    logits; every tie goes to the lower expert index."""
+    shape = synth.MoeShape(H, I, E, k)
+    layer = synth.make_layer(shape, seed=41)
+    g = np.random.default_rng(41)
+    v = np.abs(g.normal(0, 0.02, H)).astype(np.float32)
+    w_r = np.zeros((E, H), dtype=np.float32)
+    w_r[: E // 8] = -0.0                      # the lowest rows are negative zeros
+    top = [E - 1, E // 2, E // 4 + 1]         # three identical rows (in descending-id order)
+    for e in top:
+        w_r[e] = v
+    if k > 3:
+        w_r[E // 3] = 0.5 * v
+        w_r[E - 2] = 0.5 * v
+    layer.router_w = w_r
+    layer.router_bias = None
+    x = np.abs(synth.bf16_to_f32(synth.make_tokens(shape, seed=41, n_tokens=3))).astype(np.float32)
+    x_bits = synth.bf16_bits(x)
+    r = Runner(layer)
+    for t in range(3):
+        out, ids, w, counts, logits = r.decode(x_bits[t:t + 1])
+        z = logits[0]
+        assert z[0] == 0.0 and z[E // 8] == 0.0
+        ref = oracle.topk(z, k)
+        assert np.array_equal(ids[0], ref), (ids[0], ref)
+        assert list(ids[0][:min(3, k)]) == sorted(top)[:min(3, k)]
+        if k > 3:
+            assert list(ids[0][3:5]) == sorted([E // 3, E - 2])
+            assert list(ids[0][5:]) == list(range(k - 5)), "zero logits: lowest ids first"
+        np.testing.assert_allclose(w[0], oracle.renorm_weights(z.astype(np.float64), ref), rtol=0, atol=2e-6)
+        want = np.zeros(E, dtype=np.int32)
+        want[ref] = 1
+        assert np.array_equal(counts, want)
+        o_ids, _, _, _ = oracle.route_tokens(layer.router_w, x_bits[t:t + 1], k, want_logits=True)
+        assert np.array_equal(ids[0], o_ids[0])
+        parity.assert_close(out[0], oracle.moe_token(layer, x_bits[t]).out64, f"token {t}")
+
+
 def test_decode_tiny_layer_seed0():
     wl = synth.WORKLOADS["tiny"]
     layer = synth.make_layer(wl["shape"], seed=wl["seed"])
