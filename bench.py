@@ -464,6 +464,84 @@ def bench_dedup4(args, dist, binding, device, synth, torch, hbm_peak):
             "gpu_launches": (2 if binding.si_debug_decode_fused(plan, n) >= 1 else 3) * S * steps}
 
 
+def tensor_peak():
+    """Dense 16-bit tensor-core peak (TFLOP/s): the measured bf16 GEMM figure
+    (fp16 has the same dense rate on this part)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            "measured (MEASURED_PEAKS.json bf16_tflops burst / bf16_tflops_sustained)"
+    return 1900.0, 1700.0, "fallback (1.9 PFLOP/s burst, 1.7 sustained)"
+
+
+def bench_prefill(args, dist, binding, device, synth, torch):
+    """Grouped prefill of 4096 tokens through one layer of the Qwen3-30B-A3B
+    shape: routing + two tensor-core GEMMs + combine, per call."""
+    wl = synth.WORKLOADS["prefill"]
+    shape, seed, T = wl["shape"], wl["seed"], wl["n_tokens"]
+    layer = synth.make_layer(shape, seed=seed)
+    dl = device.to_device(layer)
+    plan = binding.si_moe_plan(device.desc_for(shape, max_tokens=T), torch.cuda.current_device())
+    scratch = device.alloc_scratch(plan, binding.SI_MODE_PREFILL, T)
+    x = device.tokens_to_device(synth.make_tokens(shape, seed, T))
+    out = torch.empty((T, shape.hidden), dtype=torch.float32, device="cuda")
+    L = dl.struct()
+    stream = torch.cuda.Stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    with torch.cuda.stream(stream):
+        for e in ev:  # torch creates the CUDA event on its first record
+            e.record(stream)
+        for _ in range(max(3, args.warmup)):
+            binding.si_moe_forward_prefill(plan, L, x, T, out, None, scratch, stream=stream)
+    stream.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        binding.si_moe_forward_prefill(plan, L, x, T, out, None, scratch, stream=stream)
+    stream.synchronize()
+    one = time.perf_counter() - t0
+    reps = int(min(2000, max(10, 0.6 / max(one, 1e-5))))  # ~0.6 s timed, so the clock sampler sees it
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        binding.si_moe_forward_prefill(plan, L, x, T, out, None, scratch, stream=stream)
+    e1.record(stream)
+    e1.synchronize()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / reps
+    parts = [0.0] * 4
+    nev = min(reps, 20)
+    for _ in range(nev):
+        binding.si_debug_prefill_events(plan, L, x, T, out, None, scratch, events=ev, stream=stream)
+        ev[4].synchronize()
+        for i in range(4):
+            parts[i] += ev[i].elapsed_time(ev[i + 1]) / nev
+    assert binding.si_moe_read_status(plan, scratch, stream) == binding.SI_OK
+    pairs = T * shape.top_k
+    f_gateup = 2.0 * pairs * 2 * shape.intermediate * shape.hidden
+    f_down = 2.0 * pairs * shape.hidden * shape.intermediate
+    burst, sustained, src = tensor_peak()
+    gemm_ms = parts[1] + parts[2]
+    tflops = (f_gateup + f_down) / (gemm_ms * 1e-3) / 1e12
+    tok_s = T / (ms * 1e-3)
+    del scratch
+    return {"workload": "grouped prefill, 4096 tokens x top-8 of 128 experts, one Qwen3-30B-A3B layer, seed 4",
+            "tok_per_s": dist.sum(tok_s), "ms_per_call": ms,
+            "kernels_ms": {"routing_counts_perm": parts[0], "gemm_gateup_swiglu": parts[1],
+                           "gemm_down_weight": parts[2], "combine": parts[3]},
+            "gemm_flop": f_gateup + f_down,
+            "roofline": {"bound": "tensor", "kernel": "k_prefill_gemm<0> + k_prefill_gemm<1> (fp16 operands, "
+                                                      "fp32 accumulation in tensor memory)",
+                         "achieved": tflops, "peak": burst, "unit": "TFLOP/s", "frac": tflops / burst,
+                         "frac_of_sustained": tflops / sustained, "peak_source": src,
+                         "gateup_tflops": f_gateup / (parts[1] * 1e-3) / 1e12,
+                         "down_tflops": f_down / (parts[2] * 1e-3) / 1e12},
+            "calls_timed": reps, "clocks": clocks, "gpu_launches": 6 * reps}
+
+
 def run_ours(args, dist):
     import torch
     from quantized_moe_expert_gemv_gb300 import binding, build, device, synth
@@ -490,6 +568,11 @@ def run_ours(args, dist):
             line["dedup4"] = bench_dedup4(args, dist, binding, device, synth, torch, hbm_peak)
         except Exception as exc:
             line["dedup4"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+        try:
+            line["prefill"] = bench_prefill(args, dist, binding, device, synth, torch)
+        except Exception as exc:
+            line["prefill"] = {"error": repr(exc)}
     if dist.rank == 0 and not args.no_cpu_baseline:
         cores = cpu_cores()
         n = args.cpu_sample_tokens or max(64, 16 * cores)

@@ -65,7 +65,8 @@ typedef enum si_status {
     SI_ERR_SCRATCH_TOO_SMALL = 4, /* scratch_bytes below si_moe_scratch_bytes() */
     SI_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */
     SI_ERR_TIMEOUT = 6,           /* a bounded device-side wait ran out */
-    SI_ERR_DEVICE = 7             /* another device-side check failed */
+    SI_ERR_DEVICE = 7,            /* another device-side check failed */
+    SI_ERR_RANGE = 8              /* prefill: a value outside the fp16 range of its tensor-core operands */
 } si_status;
 
 #define SI_WTYPE_Q4_K 12          /* GGUF's type id of Q4_K */
@@ -135,11 +136,25 @@ si_status si_moe_forward_decode(si_moe_plan_t plan, const si_moe_layer *layer, c
                                 int32_t n_tokens, float *out, si_moe_route_out *route_out,
                                 void *scratch, size_t scratch_bytes, si_stream_t stream);
 
-/* Grouped prefill: T tokens (1..max_tokens) routed top-k, permuted by
- * expert with on-device counts/offsets, Q4_K tiles dequantized into bf16
- * tensor-core operands (fp32 accumulation), SwiGLU, down GEMM, and the
- * weighted combine back to token order (slot order, deterministic).
- * x_bf16: [T][H] bf16; out: [T][H] fp32. */
+/* Grouped prefill (SP⚡RKINFER README, "Benchmark · Qwen3.6-35B-A3B", prefill
+ * paragraph: Q4_K dequantized into the GEMM operand; sparkinfer-k3 blog post,
+ * "v0.2.2": a chunk of tokens shares one weight-tile read): T tokens
+ * (1..max_tokens) routed top-k (fp32 logits, ties to the lower index,
+ * renormalised softmax), counts per expert, offsets = exclusive scan, perm =
+ * pair ids t*k+slot ordered by expert then pair id; per expert a 16-bit
+ * tensor-core GEMM of the gathered tokens with the gate and up rows (Q4_K
+ * dequantized to fp16, round-to-nearest-even, fp32 accumulation), h =
+ * fp16(silu(g)*u), a second GEMM with the down rows, each row times its
+ * routing weight (fp32), and out[t] = the sum of token t's k rows in slot
+ * order (deterministic).  The tensor-core operands are fp16 (weights and h
+ * rounded to nearest even, x converted exactly): bf16 weights cannot hold
+ * the output tolerance.  An input, weight or h value beyond the fp16 range
+ * is reported as SI_ERR_RANGE by si_moe_read_status.  x_bf16: [T][H] bf16; out: [T][H] fp32 (written).
+ * route_out may return ids/weights [T][k], counts [E], offsets [E+1],
+ * perm [T*k] and logits [T][E].  Needs H, I multiples of 256 (as every call)
+ * and scratch of si_moe_scratch_bytes(plan, SI_MODE_PREFILL, T).  Returns
+ * SI_ERR_UNSUPPORTED on a device without the tensor-memory MMA path.
+ * Stream-ordered, no host synchronisation, no allocation. */
 si_status si_moe_forward_prefill(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
                                  int32_t n_tokens, float *out, si_moe_route_out *route_out,
                                  void *scratch, size_t scratch_bytes, si_stream_t stream);
@@ -207,6 +222,15 @@ si_status si_debug_decode_events(si_moe_plan_t plan, const si_moe_layer *layer, 
                                  int32_t n_tokens, float *out, si_moe_route_out *route_out,
                                  void *scratch, size_t scratch_bytes, void *const *events,
                                  si_stream_t stream);
+
+/* Timing export: si_moe_forward_prefill that also records caller-created
+ * events on `stream` -- events[0] before routing, [1] before the gate/up GEMM,
+ * [2] before the down GEMM, [3] before the combine, [4] after it (any may be
+ * NULL).  Same arguments, errors and results as si_moe_forward_prefill. */
+si_status si_debug_prefill_events(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
+                                  int32_t n_tokens, float *out, si_moe_route_out *route_out,
+                                  void *scratch, size_t scratch_bytes, void *const *events,
+                                  si_stream_t stream);
 
 #ifdef __cplusplus
 }

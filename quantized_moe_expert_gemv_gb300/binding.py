@@ -26,6 +26,7 @@ SI_ERR_SCRATCH_TOO_SMALL = 4
 SI_ERR_CUDA = 5
 SI_ERR_TIMEOUT = 6
 SI_ERR_DEVICE = 7
+SI_ERR_RANGE = 8
 SI_WTYPE_Q4_K = 12
 SI_MODE_DECODE = 0
 SI_MODE_PREFILL = 1
@@ -96,6 +97,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.si_debug_decode_events.argtypes = [vp, ctypes.POINTER(si_moe_layer), vp, i32, vp,
                                            ctypes.POINTER(si_moe_route_out), vp, sz,
                                            ctypes.POINTER(vp), vp]
+    lib.si_debug_prefill_events.argtypes = [vp, ctypes.POINTER(si_moe_layer), vp, i32, vp,
+                                            ctypes.POINTER(si_moe_route_out), vp, sz,
+                                            ctypes.POINTER(vp), vp]
+    lib.si_debug_prefill_events.restype = ctypes.c_int
     lib.si_moe_forward_decode_noalloc.restype = ctypes.c_int
     lib.si_moe_forward_decode_noalloc.argtypes = [vp, ctypes.POINTER(si_moe_layer), vp, i32, vp,
                                                   ctypes.POINTER(si_moe_route_out), vp]
@@ -253,6 +258,19 @@ def si_debug_decode_events(plan, layer: si_moe_layer, x, n_tokens, out, route_ou
     _check(lib.si_debug_decode_events(plan.handle, ctypes.byref(layer), _ptr(x), int(n_tokens), _ptr(out),
                                       ro, _ptr(scratch), nbytes, ev, _stream(stream)),
            "si_debug_decode_events")
+
+
+def si_debug_prefill_events(plan, layer: si_moe_layer, x, n_tokens, out, route_out=None, scratch=None,
+                            events=(None, None, None, None, None), stream=None):
+    """Prefill with torch.cuda.Event objects recorded before routing, before
+    each GEMM, before the combine and after it."""
+    lib = load_library()
+    ev = (ctypes.c_void_p * 5)(*[None if e is None else e.cuda_event for e in events])
+    ro = ctypes.byref(route_out) if route_out is not None else None
+    nbytes = scratch.numel() * scratch.element_size()
+    _check(lib.si_debug_prefill_events(plan.handle, ctypes.byref(layer), _ptr(x), int(n_tokens), _ptr(out),
+                                       ro, _ptr(scratch), nbytes, ev, _stream(stream)),
+           "si_debug_prefill_events")
 
 
 def si_debug_plan_info(plan: Plan) -> dict:

@@ -57,6 +57,30 @@ DecodeLayout decode_layout(const si_moe_desc &d, int n) {
     return L;
 }
 
+PrefillLayout prefill_layout(const si_moe_desc &d, int n) {
+    PrefillLayout L{};
+    size_t o = 0;
+    auto take = [&o](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    const size_t pairs = (size_t)n * d.top_k;
+    L.ctrl = take(kCtrlBytes);
+    L.logits = take((size_t)n * d.n_experts * sizeof(float));
+    L.ids = take(pairs * sizeof(int32_t));
+    L.wts = take(pairs * sizeof(float));
+    L.counts = take((size_t)d.n_experts * sizeof(int32_t));
+    L.offsets = take(((size_t)d.n_experts + 1) * sizeof(int32_t));
+    L.perm = take(pairs * sizeof(int32_t));
+    L.inv = take(pairs * sizeof(int32_t));
+    L.xh = take((size_t)n * d.hidden * sizeof(uint16_t));
+    L.h = take(pairs * d.intermediate * sizeof(uint16_t));
+    L.y = take(pairs * d.hidden * sizeof(float));
+    L.total = o;
+    return L;
+}
+
 }  // namespace si
 
 extern "C" {
@@ -71,6 +95,7 @@ const char *si_status_string(si_status s) {
         case SI_ERR_CUDA: return "CUDA error";
         case SI_ERR_TIMEOUT: return "device-side wait timed out";
         case SI_ERR_DEVICE: return "device-side check failed";
+        case SI_ERR_RANGE: return "value outside the fp16 range of the prefill operands";
     }
     return "unknown status";
 }
@@ -143,6 +168,8 @@ si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *o
             cudaGetLastError();
         }
     }
+    p.prefill_ok = si::prefill_prepare(p) == cudaSuccess;
+    cudaGetLastError();
     if (cur_dev != cuda_device) cudaSetDevice(cur_dev);
     si_moe_plan_s *h = new (std::nothrow) si_moe_plan_s;
     if (!h) return SI_ERR_INVALID_ARG;
@@ -161,7 +188,11 @@ si_status si_moe_scratch_bytes(si_moe_plan_t plan, int mode, int32_t n_tokens, s
         *bytes = si::decode_layout(d, n_tokens).total;
         return SI_OK;
     }
-    if (mode == SI_MODE_PREFILL) return SI_ERR_UNSUPPORTED;
+    if (mode == SI_MODE_PREFILL) {
+        if (n_tokens < 1 || n_tokens > d.max_tokens) return SI_ERR_INVALID_ARG;
+        *bytes = si::prefill_layout(d, n_tokens).total;
+        return SI_OK;
+    }
     return SI_ERR_INVALID_ARG;
 }
 
@@ -243,13 +274,77 @@ si_status si_debug_decode_events(si_moe_plan_t plan, const si_moe_layer *layer, 
                                reinterpret_cast<cudaEvent_t const *>(events), stream);
 }
 
+static si_status forward_prefill_impl(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
+                                      int32_t n_tokens, float *out, si_moe_route_out *ro, void *scratch,
+                                      size_t scratch_bytes, cudaEvent_t const *events, si_stream_t stream) {
+    if (!plan || !layer || !x_bf16 || !out || !scratch) return SI_ERR_INVALID_ARG;
+    if (!layer->w_gate || !layer->w_up || !layer->w_down || !layer->router_w) return SI_ERR_INVALID_ARG;
+    const si_moe_desc &d = plan->p.desc;
+    if (n_tokens < 1 || n_tokens > d.max_tokens) return SI_ERR_INVALID_ARG;
+    if (!aligned(layer->w_gate, 16) || !aligned(layer->w_up, 16) || !aligned(layer->w_down, 16) ||
+        !aligned(layer->router_w, 16) || !aligned(x_bf16, 16) || !aligned(out, 16) ||
+        !aligned(scratch, 16) || (layer->router_bias && !aligned(layer->router_bias, 4)))
+        return SI_ERR_MISALIGNED;
+    if (ro && ((ro->topk_ids && !aligned(ro->topk_ids, 4)) || (ro->topk_w && !aligned(ro->topk_w, 4)) ||
+               (ro->expert_counts && !aligned(ro->expert_counts, 4)) ||
+               (ro->expert_offsets && !aligned(ro->expert_offsets, 4)) || (ro->perm && !aligned(ro->perm, 4)) ||
+               (ro->logits && !aligned(ro->logits, 4))))
+        return SI_ERR_MISALIGNED;
+    if (!plan->p.prefill_ok) return SI_ERR_UNSUPPORTED;
+    const si::PrefillLayout L = si::prefill_layout(d, n_tokens);
+    if (scratch_bytes < L.total) return SI_ERR_SCRATCH_TOO_SMALL;
+    uint8_t *sb = static_cast<uint8_t *>(scratch);
+    si::PrefillArgs a{};
+    a.wg = static_cast<const uint8_t *>(layer->w_gate);
+    a.wu = static_cast<const uint8_t *>(layer->w_up);
+    a.wd = static_cast<const uint8_t *>(layer->w_down);
+    a.router_w = layer->router_w;
+    a.router_bias = layer->router_bias;
+    a.x = static_cast<const uint16_t *>(x_bf16);
+    a.out = out;
+    a.H = d.hidden;
+    a.I = d.intermediate;
+    a.E = d.n_experts;
+    a.k = d.top_k;
+    a.T = n_tokens;
+    a.ctrl = reinterpret_cast<int32_t *>(sb + L.ctrl);
+    a.logits = reinterpret_cast<float *>(sb + L.logits);
+    a.ids = reinterpret_cast<int32_t *>(sb + L.ids);
+    a.wts = reinterpret_cast<float *>(sb + L.wts);
+    a.counts = reinterpret_cast<int32_t *>(sb + L.counts);
+    a.offsets = reinterpret_cast<int32_t *>(sb + L.offsets);
+    a.perm = reinterpret_cast<int32_t *>(sb + L.perm);
+    a.inv = reinterpret_cast<int32_t *>(sb + L.inv);
+    a.xh = reinterpret_cast<uint16_t *>(sb + L.xh);
+    a.h = reinterpret_cast<uint16_t *>(sb + L.h);
+    a.y = reinterpret_cast<float *>(sb + L.y);
+    if (ro) {
+        a.o_ids = ro->topk_ids;
+        a.o_w = ro->topk_w;
+        a.o_counts = ro->expert_counts;
+        a.o_offsets = ro->expert_offsets;
+        a.o_perm = ro->perm;
+        a.o_logits = ro->logits;
+    }
+    a.wait_budget = plan->p.wait_budget;
+    if (si::launch_prefill(plan->p, a, (cudaStream_t)stream, events) != cudaSuccess) {
+        cudaGetLastError();
+        return SI_ERR_CUDA;
+    }
+    return SI_OK;
+}
+
 si_status si_moe_forward_prefill(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
-                                 int32_t n_tokens, float *out, si_moe_route_out *route_out,
-                                 void *scratch, size_t scratch_bytes, si_stream_t stream) {
-    (void)layer; (void)x_bf16; (void)n_tokens; (void)out; (void)route_out; (void)scratch;
-    (void)scratch_bytes; (void)stream;
-    if (!plan) return SI_ERR_INVALID_ARG;
-    return SI_ERR_UNSUPPORTED;
+                                 int32_t n_tokens, float *out, si_moe_route_out *ro, void *scratch,
+                                 size_t scratch_bytes, si_stream_t stream) {
+    return forward_prefill_impl(plan, layer, x_bf16, n_tokens, out, ro, scratch, scratch_bytes, nullptr, stream);
+}
+
+si_status si_debug_prefill_events(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
+                                  int32_t n_tokens, float *out, si_moe_route_out *ro, void *scratch,
+                                  size_t scratch_bytes, void *const *events, si_stream_t stream) {
+    return forward_prefill_impl(plan, layer, x_bf16, n_tokens, out, ro, scratch, scratch_bytes,
+                                reinterpret_cast<cudaEvent_t const *>(events), stream);
 }
 
 int si_debug_plan_info(si_moe_plan_t plan, int32_t *info, int32_t n) {

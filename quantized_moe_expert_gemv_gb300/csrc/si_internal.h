@@ -43,6 +43,7 @@ struct Plan {
     bool fault_wait;        // test mode: expert kernels first wait on a flag nothing sets
     bool fused_ok[SI_MAX_DECODE_TOKENS + 1];  // fused expert kernel usable for n tokens
     bool cluster_ok;                          // cluster expert kernel usable for n = 1
+    bool prefill_ok;                          // tensor-core prefill kernels configured
     int cluster_size;                         // CTAs per cluster (all clusters co-resident)
     int cluster_active;                       // clusters of that size the device holds at once
     DecodeLayout dec;  // sized for SI_MAX_DECODE_TOKENS tokens
@@ -80,6 +81,41 @@ struct DecodeArgs {
     int sel_logits;  // single token, cluster expert kernel: the router writes ids in rank order, the
                      // selected logits (not weights) and 0/1 counts; the expert kernel forms the weights
 };
+
+// Prefill scratch: routing arrays, the permuted SwiGLU activations h (bf16)
+// and the permuted, routing-weighted expert outputs y (fp32).
+struct PrefillLayout {
+    size_t ctrl, logits, ids, wts, counts, offsets, perm, inv, xh, h, y, total;
+};
+PrefillLayout prefill_layout(const si_moe_desc &d, int n_tokens);
+
+struct PrefillArgs {
+    const uint8_t *wg, *wu, *wd;
+    const float *router_w, *router_bias;
+    const uint16_t *x;  // [T][H] bf16 bits
+    float *out;         // [T][H]
+    int H, I, E, k, T;
+    int32_t *ctrl;
+    float *logits;     // [T][E]
+    int32_t *ids;      // [T*k] pair p = t*k + slot
+    float *wts;        // [T*k] renormalised routing weights
+    int32_t *counts;   // [E]
+    int32_t *offsets;  // [E+1]
+    int32_t *perm;     // [T*k] pair ids ordered by expert, then pair id
+    int32_t *inv;      // [T*k] position of each pair in perm
+    uint16_t *xh;      // [T][H] fp16 bits: x converted for the tensor cores
+    uint16_t *h;       // [T*k][I] fp16 bits, rows in perm order
+    float *y;          // [T*k][H] fp32, rows in perm order
+    int32_t *o_ids;
+    float *o_w;
+    int32_t *o_counts, *o_offsets, *o_perm;
+    float *o_logits;
+    long long wait_budget;
+};
+
+cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s,
+                           cudaEvent_t const *events = nullptr);
+cudaError_t prefill_prepare(const Plan &p);  // kernel attributes (shared memory opt-in)
 
 cudaError_t launch_decode(const Plan &p, const DecodeArgs &a, cudaStream_t s,
                           cudaEvent_t const *events = nullptr);
