@@ -66,17 +66,22 @@ PrefillLayout prefill_layout(const si_moe_desc &d, int n) {
         return at;
     };
     const size_t pairs = (size_t)n * d.top_k;
+    const size_t rows = pairs + 32 * (size_t)d.n_experts;
+    L.rows = (int64_t)rows;
     L.ctrl = take(kCtrlBytes);
     L.logits = take((size_t)n * d.n_experts * sizeof(float));
     L.ids = take(pairs * sizeof(int32_t));
     L.wts = take(pairs * sizeof(float));
     L.counts = take((size_t)d.n_experts * sizeof(int32_t));
     L.offsets = take(((size_t)d.n_experts + 1) * sizeof(int32_t));
+    L.poff = take(((size_t)d.n_experts + 1) * sizeof(int32_t));
     L.perm = take(pairs * sizeof(int32_t));
+    L.pperm = take(rows * sizeof(int32_t));
     L.inv = take(pairs * sizeof(int32_t));
-    L.xh = take((size_t)n * d.hidden * sizeof(uint16_t));
-    L.h = take(pairs * d.intermediate * sizeof(uint16_t));
-    L.y = take(pairs * d.hidden * sizeof(float));
+    L.wp = take(rows * sizeof(float));
+    L.xp = take(rows * d.hidden * sizeof(uint16_t));
+    L.h = take(rows * d.intermediate * sizeof(uint16_t));
+    L.y = take(rows * d.hidden * sizeof(float));
     L.total = o;
     return L;
 }
@@ -313,9 +318,13 @@ static si_status forward_prefill_impl(si_moe_plan_t plan, const si_moe_layer *la
     a.wts = reinterpret_cast<float *>(sb + L.wts);
     a.counts = reinterpret_cast<int32_t *>(sb + L.counts);
     a.offsets = reinterpret_cast<int32_t *>(sb + L.offsets);
+    a.rows = L.rows;
+    a.poff = reinterpret_cast<int32_t *>(sb + L.poff);
     a.perm = reinterpret_cast<int32_t *>(sb + L.perm);
+    a.pperm = reinterpret_cast<int32_t *>(sb + L.pperm);
     a.inv = reinterpret_cast<int32_t *>(sb + L.inv);
-    a.xh = reinterpret_cast<uint16_t *>(sb + L.xh);
+    a.wp = reinterpret_cast<float *>(sb + L.wp);
+    a.xp = reinterpret_cast<uint16_t *>(sb + L.xp);
     a.h = reinterpret_cast<uint16_t *>(sb + L.h);
     a.y = reinterpret_cast<float *>(sb + L.y);
     if (ro) {

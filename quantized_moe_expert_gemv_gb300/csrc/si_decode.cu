@@ -397,9 +397,14 @@ static int pow2_at_least(int v) {
     return p;
 }
 
+// Records events[i] on s (as an external event node while s is being captured).
 static cudaError_t mark(cudaEvent_t const *events, int i, cudaStream_t s) {
     if (!events || !events[i]) return cudaSuccess;
-    return cudaEventRecordWithFlags(events[i], s, cudaEventRecordExternal);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t err = cudaStreamIsCapturing(s, &cs);
+    if (err != cudaSuccess) return err;
+    return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(events[i], s, cudaEventRecordExternal)
+                                               : cudaEventRecord(events[i], s);
 }
 
 // One CTA for up to 32 experts, else an 8-CTA cluster (portable size).

@@ -82,10 +82,12 @@ struct DecodeArgs {
                      // selected logits (not weights) and 0/1 counts; the expert kernel forms the weights
 };
 
-// Prefill scratch: routing arrays, the permuted SwiGLU activations h (bf16)
-// and the permuted, routing-weighted expert outputs y (fp32).
+// Prefill scratch: routing arrays and the expert-major rows of the two GEMMs.
+// Each expert's rows start at a multiple of 32 (padded offsets poff), so the
+// 32-row tiles of the GEMM epilogues never reach another expert's rows.
 struct PrefillLayout {
-    size_t ctrl, logits, ids, wts, counts, offsets, perm, inv, xh, h, y, total;
+    size_t ctrl, logits, ids, wts, counts, offsets, poff, perm, pperm, inv, wp, xp, h, y, total;
+    int64_t rows;  // padded row capacity: T*k + 32*E
 };
 PrefillLayout prefill_layout(const si_moe_desc &d, int n_tokens);
 
@@ -95,17 +97,21 @@ struct PrefillArgs {
     const uint16_t *x;  // [T][H] bf16 bits
     float *out;         // [T][H]
     int H, I, E, k, T;
+    int64_t rows;      // padded row capacity of pperm/wp/xp/h/y
     int32_t *ctrl;
     float *logits;     // [T][E]
     int32_t *ids;      // [T*k] pair p = t*k + slot
     float *wts;        // [T*k] renormalised routing weights
     int32_t *counts;   // [E]
-    int32_t *offsets;  // [E+1]
+    int32_t *offsets;  // [E+1] exclusive scan of counts
+    int32_t *poff;     // [E+1] exclusive scan of counts rounded up to 32
     int32_t *perm;     // [T*k] pair ids ordered by expert, then pair id
-    int32_t *inv;      // [T*k] position of each pair in perm
-    uint16_t *xh;      // [T][H] fp16 bits: x converted for the tensor cores
-    uint16_t *h;       // [T*k][I] fp16 bits, rows in perm order
-    float *y;          // [T*k][H] fp32, rows in perm order
+    int32_t *pperm;    // [rows] pair id of each padded row (-1 = padding)
+    int32_t *inv;      // [T*k] padded row of each pair
+    float *wp;         // [rows] routing weight of each padded row (0 = padding)
+    uint16_t *xp;      // [rows][H] fp16 bits: x of each padded row's token
+    uint16_t *h;       // [rows][I] fp16 bits
+    float *y;          // [rows][H] fp32
     int32_t *o_ids;
     float *o_w;
     int32_t *o_counts, *o_offsets, *o_perm;

@@ -84,12 +84,7 @@ __global__ void __launch_bounds__(kRtThreads) k_prefill_route(PrefillArgs a) {
             for (int q = tid; q < kRtTok * kRtKc; q += kRtThreads) {
                 const int tk = q / kRtKc, c = q - tk * kRtKc;
                 const int t = t0 + tk;
-                const float xv = t < a.T ? __uint_as_float((uint32_t)__ldg(a.x + (size_t)t * a.H + c0 + c) << 16) : 0.f;
-                s_x[c][tk] = xv;
-                if (e0 == 0 && t < a.T) {  // fp16 copy of x for the tensor-core GEMM
-                    if (fabsf(xv) > 65504.f) set_status(a.ctrl + kCtrlStatus, SI_ERR_RANGE);
-                    a.xh[(size_t)t * a.H + c0 + c] = __half_as_ushort(__float2half_rn(xv));
-                }
+                s_x[c][tk] = t < a.T ? __uint_as_float((uint32_t)__ldg(a.x + (size_t)t * a.H + c0 + c) << 16) : 0.f;
             }
             __syncthreads();
 #pragma unroll 8
@@ -176,28 +171,33 @@ __global__ void __launch_bounds__(kRtThreads) k_prefill_route(PrefillArgs a) {
     }
 }
 
-// offsets[e] = counts[0] + ... + counts[e-1]; offsets[E] = T*k.  One CTA.
+// offsets[e] = counts[0] + ... + counts[e-1], offsets[E] = T*k; poff the same
+// over the counts rounded up to multiples of 32.  One CTA.
 __global__ void __launch_bounds__(256) k_prefill_scan(PrefillArgs a) {
-    __shared__ int s_warp[8];
+    __shared__ int s_warp[8][2];
     const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
     const int c = e < a.E ? a.counts[e] : 0;
-    int incl = c;
+    const int cp = (c + 31) & ~31;
+    int incl = c, inclp = cp;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        const int vp = __shfl_up_sync(0xffffffffu, inclp, o);
+        if (lane >= o) incl += v, inclp += vp;
     }
-    if (lane == 31) s_warp[warp] = incl;
+    if (lane == 31) s_warp[warp][0] = incl, s_warp[warp][1] = inclp;
     __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += s_warp[w];
+    int base = 0, basep = 0;
+    for (int w = 0; w < warp; ++w) base += s_warp[w][0], basep += s_warp[w][1];
     if (e < a.E) {
         a.offsets[e] = base + incl - c;
+        a.poff[e] = basep + inclp - cp;
         if (a.o_offsets) a.o_offsets[e] = base + incl - c;
         if (a.o_counts) a.o_counts[e] = c;
     }
-    if (e == 0) {
+    if (e == a.E - 1) {
         a.offsets[a.E] = a.T * a.k;
+        a.poff[a.E] = basep + inclp;
         if (a.o_offsets) a.o_offsets[a.E] = a.T * a.k;
     }
 }
@@ -208,8 +208,12 @@ __global__ void __launch_bounds__(1024) k_prefill_perm(PrefillArgs a) {
     __shared__ int s_warp[32];
     __shared__ int s_base;
     const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int off = a.offsets[e];
+    const int off = a.offsets[e], poff = a.poff[e];
     const int np = a.T * a.k;
+    for (int r = poff + a.counts[e] + tid; r < a.poff[e + 1]; r += blockDim.x) {  // padding rows
+        a.pperm[r] = -1;
+        a.wp[r] = 0.f;
+    }
     if (tid == 0) s_base = 0;
     __syncthreads();
     for (int p0 = 0; p0 < np; p0 += 1024) {
@@ -221,10 +225,13 @@ __global__ void __launch_bounds__(1024) k_prefill_perm(PrefillArgs a) {
         int before = s_base;
         for (int w = 0; w < warp; ++w) before += s_warp[w];
         if (mine) {
-            const int pos = off + before + __popc(bal & ((1u << lane) - 1u));
-            a.perm[pos] = p;
-            a.inv[p] = pos;
-            if (a.o_perm) a.o_perm[pos] = p;
+            const int j = before + __popc(bal & ((1u << lane) - 1u));  // rank among this expert's pairs
+            const int prow = poff + j;
+            a.perm[off + j] = p;
+            if (a.o_perm) a.o_perm[off + j] = p;
+            a.inv[p] = prow;
+            a.pperm[prow] = p;
+            a.wp[prow] = a.wts[p];
         }
         __syncthreads();
         if (tid == 0) {
@@ -233,6 +240,35 @@ __global__ void __launch_bounds__(1024) k_prefill_perm(PrefillArgs a) {
             s_base += tot;
         }
         __syncthreads();
+    }
+}
+
+// Padded expert-major token rows for the gate/up GEMM: xp[r] = fp16(x[token of
+// pperm[r]]), zero for padding rows; a value beyond fp16's range is reported.
+__global__ void __launch_bounds__(256) k_prefill_xperm(PrefillArgs a) {
+    const int nrows = a.poff[a.E];
+    const int c8 = a.H / 8;
+    for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < (size_t)nrows * c8;
+         q += (size_t)gridDim.x * blockDim.x) {
+        const int r = (int)(q / c8), c = (int)(q - (size_t)r * c8);
+        const int p = __ldg(a.pperm + r);
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (p >= 0) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)(p / a.k) * a.H) + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t h[4];
+            bool big = false;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+                big |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+                const __half2 hh = __floats2half2_rn(lo, hi);
+                h[i] = *reinterpret_cast<const uint32_t *>(&hh);
+            }
+            if (big) set_status(a.ctrl + kCtrlStatus, SI_ERR_RANGE);
+            o = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+        reinterpret_cast<uint4 *>(a.xp + (size_t)r * a.H)[c] = o;
     }
 }
 
@@ -258,53 +294,60 @@ __global__ void __launch_bounds__(256) k_prefill_combine(PrefillArgs a) {
 // 4-5. Grouped GEMMs on the tensor cores
 // =====================================================================
 namespace {
-constexpr int kGW = 12;                    // warps: 0-1 gather, 2 weight copies, 3 MMA, 4-11 dequant (4-7 epilogue)
+constexpr int kGW = 16;                    // warps (see the role map in k_prefill_gemm)
 constexpr int kGThreads = kGW * 32;
 constexpr int kNS = 2;                     // operand stages (64-wide K steps)
 constexpr int kNR = 2;                     // raw Q4_K stages (256-wide K blocks)
 constexpr int kMaxTok = 512;               // tokens per pass: two 256-column accumulators
+constexpr int kBoxTok = 64;                // token rows per operand-B tensor box
 constexpr int kATile = 128 * 128;          // 128 weight rows x 64 fp16
 constexpr int kBTile = kMaxTok * 128;      // up to 512 token rows x 64 fp16
 constexpr int kStage = kATile + kBTile;
 constexpr int kRaw = 128 * kBlockBytes;    // 128 weight rows x one Q4_K block
-constexpr int kXch = 64 * 33 * 4;          // gate/up epilogue exchange: 64 rows x 32 tokens (+pad)
+constexpr int kStg = 32 * 128 * 4;         // epilogue staging: 32 rows x 128 fp32 (or 32 x 64 fp16)
 constexpr int kOffRaw = kNS * kStage;
-constexpr int kOffXch = kOffRaw + kNR * kRaw;
-constexpr int kOffRows = kOffXch + kXch;   // [kMaxTok] int64 source element offsets (-1 = pad)
-constexpr int kOffBar = kOffRows + kMaxTok * 8;
-constexpr int kNBar = 2 * kNR + 3 * kNS + 2 + 1;
+constexpr int kOffStg = kOffRaw + kNR * kRaw;
+constexpr int kOffBar = kOffStg + kStg;
+constexpr int kNBar = 2 * kNR + 3 * kNS + 4 + 1;
 constexpr int kGemmSmem = kOffBar + kNBar * 8 + 16 + 1024;  // + alignment slack
 constexpr long long kDrainG = 4000000000LL;
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
     const __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
 }
+// 2-D tensor store shared -> global (bulk-group completion), its commit and
+// the wait until the shared-memory source may be overwritten.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // The sequence of work every role walks through in the same order: units
 // (expert, row tile) strided over the grid, each in passes of <= 512 tokens.
 struct Pass {
-    int e, tile, off, sc, nt;  // expert, row tile, first pair position, first token of the pass, tokens
+    int e, tile, prow, sc, nt;  // expert, row tile, first padded row of the expert, first token, tokens
 };
 }  // namespace
 
-// MODE 0 (gate/up): A rows 0-63 = gate rows tile*64.., rows 64-127 = up rows;
-//   K = H; B row r = token of pair perm[off + sc + r]; epilogue writes
-//   h[off + sc + r][tile*64 + i] = fp16(silu(g_i) * u_i).
-// MODE 1 (down): A rows = down rows tile*128..; K = I; B row r = h row
-//   off + sc + r; epilogue writes y[pos][tile*128 + i] = w_pair * acc.
+// MODE 0 (gate/up): A row 2i = gate row tile*64+i, row 2i+1 = up row
+//   tile*64+i; K = H; B rows = padded token rows of the expert (xp);
+//   epilogue h[row][tile*64 + i] = fp16(silu(g_i) * u_i).
+// MODE 1 (down): A rows = down rows tile*128..; K = I; B rows = h rows of
+//   the expert; epilogue y[row][tile*128 + i] = wp[row] * acc.
+// Roles: warp 0 tensor-map copies (Q4_K blocks, B tiles), warp 1 MMA issue
+// and tensor-memory allocation, warps 4-11 dequantization, warps 12-15
+// epilogue (accumulators double-buffered: the epilogue of one 256-token chunk
+// overlaps the MMAs of the next).
 template <int MODE>
 __global__ void __launch_bounds__(kGThreads, 1)
     k_prefill_gemm(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                   const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_out,
                    PrefillArgs a) {
     extern __shared__ uint8_t g_smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(g_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -321,29 +364,32 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const uint32_t bar0 = smem_addr(sm + kOffBar);
     const uint32_t raw_full = bar0, raw_empty = bar0 + 8 * kNR;
     const uint32_t full_a = bar0 + 16 * kNR, full_b = full_a + 8 * kNS, empty = full_b + 8 * kNS;
-    const uint32_t d_full = empty + 8 * kNS, d_empty = d_full + 8, fin = d_empty + 8;
-    int64_t *rows = reinterpret_cast<int64_t *>(sm + kOffRows);
+    const uint32_t d_full = empty + 8 * kNS, d_empty = d_full + 16, fin = d_empty + 16;  // d_*: [2]
     volatile int *verr = &s_err;
 
     if (threadIdx.x == 0) {
         s_err = 0;
         prefetch_tensormap(&tm_a0);
         if (MODE == 0) prefetch_tensormap(&tm_a1);
+        prefetch_tensormap(&tm_b);
+        prefetch_tensormap(&tm_out);
         for (int r = 0; r < kNR; ++r) {
             mbar_init(raw_full + 8 * r, 1);
             mbar_init(raw_empty + 8 * r, 8);
         }
         for (int s = 0; s < kNS; ++s) {
             mbar_init(full_a + 8 * s, 8);
-            mbar_init(full_b + 8 * s, 64);
+            mbar_init(full_b + 8 * s, 1);
             mbar_init(empty + 8 * s, 1);
         }
-        mbar_init(d_full, 1);
-        mbar_init(d_empty, 4);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(d_full + 8 * b, 1);
+            mbar_init(d_empty + 8 * b, 4);
+        }
         mbar_init(fin, 1);
         fence_mbar_init();
     }
-    if (warp == 3) {
+    if (warp == 1) {
         tc::tmem_alloc(smem_addr(&s_taddr), 512);
         tc::tmem_relinquish();
     }
@@ -356,8 +402,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     auto for_each_pass = [&](auto &&body) {
         for (int u = blockIdx.x; u < nU && !*verr; u += gridDim.x) {
             const int e = u / tiles, tile = u - e * tiles;
-            const int ne = __ldg(a.counts + e), off = __ldg(a.offsets + e);
-            for (int sc = 0; sc < ne && !*verr; sc += kMaxTok) body(Pass{e, tile, off, sc, min(kMaxTok, ne - sc)});
+            const int ne = __ldg(a.counts + e), prow = __ldg(a.poff + e);
+            for (int sc = 0; sc < ne && !*verr; sc += kMaxTok) body(Pass{e, tile, prow, sc, min(kMaxTok, ne - sc)});
         }
     };
     auto fail = [&]() {
@@ -365,84 +411,67 @@ __global__ void __launch_bounds__(kGThreads, 1)
         *verr = 1;
     };
 
-    if (warp < 2) {
-        // ------------------------------------------------ gather: token rows -> B tiles
-        // Gather warp w owns token rows [256w, 256w + 256) of a pass: it builds
-        // their source offsets and copies them, 8 lanes per 128-byte row.
-        const int r_lo = 256 * warp;
-        const int sub = lane >> 3, c = lane & 7;
-        int step = 0;
-        for_each_pass([&](const Pass &ps) {
-            const int ntp = (ps.nt + 15) & ~15;
-            const int r_hi = min(ntp, r_lo + 256);
-            __syncwarp();
-            for (int r = r_lo + lane; r < r_hi; r += 32) {
-                int64_t src = -1;
-                if (r < ps.nt) {
-                    const int pos = ps.off + ps.sc + r;
-                    src = MODE == 0 ? (int64_t)(__ldg(a.perm + pos) / a.k) * a.H : (int64_t)pos * a.I;
-                }
-                rows[r] = src;
-            }
-            __syncwarp();
-            const uint16_t *base = MODE == 0 ? a.xh : a.h;
-            for (int kb = 0; kb < nK; ++kb, ++step) {
-                const int s = step % kNS;
-                if (step >= kNS && !mbar_wait_warp(empty + 8 * s, ((step / kNS) - 1) & 1, budget)) {
-                    fail();
-                    return;
-                }
-                const uint32_t bt = smem_addr(sm + s * kStage + kATile);
-                for (int r = r_lo + sub; r < r_hi; r += 4) {
-                    const int64_t src = rows[r];
-                    const uint32_t dst = bt + r * 128 + ((c ^ (r & 7)) << 4);
-                    cp_async16(dst, base + (src >= 0 ? src + kb * 64 + c * 8 : 0), src >= 0);
-                }
-                cp_async_arrive_noinc(full_b + 8 * s);
-            }
-        });
-        cp_async_wait_all();
-    } else if (warp == 2) {
-        // ------------------------------------------------ Q4_K weight blocks (tensor-map copies)
+    if (warp == 0) {
+        // ------------------------------------------------ tensor-map copies
         if (lane == 0) {
-            const uint64_t pol = l2_evict_first_policy();
-            int rstep = 0;
+            const uint64_t pol = l2_evict_first_policy();  // each Q4_K block is read by one CTA
+            int rstep = 0, step = 0;
             for_each_pass([&](const Pass &ps) {
-                for (int blk = 0; blk < nK / 4; ++blk, ++rstep) {
-                    const int r = rstep % kNR;
-                    if (rstep >= kNR && !mbar_wait_bounded(raw_empty + 8 * r, ((rstep / kNR) - 1) & 1, budget)) {
+                const int nbox = (ps.nt + kBoxTok - 1) / kBoxTok;
+                for (int kb = 0; kb < nK; ++kb, ++step) {
+                    if ((kb & 3) == 0) {  // next Q4_K block of the 128 weight rows
+                        const int r = rstep % kNR;
+                        if (rstep >= kNR && !mbar_wait_bounded(raw_empty + 8 * r, ((rstep / kNR) - 1) & 1, budget)) {
+                            fail();
+                            return;
+                        }
+                        const uint32_t dst = smem_addr(sm + kOffRaw + r * kRaw);
+                        mbar_arrive_expect_tx(raw_full + 8 * r, kRaw);
+                        if (MODE == 0) {
+                            const int y = ps.e * a.I + ps.tile * 64;
+                            tma_load_2d(dst, &tm_a0, kBlockBytes * (kb >> 2), y, raw_full + 8 * r, pol);
+                            tma_load_2d(dst + 64 * kBlockBytes, &tm_a1, kBlockBytes * (kb >> 2), y, raw_full + 8 * r, pol);
+                        } else {
+                            tma_load_2d(dst, &tm_a0, kBlockBytes * (kb >> 2), ps.e * a.H + ps.tile * 128,
+                                        raw_full + 8 * r, pol);
+                        }
+                        ++rstep;
+                    }
+                    const int s = step % kNS;
+                    if (step >= kNS && !mbar_wait_bounded(empty + 8 * s, ((step / kNS) - 1) & 1, budget)) {
                         fail();
                         return;
                     }
-                    const uint32_t dst = smem_addr(sm + kOffRaw + r * kRaw);
-                    mbar_arrive_expect_tx(raw_full + 8 * r, kRaw);
-                    if (MODE == 0) {
-                        const int y = ps.e * a.I + ps.tile * 64;
-                        tma_load_2d(dst, &tm_a0, kBlockBytes * blk, y, raw_full + 8 * r, pol);
-                        tma_load_2d(dst + 64 * kBlockBytes, &tm_a1, kBlockBytes * blk, y, raw_full + 8 * r, pol);
-                    } else {
-                        tma_load_2d(dst, &tm_a0, kBlockBytes * blk, ps.e * a.H + ps.tile * 128, raw_full + 8 * r,
-                                    pol);
-                    }
+                    const uint32_t bt = smem_addr(sm + s * kStage + kATile);
+                    mbar_arrive_expect_tx(full_b + 8 * s, (uint32_t)(nbox * kBoxTok * 128));
+                    for (int b = 0; b < nbox; ++b)
+                        tma_load_2d_plain(bt + b * kBoxTok * 128, &tm_b, 64 * kb, ps.prow + ps.sc + kBoxTok * b,
+                                          full_b + 8 * s);
                 }
             });
-            // drain: every issued block must have landed before the CTA exits
+            // drain: every issued Q4_K block has landed before the CTA exits
             for (int q = (rstep > kNR ? rstep - kNR : 0); q < rstep; ++q)
                 mbar_wait_bounded(raw_full + 8 * (q % kNR), (q / kNR) & 1, kDrainG);
+            for (int q = (step > kNS ? step - kNS : 0); q < step; ++q)
+                mbar_wait_bounded(full_b + 8 * (q % kNS), (q / kNS) & 1, kDrainG);
         }
         __syncwarp();
-    } else if (warp == 3) {
+    } else if (warp == 1) {
         // ------------------------------------------------ MMA issue (one thread)
         if (lane == 0) {
-            int step = 0, npass = 0;
+            int step = 0, chunk = 0;
+            int uses[2] = {0, 0};
             bool issued = false;
             for_each_pass([&](const Pass &ps) {
-                if (npass > 0 && !mbar_wait_bounded(d_empty, (npass - 1) & 1, budget)) {
-                    fail();
-                    return;
+                const int nch = (ps.nt + 255) >> 8;
+                for (int c = 0; c < nch; ++c) {  // the accumulator buffers of this pass are drained
+                    const int b = (chunk + c) & 1;
+                    if (uses[b] > 0 && !mbar_wait_bounded(d_empty + 8 * b, (uses[b] - 1) & 1, budget)) {
+                        fail();
+                        return;
+                    }
                 }
                 tc::fence_after_sync();
-                const int nch = (ps.nt + 255) >> 8;
                 for (int kb = 0; kb < nK; ++kb, ++step) {
                     const int s = step % kNS;
                     const uint32_t par = (step / kNS) & 1;
@@ -450,22 +479,27 @@ __global__ void __launch_bounds__(kGThreads, 1)
                         fail();
                         return;
                     }
-                    tc::fence_proxy_async_smem();  // gathered rows were written through the generic proxy
+                    tc::fence_proxy_async_smem();  // the dequantized A tile was written through the generic proxy
                     tc::fence_after_sync();
                     const uint32_t at = smem_addr(sm + s * kStage);
                     for (int c = 0; c < nch; ++c) {
                         const int nc = min(256, ps.nt - 256 * c);
                         const uint32_t idesc = tc::idesc_f16_f32(128, (nc + 15) & ~15);
                         const uint32_t bt = at + kATile + c * 256 * 128;
+                        const uint32_t d = taddr + 256 * ((chunk + c) & 1);
                         for (int j = 0; j < 4; ++j)
-                            tc::mma_f16kind(taddr + 256 * c, tc::sdesc_sw128(at + 32 * j), tc::sdesc_sw128(bt + 32 * j),
-                                         idesc, kb > 0 || j > 0);
+                            tc::mma_f16kind(d, tc::sdesc_sw128(at + 32 * j), tc::sdesc_sw128(bt + 32 * j), idesc,
+                                            kb > 0 || j > 0);
                     }
                     tc::mma_commit(empty + 8 * s);
                     issued = true;
                 }
-                tc::mma_commit(d_full);
-                ++npass;
+                for (int c = 0; c < nch; ++c) {
+                    const int b = (chunk + c) & 1;
+                    tc::mma_commit(d_full + 8 * b);
+                    ++uses[b];
+                }
+                chunk += nch;
             });
             if (issued) {  // every MMA has completed before the tensor memory is released
                 tc::mma_commit(fin);
@@ -473,13 +507,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------ dequant (warps 4-11), epilogue (warps 4-7)
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------ dequant (warps 4-11)
         const int d = threadIdx.x - 128;  // 0..255
         const int row = d >> 1, half = d & 1;
-        const int ew = warp - 4;          // epilogue warp 0..3 (tensor-memory lanes 32*ew..)
-        float *xch = reinterpret_cast<float *>(sm + kOffXch);
-        int astep = 0, rstep = 0, npass = 0;
+        // MODE 0: A row 2i = gate row i, 2i+1 = up row i (raw rows: gate 0-63, up 64-127)
+        const int raw_row = MODE == 0 ? ((row & 1) ? 64 + (row >> 1) : (row >> 1)) : row;
+        int astep = 0, rstep = 0;
         for_each_pass([&](const Pass &ps) {
             for (int kb = 0; kb < nK; ++kb, ++astep) {
                 const int j = kb & 3;
@@ -493,7 +527,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     fail();
                     return;
                 }
-                const uint8_t *blk = sm + kOffRaw + r * kRaw + row * kBlockBytes;
+                const uint8_t *blk = sm + kOffRaw + r * kRaw + raw_row * kBlockBytes;
                 const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
                 const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j);
                 const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * j);
@@ -531,58 +565,74 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     ++rstep;
                 }
             }
-            if (ew < 4) {
-                // -------------------------------------------- epilogue
-                if (!mbar_wait_warp(d_full, npass & 1, budget)) {
+        });
+    } else if (warp >= 12) {
+        // ------------------------------------------------ epilogue (warps 12-15)
+        const int ew = warp - 12;  // tensor-memory lanes 32*ew ..
+        const bool lead = threadIdx.x == 12 * 32;
+        uint8_t *stg = sm + kOffStg;
+        int chunk = 0;
+        int uses[2] = {0, 0};
+        for_each_pass([&](const Pass &ps) {
+            const int nch = (ps.nt + 255) >> 8;
+            for (int c = 0; c < nch; ++c, ++chunk) {
+                const int b = chunk & 1;
+                if (!mbar_wait_warp(d_full + 8 * b, uses[b] & 1, budget)) {
                     fail();
                     return;
                 }
+                ++uses[b];
                 tc::fence_after_sync();
-                const int nch = (ps.nt + 255) >> 8;
-                for (int c = 0; c < nch; ++c) {
-                    const int nc = min(256, ps.nt - 256 * c);
-                    for (int col0 = 0; col0 < nc; col0 += 32) {
-                        uint32_t v[32];
-                        tc::tmem_ld32(taddr + ((uint32_t)(32 * ew) << 16) + 256 * c + col0, v);
-                        tc::tmem_wait_ld();
-                        if (MODE == 0) {
-                            if (ew >= 2)  // up rows: hand them to the gate-row threads
-                                for (int q = 0; q < 32; ++q) xch[(32 * (ew - 2) + lane) * 33 + q] = __uint_as_float(v[q]);
-                            asm volatile("bar.sync 3, 128;" ::: "memory");
-                            if (ew < 2) {
-                                const int i = ps.tile * 64 + 32 * ew + lane;
-                                for (int q = 0; q < 32 && col0 + q < nc; ++q) {
-                                    const float gg = __uint_as_float(v[q]);
-                                    const float uu = xch[(32 * ew + lane) * 33 + q];
-                                    const float hv = silu(gg) * uu;
-                                    const size_t pos = (size_t)ps.off + ps.sc + 256 * c + col0 + q;
-                                    if (fabsf(hv) > 65504.f) set_status(status, SI_ERR_RANGE);
-                                    a.h[pos * a.I + i] = __half_as_ushort(__float2half_rn(hv));
-                                }
-                            }
-                            asm volatile("bar.sync 3, 128;" ::: "memory");
-                        } else {
-                            const int f = ps.tile * 128 + 32 * ew + lane;
-                            const int pos0 = ps.off + ps.sc + 256 * c + col0;
-                            float wl = 0.f;  // routing weight of token col0 + lane
-                            if (col0 + lane < nc) wl = __ldg(a.wts + __ldg(a.perm + pos0 + lane));
-                            for (int q = 0; q < 32; ++q) {
-                                const float wq = __shfl_sync(0xffffffffu, wl, q);
-                                if (col0 + q < nc) a.y[(size_t)(pos0 + q) * a.H + f] = wq * __uint_as_float(v[q]);
-                            }
+                const int nc = min(256, ps.nt - 256 * c);
+                for (int col0 = 0; col0 < nc; col0 += 32) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(taddr + ((uint32_t)(32 * ew) << 16) + 256 * b + col0, v);
+                    tc::tmem_wait_ld();
+                    const int row0 = ps.prow + ps.sc + 256 * c + col0;  // padded row of token col0
+                    if (MODE == 0) {
+                        // lanes 2i / 2i+1 hold g / u of intermediate row i for 32 tokens;
+                        // the even lane forms h for tokens 0-15, the odd lane for 16-31
+                        uint16_t *hs = reinterpret_cast<uint16_t *>(stg);  // [32 tokens][64] fp16
+                        const int up = lane & 1;
+                        const int il = 16 * ew + (lane >> 1);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const float send = __uint_as_float(up ? v[q] : v[q + 16]);
+                            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                            const float gg = up ? recv : __uint_as_float(v[q]);
+                            const float uu = up ? __uint_as_float(v[q + 16]) : recv;
+                            const float hv = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
+                            // columns past the pass's tokens hold stale accumulators: not checked
+                            if (col0 + q + 16 * up < nc && fabsf(hv) > 65504.f) set_status(status, SI_ERR_RANGE);
+                            hs[(q + 16 * up) * 64 + il] = __half_as_ushort(__float2half_rn(hv));
                         }
+                    } else {
+                        float *ys = reinterpret_cast<float *>(stg);  // [32 tokens][128] fp32
+                        const float wl = __ldg(a.wp + row0 + lane);  // weight of token col0 + lane (0 on padding)
+#pragma unroll
+                        for (int q = 0; q < 32; ++q)
+                            ys[q * 128 + 32 * ew + lane] = __shfl_sync(0xffffffffu, wl, q) * __uint_as_float(v[q]);
                     }
+                    // rows past the expert's tokens land in its own padding (poff is 32-aligned)
+                    tc::fence_proxy_async_smem();
+                    asm volatile("bar.sync 4, 128;" ::: "memory");
+                    if (lead) {
+                        tma_store_2d(&tm_out, MODE == 0 ? ps.tile * 64 : ps.tile * 128, row0, smem_addr(stg));
+                        bulk_commit();
+                        bulk_wait_read0();
+                    }
+                    asm volatile("bar.sync 4, 128;" ::: "memory");
                 }
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(d_empty);
+                if (lane == 0) mbar_arrive(d_empty + 8 * b);
             }
-            ++npass;
         });
+        if (lead) bulk_wait0();
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 3) {
+    if (warp == 1) {
         tc::fence_after_sync();
         tc::tmem_dealloc(taddr, 512);
     }
@@ -620,6 +670,22 @@ static bool q4k_map(const uint8_t *base, int64_t rows, int blocks_per_row, int b
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major matrix [rows][cols] of fp16 (esize 2) or fp32 (esize 4); box of
+// box_cols x box_rows; 128-byte swizzle for tensor-core operand tiles.
+static bool mat_map(const void *base, int64_t rows, int cols, int esize, int box_cols, int box_rows, bool sw128,
+                    CUtensorMap *tm) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(tm, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t prefill_prepare(const Plan &p) {
     (void)p;
     if (!encoder()) return cudaErrorNotSupported;
@@ -630,9 +696,14 @@ cudaError_t prefill_prepare(const Plan &p) {
     return cudaFuncSetAttribute(k_prefill_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
 }
 
+// Records events[i] on s (as an external event node while s is being captured).
 static cudaError_t mark(cudaEvent_t const *events, int i, cudaStream_t s) {
     if (!events || !events[i]) return cudaSuccess;
-    return cudaEventRecordWithFlags(events[i], s, cudaEventRecordExternal);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t err = cudaStreamIsCapturing(s, &cs);
+    if (err != cudaSuccess) return err;
+    return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(events[i], s, cudaEventRecordExternal)
+                                               : cudaEventRecord(events[i], s);
 }
 
 cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, cudaEvent_t const *events) {
@@ -642,18 +713,22 @@ cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, 
     k_prefill_route<<<(a.T + kRtTok - 1) / kRtTok, kRtThreads, kRtSmem, s>>>(a);
     k_prefill_scan<<<1, 256, 0, s>>>(a);
     k_prefill_perm<<<a.E, 1024, 0, s>>>(a);
+
+    k_prefill_xperm<<<4 * p.sm_count, 256, 0, s>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 1, s)) != cudaSuccess) return err;
 
-    CUtensorMap tg, tu, td;
+    CUtensorMap tg, tu, td, txp, thl, ths, tys;
     if (!q4k_map(a.wg, (int64_t)a.E * a.I, a.H / kQK, 64, &tg) || !q4k_map(a.wu, (int64_t)a.E * a.I, a.H / kQK, 64, &tu) ||
-        !q4k_map(a.wd, (int64_t)a.E * a.H, a.I / kQK, 128, &td))
+        !q4k_map(a.wd, (int64_t)a.E * a.H, a.I / kQK, 128, &td) ||
+        !mat_map(a.xp, a.rows, a.H, 2, 64, kBoxTok, true, &txp) || !mat_map(a.h, a.rows, a.I, 2, 64, kBoxTok, true, &thl) ||
+        !mat_map(a.h, a.rows, a.I, 2, 64, 32, false, &ths) || !mat_map(a.y, a.rows, a.H, 4, 128, 32, false, &tys))
         return cudaErrorInvalidValue;
     const int grid = p.sm_count;
-    k_prefill_gemm<0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, a);
+    k_prefill_gemm<0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp, ths, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 2, s)) != cudaSuccess) return err;
-    k_prefill_gemm<1><<<grid, kGThreads, kGemmSmem, s>>>(td, td, a);
+    k_prefill_gemm<1><<<grid, kGThreads, kGemmSmem, s>>>(td, td, thl, tys, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 3, s)) != cudaSuccess) return err;
     const size_t n4 = (size_t)a.T * (a.H / 4);
