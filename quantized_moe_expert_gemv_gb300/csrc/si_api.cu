@@ -69,6 +69,7 @@ PrefillLayout prefill_layout(const si_moe_desc &d, int n) {
     const size_t rows = pairs + 32 * (size_t)d.n_experts;
     L.rows = (int64_t)rows;
     L.ctrl = take(kCtrlBytes);
+    L.wt = take((size_t)((d.n_experts + 127) / 128 * 128) * d.hidden * sizeof(float));
     L.logits = take((size_t)n * d.n_experts * sizeof(float));
     L.ids = take(pairs * sizeof(int32_t));
     L.wts = take(pairs * sizeof(float));
@@ -319,6 +320,7 @@ static si_status forward_prefill_impl(si_moe_plan_t plan, const si_moe_layer *la
     a.counts = reinterpret_cast<int32_t *>(sb + L.counts);
     a.offsets = reinterpret_cast<int32_t *>(sb + L.offsets);
     a.rows = L.rows;
+    a.wt = reinterpret_cast<float *>(sb + L.wt);
     a.poff = reinterpret_cast<int32_t *>(sb + L.poff);
     a.perm = reinterpret_cast<int32_t *>(sb + L.perm);
     a.pperm = reinterpret_cast<int32_t *>(sb + L.pperm);

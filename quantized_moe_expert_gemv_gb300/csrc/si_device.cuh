@@ -247,6 +247,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// The same wait without sleeping between polls (for a thread on the critical
+// path, e.g. the one issuing tensor-core MMAs); the clock is read every 64
+// polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, long long budget) {
+    const long long t0 = clock64();
+    for (int n = 0;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63) == 63 && clock64() - t0 > budget) return false;
+    }
+}
+
 // The same wait for a whole warp with one polling lane: lane 0 spins, and
 // once it has seen the phase complete every lane takes one try_wait of its
 // own (which then succeeds at once) for the acquire of the copied bytes.

@@ -86,7 +86,7 @@ struct DecodeArgs {
 // Each expert's rows start at a multiple of 32 (padded offsets poff), so the
 // 32-row tiles of the GEMM epilogues never reach another expert's rows.
 struct PrefillLayout {
-    size_t ctrl, logits, ids, wts, counts, offsets, poff, perm, pperm, inv, wp, xp, h, y, total;
+    size_t ctrl, wt, logits, ids, wts, counts, offsets, poff, perm, pperm, inv, wp, xp, h, y, total;
     int64_t rows;  // padded row capacity: T*k + 32*E
 };
 PrefillLayout prefill_layout(const si_moe_desc &d, int n_tokens);
@@ -99,6 +99,7 @@ struct PrefillArgs {
     int H, I, E, k, T;
     int64_t rows;      // padded row capacity of pperm/wp/xp/h/y
     int32_t *ctrl;
+    float *wt;         // [H][E] router weights transposed
     float *logits;     // [T][E]
     int32_t *ids;      // [T*k] pair p = t*k + slot
     float *wts;        // [T*k] renormalised routing weights

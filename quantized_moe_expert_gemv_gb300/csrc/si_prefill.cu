@@ -37,6 +37,7 @@
 // SI_ERR_RANGE instead of becoming infinite silently.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <cstdint>
@@ -50,123 +51,176 @@ namespace si {
 // =====================================================================
 // 1-3. Routing, counts, offsets, permutation
 // =====================================================================
+// W^T [H][Ew] (fp32) of the router weights, Ew = E rounded up to 128 (zero
+// columns), so a chunk of 32 hidden columns x 128 experts is one [32][128]
+// tile for the tensor-map copies of k_prefill_route.
+__device__ __forceinline__ int router_ew(int E) { return (E + 127) & ~127; }
+__global__ void __launch_bounds__(256) k_prefill_wt(PrefillArgs a) {
+    __shared__ float tile[32][33];
+    const int c0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    const int Ew = router_ew(a.E);
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    for (int r = ty; r < 32; r += 8)
+        tile[r][tx] = (e0 + r < a.E) ? __ldg(a.router_w + (size_t)(e0 + r) * a.H + c0 + tx) : 0.f;
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8) a.wt[(size_t)(c0 + r) * Ew + e0 + tx] = tile[tx][r];
+}
+
 namespace {
-constexpr int kRtTok = 32;      // tokens per router CTA
-constexpr int kRtExp = 128;     // experts per pass of the router tile
-constexpr int kRtKc = 32;       // hidden columns per staged chunk
+constexpr int kRtTok = 32;                   // tokens per router CTA
+constexpr int kRtExp = 128;                  // experts per pass
+constexpr int kRtKc = 32;                    // hidden columns per chunk
+constexpr int kRtNS = 4;                     // W^T chunk stages
 constexpr int kRtThreads = 256;
-constexpr int kRtXBytes = kRtKc * kRtTok * 4;
-constexpr int kRtWBytes = kRtExp * (kRtKc + 1) * 4;
-constexpr int kRtSmem = kRtXBytes + kRtWBytes + kRtTok * SI_MAX_EXPERTS * 4;  // 53,760
+constexpr int kRtW = kRtKc * kRtExp * 4;     // 16 KB: W^T chunk [32][128] fp32
+constexpr int kRtX = kRtKc * kRtTok * 8;     // 8 KB: x chunk as duplicated pairs [32][32] (x, x)
+constexpr int kRtOffX = kRtNS * kRtW;
+constexpr int kRtOffZ = kRtOffX + 2 * kRtX;  // logits [32][E] fp32
+constexpr int kRtOffBar = kRtOffZ + kRtTok * SI_MAX_EXPERTS * 4;
+constexpr int kRtSmem = kRtOffBar + kRtNS * 8 + 16 + 1024;
 }  // namespace
 
-// Logits of 32 tokens x all experts (fp32 FMA, hidden order), then per token
-// (one warp each) the top-k by k rounds of a warp-wide maximum (ties to the
-// lower index), the renormalised weights and the per-expert pair counts.
-__global__ void __launch_bounds__(kRtThreads) k_prefill_route(PrefillArgs a) {
-    extern __shared__ __align__(16) uint8_t rt_smem[];
-    float(*s_x)[kRtTok] = reinterpret_cast<float(*)[kRtTok]>(rt_smem);                            // [kRtKc][kRtTok]
-    float(*s_w)[kRtKc + 1] = reinterpret_cast<float(*)[kRtKc + 1]>(rt_smem + kRtXBytes);          // [kRtExp][kRtKc+1]
-    float(*s_z)[SI_MAX_EXPERTS] = reinterpret_cast<float(*)[SI_MAX_EXPERTS]>(rt_smem + kRtXBytes + kRtWBytes);
+// Logits of 32 tokens x all experts in fp32 (packed FMA, hidden order: the
+// router GEMV's arithmetic), W^T chunks streamed by tensor-map copies; then
+// one thread per token takes the top-k by insertion in expert order with a
+// strict comparison (descending logit, ties to the lower index), the
+// renormalised weights and the per-expert pair counts.
+template <int KM>
+__global__ void __launch_bounds__(kRtThreads)
+    k_prefill_route(const __grid_constant__ CUtensorMap tm_wt, PrefillArgs a) {
+    extern __shared__ uint8_t rt_smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(rt_smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, te = tid & 31, tt = tid >> 5;  // experts 4te..4te+3, tokens 4tt..4tt+3
     const int t0 = blockIdx.x * kRtTok;
-    const int tid = threadIdx.x, te = tid & 31, tt = tid >> 5;  // experts te + 32i, tokens 4tt..4tt+3
+    const int nch = a.H / kRtKc;
+    // every CTA reads all of W^T: CTA b walks the chunks from (3b) mod nch, so
+    // the CTAs do not all request the same L2 lines at the same moment
+    const int rot = (3 * blockIdx.x) % nch;
+    const uint32_t full = smem_addr(sm + kRtOffBar);
+    float(*s_z)[SI_MAX_EXPERTS] = reinterpret_cast<float(*)[SI_MAX_EXPERTS]>(sm + kRtOffZ);
+    int32_t *status = a.ctrl + kCtrlStatus;
+    if (tid == 0) {
+        prefetch_tensormap(&tm_wt);
+        for (int s = 0; s < kRtNS; ++s) mbar_init(full + 8 * s, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    int step = 0;  // chunk copies issued so far (over all expert passes)
     for (int e0 = 0; e0 < a.E; e0 += kRtExp) {
-        float acc[4][4];
+        const int base = step;
+        auto issue = [&](int j) {  // chunk j of this expert pass into stage (base + j) % NS
+            const int q = base + j, s = q % kRtNS;
+            mbar_arrive_expect_tx(full + 8 * s, kRtW);
+            tma_load_2d_plain(smem_addr(sm + s * kRtW), &tm_wt, e0, kRtKc * ((j + rot) % nch), full + 8 * s);
+        };
+        if (tid == 0)
+            for (int j = 0; j < min(kRtNS, nch); ++j) issue(j);
+        f32x2 acc[4][2], tot[4][2];  // [token j][expert pair]: per 256 columns, and the total
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-        for (int c0 = 0; c0 < a.H; c0 += kRtKc) {
-            for (int q = tid; q < kRtExp * kRtKc; q += kRtThreads) {
-                const int r = q / kRtKc, c = q - r * kRtKc;
-                s_w[r][c] = (e0 + r < a.E) ? __ldg(a.router_w + (size_t)(e0 + r) * a.H + c0 + c) : 0.f;
+        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = tot[j][0] = tot[j][1] = pack2(0.f, 0.f);
+        const int tk = tid >> 3, c4 = (tid & 7) * 4;  // this thread's x elements of a chunk
+        const bool tok_ok = t0 + tk < a.T;
+        const uint2 *xrow = reinterpret_cast<const uint2 *>(a.x + (size_t)(tok_ok ? t0 + tk : 0) * a.H + c4);
+        uint2 raw_next = tok_ok ? __ldg(xrow + (kRtKc / 4) * rot) : make_uint2(0u, 0u);
+        for (int j = 0; j < nch; ++j) {
+            // x chunk (bf16) -> duplicated fp32 pairs [c][token]; the next chunk's x is in flight meanwhile
+            f32x2 *xd = reinterpret_cast<f32x2 *>(sm + kRtOffX + (j & 1) * kRtX);
+            {
+                const uint2 raw = raw_next;
+                if (j + 1 < nch && tok_ok) raw_next = __ldg(xrow + (kRtKc / 4) * ((j + 1 + rot) % nch));
+                const float f0 = __uint_as_float(raw.x << 16), f1 = __uint_as_float(raw.x & 0xffff0000u);
+                const float f2 = __uint_as_float(raw.y << 16), f3 = __uint_as_float(raw.y & 0xffff0000u);
+                xd[(c4 + 0) * kRtTok + tk] = pack2(f0, f0);
+                xd[(c4 + 1) * kRtTok + tk] = pack2(f1, f1);
+                xd[(c4 + 2) * kRtTok + tk] = pack2(f2, f2);
+                xd[(c4 + 3) * kRtTok + tk] = pack2(f3, f3);
             }
-            for (int q = tid; q < kRtTok * kRtKc; q += kRtThreads) {
-                const int tk = q / kRtKc, c = q - tk * kRtKc;
-                const int t = t0 + tk;
-                s_x[c][tk] = t < a.T ? __uint_as_float((uint32_t)__ldg(a.x + (size_t)t * a.H + c0 + c) << 16) : 0.f;
-            }
+            const int q = base + j, s = q % kRtNS;
+            if (!mbar_wait_warp(full + 8 * s, (q / kRtNS) & 1, a.wait_budget)) set_status(status, SI_ERR_TIMEOUT);
             __syncthreads();
-#pragma unroll 8
+            const float *wt = reinterpret_cast<const float *>(sm + s * kRtW);
+#pragma unroll 4
             for (int c = 0; c < kRtKc; ++c) {
-                const float4 xv = *reinterpret_cast<const float4 *>(&s_x[c][4 * tt]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float w = s_w[te + 32 * i][c];
-                    acc[i][0] = fmaf(w, xv.x, acc[i][0]);
-                    acc[i][1] = fmaf(w, xv.y, acc[i][1]);
-                    acc[i][2] = fmaf(w, xv.z, acc[i][2]);
-                    acc[i][3] = fmaf(w, xv.w, acc[i][3]);
-                }
+                const float4 w = *reinterpret_cast<const float4 *>(wt + c * kRtExp + 4 * te);
+                const f32x2 w01 = pack2(w.x, w.y), w23 = pack2(w.z, w.w);
+                const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(xd + c * kRtTok + 4 * tt);
+                const ulonglong2 xb = *reinterpret_cast<const ulonglong2 *>(xd + c * kRtTok + 4 * tt + 2);
+                ffma2(acc[0][0], xa.x, w01);
+                ffma2(acc[0][1], xa.x, w23);
+                ffma2(acc[1][0], xa.y, w01);
+                ffma2(acc[1][1], xa.y, w23);
+                ffma2(acc[2][0], xb.x, w01);
+                ffma2(acc[2][1], xb.x, w23);
+                ffma2(acc[3][0], xb.y, w01);
+                ffma2(acc[3][1], xb.y, w23);
             }
-            __syncthreads();
+            if ((j & 7) == 7 || j == nch - 1) {  // two-level sum: shorter fp32 accumulation chains
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        const float2 p = unpack2(acc[u][v]), q = unpack2(tot[u][v]);
+                        tot[u][v] = pack2(q.x + p.x, q.y + p.y);
+                        acc[u][v] = pack2(0.f, 0.f);
+                    }
+            }
+            __syncthreads();  // stage s and x buffer free
+            if (tid == 0 && j + kRtNS < nch) issue(j + kRtNS);
         }
+        step = base + nch;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int e = e0 + te + 32 * i;
-            if (e < a.E) {
-                const float b = a.router_bias ? __ldg(a.router_bias + e) : 0.f;
+        for (int j = 0; j < 4; ++j) {
+            const float2 p0 = unpack2(tot[j][0]), p1 = unpack2(tot[j][1]);
+            const float v[4] = {p0.x, p0.y, p1.x, p1.y};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) s_z[4 * tt + j][e] = a.router_bias ? acc[i][j] + b : acc[i][j];
+            for (int i = 0; i < 4; ++i) {
+                const int e = e0 + 4 * te + i;
+                if (e < a.E) s_z[4 * tt + j][e] = a.router_bias ? v[i] + __ldg(a.router_bias + e) : v[i];
             }
         }
     }
     __syncthreads();
-    // top-k: warp w takes tokens w, w+8, w+16, w+24
-    const int lane = tid & 31, warp = tid >> 5;
-    const int per = (a.E + 31) >> 5;
-    for (int tk = warp; tk < kRtTok; tk += kRtThreads / 32) {
-        const int t = t0 + tk;
-        if (t >= a.T) break;
-        const float *z = s_z[tk];
-        if (a.o_logits)
-            for (int e = lane; e < a.E; e += 32) a.o_logits[(size_t)t * a.E + e] = z[e];
-        // lane l holds experts per*l .. per*l+per-1 as order-preserving keys (0 = taken)
-        uint32_t key[8];
+    if (tid < kRtTok) {
+        const int t = t0 + tid;
+        if (t < a.T) {
+            const float *z = s_z[tid];
+            float top[KM];
+            int tix[KM];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int e = per * lane + q;
-            uint32_t u = 0;
-            if (q < per && e < a.E) {
-                const uint32_t b = __float_as_uint(z[e] + 0.0f);
-                u = max((b & 0x80000000u) ? ~b : (b | 0x80000000u), 1u);
+            for (int i = 0; i < KM; ++i) top[i] = -INFINITY, tix[i] = 0x7fffffff;
+            for (int e = 0; e < a.E; ++e) {
+                const float ze = z[e];
+                if (a.o_logits) a.o_logits[(size_t)t * a.E + e] = ze;
+                if (ze > top[KM - 1] || tix[KM - 1] == 0x7fffffff) {  // insertion; strict: ties keep the lower index
+                    float cz = ze;
+                    int ci = e;
+#pragma unroll
+                    for (int i = 0; i < KM; ++i) {
+                        if (cz > top[i] || tix[i] == 0x7fffffff) {
+                            const float tz = top[i];
+                            const int ti = tix[i];
+                            top[i] = cz, tix[i] = ci;
+                            cz = tz, ci = ti;
+                        }
+                    }
+                }
             }
-            key[q] = u;
-        }
-        int my_id = 0;
-        float my_z = 0.f;
-        for (int r = 0; r < a.k; ++r) {
-            uint32_t best = 0;
-            int bq = 0;
+            float den = 0.f;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (key[q] > best) best = key[q], bq = q;
-            const uint32_t top = __reduce_max_sync(0xffffffffu, best);
-            const int win = __ffs(__ballot_sync(0xffffffffu, best == top)) - 1;
-            const int wq = __shfl_sync(0xffffffffu, bq, win);
-            if (lane == win) {
+            for (int i = 0; i < KM; ++i)
+                if (i < a.k) den += expf(top[i] - top[0]);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (q == wq) key[q] = 0u;
+            for (int i = 0; i < KM; ++i) {
+                if (i < a.k) {
+                    const size_t p = (size_t)t * a.k + i;
+                    const float w = expf(top[i] - top[0]) / den;
+                    a.ids[p] = tix[i];
+                    a.wts[p] = w;
+                    if (a.o_ids) a.o_ids[p] = tix[i];
+                    if (a.o_w) a.o_w[p] = w;
+                    atomicAdd(a.counts + tix[i], 1);
+                }
             }
-            if (lane == r) {
-                my_id = per * win + wq;
-                my_z = z[my_id];
-            }
-        }
-        const float z0 = __shfl_sync(0xffffffffu, my_z, 0);
-        const float ex = lane < a.k ? expf(my_z - z0) : 0.f;
-        float den = ex;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        if (lane < a.k) {
-            const size_t p = (size_t)t * a.k + lane;
-            const float w = ex / den;
-            a.ids[p] = my_id;
-            a.wts[p] = w;
-            if (a.o_ids) a.o_ids[p] = my_id;
-            if (a.o_w) a.o_w[p] = w;
-            atomicAdd(a.counts + my_id, 1);
         }
     }
 }
@@ -296,19 +350,20 @@ __global__ void __launch_bounds__(256) k_prefill_combine(PrefillArgs a) {
 namespace {
 constexpr int kGW = 16;                    // warps (see the role map in k_prefill_gemm)
 constexpr int kGThreads = kGW * 32;
-constexpr int kNS = 2;                     // operand stages (64-wide K steps)
+constexpr int kNA = 3;                     // dequantized operand-A stages (64-wide K steps)
+constexpr int kNB = 3;                     // operand-B (token) stages
 constexpr int kNR = 2;                     // raw Q4_K stages (256-wide K blocks)
-constexpr int kMaxTok = 512;               // tokens per pass: two 256-column accumulators
+constexpr int kMaxTok = 320;               // tokens per pass (256 + 64 accumulator columns)
 constexpr int kBoxTok = 64;                // token rows per operand-B tensor box
 constexpr int kATile = 128 * 128;          // 128 weight rows x 64 fp16
-constexpr int kBTile = kMaxTok * 128;      // up to 512 token rows x 64 fp16
-constexpr int kStage = kATile + kBTile;
+constexpr int kBTile = kMaxTok * 128;      // up to 320 token rows x 64 fp16
 constexpr int kRaw = 128 * kBlockBytes;    // 128 weight rows x one Q4_K block
-constexpr int kStg = 32 * 128 * 4;         // epilogue staging: 32 rows x 128 fp32 (or 32 x 64 fp16)
-constexpr int kOffRaw = kNS * kStage;
+constexpr int kStgBuf = 8192;              // epilogue staging buffer: 32 x 64 fp16, or 16 x 128 fp32
+constexpr int kOffB = kNA * kATile;
+constexpr int kOffRaw = kOffB + kNB * kBTile;
 constexpr int kOffStg = kOffRaw + kNR * kRaw;
-constexpr int kOffBar = kOffStg + kStg;
-constexpr int kNBar = 2 * kNR + 3 * kNS + 4 + 1;
+constexpr int kOffBar = kOffStg + 2 * kStgBuf;
+constexpr int kNBar = 2 * kNR + 2 * kNA + 2 * kNB + 4 + 1;
 constexpr int kGemmSmem = kOffBar + kNBar * 8 + 16 + 1024;  // + alignment slack
 constexpr long long kDrainG = 4000000000LL;
 
@@ -325,13 +380,15 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, int x, int y, uin
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // The sequence of work every role walks through in the same order: units
 // (expert, row tile) strided over the grid, each in passes of <= 512 tokens.
 struct Pass {
     int e, tile, prow, sc, nt;  // expert, row tile, first padded row of the expert, first token, tokens
+    int rot;                    // K steps are taken from (kb + rot) % nK: the CTAs working on one expert
+                                // start at different Q4_K blocks and so read different token columns
 };
 }  // namespace
 
@@ -340,8 +397,8 @@ struct Pass {
 //   epilogue h[row][tile*64 + i] = fp16(silu(g_i) * u_i).
 // MODE 1 (down): A rows = down rows tile*128..; K = I; B rows = h rows of
 //   the expert; epilogue y[row][tile*128 + i] = wp[row] * acc.
-// Roles: warp 0 tensor-map copies (Q4_K blocks, B tiles), warp 1 MMA issue
-// and tensor-memory allocation, warps 4-11 dequantization, warps 12-15
+// Roles: warp 0 Q4_K block copies, warp 2 operand-B tile copies, warp 1 MMA
+// issue and tensor-memory allocation, warps 4-11 dequantization, warps 12-15
 // epilogue (accumulators double-buffered: the epilogue of one 256-token chunk
 // overlaps the MMAs of the next).
 template <int MODE>
@@ -363,8 +420,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
     const uint32_t bar0 = smem_addr(sm + kOffBar);
     const uint32_t raw_full = bar0, raw_empty = bar0 + 8 * kNR;
-    const uint32_t full_a = bar0 + 16 * kNR, full_b = full_a + 8 * kNS, empty = full_b + 8 * kNS;
-    const uint32_t d_full = empty + 8 * kNS, d_empty = d_full + 16, fin = d_empty + 16;  // d_*: [2]
+    const uint32_t full_a = bar0 + 16 * kNR, empty_a = full_a + 8 * kNA;
+    const uint32_t full_b = empty_a + 8 * kNA, empty_b = full_b + 8 * kNB;
+    const uint32_t d_full = empty_b + 8 * kNB, d_empty = d_full + 16, fin = d_empty + 16;  // d_*: [2]
     volatile int *verr = &s_err;
 
     if (threadIdx.x == 0) {
@@ -377,10 +435,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
             mbar_init(raw_full + 8 * r, 1);
             mbar_init(raw_empty + 8 * r, 8);
         }
-        for (int s = 0; s < kNS; ++s) {
+        for (int s = 0; s < kNA; ++s) {
             mbar_init(full_a + 8 * s, 8);
+            mbar_init(empty_a + 8 * s, 1);
+        }
+        for (int s = 0; s < kNB; ++s) {
             mbar_init(full_b + 8 * s, 1);
-            mbar_init(empty + 8 * s, 1);
+            mbar_init(empty_b + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(d_full + 8 * b, 1);
@@ -403,7 +464,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
         for (int u = blockIdx.x; u < nU && !*verr; u += gridDim.x) {
             const int e = u / tiles, tile = u - e * tiles;
             const int ne = __ldg(a.counts + e), prow = __ldg(a.poff + e);
-            for (int sc = 0; sc < ne && !*verr; sc += kMaxTok) body(Pass{e, tile, prow, sc, min(kMaxTok, ne - sc)});
+            const int rot = 4 * (tile % (nK / 4));
+            for (int sc = 0; sc < ne && !*verr; sc += kMaxTok)
+                body(Pass{e, tile, prow, sc, min(kMaxTok, ne - sc), rot});
         }
     };
     auto fail = [&]() {
@@ -412,48 +475,56 @@ __global__ void __launch_bounds__(kGThreads, 1)
     };
 
     if (warp == 0) {
-        // ------------------------------------------------ tensor-map copies
+        // ------------------------------------------------ Q4_K weight blocks (tensor-map copies)
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();  // each Q4_K block is read by one CTA
-            int rstep = 0, step = 0;
+            int rstep = 0;
             for_each_pass([&](const Pass &ps) {
-                const int nbox = (ps.nt + kBoxTok - 1) / kBoxTok;
-                for (int kb = 0; kb < nK; ++kb, ++step) {
-                    if ((kb & 3) == 0) {  // next Q4_K block of the 128 weight rows
-                        const int r = rstep % kNR;
-                        if (rstep >= kNR && !mbar_wait_bounded(raw_empty + 8 * r, ((rstep / kNR) - 1) & 1, budget)) {
-                            fail();
-                            return;
-                        }
-                        const uint32_t dst = smem_addr(sm + kOffRaw + r * kRaw);
-                        mbar_arrive_expect_tx(raw_full + 8 * r, kRaw);
-                        if (MODE == 0) {
-                            const int y = ps.e * a.I + ps.tile * 64;
-                            tma_load_2d(dst, &tm_a0, kBlockBytes * (kb >> 2), y, raw_full + 8 * r, pol);
-                            tma_load_2d(dst + 64 * kBlockBytes, &tm_a1, kBlockBytes * (kb >> 2), y, raw_full + 8 * r, pol);
-                        } else {
-                            tma_load_2d(dst, &tm_a0, kBlockBytes * (kb >> 2), ps.e * a.H + ps.tile * 128,
-                                        raw_full + 8 * r, pol);
-                        }
-                        ++rstep;
-                    }
-                    const int s = step % kNS;
-                    if (step >= kNS && !mbar_wait_bounded(empty + 8 * s, ((step / kNS) - 1) & 1, budget)) {
+                for (int bi = 0; bi < nK / 4; ++bi, ++rstep) {
+                    const int blk = ((4 * bi + ps.rot) % nK) >> 2;
+                    const int r = rstep % kNR;
+                    if (rstep >= kNR && !mbar_wait_bounded(raw_empty + 8 * r, ((rstep / kNR) - 1) & 1, budget)) {
                         fail();
                         return;
                     }
-                    const uint32_t bt = smem_addr(sm + s * kStage + kATile);
+                    const uint32_t dst = smem_addr(sm + kOffRaw + r * kRaw);
+                    mbar_arrive_expect_tx(raw_full + 8 * r, kRaw);
+                    if (MODE == 0) {
+                        const int y = ps.e * a.I + ps.tile * 64;
+                        tma_load_2d(dst, &tm_a0, kBlockBytes * blk, y, raw_full + 8 * r, pol);
+                        tma_load_2d(dst + 64 * kBlockBytes, &tm_a1, kBlockBytes * blk, y, raw_full + 8 * r, pol);
+                    } else {
+                        tma_load_2d(dst, &tm_a0, kBlockBytes * blk, ps.e * a.H + ps.tile * 128, raw_full + 8 * r, pol);
+                    }
+                }
+            });
+            // drain: every issued block has landed before the CTA exits
+            for (int q = (rstep > kNR ? rstep - kNR : 0); q < rstep; ++q)
+                mbar_wait_bounded(raw_full + 8 * (q % kNR), (q / kNR) & 1, kDrainG);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------ operand-B tiles (tensor-map copies)
+        if (lane == 0) {
+            int step = 0;
+            for_each_pass([&](const Pass &ps) {
+                const int nbox = (ps.nt + kBoxTok - 1) / kBoxTok;
+                for (int kb = 0; kb < nK; ++kb, ++step) {
+                    const int s = step % kNB;
+                    if (step >= kNB && !mbar_wait_bounded(empty_b + 8 * s, ((step / kNB) - 1) & 1, budget)) {
+                        fail();
+                        return;
+                    }
+                    const uint32_t bt = smem_addr(sm + kOffB + s * kBTile);
                     mbar_arrive_expect_tx(full_b + 8 * s, (uint32_t)(nbox * kBoxTok * 128));
+                    const int kq = (kb + ps.rot) % nK;
                     for (int b = 0; b < nbox; ++b)
-                        tma_load_2d_plain(bt + b * kBoxTok * 128, &tm_b, 64 * kb, ps.prow + ps.sc + kBoxTok * b,
+                        tma_load_2d_plain(bt + b * kBoxTok * 128, &tm_b, 64 * kq, ps.prow + ps.sc + kBoxTok * b,
                                           full_b + 8 * s);
                 }
             });
-            // drain: every issued Q4_K block has landed before the CTA exits
-            for (int q = (rstep > kNR ? rstep - kNR : 0); q < rstep; ++q)
-                mbar_wait_bounded(raw_full + 8 * (q % kNR), (q / kNR) & 1, kDrainG);
-            for (int q = (step > kNS ? step - kNS : 0); q < step; ++q)
-                mbar_wait_bounded(full_b + 8 * (q % kNS), (q / kNS) & 1, kDrainG);
+            for (int q = (step > kNB ? step - kNB : 0); q < step; ++q)
+                mbar_wait_bounded(full_b + 8 * (q % kNB), (q / kNB) & 1, kDrainG);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -466,32 +537,32 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 const int nch = (ps.nt + 255) >> 8;
                 for (int c = 0; c < nch; ++c) {  // the accumulator buffers of this pass are drained
                     const int b = (chunk + c) & 1;
-                    if (uses[b] > 0 && !mbar_wait_bounded(d_empty + 8 * b, (uses[b] - 1) & 1, budget)) {
+                    if (uses[b] > 0 && !mbar_wait_spin(d_empty + 8 * b, (uses[b] - 1) & 1, budget)) {
                         fail();
                         return;
                     }
                 }
                 tc::fence_after_sync();
                 for (int kb = 0; kb < nK; ++kb, ++step) {
-                    const int s = step % kNS;
-                    const uint32_t par = (step / kNS) & 1;
-                    if (!mbar_wait_bounded(full_a + 8 * s, par, budget) || !mbar_wait_bounded(full_b + 8 * s, par, budget)) {
+                    const int sa = step % kNA, sb = step % kNB;
+                    if (!mbar_wait_spin(full_a + 8 * sa, (step / kNA) & 1, budget) ||
+                        !mbar_wait_spin(full_b + 8 * sb, (step / kNB) & 1, budget)) {
                         fail();
                         return;
                     }
-                    tc::fence_proxy_async_smem();  // the dequantized A tile was written through the generic proxy
-                    tc::fence_after_sync();
-                    const uint32_t at = smem_addr(sm + s * kStage);
+                    tc::fence_after_sync();  // the dequant warps fenced their A-tile writes to the async proxy
+                    const uint32_t at = smem_addr(sm + sa * kATile);
                     for (int c = 0; c < nch; ++c) {
                         const int nc = min(256, ps.nt - 256 * c);
                         const uint32_t idesc = tc::idesc_f16_f32(128, (nc + 15) & ~15);
-                        const uint32_t bt = at + kATile + c * 256 * 128;
+                        const uint32_t bt = smem_addr(sm + kOffB + sb * kBTile) + c * 256 * 128;
                         const uint32_t d = taddr + 256 * ((chunk + c) & 1);
                         for (int j = 0; j < 4; ++j)
                             tc::mma_f16kind(d, tc::sdesc_sw128(at + 32 * j), tc::sdesc_sw128(bt + 32 * j), idesc,
                                             kb > 0 || j > 0);
                     }
-                    tc::mma_commit(empty + 8 * s);
+                    tc::mma_commit(empty_a + 8 * sa);
+                    tc::mma_commit(empty_b + 8 * sb);
                     issued = true;
                 }
                 for (int c = 0; c < nch; ++c) {
@@ -516,14 +587,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
         int astep = 0, rstep = 0;
         for_each_pass([&](const Pass &ps) {
             for (int kb = 0; kb < nK; ++kb, ++astep) {
-                const int j = kb & 3;
+                const int j = kb & 3;  // the rotation is whole Q4_K blocks, so chunk j of a block is kb & 3
                 const int r = rstep % kNR;
                 if (j == 0 && !mbar_wait_warp(raw_full + 8 * r, (rstep / kNR) & 1, budget)) {
                     fail();
                     return;
                 }
-                const int s = astep % kNS;
-                if (astep >= kNS && !mbar_wait_warp(empty + 8 * s, ((astep / kNS) - 1) & 1, budget)) {
+                const int s = astep % kNA;
+                if (astep >= kNA && !mbar_wait_warp(empty_a + 8 * s, ((astep / kNA) - 1) & 1, budget)) {
                     fail();
                     return;
                 }
@@ -550,7 +621,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     o[2 * t] = f16x2_rn(f0, f1);
                     o[2 * t + 1] = f16x2_rn(f2, f3);
                 }
-                uint8_t *at = sm + s * kStage + row * 128;
+                uint8_t *at = sm + s * kATile + row * 128;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int chunk = (4 * half + c) ^ (row & 7);
@@ -568,11 +639,27 @@ __global__ void __launch_bounds__(kGThreads, 1)
         });
     } else if (warp >= 12) {
         // ------------------------------------------------ epilogue (warps 12-15)
+        // Results go through two 8 KB staging buffers and tensor-map stores of
+        // 32 rows x 64 fp16 (h) or 16 rows x 128 fp32 (y); a buffer is rewritten
+        // once the store issued from it two stores earlier has read it.
         const int ew = warp - 12;  // tensor-memory lanes 32*ew ..
         const bool lead = threadIdx.x == 12 * 32;
-        uint8_t *stg = sm + kOffStg;
-        int chunk = 0;
+        int chunk = 0, nst = 0;
         int uses[2] = {0, 0};
+        auto stage_begin = [&]() -> uint8_t * {
+            if (lead && nst >= 2) bulk_wait_read1();
+            asm volatile("bar.sync 4, 128;" ::: "memory");
+            return sm + kOffStg + (nst & 1) * kStgBuf;
+        };
+        auto stage_end = [&](uint8_t *buf, int x, int y) {
+            tc::fence_proxy_async_smem();
+            asm volatile("bar.sync 4, 128;" ::: "memory");
+            if (lead) {
+                tma_store_2d(&tm_out, x, y, smem_addr(buf));
+                bulk_commit();
+            }
+            ++nst;
+        };
         for_each_pass([&](const Pass &ps) {
             const int nch = (ps.nt + 255) >> 8;
             for (int c = 0; c < nch; ++c, ++chunk) {
@@ -589,39 +676,43 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     tc::tmem_ld32(taddr + ((uint32_t)(32 * ew) << 16) + 256 * b + col0, v);
                     tc::tmem_wait_ld();
                     const int row0 = ps.prow + ps.sc + 256 * c + col0;  // padded row of token col0
+                    // rows past the expert's tokens land in its own padding (poff is 32-aligned)
                     if (MODE == 0) {
                         // lanes 2i / 2i+1 hold g / u of intermediate row i for 32 tokens;
                         // the even lane forms h for tokens 0-15, the odd lane for 16-31
-                        uint16_t *hs = reinterpret_cast<uint16_t *>(stg);  // [32 tokens][64] fp16
+                        uint16_t *hs = reinterpret_cast<uint16_t *>(stage_begin());  // [32 tokens][64] fp16
                         const int up = lane & 1;
                         const int il = 16 * ew + (lane >> 1);
+                        float hv[16];
+                        bool big = false;
 #pragma unroll
                         for (int q = 0; q < 16; ++q) {
                             const float send = __uint_as_float(up ? v[q] : v[q + 16]);
                             const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
                             const float gg = up ? recv : __uint_as_float(v[q]);
                             const float uu = up ? __uint_as_float(v[q + 16]) : recv;
-                            const float hv = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
+                            hv[q] = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
                             // columns past the pass's tokens hold stale accumulators: not checked
-                            if (col0 + q + 16 * up < nc && fabsf(hv) > 65504.f) set_status(status, SI_ERR_RANGE);
-                            hs[(q + 16 * up) * 64 + il] = __half_as_ushort(__float2half_rn(hv));
+                            big |= (col0 + q + 16 * up < nc) & (fabsf(hv[q]) > 65504.f);
                         }
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) hs[(q + 16 * up) * 64 + il] = __half_as_ushort(__float2half_rn(hv[q]));
+                        if (big) set_status(status, SI_ERR_RANGE);
+                        stage_end(reinterpret_cast<uint8_t *>(hs), ps.tile * 64, row0);
                     } else {
-                        float *ys = reinterpret_cast<float *>(stg);  // [32 tokens][128] fp32
                         const float wl = __ldg(a.wp + row0 + lane);  // weight of token col0 + lane (0 on padding)
 #pragma unroll
-                        for (int q = 0; q < 32; ++q)
-                            ys[q * 128 + 32 * ew + lane] = __shfl_sync(0xffffffffu, wl, q) * __uint_as_float(v[q]);
+                        for (int hf = 0; hf < 2; ++hf) {
+                            float yv[16];
+#pragma unroll
+                            for (int q = 0; q < 16; ++q)
+                                yv[q] = __shfl_sync(0xffffffffu, wl, 16 * hf + q) * __uint_as_float(v[16 * hf + q]);
+                            float *ys = reinterpret_cast<float *>(stage_begin());  // [16 tokens][128] fp32
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) ys[q * 128 + 32 * ew + lane] = yv[q];
+                            stage_end(reinterpret_cast<uint8_t *>(ys), ps.tile * 128, row0 + 16 * hf);
+                        }
                     }
-                    // rows past the expert's tokens land in its own padding (poff is 32-aligned)
-                    tc::fence_proxy_async_smem();
-                    asm volatile("bar.sync 4, 128;" ::: "memory");
-                    if (lead) {
-                        tma_store_2d(&tm_out, MODE == 0 ? ps.tile * 64 : ps.tile * 128, row0, smem_addr(stg));
-                        bulk_commit();
-                        bulk_wait_read0();
-                    }
-                    asm volatile("bar.sync 4, 128;" ::: "memory");
                 }
                 tc::fence_before_sync();
                 __syncwarp();
@@ -689,7 +780,9 @@ static bool mat_map(const void *base, int64_t rows, int cols, int esize, int box
 cudaError_t prefill_prepare(const Plan &p) {
     (void)p;
     if (!encoder()) return cudaErrorNotSupported;
-    cudaError_t err = cudaFuncSetAttribute(k_prefill_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+    cudaError_t err = cudaFuncSetAttribute(k_prefill_route<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(k_prefill_route<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(k_prefill_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
     if (err != cudaSuccess) return err;
@@ -710,7 +803,15 @@ cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, 
     cudaError_t err;
     if ((err = mark(events, 0, s)) != cudaSuccess) return err;
     if ((err = cudaMemsetAsync(a.counts, 0, sizeof(int32_t) * a.E, s)) != cudaSuccess) return err;
-    k_prefill_route<<<(a.T + kRtTok - 1) / kRtTok, kRtThreads, kRtSmem, s>>>(a);
+    const int Ew = (a.E + 127) & ~127;
+    k_prefill_wt<<<dim3(a.H / 32, Ew / 32), 256, 0, s>>>(a);
+    {
+        CUtensorMap twt;
+        if (!mat_map(a.wt, a.H, Ew, 4, kRtExp, kRtKc, false, &twt)) return cudaErrorInvalidValue;
+        const int grid = (a.T + kRtTok - 1) / kRtTok;
+        if (a.k <= 8) k_prefill_route<8><<<grid, kRtThreads, kRtSmem, s>>>(twt, a);
+        else k_prefill_route<16><<<grid, kRtThreads, kRtSmem, s>>>(twt, a);
+    }
     k_prefill_scan<<<1, 256, 0, s>>>(a);
     k_prefill_perm<<<a.E, 1024, 0, s>>>(a);
 
@@ -722,7 +823,7 @@ cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, 
     if (!q4k_map(a.wg, (int64_t)a.E * a.I, a.H / kQK, 64, &tg) || !q4k_map(a.wu, (int64_t)a.E * a.I, a.H / kQK, 64, &tu) ||
         !q4k_map(a.wd, (int64_t)a.E * a.H, a.I / kQK, 128, &td) ||
         !mat_map(a.xp, a.rows, a.H, 2, 64, kBoxTok, true, &txp) || !mat_map(a.h, a.rows, a.I, 2, 64, kBoxTok, true, &thl) ||
-        !mat_map(a.h, a.rows, a.I, 2, 64, 32, false, &ths) || !mat_map(a.y, a.rows, a.H, 4, 128, 32, false, &tys))
+        !mat_map(a.h, a.rows, a.I, 2, 64, 32, false, &ths) || !mat_map(a.y, a.rows, a.H, 4, 128, 16, false, &tys))
         return cudaErrorInvalidValue;
     const int grid = p.sm_count;
     k_prefill_gemm<0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp, ths, a);
