@@ -79,7 +79,6 @@ PrefillLayout prefill_layout(const si_moe_desc &d, int n) {
     L.perm = take(pairs * sizeof(int32_t));
     L.pperm = take(rows * sizeof(int32_t));
     L.inv = take(pairs * sizeof(int32_t));
-    L.wp = take(rows * sizeof(float));
     L.xp = take(rows * d.hidden * sizeof(uint16_t));
     L.h = take(rows * d.intermediate * sizeof(uint16_t));
     L.y = take(rows * d.hidden * sizeof(float));
@@ -325,7 +324,6 @@ static si_status forward_prefill_impl(si_moe_plan_t plan, const si_moe_layer *la
     a.perm = reinterpret_cast<int32_t *>(sb + L.perm);
     a.pperm = reinterpret_cast<int32_t *>(sb + L.pperm);
     a.inv = reinterpret_cast<int32_t *>(sb + L.inv);
-    a.wp = reinterpret_cast<float *>(sb + L.wp);
     a.xp = reinterpret_cast<uint16_t *>(sb + L.xp);
     a.h = reinterpret_cast<uint16_t *>(sb + L.h);
     a.y = reinterpret_cast<float *>(sb + L.y);

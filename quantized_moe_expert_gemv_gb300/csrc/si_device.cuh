@@ -347,6 +347,55 @@ __device__ __forceinline__ void st_cluster_f32(const void *local, uint32_t rank,
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Address in the cluster window of the shared-memory word that has address
+// `local` in this CTA, as seen in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+// Arrive (release at cluster scope) on an mbarrier given by its cluster-window
+// address, in this CTA or another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// try_wait with acquire at cluster scope: for phases completed by arrivals of
+// other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_spin_cluster(uint32_t bar, uint32_t parity, long long budget) {
+    const long long t0 = clock64();
+    for (int n = 0;; ++n) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((n & 63) == 63 && clock64() - t0 > budget) return false;
+    }
+}
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity, long long budget) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (clock64() - t0 > budget) return false;
+        __nanosleep(20);
+    }
+}
+// Whole warp: lane 0 polls, then every lane takes one acquiring try_wait.
+__device__ __forceinline__ bool mbar_wait_warp_cluster(uint32_t bar, uint32_t parity, long long budget) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded_cluster(bar, parity, budget);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) ok = mbar_wait_bounded_cluster(bar, parity, budget);
+    return __all_sync(0xffffffffu, ok);
+}
 
 }  // namespace si
 

@@ -86,7 +86,7 @@ struct DecodeArgs {
 // Each expert's rows start at a multiple of 32 (padded offsets poff), so the
 // 32-row tiles of the GEMM epilogues never reach another expert's rows.
 struct PrefillLayout {
-    size_t ctrl, wt, logits, ids, wts, counts, offsets, poff, perm, pperm, inv, wp, xp, h, y, total;
+    size_t ctrl, wt, logits, ids, wts, counts, offsets, poff, perm, pperm, inv, xp, h, y, total;
     int64_t rows;  // padded row capacity: T*k + 32*E
 };
 PrefillLayout prefill_layout(const si_moe_desc &d, int n_tokens);
@@ -97,7 +97,7 @@ struct PrefillArgs {
     const uint16_t *x;  // [T][H] bf16 bits
     float *out;         // [T][H]
     int H, I, E, k, T;
-    int64_t rows;      // padded row capacity of pperm/wp/xp/h/y
+    int64_t rows;      // padded row capacity of pperm/xp/h/y
     int32_t *ctrl;
     float *wt;         // [H][E] router weights transposed
     float *logits;     // [T][E]
@@ -109,10 +109,9 @@ struct PrefillArgs {
     int32_t *perm;     // [T*k] pair ids ordered by expert, then pair id
     int32_t *pperm;    // [rows] pair id of each padded row (-1 = padding)
     int32_t *inv;      // [T*k] padded row of each pair
-    float *wp;         // [rows] routing weight of each padded row (0 = padding)
     uint16_t *xp;      // [rows][H] fp16 bits: x of each padded row's token
     uint16_t *h;       // [rows][I] fp16 bits
-    float *y;          // [rows][H] fp32
+    float *y;          // [rows][H] fp32, before the routing weight
     int32_t *o_ids;
     float *o_w;
     int32_t *o_counts, *o_offsets, *o_perm;

@@ -12,21 +12,23 @@
 //   2. k_prefill_scan    offsets[E+1] = exclusive scan of the counts
 //   3. k_prefill_perm    perm: pair ids t*k+slot ordered by expert, then pair
 //                        id (stable); inv: each pair's position in perm
-//   4. k_prefill_gemm<0> per (expert, 64 intermediate rows): [gate; up] rows
-//                        (M = 128) x the expert's tokens (N <= 512 per pass)
+//   4. k_prefill_gemm<0> per (expert, 128 intermediate rows): [gate; up] rows
+//                        (M = 256) x the expert's tokens (N <= 384 per pass)
 //                        over K = H, then h = fp16(silu(g) * u) in perm order
-//   5. k_prefill_gemm<1> per (expert, 128 output rows): down rows x the
+//   5. k_prefill_gemm<1> per (expert, 256 output rows): down rows x the
 //                        expert's h rows over K = I, times the routing weight,
 //                        into y (fp32, perm order)
-//   6. k_prefill_combine out[t] = sum over slots, in slot order, of y[inv[t*k+s]]
+//   6. k_prefill_combine out[t] = sum over slots, in slot order, of w[t][s] * y[inv[t*k+s]]
 //
-// The GEMMs run on the 5th-generation tensor cores: 16-bit operands in shared
-// memory (K-major, 128-byte swizzle), fp32 accumulators in tensor memory.
-// Weights (operand A) are Q4_K blocks fetched by tensor-map copies and
-// dequantized by eight warps: w = d*sc*q - dmin*m, exact in fp32, rounded once
-// to fp16 (nearest even).  Tokens (operand B) are gathered row by row with
-// 16-byte asynchronous copies.  One MMA thread issues 128 x N x 16 MMAs; a
-// warpgroup reads the accumulators back for the epilogue.
+// The GEMMs run on the 5th-generation tensor cores as CTA pairs: 16-bit
+// operands in shared memory (K-major, 128-byte swizzle), fp32 accumulators in
+// tensor memory.  Weights (operand A) are Q4_K blocks fetched by tensor-map
+// copies and dequantized by eight warps of each CTA: w = d*sc*q - dmin*m,
+// exact in fp32, rounded once to fp16 (nearest even).  Tokens (operand B) are
+// the expert's rows of a permuted copy of x (or of h), fetched by tensor-map
+// copies, each CTA of the pair holding half of them.  One thread of the pair
+// issues 256 x N x 16 MMAs; a warpgroup of each CTA reads its 128
+// accumulator rows back for the epilogue.
 //
 // Operand precision: fp16, not bf16.  Rounding the dequantized weights to
 // bf16 (8-bit mantissa) moves a token's layer output by up to ~5e-3 relative
@@ -266,7 +268,6 @@ __global__ void __launch_bounds__(1024) k_prefill_perm(PrefillArgs a) {
     const int np = a.T * a.k;
     for (int r = poff + a.counts[e] + tid; r < a.poff[e + 1]; r += blockDim.x) {  // padding rows
         a.pperm[r] = -1;
-        a.wp[r] = 0.f;
     }
     if (tid == 0) s_base = 0;
     __syncthreads();
@@ -285,7 +286,6 @@ __global__ void __launch_bounds__(1024) k_prefill_perm(PrefillArgs a) {
             if (a.o_perm) a.o_perm[off + j] = p;
             a.inv[p] = prow;
             a.pperm[prow] = p;
-            a.wp[prow] = a.wts[p];
         }
         __syncthreads();
         if (tid == 0) {
@@ -335,42 +335,81 @@ __global__ void __launch_bounds__(256) k_prefill_combine(PrefillArgs a) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < a.k; ++s) {
         const int pos = __ldg(a.inv + (size_t)t * a.k + s);
+        const float w = __ldg(a.wts + (size_t)t * a.k + s);
         const float4 v = __ldg(reinterpret_cast<const float4 *>(a.y + (size_t)pos * a.H) + c);
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
     }
     reinterpret_cast<float4 *>(a.out + (size_t)t * a.H)[c] = acc;
 }
 
 // =====================================================================
-// 4-5. Grouped GEMMs on the tensor cores
+// 4-5. Grouped GEMMs on the tensor cores, one CTA pair per work unit
 // =====================================================================
+// A work unit is (expert, row tile of 256 A rows); its two CTAs (ranks 0, 1
+// of a 2-CTA cluster, on two SMs) each dequantize 128 A rows and load half of
+// the expert's token rows, and the even CTA issues M = 256 pair MMAs that
+// read both CTAs' shared memory.  Each SM thus receives only half of the
+// token operand per K step: the copy engine delivers about 52 bytes per clock
+// into one SM from L2, which a single-CTA M = 128 tile with ~256 tokens
+// (32 KB of tokens per 64-wide K step) would exceed.
 namespace {
 constexpr int kGW = 16;                    // warps (see the role map in k_prefill_gemm)
 constexpr int kGThreads = kGW * 32;
-constexpr int kNA = 3;                     // dequantized operand-A stages (64-wide K steps)
-constexpr int kNB = 3;                     // operand-B (token) stages
+constexpr int kNS = 4;                     // operand stages (64-wide K steps): A (dequantized) + B (tokens)
 constexpr int kNR = 2;                     // raw Q4_K stages (256-wide K blocks)
-constexpr int kMaxTok = 320;               // tokens per pass (256 + 64 accumulator columns)
-constexpr int kBoxTok = 64;                // token rows per operand-B tensor box
+constexpr int kMaxTok = 384;               // tokens per pass: one chunk of <= 256 or two of <= 192
+constexpr int kChunkRows = 96;             // first operand-B row (per CTA) of the second chunk in a stage
+constexpr int kNBuf = 2;                   // accumulator buffers of 256 tensor-memory columns
+constexpr int kBRows = 192;                // operand-B rows per CTA and stage
 constexpr int kATile = 128 * 128;          // 128 weight rows x 64 fp16
-constexpr int kBTile = kMaxTok * 128;      // up to 320 token rows x 64 fp16
+constexpr int kBTile = kBRows * 128;       // 192 token rows x 64 fp16
 constexpr int kRaw = 128 * kBlockBytes;    // 128 weight rows x one Q4_K block
-constexpr int kStgBuf = 8192;              // epilogue staging buffer: 32 x 64 fp16, or 16 x 128 fp32
-constexpr int kOffB = kNA * kATile;
-constexpr int kOffRaw = kOffB + kNB * kBTile;
+constexpr int kOffB = kNS * kATile;
+constexpr int kOffRaw = kOffB + kNS * kBTile;
+constexpr int kStgBuf = 8192;              // MODE 0 epilogue staging buffer: 32 tokens x 64 fp16
 constexpr int kOffStg = kOffRaw + kNR * kRaw;
 constexpr int kOffBar = kOffStg + 2 * kStgBuf;
-constexpr int kNBar = 2 * kNR + 2 * kNA + 2 * kNB + 4 + 1;
-constexpr int kGemmSmem = kOffBar + kNBar * 8 + 16 + 1024;  // + alignment slack
+constexpr int kNBar = 2 * kNR + 2 * kNS + 2 * kNBuf + 2;
+constexpr int kOffTok = (kOffBar + kNBar * 8 + 15) & ~15;  // 16-byte readiness tokens [kNS][8], copied odd -> even CTA
+constexpr int kGemmSmem = kOffTok + 16 * 8 * kNS + 16 + 1024;  // + alignment slack
+static_assert(kGemmSmem + 64 <= 232448, "shared memory plan exceeds the per-CTA limit");
+static_assert(kATile % 1024 == 0 && kOffB % 1024 == 0 && kBTile % 1024 == 0 && (kChunkRows * 128) % 1024 == 0,
+              "128-byte-swizzled operand tiles start on 1024-byte boundaries");
+static_assert(kOffRaw % 128 == 0 && kRaw % 128 == 0 && kOffStg % 128 == 0 && kStgBuf % 128 == 0,
+              "tensor-map copy destinations and sources are 128-byte aligned");
+static_assert(kOffBar % 8 == 0 && kOffTok % 16 == 0, "mbarriers 8-byte, bulk-copy tokens 16-byte aligned");
 constexpr long long kDrainG = 4000000000LL;
+constexpr uint16_t kPairMask = 3;          // both CTAs of the pair
 
 __device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
-    const __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&v);
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// Tensor-map load into this CTA's shared memory that completes its bytes on
+// an mbarrier of either CTA of the pair (cluster-window address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
 // 2-D tensor store shared -> global (bulk-group completion), its commit and
 // the wait until the shared-memory source may be overwritten.
 __device__ __forceinline__ void tma_store_2d(const void *tmap, int x, int y, uint32_t src) {
@@ -383,35 +422,76 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// The sequence of work every role walks through in the same order: units
-// (expert, row tile) strided over the grid, each in passes of <= 512 tokens.
+// The sequence of work every role of both CTAs walks through in the same
+// order: units (expert, row tile) strided over the CTA pairs, each in passes
+// of <= kMaxTok tokens; a pass is one chunk of n <= 256 tokens or two of
+// n <= 192 (n a multiple of 32, so every chunk starts on a 32-row boundary of
+// the expert's padded rows and each CTA's half, n/2, is a multiple of 16).
+// Chunks are numbered globally in this order; chunk g accumulates in
+// tensor-memory buffer g % kNBuf, and chunk c of a pass is issued by MMA
+// thread c (see below).
 struct Pass {
     int e, tile, prow, sc, nt;  // expert, row tile, first padded row of the expert, first token, tokens
-    int rot;                    // K steps are taken from (kb + rot) % nK: the CTAs working on one expert
+    int nch, n;                 // chunks and tokens per chunk (the last chunk may hold fewer valid tokens)
+    int rot;                    // K steps are taken from (kb + rot) % nK: the pairs working on one expert
                                 // start at different Q4_K blocks and so read different token columns
 };
+__device__ __forceinline__ Pass make_pass(int e, int tile, int prow, int sc, int ne, int nK) {
+    Pass p;
+    p.e = e;
+    p.tile = tile;
+    p.prow = prow;
+    p.sc = sc;
+    p.nt = min(kMaxTok, ne - sc);
+    p.nch = p.nt <= 256 ? 1 : 2;
+    p.n = ((p.nt + p.nch - 1) / p.nch + 31) & ~31;
+    p.rot = 4 * (tile % (nK / 4));
+    return p;
+}
 }  // namespace
 
-// MODE 0 (gate/up): A row 2i = gate row tile*64+i, row 2i+1 = up row
-//   tile*64+i; K = H; B rows = padded token rows of the expert (xp);
-//   epilogue h[row][tile*64 + i] = fp16(silu(g_i) * u_i).
-// MODE 1 (down): A rows = down rows tile*128..; K = I; B rows = h rows of
-//   the expert; epilogue y[row][tile*128 + i] = wp[row] * acc.
-// Roles: warp 0 Q4_K block copies, warp 2 operand-B tile copies, warp 1 MMA
-// issue and tensor-memory allocation, warps 4-11 dequantization, warps 12-15
-// epilogue (accumulators double-buffered: the epilogue of one 256-token chunk
-// overlaps the MMAs of the next).
+// MODE 0 (gate/up): unit tile covers intermediate rows tile*128 .. +127;
+//   CTA r holds rows tile*128 + 64r + i as A rows 2i (gate) and 2i+1 (up);
+//   K = H; B rows = padded token rows of the expert (xp); epilogue
+//   h[row][tile*128 + 64r + i] = fp16(silu(g_i) * u_i).
+// MODE 1 (down): unit tile covers output rows tile*256 .. +255; CTA r holds
+//   rows tile*256 + 128r + i; K = I; B rows = h rows of the expert; epilogue
+//   y[row][tile*256 + 128r + i] = acc (the combine applies the routing weight).
+// Roles (both CTAs): warp 0 Q4_K block copies, warp 2 operand-B copies of
+// this CTA's half of the tokens, warps 4-11 dequantization, warps 12-15
+// epilogue of this CTA's 128 accumulator rows; warp 1 allocates tensor
+// memory (collectively for the pair) and, in the even CTA, issues the MMAs.
+// Warp 3 of the even CTA is a second MMA thread: a two-chunk pass gives one
+// chunk to each thread, so that one thread's barrier wait and commit (which
+// would leave the tensor cores idle -- an issuing thread keeps only about one
+// MMA queued) overlap the other thread's MMAs.  Accumulators are two
+// 256-column buffers used round robin: the epilogue of one chunk overlaps
+// the MMAs of the next.
+// Barriers (same offsets in both CTAs).  One pair of barriers per operand
+// stage, so the MMA thread makes one wait and one commit per K step (each
+// costs it ~100 cycles, and it has ~128 cycles per 256-column MMA to spare):
+// full (even CTA) completes when the even CTA's B producer has armed it, its
+// 8 dequant warps have arrived, the B boxes of both CTAs have landed (the odd
+// CTA's tensor copies signal the even CTA's barrier) and the odd CTA's 8
+// dequant warps have each copied a 16-byte token into the even CTA after
+// fencing their A tile -- copy-engine signals, so no thread stalls on a
+// release at cluster scope (several hundred ns under this kernel's memory
+// traffic); empty (both CTAs, both MMA threads) and d_full are completed by
+// the multicast MMA commits; d_empty (even CTA) by both CTAs' epilogue
+// warps; raw_* are local.
 template <int MODE>
-__global__ void __launch_bounds__(kGThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     k_prefill_gemm(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
-                   const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_out,
-                   PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap tm_b64, const __grid_constant__ CUtensorMap tm_b16,
+                   const __grid_constant__ CUtensorMap tm_h, PrefillArgs a) {
     extern __shared__ uint8_t g_smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(g_smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint32_t s_taddr;
     __shared__ int s_err;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles = MODE == 0 ? a.I / 64 : a.H / 128;
+    const int rank = (int)cluster_ctarank();
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int tiles = MODE == 0 ? a.I / 128 : a.H / 256;
     const int nU = a.E * tiles;
     const int K = MODE == 0 ? a.H : a.I;
     const int nK = K / 64;
@@ -420,53 +500,49 @@ __global__ void __launch_bounds__(kGThreads, 1)
 
     const uint32_t bar0 = smem_addr(sm + kOffBar);
     const uint32_t raw_full = bar0, raw_empty = bar0 + 8 * kNR;
-    const uint32_t full_a = bar0 + 16 * kNR, empty_a = full_a + 8 * kNA;
-    const uint32_t full_b = empty_a + 8 * kNA, empty_b = full_b + 8 * kNB;
-    const uint32_t d_full = empty_b + 8 * kNB, d_empty = d_full + 16, fin = d_empty + 16;  // d_*: [2]
+    const uint32_t full = bar0 + 16 * kNR, empty = full + 8 * kNS;
+    const uint32_t d_full = empty + 8 * kNS, d_empty = d_full + 8 * kNBuf, fin = d_empty + 8 * kNBuf;  // fin: [2]
     volatile int *verr = &s_err;
 
     if (threadIdx.x == 0) {
         s_err = 0;
         prefetch_tensormap(&tm_a0);
         if (MODE == 0) prefetch_tensormap(&tm_a1);
-        prefetch_tensormap(&tm_b);
-        prefetch_tensormap(&tm_out);
+        prefetch_tensormap(&tm_b64);
+        prefetch_tensormap(&tm_b16);
+        if (MODE == 0) prefetch_tensormap(&tm_h);
         for (int r = 0; r < kNR; ++r) {
             mbar_init(raw_full + 8 * r, 1);
             mbar_init(raw_empty + 8 * r, 8);
         }
-        for (int s = 0; s < kNA; ++s) {
-            mbar_init(full_a + 8 * s, 8);
-            mbar_init(empty_a + 8 * s, 1);
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(full + 8 * s, 1 + 8);  // the B producer's arming + the even CTA's 8 dequant warps
+            mbar_init(empty + 8 * s, 2);     // one commit from each MMA thread
         }
-        for (int s = 0; s < kNB; ++s) {
-            mbar_init(full_b + 8 * s, 1);
-            mbar_init(empty_b + 8 * s, 1);
-        }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kNBuf; ++b) {
             mbar_init(d_full + 8 * b, 1);
-            mbar_init(d_empty + 8 * b, 4);
+            mbar_init(d_empty + 8 * b, 8);  // 4 epilogue warps of each CTA
         }
         mbar_init(fin, 1);
+        mbar_init(fin + 8, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
-        tc::tmem_alloc(smem_addr(&s_taddr), 512);
-        tc::tmem_relinquish();
+        tc::tmem_alloc_pair(smem_addr(&s_taddr), 512);
+        tc::tmem_relinquish_pair();
     }
     tc::fence_before_sync();
     __syncthreads();
+    cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
     tc::fence_after_sync();
     const uint32_t taddr = s_taddr;
 
     // every role walks the same passes
     auto for_each_pass = [&](auto &&body) {
-        for (int u = blockIdx.x; u < nU && !*verr; u += gridDim.x) {
+        for (int u = pair; u < nU && !*verr; u += npairs) {
             const int e = u / tiles, tile = u - e * tiles;
             const int ne = __ldg(a.counts + e), prow = __ldg(a.poff + e);
-            const int rot = 4 * (tile % (nK / 4));
-            for (int sc = 0; sc < ne && !*verr; sc += kMaxTok)
-                body(Pass{e, tile, prow, sc, min(kMaxTok, ne - sc), rot});
+            for (int sc = 0; sc < ne && !*verr; sc += kMaxTok) body(make_pass(e, tile, prow, sc, ne, nK));
         }
     };
     auto fail = [&]() {
@@ -475,7 +551,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     };
 
     if (warp == 0) {
-        // ------------------------------------------------ Q4_K weight blocks (tensor-map copies)
+        // ------------------------------------------------ Q4_K weight blocks of this CTA's 128 rows
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();  // each Q4_K block is read by one CTA
             int rstep = 0;
@@ -490,11 +566,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     const uint32_t dst = smem_addr(sm + kOffRaw + r * kRaw);
                     mbar_arrive_expect_tx(raw_full + 8 * r, kRaw);
                     if (MODE == 0) {
-                        const int y = ps.e * a.I + ps.tile * 64;
+                        const int y = ps.e * a.I + ps.tile * 128 + 64 * rank;
                         tma_load_2d(dst, &tm_a0, kBlockBytes * blk, y, raw_full + 8 * r, pol);
                         tma_load_2d(dst + 64 * kBlockBytes, &tm_a1, kBlockBytes * blk, y, raw_full + 8 * r, pol);
                     } else {
-                        tma_load_2d(dst, &tm_a0, kBlockBytes * blk, ps.e * a.H + ps.tile * 128, raw_full + 8 * r, pol);
+                        tma_load_2d(dst, &tm_a0, kBlockBytes * blk, ps.e * a.H + ps.tile * 256 + 128 * rank,
+                                    raw_full + 8 * r, pol);
                     }
                 }
             });
@@ -504,86 +581,97 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         __syncwarp();
     } else if (warp == 2) {
-        // ------------------------------------------------ operand-B tiles (tensor-map copies)
+        // ------------------------------------------------ this CTA's half of every chunk's token rows
         if (lane == 0) {
+            const uint32_t lead_full = mapa_shared(full, 0);
             int step = 0;
             for_each_pass([&](const Pass &ps) {
-                const int nbox = (ps.nt + kBoxTok - 1) / kBoxTok;
+                const int hr = ps.n >> 1;  // rows per chunk half (multiple of 16, <= 128; <= 96 with two chunks)
                 for (int kb = 0; kb < nK; ++kb, ++step) {
-                    const int s = step % kNB;
-                    if (step >= kNB && !mbar_wait_bounded(empty_b + 8 * s, ((step / kNB) - 1) & 1, budget)) {
+                    const int s = step % kNS;
+                    if (step >= kNS && !mbar_wait_bounded_cluster(empty + 8 * s, ((step / kNS) - 1) & 1, budget)) {
                         fail();
                         return;
                     }
                     const uint32_t bt = smem_addr(sm + kOffB + s * kBTile);
-                    mbar_arrive_expect_tx(full_b + 8 * s, (uint32_t)(nbox * kBoxTok * 128));
-                    const int kq = (kb + ps.rot) % nK;
-                    for (int b = 0; b < nbox; ++b)
-                        tma_load_2d_plain(bt + b * kBoxTok * 128, &tm_b, 64 * kq, ps.prow + ps.sc + kBoxTok * b,
-                                          full_b + 8 * s);
+                    // even CTA: both CTAs' boxes and the odd CTA's 8 A-tile tokens
+                    if (rank == 0) mbar_arrive_expect_tx(full + 8 * s, (uint32_t)(2 * ps.nch * hr * 128 + 8 * 16));
+                    const int x = 64 * ((kb + ps.rot) % nK);
+                    for (int c = 0; c < ps.nch; ++c) {
+                        const uint32_t dst = bt + c * kChunkRows * 128;
+                        const int row = ps.prow + ps.sc + c * ps.n + rank * hr;
+                        int q = 0;
+                        for (; q + 64 <= hr; q += 64) tma_load_2d_pair(dst + q * 128, &tm_b64, x, row + q, lead_full + 8 * s);
+                        for (; q < hr; q += 16) tma_load_2d_pair(dst + q * 128, &tm_b16, x, row + q, lead_full + 8 * s);
+                    }
                 }
             });
-            for (int q = (step > kNB ? step - kNB : 0); q < step; ++q)
-                mbar_wait_bounded(full_b + 8 * (q % kNB), (q / kNB) & 1, kDrainG);
+            if (rank == 0)  // the even CTA's full covers the copies of both CTAs
+                for (int q = (step > kNS ? step - kNS : 0); q < step; ++q)
+                    mbar_wait_bounded_cluster(full + 8 * (q % kNS), (q / kNS) & 1, kDrainG);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issue (one thread)
-        if (lane == 0) {
-            int step = 0, chunk = 0;
-            int uses[2] = {0, 0};
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------ pair MMA issue (even CTA: warps 1 and 3, one thread each)
+        if (lane == 0 && rank == 0) {
+            const int me = warp >> 1;  // MMA thread 0 or 1: issues chunk c == me of each pass
+            const uint64_t desc_base = tc::sdesc_sw128(smem_addr(sm));
+            int step = 0, g0 = 0;  // g0: global index of the pass's first chunk
             bool issued = false;
             for_each_pass([&](const Pass &ps) {
-                const int nch = (ps.nt + 255) >> 8;
-                for (int c = 0; c < nch; ++c) {  // the accumulator buffers of this pass are drained
-                    const int b = (chunk + c) & 1;
-                    if (uses[b] > 0 && !mbar_wait_spin(d_empty + 8 * b, (uses[b] - 1) & 1, budget)) {
+                for (int c = me; c < ps.nch; c += 2) {  // this thread's buffers of the pass are drained
+                    const int g = g0 + c;
+                    if (g >= kNBuf &&
+                        !mbar_wait_spin_cluster(d_empty + 8 * (g % kNBuf), ((g / kNBuf) - 1) & 1, budget)) {
                         fail();
                         return;
                     }
                 }
                 tc::fence_after_sync();
+                const uint32_t idesc = tc::idesc_f16_f32(256, ps.n);
                 for (int kb = 0; kb < nK; ++kb, ++step) {
-                    const int sa = step % kNA, sb = step % kNB;
-                    if (!mbar_wait_spin(full_a + 8 * sa, (step / kNA) & 1, budget) ||
-                        !mbar_wait_spin(full_b + 8 * sb, (step / kNB) & 1, budget)) {
+                    const int s = step % kNS;
+                    if (!mbar_wait_spin_cluster(full + 8 * s, (step / kNS) & 1, budget)) {
                         fail();
                         return;
                     }
                     tc::fence_after_sync();  // the dequant warps fenced their A-tile writes to the async proxy
-                    const uint32_t at = smem_addr(sm + sa * kATile);
-                    for (int c = 0; c < nch; ++c) {
-                        const int nc = min(256, ps.nt - 256 * c);
-                        const uint32_t idesc = tc::idesc_f16_f32(128, (nc + 15) & ~15);
-                        const uint32_t bt = smem_addr(sm + kOffB + sb * kBTile) + c * 256 * 128;
-                        const uint32_t d = taddr + 256 * ((chunk + c) & 1);
-                        for (int j = 0; j < 4; ++j)
-                            tc::mma_f16kind(d, tc::sdesc_sw128(at + 32 * j), tc::sdesc_sw128(bt + 32 * j), idesc,
-                                            kb > 0 || j > 0);
-                    }
-                    tc::mma_commit(empty_a + 8 * sa);
-                    tc::mma_commit(empty_b + 8 * sb);
+                    // descriptors: stage bases (1024-byte aligned) >> 4 in the address field
+                    const uint64_t ad = desc_base + (uint64_t)((s * kATile) >> 4);
+                    const uint64_t bd = desc_base + (uint64_t)((kOffB + s * kBTile) >> 4);
+                    for (int c = me; c < ps.nch; c += 2)
+                        tc::mma_pair_k64(taddr + 256 * ((g0 + c) % kNBuf), ad, bd + (uint64_t)((c * kChunkRows * 128) >> 4),
+                                         idesc, kb > 0);
+                    tc::mma_pair_commit_mc(empty + 8 * s, kPairMask);  // also when this thread had no chunk
                     issued = true;
                 }
-                for (int c = 0; c < nch; ++c) {
-                    const int b = (chunk + c) & 1;
-                    tc::mma_commit(d_full + 8 * b);
-                    ++uses[b];
-                }
-                chunk += nch;
+                for (int c = me; c < ps.nch; c += 2) tc::mma_pair_commit_mc(d_full + 8 * ((g0 + c) % kNBuf), kPairMask);
+                g0 += ps.nch;
             });
-            if (issued) {  // every MMA has completed before the tensor memory is released
-                tc::mma_commit(fin);
-                mbar_wait_bounded(fin, 0, kDrainG);
+            if (issued) {  // every MMA has completed before either CTA releases its memory
+                tc::mma_pair_commit_mc(fin + 8 * me, 1);
+                mbar_wait_bounded(fin + 8 * me, 0, kDrainG);
             }
         }
         __syncwarp();
     } else if (warp >= 4 && warp < 12) {
-        // ------------------------------------------------ dequant (warps 4-11)
+        // ------------------------------------------------ dequant (warps 4-11) of this CTA's 128 rows
         const int d = threadIdx.x - 128;  // 0..255
         const int row = d >> 1, half = d & 1;
         // MODE 0: A row 2i = gate row i, 2i+1 = up row i (raw rows: gate 0-63, up 64-127)
         const int raw_row = MODE == 0 ? ((row & 1) ? 64 + (row >> 1) : (row >> 1)) : row;
+        // The codes of this thread are bits 4*half.. of each byte.  A code q at
+        // bit p of a word becomes the fp32 value 2^23 + q*2^p by or-ing in the
+        // exponent of 2^23; fma(dsc*2^-p, that, -dsc*2^(23-p)) then equals
+        // dsc*q exactly (a 21-bit product), and subtracting dm rounds once:
+        // the same fp32 value as fma(dsc, q, -dm).  Bytes 0, 1 of a word are
+        // taken at p = 4*half, 4*half+8; bytes 2, 3 likewise after a 16-bit shift.
+        const int p0 = 4 * half;
+        const uint32_t m0 = 15u << p0, m8 = 15u << (p0 + 8);
+        const uint32_t tok = smem_addr(sm + kOffTok), lead_tok = mapa_shared(tok, 0);
+        const uint32_t lead_full = mapa_shared(full, 0);
+        const float tp0 = __uint_as_float((127u - p0) << 23), tp8 = __uint_as_float((119u - p0) << 23);    // 2^-p
+        const float to0 = -__uint_as_float((150u - p0) << 23), to8 = -__uint_as_float((142u - p0) << 23);  // -2^(23-p)
         int astep = 0, rstep = 0;
         for_each_pass([&](const Pass &ps) {
             for (int kb = 0; kb < nK; ++kb, ++astep) {
@@ -593,8 +681,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     fail();
                     return;
                 }
-                const int s = astep % kNA;
-                if (astep >= kNA && !mbar_wait_warp(empty_a + 8 * s, ((astep / kNA) - 1) & 1, budget)) {
+                const int s = astep % kNS;
+                if (astep >= kNS && !mbar_wait_warp_cluster(empty + 8 * s, ((astep / kNS) - 1) & 1, budget)) {
                     fail();
                     return;
                 }
@@ -608,18 +696,18 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 const float dmin = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
                 const float dsc = dd * (float)sc, dm = dmin * (float)m;
                 if (fmaxf(fabsf(fmaf(dsc, 15.f, -dm)), fabsf(dm)) > 65504.f) set_status(status, SI_ERR_RANGE);
+                const f32x2 C = pack2(dsc * tp0, dsc * tp8), O = pack2(dsc * to0, dsc * to8), D = pack2(-dm, -dm);
                 const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                const int sh = 4 * half;
                 uint32_t o[16];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
-                    const uint32_t b = wv[t] >> sh;
-                    const float f0 = fmaf(dsc, (float)(b & 15u), -dm);
-                    const float f1 = fmaf(dsc, (float)((b >> 8) & 15u), -dm);
-                    const float f2 = fmaf(dsc, (float)((b >> 16) & 15u), -dm);
-                    const float f3 = fmaf(dsc, (float)((b >> 24) & 15u), -dm);
-                    o[2 * t] = f16x2_rn(f0, f1);
-                    o[2 * t + 1] = f16x2_rn(f2, f3);
+                    const uint32_t w = wv[t], hi = w >> 16;
+                    const f32x2 v01 = pack2(__uint_as_float((w & m0) | 0x4B000000u), __uint_as_float((w & m8) | 0x4B000000u));
+                    const f32x2 v23 = pack2(__uint_as_float((hi & m0) | 0x4B000000u), __uint_as_float((hi & m8) | 0x4B000000u));
+                    const float2 r01 = unpack2(add2(fma2(v01, C, O), D));
+                    const float2 r23 = unpack2(add2(fma2(v23, C, O), D));
+                    o[2 * t] = f16x2_rn(r01.x, r01.y);
+                    o[2 * t + 1] = f16x2_rn(r23.x, r23.y);
                 }
                 uint8_t *at = sm + s * kATile + row * 128;
 #pragma unroll
@@ -630,7 +718,18 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 }
                 tc::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(full_a + 8 * s);
+                if (lane == 0) {
+                    if (rank == 0) {
+                        mbar_arrive(full + 8 * s);
+                    } else {
+                        const uint32_t slot = 16 * (8 * s + (warp - 4));
+                        asm volatile(
+                            "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], 16, "
+                            "[%2];" ::"r"(lead_tok + slot),
+                            "r"(tok + slot), "r"(lead_full + 8 * s)
+                            : "memory");
+                    }
+                }
                 if (j == 3) {
                     if (lane == 0) mbar_arrive(raw_empty + 8 * r);
                     ++rstep;
@@ -638,14 +737,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
         });
     } else if (warp >= 12) {
-        // ------------------------------------------------ epilogue (warps 12-15)
-        // Results go through two 8 KB staging buffers and tensor-map stores of
-        // 32 rows x 64 fp16 (h) or 16 rows x 128 fp32 (y); a buffer is rewritten
-        // once the store issued from it two stores earlier has read it.
+        // ------------------------------------------------ epilogue (warps 12-15) of this CTA's accumulator rows
+        // MODE 0: h goes through two 8 KB staging buffers and tensor-map stores
+        // of 32 tokens x 64 fp16 (128-byte rows; a buffer is rewritten once the
+        // store issued from it two stores earlier has read it).  MODE 1: y is
+        // stored straight from registers -- for one token the 32 lanes of a warp
+        // hold 32 consecutive output columns, 128 contiguous bytes.
         const int ew = warp - 12;  // tensor-memory lanes 32*ew ..
         const bool lead = threadIdx.x == 12 * 32;
-        int chunk = 0, nst = 0;
-        int uses[2] = {0, 0};
+        const uint32_t lead_d_empty = mapa_shared(d_empty, 0);
+        int chunk = 0, nst = 0;  // chunk: global index
         auto stage_begin = [&]() -> uint8_t * {
             if (lead && nst >= 2) bulk_wait_read1();
             asm volatile("bar.sync 4, 128;" ::: "memory");
@@ -655,31 +756,50 @@ __global__ void __launch_bounds__(kGThreads, 1)
             tc::fence_proxy_async_smem();
             asm volatile("bar.sync 4, 128;" ::: "memory");
             if (lead) {
-                tma_store_2d(&tm_out, x, y, smem_addr(buf));
+                tma_store_2d(&tm_h, x, y, smem_addr(buf));
                 bulk_commit();
             }
             ++nst;
         };
         for_each_pass([&](const Pass &ps) {
-            const int nch = (ps.nt + 255) >> 8;
-            for (int c = 0; c < nch; ++c, ++chunk) {
-                const int b = chunk & 1;
-                if (!mbar_wait_warp(d_full + 8 * b, uses[b] & 1, budget)) {
+            for (int c = 0; c < ps.nch; ++c, ++chunk) {
+                const int b = chunk % kNBuf;
+                const int nv = min(ps.n, ps.nt - c * ps.n);  // valid tokens of this chunk
+                const int rowc = ps.prow + ps.sc + c * ps.n;  // padded row of the chunk's first token
+                if (!mbar_wait_warp_cluster(d_full + 8 * b, (chunk / kNBuf) & 1, budget)) {
                     fail();
                     return;
                 }
-                ++uses[b];
                 tc::fence_after_sync();
-                const int nc = min(256, ps.nt - 256 * c);
-                for (int col0 = 0; col0 < nc; col0 += 32) {
+                if (MODE == 1) {
+                    // y = accumulators, straight from registers; the tensor-memory load of the
+                    // next 32 columns is in flight while this group is stored
+                    const uint32_t tcol = taddr + ((uint32_t)(32 * ew) << 16) + 256 * b;
+                    float *yc = a.y + (size_t)rowc * a.H + ps.tile * 256 + 128 * rank + 32 * ew + lane;
+                    uint32_t v[2][32];
+                    tc::tmem_ld32(tcol, v[0]);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const int col0 = 32 * g;
+                        if (col0 >= nv) break;
+                        if (g < 7 && col0 + 32 < nv) tc::tmem_ld32(tcol + col0 + 32, v[(g + 1) & 1]);
+                        const int nq = min(32, nv - col0);
+#pragma unroll
+                        for (int q = 0; q < 32; ++q)
+                            if (q < nq) __stcs(yc + (size_t)(col0 + q) * a.H, __uint_as_float(v[g & 1][q]));
+                        tc::tmem_wait_ld();
+                    }
+                }
+                for (int col0 = 0; MODE == 0 && col0 < nv; col0 += 32) {
                     uint32_t v[32];
                     tc::tmem_ld32(taddr + ((uint32_t)(32 * ew) << 16) + 256 * b + col0, v);
                     tc::tmem_wait_ld();
-                    const int row0 = ps.prow + ps.sc + 256 * c + col0;  // padded row of token col0
-                    // rows past the expert's tokens land in its own padding (poff is 32-aligned)
+                    const int row0 = rowc + col0;  // padded row of token col0
                     if (MODE == 0) {
-                        // lanes 2i / 2i+1 hold g / u of intermediate row i for 32 tokens;
-                        // the even lane forms h for tokens 0-15, the odd lane for 16-31
+                        // lanes 2i / 2i+1 hold g / u of intermediate row i for 32 tokens; the even
+                        // lane forms h for tokens 0-15, the odd lane for 16-31.  Rows past the
+                        // chunk's tokens land in the expert's own padding (32-row aligned).
                         uint16_t *hs = reinterpret_cast<uint16_t *>(stage_begin());  // [32 tokens][64] fp16
                         const int up = lane & 1;
                         const int il = 16 * ew + (lane >> 1);
@@ -692,40 +812,34 @@ __global__ void __launch_bounds__(kGThreads, 1)
                             const float gg = up ? recv : __uint_as_float(v[q]);
                             const float uu = up ? __uint_as_float(v[q + 16]) : recv;
                             hv[q] = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
-                            // columns past the pass's tokens hold stale accumulators: not checked
-                            big |= (col0 + q + 16 * up < nc) & (fabsf(hv[q]) > 65504.f);
+                            // columns past the chunk's tokens hold stale accumulators: not checked
+                            big |= (col0 + q + 16 * up < nv) & (fabsf(hv[q]) > 65504.f);
                         }
 #pragma unroll
                         for (int q = 0; q < 16; ++q) hs[(q + 16 * up) * 64 + il] = __half_as_ushort(__float2half_rn(hv[q]));
                         if (big) set_status(status, SI_ERR_RANGE);
-                        stage_end(reinterpret_cast<uint8_t *>(hs), ps.tile * 64, row0);
-                    } else {
-                        const float wl = __ldg(a.wp + row0 + lane);  // weight of token col0 + lane (0 on padding)
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            float yv[16];
-#pragma unroll
-                            for (int q = 0; q < 16; ++q)
-                                yv[q] = __shfl_sync(0xffffffffu, wl, 16 * hf + q) * __uint_as_float(v[16 * hf + q]);
-                            float *ys = reinterpret_cast<float *>(stage_begin());  // [16 tokens][128] fp32
-#pragma unroll
-                            for (int q = 0; q < 16; ++q) ys[q * 128 + 32 * ew + lane] = yv[q];
-                            stage_end(reinterpret_cast<uint8_t *>(ys), ps.tile * 128, row0 + 16 * hf);
-                        }
+                        stage_end(reinterpret_cast<uint8_t *>(hs), ps.tile * 128 + 64 * rank, row0);
                     }
                 }
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(d_empty + 8 * b);
+                if (lane == 0) {
+                    if (rank == 0) mbar_arrive(d_empty + 8 * b);
+                    else mbar_arrive_cluster(lead_d_empty + 8 * b);
+                }
             }
         });
-        if (lead) bulk_wait0();
+        if (MODE == 0 && lead) bulk_wait0();
     }
+    // Both CTAs stay until every pair MMA has completed (the even CTA waited
+    // for them) and every remote arrival has been made; then the pair releases
+    // its tensor memory together.
     tc::fence_before_sync();
     __syncthreads();
+    cluster_sync();
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(taddr, 512);
+        tc::tmem_dealloc_pair(taddr, 512);
     }
 }
 
@@ -819,17 +933,20 @@ cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, 
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 1, s)) != cudaSuccess) return err;
 
-    CUtensorMap tg, tu, td, txp, thl, ths, tys;
+    // operand B: token rows in boxes of 64 and of 16 rows (a CTA's half of a chunk is 64*a + 16*b rows)
+    CUtensorMap tg, tu, td, txp64, txp16, th64, th16, ths;
     if (!q4k_map(a.wg, (int64_t)a.E * a.I, a.H / kQK, 64, &tg) || !q4k_map(a.wu, (int64_t)a.E * a.I, a.H / kQK, 64, &tu) ||
         !q4k_map(a.wd, (int64_t)a.E * a.H, a.I / kQK, 128, &td) ||
-        !mat_map(a.xp, a.rows, a.H, 2, 64, kBoxTok, true, &txp) || !mat_map(a.h, a.rows, a.I, 2, 64, kBoxTok, true, &thl) ||
-        !mat_map(a.h, a.rows, a.I, 2, 64, 32, false, &ths) || !mat_map(a.y, a.rows, a.H, 4, 128, 16, false, &tys))
+        !mat_map(a.xp, a.rows, a.H, 2, 64, 64, true, &txp64) || !mat_map(a.xp, a.rows, a.H, 2, 64, 16, true, &txp16) ||
+        !mat_map(a.h, a.rows, a.I, 2, 64, 64, true, &th64) || !mat_map(a.h, a.rows, a.I, 2, 64, 16, true, &th16) ||
+        !mat_map(a.h, a.rows, a.I, 2, 64, 32, false, &ths))
         return cudaErrorInvalidValue;
-    const int grid = p.sm_count;
-    k_prefill_gemm<0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp, ths, a);
+    // one CTA pair (2-CTA cluster, declared on the kernel) per two SMs
+    const int grid = 2 * (p.sm_count / 2);
+    k_prefill_gemm<0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 2, s)) != cudaSuccess) return err;
-    k_prefill_gemm<1><<<grid, kGThreads, kGemmSmem, s>>>(td, td, thl, tys, a);
+    k_prefill_gemm<1><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 3, s)) != cudaSuccess) return err;
     const size_t n4 = (size_t)a.T * (a.H / 4);

@@ -97,6 +97,59 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---------------------------------------------------------------- CTA pairs (cta_group::2)
+// Two CTAs of a cluster (ranks 2p, 2p+1) act as one MMA unit: an M = 256
+// MMA issued by the even CTA reads rows 0-127 of A from its own shared
+// memory and rows 128-255 from its peer's (same offset), columns 0..N/2-1 of B
+// from its own shared memory and N/2..N-1 from its peer's, and accumulates
+// rows 0-127 of D in its own tensor memory and 128-255 in the peer's.
+// Allocation and release are collective: one warp of each CTA of the pair.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma_pair_f16kind(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+// One 64-wide K step of pair MMAs: four K = 16 MMAs whose operand
+// descriptors advance by 32 bytes (2 in the descriptor's address field) within
+// the 128-byte swizzle row; the first accumulates into D only if `acc`.
+__device__ __forceinline__ void mma_pair_k64(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %11, 0;\n\t"
+        "setp.eq.u32 q, %10, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %5, %9, p;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %2, %6, %9, q;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %3, %7, %9, q;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %4, %8, %9, q;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(a_desc + 2), "l"(a_desc + 4), "l"(a_desc + 6), "l"(b_desc), "l"(b_desc + 2), "l"(b_desc + 4),
+        "l"(b_desc + 6), "r"(idesc), "r"(0u), "r"(acc)
+        : "memory");
+}
+// Once every pair MMA this thread issued so far has completed, arrive on the
+// mbarrier at shared-memory offset `mbar` in each CTA of `cta_mask`.
+__device__ __forceinline__ void mma_pair_commit_mc(uint32_t mbar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            mbar),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // Byte offset of 16-bit element (row r, k) of a K-major 128-byte-swizzled tile
 // of 64-wide rows (k < 64).
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t k) {

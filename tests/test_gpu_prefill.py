@@ -1,6 +1,6 @@
-"""GPU parity of the grouped prefill (routing, counts/offsets/perm, tensor-core
-gate/up and down GEMMs on bf16-dequantized Q4_K operands, slot-order combine)
-against the CPU oracle, through the C ABI."""
+"""GPU parity of the grouped prefill (routing, counts/offsets/perm, CTA-pair
+tensor-core gate/up and down GEMMs on fp16-dequantized Q4_K operands,
+slot-order combine) against the CPU oracle, through the C ABI."""
 from __future__ import annotations
 
 import numpy as np
