@@ -83,6 +83,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--tokens", type=int, default=0,
                    help="tokens per step of the headline layer (default 1024; small values for ncu)")
+    p.add_argument("--prefill-only", action="store_true",
+                   help="time only the grouped prefill workload (for profiling its kernels)")
     p.add_argument("--cpu-sample-tokens", type=int, default=0,
                    help="tokens of the CPU oracle sample (default: 16 per host core, at least 64)")
     return p.parse_args()
@@ -548,6 +550,11 @@ def run_ours(args, dist):
     build.build()
     binding.load_library()
     torch.cuda.set_device(dist.local)
+    if args.prefill_only:
+        res = bench_prefill(args, dist, binding, device, synth, torch)
+        if dist.rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     hbm_peak, peak_src = peaks()
     res = bench_layer(args, dist, binding, device, synth, torch, hbm_peak)
     res["roofline"]["peak_source"] = peak_src
