@@ -69,160 +69,163 @@ __global__ void __launch_bounds__(256) k_prefill_wt(PrefillArgs a) {
 }
 
 namespace {
-constexpr int kRtTok = 32;                   // tokens per router CTA
-constexpr int kRtExp = 128;                  // experts per pass
-constexpr int kRtKc = 32;                    // hidden columns per chunk
-constexpr int kRtNS = 4;                     // W^T chunk stages
-constexpr int kRtThreads = 256;
-constexpr int kRtW = kRtKc * kRtExp * 4;     // 16 KB: W^T chunk [32][128] fp32
-constexpr int kRtX = kRtKc * kRtTok * 8;     // 8 KB: x chunk as duplicated pairs [32][32] (x, x)
+constexpr int kRtTok = 32;                       // tokens per router CTA
+constexpr int kRtExp = 128;                      // experts per pass
+constexpr int kRtKs = 64;                        // hidden columns per stage
+constexpr int kRtNS = 4;                         // stages
+constexpr int kRtThreads = 512;
+constexpr int kRtG = kRtThreads / 64;            // K groups of 64 threads (8 tokens x 8 experts each)
+constexpr int kRtW = kRtKs * kRtExp * 4;         // 32 KB: W^T rows [64][128] fp32
+constexpr int kRtX = kRtKs * kRtTok * 2;         // 4 KB: x [32 tokens][64] bf16 (tensor-map box)
 constexpr int kRtOffX = kRtNS * kRtW;
-constexpr int kRtOffZ = kRtOffX + 2 * kRtX;  // logits [32][E] fp32
+constexpr int kRtOffZ = kRtOffX + kRtNS * kRtX;  // logits [32][SI_MAX_EXPERTS] fp32
 constexpr int kRtOffBar = kRtOffZ + kRtTok * SI_MAX_EXPERTS * 4;
 constexpr int kRtSmem = kRtOffBar + kRtNS * 8 + 16 + 1024;
+static_assert(kRtG * kRtTok * kRtExp * 4 <= kRtNS * kRtW, "the K groups' partial sums fit in the W^T stages");
+static_assert(kRtKs % (2 * kRtG) == 0, "stage columns split into column pairs over the K groups");
 }  // namespace
 
-// Logits of 32 tokens x all experts in fp32 (packed FMA, hidden order: the
-// router GEMV's arithmetic), W^T chunks streamed by tensor-map copies; then
-// one thread per token takes the top-k by insertion in expert order with a
-// strict comparison (descending logit, ties to the lower index), the
-// renormalised weights and the per-expert pair counts.
-template <int KM>
-__global__ void __launch_bounds__(kRtThreads)
-    k_prefill_route(const __grid_constant__ CUtensorMap tm_wt, PrefillArgs a) {
+// Logits of 32 tokens x all experts in fp32 on the SIMT pipes, W^T streamed by
+// tensor-map copies in stages of 64 hidden columns.  The 512 threads form 8
+// K groups (columns 8g..8g+7 of every stage); in a group each thread holds
+// 8 tokens x 8 experts (packed FMA), so one 16-byte shared load feeds 8 FMAs.
+// Each group sums its H/8 columns in hidden order; the 8 group sums are
+// added in a fixed order.
+// Then one warp per token takes the top-k as k rounds of a warp-wide argmax
+// (descending logit, ties to the lower index), the renormalised weights and
+// the per-expert pair counts.
+__global__ void __launch_bounds__(kRtThreads, 1)
+    k_prefill_route(const __grid_constant__ CUtensorMap tm_wt, const __grid_constant__ CUtensorMap tm_x, PrefillArgs a) {
     extern __shared__ uint8_t rt_smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(rt_smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, te = tid & 31, tt = tid >> 5;  // experts 4te..4te+3, tokens 4tt..4tt+3
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int kg = warp >> 1;                        // K group
+    const int gi = ((warp & 1) << 5) | lane;         // thread within the group
+    const int tb = gi >> 4, eb = gi & 15;            // tokens 8tb..8tb+7, experts 8eb..8eb+7 of the pass
     const int t0 = blockIdx.x * kRtTok;
-    const int nch = a.H / kRtKc;
-    // every CTA reads all of W^T: CTA b walks the chunks from (3b) mod nch, so
+    const int nst = a.H / kRtKs;
+    // every CTA reads all of W^T: CTA b walks the stages from (3b) mod nst, so
     // the CTAs do not all request the same L2 lines at the same moment
-    const int rot = (3 * blockIdx.x) % nch;
+    const int rot = (3 * blockIdx.x) % nst;
     const uint32_t full = smem_addr(sm + kRtOffBar);
     float(*s_z)[SI_MAX_EXPERTS] = reinterpret_cast<float(*)[SI_MAX_EXPERTS]>(sm + kRtOffZ);
     int32_t *status = a.ctrl + kCtrlStatus;
     if (tid == 0) {
         prefetch_tensormap(&tm_wt);
+        prefetch_tensormap(&tm_x);
         for (int s = 0; s < kRtNS; ++s) mbar_init(full + 8 * s, 1);
         fence_mbar_init();
     }
     __syncthreads();
-    int step = 0;  // chunk copies issued so far (over all expert passes)
+    int step = 0;  // stage copies issued so far (over all expert passes)
     for (int e0 = 0; e0 < a.E; e0 += kRtExp) {
         const int base = step;
-        auto issue = [&](int j) {  // chunk j of this expert pass into stage (base + j) % NS
-            const int q = base + j, s = q % kRtNS;
-            mbar_arrive_expect_tx(full + 8 * s, kRtW);
-            tma_load_2d_plain(smem_addr(sm + s * kRtW), &tm_wt, e0, kRtKc * ((j + rot) % nch), full + 8 * s);
+        auto issue = [&](int j) {  // stage j of this expert pass into buffer (base + j) % NS
+            const int s = (base + j) % kRtNS;
+            const int c0 = kRtKs * ((j + rot) % nst);
+            mbar_arrive_expect_tx(full + 8 * s, kRtW + kRtX);
+            tma_load_2d_plain(smem_addr(sm + s * kRtW), &tm_wt, e0, c0, full + 8 * s);
+            tma_load_2d_plain(smem_addr(sm + kRtOffX + s * kRtX), &tm_x, c0, t0, full + 8 * s);  // rows >= T: zeros
         };
         if (tid == 0)
-            for (int j = 0; j < min(kRtNS, nch); ++j) issue(j);
-        f32x2 acc[4][2], tot[4][2];  // [token j][expert pair]: per 256 columns, and the total
+            for (int j = 0; j < min(kRtNS, nst); ++j) issue(j);
+        f32x2 acc[8][4];  // [token][expert pair]
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = tot[j][0] = tot[j][1] = pack2(0.f, 0.f);
-        const int tk = tid >> 3, c4 = (tid & 7) * 4;  // this thread's x elements of a chunk
-        const bool tok_ok = t0 + tk < a.T;
-        const uint2 *xrow = reinterpret_cast<const uint2 *>(a.x + (size_t)(tok_ok ? t0 + tk : 0) * a.H + c4);
-        uint2 raw_next = tok_ok ? __ldg(xrow + (kRtKc / 4) * rot) : make_uint2(0u, 0u);
-        for (int j = 0; j < nch; ++j) {
-            // x chunk (bf16) -> duplicated fp32 pairs [c][token]; the next chunk's x is in flight meanwhile
-            f32x2 *xd = reinterpret_cast<f32x2 *>(sm + kRtOffX + (j & 1) * kRtX);
-            {
-                const uint2 raw = raw_next;
-                if (j + 1 < nch && tok_ok) raw_next = __ldg(xrow + (kRtKc / 4) * ((j + 1 + rot) % nch));
-                const float f0 = __uint_as_float(raw.x << 16), f1 = __uint_as_float(raw.x & 0xffff0000u);
-                const float f2 = __uint_as_float(raw.y << 16), f3 = __uint_as_float(raw.y & 0xffff0000u);
-                xd[(c4 + 0) * kRtTok + tk] = pack2(f0, f0);
-                xd[(c4 + 1) * kRtTok + tk] = pack2(f1, f1);
-                xd[(c4 + 2) * kRtTok + tk] = pack2(f2, f2);
-                xd[(c4 + 3) * kRtTok + tk] = pack2(f3, f3);
-            }
-            const int q = base + j, s = q % kRtNS;
-            if (!mbar_wait_warp(full + 8 * s, (q / kRtNS) & 1, a.wait_budget)) set_status(status, SI_ERR_TIMEOUT);
-            __syncthreads();
-            const float *wt = reinterpret_cast<const float *>(sm + s * kRtW);
-#pragma unroll 4
-            for (int c = 0; c < kRtKc; ++c) {
-                const float4 w = *reinterpret_cast<const float4 *>(wt + c * kRtExp + 4 * te);
-                const f32x2 w01 = pack2(w.x, w.y), w23 = pack2(w.z, w.w);
-                const ulonglong2 xa = *reinterpret_cast<const ulonglong2 *>(xd + c * kRtTok + 4 * tt);
-                const ulonglong2 xb = *reinterpret_cast<const ulonglong2 *>(xd + c * kRtTok + 4 * tt + 2);
-                ffma2(acc[0][0], xa.x, w01);
-                ffma2(acc[0][1], xa.x, w23);
-                ffma2(acc[1][0], xa.y, w01);
-                ffma2(acc[1][1], xa.y, w23);
-                ffma2(acc[2][0], xb.x, w01);
-                ffma2(acc[2][1], xb.x, w23);
-                ffma2(acc[3][0], xb.y, w01);
-                ffma2(acc[3][1], xb.y, w23);
-            }
-            if ((j & 7) == 7 || j == nch - 1) {  // two-level sum: shorter fp32 accumulation chains
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+            for (int q = 0; q < 4; ++q) acc[i][q] = pack2(0.f, 0.f);
+        for (int j = 0; j < nst; ++j) {
+            const int s = (base + j) % kRtNS;
+            if (!mbar_wait_warp(full + 8 * s, ((base + j) / kRtNS) & 1, a.wait_budget)) set_status(status, SI_ERR_TIMEOUT);
+            const float *wt = reinterpret_cast<const float *>(sm + s * kRtW);  // [64 columns][128 experts] fp32
+            const uint32_t *xs = reinterpret_cast<const uint32_t *>(sm + kRtOffX + s * kRtX);  // [32 tokens][32 column pairs] bf16x2
+#pragma unroll 2
+            for (int kp = 0; kp < kRtKs / kRtG / 2; ++kp) {
+                const int k = (kRtKs / kRtG) * kg + 2 * kp;  // columns k, k + 1 in order
+                const float4 w0 = *reinterpret_cast<const float4 *>(wt + k * kRtExp + 8 * eb);
+                const float4 w1 = *reinterpret_cast<const float4 *>(wt + k * kRtExp + 8 * eb + 4);
+                const float4 v0 = *reinterpret_cast<const float4 *>(wt + (k + 1) * kRtExp + 8 * eb);
+                const float4 v1 = *reinterpret_cast<const float4 *>(wt + (k + 1) * kRtExp + 8 * eb + 4);
+                const f32x2 wp[4] = {pack2(w0.x, w0.y), pack2(w0.z, w0.w), pack2(w1.x, w1.y), pack2(w1.z, w1.w)};
+                const f32x2 vp[4] = {pack2(v0.x, v0.y), pack2(v0.z, v0.w), pack2(v1.x, v1.y), pack2(v1.z, v1.w)};
 #pragma unroll
-                    for (int v = 0; v < 2; ++v) {
-                        const float2 p = unpack2(acc[u][v]), q = unpack2(tot[u][v]);
-                        tot[u][v] = pack2(q.x + p.x, q.y + p.y);
-                        acc[u][v] = pack2(0.f, 0.f);
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t xb = xs[(8 * tb + i) * (kRtKs / 2) + (k >> 1)];  // bf16 of columns k, k + 1
+                    const float xa = __uint_as_float(xb << 16), xc = __uint_as_float(xb & 0xffff0000u);
+                    const f32x2 xx = pack2(xa, xa), xy = pack2(xc, xc);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) ffma2(acc[i][q], xx, wp[q]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) ffma2(acc[i][q], xy, vp[q]);
+                }
             }
-            __syncthreads();  // stage s and x buffer free
-            if (tid == 0 && j + kRtNS < nch) issue(j + kRtNS);
+            __syncthreads();  // buffer s (W^T and x) free
+            if (tid == 0 && j + kRtNS < nst) issue(j + kRtNS);
         }
-        step = base + nch;
+        step = base + nst;
+        // the 4 K groups' sums through shared memory (the W^T buffers are free), added in group order
+        float *part = reinterpret_cast<float *>(sm);  // [kRtG][32 tokens][128 experts]
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 p0 = unpack2(tot[j][0]), p1 = unpack2(tot[j][1]);
-            const float v[4] = {p0.x, p0.y, p1.x, p1.y};
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int e = e0 + 4 * te + i;
-                if (e < a.E) s_z[4 * tt + j][e] = a.router_bias ? v[i] + __ldg(a.router_bias + e) : v[i];
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<float2 *>(part + (kg * kRtTok + 8 * tb + i) * kRtExp + 8 * eb + 2 * q) = unpack2(acc[i][q]);
+        __syncthreads();
+        for (int idx = tid; idx < kRtTok * kRtExp; idx += kRtThreads) {
+            const int tk = idx / kRtExp, ex = idx % kRtExp, e = e0 + ex;
+            if (e < a.E) {
+                float z = part[idx];
+#pragma unroll
+                for (int g = 1; g < kRtG; ++g) z += part[idx + g * kRtTok * kRtExp];
+                s_z[tk][e] = a.router_bias ? z + __ldg(a.router_bias + e) : z;
             }
         }
+        __syncthreads();  // the W^T buffers are reused by the next pass
     }
-    __syncthreads();
-    if (tid < kRtTok) {
-        const int t = t0 + tid;
-        if (t < a.T) {
-            const float *z = s_z[tid];
-            float top[KM];
-            int tix[KM];
-#pragma unroll
-            for (int i = 0; i < KM; ++i) top[i] = -INFINITY, tix[i] = 0x7fffffff;
-            for (int e = 0; e < a.E; ++e) {
-                const float ze = z[e];
-                if (a.o_logits) a.o_logits[(size_t)t * a.E + e] = ze;
-                if (ze > top[KM - 1] || tix[KM - 1] == 0x7fffffff) {  // insertion; strict: ties keep the lower index
-                    float cz = ze;
-                    int ci = e;
-#pragma unroll
-                    for (int i = 0; i < KM; ++i) {
-                        if (cz > top[i] || tix[i] == 0x7fffffff) {
-                            const float tz = top[i];
-                            const int ti = tix[i];
-                            top[i] = cz, tix[i] = ci;
-                            cz = tz, ci = ti;
-                        }
-                    }
-                }
+    if (a.o_logits)
+        for (int idx = tid; idx < kRtTok * a.E; idx += kRtThreads) {
+            const int tk = idx / a.E, e = idx % a.E;
+            if (t0 + tk < a.T) a.o_logits[(size_t)(t0 + tk) * a.E + e] = s_z[tk][e];
+        }
+    // top-k: warp w takes tokens 2w, 2w+1; lane holds experts lane + 32m
+    for (int tt = 0; tt < kRtTok / (kRtThreads / 32); ++tt) {
+        const int tk = (kRtTok / (kRtThreads / 32)) * warp + tt, t = t0 + tk;
+        if (t >= a.T) break;
+        uint32_t taken = 0;
+        float myv = 0.f;
+        int myi = 0;
+        for (int r = 0; r < a.k; ++r) {
+            float v = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int m = 0; 32 * m + lane < a.E; ++m) {
+                const int e = 32 * m + lane;
+                const float ze = s_z[tk][e];
+                if (!((taken >> m) & 1u) && (bi == 0x7fffffff || ze > v || (ze == v && e < bi))) v = ze, bi = e;
             }
-            float den = 0.f;
 #pragma unroll
-            for (int i = 0; i < KM; ++i)
-                if (i < a.k) den += expf(top[i] - top[0]);
-#pragma unroll
-            for (int i = 0; i < KM; ++i) {
-                if (i < a.k) {
-                    const size_t p = (size_t)t * a.k + i;
-                    const float w = expf(top[i] - top[0]) / den;
-                    a.ids[p] = tix[i];
-                    a.wts[p] = w;
-                    if (a.o_ids) a.o_ids[p] = tix[i];
-                    if (a.o_w) a.o_w[p] = w;
-                    atomicAdd(a.counts + tix[i], 1);
-                }
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > v || (ov == v && oi < bi))) v = ov, bi = oi;
             }
+            v = __shfl_sync(0xffffffffu, v, 0);  // one decision for the whole warp
+            bi = __shfl_sync(0xffffffffu, bi, 0);
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            if (lane == r) myv = v, myi = bi;
+        }
+        // weights exp(z_r - z_0) / sum over the selected, the sum in slot order
+        const float z0 = __shfl_sync(0xffffffffu, myv, 0);
+        const float ex = expf(myv - z0);
+        float den = 0.f;
+        for (int r = 0; r < a.k; ++r) den += __shfl_sync(0xffffffffu, ex, r);
+        if (lane < a.k) {
+            const size_t p = (size_t)t * a.k + lane;
+            const float w = ex / den;
+            a.ids[p] = myi;
+            a.wts[p] = w;
+            if (a.o_ids) a.o_ids[p] = myi;
+            if (a.o_w) a.o_w[p] = w;
+            atomicAdd(a.counts + myi, 1);
         }
     }
 }
@@ -301,28 +304,30 @@ __global__ void __launch_bounds__(1024) k_prefill_perm(PrefillArgs a) {
 // pperm[r]]), zero for padding rows; a value beyond fp16's range is reported.
 __global__ void __launch_bounds__(256) k_prefill_xperm(PrefillArgs a) {
     const int nrows = a.poff[a.E];
-    const int c8 = a.H / 8;
-    for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < (size_t)nrows * c8;
-         q += (size_t)gridDim.x * blockDim.x) {
-        const int r = (int)(q / c8), c = (int)(q - (size_t)r * c8);
+    const int c8 = a.H / 8;  // 16-byte groups per row
+    for (int r = blockIdx.x; r < nrows; r += gridDim.x) {  // one row per CTA iteration, 32-bit indices
         const int p = __ldg(a.pperm + r);
-        uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (p >= 0) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)(p / a.k) * a.H) + c);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t h[4];
-            bool big = false;
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)(p >= 0 ? p / a.k : 0) * a.H);
+        uint4 *dst = reinterpret_cast<uint4 *>(a.xp + (size_t)r * a.H);
+        for (int c = threadIdx.x; c < c8; c += blockDim.x) {
+            uint4 o = make_uint4(0u, 0u, 0u, 0u);
+            if (p >= 0) {
+                const uint4 v = __ldg(src + c);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t h[4];
+                bool big = false;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-                big |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
-                const __half2 hh = __floats2half2_rn(lo, hi);
-                h[i] = *reinterpret_cast<const uint32_t *>(&hh);
+                for (int i = 0; i < 4; ++i) {
+                    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+                    big |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+                    const __half2 hh = __floats2half2_rn(lo, hi);
+                    h[i] = *reinterpret_cast<const uint32_t *>(&hh);
+                }
+                if (big) set_status(a.ctrl + kCtrlStatus, SI_ERR_RANGE);
+                o = make_uint4(h[0], h[1], h[2], h[3]);
             }
-            if (big) set_status(a.ctrl + kCtrlStatus, SI_ERR_RANGE);
-            o = make_uint4(h[0], h[1], h[2], h[3]);
+            __stcg(dst + c, o);
         }
-        reinterpret_cast<uint4 *>(a.xp + (size_t)r * a.H)[c] = o;
     }
 }
 
@@ -894,9 +899,7 @@ static bool mat_map(const void *base, int64_t rows, int cols, int esize, int box
 cudaError_t prefill_prepare(const Plan &p) {
     (void)p;
     if (!encoder()) return cudaErrorNotSupported;
-    cudaError_t err = cudaFuncSetAttribute(k_prefill_route<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(k_prefill_route<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+    cudaError_t err = cudaFuncSetAttribute(k_prefill_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(k_prefill_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
     if (err != cudaSuccess) return err;
@@ -921,15 +924,16 @@ cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, 
     k_prefill_wt<<<dim3(a.H / 32, Ew / 32), 256, 0, s>>>(a);
     {
         CUtensorMap twt;
-        if (!mat_map(a.wt, a.H, Ew, 4, kRtExp, kRtKc, false, &twt)) return cudaErrorInvalidValue;
+        CUtensorMap tx;  // x [T][H] bf16 bits (16-bit elements; the copy does not convert)
+        if (!mat_map(a.wt, a.H, Ew, 4, kRtExp, kRtKs, false, &twt) || !mat_map(a.x, a.T, a.H, 2, kRtKs, kRtTok, false, &tx))
+            return cudaErrorInvalidValue;
         const int grid = (a.T + kRtTok - 1) / kRtTok;
-        if (a.k <= 8) k_prefill_route<8><<<grid, kRtThreads, kRtSmem, s>>>(twt, a);
-        else k_prefill_route<16><<<grid, kRtThreads, kRtSmem, s>>>(twt, a);
+        k_prefill_route<<<grid, kRtThreads, kRtSmem, s>>>(twt, tx, a);
     }
     k_prefill_scan<<<1, 256, 0, s>>>(a);
     k_prefill_perm<<<a.E, 1024, 0, s>>>(a);
 
-    k_prefill_xperm<<<4 * p.sm_count, 256, 0, s>>>(a);
+    k_prefill_xperm<<<8 * p.sm_count, 256, 0, s>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 1, s)) != cudaSuccess) return err;
 

@@ -59,6 +59,10 @@ def check_prefill(layer, x_bits, r, sample):
             continue
         parity.same_by_id(r["ids"][t], r["w"][t], o_ids[t], o_w[t], atol=2e-6)
     assert near <= max(2, T // 100), f"{near} near-tie tokens of {T}"
+    # fp32 logits within half the tie threshold of the fp64 ones (so every token whose
+    # fp64 margin is >= the threshold is decided identically on both sides)
+    zerr = float(np.max(np.abs(r["logits"].astype(np.float64) - z64)))
+    assert zerr <= 0.5 * parity.TAU, f"router logits off by {zerr:.2e}"
     # same fp32 logits -> the same selection, bit for bit
     for t in range(0, T, max(1, T // 64)):
         assert np.array_equal(r["ids"][t], oracle.topk(r["logits"][t], s.top_k))
