@@ -388,6 +388,23 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t
         __nanosleep(20);
     }
 }
+// Whole warp, no sleep between polls (each try_wait already suspends the
+// thread for a while in hardware): for waits on the critical path of a
+// pipeline, where a sleep granule would show up as a bubble.
+__device__ __forceinline__ bool mbar_wait_warp_spin(uint32_t bar, uint32_t parity, long long budget) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_spin(bar, parity, budget);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) ok = mbar_wait_spin(bar, parity, budget);
+    return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ bool mbar_wait_warp_spin_cluster(uint32_t bar, uint32_t parity, long long budget) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_spin_cluster(bar, parity, budget);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) ok = mbar_wait_spin_cluster(bar, parity, budget);
+    return __all_sync(0xffffffffu, ok);
+}
 // Whole warp: lane 0 polls, then every lane takes one acquiring try_wait.
 __device__ __forceinline__ bool mbar_wait_warp_cluster(uint32_t bar, uint32_t parity, long long budget) {
     bool ok = true;

@@ -564,7 +564,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
                 for (int bi = 0; bi < nK / 4; ++bi, ++rstep) {
                     const int blk = ((4 * bi + ps.rot) % nK) >> 2;
                     const int r = rstep % kNR;
-                    if (rstep >= kNR && !mbar_wait_bounded(raw_empty + 8 * r, ((rstep / kNR) - 1) & 1, budget)) {
+                    if (rstep >= kNR && !mbar_wait_spin(raw_empty + 8 * r, ((rstep / kNR) - 1) & 1, budget)) {
                         fail();
                         return;
                     }
@@ -594,7 +594,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
                 const int hr = ps.n >> 1;  // rows per chunk half (multiple of 16, <= 128; <= 96 with two chunks)
                 for (int kb = 0; kb < nK; ++kb, ++step) {
                     const int s = step % kNS;
-                    if (step >= kNS && !mbar_wait_bounded_cluster(empty + 8 * s, ((step / kNS) - 1) & 1, budget)) {
+                    if (step >= kNS && !mbar_wait_spin_cluster(empty + 8 * s, ((step / kNS) - 1) & 1, budget)) {
                         fail();
                         return;
                     }
@@ -682,12 +682,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
             for (int kb = 0; kb < nK; ++kb, ++astep) {
                 const int j = kb & 3;  // the rotation is whole Q4_K blocks, so chunk j of a block is kb & 3
                 const int r = rstep % kNR;
-                if (j == 0 && !mbar_wait_warp(raw_full + 8 * r, (rstep / kNR) & 1, budget)) {
+                if (j == 0 && !mbar_wait_warp_spin(raw_full + 8 * r, (rstep / kNR) & 1, budget)) {
                     fail();
                     return;
                 }
                 const int s = astep % kNS;
-                if (astep >= kNS && !mbar_wait_warp_cluster(empty + 8 * s, ((astep / kNS) - 1) & 1, budget)) {
+                if (astep >= kNS && !mbar_wait_warp_spin_cluster(empty + 8 * s, ((astep / kNS) - 1) & 1, budget)) {
                     fail();
                     return;
                 }
@@ -771,7 +771,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
                 const int b = chunk % kNBuf;
                 const int nv = min(ps.n, ps.nt - c * ps.n);  // valid tokens of this chunk
                 const int rowc = ps.prow + ps.sc + c * ps.n;  // padded row of the chunk's first token
-                if (!mbar_wait_warp_cluster(d_full + 8 * b, (chunk / kNBuf) & 1, budget)) {
+                if (!mbar_wait_warp_spin_cluster(d_full + 8 * b, (chunk / kNBuf) & 1, budget)) {
                     fail();
                     return;
                 }
