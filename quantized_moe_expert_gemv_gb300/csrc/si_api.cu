@@ -74,6 +74,7 @@ PrefillLayout prefill_layout(const si_moe_desc &d, int n) {
     L.ids = take(pairs * sizeof(int32_t));
     L.wts = take(pairs * sizeof(float));
     L.counts = take((size_t)d.n_experts * sizeof(int32_t));
+    L.hist = take((size_t)((n + 31) / 32) * d.n_experts * sizeof(int32_t));
     L.offsets = take(((size_t)d.n_experts + 1) * sizeof(int32_t));
     L.poff = take(((size_t)d.n_experts + 1) * sizeof(int32_t));
     L.perm = take(pairs * sizeof(int32_t));
@@ -317,6 +318,7 @@ static si_status forward_prefill_impl(si_moe_plan_t plan, const si_moe_layer *la
     a.ids = reinterpret_cast<int32_t *>(sb + L.ids);
     a.wts = reinterpret_cast<float *>(sb + L.wts);
     a.counts = reinterpret_cast<int32_t *>(sb + L.counts);
+    a.hist = reinterpret_cast<int32_t *>(sb + L.hist);
     a.offsets = reinterpret_cast<int32_t *>(sb + L.offsets);
     a.rows = L.rows;
     a.wt = reinterpret_cast<float *>(sb + L.wt);

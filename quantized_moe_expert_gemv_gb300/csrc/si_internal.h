@@ -86,7 +86,7 @@ struct DecodeArgs {
 // Each expert's rows start at a multiple of 32 (padded offsets poff), so the
 // 32-row tiles of the GEMM epilogues never reach another expert's rows.
 struct PrefillLayout {
-    size_t ctrl, wt, logits, ids, wts, counts, offsets, poff, perm, pperm, inv, xp, h, y, total;
+    size_t ctrl, wt, logits, ids, wts, counts, hist, offsets, poff, perm, pperm, inv, xp, h, y, total;
     int64_t rows;  // padded row capacity: T*k + 32*E
 };
 PrefillLayout prefill_layout(const si_moe_desc &d, int n_tokens);
@@ -104,6 +104,7 @@ struct PrefillArgs {
     int32_t *ids;      // [T*k] pair p = t*k + slot
     float *wts;        // [T*k] renormalised routing weights
     int32_t *counts;   // [E]
+    int32_t *hist;     // [ceil(T/32)][E] pairs per expert of each 32-token chunk
     int32_t *offsets;  // [E+1] exclusive scan of counts
     int32_t *poff;     // [E+1] exclusive scan of counts rounded up to 32
     int32_t *perm;     // [T*k] pair ids ordered by expert, then pair id

@@ -109,7 +109,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     const int rot = (3 * blockIdx.x) % nst;
     const uint32_t full = smem_addr(sm + kRtOffBar);
     float(*s_z)[SI_MAX_EXPERTS] = reinterpret_cast<float(*)[SI_MAX_EXPERTS]>(sm + kRtOffZ);
+    __shared__ int s_hist[SI_MAX_EXPERTS];  // pairs of this chunk per expert
     int32_t *status = a.ctrl + kCtrlStatus;
+    for (int e = tid; e < a.E; e += kRtThreads) s_hist[e] = 0;
     if (tid == 0) {
         prefetch_tensormap(&tm_wt);
         prefetch_tensormap(&tm_x);
@@ -226,8 +228,11 @@ __global__ void __launch_bounds__(kRtThreads, 1)
             if (a.o_ids) a.o_ids[p] = myi;
             if (a.o_w) a.o_w[p] = w;
             atomicAdd(a.counts + myi, 1);
+            atomicAdd(s_hist + myi, 1);
         }
     }
+    __syncthreads();
+    for (int e = tid; e < a.E; e += kRtThreads) a.hist[(size_t)blockIdx.x * a.E + e] = s_hist[e];
 }
 
 // offsets[e] = counts[0] + ... + counts[e-1], offsets[E] = T*k; poff the same
@@ -261,42 +266,44 @@ __global__ void __launch_bounds__(256) k_prefill_scan(PrefillArgs a) {
     }
 }
 
-// One CTA per expert: an ordered stream compaction of the pair ids that chose
-// it (pair order), written at offsets[e].
-__global__ void __launch_bounds__(1024) k_prefill_perm(PrefillArgs a) {
-    __shared__ int s_warp[32];
-    __shared__ int s_base;
-    const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int off = a.offsets[e], poff = a.poff[e];
+// One CTA per 32-token chunk (its 32k pairs, in pair order): each pair's
+// position among its expert's pairs is the expert's offset, plus the pairs
+// of that expert in earlier chunks (from the router's per-chunk counts), plus
+// those earlier in this chunk (warp match masks and per-warp counts) -- the
+// stable order by pair id.  perm[pos] = p, inv[p] = its padded row,
+// pperm[row] = p; the CTAs also mark the padding rows (pperm = -1).
+__global__ void __launch_bounds__(512) k_prefill_perm(PrefillArgs a) {
+    __shared__ int s_base[SI_MAX_EXPERTS];
+    __shared__ int s_wcnt[16][SI_MAX_EXPERTS];  // [warp][expert] pairs of this chunk per warp
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x, nch = gridDim.x;
     const int np = a.T * a.k;
-    for (int r = poff + a.counts[e] + tid; r < a.poff[e + 1]; r += blockDim.x) {  // padding rows
-        a.pperm[r] = -1;
+    const int p = 32 * a.k * c + tid;  // this thread's pair (tid < 32k)
+    for (int e = tid; e < a.E; e += blockDim.x) {
+        int b = a.offsets[e];
+        for (int q = 0; q < c; ++q) b += __ldg(a.hist + (size_t)q * a.E + e);
+        s_base[e] = b;
+        for (int w = 0; w < 16; ++w) s_wcnt[w][e] = 0;
+        // padding rows of the experts this CTA owns
+        if (e % nch == c)
+            for (int r = a.poff[e] + a.counts[e]; r < a.poff[e + 1]; ++r) a.pperm[r] = -1;
     }
-    if (tid == 0) s_base = 0;
     __syncthreads();
-    for (int p0 = 0; p0 < np; p0 += 1024) {
-        const int p = p0 + tid;
-        const bool mine = p < np && __ldg(a.ids + p) == e;
-        const uint32_t bal = __ballot_sync(0xffffffffu, mine);
-        if (lane == 0) s_warp[warp] = __popc(bal);
-        __syncthreads();
-        int before = s_base;
-        for (int w = 0; w < warp; ++w) before += s_warp[w];
-        if (mine) {
-            const int j = before + __popc(bal & ((1u << lane) - 1u));  // rank among this expert's pairs
-            const int prow = poff + j;
-            a.perm[off + j] = p;
-            if (a.o_perm) a.o_perm[off + j] = p;
-            a.inv[p] = prow;
-            a.pperm[prow] = p;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            int tot = 0;
-            for (int w = 0; w < 32; ++w) tot += s_warp[w];
-            s_base += tot;
-        }
-        __syncthreads();
+    const bool mine = tid < 32 * a.k && p < np;
+    const int e = mine ? __ldg(a.ids + p) : -1 - lane;  // distinct dummies never match a real expert
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const int before = __popc(same & ((1u << lane) - 1u));
+    if (mine && before == 0) s_wcnt[warp][e] = __popc(same);
+    __syncthreads();
+    if (mine) {
+        int pos = s_base[e] + before;
+        for (int w = 0; w < warp; ++w) pos += s_wcnt[w][e];
+        const int j = pos - a.offsets[e];  // rank among the expert's pairs
+        const int prow = a.poff[e] + j;
+        a.perm[pos] = p;
+        if (a.o_perm) a.o_perm[pos] = p;
+        a.inv[p] = prow;
+        a.pperm[prow] = p;
     }
 }
 
@@ -931,7 +938,7 @@ cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, 
         k_prefill_route<<<grid, kRtThreads, kRtSmem, s>>>(twt, tx, a);
     }
     k_prefill_scan<<<1, 256, 0, s>>>(a);
-    k_prefill_perm<<<a.E, 1024, 0, s>>>(a);
+    k_prefill_perm<<<(a.T + 31) / 32, 512, 0, s>>>(a);
 
     k_prefill_xperm<<<8 * p.sm_count, 256, 0, s>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
