@@ -38,8 +38,9 @@ constexpr int kConsumerWarps = 8;
 constexpr int kExpertThreads = (kConsumerWarps + 1) * 32;
 constexpr long long kDrainBudget = 4000000000LL;  // cycles to wait for in-flight copies after an error
 constexpr int kMaxDownRowsPerLane = 4;            // rows per CTA <= 32
-constexpr int kStaticSmemReserve = 4096;
-constexpr int kPairsPerWarp = 2;                  // gate/up row pairs per warp per stage          // static shared memory of k_expert (routing table, flags)
+constexpr int kStaticSmemReserve = 4096;            // static shared memory of k_expert (routing table, flags)
+constexpr int kPairsPerWarp = 2;                  // gate/up row pairs per warp per stage
+constexpr int kHqStride = 20;                     // words per quantised h sub-block in shared memory (16 + pad)
 
 // ------------------------------------------------------------------ helpers
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
@@ -76,7 +77,9 @@ __device__ __forceinline__ float2 group_sum_pair(float g, float u, int li) {
 }
 
 // Per-token quantised activations in shared memory (deduplicated batches):
-// words [n][H/2], scales [n][H/64], sub-block sums [n][H/32].
+// words [n][32][H/64] (word p of every 64-column chunk together, so that the
+// lanes of a row, one chunk each, read word p from consecutive banks),
+// scales [n][H/64], sub-block sums [n][H/32].
 struct XQ {
     const uint32_t *w;
     const float *sc;
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
                 xqx[2 * c] = sa;
                 xqx[2 * c + 1] = sb;
 #pragma unroll
-                for (int p = 0; p < 32; ++p) xqw[(size_t)c * 32 + p] = wq[p];
+                for (int p = 0; p < 32; ++p) xqw[(size_t)t * a.H / 2 + p * (a.H / 64) + cc] = wq[p];
             }
             asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
             xq = XQ{xqw, xqs, xqx};
@@ -352,8 +355,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
                     const int nt_warp = __reduce_max_sync(0xffffffffu, nt);
                     for (int t = 0; t < nt_warp; ++t) {
                         const int tok = t < nt ? u->tok[s][t] : 0;
-                        const uint32_t *wrow = xq.w + (size_t)tok * a.H / 2 + 32 * chunk;
-                        auto xwf = [wrow](int pp) { return wrow[pp]; };
+                        const uint32_t *wrow = xq.w + (size_t)tok * a.H / 2 + chunk;
+                        const int cks = a.H / 64;
+                        auto xwf = [wrow, cks](int pp) { return wrow[pp * cks]; };
                         const float sc = xq.sc[tok * (a.H / 64) + chunk];
                         const float xa = xq.sum[tok * (a.H / 32) + 2 * chunk];
                         const float xb = xq.sum[tok * (a.H / 32) + 2 * chunk + 1];
@@ -405,9 +409,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
         const int nbI = a.I / kQK;
         const int rowd = nbI * kBlockBytes;
         const int nsub = a.I / 32;
-        // this warp's quantised copy of one h vector: words [I/2], scales [I/64], sums [I/32]
-        uint32_t *hq = reinterpret_cast<uint32_t *>(sm + a.fz_off_h) + (size_t)warp * (a.I / 2 + a.I / 64 + a.I / 32);
-        float *hsc = reinterpret_cast<float *>(hq + a.I / 2);
+        // this warp's quantised copy of one h vector: words [I/32][kHqStride] (16 words of a
+        // 32-value sub-block, padded so that neighbouring sub-blocks start in other banks),
+        // scales [I/64], sums [I/32]
+        uint32_t *hq = reinterpret_cast<uint32_t *>(sm + a.fz_off_h) +
+                       (size_t)warp * (a.I / 32 * kHqStride + a.I / 64 + a.I / 32);
+        float *hsc = reinterpret_cast<float *>(hq + a.I / 32 * kHqStride);
         float *hsum = hsc + a.I / 64;
         const int r8 = lane >> 2, i = lane & 3;
         // Chunk s lives in stage s % NSB.  Every stage is owned by one warp, which takes that
@@ -452,7 +459,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
                         for (int pp = 0; pp < 16; ++pp) {
                             const int lo = __float2int_rn(hv[2 * pp] * inv);
                             const int hi = __float2int_rn(hv[2 * pp + 1] * inv);
-                            hq[16 * sb + pp] = (uint32_t)(lo & 0xffff) | ((uint32_t)hi << 16);
+                            hq[kHqStride * sb + pp] = (uint32_t)(lo & 0xffff) | ((uint32_t)hi << 16);
                         }
                         hsum[sb] = sum;
                         if ((sb & 1) == 0) hsc[sb >> 1] = mx * (1.0f / 32767.0f);
@@ -462,11 +469,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
                 float acc[kMaxDownRowsPerLane] = {0.f, 0.f, 0.f, 0.f};
                 for (int bb = 0; bb < nbI; ++bb) {
                     const int c = 4 * bb + i;
-                    uint32_t hw[32];
-                    const uint4 *hqp = reinterpret_cast<const uint4 *>(hq + 32 * c);
+                    uint32_t hw[32];  // sub-blocks 2c and 2c+1
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        const uint4 v = hqp[q];
+                        const uint4 v = *reinterpret_cast<const uint4 *>(hq + kHqStride * (2 * c + (q >> 2)) + 4 * (q & 3));
                         hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
                     }
                     const float xs = hsc[c], Ha = hsum[2 * c], Hb = hsum[2 * c + 1];
@@ -534,7 +540,7 @@ bool expert_fused_layout(const si_moe_desc &d, int n, int grid, int smem_max, De
     const size_t x_bytes =
         dedup ? al((size_t)n * (d.hidden / 2 + d.hidden / 64 + d.hidden / 32) * 4) : 0;
     const size_t h_bytes =
-        al((size_t)kConsumerWarps * (d.intermediate / 2 + d.intermediate / 64 + d.intermediate / 32) * 4);
+        al((size_t)kConsumerWarps * (d.intermediate / 32 * kHqStride + d.intermediate / 64 + d.intermediate / 32) * 4);
     const size_t hs_bytes = 0;
     const size_t yw_bytes = al((size_t)umax * RB * 4);
     int NSA = nA_max < 4 ? (nA_max < 1 ? 1 : nA_max) : 4;
