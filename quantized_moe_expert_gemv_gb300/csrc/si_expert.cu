@@ -197,6 +197,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
     const uint32_t emptyB = fullB + 8 * NSB;
     int *lastA = reinterpret_cast<int *>(sm + a.fz_off_bar + 16 * (NSA + NSB));
     int *lastB = lastA + NSA;
+    // dedup phase B: every pair's h row, bulk-copied into the (then idle) phase-A stages
+    const uint32_t hbar = smem_addr(sm + a.fz_off_bar + ((20 * (NSA + NSB) + 7) & ~7));
+    const bool hstage = DEDUP && (size_t)a.n * a.k * a.I * sizeof(float) <= (size_t)NSA * stageA_bytes;
+    __shared__ int s_hcopy;
     int32_t *status = a.ctrl + kCtrlStatus;
 
     if (threadIdx.x == 0) {
@@ -211,6 +215,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
             lastB[st] = -1;
         }
         s_err = 0;
+        s_hcopy = 0;
+        mbar_init(hbar, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -237,8 +243,29 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
     {
         const long long P = (long long)U * a.I;
         const int G = gridDim.x, bid = blockIdx.x;
-        wk.p0 = (int)(P * bid / G);
-        wk.p1 = (int)(P * (bid + 1) / G);
+        if (DEDUP) {
+            // balance the phase-A dot products: row r of distinct expert s costs ntok[s] of
+            // them, so CTA b takes the rows whose cumulative cost falls in its 1/G share
+            long long W = 0;
+            for (int q = 0; q < U; ++q) W += (long long)rt.ntok[q] * a.I;
+            auto row_at = [&](long long target) -> int {  // first row pair whose cost start >= target
+                long long acc = 0;
+                for (int q = 0; q < U; ++q) {
+                    const long long c = (long long)rt.ntok[q] * a.I;
+                    if (acc + c > target) {
+                        const int nt = rt.ntok[q] > 0 ? rt.ntok[q] : 1;
+                        return q * a.I + (int)((target - acc + nt - 1) / nt);
+                    }
+                    acc += c;
+                }
+                return (int)P;
+            };
+            wk.p0 = row_at(W * bid / G);
+            wk.p1 = row_at(W * (bid + 1) / G);
+        } else {
+            wk.p0 = (int)(P * bid / G);
+            wk.p1 = (int)(P * (bid + 1) / G);
+        }
         wk.c0 = (int)((long long)a.H * bid / G);
         wk.nrows = (int)((long long)a.H * (bid + 1) / G) - wk.c0;
         wk.nA = (wk.p1 - wk.p0 + CH - 1) / CH;
@@ -395,6 +422,14 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
     if (warp == kConsumerWarps) {
         if (lane == 0 && !*verr) {
             const uint64_t pol = l2_evict_first_policy();
+            if (hstage) {  // h was written by all CTAs with ordinary stores; the copies read it
+                asm volatile("fence.proxy.async;" ::: "memory");
+                const uint32_t hrow = (uint32_t)(a.I * sizeof(float));
+                mbar_arrive_expect_tx(hbar, (uint32_t)(a.n * a.k) * hrow);
+                for (int q = 0; q < a.n * a.k; ++q)
+                    bulk_g2s(smem_addr(stA) + (uint32_t)q * hrow, a.h + (size_t)q * a.I, hrow, hbar, pol);
+                s_hcopy = 1;
+            }
             for (int s = NSB; s < wk.nB && ok; ++s)
                 produce_B(a, rt, wk, s, stB, fullB, emptyB, lastB, verr, pol, ok);
         }
@@ -417,6 +452,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
         float *hsc = reinterpret_cast<float *>(hq + a.I / 32 * kHqStride);
         float *hsum = hsc + a.I / 64;
         const int r8 = lane >> 2, i = lane & 3;
+        bool hready = hstage;
+        if (hstage && !__all_sync(0xffffffffu, mbar_wait_warp(hbar, 0, a.wait_budget))) {
+            set_status(status, SI_ERR_TIMEOUT);
+            *verr = 1;
+            hready = false;
+        }
         // Chunk s lives in stage s % NSB.  Every stage is owned by one warp, which takes that
         // stage's chunks in issue order, so no warp ever waits on a stage phase that is more
         // than one use ahead of the barrier (mbarrier phases are told apart by parity only).
@@ -440,11 +481,20 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
                     float hv[32];
                     float mx = 0.f, sum = 0.f;
                     if (sb < nsub) {
-                        const float4 *hp = reinterpret_cast<const float4 *>(a.h + (size_t)pair * a.I + 32 * sb);
+                        if (hready) {
+                            const float4 *hp = reinterpret_cast<const float4 *>(stA) + ((size_t)pair * a.I + 32 * sb) / 4;
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const float4 v = __ldcg(hp + q);
-                            hv[4 * q] = v.x, hv[4 * q + 1] = v.y, hv[4 * q + 2] = v.z, hv[4 * q + 3] = v.w;
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 v = hp[q];
+                                hv[4 * q] = v.x, hv[4 * q + 1] = v.y, hv[4 * q + 2] = v.z, hv[4 * q + 3] = v.w;
+                            }
+                        } else {
+                            const float4 *hp = reinterpret_cast<const float4 *>(a.h + (size_t)pair * a.I + 32 * sb);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 v = __ldcg(hp + q);
+                                hv[4 * q] = v.x, hv[4 * q + 1] = v.y, hv[4 * q + 2] = v.z, hv[4 * q + 3] = v.w;
+                            }
                         }
 #pragma unroll
                         for (int l = 0; l < 32; ++l) {
@@ -517,6 +567,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
             if (lastA[st] >= 0) mbar_wait_bounded(fullA + 8 * st, lastA[st], kDrainBudget);
         for (int st = 0; st < NSB; ++st)
             if (lastB[st] >= 0) mbar_wait_bounded(fullB + 8 * st, lastB[st], kDrainBudget);
+        if (s_hcopy) mbar_wait_bounded(hbar, 0, kDrainBudget);
     }
 }
 
