@@ -594,7 +594,10 @@ bool expert_fused_layout(const si_moe_desc &d, int n, int grid, int smem_max, De
         al((size_t)kConsumerWarps * (d.intermediate / 32 * kHqStride + d.intermediate / 64 + d.intermediate / 32) * 4);
     const size_t hs_bytes = 0;
     const size_t yw_bytes = al((size_t)umax * RB * 4);
-    int NSA = nA_max < 4 ? (nA_max < 1 ? 1 : nA_max) : 4;
+    // deduplicated batches spend their time computing in phase A (one row serves several tokens),
+    // so fewer A stages suffice there and the room goes to down-row stages for phase B
+    const int nsa_cap = dedup ? 3 : 4;
+    int NSA = nA_max < nsa_cap ? (nA_max < 1 ? 1 : nA_max) : nsa_cap;
     const size_t fixed = x_bytes + h_bytes + hs_bytes + yw_bytes;
     auto bar_bytes = [](int nsa, int nsb) { return (size_t)16 * (nsa + nsb) + (size_t)4 * (nsa + nsb) + 64; };
     const long long sA = (long long)stageA, sB = (long long)stageB;
@@ -610,6 +613,9 @@ bool expert_fused_layout(const si_moe_desc &d, int n, int grid, int smem_max, De
         while (NSB < umax && fits(NSA, NSB + 1)) ++NSB;
         if (NSB < 1) return false;
     }
+    // phase B: stage st belongs to consumer warp st % kConsumerWarps, so a multiple of the
+    // warp count gives every warp the same number of stages (and of experts)
+    if (NSB > kConsumerWarps) NSB -= NSB % kConsumerWarps;
     size_t off = 0;
     a.fz_off_a = (int)off;
     off += NSA * stageA;
