@@ -47,12 +47,12 @@ FALLBACK_HBM_GBS = 6800.0
 # kernel's sources are the ones that were profiled (sha256 over the files).
 PROFILED_TRAFFIC = {
     "k_expert_cluster": {
-        "bytes": 21289472,
+        "bytes": 21293312,
         "profile": "profiles/k_expert_cluster_qwen3_bs1.md",
         "sources": ["quantized_moe_expert_gemv_gb300/csrc/si_expert_cluster.cu",
                     "quantized_moe_expert_gemv_gb300/csrc/si_device.cuh",
                     "quantized_moe_expert_gemv_gb300/csrc/si_internal.h"],
-        "sha256": "00b40ab683079ef1d0b54849da3b6cad91973d2338b0ce7a94f0508fd6f18f1d",
+        "sha256": "6a1331b26dca16b93849b6227086ac7896fbb451bac6c80722d9f870109a31ec",
     },
 }
 
