@@ -580,6 +580,18 @@ def run_ours(args, dist):
             line["prefill"] = bench_prefill(args, dist, binding, device, synth, torch)
         except Exception as exc:
             line["prefill"] = {"error": repr(exc)}
+    # two-sided guard: an achieved fraction of a measured peak above 1.0 means the timed
+    # region did not do the work it is credited with
+    fracs = {"roofline": line["roofline"].get("frac"), "chain": line.get("chain", {}).get("frac_of_peak")}
+    for key in ("stack48", "dedup4"):
+        if isinstance(line.get(key), dict):
+            fracs[key] = line[key].get("frac_of_peak")
+    if isinstance(line.get("prefill"), dict) and "roofline" in line["prefill"]:
+        fracs["prefill"] = line["prefill"]["roofline"].get("frac")
+    over = {k: v for k, v in fracs.items() if v is not None and v > 1.0}
+    line["guard"] = {"max_frac_ok": not over, "over": over}
+    if over:
+        print("bench: achieved fraction above 1.0 -- rejected: %s" % over, file=sys.stderr)
     if dist.rank == 0 and not args.no_cpu_baseline:
         cores = cpu_cores()
         n = args.cpu_sample_tokens or max(64, 16 * cores)
