@@ -102,6 +102,8 @@ def test_prefill_single_token():
     (512, 256, 16, 4, 300),    # two blocks per gate row, one per down row
     (768, 768, 6, 3, 129),     # three blocks each way, ragged tiles
     (256, 256, 1, 1, 70),      # one expert
+    (256, 256, 160, 16, 96),   # two router expert passes (128 + 32), top-16
+    (512, 512, 40, 6, 777),    # ragged token chunks, one- and two-chunk passes
 ])
 def test_prefill_shapes(H, I, E, k, T):
     shape = synth.MoeShape(H, I, E, k)
