@@ -150,9 +150,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
     }
     // The token's H/64 activation chunks, quantised once (warp 0) into shared memory
     // before the dependency wait: the router launches this kernel only after its
-    // own wait on the producers of x, so x is final here.
+    // own wait on the producers of x, so x is final here.  Each chunk is a row of
+    // 32 words; its 16-byte unit q is stored at unit q ^ (row & 7), so that the
+    // lanes that load different rows into registers hit different banks.
     if (warp == 0 && lane < H / 64) {
-        uint32_t *xq = xq_s;                                   // [H/64][32] words
+        uint32_t *xq = xq_s;                                   // [H/64][32] words, 16-byte units swizzled
         float *xqf = reinterpret_cast<float *>(xq + H / 2);   // [H/64][3]: scale, Xa, Xb
         float xf[64];
         uint32_t wq[32];
@@ -171,7 +173,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
         const float sc = quantize64(xf, wq, sa, sb);
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            reinterpret_cast<uint4 *>(xq + 32 * lane)[q] = make_uint4(wq[4 * q], wq[4 * q + 1], wq[4 * q + 2], wq[4 * q + 3]);
+            reinterpret_cast<uint4 *>(xq + 32 * lane)[q ^ (lane & 7)] =
+                make_uint4(wq[4 * q], wq[4 * q + 1], wq[4 * q + 2], wq[4 * q + 3]);
         xqf[3 * lane] = sc;
         xqf[3 * lane + 1] = sa;
         xqf[3 * lane + 2] = sb;
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         uint32_t xw[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const uint4 v = reinterpret_cast<const uint4 *>(xq + 32 * chunk)[q];
+            const uint4 v = reinterpret_cast<const uint4 *>(xq + 32 * chunk)[q ^ (chunk & 7)];
             xw[4 * q] = v.x, xw[4 * q + 1] = v.y, xw[4 * q + 2] = v.z, xw[4 * q + 3] = v.w;
         }
         const float xs = xqf[3 * chunk], Xa = xqf[3 * chunk + 1], Xb = xqf[3 * chunk + 2];
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
 
     // --------------------------------------------------------- down + combine
     const bool skip = __any_sync(0xffffffffu, *verr != 0);
-    uint32_t *hq = xq_s;  // reuse: [4][32] words + [4][3]
+    uint32_t *hq = xq_s;  // reuse: [4][32] words (the same unit swizzle) + [4][3]
     float *hqf = reinterpret_cast<float *>(hq + 128);
     if (warp < kCW && !skip) {
         if (warp < 4) {  // the unit's four 64-column chunks of h: warp c quantises chunk c
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
             const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
-            hq[32 * warp + lane] = pack_q16(v.x, v.y, inv);
+            hq[32 * warp + 4 * ((lane >> 2) ^ warp) + (lane & 3)] = pack_q16(v.x, v.y, inv);
             if (lane == 0) {
                 hqf[3 * warp] = mx * (1.0f / 32767.0f);
                 hqf[3 * warp + 1] = sum;
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         uint32_t hw[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const uint4 v = reinterpret_cast<const uint4 *>(hq + 32 * i)[q];
+            const uint4 v = reinterpret_cast<const uint4 *>(hq + 32 * i)[q ^ i];
             hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
         }
         const float hs = hqf[3 * i], Ha = hqf[3 * i + 1], Hb = hqf[3 * i + 2];
