@@ -103,11 +103,20 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
     if (e < E) {
         float acc[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
         if (NJ > 0) {
+            // one partial per 256-column slice (independent chains), then a binary tree
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
+            for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
+                if (t < n) {
+                    float pj[NJ > 0 ? NJ : 1];
 #pragma unroll
-                for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
-                    if (t < n) acc[t] = dot8_bf16(wr[2 * j], wr[2 * j + 1], s_x[32 * (NJ * t + j) + lane], acc[t]);
+                    for (int j = 0; j < NJ; ++j)
+                        pj[j] = dot8_bf16(wr[2 * j], wr[2 * j + 1], s_x[32 * (NJ * t + j) + lane], 0.f);
+#pragma unroll
+                    for (int w2 = 1; w2 < NJ; w2 <<= 1) {
+#pragma unroll
+                        for (int j = 0; j + w2 < NJ; j += 2 * w2) pj[j] += pj[j + w2];
+                    }
+                    acc[t] = pj[0];
                 }
             }
         } else {
