@@ -24,6 +24,9 @@
  *   h      = silu(g) * u,  silu(g) = g / (1 + exp(-g))
  *   y      = W_down[e] h                          (H values)
  *   out    = sum_i w_i y_i
+ * and, optionally, the block around it: x replaced by rmsnorm(x) = x * gamma /
+ * sqrt(mean(x^2) + eps) on the way in and out = x + sum_i w_i y_i on the way
+ * out (a pre-normed block with its residual);
  * with every expert matrix stored as GGUF Q4_K super-blocks and read as
  * the fp32 weights the Q4_K decode defines.
  *
@@ -263,6 +266,66 @@ void or_moe_token(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_d
     free(x);
     free(y);
     free(acc);
+}
+
+/* Pre-MoE RMSNorm (the "rmsnorm" kernel of the sparkinfer README's "Layout"
+ * table runs before the MoE block of each layer):
+ *   xn_c = x_c * gamma_c / sqrt(mean_c(x_c^2) + eps)     (fp64) */
+void or_rmsnorm(const uint16_t *x_bf16, const float *gamma, float eps, int H, double *xn) {
+    double ss = 0.0;
+    for (int c = 0; c < H; ++c) {
+        double v = or_bf16_to_double(x_bf16[c]);
+        ss += v * v;
+    }
+    double inv = 1.0 / sqrt(ss / (double)H + (double)eps);
+    for (int c = 0; c < H; ++c) xn[c] = or_bf16_to_double(x_bf16[c]) * inv * (double)gamma[c];
+}
+
+/* One token through the pre-normed MoE block with its residual:
+ *   xn  = rmsnorm(x; gamma, eps)
+ *   z   = W_r xn (+ bias);  ids, w as in or_moe_token (top-k decided on
+ *         the logits rounded to fp32)
+ *   out = x + sum_i w_i W_down[e_i] (silu(W_gate[e_i] xn) * W_up[e_i] xn)
+ * Outputs: ids [k], w [k], out32 [H] (rounded once), optionally out64 [H]
+ * and the fp64 logits z [E]. */
+void or_moe_token_prenorm(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down,
+                          const float *router_w, const float *bias, const float *gamma, float eps,
+                          int H, int I, int E, int k, const uint16_t *x_bf16, int32_t *ids,
+                          double *w, float *out32, double *out64, double *z_out) {
+    double *xn = (double *)malloc(sizeof(double) * (size_t)H);
+    double *y = (double *)malloc(sizeof(double) * (size_t)H);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)H);
+    double *z = (double *)malloc(sizeof(double) * (size_t)E);
+    float *z32 = (float *)malloc(sizeof(float) * (size_t)E);
+    or_rmsnorm(x_bf16, gamma, eps, H, xn);
+    for (int e = 0; e < E; ++e) {
+        double s = 0.0;
+        for (int c = 0; c < H; ++c) s += (double)router_w[(int64_t)e * H + c] * xn[c];
+        if (bias) s += (double)bias[e];
+        z[e] = s;
+        z32[e] = (float)s;
+        if (z_out) z_out[e] = s;
+    }
+    or_topk(z32, E, k, ids);
+    or_renorm_weights(z, E, ids, k, w);
+    for (int c = 0; c < H; ++c) acc[c] = or_bf16_to_double(x_bf16[c]);  /* the residual */
+    int64_t gate_expert_bytes = (int64_t)I * (H / OR_QK) * OR_BLOCK_BYTES;
+    int64_t down_expert_bytes = (int64_t)H * (I / OR_QK) * OR_BLOCK_BYTES;
+    for (int i = 0; i < k; ++i) {
+        int e = ids[i];
+        or_expert_ffn(w_gate + e * gate_expert_bytes, w_up + e * gate_expert_bytes,
+                      w_down + e * down_expert_bytes, H, I, xn, NULL, y);
+        for (int c = 0; c < H; ++c) acc[c] += w[i] * y[c];
+    }
+    for (int c = 0; c < H; ++c) {
+        out32[c] = (float)acc[c];
+        if (out64) out64[c] = acc[c];
+    }
+    free(xn);
+    free(y);
+    free(acc);
+    free(z);
+    free(z32);
 }
 
 /* Grouped-prefill bookkeeping for T tokens routed top-k (ids [T][k]):

@@ -62,6 +62,11 @@ def _load():
             lib.or_moe_token.argtypes = [_c_u8p, _c_u8p, _c_u8p, _c_f32p, _c_f32p, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_u16p, _c_i32p,
                                          _c_f64p, _c_f32p, _c_f64p, _c_f64p]
+            lib.or_rmsnorm.argtypes = [_c_u16p, _c_f32p, ctypes.c_float, ctypes.c_int, _c_f64p]
+            lib.or_moe_token_prenorm.argtypes = [_c_u8p, _c_u8p, _c_u8p, _c_f32p, _c_f32p, _c_f32p,
+                                                 ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, _c_u16p, _c_i32p, _c_f64p, _c_f32p,
+                                                 _c_f64p, _c_f64p]
             lib.or_counts_offsets_perm.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    _c_i32p, _c_i32p, _c_i32p]
             _lib = lib
@@ -186,6 +191,54 @@ def moe_token(layer, x_bf16_row, want_h=False) -> TokenResult:
     return TokenResult(ids, w, out32, out64, h)
 
 
+def rmsnorm(x_bf16_row, gamma, eps: float) -> np.ndarray:
+    """fp64 x * gamma / sqrt(mean(x^2) + eps) of one bf16 row."""
+    x = np.ascontiguousarray(x_bf16_row, dtype=np.uint16)
+    g = np.ascontiguousarray(gamma, dtype=np.float32)
+    assert g.size == x.size
+    xn = np.empty(x.size, dtype=np.float64)
+    _load().or_rmsnorm(_ptr(x, _c_u16p), _ptr(g, _c_f32p), float(eps), x.size, _ptr(xn, _c_f64p))
+    return xn
+
+
+class PrenormResult:
+    __slots__ = ("ids", "w", "out32", "out64", "z")
+
+    def __init__(self, ids, w, out32, out64, z):
+        self.ids, self.w, self.out32, self.out64, self.z = ids, w, out32, out64, z
+
+    @property
+    def margin(self) -> float:
+        """z_(k) - z_(k+1) of the sorted fp64 logits (+inf when k == E)."""
+        k = self.ids.size
+        if k >= self.z.size:
+            return float("inf")
+        zs = np.sort(self.z)[::-1]
+        return float(zs[k - 1] - zs[k])
+
+
+def moe_token_prenorm(layer, x_bf16_row, gamma, eps: float) -> PrenormResult:
+    """out = x + MoE(rmsnorm(x)) for one token of a synth.MoeLayer-like object."""
+    s = layer.shape
+    H, I, E, k = s.hidden, s.intermediate, s.n_experts, s.top_k
+    x = np.ascontiguousarray(x_bf16_row, dtype=np.uint16)
+    g = np.ascontiguousarray(gamma, dtype=np.float32)
+    assert x.size == H and g.size == H
+    ids = np.empty(k, dtype=np.int32)
+    w = np.empty(k, dtype=np.float64)
+    out32 = np.empty(H, dtype=np.float32)
+    out64 = np.empty(H, dtype=np.float64)
+    z = np.empty(E, dtype=np.float64)
+    bias = None if layer.router_bias is None else np.ascontiguousarray(layer.router_bias,
+                                                                       dtype=np.float32)
+    _load().or_moe_token_prenorm(_ptr(layer.w_gate, _c_u8p), _ptr(layer.w_up, _c_u8p),
+                                 _ptr(layer.w_down, _c_u8p), _ptr(layer.router_w, _c_f32p),
+                                 _ptr(bias, _c_f32p), _ptr(g, _c_f32p), float(eps), H, I, E, k,
+                                 _ptr(x, _c_u16p), _ptr(ids, _c_i32p), _ptr(w, _c_f64p),
+                                 _ptr(out32, _c_f32p), _ptr(out64, _c_f64p), _ptr(z, _c_f64p))
+    return PrenormResult(ids, w, out32, out64, z)
+
+
 def counts_offsets_perm(ids: np.ndarray, n_experts: int):
     """Prefill bookkeeping for ids [T, k]: (counts [E], offsets [E+1], perm [T*k])."""
     ii = np.ascontiguousarray(ids, dtype=np.int32)
@@ -201,5 +254,5 @@ def counts_offsets_perm(ids: np.ndarray, n_experts: int):
 __all__ = [
     "build", "half_to_double", "bf16_to_double", "q4k_scale_min", "q4k_dequant",
     "router_logits", "topk", "renorm_weights", "route_tokens", "expert_ffn", "moe_token",
-    "TokenResult", "counts_offsets_perm",
+    "TokenResult", "counts_offsets_perm", "rmsnorm", "moe_token_prenorm", "PrenormResult",
 ]

@@ -107,6 +107,8 @@ class MoeLayer:
     w_down: np.ndarray        # uint8 [E, H, I/256, 144]
     router_w: np.ndarray      # float32 [E, H]
     router_bias: np.ndarray | None = None   # float32 [E] or None
+    norm_weight: np.ndarray | None = None   # float32 [H] RMSNorm gain (pre-normed block) or None
+    norm_eps: float = 1e-6
 
 
 def make_router_w(shape: MoeShape, seed: int, layer: int = 0) -> np.ndarray:
@@ -125,6 +127,12 @@ def make_layer(shape: MoeShape, seed: int, layer: int = 0,
     rw = make_router_w(shape, seed, layer)
     bias = None if router_bias is None else np.asarray(router_bias, dtype=np.float32).copy()
     return MoeLayer(shape, wg, wu, wd, rw, bias)
+
+
+def make_norm_weight(shape: MoeShape, seed: int, layer: int = 0) -> np.ndarray:
+    """RMSNorm gain of a pre-normed block: fp32 U[0.5, 1.5], [H]."""
+    g = rng(seed, layer, "norm")
+    return g.uniform(0.5, 1.5, size=shape.hidden).astype(np.float32)
 
 
 def make_tokens(shape: MoeShape, seed: int, n_tokens: int, stream: int | str = "x") -> np.ndarray:

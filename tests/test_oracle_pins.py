@@ -344,6 +344,70 @@ def test_router_bias_shifts_selection(oracle_lib):
         assert list(res.ids) == [5, 7]
 
 
+# ------------------------------------------------ pre-normed block + residual
+def test_rmsnorm_closed_forms(oracle_lib):
+    import math
+    three_four = synth.bf16_bits(np.array([3.0, 4.0], dtype=np.float32))
+    xn = oracle.rmsnorm(three_four, np.array([1.0, 2.0], dtype=np.float32), 0.0)
+    # mean square 12.5: 3 / sqrt(12.5) = 3 sqrt(2) / 5, 2 * 4 / sqrt(12.5) = 8 sqrt(2) / 5
+    np.testing.assert_allclose(xn, [3 * math.sqrt(2) / 5, 8 * math.sqrt(2) / 5], rtol=1e-15)
+    c = synth.bf16_bits(np.full(64, -2.5, dtype=np.float32))
+    gam = np.linspace(0.5, 1.5, 64).astype(np.float32)
+    np.testing.assert_allclose(oracle.rmsnorm(c, gam, 0.0), -gam.astype(np.float64), rtol=1e-15)
+    eps = 0.75
+    np.testing.assert_allclose(oracle.rmsnorm(c, gam, eps), -2.5 * gam.astype(np.float64) / math.sqrt(6.25 + eps),
+                               rtol=1e-15)
+    # without eps the norm is invariant to scaling x by a power of two (exact in bf16 and fp64)
+    xs = synth.make_tokens(synth.MoeShape(256, 256, 4, 2), seed=31, n_tokens=1)[0]
+    x2 = synth.bf16_bits(2.0 * synth.bf16_to_f32(xs))
+    assert np.array_equal(oracle.rmsnorm(xs, gam.repeat(4), 0.0), oracle.rmsnorm(x2, gam.repeat(4), 0.0))
+
+
+def test_prenorm_block_with_zero_experts_returns_the_residual(oracle_lib):
+    shape = synth.MoeShape(256, 256, 4, 2)
+    layer = synth.make_layer(shape, seed=32)
+    for name in ("w_gate", "w_up", "w_down"):
+        getattr(layer, name)[:] = 0  # d = dmin = 0: every weight is 0
+    xs = synth.make_tokens(shape, seed=32, n_tokens=3)
+    gam = synth.make_norm_weight(shape, seed=32)
+    for t in range(3):
+        res = oracle.moe_token_prenorm(layer, xs[t], gam, 1e-6)
+        assert np.array_equal(res.out32, synth.bf16_to_f32(xs[t]))
+
+
+def test_prenorm_block_on_unit_rms_input_is_x_plus_the_plain_block(oracle_lib):
+    """x of +-1 entries has mean square 1; with gain 1 and eps 0 the norm is the
+    identity, so the block is x + (the plain MoE FFN of x)."""
+    shape = synth.MoeShape(512, 256, 6, 3)
+    layer = synth.make_layer(shape, seed=33)
+    g = np.random.default_rng(33)
+    for _ in range(3):
+        x = synth.bf16_bits(g.choice([-1.0, 1.0], size=shape.hidden).astype(np.float32))
+        res = oracle.moe_token_prenorm(layer, x, np.ones(shape.hidden, np.float32), 0.0)
+        plain = oracle.moe_token(layer, x)
+        assert np.array_equal(res.ids, plain.ids)
+        np.testing.assert_allclose(res.w, plain.w, rtol=1e-13)
+        np.testing.assert_allclose(res.out64, synth.bf16_to_f32(x) + plain.out64, rtol=1e-12,
+                                   atol=1e-12 * np.abs(plain.out64).max())
+
+
+def test_prenorm_block_is_scale_invariant_up_to_the_residual(oracle_lib):
+    """eps = 0: block(2x) - 2x = block(x) - x (the norm removes the scale, the
+    residual keeps it)."""
+    shape = synth.MoeShape(256, 512, 8, 2)
+    layer = synth.make_layer(shape, seed=34, router_bias=np.linspace(-0.1, 0.1, 8))
+    gam = synth.make_norm_weight(shape, seed=34)
+    xs = synth.make_tokens(shape, seed=34, n_tokens=3)
+    for t in range(3):
+        x2 = synth.bf16_bits(2.0 * synth.bf16_to_f32(xs[t]))
+        a = oracle.moe_token_prenorm(layer, xs[t], gam, 0.0)
+        b = oracle.moe_token_prenorm(layer, x2, gam, 0.0)
+        assert np.array_equal(a.ids, b.ids)
+        xa = synth.bf16_to_f32(xs[t]).astype(np.float64)
+        np.testing.assert_allclose(b.out64 - 2 * xa, a.out64 - xa, rtol=1e-11,
+                                   atol=1e-11 * np.abs(a.out64 - xa).max())
+
+
 # --------------------------------------------------------- prefill bookkeeping
 def test_counts_offsets_perm_match_numpy(oracle_lib):
     g = np.random.default_rng(8)
