@@ -466,6 +466,38 @@ def bench_dedup4(args, dist, binding, device, synth, torch, hbm_peak):
             "gpu_launches": (2 if binding.si_debug_decode_fused(plan, n) >= 1 else 3) * S * steps}
 
 
+def bench_prenorm(args, dist, binding, device, synth, torch, hbm_peak):
+    """The headline decode workload as a pre-normed block with its residual
+    (out = x + MoE(x * gamma / rms(x))): 1024 sequential single-token calls."""
+    wl = synth.WORKLOADS["layer"]
+    shape, seed, T = wl["shape"], wl["seed"], 1024
+    layer = synth.make_layer(shape, seed=seed)
+    layer.norm_weight = synth.make_norm_weight(shape, seed=seed)
+    layer.norm_eps = 1e-6
+    dl = device.to_device(layer)
+    plan = binding.si_moe_plan(device.desc_for(shape), torch.cuda.current_device())
+    scratch = device.alloc_scratch(plan, binding.SI_MODE_DECODE, 1)
+    x = device.tokens_to_device(synth.make_tokens(shape, seed + dist.rank, T))
+    out = torch.empty((T, shape.hidden), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    g = build_layer_graph(binding, plan, dl.struct(), [x[t] for t in range(T)], [out[t] for t in range(T)],
+                          scratch, stream)
+    steps = max(1, args.steps // 2)
+    ms, clocks = time_graph(g, stream, steps, args.warmup, dist, ClockSampler(torch.cuda.current_device()))
+    st = binding.si_moe_read_status(plan, scratch, stream)
+    assert st == binding.SI_OK, binding.si_status_string(st)
+    tok_s = T * steps / (ms / 1e3)
+    expert_bytes = shape.top_k * shape.expert_bytes
+    gbs = expert_bytes * tok_s / 1e9
+    path = binding.si_debug_decode_fused(plan, 1)
+    del g
+    return {"workload": "qwen3-30b-a3b-moe-layer-decode-bs1 as a pre-normed block (RMSNorm gain U[0.5,1.5], "
+                        "eps 1e-6, residual added)",
+            "tok_per_s": dist.sum(tok_s), "us_per_token": 1e6 / tok_s, "expert_bytes_per_token": expert_bytes,
+            "achieved_gbs": gbs, "frac_of_peak": gbs / hbm_peak, "clocks": clocks,
+            "gpu_launches": {2: 2, 1: 2}.get(path, 3) * T * steps}
+
+
 def tensor_peak():
     """Dense 16-bit tensor-core peak (TFLOP/s): the measured bf16 GEMM figure
     (fp16 has the same dense rate on this part)."""
@@ -577,13 +609,18 @@ def run_ours(args, dist):
             line["dedup4"] = {"error": repr(exc)}
         torch.cuda.empty_cache()
         try:
+            line["prenorm"] = bench_prenorm(args, dist, binding, device, synth, torch, hbm_peak)
+        except Exception as exc:
+            line["prenorm"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+        try:
             line["prefill"] = bench_prefill(args, dist, binding, device, synth, torch)
         except Exception as exc:
             line["prefill"] = {"error": repr(exc)}
     # two-sided guard: an achieved fraction of a measured peak above 1.0 means the timed
     # region did not do the work it is credited with
     fracs = {"roofline": line["roofline"].get("frac"), "chain": line.get("chain", {}).get("frac_of_peak")}
-    for key in ("stack48", "dedup4"):
+    for key in ("stack48", "dedup4", "prenorm"):
         if isinstance(line.get(key), dict):
             fracs[key] = line[key].get("frac_of_peak")
     if isinstance(line.get("prefill"), dict) and "roofline" in line["prefill"]:

@@ -116,6 +116,15 @@ typedef struct si_moe_layer {
     const void *w_down;        /* Q4_K [E][H][I/256] */
     const float *router_w;     /* fp32 [E][H], row-major */
     const float *router_bias;  /* fp32 [E] added to the logits, or NULL */
+    /* Optional pre-normed block (sparkinfer README, "Layout": an RMSNorm kernel
+     * runs before the MoE block of each layer).  When norm_weight is non-NULL
+     * the call computes out = x + MoE(x * norm_weight / sqrt(mean(x^2) + norm_eps))
+     * for each token x: the MoE (router and experts) sees the normalised row,
+     * the output gets the un-normalised x back as the residual.  The norm is
+     * fused into the kernels that read x and the residual into the ones that
+     * write out; no extra launch.  NULL: out = MoE(x). */
+    const float *norm_weight;  /* fp32 [H] gain, 16-byte aligned, or NULL */
+    float norm_eps;            /* >= 0 and finite (used only with norm_weight) */
 } si_moe_layer;
 
 /* Optional routing outputs (device pointers; each may be NULL). */

@@ -169,6 +169,24 @@ void or_renorm_weights(const double *z, int E, const int32_t *ids, int k, double
     for (int i = 0; i < k; ++i) w[i] = (exp(z[ids[i]] - zmax) / total) / sel;
 }
 
+/* z_(k) - z_(k+1) of the fp64 logits (the k-th and (k+1)-th largest, found
+ * by repeated scan); +inf when k == E. */
+static double or_margin(const double *z, int E, int k) {
+    if (k >= E) return INFINITY;
+    unsigned char *taken = (unsigned char *)calloc((size_t)E, 1);
+    double kth = 0.0, next = 0.0;
+    for (int i = 0; i <= k; ++i) {
+        int best = -1;
+        for (int e = 0; e < E; ++e)
+            if (!taken[e] && (best < 0 || z[e] > z[best])) best = e;
+        taken[best] = 1;
+        if (i == k - 1) kth = z[best];
+        if (i == k) next = z[best];
+    }
+    free(taken);
+    return kth - next;
+}
+
 /* Route T tokens: ids [T][k], weights [T][k]; optionally the fp64 logits
  * [T][E] and each token's margin z_(k) - z_(k+1) (sorted fp64 logits;
  * +inf when k == E). */
@@ -184,25 +202,7 @@ void or_route_tokens(const float *router_w, const float *bias, const uint16_t *x
         or_renorm_weights(z, E, ids + (int64_t)t * k, k, w + (int64_t)t * k);
         if (z_out)
             for (int e = 0; e < E; ++e) z_out[(int64_t)t * E + e] = z[e];
-        if (margin) {
-            if (k >= E) {
-                margin[t] = INFINITY;
-            } else {
-                /* k-th and (k+1)-th largest fp64 logits by repeated scan */
-                unsigned char *taken = (unsigned char *)calloc((size_t)E, 1);
-                double kth = 0.0, next = 0.0;
-                for (int i = 0; i <= k; ++i) {
-                    int best = -1;
-                    for (int e = 0; e < E; ++e)
-                        if (!taken[e] && (best < 0 || z[e] > z[best])) best = e;
-                    taken[best] = 1;
-                    if (i == k - 1) kth = z[best];
-                    if (i == k) next = z[best];
-                }
-                free(taken);
-                margin[t] = kth - next;
-            }
-        }
+        if (margin) margin[t] = or_margin(z, E, k);
     }
     free(z);
     free(z32);
@@ -279,6 +279,34 @@ void or_rmsnorm(const uint16_t *x_bf16, const float *gamma, float eps, int H, do
     }
     double inv = 1.0 / sqrt(ss / (double)H + (double)eps);
     for (int c = 0; c < H; ++c) xn[c] = or_bf16_to_double(x_bf16[c]) * inv * (double)gamma[c];
+}
+
+/* Routing of T tokens of a pre-normed block: as or_route_tokens on
+ * rmsnorm(x) (fp64), with the same outputs. */
+void or_route_tokens_prenorm(const float *router_w, const float *bias, const float *gamma, float eps,
+                             const uint16_t *x_bf16, int T, int E, int H, int k, int32_t *ids,
+                             double *w, double *z_out, double *margin) {
+    double *xn = (double *)malloc(sizeof(double) * (size_t)H);
+    double *z = (double *)malloc(sizeof(double) * (size_t)E);
+    float *z32 = (float *)malloc(sizeof(float) * (size_t)E);
+    for (int t = 0; t < T; ++t) {
+        or_rmsnorm(x_bf16 + (int64_t)t * H, gamma, eps, H, xn);
+        for (int e = 0; e < E; ++e) {
+            double s = 0.0;
+            for (int c = 0; c < H; ++c) s += (double)router_w[(int64_t)e * H + c] * xn[c];
+            if (bias) s += (double)bias[e];
+            z[e] = s;
+            z32[e] = (float)s;
+        }
+        or_topk(z32, E, k, ids + (int64_t)t * k);
+        or_renorm_weights(z, E, ids + (int64_t)t * k, k, w + (int64_t)t * k);
+        if (z_out)
+            for (int e = 0; e < E; ++e) z_out[(int64_t)t * E + e] = z[e];
+        if (margin) margin[t] = or_margin(z, E, k);
+    }
+    free(xn);
+    free(z);
+    free(z32);
 }
 
 /* One token through the pre-normed MoE block with its residual:

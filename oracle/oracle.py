@@ -63,6 +63,9 @@ def _load():
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_u16p, _c_i32p,
                                          _c_f64p, _c_f32p, _c_f64p, _c_f64p]
             lib.or_rmsnorm.argtypes = [_c_u16p, _c_f32p, ctypes.c_float, ctypes.c_int, _c_f64p]
+            lib.or_route_tokens_prenorm.argtypes = [_c_f32p, _c_f32p, _c_f32p, ctypes.c_float, _c_u16p,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    _c_i32p, _c_f64p, _c_f64p, _c_f64p]
             lib.or_moe_token_prenorm.argtypes = [_c_u8p, _c_u8p, _c_u8p, _c_f32p, _c_f32p, _c_f32p,
                                                  ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_int, _c_u16p, _c_i32p, _c_f64p, _c_f32p,
@@ -201,6 +204,24 @@ def rmsnorm(x_bf16_row, gamma, eps: float) -> np.ndarray:
     return xn
 
 
+def route_tokens_prenorm(router_w, x_bf16, k, gamma, eps, bias=None):
+    """Routing of [T, H] tokens of a pre-normed block: (ids, w, z [T,E] f64, margin [T])."""
+    w_r = np.ascontiguousarray(router_w, dtype=np.float32)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    g = np.ascontiguousarray(gamma, dtype=np.float32)
+    E, H = w_r.shape
+    T = x.shape[0]
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    z = np.empty((T, E), dtype=np.float64)
+    margin = np.empty(T, dtype=np.float64)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    _load().or_route_tokens_prenorm(_ptr(w_r, _c_f32p), _ptr(b, _c_f32p), _ptr(g, _c_f32p), float(eps),
+                                    _ptr(x, _c_u16p), T, E, H, k, _ptr(ids, _c_i32p), _ptr(w, _c_f64p),
+                                    _ptr(z, _c_f64p), _ptr(margin, _c_f64p))
+    return ids, w, z, margin
+
+
 class PrenormResult:
     __slots__ = ("ids", "w", "out32", "out64", "z")
 
@@ -254,5 +275,5 @@ def counts_offsets_perm(ids: np.ndarray, n_experts: int):
 __all__ = [
     "build", "half_to_double", "bf16_to_double", "q4k_scale_min", "q4k_dequant",
     "router_logits", "topk", "renorm_weights", "route_tokens", "expert_ffn", "moe_token",
-    "TokenResult", "counts_offsets_perm", "rmsnorm", "moe_token_prenorm", "PrenormResult",
+    "TokenResult", "counts_offsets_perm", "rmsnorm", "moe_token_prenorm", "PrenormResult", "route_tokens_prenorm",
 ]

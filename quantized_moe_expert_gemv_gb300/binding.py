@@ -51,7 +51,8 @@ class si_moe_desc(ctypes.Structure):
 
 class si_moe_layer(ctypes.Structure):
     _fields_ = [("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
-                ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p)]
+                ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+                ("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float)]
 
 
 class si_moe_route_out(ctypes.Structure):
@@ -201,8 +202,10 @@ def si_moe_scratch_init(plan: Plan, scratch, stream=None):
            "si_moe_scratch_init")
 
 
-def layer_struct(w_gate, w_up, w_down, router_w, router_bias=None) -> si_moe_layer:
-    return si_moe_layer(_ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(router_w), _ptr(router_bias))
+def layer_struct(w_gate, w_up, w_down, router_w, router_bias=None, norm_weight=None,
+                 norm_eps: float = 0.0) -> si_moe_layer:
+    return si_moe_layer(_ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(router_w), _ptr(router_bias),
+                        _ptr(norm_weight), float(norm_eps))
 
 
 def route_struct(topk_ids=None, topk_w=None, expert_counts=None, expert_offsets=None, perm=None,

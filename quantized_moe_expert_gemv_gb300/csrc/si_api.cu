@@ -75,6 +75,8 @@ PrefillLayout prefill_layout(const si_moe_desc &d, int n) {
     L.wts = take(pairs * sizeof(float));
     L.counts = take((size_t)d.n_experts * sizeof(int32_t));
     L.hist = take((size_t)((n + 31) / 32) * d.n_experts * sizeof(int32_t));
+    L.rms = take((size_t)n * sizeof(float));
+    L.rrow = take(rows * sizeof(float));
     L.offsets = take(((size_t)d.n_experts + 1) * sizeof(int32_t));
     L.poff = take(((size_t)d.n_experts + 1) * sizeof(int32_t));
     L.perm = take(pairs * sizeof(int32_t));
@@ -223,8 +225,10 @@ static si_status forward_decode_impl(si_moe_plan_t plan, const si_moe_layer *lay
     if (n_tokens < 1 || n_tokens > SI_MAX_DECODE_TOKENS) return SI_ERR_INVALID_ARG;
     if (!aligned(layer->w_gate, 16) || !aligned(layer->w_up, 16) || !aligned(layer->w_down, 16) ||
         !aligned(layer->router_w, 16) || !aligned(x_bf16, 16) || !aligned(out, 16) ||
-        !aligned(scratch, 16) || (layer->router_bias && !aligned(layer->router_bias, 4)))
+        !aligned(scratch, 16) || (layer->router_bias && !aligned(layer->router_bias, 4)) ||
+        (layer->norm_weight && !aligned(layer->norm_weight, 16)))
         return SI_ERR_MISALIGNED;
+    if (layer->norm_weight && !(layer->norm_eps >= 0.f && layer->norm_eps <= 3.0e38f)) return SI_ERR_INVALID_ARG;
     if (ro && ((ro->topk_ids && !aligned(ro->topk_ids, 4)) || (ro->topk_w && !aligned(ro->topk_w, 4)) ||
                (ro->expert_counts && !aligned(ro->expert_counts, 4)) ||
                (ro->logits && !aligned(ro->logits, 4))))
@@ -239,6 +243,8 @@ static si_status forward_decode_impl(si_moe_plan_t plan, const si_moe_layer *lay
     a.wd = static_cast<const uint8_t *>(layer->w_down);
     a.router_w = layer->router_w;
     a.router_bias = layer->router_bias;
+    a.norm_w = layer->norm_weight;
+    a.norm_eps = layer->norm_weight ? layer->norm_eps : 0.f;
     a.x = static_cast<const uint16_t *>(x_bf16);
     a.out = out;
     a.H = d.hidden;
@@ -289,8 +295,10 @@ static si_status forward_prefill_impl(si_moe_plan_t plan, const si_moe_layer *la
     if (n_tokens < 1 || n_tokens > d.max_tokens) return SI_ERR_INVALID_ARG;
     if (!aligned(layer->w_gate, 16) || !aligned(layer->w_up, 16) || !aligned(layer->w_down, 16) ||
         !aligned(layer->router_w, 16) || !aligned(x_bf16, 16) || !aligned(out, 16) ||
-        !aligned(scratch, 16) || (layer->router_bias && !aligned(layer->router_bias, 4)))
+        !aligned(scratch, 16) || (layer->router_bias && !aligned(layer->router_bias, 4)) ||
+        (layer->norm_weight && !aligned(layer->norm_weight, 16)))
         return SI_ERR_MISALIGNED;
+    if (layer->norm_weight && !(layer->norm_eps >= 0.f && layer->norm_eps <= 3.0e38f)) return SI_ERR_INVALID_ARG;
     if (ro && ((ro->topk_ids && !aligned(ro->topk_ids, 4)) || (ro->topk_w && !aligned(ro->topk_w, 4)) ||
                (ro->expert_counts && !aligned(ro->expert_counts, 4)) ||
                (ro->expert_offsets && !aligned(ro->expert_offsets, 4)) || (ro->perm && !aligned(ro->perm, 4)) ||
@@ -306,6 +314,8 @@ static si_status forward_prefill_impl(si_moe_plan_t plan, const si_moe_layer *la
     a.wd = static_cast<const uint8_t *>(layer->w_down);
     a.router_w = layer->router_w;
     a.router_bias = layer->router_bias;
+    a.norm_w = layer->norm_weight;
+    a.norm_eps = layer->norm_weight ? layer->norm_eps : 0.f;
     a.x = static_cast<const uint16_t *>(x_bf16);
     a.out = out;
     a.H = d.hidden;
@@ -319,6 +329,8 @@ static si_status forward_prefill_impl(si_moe_plan_t plan, const si_moe_layer *la
     a.wts = reinterpret_cast<float *>(sb + L.wts);
     a.counts = reinterpret_cast<int32_t *>(sb + L.counts);
     a.hist = reinterpret_cast<int32_t *>(sb + L.hist);
+    a.rms = reinterpret_cast<float *>(sb + L.rms);
+    a.rrow = reinterpret_cast<float *>(sb + L.rrow);
     a.offsets = reinterpret_cast<int32_t *>(sb + L.offsets);
     a.rows = L.rows;
     a.wt = reinterpret_cast<float *>(sb + L.wt);

@@ -36,7 +36,21 @@ __device__ __forceinline__ float dot8_bf16(const float4 &w0, const float4 &w1, c
     return s;
 }
 
-// Router + top-k, one thread-block cluster (or one CTA for small E).  Warp
+// Sum of squares of the 8 bf16 values of xv, added to s.
+__device__ __forceinline__ float sumsq8_bf16(const uint4 &xv, float s) {
+    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float lo = __uint_as_float(w[q] << 16), hi = __uint_as_float(w[q] & 0xffff0000u);
+        s = fmaf(lo, lo, s);
+        s = fmaf(hi, hi, s);
+    }
+    return s;
+}
+
+// Router + top-k, one thread-block cluster (or one CTA for small E).  NORM (a
+// pre-normed block): the router rows are scaled by the RMSNorm gain in
+// registers and each warp scales its logit by the token's 1 / rms.  Warp
 // w of CTA c owns expert e = c*WPC + w.  NJ > 0: H == 256*NJ and the
 // expert's router row is loaded into registers before the programmatic-
 // dependent-launch wait (router weights do not depend on the token, so this
@@ -47,7 +61,7 @@ __device__ __forceinline__ float dot8_bf16(const float4 &w0, const float4 &w1, c
 // pair order).  One token feeding the cluster expert kernel (sel_logits):
 // every CTA receives every logit, each warp ranks its own expert and stores
 // the selected ones at their rank; the expert kernel forms the weights.
-template <int NJ>
+template <int NJ, bool NORM>
 __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs a) {
     __shared__ float s_z[SI_MAX_DECODE_TOKENS][SI_MAX_EXPERTS];
     __shared__ int s_ids[SI_MAX_DECODE_TOKENS][SI_MAX_TOPK];
@@ -60,6 +74,8 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
     const uint16_t *const xg_p = pin_ptr(a.x);
     float *const out_p = pin_ptr(a.out);
     const float *const bias_p = pin_ptr(a.router_bias);
+    const float *const gam_p = NORM ? pin_ptr(a.norm_w) : nullptr;  // pre-normed block: RMSNorm gain
+    const float norm_eps = a.norm_eps;
     float *const ologits_p = pin_ptr(a.o_logits);
     int32_t *const ids_p = pin_ptr(a.ids);
     float *const wts_p = pin_ptr(a.wts);
@@ -81,6 +97,16 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
             wr[2 * j + 1] = __ldg(reinterpret_cast<const float4 *>(wrow + 256 * j + 8 * lane + 4));
         }
     }
+    if (NJ > 0 && gam_p) {  // pre-normed block: z = r * sum_c (W[e][c] * gamma_c) * x_c
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gam_p + 256 * j + 8 * lane));
+            const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gam_p + 256 * j + 8 * lane + 4));
+            wr[2 * j] = make_float4(wr[2 * j].x * g0.x, wr[2 * j].y * g0.y, wr[2 * j].z * g0.z, wr[2 * j].w * g0.w);
+            wr[2 * j + 1] = make_float4(wr[2 * j + 1].x * g1.x, wr[2 * j + 1].y * g1.y, wr[2 * j + 1].z * g1.z,
+                                        wr[2 * j + 1].w * g1.w);
+        }
+    }
     if (NJ > 0) {  // the router rows must be in registers before the wait, not fetched after it
 #pragma unroll
         for (int j = 0; j < 2 * NJ; ++j)
@@ -97,11 +123,22 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
     }
     if (zero_out) {         // the cluster expert kernel accumulates the top-k combine into out
         const int nthr = gridDim.x * blockDim.x;
-        for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n * H; q += nthr) out_p[q] = 0.f;
+        for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n * H; q += nthr)
+            out_p[q] = gam_p ? bf16_bits_to_f32(__ldg(xg_p + q)) : 0.f;  // the residual, or nothing
     }
     if (NJ > 0) __syncthreads();
     if (e < E) {
         float acc[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
+        float ss[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};  // sum of squares of x (pre-normed block)
+        if (NJ > 0 && gam_p) {
+#pragma unroll
+            for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
+                if (t < n) {
+#pragma unroll
+                    for (int j = 0; j < NJ; ++j) ss[t] = sumsq8_bf16(s_x[32 * (NJ * t + j) + lane], ss[t]);
+                }
+            }
+        }
         if (NJ > 0) {
             // one partial per 256-column slice (independent chains), then a binary tree
 #pragma unroll
@@ -121,13 +158,20 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
             }
         } else {
             for (int c = 8 * lane; c < H; c += 256) {
-                const float4 w0 = __ldg(reinterpret_cast<const float4 *>(wrow + c));
-                const float4 w1 = __ldg(reinterpret_cast<const float4 *>(wrow + c + 4));
+                float4 w0 = __ldg(reinterpret_cast<const float4 *>(wrow + c));
+                float4 w1 = __ldg(reinterpret_cast<const float4 *>(wrow + c + 4));
+                if (gam_p) {
+                    const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gam_p + c));
+                    const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gam_p + c + 4));
+                    w0 = make_float4(w0.x * g0.x, w0.y * g0.y, w0.z * g0.z, w0.w * g0.w);
+                    w1 = make_float4(w1.x * g1.x, w1.y * g1.y, w1.z * g1.z, w1.w * g1.w);
+                }
 #pragma unroll
                 for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
                     if (t < n) {
                         const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(xg_p + (size_t)t * H + c));
                         acc[t] = dot8_bf16(w0, w1, xv, acc[t]);
+                        if (gam_p) ss[t] = sumsq8_bf16(xv, ss[t]);
                     }
                 }
             }
@@ -136,6 +180,7 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
         for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
             if (t < n) {
                 float z = warp_sum(acc[t]);
+                if (gam_p) z *= rms_scale(warp_sum(ss[t]), H, norm_eps);
                 if (bias_p) z += __ldg(bias_p + e);
                 if (sel_logits) {  // every CTA of the cluster gets every logit (lane c -> CTA c)
                     if (lane < (int)gridDim.x) {
@@ -303,6 +348,19 @@ __global__ void __launch_bounds__(kThreads) k_gateup_generic(DecodeArgs a) {
     const int nH = a.n * a.H;
     for (int i = threadIdx.x; i < nH; i += kThreads) xs[i] = bf16_bits_to_f32(a.x[i]);
     __syncthreads();
+    if (a.norm_w) {  // pre-normed block: the experts see x * gamma / rms(x)
+        __shared__ float s_r[SI_MAX_DECODE_TOKENS];
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (warp < a.n) {
+            float ss = 0.f;
+            for (int c = lane; c < a.H; c += 32) ss = fmaf(xs[warp * a.H + c], xs[warp * a.H + c], ss);
+            ss = warp_sum(ss);
+            if (lane == 0) s_r[warp] = rms_scale(ss, a.H, a.norm_eps);
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < nH; i += kThreads) xs[i] = xs[i] * s_r[i / a.H] * __ldg(a.norm_w + i % a.H);
+        __syncthreads();
+    }
     for (int i = threadIdx.x; i < nH / 32; i += kThreads) {
         float s = 0.f;
         for (int l = 0; l < 32; ++l) s += xs[32 * i + l];
@@ -395,7 +453,8 @@ __global__ void __launch_bounds__(kThreads) k_down_generic(DecodeArgs a) {
     if (gl == 0 && c < a.H) {
 #pragma unroll
         for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t)
-            if (t < a.n) a.out[(size_t)t * a.H + c] = acc[t];
+            if (t < a.n)  // plus the residual x in a pre-normed block
+                a.out[(size_t)t * a.H + c] = a.norm_w ? acc[t] + bf16_bits_to_f32(a.x[(size_t)t * a.H + c]) : acc[t];
     }
 }
 
@@ -437,7 +496,8 @@ static cudaError_t launch_router_t(const DecodeArgs &a, cudaStream_t s) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_router_topk<NJ>, a);
+    return a.norm_w ? cudaLaunchKernelEx(&cfg, k_router_topk<NJ, true>, a)
+                    : cudaLaunchKernelEx(&cfg, k_router_topk<NJ, false>, a);
 }
 
 static cudaError_t launch_router(const DecodeArgs &a, cudaStream_t s) {

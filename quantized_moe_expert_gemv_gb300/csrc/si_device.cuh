@@ -40,6 +40,12 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
     return __uint_as_float(bits16 << 16);
 }
 
+// RMSNorm scale of a row of H values from its sum of squares:
+// 1 / sqrt(sumsq / H + eps) (IEEE square root and division).
+__device__ __forceinline__ float rms_scale(float sumsq, int H, float eps) {
+    return 1.0f / sqrtf(sumsq / (float)H + eps);
+}
+
 // ------------------------------------------------------- packed fp32 pairs
 typedef unsigned long long f32x2;
 

@@ -176,7 +176,7 @@ __device__ void produce_B(const DecodeArgs &a, const SmemRoute &rt, const Expert
 }
 
 // ------------------------------------------------------------------ kernel
-template <int NBH, bool DEDUP>
+template <int NBH, bool DEDUP, bool NORM>
 __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t sm[];
     constexpr int GS = 4 * NBH;   // lanes per gate/up row
@@ -309,11 +309,43 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
                     xf[8 * q + 2 * e2 + 1] = __uint_as_float(wv[e2] & 0xffff0000u);
                 }
             }
+            if (NORM) {  // pre-normed block: the GS lanes of a group hold all H/64 chunks of x
+                float ss = 0.f;
+#pragma unroll
+                for (int q = 0; q < 64; ++q) ss = fmaf(xf[q], xf[q], ss);
+#pragma unroll
+                for (int o = 1; o < GS; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float r = rms_scale(ss, a.H, a.norm_eps);
+                const float4 *gp = reinterpret_cast<const float4 *>(a.norm_w + 64 * chunk);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float4 gv = __ldg(gp + q);
+                    xf[4 * q] *= r * gv.x;
+                    xf[4 * q + 1] *= r * gv.y;
+                    xf[4 * q + 2] *= r * gv.z;
+                    xf[4 * q + 3] *= r * gv.w;
+                }
+            }
             xs = quantize64(xf, xw, Xa, Xb);
         } else {
             uint32_t *xqw = reinterpret_cast<uint32_t *>(sm + a.fz_off_x);  // [n][H/2]
             float *xqs = reinterpret_cast<float *>(xqw + (size_t)a.n * a.H / 2);  // [n][H/64]
             float *xqx = xqs + (size_t)a.n * a.H / 64;                          // [n][H/32]
+            __shared__ float s_rms[SI_MAX_DECODE_TOKENS];
+            if (NORM) {  // pre-normed block: warp t finds 1 / rms of token t
+                if (warp < a.n) {
+                    float ss = 0.f;
+                    for (int c = 2 * lane; c < a.H; c += 64) {
+                        const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(a.x + (size_t)warp * a.H + c));
+                        const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+                        ss = fmaf(lo, lo, ss);
+                        ss = fmaf(hi, hi, ss);
+                    }
+                    ss = warp_sum(ss);
+                    if (lane == 0) s_rms[warp] = rms_scale(ss, a.H, a.norm_eps);
+                }
+                asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+            }
             for (int c = threadIdx.x; c < a.n * a.H / 64; c += kConsumerWarps * 32) {
                 const int t = c / (a.H / 64), cc = c - t * (a.H / 64);
                 float xf[64];
@@ -327,6 +359,18 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
                     for (int e2 = 0; e2 < 4; ++e2) {
                         xf[8 * q + 2 * e2] = __uint_as_float(wv[e2] << 16);
                         xf[8 * q + 2 * e2 + 1] = __uint_as_float(wv[e2] & 0xffff0000u);
+                    }
+                }
+                if (NORM) {
+                    const float r = s_rms[t];
+                    const float4 *gp = reinterpret_cast<const float4 *>(a.norm_w + 64 * cc);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float4 gv = __ldg(gp + q);
+                        xf[4 * q] *= r * gv.x;
+                        xf[4 * q + 1] *= r * gv.y;
+                        xf[4 * q + 2] *= r * gv.z;
+                        xf[4 * q + 3] *= r * gv.w;
                     }
                 }
                 float sa, sb;
@@ -559,6 +603,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
             const int t = idx / wk.nrows, lr = idx - t * wk.nrows;
             float sacc = 0.f;
             for (int slot = 0; slot < a.k; ++slot) sacc += yw[(size_t)(t * a.k + slot) * RB + lr];
+            if (NORM) sacc += bf16_bits_to_f32(a.x[(size_t)t * a.H + wk.c0 + lr]);  // the residual
             a.out[(size_t)t * a.H + wk.c0 + lr] = sacc;
         }
     } else if (threadIdx.x == 0) {
@@ -641,7 +686,8 @@ bool expert_fused_layout(const si_moe_desc &d, int n, int grid, int smem_max, De
 
 template <int NBH, bool DEDUP>
 static cudaError_t launch_expert_t(const DecodeArgs &a, int grid, cudaStream_t s) {
-    auto kern = k_expert<NBH, DEDUP>;  // dynamic smem limit raised at plan time
+    // dynamic smem limits raised at plan time; NORM: pre-normed block
+    auto kern = a.norm_w ? k_expert<NBH, DEDUP, true> : k_expert<NBH, DEDUP, false>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kExpertThreads);
@@ -667,22 +713,37 @@ cudaError_t launch_expert_fused(const DecodeArgs &a, int grid, cudaStream_t s) {
 }
 
 cudaError_t expert_fused_occupancy(int nbh, bool dedup, int smem, int smem_max, int *blocks_per_sm) {
-    const void *f = nullptr;
+#define SI_FZ_PAIR(B) \
+    (dedup ? fs2{(const void *)k_expert<B, true, false>, (const void *)k_expert<B, true, true>} \
+           : fs2{(const void *)k_expert<B, false, false>, (const void *)k_expert<B, false, true>})
+    struct fs2 {
+        const void *f[2];
+    };
+    fs2 fs{};
     switch (nbh) {
-        case 1: f = dedup ? (const void *)k_expert<1, true> : (const void *)k_expert<1, false>; break;
-        case 2: f = dedup ? (const void *)k_expert<2, true> : (const void *)k_expert<2, false>; break;
-        case 4: f = dedup ? (const void *)k_expert<4, true> : (const void *)k_expert<4, false>; break;
-        default: f = dedup ? (const void *)k_expert<8, true> : (const void *)k_expert<8, false>; break;
+        case 1: fs = SI_FZ_PAIR(1); break;
+        case 2: fs = SI_FZ_PAIR(2); break;
+        case 4: fs = SI_FZ_PAIR(4); break;
+        default: fs = SI_FZ_PAIR(8); break;
     }
-    cudaFuncAttributes fa;
-    cudaError_t err = cudaFuncGetAttributes(&fa, f);
-    if (err != cudaSuccess) return err;
-    // the opt-in limit covers static + dynamic shared memory
-    const int dyn_max = smem_max - (int)fa.sharedSizeBytes;
-    if (smem > dyn_max) return cudaErrorInvalidValue;
-    err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
-    if (err != cudaSuccess) return err;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, f, kExpertThreads, smem);
+#undef SI_FZ_PAIR
+    int least = 1 << 30;
+    for (const void *f : fs.f) {  // plain and pre-normed block: both must fit
+        cudaFuncAttributes fa;
+        cudaError_t err = cudaFuncGetAttributes(&fa, f);
+        if (err != cudaSuccess) return err;
+        // the opt-in limit covers static + dynamic shared memory
+        const int dyn_max = smem_max - (int)fa.sharedSizeBytes;
+        if (smem > dyn_max) return cudaErrorInvalidValue;
+        err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
+        if (err != cudaSuccess) return err;
+        int n = 0;
+        if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kExpertThreads, smem)) != cudaSuccess)
+            return err;
+        least = n < least ? n : least;
+    }
+    *blocks_per_sm = least;
+    return cudaSuccess;
 }
 
 }  // namespace si

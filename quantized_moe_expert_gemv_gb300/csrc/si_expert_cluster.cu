@@ -76,7 +76,7 @@ __device__ __forceinline__ float pair_sum(float g, float u, int li) {
 }
 }  // namespace
 
-template <int NBH>
+template <int NBH, bool NORM>
 __global__ void __launch_bounds__(kClThreads, 1)
     k_expert_cluster(const __grid_constant__ CUtensorMap tmap_down, const __grid_constant__ CUtensorMap tmap_tail,
                      DecodeArgs a) {
@@ -168,6 +168,23 @@ __global__ void __launch_bounds__(kClThreads, 1)
             for (int e2 = 0; e2 < 4; ++e2) {
                 xf[8 * q + 2 * e2] = __uint_as_float(wv[e2] << 16);
                 xf[8 * q + 2 * e2 + 1] = __uint_as_float(wv[e2] & 0xffff0000u);
+            }
+        }
+        if (NORM) {  // pre-normed block: quantise x * gamma / rms(x) (lanes 0..H/64-1 hold all of x)
+            float ss = 0.f;
+#pragma unroll
+            for (int q = 0; q < 64; ++q) ss = fmaf(xf[q], xf[q], ss);
+            const unsigned mask = H / 64 == 32 ? 0xffffffffu : (1u << (H / 64)) - 1u;
+            for (int o = 1; o < H / 64; o <<= 1) ss += __shfl_xor_sync(mask, ss, o);
+            const float r = rms_scale(ss, H, a.norm_eps);
+            const float4 *gp = reinterpret_cast<const float4 *>(a.norm_w + 64 * lane);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float4 g = __ldg(gp + q);
+                xf[4 * q] *= r * g.x;
+                xf[4 * q + 1] *= r * g.y;
+                xf[4 * q + 2] *= r * g.z;
+                xf[4 * q + 3] *= r * g.w;
             }
         }
         const float sc = quantize64(xf, wq, sa, sb);
@@ -464,7 +481,8 @@ static cudaError_t launch_cluster_t(const DecodeArgs &a, const CUtensorMap &tm, 
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH>, tm, tt, a);
+    return a.norm_w ? cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, true>, tm, tt, a)
+                    : cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false>, tm, tt, a);
 }
 
 cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s) {
@@ -482,32 +500,39 @@ cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s) {
 cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters) {
     *active_clusters = 0;
     if (!tensor_map_encoder()) return cudaErrorNotSupported;  // down blocks are fetched by a tensor map
-    const void *f = nullptr;
+    const void *fs[2] = {nullptr, nullptr};  // plain and pre-normed block
     switch (nbh) {
-        case 1: f = (const void *)k_expert_cluster<1>; break;
-        case 2: f = (const void *)k_expert_cluster<2>; break;
-        case 4: f = (const void *)k_expert_cluster<4>; break;
-        default: f = (const void *)k_expert_cluster<8>; break;
+        case 1: fs[0] = (const void *)k_expert_cluster<1, false>, fs[1] = (const void *)k_expert_cluster<1, true>; break;
+        case 2: fs[0] = (const void *)k_expert_cluster<2, false>, fs[1] = (const void *)k_expert_cluster<2, true>; break;
+        case 4: fs[0] = (const void *)k_expert_cluster<4, false>, fs[1] = (const void *)k_expert_cluster<4, true>; break;
+        default: fs[0] = (const void *)k_expert_cluster<8, false>, fs[1] = (const void *)k_expert_cluster<8, true>; break;
     }
-    cudaFuncAttributes fa;
-    cudaError_t err = cudaFuncGetAttributes(&fa, f);
-    if (err != cudaSuccess) return err;
-    const int dyn_max = smem_max - (int)fa.sharedSizeBytes;
-    if (smem > dyn_max) return cudaErrorInvalidValue;
-    if ((err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max)) != cudaSuccess)
-        return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(C);
-    cfg.blockDim = dim3(kClThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(active_clusters, f, &cfg);
+    int least = 1 << 30;
+    for (const void *f : fs) {  // both variants must fit; the smaller resident count counts
+        cudaFuncAttributes fa;
+        cudaError_t err = cudaFuncGetAttributes(&fa, f);
+        if (err != cudaSuccess) return err;
+        const int dyn_max = smem_max - (int)fa.sharedSizeBytes;
+        if (smem > dyn_max) return cudaErrorInvalidValue;
+        if ((err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max)) != cudaSuccess)
+            return err;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(C);
+        cfg.blockDim = dim3(kClThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if ((err = cudaOccupancyMaxActiveClusters(&n, f, &cfg)) != cudaSuccess) return err;
+        least = n < least ? n : least;
+    }
+    *active_clusters = least;
+    return cudaSuccess;
 }
 
 }  // namespace si

@@ -55,6 +55,8 @@ DecodeLayout decode_layout(const si_moe_desc &d, int n_tokens);
 struct DecodeArgs {
     const uint8_t *wg, *wu, *wd;
     const float *router_w, *router_bias;
+    const float *norm_w;  // [H] RMSNorm gain of a pre-normed block (out = x + MoE(norm(x))), or null
+    float norm_eps;
     const uint16_t *x;  // [n][H] bf16 bits
     float *out;         // [n][H]
     int H, I, E, k, n;
@@ -86,7 +88,7 @@ struct DecodeArgs {
 // Each expert's rows start at a multiple of 32 (padded offsets poff), so the
 // 32-row tiles of the GEMM epilogues never reach another expert's rows.
 struct PrefillLayout {
-    size_t ctrl, wt, logits, ids, wts, counts, hist, offsets, poff, perm, pperm, inv, xp, h, y, total;
+    size_t ctrl, wt, logits, ids, wts, counts, hist, offsets, poff, perm, pperm, inv, xp, h, y, rms, rrow, total;
     int64_t rows;  // padded row capacity: T*k + 32*E
 };
 PrefillLayout prefill_layout(const si_moe_desc &d, int n_tokens);
@@ -94,6 +96,8 @@ PrefillLayout prefill_layout(const si_moe_desc &d, int n_tokens);
 struct PrefillArgs {
     const uint8_t *wg, *wu, *wd;
     const float *router_w, *router_bias;
+    const float *norm_w;  // [H] RMSNorm gain of a pre-normed block (out = x + MoE(norm(x))), or null
+    float norm_eps;
     const uint16_t *x;  // [T][H] bf16 bits
     float *out;         // [T][H]
     int H, I, E, k, T;
@@ -105,6 +109,8 @@ struct PrefillArgs {
     float *wts;        // [T*k] renormalised routing weights
     int32_t *counts;   // [E]
     int32_t *hist;     // [ceil(T/32)][E] pairs per expert of each 32-token chunk
+    float *rms;        // [T] 1 / rms of each token (pre-normed block only)
+    float *rrow;       // [rows] 1 / rms of the token of each padded row, 0 on padding (pre-normed block)
     int32_t *offsets;  // [E+1] exclusive scan of counts
     int32_t *poff;     // [E+1] exclusive scan of counts rounded up to 32
     int32_t *perm;     // [T*k] pair ids ordered by expert, then pair id

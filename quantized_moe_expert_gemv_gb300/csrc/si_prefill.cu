@@ -20,6 +20,16 @@
 //                        into y (fp32, perm order)
 //   6. k_prefill_combine out[t] = sum over slots, in slot order, of w[t][s] * y[inv[t*k+s]]
 //
+// A pre-normed block (layer norm_weight set: out = x + MoE(x * gamma / rms(x)))
+// adds k_prefill_rms (1 / rms of every token) before step 1 and folds gamma
+// into the router's W^T and 1 / rms into its logits.  The expert GEMM keeps x
+// exact in its fp16 operand: gamma multiplies the dequantized gate/up weights
+// (per hidden column, before the rounding to fp16) and 1 / rms multiplies g
+// and u per token in the epilogue.  (Rounding the normalised row itself to
+// fp16 shares one rounding error per column across all intermediate rows;
+// measured against the oracle that alone gave up to 3.8e-3 rel-L2.)  Step 6
+// adds x.
+//
 // The GEMMs run on the 5th-generation tensor cores as CTA pairs: 16-bit
 // operands in shared memory (K-major, 128-byte swizzle), fp32 accumulators in
 // tensor memory.  Weights (operand A) are Q4_K blocks fetched by tensor-map
@@ -65,7 +75,25 @@ __global__ void __launch_bounds__(256) k_prefill_wt(PrefillArgs a) {
     for (int r = ty; r < 32; r += 8)
         tile[r][tx] = (e0 + r < a.E) ? __ldg(a.router_w + (size_t)(e0 + r) * a.H + c0 + tx) : 0.f;
     __syncthreads();
-    for (int r = ty; r < 32; r += 8) a.wt[(size_t)(c0 + r) * Ew + e0 + tx] = tile[tx][r];
+    // a pre-normed block folds the norm gain into the rows: z = r_t * sum_c (W[e][c] * gamma_c) * x_tc
+    for (int r = ty; r < 32; r += 8)
+        a.wt[(size_t)(c0 + r) * Ew + e0 + tx] = a.norm_w ? tile[tx][r] * __ldg(a.norm_w + c0 + r) : tile[tx][r];
+}
+
+// Pre-normed block: rms[t] = 1 / sqrt(mean(x_t^2) + eps), one warp per token.
+__global__ void __launch_bounds__(512) k_prefill_rms(PrefillArgs a) {
+    const int t = blockIdx.x * 16 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (t >= a.T) return;
+    const uint32_t *xr = reinterpret_cast<const uint32_t *>(a.x + (size_t)t * a.H);
+    float ss = 0.f;
+    for (int c = lane; c < a.H / 2; c += 32) {
+        const uint32_t v = __ldg(xr + c);
+        const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+        ss = fmaf(lo, lo, ss);
+        ss = fmaf(hi, hi, ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) a.rms[t] = rms_scale(ss, a.H, a.norm_eps);
 }
 
 namespace {
@@ -179,6 +207,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                 float z = part[idx];
 #pragma unroll
                 for (int g = 1; g < kRtG; ++g) z += part[idx + g * kRtTok * kRtExp];
+                if (a.norm_w) z *= t0 + tk < a.T ? __ldg(a.rms + t0 + tk) : 0.f;
                 s_z[tk][e] = a.router_bias ? z + __ldg(a.router_bias + e) : z;
             }
         }
@@ -309,12 +338,15 @@ __global__ void __launch_bounds__(512) k_prefill_perm(PrefillArgs a) {
 
 // Padded expert-major token rows for the gate/up GEMM: xp[r] = fp16(x[token of
 // pperm[r]]), zero for padding rows; a value beyond fp16's range is reported.
+// A pre-normed block keeps x exact here and records each row's 1 / rms in
+// rrow[r] for the gate/up epilogue (0 on padding rows).
 __global__ void __launch_bounds__(256) k_prefill_xperm(PrefillArgs a) {
     const int nrows = a.poff[a.E];
     const int c8 = a.H / 8;  // 16-byte groups per row
     for (int r = blockIdx.x; r < nrows; r += gridDim.x) {  // one row per CTA iteration, 32-bit indices
         const int p = __ldg(a.pperm + r);
         const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)(p >= 0 ? p / a.k : 0) * a.H);
+        if (a.norm_w && threadIdx.x == 0) a.rrow[r] = p >= 0 ? __ldg(a.rms + p / a.k) : 0.f;  // pre-normed block
         uint4 *dst = reinterpret_cast<uint4 *>(a.xp + (size_t)r * a.H);
         for (int c = threadIdx.x; c < c8; c += blockDim.x) {
             uint4 o = make_uint4(0u, 0u, 0u, 0u);
@@ -338,7 +370,8 @@ __global__ void __launch_bounds__(256) k_prefill_xperm(PrefillArgs a) {
     }
 }
 
-// out[t][c] = sum over slots s = 0..k-1 (in order) of y[inv[t*k+s]][c].
+// out[t][c] = sum over slots s = 0..k-1 (in order) of y[inv[t*k+s]][c] (+ x[t][c]
+// in a pre-normed block).
 __global__ void __launch_bounds__(256) k_prefill_combine(PrefillArgs a) {
     const int c4 = a.H / 4;
     const size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -353,6 +386,13 @@ __global__ void __launch_bounds__(256) k_prefill_combine(PrefillArgs a) {
         acc.y += w * v.y;
         acc.z += w * v.z;
         acc.w += w * v.w;
+    }
+    if (a.norm_w) {  // the residual of a pre-normed block
+        const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(a.x + (size_t)t * a.H) + c);
+        acc.x += __uint_as_float(xv.x << 16);
+        acc.y += __uint_as_float(xv.x & 0xffff0000u);
+        acc.z += __uint_as_float(xv.y << 16);
+        acc.w += __uint_as_float(xv.y & 0xffff0000u);
     }
     reinterpret_cast<float4 *>(a.out + (size_t)t * a.H)[c] = acc;
 }
@@ -404,6 +444,11 @@ __device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
 __device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
     f32x2 r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
@@ -491,7 +536,7 @@ __device__ __forceinline__ Pass make_pass(int e, int tile, int prow, int sc, int
 // traffic); empty (both CTAs, both MMA threads) and d_full are completed by
 // the multicast MMA commits; d_empty (even CTA) by both CTAs' epilogue
 // warps; raw_* are local.
-template <int MODE>
+template <int MODE, bool NORM>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     k_prefill_gemm(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                    const __grid_constant__ CUtensorMap tm_b64, const __grid_constant__ CUtensorMap tm_b16,
@@ -669,6 +714,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------ dequant (warps 4-11) of this CTA's 128 rows
         const int d = threadIdx.x - 128;  // 0..255
+        const float *const gam = (MODE == 0 && NORM) ? a.norm_w : nullptr;  // pre-normed block: RMSNorm gain
         const int row = d >> 1, half = d & 1;
         // MODE 0: A row 2i = gate row i, 2i+1 = up row i (raw rows: gate 0-63, up 64-127)
         const int raw_row = MODE == 0 ? ((row & 1) ? 64 + (row >> 1) : (row >> 1)) : row;
@@ -711,15 +757,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
                 const f32x2 C = pack2(dsc * tp0, dsc * tp8), O = pack2(dsc * to0, dsc * to8), D = pack2(-dm, -dm);
                 const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                 uint32_t o[16];
+                if (MODE == 0 && gam) {
+                    // pre-normed block: the gate/up weights of hidden column c times gamma_c (the
+                    // token's 1 / rms is applied to g and u in the epilogue), so x stays exact
+                    const float4 *gp = reinterpret_cast<const float4 *>(gam + 64 * ((kb + ps.rot) % nK) + 32 * half);
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const uint32_t w = wv[t], hi = w >> 16;
-                    const f32x2 v01 = pack2(__uint_as_float((w & m0) | 0x4B000000u), __uint_as_float((w & m8) | 0x4B000000u));
-                    const f32x2 v23 = pack2(__uint_as_float((hi & m0) | 0x4B000000u), __uint_as_float((hi & m8) | 0x4B000000u));
-                    const float2 r01 = unpack2(add2(fma2(v01, C, O), D));
-                    const float2 r23 = unpack2(add2(fma2(v23, C, O), D));
-                    o[2 * t] = f16x2_rn(r01.x, r01.y);
-                    o[2 * t + 1] = f16x2_rn(r23.x, r23.y);
+                    for (int t = 0; t < 8; ++t) {
+                        const float4 g4 = __ldg(gp + t);
+                        const uint32_t w = wv[t], hi = w >> 16;
+                        const f32x2 v01 = pack2(__uint_as_float((w & m0) | 0x4B000000u), __uint_as_float((w & m8) | 0x4B000000u));
+                        const f32x2 v23 = pack2(__uint_as_float((hi & m0) | 0x4B000000u), __uint_as_float((hi & m8) | 0x4B000000u));
+                        const float2 r01 = unpack2(mul2(add2(fma2(v01, C, O), D), pack2(g4.x, g4.y)));
+                        const float2 r23 = unpack2(mul2(add2(fma2(v23, C, O), D), pack2(g4.z, g4.w)));
+                        o[2 * t] = f16x2_rn(r01.x, r01.y);
+                        o[2 * t + 1] = f16x2_rn(r23.x, r23.y);
+                    }
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const uint32_t w = wv[t], hi = w >> 16;
+                        const f32x2 v01 = pack2(__uint_as_float((w & m0) | 0x4B000000u), __uint_as_float((w & m8) | 0x4B000000u));
+                        const f32x2 v23 = pack2(__uint_as_float((hi & m0) | 0x4B000000u), __uint_as_float((hi & m8) | 0x4B000000u));
+                        const float2 r01 = unpack2(add2(fma2(v01, C, O), D));
+                        const float2 r23 = unpack2(add2(fma2(v23, C, O), D));
+                        o[2 * t] = f16x2_rn(r01.x, r01.y);
+                        o[2 * t + 1] = f16x2_rn(r23.x, r23.y);
+                    }
                 }
                 uint8_t *at = sm + s * kATile + row * 128;
 #pragma unroll
@@ -756,6 +819,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
         // stored straight from registers -- for one token the 32 lanes of a warp
         // hold 32 consecutive output columns, 128 contiguous bytes.
         const int ew = warp - 12;  // tensor-memory lanes 32*ew ..
+        const float *const rrow = (MODE == 0 && NORM) ? a.rrow : nullptr;  // pre-normed block: 1 / rms per row
         const bool lead = threadIdx.x == 12 * 32;
         const uint32_t lead_d_empty = mapa_shared(d_empty, 0);
         int chunk = 0, nst = 0;  // chunk: global index
@@ -821,8 +885,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
                         for (int q = 0; q < 16; ++q) {
                             const float send = __uint_as_float(up ? v[q] : v[q + 16]);
                             const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-                            const float gg = up ? recv : __uint_as_float(v[q]);
-                            const float uu = up ? __uint_as_float(v[q + 16]) : recv;
+                            // pre-normed block: g and u of this token times its 1 / rms
+                            const float rq = rrow ? __ldg(rrow + row0 + q + 16 * up) : 1.f;
+                            const float gg = (up ? recv : __uint_as_float(v[q])) * rq;
+                            const float uu = (up ? __uint_as_float(v[q + 16]) : recv) * rq;
                             hv[q] = __fdividef(gg, 1.0f + __expf(-gg)) * uu;
                             // columns past the chunk's tokens hold stale accumulators: not checked
                             big |= (col0 + q + 16 * up < nv) & (fabsf(hv[q]) > 65504.f);
@@ -908,9 +974,11 @@ cudaError_t prefill_prepare(const Plan &p) {
     if (!encoder()) return cudaErrorNotSupported;
     cudaError_t err = cudaFuncSetAttribute(k_prefill_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(k_prefill_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    err = cudaFuncSetAttribute(k_prefill_gemm<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
     if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(k_prefill_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    err = cudaFuncSetAttribute(k_prefill_gemm<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    if (err != cudaSuccess) return err;
+    return cudaFuncSetAttribute(k_prefill_gemm<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
 }
 
 // Records events[i] on s (as an external event node while s is being captured).
@@ -929,6 +997,7 @@ cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, 
     if ((err = cudaMemsetAsync(a.counts, 0, sizeof(int32_t) * a.E, s)) != cudaSuccess) return err;
     const int Ew = (a.E + 127) & ~127;
     k_prefill_wt<<<dim3(a.H / 32, Ew / 32), 256, 0, s>>>(a);
+    if (a.norm_w) k_prefill_rms<<<(a.T + 15) / 16, 512, 0, s>>>(a);
     {
         CUtensorMap twt;
         CUtensorMap tx;  // x [T][H] bf16 bits (16-bit elements; the copy does not convert)
@@ -954,10 +1023,13 @@ cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, 
         return cudaErrorInvalidValue;
     // one CTA pair (2-CTA cluster, declared on the kernel) per two SMs
     const int grid = 2 * (p.sm_count / 2);
-    k_prefill_gemm<0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
+    if (a.norm_w)  // pre-normed block: gamma folded into the weights, 1 / rms into the epilogue
+        k_prefill_gemm<0, true><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
+    else
+        k_prefill_gemm<0, false><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 2, s)) != cudaSuccess) return err;
-    k_prefill_gemm<1><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
+    k_prefill_gemm<1, false><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 3, s)) != cudaSuccess) return err;
     const size_t n4 = (size_t)a.T * (a.H / 4);

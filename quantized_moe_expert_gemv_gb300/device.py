@@ -23,10 +23,12 @@ class DeviceLayer:
     w_down: torch.Tensor      # uint8 [E, H, I/256, 144]
     router_w: torch.Tensor    # float32 [E, H]
     router_bias: Optional[torch.Tensor] = None
+    norm_weight: Optional[torch.Tensor] = None   # float32 [H]: pre-normed block with residual
+    norm_eps: float = 0.0
 
     def struct(self) -> binding.si_moe_layer:
         return binding.layer_struct(self.w_gate, self.w_up, self.w_down, self.router_w,
-                                    self.router_bias)
+                                    self.router_bias, self.norm_weight, self.norm_eps)
 
     @property
     def nbytes(self) -> int:
@@ -38,8 +40,9 @@ def to_device(layer: MoeLayer, device="cuda") -> DeviceLayer:
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(device)
     bias = None if layer.router_bias is None else up(layer.router_bias)
+    norm = None if layer.norm_weight is None else up(layer.norm_weight)
     return DeviceLayer(layer.shape, up(layer.w_gate), up(layer.w_up), up(layer.w_down),
-                       up(layer.router_w), bias)
+                       up(layer.router_w), bias, norm, float(layer.norm_eps) if norm is not None else 0.0)
 
 
 def tokens_to_device(x_bits: np.ndarray, device="cuda") -> torch.Tensor:

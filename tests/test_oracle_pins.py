@@ -391,6 +391,26 @@ def test_prenorm_block_on_unit_rms_input_is_x_plus_the_plain_block(oracle_lib):
                                    atol=1e-12 * np.abs(plain.out64).max())
 
 
+def test_prenorm_routing_agrees_with_the_block(oracle_lib):
+    shape = synth.MoeShape(256, 256, 12, 3)
+    layer = synth.make_layer(shape, seed=35, router_bias=np.linspace(0.0, 0.2, 12))
+    gam = synth.make_norm_weight(shape, seed=35)
+    xs = synth.make_tokens(shape, seed=35, n_tokens=5)
+    ids, w, z, margin = oracle.route_tokens_prenorm(layer.router_w, xs, 3, gam, 1e-6, bias=layer.router_bias)
+    for t in range(5):
+        res = oracle.moe_token_prenorm(layer, xs[t], gam, 1e-6)
+        assert np.array_equal(ids[t], res.ids)
+        assert np.array_equal(w[t], res.w) and np.array_equal(z[t], res.z)
+        assert margin[t] == res.margin
+    # x of +-1 with unit gain and no eps: the plain routing of x
+    x = synth.bf16_bits(np.random.default_rng(35).choice([-1.0, 1.0], size=(4, 256)).astype(np.float32))
+    a = oracle.route_tokens_prenorm(layer.router_w, x, 3, np.ones(256, np.float32), 0.0, bias=layer.router_bias)
+    b = oracle.route_tokens(layer.router_w, x, 3, bias=layer.router_bias, want_logits=True)
+    assert np.array_equal(a[0], b[0])
+    np.testing.assert_allclose(a[2], b[2], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(a[3], b[3], rtol=1e-9, atol=1e-13)
+
+
 def test_prenorm_block_is_scale_invariant_up_to_the_residual(oracle_lib):
     """eps = 0: block(2x) - 2x = block(x) - x (the norm removes the scale, the
     residual keeps it)."""
