@@ -121,12 +121,17 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
         const uint4 *xg = reinterpret_cast<const uint4 *>(xg_p);
         for (int q = threadIdx.x; q < n * 32 * NJ; q += blockDim.x) s_x[q] = __ldg(xg + q);
     }
-    if (zero_out) {         // the cluster expert kernel accumulates the top-k combine into out
+    if (zero_out && !(NORM && NJ > 0)) {  // the cluster expert kernel accumulates the top-k combine into out
         const int nthr = gridDim.x * blockDim.x;
         for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n * H; q += nthr)
-            out_p[q] = gam_p ? bf16_bits_to_f32(__ldg(xg_p + q)) : 0.f;  // the residual, or nothing
+            out_p[q] = NORM ? bf16_bits_to_f32(__ldg(xg_p + q)) : 0.f;  // the residual, or nothing
     }
     if (NJ > 0) __syncthreads();
+    if (zero_out && NORM && NJ > 0) {  // the residual, from the copy of x in shared memory
+        const uint16_t *xs16 = reinterpret_cast<const uint16_t *>(s_x);
+        const int nthr = gridDim.x * blockDim.x;
+        for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n * H; q += nthr) out_p[q] = bf16_bits_to_f32(xs16[q]);
+    }
     if (e < E) {
         float acc[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
         float ss[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};  // sum of squares of x (pre-normed block)

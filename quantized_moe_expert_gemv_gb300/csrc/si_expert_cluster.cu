@@ -153,34 +153,47 @@ __global__ void __launch_bounds__(kClThreads, 1)
     // own wait on the producers of x, so x is final here.  Each chunk is a row of
     // 32 words; its 16-byte unit q is stored at unit q ^ (row & 7), so that the
     // lanes that load different rows into registers hit different banks.
-    if (warp == 0 && lane < H / 64) {
+    // A pre-normed block stages the norm gain in the (still idle) gate/up stages
+    // while warp 0's loads of x are in flight; warp 0 then quantises
+    // x * gamma / rms(x) (lanes 0..H/64-1 hold all of x).
+    const bool xq_lane = warp == 0 && lane < H / 64;
+    uint4 xr[8];
+    if (xq_lane) {
+        const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + 64 * lane);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xr[q] = __ldg(xp + q);
+    }
+    float4 *const gam_s = reinterpret_cast<float4 *>(stA);  // [H/4]
+    if (NORM) {
+        for (int i = threadIdx.x; i < H / 4; i += blockDim.x)
+            gam_s[i] = __ldg(reinterpret_cast<const float4 *>(a.norm_w) + i);
+        __syncthreads();
+    }
+    if (xq_lane) {
         uint32_t *xq = xq_s;                                   // [H/64][32] words, 16-byte units swizzled
         float *xqf = reinterpret_cast<float *>(xq + H / 2);   // [H/64][3]: scale, Xa, Xb
         float xf[64];
         uint32_t wq[32];
         float sa, sb;
-        const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + 64 * lane);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const uint4 v = __ldg(xp + q);
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            const uint32_t wv[4] = {xr[q].x, xr[q].y, xr[q].z, xr[q].w};
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
                 xf[8 * q + 2 * e2] = __uint_as_float(wv[e2] << 16);
                 xf[8 * q + 2 * e2 + 1] = __uint_as_float(wv[e2] & 0xffff0000u);
             }
         }
-        if (NORM) {  // pre-normed block: quantise x * gamma / rms(x) (lanes 0..H/64-1 hold all of x)
+        if (NORM) {
             float ss = 0.f;
 #pragma unroll
             for (int q = 0; q < 64; ++q) ss = fmaf(xf[q], xf[q], ss);
             const unsigned mask = H / 64 == 32 ? 0xffffffffu : (1u << (H / 64)) - 1u;
             for (int o = 1; o < H / 64; o <<= 1) ss += __shfl_xor_sync(mask, ss, o);
             const float r = rms_scale(ss, H, a.norm_eps);
-            const float4 *gp = reinterpret_cast<const float4 *>(a.norm_w + 64 * lane);
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-                const float4 g = __ldg(gp + q);
+                const float4 g = gam_s[16 * lane + q];
                 xf[4 * q] *= r * g.x;
                 xf[4 * q + 1] *= r * g.y;
                 xf[4 * q + 2] *= r * g.z;
@@ -196,6 +209,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
         xqf[3 * lane + 1] = sa;
         xqf[3 * lane + 2] = sb;
     }
+    // the gate/up stages are written by the copy engine later: order the staging's
+    // shared-memory accesses before those asynchronous writes
+    if (NORM) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     pdl_wait();  // routing of this token is complete
     // The router left the k selected experts in rank order with their logits;
