@@ -151,6 +151,7 @@ class Dist:
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.device = "cuda" if n_gpus > 0 else "cpu"  # where the reduction tensors live (nccl / gloo)
         if self.world > 1:
             import torch.distributed as dist
             dist.init_process_group("nccl" if n_gpus > 0 else "gloo")
@@ -164,7 +165,7 @@ class Dist:
         if not self.pg:
             return v
         import torch
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
@@ -172,7 +173,7 @@ class Dist:
         if not self.pg:
             return v
         import torch
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
         self.pg.all_reduce(t)
         return float(t.item())
 
