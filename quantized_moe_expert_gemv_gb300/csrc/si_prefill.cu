@@ -594,10 +594,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     tc::fence_after_sync();
     const uint32_t taddr = s_taddr;
 
+    // Work units (expert, row tile) go to the pairs round by round in a snake
+    // order over the experts sorted by descending pair count (ties: lower id):
+    // the last, partial round gets the cheapest units and every pair a mix of
+    // large and small ones.  Both CTAs of a pair derive the same order.
+    __shared__ int s_cnt[SI_MAX_EXPERTS], s_order[SI_MAX_EXPERTS];
+    for (int t = threadIdx.x; t < a.E; t += blockDim.x) s_cnt[t] = __ldg(a.counts + t);
+    __syncthreads();
+    for (int t = threadIdx.x; t < a.E; t += blockDim.x) {
+        const int ct = s_cnt[t];
+        int rk = 0;
+        for (int j = 0; j < a.E; ++j) rk += (s_cnt[j] > ct) | ((s_cnt[j] == ct) & (j < t));
+        s_order[rk] = t;
+    }
+    __syncthreads();
+
     // every role walks the same passes
     auto for_each_pass = [&](auto &&body) {
-        for (int u = pair; u < nU && !*verr; u += npairs) {
-            const int e = u / tiles, tile = u - e * tiles;
+        for (int rr = 0; rr * npairs < nU && !*verr; ++rr) {
+            const int u = rr * npairs + ((rr & 1) ? npairs - 1 - pair : pair);
+            if (u >= nU) continue;
+            const int e = s_order[u / tiles], tile = u - (u / tiles) * tiles;
             const int ne = __ldg(a.counts + e), prow = __ldg(a.poff + e);
             for (int sc = 0; sc < ne && !*verr; sc += kMaxTok) body(make_pass(e, tile, prow, sc, ne, nK));
         }
