@@ -17,7 +17,8 @@
 //     [H*c/C, H*(c+1)/C) of expert e to that h slice and adds w_s * y into the
 //     output with float reductions (the top-k combine: every output row sums
 //     one partial per (slot, block column)).
-// The router kernel zeroes the output first.  Weight bytes: gate/up rows by
+// The router kernel first sets the output to zero (to x in a pre-normed
+// block, whose residual it is).  Weight bytes: gate/up rows by
 // 1-D bulk copies; down blocks, 144-byte pieces with a 432-byte row stride,
 // by 2-D tensor maps (boxes of 144 bytes x 128 rows, one mbarrier per box, so
 // the down phase starts on the first box while the later ones land; the last
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     constexpr int rowg = NBH * kBlockBytes;
     constexpr int stageA = 2 * CH * rowg;
     __shared__ int s_err;
-    __shared__ int s_expert, s_slot;
+    __shared__ int s_expert;
     __shared__ float s_w;
     __shared__ int s_lastA[8];
     __shared__ int s_lastB;
@@ -227,7 +228,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
         for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
         const float w = ex / den;
         if (lane == slot) {
-            s_slot = slot;
             s_expert = id;
             s_w = w;
         }

@@ -79,7 +79,7 @@ struct DecodeArgs {
     // shared-memory plan of the cluster expert kernel (set by expert_cluster_layout)
     int cl_off_a, cl_off_b, cl_off_h, cl_off_x, cl_off_y, cl_off_bar;
     int cl_nsa, cl_C, cl_tail_rows, cl_nbox, cl_box_stride, cl_smem;
-    int zero_out;  // router zeroes out[n][H] (the expert kernel accumulates into it)
+    int zero_out;  // router sets out[n][H] to 0, or to x in a pre-normed block (the expert kernel accumulates into it)
     int sel_logits;  // single token, cluster expert kernel: the router writes ids in rank order, the
                      // selected logits (not weights) and 0/1 counts; the expert kernel forms the weights
 };
