@@ -519,9 +519,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
             for (int jt = 0; jt < nt; ++jt) {
                 const int pair = u->tok[s][jt] * a.k + u->slot[s][jt];
                 const float wgt = rt.wts[pair];
-                // quantise h of this (token, slot): lane = sub-block, partner lane^1 shares the chunk
+                // quantise h of this (token, slot): lane = sub-block, partner lane^1 shares the chunk.
+                // A lane reads the eight 16-byte units of its 128-byte sub-block starting at unit
+                // sb & 7 (hv[4q..4q+3] = unit (q + sb) & 7), so the lanes of a quarter warp hit
+                // different banks; the packed words go back to their own positions.
                 for (int sb0 = 0; sb0 < nsub; sb0 += 32) {
-                    const int sb = sb0 + lane;
+                    const int sb = sb0 + lane, rot = sb & 7;
                     float hv[32];
                     float mx = 0.f, sum = 0.f;
                     if (sb < nsub) {
@@ -529,22 +532,34 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
                             const float4 *hp = reinterpret_cast<const float4 *>(stA) + ((size_t)pair * a.I + 32 * sb) / 4;
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
-                                const float4 v = hp[q];
+                                const float4 v = hp[(q + rot) & 7];
                                 hv[4 * q] = v.x, hv[4 * q + 1] = v.y, hv[4 * q + 2] = v.z, hv[4 * q + 3] = v.w;
                             }
                         } else {
                             const float4 *hp = reinterpret_cast<const float4 *>(a.h + (size_t)pair * a.I + 32 * sb);
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
-                                const float4 v = __ldcg(hp + q);
+                                const float4 v = __ldcg(hp + ((q + rot) & 7));
                                 hv[4 * q] = v.x, hv[4 * q + 1] = v.y, hv[4 * q + 2] = v.z, hv[4 * q + 3] = v.w;
                             }
                         }
+                        float m8[8], s8[8];  // balanced trees: short dependency chains
 #pragma unroll
-                        for (int l = 0; l < 32; ++l) {
-                            mx = fmaxf(mx, fabsf(hv[l]));
-                            sum += hv[l];
+                        for (int q = 0; q < 8; ++q) {
+                            m8[q] = fmaxf(fmaxf(fabsf(hv[4 * q]), fabsf(hv[4 * q + 1])),
+                                          fmaxf(fabsf(hv[4 * q + 2]), fabsf(hv[4 * q + 3])));
+                            s8[q] = (hv[4 * q] + hv[4 * q + 1]) + (hv[4 * q + 2] + hv[4 * q + 3]);
                         }
+#pragma unroll
+                        for (int w2 = 4; w2 >= 1; w2 >>= 1) {
+#pragma unroll
+                            for (int q = 0; q < w2; ++q) {
+                                m8[q] = fmaxf(m8[q], m8[q + w2]);
+                                s8[q] += s8[q + w2];
+                            }
+                        }
+                        mx = m8[0];
+                        sum = s8[0];
                     }
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                     if (sb < nsub) {
@@ -553,7 +568,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(DecodeArgs a) {
                         for (int pp = 0; pp < 16; ++pp) {
                             const int lo = __float2int_rn(hv[2 * pp] * inv);
                             const int hi = __float2int_rn(hv[2 * pp + 1] * inv);
-                            hq[kHqStride * sb + pp] = (uint32_t)(lo & 0xffff) | ((uint32_t)hi << 16);
+                            hq[kHqStride * sb + 2 * (((pp >> 1) + rot) & 7) + (pp & 1)] =
+                                (uint32_t)(lo & 0xffff) | ((uint32_t)hi << 16);
                         }
                         hsum[sb] = sum;
                         if ((sb & 1) == 0) hsc[sb >> 1] = mx * (1.0f / 32767.0f);
