@@ -47,12 +47,12 @@ FALLBACK_HBM_GBS = 6800.0
 # kernel's sources are the ones that were profiled (sha256 over the files).
 PROFILED_TRAFFIC = {
     "k_expert_cluster": {
-        "bytes": 21294592,
+        "bytes": 21295616,
         "profile": "profiles/k_expert_cluster_qwen3_bs1.md",
         "sources": ["quantized_moe_expert_gemv_gb300/csrc/si_expert_cluster.cu",
                     "quantized_moe_expert_gemv_gb300/csrc/si_device.cuh",
                     "quantized_moe_expert_gemv_gb300/csrc/si_internal.h"],
-        "sha256": "df04f107dbf4b0e55de583c7c03e1e003a8829af7334cccca56ca6624e78c10d",
+        "sha256": "c440d01597359c740364c6825828c3a2e9971d89e2300c6148d7ba278bf0fe4e",
     },
 }
 
