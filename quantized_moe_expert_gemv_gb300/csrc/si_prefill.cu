@@ -341,20 +341,30 @@ __global__ void __launch_bounds__(512) k_prefill_perm(PrefillArgs a) {
 // A pre-normed block keeps x exact here and records each row's 1 / rms in
 // rrow[r] for the gate/up epilogue (0 on padding rows).
 __global__ void __launch_bounds__(256) k_prefill_xperm(PrefillArgs a) {
+    constexpr int kRows = 4;  // rows per CTA iteration, their loads in flight together
     const int nrows = a.poff[a.E];
     const int c8 = a.H / 8;  // 16-byte groups per row
-    for (int r = blockIdx.x; r < nrows; r += gridDim.x) {  // one row per CTA iteration, 32-bit indices
-        const int p = __ldg(a.pperm + r);
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)(p >= 0 ? p / a.k : 0) * a.H);
-        if (a.norm_w && threadIdx.x == 0) a.rrow[r] = p >= 0 ? __ldg(a.rms + p / a.k) : 0.f;  // pre-normed block
-        uint4 *dst = reinterpret_cast<uint4 *>(a.xp + (size_t)r * a.H);
+    const int G = gridDim.x;
+    for (int r0 = blockIdx.x; r0 < nrows; r0 += kRows * G) {  // rows r0 + u*G, 32-bit indices
+        int p[kRows];
+#pragma unroll
+        for (int u = 0; u < kRows; ++u) p[u] = r0 + u * G < nrows ? __ldg(a.pperm + r0 + u * G) : -1;
+        if (a.norm_w && threadIdx.x == 0)  // pre-normed block
+#pragma unroll
+            for (int u = 0; u < kRows; ++u)
+                if (r0 + u * G < nrows) a.rrow[r0 + u * G] = p[u] >= 0 ? __ldg(a.rms + p[u] / a.k) : 0.f;
         for (int c = threadIdx.x; c < c8; c += blockDim.x) {
-            uint4 o = make_uint4(0u, 0u, 0u, 0u);
-            if (p >= 0) {
-                const uint4 v = __ldg(src + c);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint4 v[kRows];
+#pragma unroll
+            for (int u = 0; u < kRows; ++u)
+                v[u] = p[u] >= 0 ? __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)(p[u] / a.k) * a.H) + c)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            bool big = false;
+#pragma unroll
+            for (int u = 0; u < kRows; ++u) {
+                if (r0 + u * G >= nrows) break;
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
                 uint32_t h[4];
-                bool big = false;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
@@ -362,10 +372,9 @@ __global__ void __launch_bounds__(256) k_prefill_xperm(PrefillArgs a) {
                     const __half2 hh = __floats2half2_rn(lo, hi);
                     h[i] = *reinterpret_cast<const uint32_t *>(&hh);
                 }
-                if (big) set_status(a.ctrl + kCtrlStatus, SI_ERR_RANGE);
-                o = make_uint4(h[0], h[1], h[2], h[3]);
+                __stcg(reinterpret_cast<uint4 *>(a.xp + (size_t)(r0 + u * G) * a.H) + c, make_uint4(h[0], h[1], h[2], h[3]));
             }
-            __stcg(dst + c, o);
+            if (big) set_status(a.ctrl + kCtrlStatus, SI_ERR_RANGE);
         }
     }
 }
