@@ -6,7 +6,9 @@
  * What the library computes, per token x (H values):
  *   z = W_r x (+ bias); ids = k largest z (descending, equal z -> lower
  *   index); w_i = softmax(z)[ids_i] / sum_j softmax(z)[ids_j];
- *   h_i = silu(W_gate[ids_i] x) * (W_up[ids_i] x);  out = sum_i w_i W_down[ids_i] h_i.
+ *   h_i = silu(W_gate[ids_i] x) * (W_up[ids_i] x);  out = sum_i w_i W_down[ids_i] h_i;
+ * or, for a pre-normed block (si_moe_layer.norm_weight), the same on
+ * x * gamma / sqrt(mean(x^2) + eps) with x added to out.
  * Sources: sparkinfer README (luciferlive112116), opening section (experts
  * "quantized-resident, dequantized on-read", greedy bs=1 decode of a Q4_K_M
  * GGUF Qwen3-30B-A3B) and "Layout" table (kernels: "decode GEMV", "fused
@@ -158,7 +160,9 @@ si_status si_moe_forward_decode(si_moe_plan_t plan, const si_moe_layer *layer, c
  * order (deterministic).  The tensor-core operands are fp16 (weights and h
  * rounded to nearest even, x converted exactly): bf16 weights cannot hold
  * the output tolerance.  An input, weight or h value beyond the fp16 range
- * is reported as SI_ERR_RANGE by si_moe_read_status.  x_bf16: [T][H] bf16; out: [T][H] fp32 (written).
+ * is reported as SI_ERR_RANGE by si_moe_read_status (in a pre-normed block
+ * the weight check is made before the norm gain is multiplied in, so a gain
+ * that pushes a weight past 65504 is not reported).  x_bf16: [T][H] bf16; out: [T][H] fp32 (written).
  * route_out may return ids/weights [T][k], counts [E], offsets [E+1],
  * perm [T*k] and logits [T][E].  Needs H, I multiples of 256 (as every call)
  * and scratch of si_moe_scratch_bytes(plan, SI_MODE_PREFILL, T).  Returns
