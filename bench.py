@@ -16,7 +16,9 @@ kernel's HBM roofline (its CUDA-event time on its own stream), the whole
 chain's achieved bandwidth, nvidia-smi clocks sampled during the timed
 region, an end-to-end figure with host<->device copies in the timed
 region, the CPU oracle's throughput on a bounded sample, and (unless
---no-extras) the 48-layer stack and the 4-token deduplicated workloads.
+--no-extras) the 48-layer stack, the 4-token deduplicated workload, the
+headline workload as a pre-normed block, and the 4096-token grouped prefill
+with its tensor-core roofline.
 
 --impl reference times the CPU oracle (the reference implementation of the
 method) on a bounded sample of the same workload on the host cores.
@@ -79,7 +81,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--no-extras", action="store_true", help="skip the stack/dedup workloads")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the stack, dedup, pre-normed and prefill workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--tokens", type=int, default=0,
                    help="tokens per step of the headline layer (default 1024; small values for ncu)")
