@@ -147,7 +147,7 @@ si_status si_moe_forward_decode(si_moe_plan_t plan, const si_moe_layer *layer, c
                                 int32_t n_tokens, float *out, si_moe_route_out *route_out,
                                 void *scratch, size_t scratch_bytes, si_stream_t stream);
 
-/* Grouped prefill (SP⚡RKINFER README, "Benchmark · Qwen3.6-35B-A3B", prefill
+/* Grouped prefill (SP⚡RKINFER README, "Benchmark · Qwen3.8-27B", prefill
  * paragraph: Q4_K dequantized into the GEMM operand; sparkinfer-k3 blog post,
  * "v0.2.2": a chunk of tokens shares one weight-tile read): T tokens
  * (1..max_tokens) routed top-k (fp32 logits, ties to the lower index,
@@ -183,24 +183,33 @@ const char *si_status_string(si_status status);
  * pool owns all device memory and gives it no allocator, or a latency-
  * critical decode loop where cudaMalloc would synchronise the device.  (The
  * sparkinfer pages have no counterpart of this entry point.)
- * Same arguments, results and errors as si_moe_forward_decode, minus the
- * scratch pointer and size.  The scratch is one fixed device array of
+ * Same arguments and results as si_moe_forward_decode, minus the scratch
+ * pointer and size, and the same argument errors, all returned before
+ * anything is launched or written.  The scratch is one fixed device array of
  * SI_STATIC_SCRATCH_BYTES per GPU, part of the library's module image: every
  * GPU that loads the library holds it until the process exits.  A call whose
  * shape needs more scratch (si_moe_scratch_bytes) is rejected with
- * SI_ERR_SCRATCH_TOO_SMALL before any launch.  The call allocates nothing
- * (no cudaMalloc, cudaFree or allocating library routine).  The first call on
- * a device looks up the array's device address with that device current; make
- * that first call before any stream capture.  Every call on a device shares
- * the one array, which keeps the previous call's contents; each call clears
- * the words that must start at zero (stream-ordered).  Calls that may overlap
- * on the GPU (different streams, or unordered host threads) race on the array:
- * order them.  Device-side status of these calls is not readable through
- * si_moe_read_status. */
+ * SI_ERR_SCRATCH_TOO_SMALL.  The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).  The first call on a device looks
+ * up the array's device address with that device current; make that first
+ * call before any stream capture.  After cudaDeviceReset the looked-up
+ * address is stale and these entry points must not be used on that device.
+ * Every call on a device shares the one array, which keeps the previous
+ * call's contents; each call clears the words that must start at zero
+ * (stream-ordered).  Calls that may overlap on the GPU (different streams, or
+ * unordered host threads) race on the array: order them.  Device-side errors
+ * (a bounded wait that ran out) are kept in the array's status word until
+ * si_moe_read_status_noalloc reads them. */
 #define SI_STATIC_SCRATCH_BYTES (1u << 20)
 si_status si_moe_forward_decode_noalloc(si_moe_plan_t plan, const si_moe_layer *layer,
                                         const void *x_bf16, int32_t n_tokens, float *out,
                                         si_moe_route_out *route_out, si_stream_t stream);
+
+/* Synchronise `stream` and return the device-side status that calls of
+ * si_moe_forward_decode_noalloc on the current device recorded since the last
+ * read (SI_OK if none), then clear it.  Like si_moe_read_status, but for the
+ * fixed array of those calls; allocates nothing. */
+si_status si_moe_read_status_noalloc(si_stream_t stream);
 
 /* Test/bench export: which expert kernels decode of n_tokens tokens runs
  * after the router launch: 2 = the cluster kernel (one launch, n_tokens == 1),
@@ -224,6 +233,18 @@ si_status si_debug_q4k_dequant(const void *blocks, int64_t n_blocks, float *out_
                                uint16_t *out_bf16, si_stream_t stream);
 si_status si_debug_topk(const float *logits, int32_t n, const si_moe_desc *desc,
                         si_moe_route_out *route_out, si_stream_t stream);
+
+/* Test export: the grouped prefill's own Q4_K -> fp16 operand conversion (the
+ * device function its GEMM dequantization warps run; SP-RKINFER README,
+ * "Benchmark - Qwen3.8-27B", prefill paragraph: Q4_K is dequantized into the
+ * GEMM operand on every prefill pass) applied to n_blocks blocks.
+ * out_f16[256*b + c] (fp16 bits) = round-to-nearest-even fp16 of the fp32
+ * weight w = d*sc*q - dmin*m of column c of block b, or, when gamma
+ * ([n_blocks*256] fp32, 16-byte aligned) is non-NULL, of the fp32 product
+ * fp32(w) * gamma[256*b + c] (the gate/up operand of a pre-normed block).
+ * blocks, out_f16 16-byte aligned.  Stream-ordered. */
+si_status si_debug_q4k_dequant_f16(const void *blocks, int64_t n_blocks, const float *gamma, uint16_t *out_f16,
+                                   si_stream_t stream);
 
 /* Timing export: si_moe_forward_decode that also records caller-created
  * cudaEvent_t handles on `stream` -- events[0] before the router kernel,

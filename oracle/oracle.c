@@ -27,8 +27,9 @@
  * and, optionally, the block around it: x replaced by rmsnorm(x) = x * gamma /
  * sqrt(mean(x^2) + eps) on the way in and out = x + sum_i w_i y_i on the way
  * out (a pre-normed block with its residual);
- * with every expert matrix stored as GGUF Q4_K super-blocks and read as
- * the fp32 weights the Q4_K decode defines.
+ * with every expert matrix stored as GGUF Q4_K super-blocks (or NVFP4
+ * super-blocks, defined below) and read as the fp32 weights the format's
+ * decode defines.
  *
  * Precision: all products and sums are fp64 over the exact fp32 weights and
  * the exact fp32 value of each bf16 activation; results are rounded to
@@ -128,6 +129,54 @@ static void or_q4k_row(const uint8_t *row_blocks, int cols, float *out) {
     or_q4k_dequant(row_blocks, cols / OR_QK, out);
 }
 
+/* ------------------------------------------------------------------ NVFP4
+ * NVFP4 experts (the sparkinfer README's "Milestone 2" names NVFP4 experts as
+ * the next bytes-per-token step; the SP-RKINFER README, "Native NVFP4 - two
+ * supported checkpoints", runs NVFP4 weights directly; the CuTe-DSL README's
+ * moe row lists a W4A16 mode: BF16 activations, inline FP4 weight dequant).
+ * The pages give no bit layout; the format is taken as NVIDIA defines NVFP4:
+ *   element  E2M1: bit 3 sign, bits 2-1 exponent e (bias 1), bit 0 mantissa m;
+ *            e = 0: value m * 0.5 (subnormal); e > 0: 2^(e-1) * (1 + m/2)
+ *   block    16 consecutive elements of a row share one scale in FP8 E4M3:
+ *            bit 7 sign, bits 6-3 exponent E (bias 7), bits 2-0 mantissa M;
+ *            E = 0: M/8 * 2^-6 (subnormal); E = 15 and M = 7: NaN (no inf);
+ *            otherwise 2^(E-7) * (1 + M/8)
+ *   tensor   one fp32 scale g per expert matrix
+ *   weight = e2m1 * e4m3 * g
+ * Storage (this library's reading; a lossless repack of a checkpoint's
+ * separate code and scale tensors): super-blocks of 256 weights, 144 bytes,
+ *   bytes 0-15    the E4M3 scales of weights 16j .. 16j+15 (j = 0..15)
+ *   bytes 16-143  codes: byte 16 + l holds weight 2l in its low nibble and
+ *                 weight 2l+1 in its high nibble. */
+double or_e2m1_to_double(int code) {
+    int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    double v = e == 0 ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+    return sign ? -v : v;
+}
+
+double or_e4m3_to_double(uint8_t b) {
+    int sign = (b >> 7) & 1, E = (b >> 3) & 15, M = b & 7;
+    double v;
+    if (E == 15 && M == 7) v = NAN;
+    else if (E == 0) v = ldexp((double)M / 8.0, -6);
+    else v = ldexp(1.0 + (double)M / 8.0, E - 7);
+    return sign ? -v : v;
+}
+
+/* Decode NVFP4 super-blocks into fp32 weights: e2m1 * e4m3 * g formed in
+ * fp64 (exact: at most 2 + 4 + 24 significant bits) and rounded once. */
+void or_nvfp4_dequant(const uint8_t *blocks, int64_t n_blocks, float g, float *out) {
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        const uint8_t *blk = blocks + b * OR_BLOCK_BYTES;
+        for (int i = 0; i < OR_QK; ++i) {
+            int byte = blk[16 + i / 2];
+            int code = (i % 2 == 0) ? (byte & 15) : (byte >> 4);
+            double w = or_e2m1_to_double(code) * or_e4m3_to_double(blk[i / 16]) * (double)g;
+            out[b * OR_QK + i] = (float)w;
+        }
+    }
+}
+
 /* Router logits in fp64: z_e = sum_c W_r[e][c] * x_c (+ bias_e). */
 void or_router_logits(const float *router_w, const float *bias, const uint16_t *x_bf16,
                       int E, int H, double *z) {
@@ -210,28 +259,39 @@ void or_route_tokens(const float *router_w, const float *bias, const uint16_t *x
 
 static double or_silu(double g) { return g / (1.0 + exp(-g)); }
 
-/* One expert's SwiGLU FFN in fp64:
+#define OR_WTYPE_Q4_K 12
+#define OR_WTYPE_NVFP4 100
+
+/* One row of `cols` weights of either format as fp32 (g: the matrix's NVFP4
+ * tensor scale, unused for Q4_K). */
+static void or_row(int wtype, const uint8_t *row_blocks, int cols, float g, float *out) {
+    if (wtype == OR_WTYPE_NVFP4) or_nvfp4_dequant(row_blocks, cols / OR_QK, g, out);
+    else or_q4k_row(row_blocks, cols, out);
+}
+
+/* One expert's SwiGLU FFN in fp64, weights of type wtype:
  *   g_r = sum_c Wg[r][c] x_c,  u_r = sum_c Wu[r][c] x_c,  h_r = silu(g_r) u_r,
  *   y_c = sum_r Wd[c][r] h_r.
- * wg, wu: this expert's [I][H/256] blocks; wd: its [H][I/256] blocks. */
-void or_expert_ffn(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd,
-                   int H, int I, const double *x, double *h_out, double *y) {
+ * wg, wu: this expert's [I][H/256] blocks; wd: its [H][I/256] blocks; gg,
+ * gu, gd: the three matrices' NVFP4 tensor scales (ignored for Q4_K). */
+void or_expert_ffn_wt(int wtype, const uint8_t *wg, const uint8_t *wu, const uint8_t *wd, float gg,
+                      float gu, float gd, int H, int I, const double *x, double *h_out, double *y) {
     float *row = (float *)malloc(sizeof(float) * (size_t)(H > I ? H : I));
     double *h = (double *)malloc(sizeof(double) * (size_t)I);
     int64_t gate_row_bytes = (int64_t)(H / OR_QK) * OR_BLOCK_BYTES;
     int64_t down_row_bytes = (int64_t)(I / OR_QK) * OR_BLOCK_BYTES;
     for (int r = 0; r < I; ++r) {
         double g = 0.0, u = 0.0;
-        or_q4k_row(wg + r * gate_row_bytes, H, row);
+        or_row(wtype, wg + r * gate_row_bytes, H, gg, row);
         for (int c = 0; c < H; ++c) g += (double)row[c] * x[c];
-        or_q4k_row(wu + r * gate_row_bytes, H, row);
+        or_row(wtype, wu + r * gate_row_bytes, H, gu, row);
         for (int c = 0; c < H; ++c) u += (double)row[c] * x[c];
         h[r] = or_silu(g) * u;
         if (h_out) h_out[r] = h[r];
     }
     for (int c = 0; c < H; ++c) {
         double s = 0.0;
-        or_q4k_row(wd + c * down_row_bytes, I, row);
+        or_row(wtype, wd + c * down_row_bytes, I, gd, row);
         for (int r = 0; r < I; ++r) s += (double)row[r] * h[r];
         y[c] = s;
     }
@@ -239,12 +299,20 @@ void or_expert_ffn(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd,
     free(h);
 }
 
-/* The whole MoE FFN for one token.  Outputs: ids [k], w [k], out32 [H]
- * (fp32-rounded), and optionally out64 [H] and h [k][I] (fp64). */
-void or_moe_token(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down,
-                  const float *router_w, const float *bias, int H, int I, int E, int k,
-                  const uint16_t *x_bf16, int32_t *ids, double *w, float *out32,
-                  double *out64, double *h_out) {
+/* The Q4_K expert FFN (as or_expert_ffn_wt with Q4_K weights). */
+void or_expert_ffn(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd,
+                   int H, int I, const double *x, double *h_out, double *y) {
+    or_expert_ffn_wt(OR_WTYPE_Q4_K, wg, wu, wd, 0.f, 0.f, 0.f, H, I, x, h_out, y);
+}
+
+/* The whole MoE FFN for one token, experts of type wtype (gsc: the NVFP4
+ * tensor scales [E][3] of each expert's gate, up and down matrices, or NULL
+ * for Q4_K).  Outputs: ids [k], w [k], out32 [H] (fp32-rounded), and
+ * optionally out64 [H] and h [k][I] (fp64). */
+void or_moe_token_wt(int wtype, const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down,
+                     const float *gsc, const float *router_w, const float *bias, int H, int I, int E,
+                     int k, const uint16_t *x_bf16, int32_t *ids, double *w, float *out32,
+                     double *out64, double *h_out) {
     double *x = (double *)malloc(sizeof(double) * (size_t)H);
     double *y = (double *)malloc(sizeof(double) * (size_t)H);
     double *acc = (double *)calloc((size_t)H, sizeof(double));
@@ -254,9 +322,9 @@ void or_moe_token(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_d
     int64_t down_expert_bytes = (int64_t)H * (I / OR_QK) * OR_BLOCK_BYTES;
     for (int i = 0; i < k; ++i) {
         int e = ids[i];
-        or_expert_ffn(w_gate + e * gate_expert_bytes, w_up + e * gate_expert_bytes,
-                      w_down + e * down_expert_bytes, H, I, x,
-                      h_out ? h_out + (int64_t)i * I : NULL, y);
+        or_expert_ffn_wt(wtype, w_gate + e * gate_expert_bytes, w_up + e * gate_expert_bytes,
+                         w_down + e * down_expert_bytes, gsc ? gsc[3 * e] : 0.f, gsc ? gsc[3 * e + 1] : 0.f,
+                         gsc ? gsc[3 * e + 2] : 0.f, H, I, x, h_out ? h_out + (int64_t)i * I : NULL, y);
         for (int c = 0; c < H; ++c) acc[c] += w[i] * y[c];
     }
     for (int c = 0; c < H; ++c) {
@@ -266,6 +334,14 @@ void or_moe_token(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_d
     free(x);
     free(y);
     free(acc);
+}
+
+void or_moe_token(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down,
+                  const float *router_w, const float *bias, int H, int I, int E, int k,
+                  const uint16_t *x_bf16, int32_t *ids, double *w, float *out32,
+                  double *out64, double *h_out) {
+    or_moe_token_wt(OR_WTYPE_Q4_K, w_gate, w_up, w_down, NULL, router_w, bias, H, I, E, k, x_bf16, ids, w,
+                    out32, out64, h_out);
 }
 
 /* Pre-MoE RMSNorm (the "rmsnorm" kernel of the sparkinfer README's "Layout"

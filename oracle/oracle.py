@@ -50,6 +50,16 @@ def _load():
             lib.or_q4k_scale_min.argtypes = [_c_u8p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                              ctypes.POINTER(ctypes.c_int)]
             lib.or_q4k_dequant.argtypes = [_c_u8p, ctypes.c_int64, _c_f32p]
+            lib.or_e2m1_to_double.restype = ctypes.c_double
+            lib.or_e2m1_to_double.argtypes = [ctypes.c_int]
+            lib.or_e4m3_to_double.restype = ctypes.c_double
+            lib.or_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.or_nvfp4_dequant.argtypes = [_c_u8p, ctypes.c_int64, ctypes.c_float, _c_f32p]
+            lib.or_expert_ffn_wt.argtypes = [ctypes.c_int, _c_u8p, _c_u8p, _c_u8p, ctypes.c_float, ctypes.c_float,
+                                             ctypes.c_float, ctypes.c_int, ctypes.c_int, _c_f64p, _c_f64p, _c_f64p]
+            lib.or_moe_token_wt.argtypes = [ctypes.c_int, _c_u8p, _c_u8p, _c_u8p, _c_f32p, _c_f32p, _c_f32p,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _c_u16p,
+                                            _c_i32p, _c_f64p, _c_f32p, _c_f64p, _c_f64p]
             lib.or_router_logits.argtypes = [_c_f32p, _c_f32p, _c_u16p, ctypes.c_int, ctypes.c_int,
                                              _c_f64p]
             lib.or_topk.argtypes = [_c_f32p, ctypes.c_int, ctypes.c_int, _c_i32p]
@@ -109,6 +119,28 @@ def q4k_dequant(blocks: np.ndarray) -> np.ndarray:
     return out
 
 
+WTYPE_Q4_K = 12
+WTYPE_NVFP4 = 100
+
+
+def e2m1_to_double(code: int) -> float:
+    return _load().or_e2m1_to_double(int(code))
+
+
+def e4m3_to_double(b: int) -> float:
+    return _load().or_e4m3_to_double(int(b))
+
+
+def nvfp4_dequant(blocks: np.ndarray, g: float) -> np.ndarray:
+    """fp32 weights of NVFP4 super-blocks (144 bytes per 256 weights) with tensor scale g."""
+    b = np.ascontiguousarray(blocks, dtype=np.uint8)
+    n = b.size // 144
+    assert n * 144 == b.size
+    out = np.empty(n * 256, dtype=np.float32)
+    _load().or_nvfp4_dequant(_ptr(b, _c_u8p), n, float(np.float32(g)), _ptr(out, _c_f32p))
+    return out
+
+
 def router_logits(router_w: np.ndarray, x_bf16: np.ndarray, bias: np.ndarray | None = None):
     w = np.ascontiguousarray(router_w, dtype=np.float32)
     x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
@@ -153,16 +185,18 @@ def route_tokens(router_w, x_bf16, k, bias=None, want_logits=False):
     return ids, w, z, margin
 
 
-def expert_ffn(wg_e, wu_e, wd_e, x64, H, I):
-    """One expert's SwiGLU FFN in fp64.  Returns (h [I], y [H])."""
+def expert_ffn(wg_e, wu_e, wd_e, x64, H, I, wtype=WTYPE_Q4_K, gscales=(0.0, 0.0, 0.0)):
+    """One expert's SwiGLU FFN in fp64 (Q4_K, or NVFP4 with the three matrices'
+    tensor scales).  Returns (h [I], y [H])."""
     g = np.ascontiguousarray(wg_e, dtype=np.uint8)
     u = np.ascontiguousarray(wu_e, dtype=np.uint8)
     d = np.ascontiguousarray(wd_e, dtype=np.uint8)
     x = np.ascontiguousarray(x64, dtype=np.float64)
     h = np.empty(I, dtype=np.float64)
     y = np.empty(H, dtype=np.float64)
-    _load().or_expert_ffn(_ptr(g, _c_u8p), _ptr(u, _c_u8p), _ptr(d, _c_u8p), H, I,
-                          _ptr(x, _c_f64p), _ptr(h, _c_f64p), _ptr(y, _c_f64p))
+    gg, gu, gd = (float(np.float32(v)) for v in gscales)
+    _load().or_expert_ffn_wt(int(wtype), _ptr(g, _c_u8p), _ptr(u, _c_u8p), _ptr(d, _c_u8p), gg, gu, gd, H, I,
+                             _ptr(x, _c_f64p), _ptr(h, _c_f64p), _ptr(y, _c_f64p))
     return h, y
 
 
@@ -186,11 +220,16 @@ def moe_token(layer, x_bf16_row, want_h=False) -> TokenResult:
     h = np.empty((k, I), dtype=np.float64) if want_h else None
     bias = None if layer.router_bias is None else np.ascontiguousarray(layer.router_bias,
                                                                        dtype=np.float32)
-    _load().or_moe_token(_ptr(layer.w_gate, _c_u8p), _ptr(layer.w_up, _c_u8p),
-                         _ptr(layer.w_down, _c_u8p), _ptr(layer.router_w, _c_f32p),
-                         _ptr(bias, _c_f32p), H, I, E, k, _ptr(x, _c_u16p), _ptr(ids, _c_i32p),
-                         _ptr(w, _c_f64p), _ptr(out32, _c_f32p), _ptr(out64, _c_f64p),
-                         _ptr(h, _c_f64p))
+    wtype = getattr(layer, "wtype", WTYPE_Q4_K)
+    gsc = None
+    if wtype == WTYPE_NVFP4:
+        gsc = np.ascontiguousarray(layer.gscale, dtype=np.float32)
+        assert gsc.shape == (E, 3)
+    _load().or_moe_token_wt(int(wtype), _ptr(layer.w_gate, _c_u8p), _ptr(layer.w_up, _c_u8p),
+                            _ptr(layer.w_down, _c_u8p), _ptr(gsc, _c_f32p), _ptr(layer.router_w, _c_f32p),
+                            _ptr(bias, _c_f32p), H, I, E, k, _ptr(x, _c_u16p), _ptr(ids, _c_i32p),
+                            _ptr(w, _c_f64p), _ptr(out32, _c_f32p), _ptr(out64, _c_f64p),
+                            _ptr(h, _c_f64p))
     return TokenResult(ids, w, out32, out64, h)
 
 
@@ -274,6 +313,7 @@ def counts_offsets_perm(ids: np.ndarray, n_experts: int):
 
 __all__ = [
     "build", "half_to_double", "bf16_to_double", "q4k_scale_min", "q4k_dequant",
+    "WTYPE_Q4_K", "WTYPE_NVFP4", "e2m1_to_double", "e4m3_to_double", "nvfp4_dequant",
     "router_logits", "topk", "renorm_weights", "route_tokens", "expert_ffn", "moe_token",
     "TokenResult", "counts_offsets_perm", "rmsnorm", "moe_token_prenorm", "PrenormResult", "route_tokens_prenorm",
 ]

@@ -113,6 +113,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.si_moe_read_status.argtypes = [vp, vp, vp]
     lib.si_debug_q4k_dequant.restype = ctypes.c_int
     lib.si_debug_q4k_dequant.argtypes = [vp, i64, vp, vp, vp]
+    lib.si_debug_q4k_dequant_f16.restype = ctypes.c_int
+    lib.si_debug_q4k_dequant_f16.argtypes = [vp, i64, vp, vp, vp]
+    lib.si_moe_read_status_noalloc.restype = ctypes.c_int
+    lib.si_moe_read_status_noalloc.argtypes = [vp]
     lib.si_debug_topk.restype = ctypes.c_int
     lib.si_debug_topk.argtypes = [vp, i32, ctypes.POINTER(si_moe_desc),
                                   ctypes.POINTER(si_moe_route_out), vp]
@@ -294,6 +298,15 @@ def si_moe_read_status(plan: Plan, scratch, stream=None) -> int:
 def si_debug_q4k_dequant(blocks, n_blocks, out_f32=None, out_bf16=None, stream=None):
     _check(load_library().si_debug_q4k_dequant(_ptr(blocks), int(n_blocks), _ptr(out_f32),
                                                _ptr(out_bf16), _stream(stream)), "si_debug_q4k_dequant")
+
+
+def si_debug_q4k_dequant_f16(blocks, n_blocks, out_f16, gamma=None, stream=None):
+    _check(load_library().si_debug_q4k_dequant_f16(_ptr(blocks), int(n_blocks), _ptr(gamma), _ptr(out_f16),
+                                                   _stream(stream)), "si_debug_q4k_dequant_f16")
+
+
+def si_moe_read_status_noalloc(stream=None) -> int:
+    return load_library().si_moe_read_status_noalloc(_stream(stream))
 
 
 def si_debug_topk(logits, n, desc: si_moe_desc, route_out: si_moe_route_out, stream=None):

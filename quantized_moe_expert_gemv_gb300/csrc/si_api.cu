@@ -216,16 +216,17 @@ si_status si_moe_scratch_init(si_moe_plan_t plan, void *scratch, size_t scratch_
     return SI_OK;
 }
 
-static si_status forward_decode_impl(si_moe_plan_t plan, const si_moe_layer *layer,
-                                     const void *x_bf16, int32_t n_tokens, float *out,
-                                     si_moe_route_out *ro, void *scratch, size_t scratch_bytes,
-                                     cudaEvent_t const *events, si_stream_t stream) {
-    if (!plan || !layer || !x_bf16 || !out || !scratch) return SI_ERR_INVALID_ARG;
+}  // extern "C"
+
+// Every argument check of a decode call except those of the scratch buffer.
+si_status si::check_decode_args(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
+                                int32_t n_tokens, const float *out, const si_moe_route_out *ro) {
+    if (!plan || !layer || !x_bf16 || !out) return SI_ERR_INVALID_ARG;
     if (!layer->w_gate || !layer->w_up || !layer->w_down || !layer->router_w) return SI_ERR_INVALID_ARG;
     if (n_tokens < 1 || n_tokens > SI_MAX_DECODE_TOKENS) return SI_ERR_INVALID_ARG;
     if (!aligned(layer->w_gate, 16) || !aligned(layer->w_up, 16) || !aligned(layer->w_down, 16) ||
         !aligned(layer->router_w, 16) || !aligned(x_bf16, 16) || !aligned(out, 16) ||
-        !aligned(scratch, 16) || (layer->router_bias && !aligned(layer->router_bias, 4)) ||
+        (layer->router_bias && !aligned(layer->router_bias, 4)) ||
         (layer->norm_weight && !aligned(layer->norm_weight, 16)))
         return SI_ERR_MISALIGNED;
     if (layer->norm_weight && !(layer->norm_eps >= 0.f && layer->norm_eps <= 3.0e38f)) return SI_ERR_INVALID_ARG;
@@ -233,6 +234,19 @@ static si_status forward_decode_impl(si_moe_plan_t plan, const si_moe_layer *lay
                (ro->expert_counts && !aligned(ro->expert_counts, 4)) ||
                (ro->logits && !aligned(ro->logits, 4))))
         return SI_ERR_MISALIGNED;
+    return SI_OK;
+}
+
+extern "C" {
+
+static si_status forward_decode_impl(si_moe_plan_t plan, const si_moe_layer *layer,
+                                     const void *x_bf16, int32_t n_tokens, float *out,
+                                     si_moe_route_out *ro, void *scratch, size_t scratch_bytes,
+                                     cudaEvent_t const *events, si_stream_t stream) {
+    const si_status chk = si::check_decode_args(plan, layer, x_bf16, n_tokens, out, ro);
+    if (chk != SI_OK) return chk;
+    if (!scratch) return SI_ERR_INVALID_ARG;
+    if (!aligned(scratch, 16)) return SI_ERR_MISALIGNED;
     const si_moe_desc &d = plan->p.desc;
     const DecodeLayout L = si::decode_layout(d, n_tokens);
     if (scratch_bytes < L.total) return SI_ERR_SCRATCH_TOO_SMALL;
@@ -415,6 +429,18 @@ si_status si_debug_q4k_dequant(const void *blocks, int64_t n_blocks, float *out_
     if (si::launch_debug_dequant(static_cast<const uint8_t *>(blocks), n_blocks, out_f32, out_bf16,
                                  (cudaStream_t)stream) != cudaSuccess)
         return SI_ERR_CUDA;
+    return SI_OK;
+}
+
+si_status si_debug_q4k_dequant_f16(const void *blocks, int64_t n_blocks, const float *gamma, uint16_t *out_f16,
+                                   si_stream_t stream) {
+    if (!blocks || n_blocks < 0 || !out_f16) return SI_ERR_INVALID_ARG;
+    if (!aligned(blocks, 16) || !aligned(out_f16, 16) || (gamma && !aligned(gamma, 16))) return SI_ERR_MISALIGNED;
+    if (si::launch_debug_dequant_f16(static_cast<const uint8_t *>(blocks), n_blocks, gamma, out_f16,
+                                     (cudaStream_t)stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SI_ERR_CUDA;
+    }
     return SI_OK;
 }
 

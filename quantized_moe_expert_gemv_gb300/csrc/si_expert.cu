@@ -709,11 +709,15 @@ static cudaError_t launch_expert_t(const DecodeArgs &a, int grid, cudaStream_t s
     cfg.blockDim = dim3(kExpertThreads);
     cfg.dynamicSmemBytes = a.fz_smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    // The grid barrier between gate/up and down needs every CTA resident at
+    // once: a cooperative launch guarantees that, or fails at launch time.
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

@@ -20,13 +20,16 @@
 // The router kernel first sets the output to zero (to x in a pre-normed
 // block, whose residual it is).  Weight bytes: gate/up rows by
 // 1-D bulk copies; down blocks, 144-byte pieces with a 432-byte row stride,
-// by 2-D tensor maps (boxes of 144 bytes x 128 rows, one mbarrier per box, so
-// the down phase starts on the first box while the later ones land; the last
-// box of a CTA uses a second map whose box height is the remainder).  The
-// barriers' transaction counts are posted before the dependency wait, and one
-// producer thread issues every copy as soon as the expert id is known (L2
-// evict-first).  The kernel lets the next kernel of the stream launch at once:
-// that kernel's own dependency wait still covers all of this kernel's work.
+// by 2-D tensor maps (boxes of 144 bytes x 128 rows, all completing on one
+// mbarrier: they are issued after the gate/up rows and land while those are
+// computed, and every wait on an mbarrier costs its warp a few hundred
+// cycles even when the phase is already complete; the last box of a CTA uses
+// a second map whose box height is the remainder).  The barriers'
+// transaction counts are posted before the dependency wait, and the producer
+// thread reads its unit's expert id and issues every copy right after that
+// wait (L2 evict-first).  The kernel lets the next kernel of the stream
+// launch at once: that kernel's own dependency wait still covers all of this
+// kernel's work.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -88,7 +91,6 @@ __global__ void __launch_bounds__(kClThreads, 1)
     constexpr int rowg = NBH * kBlockBytes;
     constexpr int stageA = 2 * CH * rowg;
     __shared__ int s_err;
-    __shared__ int s_expert;
     __shared__ float s_w;
     __shared__ int s_lastA[8];
     __shared__ int s_lastB;
@@ -127,10 +129,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
     uint32_t *const xq_s = reinterpret_cast<uint32_t *>(sm + pin_i32(a.cl_off_x));  // quantised x, later h
     const uint32_t fullA = smem_addr(sm + pin_i32(a.cl_off_bar));
     const uint32_t emptyA = fullA + 8 * NSA;
-    const uint32_t fullB = emptyA + 8 * NSA;  // [nbox]
+    const uint32_t fullB = emptyA + 8 * NSA;  // all down boxes complete on this one barrier
     int32_t *status = ctrl + kCtrlStatus;
     auto stage_bytes = [&](int j) { return (uint32_t)((min(CH * (j + 1), n_rp) - CH * j) * rowg); };
-    auto box_bytes = [&](int bx) { return (uint32_t)((bx == nbox - 1 ? tail_rows : kBoxRows) * kBlockBytes); };
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tmap_down);  // descriptor fetches off the critical path
@@ -140,14 +141,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
             mbar_init(emptyA + 8 * st, kCW);
             s_lastA[st] = -1;
         }
-        for (int bx = 0; bx < nbox; ++bx) mbar_init(fullB + 8 * bx, 1);
+        mbar_init(fullB, 1);
         s_lastB = -1;
         s_err = 0;
         fence_mbar_init();
         // the byte counts of the first ring pass and of every down box do not
         // depend on the routing: post them now (the producer's arrival)
         for (int j = 0; j < min(nA, NSA); ++j) mbar_arrive_expect_tx(fullA + 8 * j, 2 * stage_bytes(j));
-        for (int bx = 0; bx < nbox; ++bx) mbar_arrive_expect_tx(fullB + 8 * bx, box_bytes(bx));
+        // the bytes the box copies deliver: the last box is tail_rows high for every
+        // CTA (the largest CTA's remainder), which may exceed this CTA's n_rows
+        mbar_arrive_expect_tx(fullB, (uint32_t)(((nbox - 1) * kBoxRows + tail_rows) * kBlockBytes));
     }
     // The token's H/64 activation chunks, quantised once (warp 0) into shared memory
     // before the dependency wait: the router launches this kernel only after its
@@ -215,11 +218,14 @@ __global__ void __launch_bounds__(kClThreads, 1)
     if (NORM) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     pdl_wait();  // routing of this token is complete
-    // The router left the k selected experts in rank order with their logits;
-    // the renormalised weight of rank r is exp(z_r - z_0) / sum_j exp(z_j - z_0)
-    // (z_0 is the largest).  Warp 0 forms all k; CTA 0 reports them.
+    // The router left the k selected experts in rank order with their logits.
+    // Only the producer thread needs this unit's expert id, to address its
+    // copies: it reads it itself and issues them at once.  The renormalised
+    // weight of rank r, exp(z_r - z_0) / sum_j exp(z_j - z_0) (z_0 the
+    // largest), is needed only by the final reductions: warp 0 forms all k
+    // meanwhile (CTA 0 reports them); the __syncthreads before the reductions
+    // publishes it.
     if (warp == 0) {
-        const int id = lane < k ? ids[lane] : 0;
         const float zr = lane < k ? zsel[lane] : 0.f;
         const float z0 = __shfl_sync(0xffffffffu, zr, 0);
         const float ex = lane < k ? expf(zr - z0) : 0.f;
@@ -227,19 +233,15 @@ __global__ void __launch_bounds__(kClThreads, 1)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
         const float w = ex / den;
-        if (lane == slot) {
-            s_expert = id;
-            s_w = w;
-        }
+        if (lane == slot) s_w = w;
         if (blockIdx.x == 0 && o_w && lane < k) o_w[lane] = w;
     }
-    __syncthreads();
-    const int e = s_expert;
     volatile int *verr = &s_err;
 
     // --------------------------------------------------------- producer
     if (warp == kCW) {
         if (lane == 0) {
+            const int e = ids[slot];
             const uint64_t pol = l2_evict_first_policy();
             auto issueA = [&](int j) -> bool {
                 const int st = j % NSA;
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             // tail_rows high (its own map); each box completes its own barrier
             for (int bx = 0; bx < nbox; ++bx)
                 tma_load_2d(smem_addr(stB + (size_t)bx * box_stride), bx == nbox - 1 ? &tmap_tail : &tmap_down,
-                            kBlockBytes * bcol, e * H + c_lo + bx * kBoxRows, fullB + 8 * bx, pol);
+                            kBlockBytes * bcol, e * H + c_lo + bx * kBoxRows, fullB, pol);
             s_lastB = 0;
             for (int j = first; j < nA; ++j)
                 if (!issueA(j)) break;
@@ -312,12 +314,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
 #pragma unroll
             for (int m = 0; m < kPairs; ++m) {
                 const int ql = (warp * RPW + g) * kPairs + m;  // row pair within the stage
-                const uint8_t *grow = stage + ql * rowg + b * kBlockBytes;
-                const uint8_t *urow = grow + CH * rowg;
-                const uint4 hg = ld_s128(grow), qg0 = ld_s128(grow + 16 + 32 * i), qg1 = ld_s128(grow + 32 + 32 * i);
-                const uint4 hu = ld_s128(urow), qu0 = ld_s128(urow + 16 + 32 * i), qu1 = ld_s128(urow + 32 + 32 * i);
-                part[2 * m] = chunk_contrib_i(chunk_scales_i(hg, i), chunk_isums(qg0, qg1, xwf), xs, Xa, Xb);
-                part[2 * m + 1] = chunk_contrib_i(chunk_scales_i(hu, i), chunk_isums(qu0, qu1, xwf), xs, Xa, Xb);
+                part[2 * m] = part[2 * m + 1] = 0.f;
+                // a partly filled stage: skip the empty slots (warp-uniform when a warp holds one row)
+                if (RPW > 1 || CH * j + ql < n_rp) {
+                    const uint8_t *grow = stage + ql * rowg + b * kBlockBytes;
+                    const uint8_t *urow = grow + CH * rowg;
+                    const uint4 hg = ld_s128(grow), qg0 = ld_s128(grow + 16 + 32 * i), qg1 = ld_s128(grow + 32 + 32 * i);
+                    const uint4 hu = ld_s128(urow), qu0 = ld_s128(urow + 16 + 32 * i), qu1 = ld_s128(urow + 32 + 32 * i);
+                    part[2 * m] = chunk_contrib_i(chunk_scales_i(hg, i), chunk_isums(qg0, qg1, xwf), xs, Xa, Xb);
+                    part[2 * m + 1] = chunk_contrib_i(chunk_scales_i(hu, i), chunk_isums(qu0, qu1, xwf), xs, Xa, Xb);
+                }
             }
             // totals: g0 at group lane 0, u0 at GS/4, g1 at GS/2, u1 at 3GS/4
             const float tot = quad_sum<GS>(part[0], part[1], part[2], part[3], li);
@@ -373,15 +379,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
         const float hs = hqf[3 * i], Ha = hqf[3 * i + 1], Hb = hqf[3 * i + 2];
         auto hwf = [&hw](int p) { return hw[p]; };
-        // box m holds rows [128m, 128m + 128) = the rows of iteration m; every warp
-        // waits for every box (so none is left in flight), rows past n_rows are skipped
+        // box m holds rows [128m, 128m + 128) = the rows of iteration m; every box
+        // completes on one barrier (they land while gate/up is computed), rows past
+        // n_rows are skipped
+        const bool landed = mbar_wait_warp(fullB, 0, budget);
+        if (!landed) {
+            set_status(status, SI_ERR_TIMEOUT);
+            *verr = 1;
+        }
 #pragma unroll 1
-        for (int m = 0; m < nbox; ++m) {
-            if (!mbar_wait_warp(fullB + 8 * m, 0, budget)) {
-                set_status(status, SI_ERR_TIMEOUT);
-                *verr = 1;
-                break;
-            }
+        for (int m = 0; m < (landed ? nbox : 0); ++m) {
             const int lr = kBoxRows * m + 8 * warp + r8;
             float v = 0.f;
             if (lr < n_rows) {
@@ -402,8 +409,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     } else if (threadIdx.x == 0) {  // no copy may still be writing this CTA's shared memory at exit
         for (int st = 0; st < NSA; ++st)
             if (s_lastA[st] >= 0) mbar_wait_bounded(fullA + 8 * st, s_lastA[st], kDrain);
-        if (s_lastB >= 0)
-            for (int bx = 0; bx < nbox; ++bx) mbar_wait_bounded(fullB + 8 * bx, 0, kDrain);
+        if (s_lastB >= 0) mbar_wait_bounded(fullB, 0, kDrain);
     }
 }
 
@@ -453,7 +459,7 @@ bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs
     a.cl_off_y = off;
     off += al(rpc * 4);
     a.cl_off_bar = off;
-    off += 8 * (2 * NSA + nbox) + 64;
+    off += 8 * (2 * NSA + 1) + 64;
     if (off + 1024 > smem_max) return false;  // + static shared memory
     a.cl_nsa = NSA;
     a.cl_C = C;

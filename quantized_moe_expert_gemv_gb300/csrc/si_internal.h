@@ -51,6 +51,11 @@ struct Plan {
 
 DecodeLayout decode_layout(const si_moe_desc &d, int n_tokens);
 
+// Argument checks of a decode call (everything but the scratch buffer), made
+// before any launch.
+si_status check_decode_args(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
+                            int32_t n_tokens, const float *out, const si_moe_route_out *ro);
+
 // Arguments of the decode kernels (device pointers + sizes).
 struct DecodeArgs {
     const uint8_t *wg, *wu, *wd;
@@ -140,6 +145,8 @@ cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s);
 cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters);
 cudaError_t launch_debug_dequant(const uint8_t *blocks, int64_t n_blocks, float *out_f32,
                                  uint16_t *out_bf16, cudaStream_t s);
+cudaError_t launch_debug_dequant_f16(const uint8_t *blocks, int64_t n_blocks, const float *gamma, uint16_t *out,
+                                     cudaStream_t s);
 cudaError_t launch_debug_topk(const float *logits, int n, int E, int k, int32_t *ids, float *w,
                               int32_t *counts, cudaStream_t s);
 

@@ -1,6 +1,6 @@
 // si_prefill.cu -- grouped prefill: T tokens through the mixture-of-experts FFN.
 //
-// SP⚡RKINFER README (gittensor-ai-lab), "Benchmark · Qwen3.6-35B-A3B", prefill
+// SP⚡RKINFER README (gittensor-ai-lab), "Benchmark · Qwen3.8-27B", prefill
 // paragraph: the Q4_K weights are dequantized into the GEMM operand on every
 // prefill pass; sparkinfer-k3 blog post, "v0.2.2": a chunk of tokens shares one
 // weight-tile read; sparkinfer README (luciferlive112116), "Layout", moe/:
@@ -516,6 +516,66 @@ __device__ __forceinline__ Pass make_pass(int e, int tile, int prow, int sc, int
 }
 }  // namespace
 
+// Q4_K -> fp16 operand conversion, one thread's share: sub-block 2j + half of
+// the 144-byte block blk (32 weights, block columns 64j + 32half .. +31).
+// A 4-bit code q at bit p of a word becomes the fp32 value 2^23 + q*2^p by
+// or-ing in the exponent of 2^23; fma(dsc*2^-p, that, -dsc*2^(23-p)) then
+// equals dsc*q exactly (a 21-bit product), and subtracting dm rounds once:
+// the fp32 value w = d*sc*q - dmin*m (the same as fma(dsc, q, -dm)).  With
+// GAMMA, w is multiplied in fp32 by gp[l], the gain of column l (a pre-normed
+// block's RMSNorm gain).  The result is rounded to fp16 (round-to-nearest-
+// even): o[i] holds columns 2i (low half) and 2i+1.  Bytes 0, 1 of a word are
+// taken at p = 4*half, 4*half+8; bytes 2, 3 likewise after a 16-bit shift.
+// Returns true when a weight of the sub-block (before the gain) lies beyond
+// fp16's finite range.  The GEMM's dequantization warps and the test export
+// si_debug_q4k_dequant_f16 both run this function.
+struct Q4F16Lane {
+    uint32_t m0, m8;           // nibble masks at p = 4*half and 4*half + 8
+    float tp0, tp8, to0, to8;  // 2^-p and -2^(23-p) for both
+};
+__device__ __forceinline__ Q4F16Lane q4f16_lane(int half) {
+    const int p0 = 4 * half;
+    Q4F16Lane c;
+    c.m0 = 15u << p0;
+    c.m8 = 15u << (p0 + 8);
+    c.tp0 = __uint_as_float((127u - p0) << 23);
+    c.tp8 = __uint_as_float((119u - p0) << 23);
+    c.to0 = -__uint_as_float((150u - p0) << 23);
+    c.to8 = -__uint_as_float((142u - p0) << 23);
+    return c;
+}
+template <bool GAMMA>
+__device__ __forceinline__ bool q4k_subblock_f16(const Q4F16Lane &c, const uint8_t *blk, int j, int half,
+                                                 const float *gp, uint32_t (&o)[16]) {
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * j);
+    int sc, m;
+    unpack_sc_m(hdr, 2 * j + half, sc, m);
+    const float dd = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffffu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+    const float dsc = dd * (float)sc, dm = dmin * (float)m;
+    const bool bad = fmaxf(fabsf(fmaf(dsc, 15.f, -dm)), fabsf(dm)) > 65504.f;
+    const f32x2 C = pack2(dsc * c.tp0, dsc * c.tp8), O = pack2(dsc * c.to0, dsc * c.to8), D = pack2(-dm, -dm);
+    const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t w = wv[t], hi = w >> 16;
+        const f32x2 v01 = pack2(__uint_as_float((w & c.m0) | 0x4B000000u), __uint_as_float((w & c.m8) | 0x4B000000u));
+        const f32x2 v23 = pack2(__uint_as_float((hi & c.m0) | 0x4B000000u), __uint_as_float((hi & c.m8) | 0x4B000000u));
+        f32x2 r01 = add2(fma2(v01, C, O), D), r23 = add2(fma2(v23, C, O), D);
+        if (GAMMA) {
+            const float4 g4 = __ldg(reinterpret_cast<const float4 *>(gp) + t);
+            r01 = mul2(r01, pack2(g4.x, g4.y));
+            r23 = mul2(r23, pack2(g4.z, g4.w));
+        }
+        const float2 a01 = unpack2(r01), a23 = unpack2(r23);
+        o[2 * t] = f16x2_rn(a01.x, a01.y);
+        o[2 * t + 1] = f16x2_rn(a23.x, a23.y);
+    }
+    return bad;
+}
+
 // MODE 0 (gate/up): unit tile covers intermediate rows tile*128 .. +127;
 //   CTA r holds rows tile*128 + 64r + i as A rows 2i (gate) and 2i+1 (up);
 //   K = H; B rows = padded token rows of the expert (xp); epilogue
@@ -744,18 +804,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
         const int row = d >> 1, half = d & 1;
         // MODE 0: A row 2i = gate row i, 2i+1 = up row i (raw rows: gate 0-63, up 64-127)
         const int raw_row = MODE == 0 ? ((row & 1) ? 64 + (row >> 1) : (row >> 1)) : row;
-        // The codes of this thread are bits 4*half.. of each byte.  A code q at
-        // bit p of a word becomes the fp32 value 2^23 + q*2^p by or-ing in the
-        // exponent of 2^23; fma(dsc*2^-p, that, -dsc*2^(23-p)) then equals
-        // dsc*q exactly (a 21-bit product), and subtracting dm rounds once:
-        // the same fp32 value as fma(dsc, q, -dm).  Bytes 0, 1 of a word are
-        // taken at p = 4*half, 4*half+8; bytes 2, 3 likewise after a 16-bit shift.
-        const int p0 = 4 * half;
-        const uint32_t m0 = 15u << p0, m8 = 15u << (p0 + 8);
+        const Q4F16Lane lc = q4f16_lane(half);  // the codes of this thread are bits 4*half.. of each byte
         const uint32_t tok = smem_addr(sm + kOffTok), lead_tok = mapa_shared(tok, 0);
         const uint32_t lead_full = mapa_shared(full, 0);
-        const float tp0 = __uint_as_float((127u - p0) << 23), tp8 = __uint_as_float((119u - p0) << 23);    // 2^-p
-        const float to0 = -__uint_as_float((150u - p0) << 23), to8 = -__uint_as_float((142u - p0) << 23);  // -2^(23-p)
         int astep = 0, rstep = 0;
         for_each_pass([&](const Pass &ps) {
             for (int kb = 0; kb < nK; ++kb, ++astep) {
@@ -771,45 +822,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
                     return;
                 }
                 const uint8_t *blk = sm + kOffRaw + r * kRaw + raw_row * kBlockBytes;
-                const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-                const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j);
-                const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * j);
-                int sc, m;
-                unpack_sc_m(hdr, 2 * j + half, sc, m);
-                const float dd = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffffu)));
-                const float dmin = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
-                const float dsc = dd * (float)sc, dm = dmin * (float)m;
-                if (fmaxf(fabsf(fmaf(dsc, 15.f, -dm)), fabsf(dm)) > 65504.f) set_status(status, SI_ERR_RANGE);
-                const f32x2 C = pack2(dsc * tp0, dsc * tp8), O = pack2(dsc * to0, dsc * to8), D = pack2(-dm, -dm);
-                const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                 uint32_t o[16];
-                if (MODE == 0 && gam) {
-                    // pre-normed block: the gate/up weights of hidden column c times gamma_c (the
-                    // token's 1 / rms is applied to g and u in the epilogue), so x stays exact
-                    const float4 *gp = reinterpret_cast<const float4 *>(gam + 64 * ((kb + ps.rot) % nK) + 32 * half);
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        const float4 g4 = __ldg(gp + t);
-                        const uint32_t w = wv[t], hi = w >> 16;
-                        const f32x2 v01 = pack2(__uint_as_float((w & m0) | 0x4B000000u), __uint_as_float((w & m8) | 0x4B000000u));
-                        const f32x2 v23 = pack2(__uint_as_float((hi & m0) | 0x4B000000u), __uint_as_float((hi & m8) | 0x4B000000u));
-                        const float2 r01 = unpack2(mul2(add2(fma2(v01, C, O), D), pack2(g4.x, g4.y)));
-                        const float2 r23 = unpack2(mul2(add2(fma2(v23, C, O), D), pack2(g4.z, g4.w)));
-                        o[2 * t] = f16x2_rn(r01.x, r01.y);
-                        o[2 * t + 1] = f16x2_rn(r23.x, r23.y);
-                    }
-                } else {
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        const uint32_t w = wv[t], hi = w >> 16;
-                        const f32x2 v01 = pack2(__uint_as_float((w & m0) | 0x4B000000u), __uint_as_float((w & m8) | 0x4B000000u));
-                        const f32x2 v23 = pack2(__uint_as_float((hi & m0) | 0x4B000000u), __uint_as_float((hi & m8) | 0x4B000000u));
-                        const float2 r01 = unpack2(add2(fma2(v01, C, O), D));
-                        const float2 r23 = unpack2(add2(fma2(v23, C, O), D));
-                        o[2 * t] = f16x2_rn(r01.x, r01.y);
-                        o[2 * t + 1] = f16x2_rn(r23.x, r23.y);
-                    }
-                }
+                // pre-normed block: the gate/up weights of hidden column c times gamma_c (the
+                // token's 1 / rms is applied to g and u in the epilogue), so x stays exact
+                const float *gp = (MODE == 0 && NORM) ? gam + 64 * ((kb + ps.rot) % nK) + 32 * half : nullptr;
+                if (q4k_subblock_f16<MODE == 0 && NORM>(lc, blk, j, half, gp, o)) set_status(status, SI_ERR_RANGE);
                 uint8_t *at = sm + s * kATile + row * 128;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -945,6 +962,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
         tc::fence_after_sync();
         tc::tmem_dealloc_pair(taddr, 512);
     }
+}
+
+// Test export: the GEMM operand conversion above on n_blocks blocks, one
+// thread per sub-block; out[256b + c] = fp16 of column c of block b.
+__global__ void __launch_bounds__(256) k_debug_dequant_f16(const uint8_t *blocks, int64_t n_blocks,
+                                                           const float *gamma, uint16_t *out) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= n_blocks * 8) return;
+    const int64_t b = t >> 3;
+    const int j = (int)(t & 7) >> 1, half = (int)(t & 1);
+    const Q4F16Lane lc = q4f16_lane(half);
+    const uint8_t *blk = blocks + b * kBlockBytes;
+    uint32_t o[16];
+    if (gamma)
+        q4k_subblock_f16<true>(lc, blk, j, half, gamma + 256 * b + 64 * j + 32 * half, o);
+    else
+        q4k_subblock_f16<false>(lc, blk, j, half, nullptr, o);
+    uint4 *dst = reinterpret_cast<uint4 *>(out + 256 * b + 64 * j + 32 * half);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+
+cudaError_t launch_debug_dequant_f16(const uint8_t *blocks, int64_t n_blocks, const float *gamma, uint16_t *out,
+                                     cudaStream_t s) {
+    if (n_blocks == 0) return cudaSuccess;
+    const int64_t threads = n_blocks * 8;
+    k_debug_dequant_f16<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(blocks, n_blocks, gamma, out);
+    return cudaGetLastError();
 }
 
 // =====================================================================

@@ -9,7 +9,7 @@ import pytest
 import oracle
 from quantized_moe_expert_gemv_gb300 import binding, build, device, synth
 from tests import parity
-from tests.q4k_fixtures import make_block
+from tests.q4k_fixtures import dequant_test_blocks
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -73,25 +73,7 @@ def check_tokens(layer, x_bits, out, ids, w, sample=None):
 
 # ------------------------------------------------------------------ dequant
 def test_debug_dequant_bit_exact_against_oracle():
-    g = synth.rng(100)
-    tiny = synth.make_layer(synth.TINY, seed=0)
-    parts = [tiny.w_gate.reshape(-1, 144), tiny.w_down.reshape(-1, 144),
-             synth.q4k_random_blocks(g, 5000)]
-    # closed-form blocks: every sub-block alone, scales with the high bits set
-    for j in range(8):
-        sc = [0] * 8
-        sc[j] = 63 - j
-        m = [0] * 8
-        m[(j + 3) % 8] = 40 + j
-        parts.append(make_block(0.0017, 0.0009, sc, m, np.full((8, 32), j + 3))[None])
-    # special fp16 values of d and dmin: subnormals, zero, largest finite
-    spec = synth.q4k_random_blocks(g, 6)
-    for i, (dh, mh) in enumerate([(0x0001, 0x03ff), (0x0000, 0x0400), (0x7bff, 0x0000),
-                                  (0x3c00, 0x3c00), (0x8001, 0x0002), (0x1234, 0xb800)]):
-        spec[i, 0:2] = np.array([dh & 255, dh >> 8], dtype=np.uint8)
-        spec[i, 2:4] = np.array([mh & 255, mh >> 8], dtype=np.uint8)
-    parts.append(spec)
-    blocks = np.ascontiguousarray(np.concatenate(parts, axis=0))
+    blocks = dequant_test_blocks()
     n = blocks.shape[0]
     ref = oracle.q4k_dequant(blocks)
     dev_blocks = torch.from_numpy(blocks).cuda()

@@ -9,6 +9,7 @@ import pytest
 import oracle
 from quantized_moe_expert_gemv_gb300 import binding, build, device, synth
 from tests import parity
+from tests.q4k_fixtures import dequant_test_blocks
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -144,3 +145,119 @@ def test_prefill_argument_errors():
     st = binding.si_moe_forward_prefill(plan, dl.struct(), x[:, 1:], 16, out, None, scratch, raw_status=True)
     assert st == binding.SI_ERR_MISALIGNED
     assert binding.si_moe_read_status(plan, scratch) == binding.SI_OK
+
+
+# ------------------------------------------------- the GEMM operand conversion
+def _f16_bits(values_f32: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even fp16 of fp32 values, as uint16 bits."""
+    with np.errstate(over="ignore"):  # beyond fp16's range -> inf, as the GPU's conversion gives
+        return np.asarray(values_f32, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def test_prefill_operand_dequant_bit_exact_against_oracle():
+    """The grouped prefill's own Q4_K -> fp16 conversion (the device function
+    its GEMM dequantization warps run, exported for this test) equals the
+    round-to-nearest-even fp16 of the oracle's fp32 weight, bit for bit."""
+    blocks = dequant_test_blocks()
+    n = blocks.shape[0]
+    ref = oracle.q4k_dequant(blocks)
+    out = torch.empty(n * 256, dtype=torch.int16, device="cuda")
+    binding.si_debug_q4k_dequant_f16(torch.from_numpy(blocks).cuda(), n, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint16)
+    finite = np.isfinite(ref)
+    assert finite.sum() > 0.99 * ref.size
+    assert np.array_equal(got[finite], _f16_bits(ref)[finite])
+    # the random blocks of the prefill workload's own layer
+    wl = synth.WORKLOADS["prefill"]
+    layer_blocks = synth.q4k_random_blocks(synth.rng(wl["seed"], 0, "gate"), 100_000)
+    ref = oracle.q4k_dequant(layer_blocks)
+    out = torch.empty(ref.size, dtype=torch.int16, device="cuda")
+    binding.si_debug_q4k_dequant_f16(torch.from_numpy(layer_blocks).cuda(), layer_blocks.shape[0], out)
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), _f16_bits(ref))
+
+
+def test_prefill_operand_dequant_with_norm_gain_bit_exact():
+    """Pre-normed block: the gate/up operand is fp16(fp32(w) * gamma_c), the
+    fp32 product of the oracle's fp32 weight and the column's gain, rounded
+    to nearest even in fp32 and then in fp16."""
+    blocks = dequant_test_blocks()
+    n = blocks.shape[0]
+    gamma = synth.rng(101, "gain").uniform(0.5, 1.5, n * 256).astype(np.float32)
+    gamma[:256] = 1.0  # unit gain: the plain conversion
+    gamma[256:512] = np.float32(2.0) ** synth.rng(102).integers(-3, 4, 256)  # powers of two: exact products
+    ref = oracle.q4k_dequant(blocks)
+    expect = _f16_bits(ref * gamma)  # numpy float32 * float32 rounds once, to nearest even
+    out = torch.empty(n * 256, dtype=torch.int16, device="cuda")
+    binding.si_debug_q4k_dequant_f16(torch.from_numpy(blocks).cuda(), n, out, gamma=torch.from_numpy(gamma).cuda())
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint16)
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], expect[finite])
+    assert np.array_equal(got[:256][finite[:256]], _f16_bits(ref[:256])[finite[:256]])
+
+
+# --------------------------------------------------------------- fp16 range
+def _status_after_prefill(layer, x_bits):
+    s = layer.shape
+    T = x_bits.shape[0]
+    dl = device.to_device(layer)
+    plan = binding.si_moe_plan(binding.make_desc(s.hidden, s.intermediate, s.n_experts, s.top_k, max_tokens=T))
+    scratch = device.alloc_scratch(plan, binding.SI_MODE_PREFILL, T)
+    out = torch.empty((T, s.hidden), dtype=torch.float32, device="cuda")
+    binding.si_moe_forward_prefill(plan, dl.struct(), device.tokens_to_device(x_bits), T, out, None, scratch)
+    return binding.si_moe_read_status(plan, scratch), plan, scratch, dl
+
+
+def _prefill_again_is_correct(layer, plan, scratch, dl):
+    """After an error: re-initialise the scratch, run a normal prefill of the
+    tiny layer's tokens and check it against the oracle."""
+    s = layer.shape
+    T = 8  # within the plan's max_tokens (10)
+    x = synth.make_tokens(s, seed=3, n_tokens=T)
+    binding.si_moe_scratch_init(plan, scratch)
+    out = torch.full((T, s.hidden), float("nan"), dtype=torch.float32, device="cuda")
+    ids = torch.full((T, s.top_k), -1, dtype=torch.int32, device="cuda")
+    binding.si_moe_forward_prefill(plan, dl.struct(), device.tokens_to_device(x), T, out,
+                                   binding.route_struct(topk_ids=ids), scratch)
+    assert binding.si_moe_read_status(plan, scratch) == binding.SI_OK
+    got, gids = out.cpu().numpy(), ids.cpu().numpy()
+    for t in range(T):
+        ref = oracle.moe_token(layer, x[t])
+        if np.array_equal(gids[t], ref.ids):
+            parity.assert_close(got[t], ref.out64, f"token {t} after a range error")
+
+
+def test_prefill_input_beyond_fp16_range_reports_range_error():
+    layer = synth.make_layer(synth.TINY, seed=0)
+    x = synth.make_tokens(synth.TINY, seed=2, n_tokens=10)
+    x[4, 17] = synth.bf16_bits(np.array([1.0e5], dtype=np.float32))[0]
+    st, plan, scratch, dl = _status_after_prefill(layer, x)
+    assert st == binding.SI_ERR_RANGE
+    _prefill_again_is_correct(layer, plan, scratch, dl)
+
+
+def test_prefill_h_beyond_fp16_range_reports_range_error():
+    """Weights within fp16's range (d = 0.25, dmin = 0: |w| <= 236) whose
+    SwiGLU output h = silu(g) * u reaches millions for N(0,1) tokens."""
+    layer = synth.make_layer(synth.TINY, seed=0)
+    big = synth.make_layer(synth.TINY, seed=0)
+    for w in (big.w_gate, big.w_up):
+        w[..., 0:2] = np.array([0.25], dtype="<f2").view(np.uint8)
+        w[..., 2:4] = 0
+    x = synth.make_tokens(synth.TINY, seed=2, n_tokens=10)
+    st, plan, scratch, _ = _status_after_prefill(big, x)
+    assert st == binding.SI_ERR_RANGE
+    _prefill_again_is_correct(layer, plan, scratch, device.to_device(layer))
+
+
+def test_prefill_weight_beyond_fp16_range_reports_range_error():
+    """A block scale d = 65504 (the largest finite fp16): d*sc*q overflows fp16."""
+    layer = synth.make_layer(synth.TINY, seed=0)
+    bad = synth.make_layer(synth.TINY, seed=0)
+    bad.w_down[:, 100, 0, 0:2] = np.array([65504.0], dtype="<f2").view(np.uint8)  # in every expert
+    bad.w_down[:, 100, 0, 4:16] = 0xFF  # every 6-bit scale 63
+    x = synth.make_tokens(synth.TINY, seed=2, n_tokens=10)
+    st, plan, scratch, _ = _status_after_prefill(bad, x)
+    assert st == binding.SI_ERR_RANGE
+    _prefill_again_is_correct(layer, plan, scratch, device.to_device(layer))

@@ -63,6 +63,9 @@ def test_noalloc_decode_matches_caller_scratch_decode_on_two_calls_in_a_row():
         assert np.isfinite(o_h).all()
         for t in range(o_h.shape[0]):
             parity.assert_close(o_h[t], r_h[t], "no-allocation decode vs caller-scratch decode")
+    # no device-side error was recorded in the fixed array, and reading clears nothing else
+    assert binding.si_moe_read_status_noalloc() == binding.SI_OK
+    assert binding.si_moe_read_status(plan, scratch) == binding.SI_OK
 
 
 def test_noalloc_decode_rejects_bad_arguments():
@@ -75,3 +78,23 @@ def test_noalloc_decode_rejects_bad_arguments():
     assert st == binding.SI_ERR_INVALID_ARG
     st = binding.si_moe_forward_decode_noalloc(plan, dl.struct(), x, 1, out[:, 1:], raw_status=True)
     assert st == binding.SI_ERR_MISALIGNED
+    st = binding.si_moe_forward_decode_noalloc(plan, dl.struct(), x[:, 1:], 1, out, raw_status=True)
+    assert st == binding.SI_ERR_MISALIGNED
+    assert binding.si_moe_read_status_noalloc() == binding.SI_OK
+
+
+def test_noalloc_decode_rejects_a_shape_beyond_the_fixed_array():
+    """A layer whose decode scratch exceeds SI_STATIC_SCRATCH_BYTES (16 tokens'
+    worth of h for intermediate 4096, top-16, 4 tokens: 1 MiB of h alone) is
+    refused with SI_ERR_SCRATCH_TOO_SMALL, and nothing is written."""
+    shape = synth.MoeShape(hidden=256, intermediate=4096, n_experts=16, top_k=16)
+    plan = binding.si_moe_plan(device.desc_for(shape))
+    assert binding.si_moe_scratch_bytes(plan, binding.SI_MODE_DECODE, 4) > binding.SI_STATIC_SCRATCH_BYTES
+    dl = device.to_device(synth.make_layer(shape, seed=0))
+    x = device.tokens_to_device(synth.make_tokens(shape, seed=0, n_tokens=4))
+    out = torch.full((4, shape.hidden), float("nan"), dtype=torch.float32, device="cuda")
+    st = binding.si_moe_forward_decode_noalloc(plan, dl.struct(), x, 4, out, raw_status=True)
+    assert st == binding.SI_ERR_SCRATCH_TOO_SMALL
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all()
+    assert binding.si_moe_read_status_noalloc() == binding.SI_OK
