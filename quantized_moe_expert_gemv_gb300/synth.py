@@ -99,6 +99,10 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+WTYPE_Q4_K = 12      # GGUF's type id of Q4_K
+WTYPE_NVFP4 = 100    # NVFP4 super-blocks (layout below)
+
+
 @dataclass
 class MoeLayer:
     shape: MoeShape
@@ -109,6 +113,8 @@ class MoeLayer:
     router_bias: np.ndarray | None = None   # float32 [E] or None
     norm_weight: np.ndarray | None = None   # float32 [H] RMSNorm gain (pre-normed block) or None
     norm_eps: float = 1e-6
+    wtype: int = WTYPE_Q4_K
+    gscale: np.ndarray | None = None        # float32 [E, 3] NVFP4 tensor scales of gate, up, down
 
 
 def make_router_w(shape: MoeShape, seed: int, layer: int = 0) -> np.ndarray:
@@ -127,6 +133,39 @@ def make_layer(shape: MoeShape, seed: int, layer: int = 0,
     rw = make_router_w(shape, seed, layer)
     bias = None if router_bias is None else np.asarray(router_bias, dtype=np.float32).copy()
     return MoeLayer(shape, wg, wu, wd, rw, bias)
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 experts: 4-bit E2M1 codes, one FP8 E4M3 scale per 16 weights and one
+# fp32 scale per expert matrix, stored in super-blocks of 256 weights with the
+# same size as a Q4_K block (144 bytes): bytes 0-15 the 16 E4M3 scales of
+# weights 16j .. 16j+15, bytes 16-143 the codes (byte 16 + l holds weight 2l
+# in its low nibble and weight 2l+1 in its high nibble).  Synthetic recipe:
+# codes uniform random nibbles; block scales E4M3 with exponent field 7..9
+# and a random mantissa (values in [1, 8)); tensor scales 2^-6 * U[0.5, 1.5]
+# rounded to fp32, so weights have magnitudes like the Q4_K recipe's.
+# ---------------------------------------------------------------------------
+def nvfp4_random_blocks(g: np.random.Generator, n_blocks: int) -> np.ndarray:
+    """n_blocks random NVFP4 super-blocks, uint8 [n_blocks, 144]."""
+    raw = np.frombuffer(g.bytes(n_blocks * Q4K_BLOCK_BYTES), dtype=np.uint8)
+    raw = raw.reshape(n_blocks, Q4K_BLOCK_BYTES).copy()
+    exp = g.integers(7, 10, size=(n_blocks, 16), dtype=np.uint8)
+    man = g.integers(0, 8, size=(n_blocks, 16), dtype=np.uint8)
+    raw[:, 0:16] = (exp << 3) | man
+    return raw
+
+
+def make_layer_nvfp4(shape: MoeShape, seed: int, layer: int = 0,
+                     router_bias: np.ndarray | None = None) -> MoeLayer:
+    E, H, I = shape.n_experts, shape.hidden, shape.intermediate
+    nbh, nbi = shape.blocks_per_gate_row, shape.blocks_per_down_row
+    wg = nvfp4_random_blocks(rng(seed, layer, "nvfp4-gate"), E * I * nbh).reshape(E, I, nbh, Q4K_BLOCK_BYTES)
+    wu = nvfp4_random_blocks(rng(seed, layer, "nvfp4-up"), E * I * nbh).reshape(E, I, nbh, Q4K_BLOCK_BYTES)
+    wd = nvfp4_random_blocks(rng(seed, layer, "nvfp4-down"), E * H * nbi).reshape(E, H, nbi, Q4K_BLOCK_BYTES)
+    gsc = (rng(seed, layer, "nvfp4-tensor-scale").uniform(0.5, 1.5, size=(E, 3)) / 64.0).astype(np.float32)
+    rw = make_router_w(shape, seed, layer)
+    bias = None if router_bias is None else np.asarray(router_bias, dtype=np.float32).copy()
+    return MoeLayer(shape, wg, wu, wd, rw, bias, wtype=WTYPE_NVFP4, gscale=gsc)
 
 
 def make_norm_weight(shape: MoeShape, seed: int, layer: int = 0) -> np.ndarray:

@@ -453,3 +453,125 @@ def test_stored_dedup_beta_gives_sixty_percent_hot_mass(oracle_lib):
     hot = np.isin(ids, synth.dedup_hot_set(seed))
     share = float((w * hot).sum() / w.sum())
     assert abs(share - 0.60) <= 0.005, share
+
+
+# ------------------------------------------------------------------------ NVFP4
+# The E2M1 element values as the format's value table lists them (codes 0-7,
+# then the same magnitudes negated for codes 8-15).
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def _nvfp4_block(scales16, codes256) -> np.ndarray:
+    """Pack 16 E4M3 scale bytes and 256 4-bit codes into this library's NVFP4 super-block."""
+    codes = np.asarray(codes256, dtype=np.uint8)
+    blk = np.zeros(144, dtype=np.uint8)
+    blk[0:16] = np.asarray(scales16, dtype=np.uint8)
+    blk[16:] = codes[0::2] | (codes[1::2] << 4)
+    return blk
+
+
+def test_e2m1_values_match_the_format_table(oracle_lib):
+    got = [oracle.e2m1_to_double(c) for c in range(16)]
+    assert got == E2M1_TABLE
+    assert [np.signbit(v) for v in got] == [c >= 8 for c in range(16)]
+
+
+def test_e4m3_matches_torch_for_every_byte(oracle_lib):
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    b = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = b.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(i) for i in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.array_equal(np.signbit(got[fin]), np.signbit(ref[fin]))
+    assert oracle.e4m3_to_double(0x7E) == 448.0 and oracle.e4m3_to_double(0x01) == 2.0 ** -9
+
+
+def test_nvfp4_element_order_scale_blocks_and_tensor_scale(oracle_lib):
+    """Weight i of a super-block is code i (low nibble of byte 16 + i/2 for even
+    i) times the E4M3 scale of block i/16 times the tensor scale."""
+    codes = np.arange(256) % 16
+    scales = [0x38 + 8 * (j % 4) for j in range(16)]      # 1, 2, 4, 8, 1, 2, ...
+    blk = _nvfp4_block(scales, codes)
+    for g in (1.0, 0.5, 3.0):
+        w = oracle.nvfp4_dequant(blk, g)
+        want = np.array([E2M1_TABLE[codes[i]] * (2.0 ** ((i // 16) % 4)) * g for i in range(256)], dtype=np.float32)
+        assert np.array_equal(w, want)
+    # a single nonzero scale: only its 16 weights survive
+    for j in (0, 7, 15):
+        sc = [0] * 16
+        sc[j] = 0x40  # 2.0
+        w = oracle.nvfp4_dequant(_nvfp4_block(sc, np.full(256, 7)), 1.0)  # every code 6.0
+        assert np.array_equal(np.nonzero(w)[0], np.arange(16 * j, 16 * j + 16))
+        assert np.all(w[16 * j: 16 * j + 16] == 12.0)
+
+
+def test_nvfp4_dequant_is_the_exactly_rounded_value(oracle_lib):
+    """Random super-blocks and tensor scales: each weight equals the exact
+    rational e2m1 * e4m3 * g rounded once to fp32."""
+    g = synth.rng(31)
+    blocks = synth.nvfp4_random_blocks(g, 12)
+    blocks[0, 0:16] = [0x01, 0x07, 0x08, 0x7E, 0xFE, 0x30, 0x00, 0x81, 0x39, 0x3A, 0x3B, 0x3C, 0x3D, 0x3E, 0x3F, 0x40]
+    for gs in (np.float32(1.0 / 3.0), np.float32(0.0123), np.float32(7.77)):
+        w = oracle.nvfp4_dequant(blocks, float(gs)).reshape(12, 256)
+        for b in range(12):
+            for i in range(0, 256, 3):
+                code = (blocks[b, 16 + i // 2] >> (4 * (i % 2))) & 15
+                sb = int(blocks[b, i // 16])
+                sign = -1 if sb & 0x80 else 1
+                E, M = (sb >> 3) & 15, sb & 7
+                scale = Fraction(M, 8) * Fraction(1, 64) if E == 0 else (1 + Fraction(M, 8)) * Fraction(2) ** (E - 7)
+                exact = Fraction(E2M1_TABLE[code]) * sign * scale * Fraction(float(gs))
+                assert w[b, i] == np.float32(float(exact)), (b, i)
+
+
+def _dequant_any(layer, name, e):
+    arr = getattr(layer, name)[e]
+    if layer.wtype == synth.WTYPE_NVFP4:
+        k = {"w_gate": 0, "w_up": 1, "w_down": 2}[name]
+        return oracle.nvfp4_dequant(arr, float(layer.gscale[e, k]))
+    return oracle.q4k_dequant(arr)
+
+
+@pytest.mark.parametrize("shape", [synth.MoeShape(256, 256, 4, 2), synth.MoeShape(512, 256, 5, 3)])
+def test_nvfp4_moe_token_matches_dense_brute_force(oracle_lib, shape):
+    layer = synth.make_layer_nvfp4(shape, seed=33)
+    H, I, E, k = shape.hidden, shape.intermediate, shape.n_experts, shape.top_k
+    xs = synth.make_tokens(shape, seed=33, n_tokens=3)
+    for t in range(3):
+        res = oracle.moe_token(layer, xs[t])
+        x = synth.bf16_to_f32(xs[t]).astype(np.float64)
+        z = layer.router_w.astype(np.float64) @ x
+        sel = np.argsort(-z.astype(np.float32), kind="stable")[:k]
+        p = scipy.special.softmax(z)
+        wsel = p[sel] / p[sel].sum()
+        out = np.zeros(H)
+        for e in range(E):  # every expert, masked afterwards
+            Wg = _dequant_any(layer, "w_gate", e).reshape(I, H).astype(np.float64)
+            Wu = _dequant_any(layer, "w_up", e).reshape(I, H).astype(np.float64)
+            Wd = _dequant_any(layer, "w_down", e).reshape(H, I).astype(np.float64)
+            gg = Wg @ x
+            y = Wd @ (gg * scipy.special.expit(gg) * (Wu @ x))
+            if e in sel:
+                out += wsel[list(sel).index(e)] * y
+        assert np.array_equal(res.ids, sel)
+        np.testing.assert_allclose(res.out64, out, rtol=1e-10, atol=1e-12 * np.abs(out).max())
+
+
+def test_nvfp4_identical_experts_reduce_to_one_expert(oracle_lib):
+    shape = synth.MoeShape(256, 256, 6, 3)
+    layer = synth.make_layer_nvfp4(shape, seed=34)
+    for name in ("w_gate", "w_up", "w_down"):
+        arr = getattr(layer, name)
+        arr[:] = arr[0]
+    layer.gscale[:] = layer.gscale[0]
+    xs = synth.make_tokens(shape, seed=34, n_tokens=3)
+    for t in range(3):
+        res = oracle.moe_token(layer, xs[t])
+        x = synth.bf16_to_f32(xs[t]).astype(np.float64)
+        _, y = oracle.expert_ffn(layer.w_gate[0], layer.w_up[0], layer.w_down[0], x, 256, 256,
+                                 wtype=oracle.WTYPE_NVFP4, gscales=layer.gscale[0])
+        np.testing.assert_allclose(res.out64, y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
