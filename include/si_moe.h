@@ -72,6 +72,7 @@ typedef enum si_status {
 } si_status;
 
 #define SI_WTYPE_Q4_K 12          /* GGUF's type id of Q4_K */
+#define SI_WTYPE_NVFP4 100        /* NVFP4 super-blocks (see si_moe_layer.w_scale) */
 #define SI_MODE_DECODE 0
 #define SI_MODE_PREFILL 1
 #define SI_MAX_EXPERTS 256
@@ -81,7 +82,7 @@ typedef enum si_status {
 /* Layer shape.  hidden and intermediate are multiples of 256 (one Q4_K
  * super-block); 1 <= top_k <= min(n_experts, SI_MAX_TOPK);
  * n_experts <= SI_MAX_EXPERTS; max_tokens bounds the prefill token count.
- * wtype must be SI_WTYPE_Q4_K; flags must be 0. */
+ * wtype is SI_WTYPE_Q4_K or SI_WTYPE_NVFP4; flags must be 0. */
 typedef struct si_moe_desc {
     int32_t hidden;
     int32_t intermediate;
@@ -127,6 +128,19 @@ typedef struct si_moe_layer {
      * write out; no extra launch.  NULL: out = MoE(x). */
     const float *norm_weight;  /* fp32 [H] gain, 16-byte aligned, or NULL */
     float norm_eps;            /* >= 0 and finite (used only with norm_weight) */
+    /* NVFP4 experts (wtype SI_WTYPE_NVFP4; sparkinfer README, "Milestone 2":
+     * NVFP4 experts; SP-RKINFER README, "Native NVFP4 - two supported
+     * checkpoints"; the CuTe-DSL README's moe row: a W4A16 mode with bf16
+     * activations and inline FP4 weight dequant).  w_gate, w_up and w_down
+     * then hold super-blocks of 256 weights in 144 bytes (the size of a Q4_K
+     * block, so the same row layout): bytes 0-15 the FP8 E4M3 scales of
+     * weights 16j .. 16j+15, bytes 16-143 the 4-bit E2M1 codes (byte 16 + l:
+     * weight 2l in its low nibble, 2l+1 in its high nibble); a weight is
+     * e2m1 * e4m3 * g with g the matrix's fp32 tensor scale, given here as
+     * [E][3] (gate, up, down of each expert), 4-byte aligned.  NULL for Q4_K
+     * (and required for NVFP4).  A checkpoint's separate code and scale
+     * tensors are repacked into this layout once, losslessly. */
+    const float *w_scale;
 } si_moe_layer;
 
 /* Optional routing outputs (device pointers; each may be NULL). */
@@ -245,6 +259,15 @@ si_status si_debug_topk(const float *logits, int32_t n, const si_moe_desc *desc,
  * blocks, out_f16 16-byte aligned.  Stream-ordered. */
 si_status si_debug_q4k_dequant_f16(const void *blocks, int64_t n_blocks, const float *gamma, uint16_t *out_f16,
                                    si_stream_t stream);
+
+/* Test export: the grouped prefill's NVFP4 -> fp16 operand conversion (the
+ * device function its GEMM dequantization warps run for SI_WTYPE_NVFP4)
+ * applied to n_blocks NVFP4 super-blocks with tensor scale g.
+ * out_f16[256*b + c] (fp16 bits) = round-to-nearest-even fp16 of the fp32
+ * weight e2m1 * e4m3 * g (one rounding) of column c of block b.  blocks,
+ * out_f16 16-byte aligned.  Stream-ordered. */
+si_status si_debug_nvfp4_dequant_f16(const void *blocks, int64_t n_blocks, float g, uint16_t *out_f16,
+                                     si_stream_t stream);
 
 /* Timing export: si_moe_forward_decode that also records caller-created
  * cudaEvent_t handles on `stream` -- events[0] before the router kernel,

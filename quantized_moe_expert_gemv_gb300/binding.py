@@ -28,6 +28,7 @@ SI_ERR_TIMEOUT = 6
 SI_ERR_DEVICE = 7
 SI_ERR_RANGE = 8
 SI_WTYPE_Q4_K = 12
+SI_WTYPE_NVFP4 = 100
 SI_MODE_DECODE = 0
 SI_MODE_PREFILL = 1
 SI_MAX_EXPERTS = 256
@@ -52,7 +53,7 @@ class si_moe_desc(ctypes.Structure):
 class si_moe_layer(ctypes.Structure):
     _fields_ = [("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
                 ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
-                ("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float)]
+                ("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float), ("w_scale", ctypes.c_void_p)]
 
 
 class si_moe_route_out(ctypes.Structure):
@@ -115,6 +116,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.si_debug_q4k_dequant.argtypes = [vp, i64, vp, vp, vp]
     lib.si_debug_q4k_dequant_f16.restype = ctypes.c_int
     lib.si_debug_q4k_dequant_f16.argtypes = [vp, i64, vp, vp, vp]
+    lib.si_debug_nvfp4_dequant_f16.restype = ctypes.c_int
+    lib.si_debug_nvfp4_dequant_f16.argtypes = [vp, i64, ctypes.c_float, vp, vp]
     lib.si_moe_read_status_noalloc.restype = ctypes.c_int
     lib.si_moe_read_status_noalloc.argtypes = [vp]
     lib.si_debug_topk.restype = ctypes.c_int
@@ -207,9 +210,9 @@ def si_moe_scratch_init(plan: Plan, scratch, stream=None):
 
 
 def layer_struct(w_gate, w_up, w_down, router_w, router_bias=None, norm_weight=None,
-                 norm_eps: float = 0.0) -> si_moe_layer:
+                 norm_eps: float = 0.0, w_scale=None) -> si_moe_layer:
     return si_moe_layer(_ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(router_w), _ptr(router_bias),
-                        _ptr(norm_weight), float(norm_eps))
+                        _ptr(norm_weight), float(norm_eps), _ptr(w_scale))
 
 
 def route_struct(topk_ids=None, topk_w=None, expert_counts=None, expert_offsets=None, perm=None,
@@ -303,6 +306,11 @@ def si_debug_q4k_dequant(blocks, n_blocks, out_f32=None, out_bf16=None, stream=N
 def si_debug_q4k_dequant_f16(blocks, n_blocks, out_f16, gamma=None, stream=None):
     _check(load_library().si_debug_q4k_dequant_f16(_ptr(blocks), int(n_blocks), _ptr(gamma), _ptr(out_f16),
                                                    _stream(stream)), "si_debug_q4k_dequant_f16")
+
+
+def si_debug_nvfp4_dequant_f16(blocks, n_blocks, g, out_f16, stream=None):
+    _check(load_library().si_debug_nvfp4_dequant_f16(_ptr(blocks), int(n_blocks), float(g), _ptr(out_f16),
+                                                     _stream(stream)), "si_debug_nvfp4_dequant_f16")
 
 
 def si_moe_read_status_noalloc(stream=None) -> int:

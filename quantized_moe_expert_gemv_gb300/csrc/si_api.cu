@@ -23,7 +23,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 si_status validate_desc(const si_moe_desc *d) {
     if (!d) return SI_ERR_INVALID_ARG;
-    if (d->wtype != SI_WTYPE_Q4_K || d->flags != 0) return SI_ERR_UNSUPPORTED;
+    if ((d->wtype != SI_WTYPE_Q4_K && d->wtype != SI_WTYPE_NVFP4) || d->flags != 0) return SI_ERR_UNSUPPORTED;
     if (d->hidden <= 0 || d->intermediate <= 0 || d->hidden % 256 || d->intermediate % 256)
         return SI_ERR_INVALID_ARG;
     if (d->n_experts < 1 || d->n_experts > SI_MAX_EXPERTS) return SI_ERR_INVALID_ARG;
@@ -146,7 +146,7 @@ si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *o
     for (int n = 1; n <= SI_MAX_DECODE_TOKENS; ++n) {
         si::DecodeArgs tmp{};
         p.fused_ok[n] = false;
-        if (si::expert_fused_layout(*desc, n, p.sm_count, p.smem_optin, tmp)) {
+        if (desc->wtype == SI_WTYPE_Q4_K && si::expert_fused_layout(*desc, n, p.sm_count, p.smem_optin, tmp)) {
             int per_sm = 0;
             if (si::expert_fused_occupancy(desc->hidden / 256, n > 1, tmp.fz_smem, p.smem_optin, &per_sm) == cudaSuccess &&
                 per_sm >= 1)
@@ -218,6 +218,19 @@ si_status si_moe_scratch_init(si_moe_plan_t plan, void *scratch, size_t scratch_
 
 }  // extern "C"
 
+// NVFP4 layers carry their tensor scales (and, in this build, no pre-norm);
+// Q4_K layers carry none.
+static si_status check_weight_scales(const si_moe_desc &d, const si_moe_layer *layer) {
+    if (d.wtype == SI_WTYPE_NVFP4) {
+        if (!layer->w_scale) return SI_ERR_INVALID_ARG;
+        if (!aligned(layer->w_scale, 4)) return SI_ERR_MISALIGNED;
+        if (layer->norm_weight) return SI_ERR_UNSUPPORTED;
+    } else if (layer->w_scale) {
+        return SI_ERR_INVALID_ARG;
+    }
+    return SI_OK;
+}
+
 // Every argument check of a decode call except those of the scratch buffer.
 si_status si::check_decode_args(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
                                 int32_t n_tokens, const float *out, const si_moe_route_out *ro) {
@@ -234,6 +247,8 @@ si_status si::check_decode_args(si_moe_plan_t plan, const si_moe_layer *layer, c
                (ro->expert_counts && !aligned(ro->expert_counts, 4)) ||
                (ro->logits && !aligned(ro->logits, 4))))
         return SI_ERR_MISALIGNED;
+    const si_status wst = check_weight_scales(plan->p.desc, layer);
+    if (wst != SI_OK) return wst;
     return SI_OK;
 }
 
@@ -259,6 +274,8 @@ static si_status forward_decode_impl(si_moe_plan_t plan, const si_moe_layer *lay
     a.router_bias = layer->router_bias;
     a.norm_w = layer->norm_weight;
     a.norm_eps = layer->norm_weight ? layer->norm_eps : 0.f;
+    a.wtype = d.wtype;
+    a.wscale = layer->w_scale;
     a.x = static_cast<const uint16_t *>(x_bf16);
     a.out = out;
     a.H = d.hidden;
@@ -318,6 +335,8 @@ static si_status forward_prefill_impl(si_moe_plan_t plan, const si_moe_layer *la
                (ro->expert_offsets && !aligned(ro->expert_offsets, 4)) || (ro->perm && !aligned(ro->perm, 4)) ||
                (ro->logits && !aligned(ro->logits, 4))))
         return SI_ERR_MISALIGNED;
+    const si_status wst = check_weight_scales(d, layer);
+    if (wst != SI_OK) return wst;
     if (!plan->p.prefill_ok) return SI_ERR_UNSUPPORTED;
     const si::PrefillLayout L = si::prefill_layout(d, n_tokens);
     if (scratch_bytes < L.total) return SI_ERR_SCRATCH_TOO_SMALL;
@@ -330,6 +349,8 @@ static si_status forward_prefill_impl(si_moe_plan_t plan, const si_moe_layer *la
     a.router_bias = layer->router_bias;
     a.norm_w = layer->norm_weight;
     a.norm_eps = layer->norm_weight ? layer->norm_eps : 0.f;
+    a.wtype = d.wtype;
+    a.wscale = layer->w_scale;
     a.x = static_cast<const uint16_t *>(x_bf16);
     a.out = out;
     a.H = d.hidden;
@@ -438,6 +459,18 @@ si_status si_debug_q4k_dequant_f16(const void *blocks, int64_t n_blocks, const f
     if (!aligned(blocks, 16) || !aligned(out_f16, 16) || (gamma && !aligned(gamma, 16))) return SI_ERR_MISALIGNED;
     if (si::launch_debug_dequant_f16(static_cast<const uint8_t *>(blocks), n_blocks, gamma, out_f16,
                                      (cudaStream_t)stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SI_ERR_CUDA;
+    }
+    return SI_OK;
+}
+
+si_status si_debug_nvfp4_dequant_f16(const void *blocks, int64_t n_blocks, float g, uint16_t *out_f16,
+                                     si_stream_t stream) {
+    if (!blocks || n_blocks < 0 || !out_f16) return SI_ERR_INVALID_ARG;
+    if (!aligned(blocks, 16) || !aligned(out_f16, 16)) return SI_ERR_MISALIGNED;
+    if (si::launch_debug_nvfp4_f16(static_cast<const uint8_t *>(blocks), n_blocks, g, out_f16, (cudaStream_t)stream) !=
+        cudaSuccess) {
         cudaGetLastError();
         return SI_ERR_CUDA;
     }

@@ -324,6 +324,7 @@ __device__ __forceinline__ void gateup_rowpair(const DecodeArgs &a, const float 
                     qg1 = ldg_nc_v4(bg + 32 + 32 * i);
         const uint4 hu = ldg_nc_v4(bu), qu0 = ldg_nc_v4(bu + 16 + 32 * i),
                     qu1 = ldg_nc_v4(bu + 32 + 32 * i);
+        const bool fp4 = a.wtype == SI_WTYPE_NVFP4;
         const SubScales sg = chunk_scales(hg, i), su = chunk_scales(hu, i);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -334,14 +335,21 @@ __device__ __forceinline__ void gateup_rowpair(const DecodeArgs &a, const float 
             auto xb2 = [pb](int p) { return pb[p]; };
             const float Xa = Xs[tok[t] * (a.H / 32) + 8 * b + 2 * i];
             const float Xb = Xs[tok[t] * (a.H / 32) + 8 * b + 2 * i + 1];
-            g[t] += chunk_contrib(sg, chunk_code_sums(qg0, qg1, xa2, xb2), Xa, Xb);
-            uu[t] += chunk_contrib(su, chunk_code_sums(qu0, qu1, xa2, xb2), Xa, Xb);
+            if (fp4) {  // NVFP4: the tensor scales are applied to the row sums below
+                g[t] += chunk_contrib_nvfp4_f32(hg, i, qg0, qg1, xa2, xb2);
+                uu[t] += chunk_contrib_nvfp4_f32(hu, i, qu0, qu1, xa2, xb2);
+            } else {
+                g[t] += chunk_contrib(sg, chunk_code_sums(qg0, qg1, xa2, xb2), Xa, Xb);
+                uu[t] += chunk_contrib(su, chunk_code_sums(qu0, qu1, xa2, xb2), Xa, Xb);
+            }
         }
     }
 #pragma unroll
+    const float tsg = a.wtype == SI_WTYPE_NVFP4 ? a.wscale[3 * e] : 1.f;
+    const float tsu = a.wtype == SI_WTYPE_NVFP4 ? a.wscale[3 * e + 1] : 1.f;
     for (int t = 0; t < NT; ++t) {
-        const float gs = warp_sum(g[t]);
-        const float us = warp_sum(uu[t]);
+        const float gs = tsg * warp_sum(g[t]);
+        const float us = tsu * warp_sum(uu[t]);
         if (lane == 0) a.h[((size_t)tok[t] * a.k + slot[t]) * a.I + r] = silu(gs) * us;
     }
 }
@@ -429,6 +437,7 @@ __global__ void __launch_bounds__(kThreads) k_down_generic(DecodeArgs a) {
             const uint4 hd = ldg_nc_v4(blk), q0 = ldg_nc_v4(blk + 16 + 32 * i),
                         q1 = ldg_nc_v4(blk + 32 + 32 * i);
             const SubScales sc = chunk_scales(hd, i);
+            const bool fp4 = a.wtype == SI_WTYPE_NVFP4;
 #pragma unroll
             for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
                 if (t < nt) {
@@ -439,14 +448,15 @@ __global__ void __launch_bounds__(kThreads) k_down_generic(DecodeArgs a) {
                     auto xb2 = [pb](int p) { return __ldg(pb + p); };
                     const float Xa = Hs[sl[t] * nIs + 8 * b + 2 * i];
                     const float Xb = Hs[sl[t] * nIs + 8 * b + 2 * i + 1];
-                    y[t] += chunk_contrib(sc, chunk_code_sums(q0, q1, xa2, xb2), Xa, Xb);
+                    y[t] += fp4 ? chunk_contrib_nvfp4_f32(hd, i, q0, q1, xa2, xb2)
+                                : chunk_contrib(sc, chunk_code_sums(q0, q1, xa2, xb2), Xa, Xb);
                 }
             }
         }
 #pragma unroll
         for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
             if (t < nt) {
-                const float ys = group_sum<GS>(y[t]);
+                const float ys = (a.wtype == SI_WTYPE_NVFP4 ? a.wscale[3 * e + 2] : 1.f) * group_sum<GS>(y[t]);
                 const int tk = u->tok[s][t];
                 const float w = a.wts[sl[t]];
 #pragma unroll

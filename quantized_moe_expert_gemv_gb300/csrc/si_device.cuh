@@ -543,6 +543,121 @@ __device__ __forceinline__ float chunk_contrib_i(const ChunkScalesI &c, int2 I, 
     return fmaf(c.d * xs, (float)sc, -c.dmin * mm);
 }
 
+// =====================================================================
+// NVFP4 super-blocks (144 bytes per 256 weights): bytes 0-15 the FP8 E4M3
+// scales of weights 16j .. 16j+15, bytes 16-143 the E2M1 codes (byte 16 + l:
+// weight 2l in its low nibble, 2l+1 in its high nibble); weight = e2m1 *
+// e4m3 * g, g the matrix's fp32 tensor scale.  E2M1 code c: bit 3 sign,
+// bits 2-1 exponent (bias 1), bit 0 mantissa: magnitudes 0, 0.5, 1, 1.5, 2,
+// 3, 4, 6.  (sparkinfer README, "Milestone 2": NVFP4 experts; the CuTe-DSL
+// README's moe row: W4A16, bf16 activations with inline FP4 weight dequant.)
+// The GEMV takes each code through the integer T(c) = 12 + 2*e2m1(c) in
+// [0, 24] and the same int16 activations as the Q4_K path:
+//   sum_l e2m1_l x_l ~= s/2 * (sum_l T_l xq_l - 12 * sum_l xq_l)
+// per 16-weight block, exact in int32; the block's E4M3 scale, the
+// activation scale s and the tensor scale multiply the block sums.
+// =====================================================================
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// T of the four codes in the low 16 bits of `codes` (code k -> byte k).  A
+// byte permute selects from an 8-entry table by the low three bits of each
+// code; with the code's bit 3 set it returns the sign of the selected byte
+// instead (0: every entry is below 128).  So one permute gives T for the
+// positive codes and 0 for the negative ones, the other (bit 3 flipped) the
+// reverse, and the two are or-ed.
+__device__ __forceinline__ uint32_t e2m1_t4(uint32_t codes) {
+    // positive codes m = 0..7: 12 + 2*{0, .5, 1, 1.5, 2, 3, 4, 6}; negative: 12 - 2*...
+    return prmt(0x0F0E0D0Cu, 0x18141210u, codes) | prmt(0x090A0B0Cu, 0x00040608u, codes ^ 0x8888u);
+}
+
+// FP8 E4M3 byte (bit 7 sign, bits 6-3 exponent E with bias 7, bits 2-0
+// mantissa M) -> fp32, exactly: E > 0: 2^(E-7) * (1 + M/8); E == 0: M * 2^-9.
+// (S.1111.111 is NaN in E4M3; block scales never hold it.)
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    const uint32_t E = (b >> 3) & 15u, M = b & 7u;
+    const float v = E ? __uint_as_float(((E + 120u) << 23) | (M << 20)) : (float)M * 0.001953125f;
+    return __uint_as_float(__float_as_uint(v) | ((b & 0x80u) << 24));
+}
+
+// Integer sums of the int16 activations of one 64-column chunk (32 words)
+// over its four 16-column blocks.
+__device__ __forceinline__ void xq_block_sums(const uint32_t (&w)[32], int (&XQ)[4]) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        int s = 0;
+#pragma unroll
+        for (int p = 8 * b; p < 8 * b + 8; ++p) s += (int)(int16_t)(w[p] & 0xffffu) + ((int)w[p] >> 16);
+        XQ[b] = s;
+    }
+}
+
+// Contribution of chunk i (64 weights: scale blocks 4i .. 4i+3, codes q0, q1)
+// of an NVFP4 super-block with header hdr (its 16 scale bytes) to a row dot
+// product with int16 activations xw(p) of scale xs and block sums XQ, before
+// the tensor scale.
+template <typename XW>
+__device__ __forceinline__ float chunk_contrib_nvfp4(const uint4 &hdr, int i, const uint4 &q0, const uint4 &q1, XW xw,
+                                                     float xs, const int (&XQ)[4]) {
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    int blk[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        int a0 = 0, a1 = 0;
+#pragma unroll
+        for (int t = 2 * b; t < 2 * b + 2; ++t) {
+            const uint32_t lo = e2m1_t4(w[t]), hi = e2m1_t4(w[t] >> 16);  // weights 8t..8t+3, 8t+4..8t+7
+            a0 = dp2a_lo(xw(4 * t), lo, a0);
+            a1 = dp2a_hi(xw(4 * t + 1), lo, a1);
+            a0 = dp2a_lo(xw(4 * t + 2), hi, a0);
+            a1 = dp2a_hi(xw(4 * t + 3), hi, a1);
+        }
+        blk[b] = a0 + a1 - 12 * XQ[b];
+    }
+    // the four scale bytes of this chunk are 32-bit word i of the header (i varies across lanes)
+    const uint32_t sw = i == 0 ? hdr.x : (i == 1 ? hdr.y : (i == 2 ? hdr.z : hdr.w));
+    float r = e4m3_to_f32(sw & 0xffu) * (float)blk[0];
+    r = fmaf(e4m3_to_f32((sw >> 8) & 0xffu), (float)blk[1], r);
+    r = fmaf(e4m3_to_f32((sw >> 16) & 0xffu), (float)blk[2], r);
+    r = fmaf(e4m3_to_f32(sw >> 24), (float)blk[3], r);
+    return 0.5f * xs * r;
+}
+
+// The same chunk with fp32 activations: xa2(p) = {x[2p], x[2p+1]} for the
+// chunk's weights 0..31 and xb2(p) for 32..63 (p = 0..15); before the tensor
+// scale.  (The generic kernels keep the activations in fp32.)
+template <typename XA, typename XB>
+__device__ __forceinline__ float chunk_contrib_nvfp4_f32(const uint4 &hdr, int i, const uint4 &q0, const uint4 &q1,
+                                                         XA xa2, XB xb2) {
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t sw = i == 0 ? hdr.x : (i == 1 ? hdr.y : (i == 2 ? hdr.z : hdr.w));
+    float r = 0.f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        float acc = 0.f;
+#pragma unroll
+        for (int t = 2 * b; t < 2 * b + 2; ++t) {
+            const uint32_t v[2] = {e2m1_t4(w[t]), e2m1_t4(w[t] >> 16)};  // weights 8t..8t+3, 8t+4..8t+7
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+                for (int pr = 0; pr < 2; ++pr) {
+                    const int p = 4 * t + 2 * hh + pr;  // activation pair of weights 2p, 2p+1 of the chunk
+                    const f32x2 xp = p < 16 ? xa2(p) : xb2(p - 16);
+                    const float2 x2 = unpack2(xp);
+                    acc = fmaf((float)((int)((v[hh] >> (16 * pr)) & 0xffu) - 12), x2.x, acc);
+                    acc = fmaf((float)((int)((v[hh] >> (16 * pr + 8)) & 0xffu) - 12), x2.y, acc);
+                }
+            }
+        }
+        r = fmaf(e4m3_to_f32((sw >> (8 * b)) & 0xffu), acc, r);
+    }
+    return 0.5f * r;
+}
+
 // Top-k of n rows of logits z[t][0..E) by ranks, using all threads of a CTA:
 // the rank of z[t][e] is the number of logits that beat it (greater, or equal
 // with a lower index); the experts of rank < k are the selection, stored at

@@ -80,7 +80,11 @@ __device__ __forceinline__ float pair_sum(float g, float u, int li) {
 }
 }  // namespace
 
-template <int NBH, bool NORM>
+// NVFP4 (WF = 1) instead of Q4_K (WF = 0) weights: the same data movement
+// (144-byte super-blocks), a different chunk dot product (si_device.cuh), the
+// activations' 16-column integer sums next to their scale, and the matrices'
+// tensor scales on the gate and up partials and on the combine weight.
+template <int NBH, bool NORM, int WF>
 __global__ void __launch_bounds__(kClThreads, 1)
     k_expert_cluster(const __grid_constant__ CUtensorMap tmap_down, const __grid_constant__ CUtensorMap tmap_tail,
                      DecodeArgs a) {
@@ -107,6 +111,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const long long budget = (long long)pin_u64((uint64_t)a.wait_budget);
     const int fault_wait = pin_i32(a.fault_wait);
     const int I = pin_i32(a.I), H = pin_i32(a.H);
+    const float *const wsc = WF ? pin_ptr(a.wscale) : nullptr;  // NVFP4 tensor scales [E][3]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = (int)cluster_nctarank();
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     }
     if (xq_lane) {
         uint32_t *xq = xq_s;                                   // [H/64][32] words, 16-byte units swizzled
-        float *xqf = reinterpret_cast<float *>(xq + H / 2);   // [H/64][3]: scale, Xa, Xb
+        float *xqf = reinterpret_cast<float *>(xq + H / 2);   // [H/64][7]: scale, Xa, Xb, 4 x 16-column int sums
         float xf[64];
         uint32_t wq[32];
         float sa, sb;
@@ -209,9 +214,15 @@ __global__ void __launch_bounds__(kClThreads, 1)
         for (int q = 0; q < 8; ++q)
             reinterpret_cast<uint4 *>(xq + 32 * lane)[q ^ (lane & 7)] =
                 make_uint4(wq[4 * q], wq[4 * q + 1], wq[4 * q + 2], wq[4 * q + 3]);
-        xqf[3 * lane] = sc;
-        xqf[3 * lane + 1] = sa;
-        xqf[3 * lane + 2] = sb;
+        xqf[7 * lane] = sc;
+        xqf[7 * lane + 1] = sa;
+        xqf[7 * lane + 2] = sb;
+        if (WF) {
+            int XQ[4];
+            xq_block_sums(wq, XQ);
+#pragma unroll
+            for (int b4 = 0; b4 < 4; ++b4) reinterpret_cast<int *>(xqf)[7 * lane + 3 + b4] = XQ[b4];
+        }
     }
     // the gate/up stages are written by the copy engine later: order the staging's
     // shared-memory accesses before those asynchronous writes
@@ -233,7 +244,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
         const float w = ex / den;
-        if (lane == slot) s_w = w;
+        if (lane == slot) s_w = WF ? w * wsc[3 * ids[slot] + 2] : w;  // NVFP4: times the down tensor scale
         if (blockIdx.x == 0 && o_w && lane < k) o_w[lane] = w;
     }
     volatile int *verr = &s_err;
@@ -293,8 +304,18 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const uint4 v = reinterpret_cast<const uint4 *>(xq + 32 * chunk)[q ^ (chunk & 7)];
             xw[4 * q] = v.x, xw[4 * q + 1] = v.y, xw[4 * q + 2] = v.z, xw[4 * q + 3] = v.w;
         }
-        const float xs = xqf[3 * chunk], Xa = xqf[3 * chunk + 1], Xb = xqf[3 * chunk + 2];
+        const float xs = xqf[7 * chunk], Xa = xqf[7 * chunk + 1], Xb = xqf[7 * chunk + 2];
+        int XQ[4];
+#pragma unroll
+        for (int b4 = 0; b4 < 4; ++b4) XQ[b4] = WF ? reinterpret_cast<const int *>(xqf)[7 * chunk + 3 + b4] : 0;
         auto xwf = [&xw](int p) { return xw[p]; };
+        // NVFP4: this unit's expert's gate and up tensor scales
+        float tsg = 1.f, tsu = 1.f;
+        if (WF) {
+            const int eu = ids[slot];
+            tsg = wsc[3 * eu];
+            tsu = wsc[3 * eu + 1];
+        }
         if (fault_wait) {
             const bool got = wait_flag_bounded(ctrl + kCtrlFaultFlag, budget);
             if (!__all_sync(0xffffffffu, got)) {
@@ -321,8 +342,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
                     const uint8_t *urow = grow + CH * rowg;
                     const uint4 hg = ld_s128(grow), qg0 = ld_s128(grow + 16 + 32 * i), qg1 = ld_s128(grow + 32 + 32 * i);
                     const uint4 hu = ld_s128(urow), qu0 = ld_s128(urow + 16 + 32 * i), qu1 = ld_s128(urow + 32 + 32 * i);
-                    part[2 * m] = chunk_contrib_i(chunk_scales_i(hg, i), chunk_isums(qg0, qg1, xwf), xs, Xa, Xb);
-                    part[2 * m + 1] = chunk_contrib_i(chunk_scales_i(hu, i), chunk_isums(qu0, qu1, xwf), xs, Xa, Xb);
+                    if (WF) {
+                        part[2 * m] = tsg * chunk_contrib_nvfp4(hg, i, qg0, qg1, xwf, xs, XQ);
+                        part[2 * m + 1] = tsu * chunk_contrib_nvfp4(hu, i, qu0, qu1, xwf, xs, XQ);
+                    } else {
+                        part[2 * m] = chunk_contrib_i(chunk_scales_i(hg, i), chunk_isums(qg0, qg1, xwf), xs, Xa, Xb);
+                        part[2 * m + 1] = chunk_contrib_i(chunk_scales_i(hu, i), chunk_isums(qu0, qu1, xwf), xs, Xa, Xb);
+                    }
                 }
             }
             // totals: g0 at group lane 0, u0 at GS/4, g1 at GS/2, u1 at 3GS/4
@@ -348,7 +374,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
 
     // --------------------------------------------------------- down + combine
     const bool skip = __any_sync(0xffffffffu, *verr != 0);
-    uint32_t *hq = xq_s;  // reuse: [4][32] words (the same unit swizzle) + [4][3]
+    uint32_t *hq = xq_s;  // reuse: [4][32] words (the same unit swizzle) + [4][7]
     float *hqf = reinterpret_cast<float *>(hq + 128);
     if (warp < kCW && !skip) {
         if (warp < 4) {  // the unit's four 64-column chunks of h: warp c quantises chunk c
@@ -362,10 +388,18 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
             hq[32 * warp + 4 * ((lane >> 2) ^ warp) + (lane & 3)] = pack_q16(v.x, v.y, inv);
             if (lane == 0) {
-                hqf[3 * warp] = mx * (1.0f / 32767.0f);
-                hqf[3 * warp + 1] = sum;
+                hqf[7 * warp] = mx * (1.0f / 32767.0f);
+                hqf[7 * warp + 1] = sum;
             }
-            if (lane == 16) hqf[3 * warp + 2] = sum;
+            if (lane == 16) hqf[7 * warp + 2] = sum;
+            if (WF) {  // integer sums of the quantised h over 16-column blocks (8 lanes each)
+                const uint32_t wq2 = pack_q16(v.x, v.y, inv);
+                int s2 = (int)(int16_t)(wq2 & 0xffffu) + ((int)wq2 >> 16);
+                s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+                s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+                s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
+                if ((lane & 7) == 0) reinterpret_cast<int *>(hqf)[7 * warp + 3 + (lane >> 3)] = s2;
+            }
         }
     }
     if (warp < kCW) asm volatile("bar.sync 1, %0;" ::"r"(kCW * 32) : "memory");  // consumer warps only
@@ -377,7 +411,10 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const uint4 v = reinterpret_cast<const uint4 *>(hq + 32 * i)[q ^ i];
             hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
         }
-        const float hs = hqf[3 * i], Ha = hqf[3 * i + 1], Hb = hqf[3 * i + 2];
+        const float hs = hqf[7 * i], Ha = hqf[7 * i + 1], Hb = hqf[7 * i + 2];
+        int HQ[4];
+#pragma unroll
+        for (int b4 = 0; b4 < 4; ++b4) HQ[b4] = WF ? reinterpret_cast<const int *>(hqf)[7 * i + 3 + b4] : 0;
         auto hwf = [&hw](int p) { return hw[p]; };
         // box m holds rows [128m, 128m + 128) = the rows of iteration m; every box
         // completes on one barrier (they land while gate/up is computed), rows past
@@ -394,7 +431,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (lr < n_rows) {
                 const uint8_t *blk = stB + (size_t)m * box_stride + (size_t)(8 * warp + r8) * kBlockBytes;
                 const uint4 hd = ld_s128(blk), q0 = ld_s128(blk + 16 + 32 * i), q1 = ld_s128(blk + 32 + 32 * i);
-                v = chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums(q0, q1, hwf), hs, Ha, Hb);
+                v = WF ? chunk_contrib_nvfp4(hd, i, q0, q1, hwf, hs, HQ)
+                       : chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums(q0, q1, hwf), hs, Ha, Hb);
             }
             v += __shfl_xor_sync(0xffffffffu, v, 1);
             v += __shfl_xor_sync(0xffffffffu, v, 2);
@@ -454,8 +492,8 @@ bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs
     off += (nbox - 1) * box_stride + al(tail * kBlockBytes);
     a.cl_off_h = off;
     off += al(kQK * 4);
-    a.cl_off_x = off;  // quantised x: [H/64][32] words + [H/64][3] floats (later: quantised h)
-    off += al(d.hidden / 2 * 4 + d.hidden / 64 * 3 * 4);
+    a.cl_off_x = off;  // quantised x: [H/64][32] words + [H/64][7] (later: quantised h)
+    off += al(d.hidden / 2 * 4 + d.hidden / 64 * 7 * 4);
     a.cl_off_y = off;
     off += al(rpc * 4);
     a.cl_off_bar = off;
@@ -503,8 +541,9 @@ static cudaError_t launch_cluster_t(const DecodeArgs &a, const CUtensorMap &tm, 
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return a.norm_w ? cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, true>, tm, tt, a)
-                    : cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false>, tm, tt, a);
+    if (a.wtype == SI_WTYPE_NVFP4) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 1>, tm, tt, a);
+    return a.norm_w ? cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, true, 0>, tm, tt, a)
+                    : cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 0>, tm, tt, a);
 }
 
 cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s) {
@@ -522,15 +561,19 @@ cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s) {
 cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters) {
     *active_clusters = 0;
     if (!tensor_map_encoder()) return cudaErrorNotSupported;  // down blocks are fetched by a tensor map
-    const void *fs[2] = {nullptr, nullptr};  // plain and pre-normed block
+    const void *fs[3] = {nullptr, nullptr, nullptr};  // plain and pre-normed Q4_K block, NVFP4
     switch (nbh) {
-        case 1: fs[0] = (const void *)k_expert_cluster<1, false>, fs[1] = (const void *)k_expert_cluster<1, true>; break;
-        case 2: fs[0] = (const void *)k_expert_cluster<2, false>, fs[1] = (const void *)k_expert_cluster<2, true>; break;
-        case 4: fs[0] = (const void *)k_expert_cluster<4, false>, fs[1] = (const void *)k_expert_cluster<4, true>; break;
-        default: fs[0] = (const void *)k_expert_cluster<8, false>, fs[1] = (const void *)k_expert_cluster<8, true>; break;
+        case 1: fs[0] = (const void *)k_expert_cluster<1, false, 0>, fs[1] = (const void *)k_expert_cluster<1, true, 0>,
+                fs[2] = (const void *)k_expert_cluster<1, false, 1>; break;
+        case 2: fs[0] = (const void *)k_expert_cluster<2, false, 0>, fs[1] = (const void *)k_expert_cluster<2, true, 0>,
+                fs[2] = (const void *)k_expert_cluster<2, false, 1>; break;
+        case 4: fs[0] = (const void *)k_expert_cluster<4, false, 0>, fs[1] = (const void *)k_expert_cluster<4, true, 0>,
+                fs[2] = (const void *)k_expert_cluster<4, false, 1>; break;
+        default: fs[0] = (const void *)k_expert_cluster<8, false, 0>, fs[1] = (const void *)k_expert_cluster<8, true, 0>,
+                 fs[2] = (const void *)k_expert_cluster<8, false, 1>; break;
     }
     int least = 1 << 30;
-    for (const void *f : fs) {  // both variants must fit; the smaller resident count counts
+    for (const void *f : fs) {  // every variant must fit; the smallest resident count counts
         cudaFuncAttributes fa;
         cudaError_t err = cudaFuncGetAttributes(&fa, f);
         if (err != cudaSuccess) return err;

@@ -62,6 +62,8 @@ struct DecodeArgs {
     const float *router_w, *router_bias;
     const float *norm_w;  // [H] RMSNorm gain of a pre-normed block (out = x + MoE(norm(x))), or null
     float norm_eps;
+    int wtype;              // SI_WTYPE_Q4_K or SI_WTYPE_NVFP4
+    const float *wscale;    // NVFP4: [E][3] tensor scales of gate, up, down
     const uint16_t *x;  // [n][H] bf16 bits
     float *out;         // [n][H]
     int H, I, E, k, n;
@@ -103,6 +105,8 @@ struct PrefillArgs {
     const float *router_w, *router_bias;
     const float *norm_w;  // [H] RMSNorm gain of a pre-normed block (out = x + MoE(norm(x))), or null
     float norm_eps;
+    int wtype;              // SI_WTYPE_Q4_K or SI_WTYPE_NVFP4
+    const float *wscale;    // NVFP4: [E][3] tensor scales of gate, up, down
     const uint16_t *x;  // [T][H] bf16 bits
     float *out;         // [T][H]
     int H, I, E, k, T;
@@ -145,6 +149,7 @@ cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s);
 cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters);
 cudaError_t launch_debug_dequant(const uint8_t *blocks, int64_t n_blocks, float *out_f32,
                                  uint16_t *out_bf16, cudaStream_t s);
+cudaError_t launch_debug_nvfp4_f16(const uint8_t *blocks, int64_t n_blocks, float g, uint16_t *out, cudaStream_t s);
 cudaError_t launch_debug_dequant_f16(const uint8_t *blocks, int64_t n_blocks, const float *gamma, uint16_t *out,
                                      cudaStream_t s);
 cudaError_t launch_debug_topk(const float *logits, int n, int E, int k, int32_t *ids, float *w,

@@ -576,6 +576,40 @@ __device__ __forceinline__ bool q4k_subblock_f16(const Q4F16Lane &c, const uint8
     return bad;
 }
 
+// NVFP4 -> fp16 operand conversion, one thread's share: weights 64j + 32half
+// .. +31 of the super-block at blk (scale blocks 4j + 2half and 4j + 2half + 1).
+// Each w = e2m1 * e4m3 * g is formed in fp32 -- (T - 12) * (e4m3 / 2) is the
+// exact product e2m1 * e4m3, one rounding for g -- and rounded to fp16
+// (nearest even); o[i] holds columns 2i (low half) and 2i+1.  Returns true
+// when a weight lies beyond fp16's finite range.  The GEMM's dequantization
+// warps and the test export si_debug_nvfp4_dequant_f16 both run it.
+__device__ __forceinline__ bool nvfp4_half_f16(const uint8_t *blk, int j, int half, float g, uint32_t (&o)[16]) {
+    const uint4 c4 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * j + 16 * half);  // 32 codes
+    const uint32_t sw = *reinterpret_cast<const uint32_t *>(blk + 4 * j) >> (16 * half);  // their 2 scale bytes
+    const float s0 = 0.5f * e4m3_to_f32(sw & 0xffu), s1 = 0.5f * e4m3_to_f32((sw >> 8) & 0xffu);
+    const bool bad = fmaxf(fabsf(s0), fabsf(s1)) * 12.f * fabsf(g) > 65504.f;
+    const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
+    // e2m1 of code n of a word: (T - 12) / 2 in fp32, with the code's sign bit
+    // or-ed in so that code 8 is -0 (the value is already negative otherwise)
+    auto e2 = [](uint32_t vv, int byte, uint32_t word, int n) {
+        const float v = (float)((int)((vv >> (8 * byte)) & 0xffu) - 12);
+        return __uint_as_float(__float_as_uint(v) | ((word << (28 - 4 * n)) & 0x80000000u));
+    };
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {  // codes 8t .. 8t+7
+        const float sc = t < 2 ? s0 : s1;
+        const uint32_t v[2] = {e2m1_t4(cw[t]), e2m1_t4(cw[t] >> 16)};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {  // codes 8t + 2m, 8t + 2m + 1
+            const uint32_t vv = v[m >> 1] >> (16 * (m & 1));
+            const float w0 = __fmul_rn(__fmul_rn(e2(vv, 0, cw[t], 2 * m), sc), g);
+            const float w1 = __fmul_rn(__fmul_rn(e2(vv, 1, cw[t], 2 * m + 1), sc), g);
+            o[4 * t + m] = f16x2_rn(w0, w1);
+        }
+    }
+    return bad;
+}
+
 // MODE 0 (gate/up): unit tile covers intermediate rows tile*128 .. +127;
 //   CTA r holds rows tile*128 + 64r + i as A rows 2i (gate) and 2i+1 (up);
 //   K = H; B rows = padded token rows of the expert (xp); epilogue
@@ -605,7 +639,9 @@ __device__ __forceinline__ bool q4k_subblock_f16(const Q4F16Lane &c, const uint8
 // traffic); empty (both CTAs, both MMA threads) and d_full are completed by
 // the multicast MMA commits; d_empty (even CTA) by both CTAs' epilogue
 // warps; raw_* are local.
-template <int MODE, bool NORM>
+// WF = 1: NVFP4 weights (the same 144-byte blocks; nvfp4_half_f16 instead of
+// q4k_subblock_f16, times the expert matrix's tensor scale).
+template <int MODE, bool NORM, int WF>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     k_prefill_gemm(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                    const __grid_constant__ CUtensorMap tm_b64, const __grid_constant__ CUtensorMap tm_b16,
@@ -826,7 +862,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
                 // pre-normed block: the gate/up weights of hidden column c times gamma_c (the
                 // token's 1 / rms is applied to g and u in the epilogue), so x stays exact
                 const float *gp = (MODE == 0 && NORM) ? gam + 64 * ((kb + ps.rot) % nK) + 32 * half : nullptr;
-                if (q4k_subblock_f16<MODE == 0 && NORM>(lc, blk, j, half, gp, o)) set_status(status, SI_ERR_RANGE);
+                if (WF) {
+                    const float g = a.wscale[3 * ps.e + (MODE == 1 ? 2 : (raw_row >= 64 ? 1 : 0))];
+                    if (nvfp4_half_f16(blk, j, half, g, o)) set_status(status, SI_ERR_RANGE);
+                } else if (q4k_subblock_f16<MODE == 0 && NORM>(lc, blk, j, half, gp, o)) {
+                    set_status(status, SI_ERR_RANGE);
+                }
                 uint8_t *at = sm + s * kATile + row * 128;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -984,6 +1025,26 @@ __global__ void __launch_bounds__(256) k_debug_dequant_f16(const uint8_t *blocks
     for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
 }
 
+__global__ void __launch_bounds__(256) k_debug_nvfp4_f16(const uint8_t *blocks, int64_t n_blocks, float g,
+                                                         uint16_t *out) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= n_blocks * 8) return;
+    const int64_t b = t >> 3;
+    const int j = (int)(t & 7) >> 1, half = (int)(t & 1);
+    uint32_t o[16];
+    nvfp4_half_f16(blocks + b * kBlockBytes, j, half, g, o);
+    uint4 *dst = reinterpret_cast<uint4 *>(out + 256 * b + 64 * j + 32 * half);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+
+cudaError_t launch_debug_nvfp4_f16(const uint8_t *blocks, int64_t n_blocks, float g, uint16_t *out, cudaStream_t s) {
+    if (n_blocks == 0) return cudaSuccess;
+    const int64_t threads = n_blocks * 8;
+    k_debug_nvfp4_f16<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(blocks, n_blocks, g, out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_debug_dequant_f16(const uint8_t *blocks, int64_t n_blocks, const float *gamma, uint16_t *out,
                                      cudaStream_t s) {
     if (n_blocks == 0) return cudaSuccess;
@@ -1045,11 +1106,13 @@ cudaError_t prefill_prepare(const Plan &p) {
     if (!encoder()) return cudaErrorNotSupported;
     cudaError_t err = cudaFuncSetAttribute(k_prefill_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(k_prefill_gemm<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(k_prefill_gemm<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-    if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(k_prefill_gemm<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    const void *fs[5] = {(const void *)k_prefill_gemm<0, false, 0>, (const void *)k_prefill_gemm<0, true, 0>,
+                         (const void *)k_prefill_gemm<1, false, 0>, (const void *)k_prefill_gemm<0, false, 1>,
+                         (const void *)k_prefill_gemm<1, false, 1>};
+    for (const void *f : fs)
+        if ((err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem)) != cudaSuccess)
+            return err;
+    return cudaSuccess;
 }
 
 // Records events[i] on s (as an external event node while s is being captured).
@@ -1095,12 +1158,17 @@ cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, 
     // one CTA pair (2-CTA cluster, declared on the kernel) per two SMs
     const int grid = 2 * (p.sm_count / 2);
     if (a.norm_w)  // pre-normed block: gamma folded into the weights, 1 / rms into the epilogue
-        k_prefill_gemm<0, true><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
+        k_prefill_gemm<0, true, 0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
+    else if (a.wtype == SI_WTYPE_NVFP4)
+        k_prefill_gemm<0, false, 1><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
     else
-        k_prefill_gemm<0, false><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
+        k_prefill_gemm<0, false, 0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 2, s)) != cudaSuccess) return err;
-    k_prefill_gemm<1, false><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
+    if (a.wtype == SI_WTYPE_NVFP4)
+        k_prefill_gemm<1, false, 1><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
+    else
+        k_prefill_gemm<1, false, 0><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 3, s)) != cudaSuccess) return err;
     const size_t n4 = (size_t)a.T * (a.H / 4);

@@ -1,7 +1,8 @@
 """Device residency for layers and tokens (torch owns the memory).
 
-Weights stay in GGUF Q4_K form in HBM, exactly the bytes the generator (or
-a GGUF file) holds; nothing is repacked or dequantized ahead of time.
+Weights stay in their quantized form in HBM (GGUF Q4_K blocks, or NVFP4
+super-blocks), exactly the bytes the generator holds; nothing is
+dequantized ahead of time.
 """
 from __future__ import annotations
 
@@ -25,10 +26,11 @@ class DeviceLayer:
     router_bias: Optional[torch.Tensor] = None
     norm_weight: Optional[torch.Tensor] = None   # float32 [H]: pre-normed block with residual
     norm_eps: float = 0.0
+    w_scale: Optional[torch.Tensor] = None       # float32 [E, 3]: NVFP4 tensor scales
 
     def struct(self) -> binding.si_moe_layer:
         return binding.layer_struct(self.w_gate, self.w_up, self.w_down, self.router_w,
-                                    self.router_bias, self.norm_weight, self.norm_eps)
+                                    self.router_bias, self.norm_weight, self.norm_eps, self.w_scale)
 
     @property
     def nbytes(self) -> int:
@@ -41,8 +43,9 @@ def to_device(layer: MoeLayer, device="cuda") -> DeviceLayer:
         return torch.from_numpy(np.ascontiguousarray(a)).to(device)
     bias = None if layer.router_bias is None else up(layer.router_bias)
     norm = None if layer.norm_weight is None else up(layer.norm_weight)
+    wsc = None if getattr(layer, "gscale", None) is None else up(layer.gscale)
     return DeviceLayer(layer.shape, up(layer.w_gate), up(layer.w_up), up(layer.w_down),
-                       up(layer.router_w), bias, norm, float(layer.norm_eps) if norm is not None else 0.0)
+                       up(layer.router_w), bias, norm, float(layer.norm_eps) if norm is not None else 0.0, wsc)
 
 
 def tokens_to_device(x_bits: np.ndarray, device="cuda") -> torch.Tensor:
@@ -51,8 +54,8 @@ def tokens_to_device(x_bits: np.ndarray, device="cuda") -> torch.Tensor:
     return t.to(device).view(torch.bfloat16)
 
 
-def desc_for(shape: MoeShape, max_tokens: int = 1) -> binding.si_moe_desc:
-    return binding.make_desc(shape.hidden, shape.intermediate, shape.n_experts, shape.top_k, max_tokens)
+def desc_for(shape: MoeShape, max_tokens: int = 1, wtype: int = binding.SI_WTYPE_Q4_K) -> binding.si_moe_desc:
+    return binding.make_desc(shape.hidden, shape.intermediate, shape.n_experts, shape.top_k, max_tokens, wtype)
 
 
 def alloc_scratch(plan: binding.Plan, mode: int, n_tokens: int, device="cuda",
