@@ -51,12 +51,13 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILED_TRAFFIC = {
     "k_expert_cluster": {
         "bytes": 21295616,
-        "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:k_expert_cluster "
-                   "on bench.py --tokens 64 --no-extras (launch 21)",
+        "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
+                   "-k regex:k_expert_cluster -s 20 -c 3 on bench.py --tokens 64 --steps 2 --warmup 1 "
+                   "--no-extras --no-cpu-baseline (launch 21)",
         "sources": ["quantized_moe_expert_gemv_gb300/csrc/si_expert_cluster.cu",
                     "quantized_moe_expert_gemv_gb300/csrc/si_device.cuh",
                     "quantized_moe_expert_gemv_gb300/csrc/si_internal.h"],
-        "sha256": "c440d01597359c740364c6825828c3a2e9971d89e2300c6148d7ba278bf0fe4e",
+        "sha256": "581020c77443651c6737492b061bfcbdaad2f440ad4a46bf094b0100db71ffcc",
     },
 }
 
