@@ -264,16 +264,12 @@ __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, lo
     }
 }
 
-// The same wait for a whole warp with one polling lane: lane 0 spins, and
-// once it has seen the phase complete every lane takes one try_wait of its
-// own (which then succeeds at once) for the acquire of the copied bytes.
-// Polling from one lane keeps the barrier word free for the producer's and
-// the copy engine's updates.  Warp-uniform result.
+// The same wait for a whole warp: every lane polls, so that each lane's own
+// try_wait is the acquire of the copied bytes (one instruction for the warp;
+// letting lane 0 poll alone and then repeating the wait on every lane
+// measured slower).  Warp-uniform result.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, long long budget) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, budget);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) ok = mbar_wait_bounded(bar, parity, budget);
+    const bool ok = mbar_wait_bounded(bar, parity, budget);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -349,6 +345,26 @@ __device__ __forceinline__ void st_cluster_f32(const void *local, uint32_t rank,
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_addr(local)), "r"(rank));
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(raddr), "f"(v) : "memory");
 }
+// Store the 32-bit v into shared memory of CTA `rank` of this cluster, at the
+// address that `local` has in this CTA, and count its 4 bytes against the
+// transaction count of that CTA's mbarrier at the address `bar` has here.  A
+// thread that sees the barrier's phase complete also sees the stored value.
+__device__ __forceinline__ void st_async_cluster_u32(const void *local, uint32_t bar, uint32_t rank, uint32_t v) {
+    uint32_t raddr, rbar;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(bar), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr), "r"(v),
+                 "r"(rbar)
+                 : "memory");
+}
+// Split cluster barrier: every thread of every CTA of the cluster arrives
+// (relaxed: order earlier writes with a fence first, e.g. fence_mbar_init)
+// and later waits (acquire).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
 // All threads of all CTAs of the cluster; release/acquire orders DSMEM stores.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -404,19 +420,21 @@ __device__ __forceinline__ bool mbar_wait_warp_spin(uint32_t bar, uint32_t parit
     if (ok) ok = mbar_wait_spin(bar, parity, budget);
     return __all_sync(0xffffffffu, ok);
 }
+// Every lane of the warp waits (bounded, sleeping between polls) with
+// cluster-scope acquire: for barriers completed by other CTAs' st.async.
+__device__ __forceinline__ bool mbar_wait_warp_cluster(uint32_t bar, uint32_t parity, long long budget) {
+    bool ok = mbar_try_wait_cluster(bar, parity);
+    if (!ok) {
+        const long long t0 = clock64();
+        while (!(ok = mbar_try_wait_cluster(bar, parity)) && clock64() - t0 <= budget) __nanosleep(20);
+    }
+    return __all_sync(0xffffffffu, ok);
+}
 __device__ __forceinline__ bool mbar_wait_warp_spin_cluster(uint32_t bar, uint32_t parity, long long budget) {
     bool ok = true;
     if ((threadIdx.x & 31) == 0) ok = mbar_wait_spin_cluster(bar, parity, budget);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) ok = mbar_wait_spin_cluster(bar, parity, budget);
-    return __all_sync(0xffffffffu, ok);
-}
-// Whole warp: lane 0 polls, then every lane takes one acquiring try_wait.
-__device__ __forceinline__ bool mbar_wait_warp_cluster(uint32_t bar, uint32_t parity, long long budget) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded_cluster(bar, parity, budget);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) ok = mbar_wait_bounded_cluster(bar, parity, budget);
     return __all_sync(0xffffffffu, ok);
 }
 
