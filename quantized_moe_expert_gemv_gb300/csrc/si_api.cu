@@ -53,6 +53,7 @@ DecodeLayout decode_layout(const si_moe_desc &d, int n) {
     L.counts = take((size_t)d.n_experts * sizeof(int32_t));
     L.uniq = take(sizeof(UniqTable));
     L.h = take((size_t)n * d.top_k * d.intermediate * sizeof(float));
+    L.xq = take((size_t)(d.hidden / 64) * kXqWords * sizeof(uint32_t));
     L.total = o;
     return L;
 }
@@ -290,6 +291,7 @@ static si_status forward_decode_impl(si_moe_plan_t plan, const si_moe_layer *lay
     a.counts = reinterpret_cast<int32_t *>(sb + L.counts);
     a.uniq = reinterpret_cast<si::UniqTable *>(sb + L.uniq);
     a.h = reinterpret_cast<float *>(sb + L.h);
+    a.xq = reinterpret_cast<uint32_t *>(sb + L.xq);
     if (ro) {
         a.o_ids = ro->topk_ids;
         a.o_w = ro->topk_w;

@@ -83,8 +83,14 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
     float *const ow_p = pin_ptr(a.o_w);
     int32_t *const counts_p = pin_ptr(a.counts);
     int32_t *const ocounts_p = pin_ptr(a.o_counts);
+    uint32_t *const xq_p = pin_ptr(a.xq);
     const int n = pin_i32(a.n), H = pin_i32(a.H), E = pin_i32(a.E), k = pin_i32(a.k);
     const int zero_out = pin_i32(a.zero_out), sel_logits = pin_i32(a.sel_logits);
+    // One plain token for the cluster expert kernel: that kernel's work before its
+    // own dependency wait reads nothing this call produces (x is quantised here),
+    // so it may be launched at once and be resident when this grid completes.
+    const bool early_dependents = !NORM && sel_logits;
+    if (early_dependents) pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wpc = blockDim.x >> 5;
     const int e = blockIdx.x * wpc + warp;
@@ -115,8 +121,8 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
     // Warm L2 with x (a prefetch returns no data: if an earlier kernel is still
     // writing x, L2 stays coherent and the loads below happen after the wait).
     if (blockIdx.x == 0 && threadIdx.x < (n * H * 2) / 128) prefetch_l2(reinterpret_cast<const uint8_t *>(xg_p) + 128 * threadIdx.x);
-    pdl_wait();               // x and the scratch are ready (previous kernels complete)
-    pdl_launch_dependents();  // the expert kernel may become resident now (x is final)
+    pdl_wait();  // x and the scratch are ready (previous kernels complete)
+    if (!early_dependents) pdl_launch_dependents();  // the expert kernel may become resident now (x is final)
     if (NJ > 0) {             // x once per CTA into shared memory (every warp reads all of it)
         const uint4 *xg = reinterpret_cast<const uint4 *>(xg_p);
         for (int q = threadIdx.x; q < n * 32 * NJ; q += blockDim.x) s_x[q] = __ldg(xg + q);
@@ -198,6 +204,38 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
                 }
                 if (lane == 0 && ologits_p) ologits_p[t * E + e] = z;
             }
+        }
+    }
+    // One plain token for the cluster expert kernel: quantise x per 64-column chunk
+    // into the scratch (int16 pairs, xq = rint(x / s), s = max|x| / 32767; the two
+    // 32-column sums; the four 16-column sums of xq), one warp per chunk, in the
+    // layout the expert kernel copies into its shared memory as it is.
+    if (early_dependents) {
+        const uint32_t *xw32 = NJ > 0 ? reinterpret_cast<const uint32_t *>(s_x) : reinterpret_cast<const uint32_t *>(xg_p);
+        const int NC = H / 64;
+        for (int c = blockIdx.x + gridDim.x * warp; c < NC; c += gridDim.x * wpc) {
+            const uint32_t wv = xw32[32 * c + lane];  // columns 2*lane, 2*lane + 1 of chunk c
+            const float v0 = __uint_as_float(wv << 16), v1 = __uint_as_float(wv & 0xffff0000u);
+            float mx = fmaxf(fabsf(v0), fabsf(v1));
+            float sum = v0 + v1;  // lanes 0..15: the first 32 columns, 16..31: the second
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
+            const uint32_t q = pack_q16(v0, v1, inv);
+            int s2 = (int)(int16_t)(q & 0xffffu) + ((int)q >> 16);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
+            xq_p[32 * c + 4 * ((lane >> 2) ^ (c & 7)) + (lane & 3)] = q;
+            uint32_t *dst = xq_p + 32 * NC + 8 * c;
+            if (lane == 0) {
+                dst[0] = __float_as_uint(mx * (1.0f / 32767.0f));
+                dst[1] = __float_as_uint(sum);
+            }
+            if (lane == 16) dst[2] = __float_as_uint(sum);
+            if ((lane & 7) == 0) dst[3 + (lane >> 3)] = (uint32_t)s2;
         }
     }
     if (gridDim.x > 1) cluster_sync();

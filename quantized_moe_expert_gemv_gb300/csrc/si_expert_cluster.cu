@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const int fault_wait = pin_i32(a.fault_wait);
     const int I = pin_i32(a.I), H = pin_i32(a.H);
     const float *const wsc = WF ? pin_ptr(a.wscale) : nullptr;  // NVFP4 tensor scales [E][3]
+    const uint32_t *const xq_g = pin_ptr(a.xq);  // x quantised by the router (plain block)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = (int)cluster_nctarank();
@@ -141,6 +142,8 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const uint32_t emptyA = fullA + 8 * NSA;
     const uint32_t fullB = emptyA + 8 * NSA;  // all down boxes complete on this one barrier
     const uint32_t hbar = fullB + 8;          // the unit's 256 h values, stored by every CTA of the cluster
+    const uint32_t xbar = hbar + 8;           // the router's quantised x (plain block)
+    const uint32_t xq_bytes = (uint32_t)(H / 64) * kXqWords * 4;
     int32_t *status = ctrl + kCtrlStatus;
     auto stage_bytes = [&](int j) { return (uint32_t)((min(CH * (j + 1), n_rp) - CH * j) * rowg); };
 
@@ -154,6 +157,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         }
         mbar_init(fullB, 1);
         mbar_init(hbar, 1);
+        mbar_init(xbar, 1);
         s_lastB = -1;
         s_err = 0;
         fence_mbar_init();
@@ -164,16 +168,19 @@ __global__ void __launch_bounds__(kClThreads, 1)
         // CTA (the largest CTA's remainder), which may exceed this CTA's n_rows
         mbar_arrive_expect_tx(fullB, (uint32_t)(((nbox - 1) * kBoxRows + tail_rows) * kBlockBytes));
         mbar_arrive_expect_tx(hbar, (uint32_t)(kQK * 4));  // every h value of the unit, once
+        if (!NORM) mbar_arrive_expect_tx(xbar, xq_bytes);
     }
-    // The token's H/64 activation chunks, quantised once (warp 0) into shared memory
-    // before the dependency wait: the router launches this kernel only after its
-    // own wait on the producers of x, so x is final here.  Each chunk is a row of
-    // 32 words; its 16-byte unit q is stored at unit q ^ (row & 7), so that the
-    // lanes that load different rows into registers hit different banks.
-    // A pre-normed block stages the norm gain in the (still idle) gate/up stages
-    // while warp 0's loads of x are in flight; warp 0 then quantises
-    // x * gamma / rms(x) (lanes 0..H/64-1 hold all of x).
-    const bool xq_lane = warp == 0 && lane < H / 64;
+    // A plain block reads x quantised by the router (after the dependency wait, in
+    // the consumer warps), so this kernel may be launched before the router has
+    // read x.  A pre-normed block quantises x * gamma / rms(x) here, before the
+    // dependency wait (the router launches it only after its own wait on the
+    // producers of x, so x is final): warp 0 quantises the token's H/64 chunks
+    // into shared memory, each a row of 32 words whose 16-byte unit q is stored
+    // at unit q ^ (row & 7), so that the lanes that load different rows into
+    // registers hit different banks; the norm gain is staged in the (still idle)
+    // gate/up stages while warp 0's loads of x are in flight (lanes 0..H/64-1
+    // hold all of x).
+    const bool xq_lane = NORM && warp == 0 && lane < H / 64;
     uint4 xr[8];
     if (xq_lane) {
         const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + 64 * lane);
@@ -263,8 +270,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
     // --------------------------------------------------------- producer
     if (warp == kCW) {
         if (lane == 0) {
-            const int e = ids[slot];
             const uint64_t pol = l2_evict_first_policy();
+            // the router's quantised x first (every consumer warp needs it for stage 0),
+            // one copy into this CTA's shared memory
+            if (!NORM) bulk_g2s(smem_addr(xq_s), xq_g, xq_bytes, xbar, l2_evict_last_policy());
+            const int e = ids[slot];
             auto issueA = [&](int j) -> bool {
                 const int st = j % NSA;
                 const uint32_t bytes = stage_bytes(j);
@@ -308,18 +318,36 @@ __global__ void __launch_bounds__(kClThreads, 1)
     if (warp < kCW) {
         const int g = lane / GS, li = lane % GS, b = li >> 2, i = li & 3;
         const int chunk = 4 * b + i;
-        const uint32_t *xq = xq_s;  // quantised in the prologue
-        const float *xqf = reinterpret_cast<const float *>(xq + H / 2);
         uint32_t xw[32];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const uint4 v = reinterpret_cast<const uint4 *>(xq + 32 * chunk)[q ^ (chunk & 7)];
-            xw[4 * q] = v.x, xw[4 * q + 1] = v.y, xw[4 * q + 2] = v.z, xw[4 * q + 3] = v.w;
-        }
-        const float xs = xqf[7 * chunk], Xa = xqf[7 * chunk + 1], Xb = xqf[7 * chunk + 2];
+        float xs, Xa, Xb;
         int XQ[4];
+        if (NORM) {  // quantised in the prologue
+            const uint32_t *xq = xq_s;
+            const float *xqf = reinterpret_cast<const float *>(xq + H / 2);
 #pragma unroll
-        for (int b4 = 0; b4 < 4; ++b4) XQ[b4] = WF ? reinterpret_cast<const int *>(xqf)[7 * chunk + 3 + b4] : 0;
+            for (int q = 0; q < 8; ++q) {
+                const uint4 v = reinterpret_cast<const uint4 *>(xq + 32 * chunk)[q ^ (chunk & 7)];
+                xw[4 * q] = v.x, xw[4 * q + 1] = v.y, xw[4 * q + 2] = v.z, xw[4 * q + 3] = v.w;
+            }
+            xs = xqf[7 * chunk], Xa = xqf[7 * chunk + 1], Xb = xqf[7 * chunk + 2];
+#pragma unroll
+            for (int b4 = 0; b4 < 4; ++b4) XQ[b4] = WF ? reinterpret_cast<const int *>(xqf)[7 * chunk + 3 + b4] : 0;
+        } else {  // quantised by the router, copied by the producer
+            if (!mbar_wait_warp(xbar, 0, budget)) {
+                set_status(status, SI_ERR_TIMEOUT);
+                *verr = 1;
+            }
+            const uint32_t *xq = xq_s;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint4 v = reinterpret_cast<const uint4 *>(xq + 32 * chunk)[q ^ (chunk & 7)];
+                xw[4 * q] = v.x, xw[4 * q + 1] = v.y, xw[4 * q + 2] = v.z, xw[4 * q + 3] = v.w;
+            }
+            const uint4 f = reinterpret_cast<const uint4 *>(xq + H / 2 + 8 * chunk)[0];
+            const uint4 f2 = reinterpret_cast<const uint4 *>(xq + H / 2 + 8 * chunk)[1];
+            xs = __uint_as_float(f.x), Xa = __uint_as_float(f.y), Xb = __uint_as_float(f.z);
+            XQ[0] = (int)f.w, XQ[1] = (int)f2.x, XQ[2] = (int)f2.y, XQ[3] = (int)f2.z;
+        }
         auto xwf = [&xw](int p) { return xw[p]; };
         // NVFP4: this unit's expert's gate and up tensor scales
         float tsg = 1.f, tsu = 1.f;
@@ -468,6 +496,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         for (int st = 0; st < NSA; ++st)
             if (s_lastA[st] >= 0) mbar_wait_bounded(fullA + 8 * st, s_lastA[st], kDrain);
         if (s_lastB >= 0) mbar_wait_bounded(fullB, 0, kDrain);
+        if (!NORM) mbar_wait_bounded(xbar, 0, kDrain);  // issued by the producer in every case
     }
 }
 
@@ -513,11 +542,11 @@ bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs
     a.cl_off_h = off;
     off += al(kQK * 4);
     a.cl_off_x = off;  // quantised x: [H/64][32] words + [H/64][7] (later: quantised h)
-    off += al(d.hidden / 2 * 4 + d.hidden / 64 * 7 * 4);
+    off += al(d.hidden / 64 * kXqWords * 4);
     a.cl_off_y = off;
     off += al(rpc * 4);
     a.cl_off_bar = off;
-    off += 8 * (2 * NSA + 2) + 64;
+    off += 8 * (2 * NSA + 3) + 64;
     if (off + 1024 > smem_max) return false;  // + static shared memory
     a.cl_nsa = NSA;
     a.cl_C = C;

@@ -19,6 +19,11 @@ enum CtrlWord : int {
     kCtrlWords = 64,
 };
 constexpr size_t kCtrlBytes = kCtrlWords * sizeof(int32_t);
+// x quantised per 64-column chunk (NC = H/64 chunks) as one block of 40*NC
+// words: first the int16 pairs, chunk c at words 32c.. with its 16-byte unit q
+// stored at unit q ^ (c & 7); then 8 words per chunk: the scale, the two
+// 32-column sums (fp32 bits), four 16-column integer sums and a pad.
+constexpr int kXqWords = 40;
 constexpr int kMaxSlots = SI_MAX_DECODE_TOKENS * SI_MAX_TOPK;  // 64
 
 // Table of the distinct experts of one decode call (all int32).
@@ -30,7 +35,7 @@ struct UniqTable {
 };
 
 struct DecodeLayout {
-    size_t ctrl, logits, ids, wts, counts, uniq, h, total;
+    size_t ctrl, logits, ids, wts, counts, uniq, h, xq, total;
 };
 
 struct Plan {
@@ -74,6 +79,7 @@ struct DecodeArgs {
     int32_t *counts;
     UniqTable *uniq;
     float *h;  // [n][k][I]
+    uint32_t *xq;  // [H/64][kXqWords]: one token's x quantised per 64 columns by the router (cluster path)
     int32_t *o_ids;
     float *o_w;
     int32_t *o_counts;
