@@ -55,12 +55,15 @@ __device__ __forceinline__ float sumsq8_bf16(const uint4 &xv, float s) {
 // expert's router row is loaded into registers before the programmatic-
 // dependent-launch wait (router weights do not depend on the token, so this
 // overlaps the previous kernel's tail).  NJ == 0: any H, loaded after the wait.
-// Logits are gathered into CTA 0 through distributed shared memory; CTA 0
-// takes softmax, top-k, renormalised weights, per-expert counts and the
-// table of distinct experts (deterministic: ascending expert id, tokens in
-// pair order).  One token feeding the cluster expert kernel (sel_logits):
-// every CTA receives every logit, each warp ranks its own expert and stores
-// the selected ones at their rank; the expert kernel forms the weights.
+// Logits are gathered into CTA 0 through distributed shared memory
+// (asynchronous stores that count their bytes on the receiving CTA's
+// mbarrier, which that CTA waits on: cheaper than a release/acquire cluster
+// barrier); CTA 0 takes softmax, top-k, renormalised weights, per-expert
+// counts and the table of distinct experts (deterministic: ascending expert
+// id, tokens in pair order).  One token feeding the cluster expert kernel
+// (sel_logits): every CTA receives every logit, each warp ranks its own
+// expert and stores the selected ones at their rank; the expert kernel forms
+// the weights.  A plain block also quantises x for that kernel.
 template <int NJ, bool NORM>
 __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs a) {
     __shared__ float s_z[SI_MAX_DECODE_TOKENS][SI_MAX_EXPERTS];
@@ -69,6 +72,7 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
     __shared__ int s_counts[SI_MAX_EXPERTS];
     __shared__ int s_pos[SI_MAX_EXPERTS];
     __shared__ int s_U;
+    __shared__ __align__(8) uint64_t s_zbar;  // completes when this CTA has received its logits
     __shared__ uint4 s_x[NJ > 0 ? SI_MAX_DECODE_TOKENS * 32 * NJ : 1];  // x [n][H] bf16 (NJ > 0)
     // parameters used after the dependency wait, read now
     const uint16_t *const xg_p = pin_ptr(a.x);
@@ -121,6 +125,17 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
     // Warm L2 with x (a prefetch returns no data: if an earlier kernel is still
     // writing x, L2 stays coherent and the loads below happen after the wait).
     if (blockIdx.x == 0 && threadIdx.x < (n * H * 2) / 128) prefetch_l2(reinterpret_cast<const uint8_t *>(xg_p) + 128 * threadIdx.x);
+    const bool zsa = gridDim.x > 1;  // a cluster: logits by asynchronous stores
+    if (zsa) {
+        if (threadIdx.x == 0) {
+            mbar_init(smem_addr(&s_zbar), 1);
+            fence_mbar_init();
+            // a single token: every CTA receives all n*E logits; several: CTA 0 alone
+            if (sel_logits || cluster_ctarank() == 0) mbar_arrive_expect_tx(smem_addr(&s_zbar), (uint32_t)(n * E * 4));
+        }
+        __syncthreads();
+        cluster_arrive_relaxed();
+    }
     pdl_wait();  // x and the scratch are ready (previous kernels complete)
     if (!early_dependents) pdl_launch_dependents();  // the expert kernel may become resident now (x is final)
     if (NJ > 0) {             // x once per CTA into shared memory (every warp reads all of it)
@@ -187,6 +202,7 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
                 }
             }
         }
+        if (zsa) cluster_wait();  // every CTA's barrier is initialised
 #pragma unroll
         for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {
             if (t < n) {
@@ -195,11 +211,11 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
                 if (bias_p) z += __ldg(bias_p + e);
                 if (sel_logits) {  // every CTA of the cluster gets every logit (lane c -> CTA c)
                     if (lane < (int)gridDim.x) {
-                        if (gridDim.x > 1) st_cluster_f32(&s_z[t][e], (uint32_t)lane, z);
+                        if (zsa) st_async_cluster_u32(&s_z[t][e], smem_addr(&s_zbar), (uint32_t)lane, __float_as_uint(z));
                         else s_z[t][e] = z;
                     }
                 } else if (lane == 0) {
-                    if (gridDim.x > 1) st_cluster_f32(&s_z[t][e], 0, z);
+                    if (zsa) st_async_cluster_u32(&s_z[t][e], smem_addr(&s_zbar), 0, __float_as_uint(z));
                     else s_z[t][e] = z;
                 }
                 if (lane == 0 && ologits_p) ologits_p[t * E + e] = z;
@@ -238,8 +254,14 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
             if ((lane & 7) == 0) dst[3 + (lane >> 3)] = (uint32_t)s2;
         }
     }
-    if (gridDim.x > 1) cluster_sync();
-    else __syncthreads();
+    if (zsa) {
+        if (e >= E) cluster_wait();  // warps without an expert still take the cluster barrier
+        if (sel_logits || cluster_ctarank() == 0) {
+            if (!mbar_wait_warp_cluster(smem_addr(&s_zbar), 0, a.wait_budget)) set_status(a.ctrl + kCtrlStatus, SI_ERR_TIMEOUT);
+        }
+    } else {
+        __syncthreads();
+    }
 
     // ---- one token feeding the cluster expert kernel: every warp ranks its own
     // expert against all E logits (the number of logits that beat it: greater,
