@@ -575,7 +575,202 @@ static cudaError_t launch_router_t(const DecodeArgs &a, cudaStream_t s) {
                     : cudaLaunchKernelEx(&cfg, k_router_topk<NJ, false>, a);
 }
 
+// Router + top-k of ONE plain token for the cluster expert kernel, on an
+// 8-CTA cluster, WPC experts per CTA (E == 8*WPC) and CPT columns per thread
+// (H == 32*WPC*CPT).  Thread t of CTA c holds, in registers loaded before the
+// dependency wait, the router weights of the CTA's WPC experts at columns
+// CPT*t .. CPT*t+CPT-1, so that x is read once per CTA (CPT columns per
+// thread, no shared copy) instead of once per expert.  Each thread forms WPC
+// partial sums; a reduce-scatter across the warp's lanes (log2(WPC) halving
+// shuffle steps) leaves each expert's warp sum in 32/WPC lanes, and the warps'
+// sums are added in shared memory (fixed order).  Then, as in k_router_topk:
+// every CTA receives every logit by asynchronous stores, each warp ranks its
+// own expert and stores the selected ones at their rank; x is quantised for
+// the expert kernel, which is launched at once.
+template <int WPC, int CPT>
+__global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
+    __shared__ float s_z[SI_MAX_EXPERTS];
+    __shared__ float s_part[WPC][WPC];  // [warp][local expert]
+    __shared__ __align__(8) uint64_t s_zbar;
+    const uint16_t *const xg_p = pin_ptr(a.x);
+    float *const out_p = pin_ptr(a.out);
+    const float *const bias_p = pin_ptr(a.router_bias);
+    float *const ologits_p = pin_ptr(a.o_logits);
+    int32_t *const ids_p = pin_ptr(a.ids);
+    float *const wts_p = pin_ptr(a.wts);
+    int32_t *const oids_p = pin_ptr(a.o_ids);
+    int32_t *const counts_p = pin_ptr(a.counts);
+    int32_t *const ocounts_p = pin_ptr(a.o_counts);
+    uint32_t *const xq_p = pin_ptr(a.xq);
+    const int H = pin_i32(a.H), E = pin_i32(a.E), k = pin_i32(a.k);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = (int)gridDim.x;
+    const int e0 = blockIdx.x * WPC;  // this CTA's experts
+    pdl_launch_dependents();  // the cluster expert kernel reads nothing of this call before its own wait
+    float w[WPC][CPT];
+#pragma unroll
+    for (int q = 0; q < WPC; ++q) {
+        const float *row = a.router_w + (size_t)(e0 + q) * H + CPT * threadIdx.x;
+        if (CPT == 2) {
+            const float2 v = __ldg(reinterpret_cast<const float2 *>(row));
+            w[q][0] = v.x, w[q][1] = v.y;
+        } else {
+#pragma unroll
+            for (int c4 = 0; c4 < CPT / 4; ++c4) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(row) + c4);
+                w[q][4 * c4] = v.x, w[q][4 * c4 + 1] = v.y, w[q][4 * c4 + 2] = v.z, w[q][4 * c4 + 3] = v.w;
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < WPC; ++q)  // the weights are in registers before the wait, not fetched after it
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) asm volatile("" ::"f"(w[q][c]));
+    if (blockIdx.x == 0 && threadIdx.x < (H * 2) / 128) prefetch_l2(reinterpret_cast<const uint8_t *>(xg_p) + 128 * threadIdx.x);
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&s_zbar), 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(smem_addr(&s_zbar), (uint32_t)(E * 4));  // every logit, once
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();
+    pdl_wait();  // x and the scratch are ready (previous kernels complete)
+    float xf[CPT];
+    {
+        const uint16_t *xp = xg_p + CPT * threadIdx.x;
+        uint32_t xw[CPT / 2];
+        if (CPT == 2) xw[0] = __ldg(reinterpret_cast<const uint32_t *>(xp));
+        else if (CPT == 4) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(xp));
+            xw[0] = v.x, xw[1 % (CPT / 2)] = v.y;
+        } else {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xp));
+            xw[0] = v.x, xw[1 % (CPT / 2)] = v.y, xw[2 % (CPT / 2)] = v.z, xw[3 % (CPT / 2)] = v.w;
+        }
+#pragma unroll
+        for (int c = 0; c < CPT / 2; ++c) {
+            xf[2 * c] = __uint_as_float(xw[c] << 16);
+            xf[2 * c + 1] = __uint_as_float(xw[c] & 0xffff0000u);
+        }
+    }
+    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < H; q += C * blockDim.x) out_p[q] = 0.f;  // the combine accumulates
+    float v[WPC];
+#pragma unroll
+    for (int q = 0; q < WPC; ++q) {
+        float acc = w[q][0] * xf[0];
+#pragma unroll
+        for (int c = 1; c < CPT; ++c) acc = fmaf(w[q][c], xf[c], acc);
+        v[q] = acc;
+    }
+    // reduce-scatter across the lanes: step s halves the experts a lane keeps
+#pragma unroll
+    for (int s = 0; (1 << s) < WPC; ++s) {
+        const int half = WPC >> (s + 1), mask = 16 >> s;
+        const bool up = (lane & mask) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float keep = up ? v[i + half] : v[i], send = up ? v[i] : v[i + half];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        }
+    }
+    constexpr int kGroup = 32 / WPC;  // lanes that share one expert after the halving steps
+#pragma unroll
+    for (int m = kGroup / 2; m > 0; m >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+    if (lane % kGroup == 0) s_part[warp][lane / kGroup] = v[0];
+    __syncthreads();
+    cluster_wait();  // every CTA's mbarrier is initialised (all arrived long ago)
+    {  // warp q: the logit of expert e0 + q, the sum of the WPC warps' partials
+        float z = lane < WPC ? s_part[lane][warp] : 0.f;
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) z += __shfl_xor_sync(0xffffffffu, z, m);
+        const int e = e0 + warp;
+        if (bias_p) z += __ldg(bias_p + e);
+        if (lane < C) st_async_cluster_u32(&s_z[e], smem_addr(&s_zbar), (uint32_t)lane, __float_as_uint(z));
+        if (lane == 0 && ologits_p) ologits_p[e] = z;
+    }
+    // x quantised per 64-column chunk for the expert kernel (the layout of k_router_topk)
+    {
+        const uint32_t *xw32 = reinterpret_cast<const uint32_t *>(xg_p);
+        const int NC = H / 64;
+        for (int c = blockIdx.x + C * warp; c < NC; c += C * WPC) {
+            const uint32_t wv = xw32[32 * c + lane];
+            const float v0 = __uint_as_float(wv << 16), v1 = __uint_as_float(wv & 0xffff0000u);
+            float mx = fmaxf(fabsf(v0), fabsf(v1));
+            float sum = v0 + v1;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
+            const uint32_t qw = pack_q16(v0, v1, inv);
+            int s2 = (int)(int16_t)(qw & 0xffffu) + ((int)qw >> 16);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
+            xq_p[32 * c + 4 * ((lane >> 2) ^ (c & 7)) + (lane & 3)] = qw;
+            uint32_t *dst = xq_p + 32 * NC + 8 * c;
+            if (lane == 0) {
+                dst[0] = __float_as_uint(mx * (1.0f / 32767.0f));
+                dst[1] = __float_as_uint(sum);
+            }
+            if (lane == 16) dst[2] = __float_as_uint(sum);
+            if ((lane & 7) == 0) dst[3 + (lane >> 3)] = (uint32_t)s2;
+        }
+    }
+    if (!mbar_wait_warp_cluster(smem_addr(&s_zbar), 0, a.wait_budget)) set_status(a.ctrl + kCtrlStatus, SI_ERR_TIMEOUT);
+    // warp q ranks expert e0 + q against all E logits (greater, or equal with a
+    // lower index, beats it) and stores it at its rank if selected
+    const int e = e0 + warp;
+    const float ze = s_z[e];
+    int cnt = 0;
+#pragma unroll
+    for (int q = 0; q < SI_MAX_EXPERTS / 32; ++q) {
+        const int j = lane + 32 * q;
+        if (j < E) {
+            const float zj = s_z[j];
+            cnt += (zj > ze) | ((zj == ze) & (j < e));
+        }
+    }
+    const int r = __reduce_add_sync(0xffffffffu, cnt);
+    if (lane == 0) {
+        if (r < k) {
+            ids_p[r] = e;
+            wts_p[r] = ze;  // the expert kernel turns these into renormalised weights
+            if (oids_p) oids_p[r] = e;
+        }
+        counts_p[e] = r < k ? 1 : 0;
+        if (ocounts_p) ocounts_p[e] = r < k ? 1 : 0;
+    }
+}
+
+template <int WPC, int CPT>
+static cudaError_t launch_router_one(const DecodeArgs &a, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(8);
+    cfg.blockDim = dim3(32 * WPC);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 8;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_router_one<WPC, CPT>, a);
+}
+
 static cudaError_t launch_router(const DecodeArgs &a, cudaStream_t s) {
+    // one plain token for the cluster expert kernel: the column-split router
+    if (a.sel_logits && !a.norm_w && a.E % 8 == 0) {
+        const int wpc = a.E / 8;
+        if (wpc == 16 && a.H == 512 * 4) return launch_router_one<16, 4>(a, s);
+        if (wpc == 16 && a.H == 512 * 2) return launch_router_one<16, 2>(a, s);
+        if (wpc == 8 && a.H == 256 * 8) return launch_router_one<8, 8>(a, s);
+        if (wpc == 8 && a.H == 256 * 4) return launch_router_one<8, 4>(a, s);
+    }
     // register prefetch of the router rows: 2*NJ float4 per lane; with 1024
     // threads per CTA (E > 128) keep the register footprint small instead
     if ((a.E + router_cluster_size(a.E) - 1) / router_cluster_size(a.E) > 16) return launch_router_t<0>(a, s);
