@@ -449,3 +449,124 @@ void or_counts_offsets_perm(const int32_t *ids, int T, int k, int E,
         for (int64_t p = 0; p < P; ++p)
             if (ids[p] == e) perm[pos++] = (int32_t)p;
 }
+
+/* ---------------------------------------------------------------------
+ * int8-activation mode (the "on-read dp4a MMVQ" of the sparkinfer README,
+ * "Milestone 1", with the activation quantised once per vector -- "one
+ * quantise per activation"): an approximation of the FFN above, defined
+ * here step by step so that a kernel taking the same steps can be checked
+ * closely, and the approximation itself measured against the exact FFN.
+ * The pages give no activation format; this reading takes 32-column blocks
+ * (one Q4_K sub-block each):
+ *   mx = max_l |v_l| over the block (v the activation as fp32),
+ *   inv = fp32(127 / mx) (0 when mx = 0),  q_l = round-half-even(v_l * inv)
+ *   (the product taken exactly), so |q_l| <= 127,
+ *   d = fp32(mx * fp32(1/127)),  s = sum_l v_l (the exact block sum).
+ * A Q4_K row dot over one sub-block j of a block (dsc = d*sc_j, dm = dmin*m_j
+ * as fp32 products, c_l the 4-bit codes) is then
+ *   dsc * d * sum_l c_l q_l  -  dm * s
+ * -- the scale term on the quantised activation, the min term on the exact
+ * one.  x is quantised this way; h = silu(g) u is rounded to fp32 and then
+ * quantised the same way for the down projection.
+ * ------------------------------------------------------------------- */
+
+/* Quantise n (a multiple of 32) fp32 values per 32-value block. */
+void or_act8_quant(const float *v, int n, int8_t *q, float *d, double *s) {
+    for (int b = 0; b < n / 32; ++b) {
+        float mx = 0.f;
+        double sum = 0.0;
+        for (int l = 0; l < 32; ++l) {
+            float a = fabsf(v[32 * b + l]);
+            if (a > mx) mx = a;
+            sum += (double)v[32 * b + l];
+        }
+        float inv = mx > 0.f ? 127.0f / mx : 0.f;
+        for (int l = 0; l < 32; ++l) q[32 * b + l] = (int8_t)nearbyint((double)v[32 * b + l] * (double)inv);
+        d[b] = mx * (1.0f / 127.0f);
+        s[b] = sum;
+    }
+}
+
+/* One Q4_K row of `cols` weights dotted with a quantised activation. */
+static double or_q4k_row_dot_act8(const uint8_t *row_blocks, int cols, const int8_t *q, const float *d,
+                                  const double *s) {
+    double acc = 0.0;
+    for (int b = 0; b < cols / OR_QK; ++b) {
+        const uint8_t *blk = row_blocks + (int64_t)b * OR_BLOCK_BYTES;
+        float dd = (float)or_half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+        float dmin = (float)or_half_to_double((uint16_t)(blk[2] | (blk[3] << 8)));
+        for (int j = 0; j < 8; ++j) {
+            int sc, m;
+            or_q4k_scale_min(blk + 4, j, &sc, &m);
+            float dsc = dd * (float)sc, dm = dmin * (float)m;
+            int64_t isum = 0;
+            for (int l = 0; l < 32; ++l) {
+                uint8_t byte = blk[16 + 32 * (j / 2) + l];
+                int c = (j & 1) ? (byte >> 4) : (byte & 15);
+                isum += (int64_t)c * q[b * OR_QK + 32 * j + l];
+            }
+            int sb = b * 8 + j;
+            acc += (double)dsc * (double)d[sb] * (double)isum - (double)dm * s[sb];
+        }
+    }
+    return acc;
+}
+
+/* One Q4_K expert's FFN in the int8-activation mode (x: the exact activation
+ * as fp64, converted to fp32 for the quantisation -- bf16 inputs are exact). */
+void or_expert_ffn_act8(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd, int H, int I,
+                        const double *x, double *h_out, double *y) {
+    float *xf = (float *)malloc(sizeof(float) * (size_t)H);
+    int8_t *xq = (int8_t *)malloc((size_t)H);
+    float *xd = (float *)malloc(sizeof(float) * (size_t)(H / 32));
+    double *xs = (double *)malloc(sizeof(double) * (size_t)(H / 32));
+    float *hf = (float *)malloc(sizeof(float) * (size_t)I);
+    int8_t *hq = (int8_t *)malloc((size_t)I);
+    float *hd = (float *)malloc(sizeof(float) * (size_t)(I / 32));
+    double *hs = (double *)malloc(sizeof(double) * (size_t)(I / 32));
+    int64_t gate_row_bytes = (int64_t)(H / OR_QK) * OR_BLOCK_BYTES;
+    int64_t down_row_bytes = (int64_t)(I / OR_QK) * OR_BLOCK_BYTES;
+    for (int c = 0; c < H; ++c) xf[c] = (float)x[c];
+    or_act8_quant(xf, H, xq, xd, xs);
+    for (int r = 0; r < I; ++r) {
+        double g = or_q4k_row_dot_act8(wg + r * gate_row_bytes, H, xq, xd, xs);
+        double u = or_q4k_row_dot_act8(wu + r * gate_row_bytes, H, xq, xd, xs);
+        double h = or_silu(g) * u;
+        if (h_out) h_out[r] = h;
+        hf[r] = (float)h;
+    }
+    or_act8_quant(hf, I, hq, hd, hs);
+    for (int c = 0; c < H; ++c) y[c] = or_q4k_row_dot_act8(wd + c * down_row_bytes, I, hq, hd, hs);
+    free(xf);
+    free(xq);
+    free(xd);
+    free(xs);
+    free(hf);
+    free(hq);
+    free(hd);
+    free(hs);
+}
+
+/* The MoE FFN for one token in the int8-activation mode: the routing of
+ * or_moe_token (exact logits), the experts by or_expert_ffn_act8. */
+void or_moe_token_act8(const uint8_t *w_gate, const uint8_t *w_up, const uint8_t *w_down, const float *router_w,
+                       const float *bias, int H, int I, int E, int k, const uint16_t *x_bf16, int32_t *ids,
+                       double *w, double *out64) {
+    double *x = (double *)malloc(sizeof(double) * (size_t)H);
+    double *y = (double *)malloc(sizeof(double) * (size_t)H);
+    for (int c = 0; c < H; ++c) {
+        x[c] = or_bf16_to_double(x_bf16[c]);
+        out64[c] = 0.0;
+    }
+    or_route_tokens(router_w, bias, x_bf16, 1, E, H, k, ids, w, NULL, NULL);
+    int64_t gate_expert_bytes = (int64_t)I * (H / OR_QK) * OR_BLOCK_BYTES;
+    int64_t down_expert_bytes = (int64_t)H * (I / OR_QK) * OR_BLOCK_BYTES;
+    for (int i = 0; i < k; ++i) {
+        int e = ids[i];
+        or_expert_ffn_act8(w_gate + e * gate_expert_bytes, w_up + e * gate_expert_bytes,
+                           w_down + e * down_expert_bytes, H, I, x, NULL, y);
+        for (int c = 0; c < H; ++c) out64[c] += w[i] * y[c];
+    }
+    free(x);
+    free(y);
+}

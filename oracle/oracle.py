@@ -82,6 +82,12 @@ def _load():
                                                  _c_f64p, _c_f64p]
             lib.or_counts_offsets_perm.argtypes = [_c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    _c_i32p, _c_i32p, _c_i32p]
+            _c_i8p = ctypes.POINTER(ctypes.c_int8)
+            lib.or_act8_quant.argtypes = [_c_f32p, ctypes.c_int, _c_i8p, _c_f32p, _c_f64p]
+            lib.or_expert_ffn_act8.argtypes = [_c_u8p, _c_u8p, _c_u8p, ctypes.c_int, ctypes.c_int, _c_f64p,
+                                               _c_f64p, _c_f64p]
+            lib.or_moe_token_act8.argtypes = [_c_u8p, _c_u8p, _c_u8p, _c_f32p, _c_f32p, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, _c_u16p, _c_i32p, _c_f64p, _c_f64p]
             _lib = lib
     return _lib
 
@@ -316,4 +322,48 @@ __all__ = [
     "WTYPE_Q4_K", "WTYPE_NVFP4", "e2m1_to_double", "e4m3_to_double", "nvfp4_dequant",
     "router_logits", "topk", "renorm_weights", "route_tokens", "expert_ffn", "moe_token",
     "TokenResult", "counts_offsets_perm", "rmsnorm", "moe_token_prenorm", "PrenormResult", "route_tokens_prenorm",
+    "act8_quant", "expert_ffn_act8", "moe_token_act8",
 ]
+
+
+# ----------------------------------------------------------------- int8-activation mode
+def act8_quant(v32: np.ndarray):
+    """Quantise fp32 values (a multiple of 32 of them) per 32-value block:
+    (q int8 [n], d fp32 [n/32], s fp64 [n/32]) -- see oracle.c, int8-activation mode."""
+    v = np.ascontiguousarray(v32, dtype=np.float32)
+    n = v.size
+    assert n % 32 == 0
+    q = np.empty(n, dtype=np.int8)
+    d = np.empty(n // 32, dtype=np.float32)
+    s = np.empty(n // 32, dtype=np.float64)
+    _load().or_act8_quant(_ptr(v, _c_f32p), n, q.ctypes.data_as(ctypes.POINTER(ctypes.c_int8)), _ptr(d, _c_f32p),
+                          _ptr(s, _c_f64p))
+    return q, d, s
+
+
+def expert_ffn_act8(wg_e, wu_e, wd_e, x64, H, I):
+    """One Q4_K expert's FFN in the int8-activation mode: (h [I], y [H]) in fp64."""
+    g = np.ascontiguousarray(wg_e, dtype=np.uint8)
+    u = np.ascontiguousarray(wu_e, dtype=np.uint8)
+    d = np.ascontiguousarray(wd_e, dtype=np.uint8)
+    x = np.ascontiguousarray(x64, dtype=np.float64)
+    h = np.empty(I, dtype=np.float64)
+    y = np.empty(H, dtype=np.float64)
+    _load().or_expert_ffn_act8(_ptr(g, _c_u8p), _ptr(u, _c_u8p), _ptr(d, _c_u8p), H, I, _ptr(x, _c_f64p),
+                               _ptr(h, _c_f64p), _ptr(y, _c_f64p))
+    return h, y
+
+
+def moe_token_act8(layer, x_bf16_row):
+    """The MoE FFN of one token in the int8-activation mode (Q4_K layers): (ids, w, out64)."""
+    s = layer.shape
+    H, I, E, k = s.hidden, s.intermediate, s.n_experts, s.top_k
+    x = np.ascontiguousarray(x_bf16_row, dtype=np.uint16)
+    ids = np.empty(k, dtype=np.int32)
+    w = np.empty(k, dtype=np.float64)
+    out64 = np.empty(H, dtype=np.float64)
+    bias = None if layer.router_bias is None else np.ascontiguousarray(layer.router_bias, dtype=np.float32)
+    _load().or_moe_token_act8(_ptr(layer.w_gate, _c_u8p), _ptr(layer.w_up, _c_u8p), _ptr(layer.w_down, _c_u8p),
+                              _ptr(layer.router_w, _c_f32p), _ptr(bias, _c_f32p), H, I, E, k, _ptr(x, _c_u16p),
+                              _ptr(ids, _c_i32p), _ptr(w, _c_f64p), _ptr(out64, _c_f64p))
+    return ids, w, out64

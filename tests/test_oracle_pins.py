@@ -575,3 +575,116 @@ def test_nvfp4_identical_experts_reduce_to_one_expert(oracle_lib):
         _, y = oracle.expert_ffn(layer.w_gate[0], layer.w_up[0], layer.w_down[0], x, 256, 256,
                                  wtype=oracle.WTYPE_NVFP4, gscales=layer.gscale[0])
         np.testing.assert_allclose(res.out64, y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
+
+
+# ----------------------------------------------------------------- int8-activation mode
+def _rne(fr: Fraction) -> int:
+    """Round a rational to the nearest integer, ties to even."""
+    fl = fr.numerator // fr.denominator
+    rem = fr - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        return fl + 1
+    return fl
+
+
+def test_act8_quant_rules(oracle_lib):
+    g = np.random.default_rng(81)
+    v = (g.standard_normal(32 * 40) * np.exp(g.uniform(-6, 6, 32 * 40))).astype(np.float32)
+    v[32 * 3:32 * 4] = 0.0                       # an all-zero block
+    v[32 * 5:32 * 6] = np.float32(-1e-3)         # a constant negative block
+    v[32 * 7:32 * 8] = np.array([127.0] + [2.5, 3.5, -4.5, 0.5, -0.5, 1.5, -1.5] + [0.0] * 24, dtype=np.float32)
+    q, d, s = oracle.act8_quant(v)
+    for b in range(40):
+        blk = v[32 * b:32 * b + 32]
+        mx = np.float32(np.abs(blk).max())
+        assert d[b] == np.float32(mx * np.float32(1.0 / 127.0))
+        assert s[b] == sum(Fraction(float(t)) for t in blk)  # the exact sum (32 fp32 values fit in fp64 here)
+        if mx == 0:
+            assert not q[32 * b:32 * b + 32].any()
+            continue
+        inv = np.float32(127.0) / mx                 # fp32 division, correctly rounded
+        want = [_rne(Fraction(float(t)) * Fraction(float(inv))) for t in blk]
+        assert list(q[32 * b:32 * b + 32]) == want
+        assert abs(int(q[32 * b + int(np.argmax(np.abs(blk)))])) == 127
+        # reconstruction error within half a step (plus the rounding of inv)
+        err = np.abs(blk.astype(np.float64) - float(d[b]) * q[32 * b:32 * b + 32])
+        assert err.max() <= 0.5 * float(d[b]) * (1 + 1e-6) + 127 * float(d[b]) * 2e-7
+    # ties go to the even integer (inv == 1 exactly in block 7)
+    assert list(q[32 * 7:32 * 7 + 8]) == [127, 2, 4, -4, 0, 0, 2, -2]
+    assert list(q[32 * 5:32 * 5 + 32]) == [-127] * 32
+
+
+def _subblock_dm_dsc(blocks: np.ndarray):
+    """(dsc, dm) of every 32-weight sub-block of Q4_K blocks [n][144], as fp32 products."""
+    n = blocks.shape[0]
+    dsc = np.empty((n, 8), dtype=np.float32)
+    dm = np.empty((n, 8), dtype=np.float32)
+    for i in range(n):
+        dd = np.float32(oracle.half_to_double(int(blocks[i, 0]) | (int(blocks[i, 1]) << 8)))
+        dmin = np.float32(oracle.half_to_double(int(blocks[i, 2]) | (int(blocks[i, 3]) << 8)))
+        for j in range(8):
+            sc, m = oracle.q4k_scale_min(blocks[i, 4:16], j)
+            dsc[i, j] = dd * np.float32(sc)
+            dm[i, j] = dmin * np.float32(m)
+    return dsc, dm
+
+
+def _act8_dot_dense(W, dm_rows, qv, dv, sv):
+    """Rows of W (exact weights) against the quantised activation: the scale term
+    on d*q and the min term on the exact block sums, written as the dense product
+    with the quantised activation plus the min-term correction."""
+    xhat = np.repeat(dv.astype(np.float64), 32) * qv.astype(np.float64)
+    corr = dm_rows.astype(np.float64) @ (np.add.reduceat(xhat, np.arange(0, xhat.size, 32)) - sv)
+    return W @ xhat + corr
+
+
+def _q4k_w64(blocks: np.ndarray, rows: int):
+    """Weights of Q4_K blocks [n][144] as fp64 dsc*c - dm (no rounding to fp32),
+    the codes c read from the nibbles: qs[32i + l] = weight l of sub-blocks 2i
+    (low nibble) and 2i+1 (high nibble)."""
+    dsc, dm = _subblock_dm_dsc(blocks)
+    qs = blocks[:, 16:].reshape(-1, 4, 32)
+    codes = np.stack([qs & 15, qs >> 4], axis=2).reshape(-1, 8, 32).astype(np.float64)
+    w = dsc.astype(np.float64)[:, :, None] * codes - dm.astype(np.float64)[:, :, None]
+    return w.reshape(rows, -1), dm.reshape(rows, -1)
+
+
+@pytest.mark.parametrize("H,I", [(256, 256), (512, 768)])
+def test_act8_expert_ffn_matches_dense_rewrite(oracle_lib, H, I):
+    shape = synth.MoeShape(H, I, 2, 1)
+    layer = synth.make_layer(shape, seed=H + I)
+    x = synth.make_tokens(shape, seed=5, n_tokens=1)[0]
+    x64 = np.array([oracle.bf16_to_double(int(b)) for b in x])
+    h, y = oracle.expert_ffn_act8(layer.w_gate[1], layer.w_up[1], layer.w_down[1], x64, H, I)
+    # the same steps from pinned pieces: dense fp64 weights (before their fp32
+    # rounding, which the mode does not take), the quantiser, per-sub-block dm
+    Wg, dmg = _q4k_w64(np.asarray(layer.w_gate[1]).reshape(-1, 144), I)
+    Wu, dmu = _q4k_w64(np.asarray(layer.w_up[1]).reshape(-1, 144), I)
+    Wd, dmd = _q4k_w64(np.asarray(layer.w_down[1]).reshape(-1, 144), H)
+    # those fp64 weights round to the oracle's fp32 ones
+    assert np.array_equal(Wg.astype(np.float32).ravel(), oracle.q4k_dequant(layer.w_gate[1]))
+    qx, dx, sx = oracle.act8_quant(x64.astype(np.float32))
+    g = _act8_dot_dense(Wg, dmg, qx, dx, sx)
+    u = _act8_dot_dense(Wu, dmu, qx, dx, sx)
+    hh = g * scipy.special.expit(g) * u
+    np.testing.assert_allclose(h, hh, rtol=1e-9, atol=1e-12 * np.abs(hh).max())
+    qh, dh, shh = oracle.act8_quant(h.astype(np.float32))
+    yy = _act8_dot_dense(Wd, dmd, qh, dh, shh)
+    np.testing.assert_allclose(y, yy, rtol=1e-9, atol=1e-12 * np.abs(yy).max())
+
+
+def test_act8_mode_error_against_the_exact_block(oracle_lib):
+    """The approximation itself: same routing, output within about 1e-2 rel-L2 on
+    these tokens (a token whose h has a large outlier in some 32-column block
+    can reach several 1e-2 on larger layers; the mode is reported separately)."""
+    shape = synth.MoeShape(512, 256, 8, 2)
+    layer = synth.make_layer(shape, seed=33)
+    xs = synth.make_tokens(shape, seed=33, n_tokens=4)
+    errs = []
+    for t in range(4):
+        ids, w, out = oracle.moe_token_act8(layer, xs[t])
+        ref = oracle.moe_token(layer, xs[t])
+        assert np.array_equal(ids, ref.ids)
+        np.testing.assert_allclose(w, ref.w, rtol=1e-12)
+        errs.append(np.linalg.norm(out - ref.out64) / np.linalg.norm(ref.out64))
+    assert 1e-4 < max(errs) < 3e-2
