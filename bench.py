@@ -18,8 +18,8 @@ region, an end-to-end figure with host<->device copies in the timed
 region, the CPU oracle's throughput on a bounded sample, and (unless
 --no-extras) the 48-layer stack, the 4-token deduplicated workload, the
 headline workload as a pre-normed block, the 4096-token grouped prefill
-with its tensor-core roofline, and the headline decode and the prefill with
-NVFP4 experts.
+with its tensor-core roofline, the headline decode and the prefill with
+NVFP4 experts, and the headline decode in the int8-activation mode.
 
 --impl reference times the CPU oracle (the reference implementation of the
 method) on a bounded sample of the same workload on the host cores.
@@ -85,7 +85,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extras", action="store_true",
-                   help="skip the stack, dedup, pre-normed, prefill and NVFP4 workloads")
+                   help="skip the stack, dedup, pre-normed, prefill, NVFP4 and int8-activation workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--tokens", type=int, default=0,
                    help="tokens per step of the headline layer (default 1024; small values for ncu)")
@@ -583,6 +583,39 @@ def bench_nvfp4(args, dist, binding, device, synth, torch, hbm_peak):
             "gpu_launches": {2: 2, 1: 2}.get(path, 3) * T * steps}
 
 
+def bench_act8(args, dist, binding, device, synth, torch, hbm_peak):
+    """The headline decode workload (1024 sequential single-token calls in one
+    CUDA graph) in the int8-activation mode (SI_FLAG_ACT_INT8: x and h int8
+    per 32 columns, dp4a).  An approximation with its own tolerance, measured
+    by tests/test_gpu_act8.py against the exact block; this entry times it."""
+    wl = synth.WORKLOADS["layer"]
+    shape, seed, T = wl["shape"], wl["seed"], 1024
+    layer = synth.make_layer(shape, seed=seed)
+    dl = device.to_device(layer)
+    plan = binding.si_moe_plan(device.desc_for(shape, flags=binding.SI_FLAG_ACT_INT8), torch.cuda.current_device())
+    scratch = device.alloc_scratch(plan, binding.SI_MODE_DECODE, 1)
+    x = device.tokens_to_device(synth.make_tokens(shape, seed, T))
+    out = torch.empty((T, shape.hidden), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    g = build_layer_graph(binding, plan, dl.struct(), [x[t] for t in range(T)], [out[t] for t in range(T)],
+                          scratch, stream)
+    steps = max(1, args.steps // 2)
+    ms, clocks = time_graph(g, stream, steps, args.warmup, dist, ClockSampler(torch.cuda.current_device()))
+    st = binding.si_moe_read_status(plan, scratch, stream)
+    assert st == binding.SI_OK, binding.si_status_string(st)
+    tok_s = T * steps / (ms / 1e3)
+    expert_bytes = shape.top_k * shape.expert_bytes
+    gbs = expert_bytes * tok_s / 1e9
+    path = binding.si_debug_decode_fused(plan, 1)
+    del g
+    return {"workload": "qwen3-30b-a3b-moe-layer-decode-bs1, int8 activations per 32 columns (approximate mode), "
+                        "1024 tokens",
+            "dtype": "q4k-w x int8-act (per 32 columns) -> fp32 accumulate",
+            "tok_per_s": dist.sum(tok_s), "us_per_token": 1e6 / tok_s, "expert_bytes_per_token": expert_bytes,
+            "achieved_gbs": gbs, "frac_of_peak": gbs / hbm_peak, "clocks": clocks,
+            "gpu_launches": {2: 2, 1: 2}.get(path, 3) * T * steps}
+
+
 def tensor_peak():
     """Dense 16-bit tensor-core peak (TFLOP/s): the measured bf16 GEMM figure
     (fp16 has the same dense rate on this part)."""
@@ -712,6 +745,11 @@ def run_ours(args, dist):
             line["nvfp4"]["prefill"] = bench_prefill(args, dist, binding, device, synth, torch, nvfp4=True)
         except Exception as exc:
             line["nvfp4"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+        try:
+            line["act8"] = bench_act8(args, dist, binding, device, synth, torch, hbm_peak)
+        except Exception as exc:
+            line["act8"] = {"error": repr(exc)}
     # two-sided guard: an achieved fraction of a measured peak above 1.0 means the timed
     # region did not do the work it is credited with
     fracs = {"roofline": line["roofline"].get("frac"), "chain": line.get("chain", {}).get("frac_of_peak")}

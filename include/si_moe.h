@@ -73,6 +73,19 @@ typedef enum si_status {
 
 #define SI_WTYPE_Q4_K 12          /* GGUF's type id of Q4_K */
 #define SI_WTYPE_NVFP4 100        /* NVFP4 super-blocks (see si_moe_layer.w_scale) */
+/* si_moe_desc.flags: int8-activation mode of single-token decode (the dp4a
+ * matrix-vector product on quantised weights that the sparkinfer README's
+ * "Milestone 1" plans, with each activation vector quantised once).  x and h are quantised to int8 per 32
+ * columns (q = round-half-even(v * 127/max|v|), scale max|v|/127) and dotted
+ * with the 4-bit codes by dp4a; the Q4_K min term uses the exact 32-column
+ * sums.  An approximation with its own, looser tolerance (measured against
+ * the exact block: about 1e-3 .. 1e-2 rel-L2 per token on synthetic layers,
+ * several 1e-2 for a token whose h has an outlier in some 32-column block),
+ * reported separately from the default path.  Q4_K only, not with a
+ * pre-normed block (SI_ERR_UNSUPPORTED).  It applies where single-token
+ * decode runs on the cluster expert kernel (si_debug_decode_fused = 2);
+ * batched decode and prefill keep their precision. */
+#define SI_FLAG_ACT_INT8 1u
 #define SI_MODE_DECODE 0
 #define SI_MODE_PREFILL 1
 #define SI_MAX_EXPERTS 256
@@ -82,7 +95,8 @@ typedef enum si_status {
 /* Layer shape.  hidden and intermediate are multiples of 256 (one Q4_K
  * super-block); 1 <= top_k <= min(n_experts, SI_MAX_TOPK);
  * n_experts <= SI_MAX_EXPERTS; max_tokens bounds the prefill token count.
- * wtype is SI_WTYPE_Q4_K or SI_WTYPE_NVFP4; flags must be 0. */
+ * wtype is SI_WTYPE_Q4_K or SI_WTYPE_NVFP4; flags is 0 or SI_FLAG_ACT_INT8
+ * (other bits: SI_ERR_UNSUPPORTED). */
 typedef struct si_moe_desc {
     int32_t hidden;
     int32_t intermediate;

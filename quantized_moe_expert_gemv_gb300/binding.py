@@ -29,6 +29,7 @@ SI_ERR_DEVICE = 7
 SI_ERR_RANGE = 8
 SI_WTYPE_Q4_K = 12
 SI_WTYPE_NVFP4 = 100
+SI_FLAG_ACT_INT8 = 1
 SI_MODE_DECODE = 0
 SI_MODE_PREFILL = 1
 SI_MAX_EXPERTS = 256

@@ -23,7 +23,9 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 si_status validate_desc(const si_moe_desc *d) {
     if (!d) return SI_ERR_INVALID_ARG;
-    if ((d->wtype != SI_WTYPE_Q4_K && d->wtype != SI_WTYPE_NVFP4) || d->flags != 0) return SI_ERR_UNSUPPORTED;
+    if (d->wtype != SI_WTYPE_Q4_K && d->wtype != SI_WTYPE_NVFP4) return SI_ERR_UNSUPPORTED;
+    if ((d->flags & ~SI_FLAG_ACT_INT8) != 0) return SI_ERR_UNSUPPORTED;
+    if ((d->flags & SI_FLAG_ACT_INT8) && d->wtype != SI_WTYPE_Q4_K) return SI_ERR_UNSUPPORTED;
     if (d->hidden <= 0 || d->intermediate <= 0 || d->hidden % 256 || d->intermediate % 256)
         return SI_ERR_INVALID_ARG;
     if (d->n_experts < 1 || d->n_experts > SI_MAX_EXPERTS) return SI_ERR_INVALID_ARG;
@@ -229,6 +231,7 @@ static si_status check_weight_scales(const si_moe_desc &d, const si_moe_layer *l
     } else if (layer->w_scale) {
         return SI_ERR_INVALID_ARG;
     }
+    if ((d.flags & SI_FLAG_ACT_INT8) && layer->norm_weight) return SI_ERR_UNSUPPORTED;
     return SI_OK;
 }
 

@@ -48,6 +48,50 @@ __device__ __forceinline__ float sumsq8_bf16(const uint4 &xv, float s) {
     return s;
 }
 
+// Chunk c (64 columns) of one token's x, held by a warp as bf16 pairs (lane l:
+// word wv = columns 2l, 2l+1), quantised into the cluster expert kernel's
+// activation record at xq (NC = H/64 chunks): int16 pairs, xq = rint(x / s),
+// s = max|x| / 32767, with the two 32-column sums and the four 16-column sums
+// of xq; or, in the int8-activation mode, int8 per 32 columns with their
+// scales and sums (layouts: kXqWords, kXq8Words).
+__device__ __forceinline__ void router_quant_chunk(uint32_t wv, int c, int NC, uint32_t *xq_p, int lane, bool act8) {
+    const float v0 = __uint_as_float(wv << 16), v1 = __uint_as_float(wv & 0xffff0000u);
+    if (act8) {
+        float d, sum;
+        const uint32_t lo = quant_pair8(v0, v1, &d, &sum);
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, lo, 1);
+        if ((lane & 1) == 0) {  // word lane/2 = columns 2*lane .. 2*lane+3
+            const int w = lane >> 1;
+            reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(xq_p) + xq8_unit_byte(c, w >> 2))[w & 3] =
+                lo | (hi << 16);
+        }
+        float *sc = reinterpret_cast<float *>(xq_p + 16 * NC + 4 * c);
+        if (lane == 0) sc[0] = d, sc[2] = sum;
+        if (lane == 16) sc[1] = d, sc[3] = sum;
+        return;
+    }
+    float mx = fmaxf(fabsf(v0), fabsf(v1));
+    float sum = v0 + v1;  // lanes 0..15: the first 32 columns, 16..31: the second
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
+    const uint32_t q = pack_q16(v0, v1, inv);
+    int s2 = (int)(int16_t)(q & 0xffffu) + ((int)q >> 16);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
+    xq_p[32 * c + 4 * ((lane >> 2) ^ (c & 7)) + (lane & 3)] = q;
+    uint32_t *dst = xq_p + 32 * NC + 8 * c;
+    if (lane == 0) {
+        dst[0] = __float_as_uint(mx * (1.0f / 32767.0f));
+        dst[1] = __float_as_uint(sum);
+    }
+    if (lane == 16) dst[2] = __float_as_uint(sum);
+    if ((lane & 7) == 0) dst[3 + (lane >> 3)] = (uint32_t)s2;
+}
+
 // Router + top-k, one thread-block cluster (or one CTA for small E).  NORM (a
 // pre-normed block): the router rows are scaled by the RMSNorm gain in
 // registers and each warp scales its logit by the token's 1 / rms.  Warp
@@ -229,30 +273,9 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
     if (early_dependents) {
         const uint32_t *xw32 = NJ > 0 ? reinterpret_cast<const uint32_t *>(s_x) : reinterpret_cast<const uint32_t *>(xg_p);
         const int NC = H / 64;
-        for (int c = blockIdx.x + gridDim.x * warp; c < NC; c += gridDim.x * wpc) {
-            const uint32_t wv = xw32[32 * c + lane];  // columns 2*lane, 2*lane + 1 of chunk c
-            const float v0 = __uint_as_float(wv << 16), v1 = __uint_as_float(wv & 0xffff0000u);
-            float mx = fmaxf(fabsf(v0), fabsf(v1));
-            float sum = v0 + v1;  // lanes 0..15: the first 32 columns, 16..31: the second
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
-            const uint32_t q = pack_q16(v0, v1, inv);
-            int s2 = (int)(int16_t)(q & 0xffffu) + ((int)q >> 16);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
-            xq_p[32 * c + 4 * ((lane >> 2) ^ (c & 7)) + (lane & 3)] = q;
-            uint32_t *dst = xq_p + 32 * NC + 8 * c;
-            if (lane == 0) {
-                dst[0] = __float_as_uint(mx * (1.0f / 32767.0f));
-                dst[1] = __float_as_uint(sum);
-            }
-            if (lane == 16) dst[2] = __float_as_uint(sum);
-            if ((lane & 7) == 0) dst[3 + (lane >> 3)] = (uint32_t)s2;
-        }
+        const bool act8 = pin_i32(a.act8) != 0;
+        for (int c = blockIdx.x + gridDim.x * warp; c < NC; c += gridDim.x * wpc)
+            router_quant_chunk(xw32[32 * c + lane], c, NC, xq_p, lane, act8);
     }
     if (zsa) {
         if (e >= E) cluster_wait();  // warps without an expert still take the cluster barrier
@@ -404,9 +427,9 @@ __device__ __forceinline__ void gateup_rowpair(const DecodeArgs &a, const float 
             }
         }
     }
-#pragma unroll
     const float tsg = a.wtype == SI_WTYPE_NVFP4 ? a.wscale[3 * e] : 1.f;
     const float tsu = a.wtype == SI_WTYPE_NVFP4 ? a.wscale[3 * e + 1] : 1.f;
+#pragma unroll
     for (int t = 0; t < NT; ++t) {
         const float gs = tsg * warp_sum(g[t]);
         const float us = tsu * warp_sum(uu[t]);
@@ -688,34 +711,12 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
         if (lane < C) st_async_cluster_u32(&s_z[e], smem_addr(&s_zbar), (uint32_t)lane, __float_as_uint(z));
         if (lane == 0 && ologits_p) ologits_p[e] = z;
     }
-    // x quantised per 64-column chunk for the expert kernel (the layout of k_router_topk)
+    // x quantised per 64-column chunk for the expert kernel (as in k_router_topk)
     {
         const uint32_t *xw32 = reinterpret_cast<const uint32_t *>(xg_p);
         const int NC = H / 64;
-        for (int c = blockIdx.x + C * warp; c < NC; c += C * WPC) {
-            const uint32_t wv = xw32[32 * c + lane];
-            const float v0 = __uint_as_float(wv << 16), v1 = __uint_as_float(wv & 0xffff0000u);
-            float mx = fmaxf(fabsf(v0), fabsf(v1));
-            float sum = v0 + v1;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
-            const uint32_t qw = pack_q16(v0, v1, inv);
-            int s2 = (int)(int16_t)(qw & 0xffffu) + ((int)qw >> 16);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
-            xq_p[32 * c + 4 * ((lane >> 2) ^ (c & 7)) + (lane & 3)] = qw;
-            uint32_t *dst = xq_p + 32 * NC + 8 * c;
-            if (lane == 0) {
-                dst[0] = __float_as_uint(mx * (1.0f / 32767.0f));
-                dst[1] = __float_as_uint(sum);
-            }
-            if (lane == 16) dst[2] = __float_as_uint(sum);
-            if ((lane & 7) == 0) dst[3 + (lane >> 3)] = (uint32_t)s2;
-        }
+        const bool act8 = pin_i32(a.act8) != 0;
+        for (int c = blockIdx.x + C * warp; c < NC; c += C * WPC) router_quant_chunk(xw32[32 * c + lane], c, NC, xq_p, lane, act8);
     }
     if (!mbar_wait_warp_cluster(smem_addr(&s_zbar), 0, a.wait_budget)) set_status(a.ctrl + kCtrlStatus, SI_ERR_TIMEOUT);
     // warp q ranks expert e0 + q against all E logits (greater, or equal with a
@@ -796,6 +797,7 @@ cudaError_t launch_decode(const Plan &p, const DecodeArgs &a_in, cudaStream_t s,
         a.n == 1 && p.cluster_ok && expert_cluster_layout(p.desc, p.cluster_size, p.smem_optin, a);
     a.zero_out = cluster ? 1 : 0;
     a.sel_logits = cluster ? 1 : 0;
+    a.act8 = cluster && (p.desc.flags & SI_FLAG_ACT_INT8) ? 1 : 0;  // the other decode paths keep their precision
     cudaError_t err = mark(events, 0, s);
     if (err != cudaSuccess) return err;
     err = launch_router(a, s);

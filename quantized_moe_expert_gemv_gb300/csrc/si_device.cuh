@@ -562,6 +562,59 @@ __device__ __forceinline__ ChunkScalesI chunk_scales_i(const uint4 &hdr, int i) 
     return s;
 }
 
+// int8-activation mode.  Unsigned bytes (a) times signed bytes (b), summed into c.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// I_a = sum_l q_lo(l)*xa[l], I_b = sum_l q_hi(l)*xb[l] over one 32-byte chunk
+// (q0, q1) against int8 activations: xw(t) holds columns 4t..4t+3 of
+// sub-block a (t < 8) and of sub-block b (t >= 8, columns 32+4(t-8)..).
+template <typename XW>
+__device__ __forceinline__ int2 chunk_isums8(const uint4 &q0, const uint4 &q1, XW xw) {
+    int a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int t = 0; t < 8; t += 2) {
+        a0 = dp4a_us(w[t] & 0x0f0f0f0fu, xw(t), a0);
+        b0 = dp4a_us(w[t] & 0xf0f0f0f0u, xw(8 + t), b0);  // 16 x the codes of sub-block b
+        a1 = dp4a_us(w[t + 1] & 0x0f0f0f0fu, xw(t + 1), a1);
+        b1 = dp4a_us(w[t + 1] & 0xf0f0f0f0u, xw(9 + t), b1);
+    }
+    return make_int2(a0 + a1, (b0 + b1) >> 4);  // b sums are exact multiples of 16
+}
+
+// d*(sc_a*da*I_a + sc_b*db*I_b) - dmin*(m_a*Xa + m_b*Xb): the scale term on the
+// int8 activations (scales da, db), the min term on the exact sums Xa, Xb.
+__device__ __forceinline__ float chunk_contrib_i8(const ChunkScalesI &c, int2 I, float da, float db, float Xa,
+                                                  float Xb) {
+    const float s = fmaf((float)c.sca * da, (float)I.x, (float)c.scb * db * (float)I.y);
+    return fmaf(c.d, s, -c.dmin * fmaf((float)c.ma, Xa, (float)c.mb * Xb));
+}
+
+// One 64-column chunk held by a warp as lane pairs (lane l: columns 2l, 2l+1)
+// quantised per 32 columns to int8: q = rint(v * 127/mx) (the product rounded
+// once), scale mx * (1/127).  Returns this lane's two codes as the low 16 bits
+// (column 2l in the low byte); on return lane 0 holds (scale, sum) of columns
+// 0..31 and lane 16 of columns 32..63 in *d, *s.
+__device__ __forceinline__ uint32_t quant_pair8(float v0, float v1, float *d, float *s) {
+    float mx = fmaxf(fabsf(v0), fabsf(v1));
+    float sum = v0 + v1;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {  // within each half of the warp (one 32-column block each)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    }
+    const float inv = mx > 0.f ? 127.0f / mx : 0.f;
+    const int q0 = (int)(__float_as_uint(fmaf(v0, inv, 12582912.0f)) & 0xffu);  // low byte of 1.5*2^23 + round(v*inv)
+    const int q1 = (int)(__float_as_uint(fmaf(v1, inv, 12582912.0f)) & 0xffu);
+    *d = mx * (1.0f / 127.0f);
+    *s = sum;
+    return (uint32_t)(q0 | (q1 << 8));
+}
+
 __device__ __forceinline__ float chunk_contrib_i(const ChunkScalesI &c, int2 I, float xs, float Xa, float Xb) {
     const int sc = c.sca * I.x + c.scb * I.y;
     const float mm = fmaf((float)c.ma, Xa, (float)c.mb * Xb);

@@ -89,6 +89,8 @@ __device__ __forceinline__ float pair_sum(float g, float u, int li) {
 // (144-byte super-blocks), a different chunk dot product (si_device.cuh), the
 // activations' 16-column integer sums next to their scale, and the matrices'
 // tensor scales on the gate and up partials and on the combine weight.
+// WF = 2: Q4_K weights in the int8-activation mode (SI_FLAG_ACT_INT8): x (from
+// the router) and h are int8 per 32 columns, dotted with dp4a.
 template <int NBH, bool NORM, int WF>
 __global__ void __launch_bounds__(kClThreads, 1)
     k_expert_cluster(const __grid_constant__ CUtensorMap tmap_down, const __grid_constant__ CUtensorMap tmap_tail,
@@ -99,6 +101,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     constexpr int CH = kCW * RPW * kPairs;  // row pairs per stage
     constexpr int rowg = NBH * kBlockBytes;
     constexpr int stageA = 2 * CH * rowg;
+    constexpr bool FP4 = WF == 1, A8 = WF == 2;
     __shared__ int s_err;
     __shared__ float s_w;
     __shared__ int s_lastA[8];
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const long long budget = (long long)pin_u64((uint64_t)a.wait_budget);
     const int fault_wait = pin_i32(a.fault_wait);
     const int I = pin_i32(a.I), H = pin_i32(a.H);
-    const float *const wsc = WF ? pin_ptr(a.wscale) : nullptr;  // NVFP4 tensor scales [E][3]
+    const float *const wsc = FP4 ? pin_ptr(a.wscale) : nullptr;  // NVFP4 tensor scales [E][3]
     const uint32_t *const xq_g = pin_ptr(a.xq);  // x quantised by the router (plain block)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const uint32_t fullB = emptyA + 8 * NSA;  // all down boxes complete on this one barrier
     const uint32_t hbar = fullB + 8;          // the unit's 256 h values, stored by every CTA of the cluster
     const uint32_t xbar = hbar + 8;           // the router's quantised x (plain block)
-    const uint32_t xq_bytes = (uint32_t)(H / 64) * kXqWords * 4;
+    const uint32_t xq_bytes = (uint32_t)(H / 64) * (A8 ? kXq8Words : kXqWords) * 4;
     int32_t *status = ctrl + kCtrlStatus;
     auto stage_bytes = [&](int j) { return (uint32_t)((min(CH * (j + 1), n_rp) - CH * j) * rowg); };
 
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         xqf[7 * lane] = sc;
         xqf[7 * lane + 1] = sa;
         xqf[7 * lane + 2] = sb;
-        if (WF) {
+        if (FP4) {
             int XQ[4];
             xq_block_sums(wq, XQ);
 #pragma unroll
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
         const float w = ex / den;
-        if (lane == slot) s_w = WF ? w * wsc[3 * ids[slot] + 2] : w;  // NVFP4: times the down tensor scale
+        if (lane == slot) s_w = FP4 ? w * wsc[3 * ids[slot] + 2] : w;  // NVFP4: times the down tensor scale
         if (blockIdx.x == 0 && o_w && lane < k) o_w[lane] = w;
     }
     volatile int *verr = &s_err;
@@ -331,7 +334,21 @@ __global__ void __launch_bounds__(kClThreads, 1)
             }
             xs = xqf[7 * chunk], Xa = xqf[7 * chunk + 1], Xb = xqf[7 * chunk + 2];
 #pragma unroll
-            for (int b4 = 0; b4 < 4; ++b4) XQ[b4] = WF ? reinterpret_cast<const int *>(xqf)[7 * chunk + 3 + b4] : 0;
+            for (int b4 = 0; b4 < 4; ++b4) XQ[b4] = FP4 ? reinterpret_cast<const int *>(xqf)[7 * chunk + 3 + b4] : 0;
+        } else if (A8) {  // int8 per 32 columns, quantised by the router, copied by the producer
+            if (!mbar_wait_warp(xbar, 0, budget)) {
+                set_status(status, SI_ERR_TIMEOUT);
+                *verr = 1;
+            }
+            const uint8_t *xq8 = reinterpret_cast<const uint8_t *>(xq_s);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(xq8 + xq8_unit_byte(chunk, q));
+                xw[4 * q] = v.x, xw[4 * q + 1] = v.y, xw[4 * q + 2] = v.z, xw[4 * q + 3] = v.w;
+            }
+            const float4 f = reinterpret_cast<const float4 *>(xq_s + 16 * (H / 64))[chunk];
+            xs = f.x, XQ[0] = __float_as_int(f.y), Xa = f.z, Xb = f.w;  // da, db (bits), the two sums
+            XQ[1] = XQ[2] = XQ[3] = 0;
         } else {  // quantised by the router, copied by the producer
             if (!mbar_wait_warp(xbar, 0, budget)) {
                 set_status(status, SI_ERR_TIMEOUT);
@@ -351,7 +368,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         auto xwf = [&xw](int p) { return xw[p]; };
         // NVFP4: this unit's expert's gate and up tensor scales
         float tsg = 1.f, tsu = 1.f;
-        if (WF) {
+        if (FP4) {
             const int eu = ids[slot];
             tsg = wsc[3 * eu];
             tsu = wsc[3 * eu + 1];
@@ -387,9 +404,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
                     const uint8_t *urow = grow + CH * rowg;
                     const uint4 hg = ld_s128(grow), qg0 = ld_s128(grow + 16 + 32 * i), qg1 = ld_s128(grow + 32 + 32 * i);
                     const uint4 hu = ld_s128(urow), qu0 = ld_s128(urow + 16 + 32 * i), qu1 = ld_s128(urow + 32 + 32 * i);
-                    if (WF) {
+                    if (FP4) {
                         part[2 * m] = tsg * chunk_contrib_nvfp4(hg, i, qg0, qg1, xwf, xs, XQ);
                         part[2 * m + 1] = tsu * chunk_contrib_nvfp4(hu, i, qu0, qu1, xwf, xs, XQ);
+                    } else if (A8) {
+                        const float db = __int_as_float(XQ[0]);
+                        part[2 * m] = chunk_contrib_i8(chunk_scales_i(hg, i), chunk_isums8(qg0, qg1, xwf), xs, db, Xa, Xb);
+                        part[2 * m + 1] = chunk_contrib_i8(chunk_scales_i(hu, i), chunk_isums8(qu0, qu1, xwf), xs, db, Xa, Xb);
                     } else {
                         part[2 * m] = chunk_contrib_i(chunk_scales_i(hg, i), chunk_isums(qg0, qg1, xwf), xs, Xa, Xb);
                         part[2 * m + 1] = chunk_contrib_i(chunk_scales_i(hu, i), chunk_isums(qu0, qu1, xwf), xs, Xa, Xb);
@@ -425,7 +446,20 @@ __global__ void __launch_bounds__(kClThreads, 1)
     uint32_t *hq = xq_s;  // reuse: [4][32] words (the same unit swizzle) + [4][7]
     float *hqf = reinterpret_cast<float *>(hq + 128);
     if (warp < kCW && !skip) {
-        if (warp < 4) {  // the unit's four 64-column chunks of h: warp c quantises chunk c
+        if (A8 && warp < 4) {  // int8 per 32 columns, the layout of the router's x (kXq8Words)
+            const float2 v = reinterpret_cast<const float2 *>(hslice + 64 * warp)[lane];  // columns 2l, 2l+1
+            float d, sum;
+            const uint32_t lo = quant_pair8(v.x, v.y, &d, &sum);
+            const uint32_t hi = __shfl_down_sync(0xffffffffu, lo, 1);
+            if ((lane & 1) == 0) {
+                const int w = lane >> 1;
+                reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(hq) + xq8_unit_byte(warp, w >> 2))[w & 3] =
+                    lo | (hi << 16);
+            }
+            float *sc = reinterpret_cast<float *>(hq + 16 * 4) + 4 * warp;
+            if (lane == 0) sc[0] = d, sc[2] = sum;
+            if (lane == 16) sc[1] = d, sc[3] = sum;
+        } else if (warp < 4) {  // the unit's four 64-column chunks of h: warp c quantises chunk c
             const float2 v = reinterpret_cast<const float2 *>(hslice + 64 * warp)[lane];  // columns 2l, 2l+1
             float mx = fmaxf(fabsf(v.x), fabsf(v.y));
             float sum = v.x + v.y;  // lanes 0..15: sub-block a, 16..31: sub-block b
@@ -440,7 +474,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 hqf[7 * warp + 1] = sum;
             }
             if (lane == 16) hqf[7 * warp + 2] = sum;
-            if (WF) {  // integer sums of the quantised h over 16-column blocks (8 lanes each)
+            if (FP4) {  // integer sums of the quantised h over 16-column blocks (8 lanes each)
                 const uint32_t wq2 = pack_q16(v.x, v.y, inv);
                 int s2 = (int)(int16_t)(wq2 & 0xffffu) + ((int)wq2 >> 16);
                 s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
@@ -454,15 +488,26 @@ __global__ void __launch_bounds__(kClThreads, 1)
     if (warp < kCW && !skip) {
         const int r8 = lane >> 2, i = lane & 3;
         uint32_t hw[32];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const uint4 v = reinterpret_cast<const uint4 *>(hq + 32 * i)[q ^ i];
-            hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
-        }
-        const float hs = hqf[7 * i], Ha = hqf[7 * i + 1], Hb = hqf[7 * i + 2];
+        float hs, Ha, Hb, hdb = 0.f;
         int HQ[4];
+        if (A8) {
 #pragma unroll
-        for (int b4 = 0; b4 < 4; ++b4) HQ[b4] = WF ? reinterpret_cast<const int *>(hqf)[7 * i + 3 + b4] : 0;
+            for (int q = 0; q < 4; ++q) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(hq) + xq8_unit_byte(i, q));
+                hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
+            }
+            const float4 f = reinterpret_cast<const float4 *>(hq + 16 * 4)[i];
+            hs = f.x, hdb = f.y, Ha = f.z, Hb = f.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint4 v = reinterpret_cast<const uint4 *>(hq + 32 * i)[q ^ i];
+                hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
+            }
+            hs = hqf[7 * i], Ha = hqf[7 * i + 1], Hb = hqf[7 * i + 2];
+        }
+#pragma unroll
+        for (int b4 = 0; b4 < 4; ++b4) HQ[b4] = FP4 ? reinterpret_cast<const int *>(hqf)[7 * i + 3 + b4] : 0;
         auto hwf = [&hw](int p) { return hw[p]; };
         // box m holds rows [128m, 128m + 128) = the rows of iteration m; every box
         // completes on one barrier (they land while gate/up is computed), rows past
@@ -479,8 +524,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
             if (lr < n_rows) {
                 const uint8_t *blk = stB + (size_t)m * box_stride + (size_t)(8 * warp + r8) * kBlockBytes;
                 const uint4 hd = ld_s128(blk), q0 = ld_s128(blk + 16 + 32 * i), q1 = ld_s128(blk + 32 + 32 * i);
-                v = WF ? chunk_contrib_nvfp4(hd, i, q0, q1, hwf, hs, HQ)
-                       : chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums(q0, q1, hwf), hs, Ha, Hb);
+                v = FP4  ? chunk_contrib_nvfp4(hd, i, q0, q1, hwf, hs, HQ)
+                    : A8 ? chunk_contrib_i8(chunk_scales_i(hd, i), chunk_isums8(q0, q1, hwf), hs, hdb, Ha, Hb)
+                         : chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums(q0, q1, hwf), hs, Ha, Hb);
             }
             v += __shfl_xor_sync(0xffffffffu, v, 1);
             v += __shfl_xor_sync(0xffffffffu, v, 2);
@@ -591,6 +637,7 @@ static cudaError_t launch_cluster_t(const DecodeArgs &a, const CUtensorMap &tm, 
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (a.wtype == SI_WTYPE_NVFP4) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 1>, tm, tt, a);
+    if (a.act8) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 2>, tm, tt, a);
     return a.norm_w ? cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, true, 0>, tm, tt, a)
                     : cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 0>, tm, tt, a);
 }
@@ -610,16 +657,16 @@ cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s) {
 cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters) {
     *active_clusters = 0;
     if (!tensor_map_encoder()) return cudaErrorNotSupported;  // down blocks are fetched by a tensor map
-    const void *fs[3] = {nullptr, nullptr, nullptr};  // plain and pre-normed Q4_K block, NVFP4
+    const void *fs[4] = {nullptr, nullptr, nullptr, nullptr};  // plain and pre-normed Q4_K block, NVFP4, int8 activations
     switch (nbh) {
         case 1: fs[0] = (const void *)k_expert_cluster<1, false, 0>, fs[1] = (const void *)k_expert_cluster<1, true, 0>,
-                fs[2] = (const void *)k_expert_cluster<1, false, 1>; break;
+                fs[2] = (const void *)k_expert_cluster<1, false, 1>, fs[3] = (const void *)k_expert_cluster<1, false, 2>; break;
         case 2: fs[0] = (const void *)k_expert_cluster<2, false, 0>, fs[1] = (const void *)k_expert_cluster<2, true, 0>,
-                fs[2] = (const void *)k_expert_cluster<2, false, 1>; break;
+                fs[2] = (const void *)k_expert_cluster<2, false, 1>, fs[3] = (const void *)k_expert_cluster<2, false, 2>; break;
         case 4: fs[0] = (const void *)k_expert_cluster<4, false, 0>, fs[1] = (const void *)k_expert_cluster<4, true, 0>,
-                fs[2] = (const void *)k_expert_cluster<4, false, 1>; break;
+                fs[2] = (const void *)k_expert_cluster<4, false, 1>, fs[3] = (const void *)k_expert_cluster<4, false, 2>; break;
         default: fs[0] = (const void *)k_expert_cluster<8, false, 0>, fs[1] = (const void *)k_expert_cluster<8, true, 0>,
-                 fs[2] = (const void *)k_expert_cluster<8, false, 1>; break;
+                 fs[2] = (const void *)k_expert_cluster<8, false, 1>, fs[3] = (const void *)k_expert_cluster<8, false, 2>; break;
     }
     int least = 1 << 30;
     for (const void *f : fs) {  // every variant must fit; the smallest resident count counts

@@ -24,6 +24,12 @@ constexpr size_t kCtrlBytes = kCtrlWords * sizeof(int32_t);
 // stored at unit q ^ (c & 7); then 8 words per chunk: the scale, the two
 // 32-column sums (fp32 bits), four 16-column integer sums and a pad.
 constexpr int kXqWords = 40;
+// int8-activation mode: 20*NC words: first the int8 codes, 16 words per chunk,
+// chunk c's 16-byte unit q (4 bytes = 4 columns per word) at byte
+// 128*(c/2) + 16*((4*(c%2) + q) ^ ((c/2) % 8)); then 4 words per chunk: the
+// two 32-column scales and the two 32-column sums (fp32 bits).
+constexpr int kXq8Words = 20;
+__host__ __device__ constexpr int xq8_unit_byte(int c, int q) { return 128 * (c >> 1) + 16 * ((4 * (c & 1) + q) ^ ((c >> 1) & 7)); }
 constexpr int kMaxSlots = SI_MAX_DECODE_TOKENS * SI_MAX_TOPK;  // 64
 
 // Table of the distinct experts of one decode call (all int32).
@@ -93,6 +99,7 @@ struct DecodeArgs {
     int cl_off_a, cl_off_b, cl_off_h, cl_off_x, cl_off_y, cl_off_bar;
     int cl_nsa, cl_C, cl_tail_rows, cl_nbox, cl_box_stride, cl_smem;
     int zero_out;  // router sets out[n][H] to 0, or to x in a pre-normed block (the expert kernel accumulates into it)
+    int act8;      // int8-activation mode (SI_FLAG_ACT_INT8) on the single-token cluster path
     int sel_logits;  // single token, cluster expert kernel: the router writes ids in rank order, the
                      // selected logits (not weights) and 0/1 counts; the expert kernel forms the weights
 };

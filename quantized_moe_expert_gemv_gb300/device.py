@@ -54,8 +54,10 @@ def tokens_to_device(x_bits: np.ndarray, device="cuda") -> torch.Tensor:
     return t.to(device).view(torch.bfloat16)
 
 
-def desc_for(shape: MoeShape, max_tokens: int = 1, wtype: int = binding.SI_WTYPE_Q4_K) -> binding.si_moe_desc:
-    return binding.make_desc(shape.hidden, shape.intermediate, shape.n_experts, shape.top_k, max_tokens, wtype)
+def desc_for(shape: MoeShape, max_tokens: int = 1, wtype: int = binding.SI_WTYPE_Q4_K,
+             flags: int = 0) -> binding.si_moe_desc:
+    return binding.make_desc(shape.hidden, shape.intermediate, shape.n_experts, shape.top_k, max_tokens, wtype,
+                             flags)
 
 
 def alloc_scratch(plan: binding.Plan, mode: int, n_tokens: int, device="cuda",

@@ -50,7 +50,9 @@ def test_plan_rejects_bad_descriptors_before_touching_a_device(lib):
         (D(2048, 768, 128, 0), binding.SI_ERR_INVALID_ARG),
         (D(2048, 768, 128, 8, max_tokens=0), binding.SI_ERR_INVALID_ARG),
         (D(2048, 768, 128, 8, wtype=2), binding.SI_ERR_UNSUPPORTED),   # not Q4_K
-        (D(2048, 768, 128, 8, flags=1), binding.SI_ERR_UNSUPPORTED),
+        (D(2048, 768, 128, 8, flags=2), binding.SI_ERR_UNSUPPORTED),   # an unknown flag
+        (D(2048, 768, 128, 8, wtype=binding.SI_WTYPE_NVFP4, flags=binding.SI_FLAG_ACT_INT8),
+         binding.SI_ERR_UNSUPPORTED),                                  # int8 activations: Q4_K only
     ]
     for desc, want in bad:
         assert binding.si_moe_plan_status(desc) == want
