@@ -124,6 +124,44 @@ void or_q4k_dequant(const uint8_t *blocks, int64_t n_blocks, float *out) {
         or_q4k_block(blocks + b * OR_BLOCK_BYTES, out + b * OR_QK);
 }
 
+/* ------------------------------------------------------------------ Q5_K
+ * Another GGUF K-quant block type (a Q4_K_M / Q5_K_M file mixes K-quant
+ * types; the pages name Q4_K_M files but give no mix).  The layout is GGUF's
+ * Q5_K, taken from the format's public definition (a reading: the pages do not
+ * define it): 176 bytes per 256 weights,
+ *   bytes 0-1    d (binary16),  bytes 2-3  dmin (binary16)
+ *   bytes 4-15   scales[12]: the same eight 6-bit scales and mins as Q4_K
+ *   bytes 16-47  qh[32]: bit j of qh[l] is the fifth (value-16) bit of
+ *                weight l of sub-block j
+ *   bytes 48-175 qs[128]: the low four bits, arranged as Q4_K's qs
+ *   q = low4 + 16 * high bit (0..31),  weight = d * sc_j * q - dmin * m_j */
+#define OR_Q5K_BLOCK_BYTES 176
+
+static void or_q5k_block(const uint8_t *blk, float *out) {
+    double d = or_half_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+    double dmin = or_half_to_double((uint16_t)(blk[2] | (blk[3] << 8)));
+    const uint8_t *scales = blk + 4;
+    const uint8_t *qh = blk + 16;
+    const uint8_t *qs = blk + 48;
+    for (int j = 0; j < 8; ++j) {
+        int sc, m;
+        or_q4k_scale_min(scales, j, &sc, &m);
+        int i = j / 2;
+        for (int l = 0; l < 32; ++l) {
+            int byte = qs[32 * i + l];
+            int low4 = (j % 2 == 0) ? (byte & 15) : (byte >> 4);
+            int q = low4 + 16 * ((qh[l] >> j) & 1);
+            double w = d * (double)sc * (double)q - dmin * (double)m;  /* exact in fp64 */
+            out[32 * j + l] = (float)w;
+        }
+    }
+}
+
+void or_q5k_dequant(const uint8_t *blocks, int64_t n_blocks, float *out) {
+    for (int64_t b = 0; b < n_blocks; ++b)
+        or_q5k_block(blocks + b * OR_Q5K_BLOCK_BYTES, out + b * OR_QK);
+}
+
 /* One row of a Q4_K matrix with `cols` input columns, as fp32 weights. */
 static void or_q4k_row(const uint8_t *row_blocks, int cols, float *out) {
     or_q4k_dequant(row_blocks, cols / OR_QK, out);
@@ -260,12 +298,17 @@ void or_route_tokens(const float *router_w, const float *bias, const uint16_t *x
 static double or_silu(double g) { return g / (1.0 + exp(-g)); }
 
 #define OR_WTYPE_Q4_K 12
+#define OR_WTYPE_Q5_K 13
 #define OR_WTYPE_NVFP4 100
 
-/* One row of `cols` weights of either format as fp32 (g: the matrix's NVFP4
- * tensor scale, unused for Q4_K). */
+/* Bytes of one 256-weight block of the format. */
+static int64_t or_block_bytes(int wtype) { return wtype == OR_WTYPE_Q5_K ? OR_Q5K_BLOCK_BYTES : OR_BLOCK_BYTES; }
+
+/* One row of `cols` weights of any format as fp32 (g: the matrix's NVFP4
+ * tensor scale, unused otherwise). */
 static void or_row(int wtype, const uint8_t *row_blocks, int cols, float g, float *out) {
     if (wtype == OR_WTYPE_NVFP4) or_nvfp4_dequant(row_blocks, cols / OR_QK, g, out);
+    else if (wtype == OR_WTYPE_Q5_K) or_q5k_dequant(row_blocks, cols / OR_QK, out);
     else or_q4k_row(row_blocks, cols, out);
 }
 
@@ -278,8 +321,8 @@ void or_expert_ffn_wt(int wtype, const uint8_t *wg, const uint8_t *wu, const uin
                       float gu, float gd, int H, int I, const double *x, double *h_out, double *y) {
     float *row = (float *)malloc(sizeof(float) * (size_t)(H > I ? H : I));
     double *h = (double *)malloc(sizeof(double) * (size_t)I);
-    int64_t gate_row_bytes = (int64_t)(H / OR_QK) * OR_BLOCK_BYTES;
-    int64_t down_row_bytes = (int64_t)(I / OR_QK) * OR_BLOCK_BYTES;
+    int64_t gate_row_bytes = (int64_t)(H / OR_QK) * or_block_bytes(wtype);
+    int64_t down_row_bytes = (int64_t)(I / OR_QK) * or_block_bytes(wtype);
     for (int r = 0; r < I; ++r) {
         double g = 0.0, u = 0.0;
         or_row(wtype, wg + r * gate_row_bytes, H, gg, row);
@@ -318,8 +361,8 @@ void or_moe_token_wt(int wtype, const uint8_t *w_gate, const uint8_t *w_up, cons
     double *acc = (double *)calloc((size_t)H, sizeof(double));
     for (int c = 0; c < H; ++c) x[c] = or_bf16_to_double(x_bf16[c]);
     or_route_tokens(router_w, bias, x_bf16, 1, E, H, k, ids, w, NULL, NULL);
-    int64_t gate_expert_bytes = (int64_t)I * (H / OR_QK) * OR_BLOCK_BYTES;
-    int64_t down_expert_bytes = (int64_t)H * (I / OR_QK) * OR_BLOCK_BYTES;
+    int64_t gate_expert_bytes = (int64_t)I * (H / OR_QK) * or_block_bytes(wtype);
+    int64_t down_expert_bytes = (int64_t)H * (I / OR_QK) * or_block_bytes(wtype);
     for (int i = 0; i < k; ++i) {
         int e = ids[i];
         or_expert_ffn_wt(wtype, w_gate + e * gate_expert_bytes, w_up + e * gate_expert_bytes,

@@ -55,6 +55,7 @@ def _load():
             lib.or_e4m3_to_double.restype = ctypes.c_double
             lib.or_e4m3_to_double.argtypes = [ctypes.c_uint8]
             lib.or_nvfp4_dequant.argtypes = [_c_u8p, ctypes.c_int64, ctypes.c_float, _c_f32p]
+            lib.or_q5k_dequant.argtypes = [_c_u8p, ctypes.c_int64, _c_f32p]
             lib.or_expert_ffn_wt.argtypes = [ctypes.c_int, _c_u8p, _c_u8p, _c_u8p, ctypes.c_float, ctypes.c_float,
                                              ctypes.c_float, ctypes.c_int, ctypes.c_int, _c_f64p, _c_f64p, _c_f64p]
             lib.or_moe_token_wt.argtypes = [ctypes.c_int, _c_u8p, _c_u8p, _c_u8p, _c_f32p, _c_f32p, _c_f32p,
@@ -126,7 +127,18 @@ def q4k_dequant(blocks: np.ndarray) -> np.ndarray:
 
 
 WTYPE_Q4_K = 12
+WTYPE_Q5_K = 13
 WTYPE_NVFP4 = 100
+
+
+def q5k_dequant(blocks: np.ndarray) -> np.ndarray:
+    """fp32 weights of Q5_K blocks: any uint8 array whose size is a multiple of 176."""
+    b = np.ascontiguousarray(blocks, dtype=np.uint8)
+    n = b.size // 176
+    assert n * 176 == b.size
+    out = np.empty(n * 256, dtype=np.float32)
+    _load().or_q5k_dequant(_ptr(b, _c_u8p), n, _ptr(out, _c_f32p))
+    return out
 
 
 def e2m1_to_double(code: int) -> float:
@@ -319,7 +331,7 @@ def counts_offsets_perm(ids: np.ndarray, n_experts: int):
 
 __all__ = [
     "build", "half_to_double", "bf16_to_double", "q4k_scale_min", "q4k_dequant",
-    "WTYPE_Q4_K", "WTYPE_NVFP4", "e2m1_to_double", "e4m3_to_double", "nvfp4_dequant",
+    "WTYPE_Q4_K", "WTYPE_Q5_K", "q5k_dequant", "WTYPE_NVFP4", "e2m1_to_double", "e4m3_to_double", "nvfp4_dequant",
     "router_logits", "topk", "renorm_weights", "route_tokens", "expert_ffn", "moe_token",
     "TokenResult", "counts_offsets_perm", "rmsnorm", "moe_token_prenorm", "PrenormResult", "route_tokens_prenorm",
     "act8_quant", "expert_ffn_act8", "moe_token_act8",

@@ -100,7 +100,9 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
 
 
 WTYPE_Q4_K = 12      # GGUF's type id of Q4_K
+WTYPE_Q5_K = 13      # GGUF's type id of Q5_K (layout below)
 WTYPE_NVFP4 = 100    # NVFP4 super-blocks (layout below)
+Q5K_BLOCK_BYTES = 176
 
 
 @dataclass
@@ -261,3 +263,33 @@ def make_tokens_torch(n: int, hidden: int, seed_key: tuple, device="cuda"):
     g = torch.Generator(device=device)
     g.manual_seed(_torch_seed(*seed_key))
     return torch.randn((n, hidden), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# Q5_K experts (GGUF's Q5_K block, 176 bytes per 256 weights: d, dmin, the
+# Q4_K scale/min bytes, qh[32] -- bit j of qh[l] is the value-16 bit of weight
+# l of sub-block j -- and qs[128] arranged as Q4_K's).  Synthetic recipe: like
+# q4k_random_blocks with uniform random qh and qs bytes and d ~ U[5e-5, 1e-3]
+# (half the Q4_K range: the codes reach 31), dmin ~ U[0, 1e-3].
+# ---------------------------------------------------------------------------
+def q5k_random_blocks(g: np.random.Generator, n_blocks: int) -> np.ndarray:
+    """n_blocks random Q5_K super-blocks, uint8 [n_blocks, 176]."""
+    raw = np.frombuffer(g.bytes(n_blocks * Q5K_BLOCK_BYTES), dtype=np.uint8)
+    raw = raw.reshape(n_blocks, Q5K_BLOCK_BYTES).copy()
+    d = g.uniform(5e-5, 1e-3, n_blocks).astype(np.float16)
+    dmin = g.uniform(0.0, 1e-3, n_blocks).astype(np.float16)
+    raw[:, 0:2] = d.astype("<f2").view(np.uint8).reshape(n_blocks, 2)
+    raw[:, 2:4] = dmin.astype("<f2").view(np.uint8).reshape(n_blocks, 2)
+    return raw
+
+
+def make_layer_q5k(shape: MoeShape, seed: int, layer: int = 0,
+                   router_bias: np.ndarray | None = None) -> MoeLayer:
+    E, H, I = shape.n_experts, shape.hidden, shape.intermediate
+    nbh, nbi = shape.blocks_per_gate_row, shape.blocks_per_down_row
+    wg = q5k_random_blocks(rng(seed, layer, "q5k-gate"), E * I * nbh).reshape(E, I, nbh, Q5K_BLOCK_BYTES)
+    wu = q5k_random_blocks(rng(seed, layer, "q5k-up"), E * I * nbh).reshape(E, I, nbh, Q5K_BLOCK_BYTES)
+    wd = q5k_random_blocks(rng(seed, layer, "q5k-down"), E * H * nbi).reshape(E, H, nbi, Q5K_BLOCK_BYTES)
+    rw = make_router_w(shape, seed, layer)
+    bias = None if router_bias is None else np.asarray(router_bias, dtype=np.float32).copy()
+    return MoeLayer(shape, wg, wu, wd, rw, bias, wtype=WTYPE_Q5_K)

@@ -688,3 +688,68 @@ def test_act8_mode_error_against_the_exact_block(oracle_lib):
         np.testing.assert_allclose(w, ref.w, rtol=1e-12)
         errs.append(np.linalg.norm(out - ref.out64) / np.linalg.norm(ref.out64))
     assert 1e-4 < max(errs) < 3e-2
+
+
+# ----------------------------------------------------------------- Q5_K
+def _q5k_from_q4k(q4: np.ndarray, qh: np.ndarray) -> np.ndarray:
+    """The Q5_K blocks with the Q4_K blocks' d, dmin, scales and qs and the given qh bytes."""
+    n = q4.shape[0]
+    out = np.zeros((n, 176), dtype=np.uint8)
+    out[:, 0:16] = q4[:, 0:16]
+    out[:, 16:48] = qh
+    out[:, 48:176] = q4[:, 16:144]
+    return out
+
+
+def test_q5k_with_no_high_bits_is_q4k(oracle_lib):
+    g = synth.rng(91)
+    q4 = synth.q4k_random_blocks(g, 200)
+    q5 = _q5k_from_q4k(q4, np.zeros((200, 32), dtype=np.uint8))
+    assert np.array_equal(oracle.q5k_dequant(q5), oracle.q4k_dequant(q4))
+
+
+def test_q5k_each_high_bit_adds_sixteen_steps_to_one_weight(oracle_lib):
+    g = synth.rng(92)
+    q4 = synth.q4k_random_blocks(g, 3)
+    base_qh = np.zeros((3, 32), dtype=np.uint8)
+    base = oracle.q5k_dequant(_q5k_from_q4k(q4, base_qh)).reshape(3, 256)
+    for blk in range(3):
+        dd = Fraction(oracle.half_to_double(int(q4[blk, 0]) | (int(q4[blk, 1]) << 8)))
+        dmin = Fraction(oracle.half_to_double(int(q4[blk, 2]) | (int(q4[blk, 3]) << 8)))
+        for j in range(8):
+            sc, m = oracle.q4k_scale_min(q4[blk, 4:16], j)
+            for l in (0, 5, 31):
+                qh = base_qh.copy()
+                qh[blk, l] = 1 << j
+                got = oracle.q5k_dequant(_q5k_from_q4k(q4, qh)).reshape(3, 256)
+                diff = np.nonzero(got != base)
+                # only weight l of sub-block j of this block moved ...
+                assert list(zip(*diff)) in ([(blk, 32 * j + l)], []), (blk, j, l, diff)
+                # ... to the exactly rounded value of its code plus 16
+                qs_byte = int(q4[blk, 16 + 32 * (j // 2) + l])
+                code = (qs_byte >> 4 if j % 2 else qs_byte & 15) + 16
+                want = float(np.float32(float(dd * sc * code - dmin * m)))
+                assert got[blk, 32 * j + l] == want
+
+
+@pytest.mark.parametrize("shape", [synth.MoeShape(256, 256, 4, 2), synth.MoeShape(512, 256, 6, 3)])
+def test_q5k_moe_token_matches_dense_brute_force(oracle_lib, shape):
+    layer = synth.make_layer_q5k(shape, seed=23)
+    xs = synth.make_tokens(shape, seed=23, n_tokens=2)
+    H, I = shape.hidden, shape.intermediate
+    for t in range(2):
+        res = oracle.moe_token(layer, xs[t])
+        x = synth.bf16_to_f32(xs[t]).astype(np.float64)
+        z = layer.router_w.astype(np.float64) @ x
+        sel = oracle.topk(z.astype(np.float32), shape.top_k)
+        p = np.exp(z[sel] - z[sel].max())
+        wsel = p / p.sum()
+        out = np.zeros(H)
+        for e, w in zip(sel, wsel):
+            Wg = oracle.q5k_dequant(layer.w_gate[e]).reshape(I, H).astype(np.float64)
+            Wu = oracle.q5k_dequant(layer.w_up[e]).reshape(I, H).astype(np.float64)
+            Wd = oracle.q5k_dequant(layer.w_down[e]).reshape(H, I).astype(np.float64)
+            gg = Wg @ x
+            out += w * (Wd @ (gg * scipy.special.expit(gg) * (Wu @ x)))
+        assert np.array_equal(res.ids, sel)
+        np.testing.assert_allclose(res.out64, out, rtol=1e-10, atol=1e-12 * np.abs(out).max())
