@@ -45,6 +45,14 @@
  *   w_gate, w_up: [E][I rows][H/256 blocks]   (row r of expert e at byte
  *                 ((e*I + r) * H/256) * 144)
  *   w_down:       [E][H rows][I/256 blocks]
+ * Q5_K weights (SI_WTYPE_Q5_K; another GGUF K-quant block type -- a Q4_K_M
+ * or Q5_K_M file mixes K-quant types; the layout is GGUF's, a reading from
+ * outside the pages): 176-byte super-blocks {fp16 d, fp16 dmin, u8
+ * scales[12] as in Q4_K, u8 qh[32], u8 qs[128]}, code q = low four bits from
+ * qs (arranged as Q4_K's) + 16 * bit j of qh[l] for weight l of sub-block j,
+ * weight = d*sc_j*q - dmin*m_j; the same expert-major layout with 176 in
+ * place of 144.  All three matrices of a layer have the plan's wtype.  Q5_K
+ * layers are plain blocks (a norm_weight gives SI_ERR_UNSUPPORTED).
  */
 #ifndef SI_MOE_H
 #define SI_MOE_H
@@ -72,6 +80,7 @@ typedef enum si_status {
 } si_status;
 
 #define SI_WTYPE_Q4_K 12          /* GGUF's type id of Q4_K */
+#define SI_WTYPE_Q5_K 13          /* GGUF's type id of Q5_K: 176-byte super-blocks (see below) */
 #define SI_WTYPE_NVFP4 100        /* NVFP4 super-blocks (see si_moe_layer.w_scale) */
 /* si_moe_desc.flags: int8-activation mode of single-token decode (the dp4a
  * matrix-vector product on quantised weights that the sparkinfer README's
@@ -95,7 +104,7 @@ typedef enum si_status {
 /* Layer shape.  hidden and intermediate are multiples of 256 (one Q4_K
  * super-block); 1 <= top_k <= min(n_experts, SI_MAX_TOPK);
  * n_experts <= SI_MAX_EXPERTS; max_tokens bounds the prefill token count.
- * wtype is SI_WTYPE_Q4_K or SI_WTYPE_NVFP4; flags is 0 or SI_FLAG_ACT_INT8
+ * wtype is SI_WTYPE_Q4_K, SI_WTYPE_Q5_K or SI_WTYPE_NVFP4; flags is 0 or SI_FLAG_ACT_INT8
  * (other bits: SI_ERR_UNSUPPORTED). */
 typedef struct si_moe_desc {
     int32_t hidden;
@@ -272,6 +281,15 @@ si_status si_debug_topk(const float *logits, int32_t n, const si_moe_desc *desc,
  * fp32(w) * gamma[256*b + c] (the gate/up operand of a pre-normed block).
  * blocks, out_f16 16-byte aligned.  Stream-ordered. */
 si_status si_debug_q4k_dequant_f16(const void *blocks, int64_t n_blocks, const float *gamma, uint16_t *out_f16,
+                                   si_stream_t stream);
+
+/* Test export: the grouped prefill's Q5_K -> fp16 operand conversion (the
+ * device function its GEMM dequantization warps run for SI_WTYPE_Q5_K)
+ * applied to n_blocks 176-byte Q5_K blocks: out_f16[256*b + c] (fp16 bits) =
+ * round-to-nearest-even fp16 of the fp32 weight of column c of block b, or,
+ * when gamma is non-NULL, of fp32(w) * gamma[256*b + c].  blocks, out_f16
+ * (and gamma) 16-byte aligned.  Stream-ordered. */
+si_status si_debug_q5k_dequant_f16(const void *blocks, int64_t n_blocks, const float *gamma, uint16_t *out_f16,
                                    si_stream_t stream);
 
 /* Test export: the grouped prefill's NVFP4 -> fp16 operand conversion (the

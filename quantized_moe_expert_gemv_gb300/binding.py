@@ -29,6 +29,7 @@ SI_ERR_DEVICE = 7
 SI_ERR_RANGE = 8
 SI_WTYPE_Q4_K = 12
 SI_WTYPE_NVFP4 = 100
+SI_WTYPE_Q5_K = 13
 SI_FLAG_ACT_INT8 = 1
 SI_MODE_DECODE = 0
 SI_MODE_PREFILL = 1
@@ -119,6 +120,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.si_debug_q4k_dequant_f16.argtypes = [vp, i64, vp, vp, vp]
     lib.si_debug_nvfp4_dequant_f16.restype = ctypes.c_int
     lib.si_debug_nvfp4_dequant_f16.argtypes = [vp, i64, ctypes.c_float, vp, vp]
+    lib.si_debug_q5k_dequant_f16.restype = ctypes.c_int
+    lib.si_debug_q5k_dequant_f16.argtypes = [vp, i64, vp, vp, vp]
     lib.si_moe_read_status_noalloc.restype = ctypes.c_int
     lib.si_moe_read_status_noalloc.argtypes = [vp]
     lib.si_debug_topk.restype = ctypes.c_int
@@ -312,6 +315,11 @@ def si_debug_q4k_dequant_f16(blocks, n_blocks, out_f16, gamma=None, stream=None)
 def si_debug_nvfp4_dequant_f16(blocks, n_blocks, g, out_f16, stream=None):
     _check(load_library().si_debug_nvfp4_dequant_f16(_ptr(blocks), int(n_blocks), float(g), _ptr(out_f16),
                                                      _stream(stream)), "si_debug_nvfp4_dequant_f16")
+
+
+def si_debug_q5k_dequant_f16(blocks, n_blocks, gamma, out_f16, stream=None):
+    _check(load_library().si_debug_q5k_dequant_f16(_ptr(blocks), int(n_blocks), _ptr(gamma), _ptr(out_f16),
+                                                   _stream(stream)), "si_debug_q5k_dequant_f16")
 
 
 def si_moe_read_status_noalloc(stream=None) -> int:

@@ -23,7 +23,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 si_status validate_desc(const si_moe_desc *d) {
     if (!d) return SI_ERR_INVALID_ARG;
-    if (d->wtype != SI_WTYPE_Q4_K && d->wtype != SI_WTYPE_NVFP4) return SI_ERR_UNSUPPORTED;
+    if (d->wtype != SI_WTYPE_Q4_K && d->wtype != SI_WTYPE_Q5_K && d->wtype != SI_WTYPE_NVFP4) return SI_ERR_UNSUPPORTED;
     if ((d->flags & ~SI_FLAG_ACT_INT8) != 0) return SI_ERR_UNSUPPORTED;
     if ((d->flags & SI_FLAG_ACT_INT8) && d->wtype != SI_WTYPE_Q4_K) return SI_ERR_UNSUPPORTED;
     if (d->hidden <= 0 || d->intermediate <= 0 || d->hidden % 256 || d->intermediate % 256)
@@ -232,6 +232,7 @@ static si_status check_weight_scales(const si_moe_desc &d, const si_moe_layer *l
         return SI_ERR_INVALID_ARG;
     }
     if ((d.flags & SI_FLAG_ACT_INT8) && layer->norm_weight) return SI_ERR_UNSUPPORTED;
+    if (d.wtype == SI_WTYPE_Q5_K && layer->norm_weight) return SI_ERR_UNSUPPORTED;  // plain Q5_K blocks only
     return SI_OK;
 }
 
@@ -464,6 +465,18 @@ si_status si_debug_q4k_dequant_f16(const void *blocks, int64_t n_blocks, const f
     if (!aligned(blocks, 16) || !aligned(out_f16, 16) || (gamma && !aligned(gamma, 16))) return SI_ERR_MISALIGNED;
     if (si::launch_debug_dequant_f16(static_cast<const uint8_t *>(blocks), n_blocks, gamma, out_f16,
                                      (cudaStream_t)stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SI_ERR_CUDA;
+    }
+    return SI_OK;
+}
+
+si_status si_debug_q5k_dequant_f16(const void *blocks, int64_t n_blocks, const float *gamma, uint16_t *out_f16,
+                                   si_stream_t stream) {
+    if (!blocks || n_blocks < 0 || !out_f16) return SI_ERR_INVALID_ARG;
+    if (!aligned(blocks, 16) || !aligned(out_f16, 16) || (gamma && !aligned(gamma, 16))) return SI_ERR_MISALIGNED;
+    if (si::launch_debug_q5k_f16(static_cast<const uint8_t *>(blocks), n_blocks, gamma, out_f16,
+                                 (cudaStream_t)stream) != cudaSuccess) {
         cudaGetLastError();
         return SI_ERR_CUDA;
     }

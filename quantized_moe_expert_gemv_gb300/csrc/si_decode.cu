@@ -387,7 +387,9 @@ __device__ __forceinline__ void gateup_rowpair(const DecodeArgs &a, const float 
                                                int lane) {
     const int e = u->expert[s];
     const int nbH = a.H / kQK;
-    const size_t row_bytes = (size_t)nbH * kBlockBytes;
+    const bool q5 = a.wtype == SI_WTYPE_Q5_K;
+    const int BB = q5 ? kQ5BlockBytes : kBlockBytes, qoff = q5 ? kQ5QsOff : 16;
+    const size_t row_bytes = (size_t)nbH * BB;
     const uint8_t *gbase = a.wg + ((size_t)e * a.I + r) * row_bytes;
     const uint8_t *ubase = a.wu + ((size_t)e * a.I + r) * row_bytes;
     int tok[NT], slot[NT];
@@ -401,12 +403,17 @@ __device__ __forceinline__ void gateup_rowpair(const DecodeArgs &a, const float 
     for (int t = 0; t < NT; ++t) g[t] = uu[t] = 0.f;
     for (int it = lane; it < 4 * nbH; it += 32) {
         const int b = it >> 2, i = it & 3;
-        const uint8_t *bg = gbase + b * kBlockBytes;
-        const uint8_t *bu = ubase + b * kBlockBytes;
-        const uint4 hg = ldg_nc_v4(bg), qg0 = ldg_nc_v4(bg + 16 + 32 * i),
-                    qg1 = ldg_nc_v4(bg + 32 + 32 * i);
-        const uint4 hu = ldg_nc_v4(bu), qu0 = ldg_nc_v4(bu + 16 + 32 * i),
-                    qu1 = ldg_nc_v4(bu + 32 + 32 * i);
+        const uint8_t *bg = gbase + b * BB;
+        const uint8_t *bu = ubase + b * BB;
+        const uint4 hg = ldg_nc_v4(bg), qg0 = ldg_nc_v4(bg + qoff + 32 * i),
+                    qg1 = ldg_nc_v4(bg + qoff + 16 + 32 * i);
+        const uint4 hu = ldg_nc_v4(bu), qu0 = ldg_nc_v4(bu + qoff + 32 * i),
+                    qu1 = ldg_nc_v4(bu + qoff + 16 + 32 * i);
+        uint4 hg0 = make_uint4(0, 0, 0, 0), hg1 = hg0, hu0 = hg0, hu1 = hg0;  // Q5_K: the qh bytes
+        if (q5) {
+            hg0 = ldg_nc_v4(bg + kQ5QhOff), hg1 = ldg_nc_v4(bg + kQ5QhOff + 16);
+            hu0 = ldg_nc_v4(bu + kQ5QhOff), hu1 = ldg_nc_v4(bu + kQ5QhOff + 16);
+        }
         const bool fp4 = a.wtype == SI_WTYPE_NVFP4;
         const SubScales sg = chunk_scales(hg, i), su = chunk_scales(hu, i);
 #pragma unroll
@@ -421,6 +428,9 @@ __device__ __forceinline__ void gateup_rowpair(const DecodeArgs &a, const float 
             if (fp4) {  // NVFP4: the tensor scales are applied to the row sums below
                 g[t] += chunk_contrib_nvfp4_f32(hg, i, qg0, qg1, xa2, xb2);
                 uu[t] += chunk_contrib_nvfp4_f32(hu, i, qu0, qu1, xa2, xb2);
+            } else if (q5) {
+                g[t] += chunk_contrib(sg, chunk_code_sums5(qg0, qg1, hg0, hg1, i, xa2, xb2), Xa, Xb);
+                uu[t] += chunk_contrib(su, chunk_code_sums5(qu0, qu1, hu0, hu1, i, xa2, xb2), Xa, Xb);
             } else {
                 g[t] += chunk_contrib(sg, chunk_code_sums(qg0, qg1, xa2, xb2), Xa, Xb);
                 uu[t] += chunk_contrib(su, chunk_code_sums(qu0, qu1, xa2, xb2), Xa, Xb);
@@ -501,7 +511,9 @@ __global__ void __launch_bounds__(kThreads) k_down_generic(DecodeArgs a) {
     const int c = (blockIdx.x * kWarps + warp) * kGroups + lane / GS;
     if ((blockIdx.x * kWarps + warp) * kGroups >= a.H) return;  // whole warp idle
     const int nbI = a.I / kQK;
-    const size_t row_bytes = (size_t)nbI * kBlockBytes;
+    const bool q5 = a.wtype == SI_WTYPE_Q5_K;
+    const int BB = q5 ? kQ5BlockBytes : kBlockBytes, qoff = q5 ? kQ5QsOff : 16;
+    const size_t row_bytes = (size_t)nbI * BB;
     const UniqTable *u = a.uniq;
     const int U = a.ctrl[kCtrlNumUnique];
     float acc[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
@@ -516,9 +528,11 @@ __global__ void __launch_bounds__(kThreads) k_down_generic(DecodeArgs a) {
         float y[SI_MAX_DECODE_TOKENS] = {0.f, 0.f, 0.f, 0.f};
         for (int it = gl; it < 4 * nbI; it += GS) {
             const int b = it >> 2, i = it & 3;
-            const uint8_t *blk = row + b * kBlockBytes;
-            const uint4 hd = ldg_nc_v4(blk), q0 = ldg_nc_v4(blk + 16 + 32 * i),
-                        q1 = ldg_nc_v4(blk + 32 + 32 * i);
+            const uint8_t *blk = row + b * BB;
+            const uint4 hd = ldg_nc_v4(blk), q0 = ldg_nc_v4(blk + qoff + 32 * i),
+                        q1 = ldg_nc_v4(blk + qoff + 16 + 32 * i);
+            uint4 qh0 = make_uint4(0, 0, 0, 0), qh1 = qh0;  // Q5_K: the qh bytes
+            if (q5) qh0 = ldg_nc_v4(blk + kQ5QhOff), qh1 = ldg_nc_v4(blk + kQ5QhOff + 16);
             const SubScales sc = chunk_scales(hd, i);
             const bool fp4 = a.wtype == SI_WTYPE_NVFP4;
 #pragma unroll
@@ -531,8 +545,9 @@ __global__ void __launch_bounds__(kThreads) k_down_generic(DecodeArgs a) {
                     auto xb2 = [pb](int p) { return __ldg(pb + p); };
                     const float Xa = Hs[sl[t] * nIs + 8 * b + 2 * i];
                     const float Xb = Hs[sl[t] * nIs + 8 * b + 2 * i + 1];
-                    y[t] += fp4 ? chunk_contrib_nvfp4_f32(hd, i, q0, q1, xa2, xb2)
-                                : chunk_contrib(sc, chunk_code_sums(q0, q1, xa2, xb2), Xa, Xb);
+                    y[t] += fp4  ? chunk_contrib_nvfp4_f32(hd, i, q0, q1, xa2, xb2)
+                            : q5 ? chunk_contrib(sc, chunk_code_sums5(q0, q1, qh0, qh1, i, xa2, xb2), Xa, Xb)
+                                 : chunk_contrib(sc, chunk_code_sums(q0, q1, xa2, xb2), Xa, Xb);
                 }
             }
         }

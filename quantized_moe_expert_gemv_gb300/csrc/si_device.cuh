@@ -25,7 +25,13 @@
 namespace si {
 
 constexpr int kQK = 256;          // weights per super-block
-constexpr int kBlockBytes = 144;  // bytes per super-block
+constexpr int kBlockBytes = 144;  // bytes per super-block (Q4_K, NVFP4)
+// Q5_K (GGUF's K-quant with 5-bit codes): 176 bytes per 256 weights -- d,
+// dmin and the 12 scale/min bytes as in Q4_K (bytes 0-15), qh[32] (bytes
+// 16-47: bit j of qh[l] is the value-16 bit of weight l of sub-block j) and
+// qs[128] (bytes 48-175, arranged as Q4_K's).
+constexpr int kQ5BlockBytes = 176;
+constexpr int kQ5QhOff = 16, kQ5QsOff = 48;
 
 // ---------------------------------------------------------------- loads
 __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
@@ -120,6 +126,34 @@ __device__ __forceinline__ ChunkSums chunk_code_sums(const uint4 &q0, const uint
     for (int t = 0; t < 8; ++t) {
         const uint32_t lo = w[t] & 0x0f0f0f0fu;
         const uint32_t hi = (w[t] >> 4) & 0x0f0f0f0fu;
+        ffma2(acc_a, pack2(code_plus_128<0>(lo), code_plus_128<1>(lo)), xa2(2 * t));
+        ffma2(acc_a, pack2(code_plus_128<2>(lo), code_plus_128<3>(lo)), xa2(2 * t + 1));
+        ffma2(acc_b, pack2(code_plus_128<0>(hi), code_plus_128<1>(hi)), xb2(2 * t));
+        ffma2(acc_b, pack2(code_plus_128<2>(hi), code_plus_128<3>(hi)), xb2(2 * t + 1));
+    }
+    const float2 a = unpack2(acc_a), b = unpack2(acc_b);
+    return ChunkSums{a.x + a.y, b.x + b.y};
+}
+
+// Q5_K: the 5-bit codes of sub-blocks 2i (lo) and 2i+1 (hi) for the four
+// weights of word t of a chunk's qs (w) and qh (qhw) bytes, one code per byte.
+__device__ __forceinline__ uint32_t q5_codes_lo(uint32_t w, uint32_t qhw, int i) {
+    return (w & 0x0f0f0f0fu) | (((qhw >> (2 * i)) & 0x01010101u) << 4);
+}
+__device__ __forceinline__ uint32_t q5_codes_hi(uint32_t w, uint32_t qhw, int i) {
+    return ((w >> 4) & 0x0f0f0f0fu) | (((qhw >> (2 * i + 1)) & 0x01010101u) << 4);
+}
+
+// chunk_code_sums for Q5_K codes (qh0, qh1: the block's 32 qh bytes).
+template <typename XA, typename XB>
+__device__ __forceinline__ ChunkSums chunk_code_sums5(const uint4 &q0, const uint4 &q1, const uint4 &qh0,
+                                                      const uint4 &qh1, int i, XA xa2, XB xb2) {
+    f32x2 acc_a = 0ull, acc_b = 0ull;
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t h[8] = {qh0.x, qh0.y, qh0.z, qh0.w, qh1.x, qh1.y, qh1.z, qh1.w};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t lo = q5_codes_lo(w[t], h[t], i), hi = q5_codes_hi(w[t], h[t], i);
         ffma2(acc_a, pack2(code_plus_128<0>(lo), code_plus_128<1>(lo)), xa2(2 * t));
         ffma2(acc_a, pack2(code_plus_128<2>(lo), code_plus_128<3>(lo)), xa2(2 * t + 1));
         ffma2(acc_b, pack2(code_plus_128<0>(hi), code_plus_128<1>(hi)), xb2(2 * t));
@@ -533,6 +567,24 @@ __device__ __forceinline__ int2 chunk_isums(const uint4 &q0, const uint4 &q1, XW
         b1 = dp2a_hi(xw(16 + 2 * t + 1), hi, b1);
     }
     return make_int2(a0 + a1, (b0 + b1) >> 4);  // b sums are exact multiples of 16
+}
+
+// chunk_isums for Q5_K codes (qh0, qh1: the block's 32 qh bytes; i the chunk).
+template <typename XW>
+__device__ __forceinline__ int2 chunk_isums5(const uint4 &q0, const uint4 &q1, const uint4 &qh0, const uint4 &qh1,
+                                            int i, XW xw) {
+    int a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t h[8] = {qh0.x, qh0.y, qh0.z, qh0.w, qh1.x, qh1.y, qh1.z, qh1.w};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t lo = q5_codes_lo(w[t], h[t], i), hi = q5_codes_hi(w[t], h[t], i);
+        a0 = dp2a_lo(xw(2 * t), lo, a0);
+        a1 = dp2a_hi(xw(2 * t + 1), lo, a1);
+        b0 = dp2a_lo(xw(16 + 2 * t), hi, b0);
+        b1 = dp2a_hi(xw(16 + 2 * t + 1), hi, b1);
+    }
+    return make_int2(a0 + a1, b0 + b1);
 }
 
 struct ChunkScalesI {

@@ -91,6 +91,8 @@ __device__ __forceinline__ float pair_sum(float g, float u, int li) {
 // tensor scales on the gate and up partials and on the combine weight.
 // WF = 2: Q4_K weights in the int8-activation mode (SI_FLAG_ACT_INT8): x (from
 // the router) and h are int8 per 32 columns, dotted with dp4a.
+// WF = 3: Q5_K weights (176-byte super-blocks: the fifth code bit of every
+// weight in 32 qh bytes ahead of the Q4_K-style codes), int16 activations.
 template <int NBH, bool NORM, int WF>
 __global__ void __launch_bounds__(kClThreads, 1)
     k_expert_cluster(const __grid_constant__ CUtensorMap tmap_down, const __grid_constant__ CUtensorMap tmap_tail,
@@ -99,9 +101,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
     constexpr int GS = 4 * NBH;
     constexpr int RPW = 32 / GS;
     constexpr int CH = kCW * RPW * kPairs;  // row pairs per stage
-    constexpr int rowg = NBH * kBlockBytes;
+    constexpr bool FP4 = WF == 1, A8 = WF == 2, Q5 = WF == 3;
+    constexpr int BB = Q5 ? kQ5BlockBytes : kBlockBytes;  // bytes per super-block
+    constexpr int QO = Q5 ? kQ5QsOff : 16;                // offset of the codes in a block
+    constexpr int rowg = NBH * BB;
     constexpr int stageA = 2 * CH * rowg;
-    constexpr bool FP4 = WF == 1, A8 = WF == 2;
     __shared__ int s_err;
     __shared__ float s_w;
     __shared__ int s_lastA[8];
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         for (int j = 0; j < min(nA, NSA); ++j) mbar_arrive_expect_tx(fullA + 8 * j, 2 * stage_bytes(j));
         // the bytes the box copies deliver: the last box is tail_rows high for every
         // CTA (the largest CTA's remainder), which may exceed this CTA's n_rows
-        mbar_arrive_expect_tx(fullB, (uint32_t)(((nbox - 1) * kBoxRows + tail_rows) * kBlockBytes));
+        mbar_arrive_expect_tx(fullB, (uint32_t)(((nbox - 1) * kBoxRows + tail_rows) * BB));
         mbar_arrive_expect_tx(hbar, (uint32_t)(kQK * 4));  // every h value of the unit, once
         if (!NORM) mbar_arrive_expect_tx(xbar, xq_bytes);
     }
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 const size_t src = ((size_t)e * I + r_lo + q0) * rowg;
                 const uint32_t dst = smem_addr(stA + (size_t)st * stageA);
                 bulk_g2s(dst, wg + src, bytes, fullA + 8 * st, pol);
-                bulk_g2s(dst + CH * rowg, wu + src, bytes, fullA + 8 * st, pol);
+                bulk_g2s(dst + bytes, wu + src, bytes, fullA + 8 * st, pol);  // the up rows follow the gate rows
                 s_lastA[st] = (j / NSA) & 1;
                 return true;
             };
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             // tail_rows high (its own map); each box completes its own barrier
             for (int bx = 0; bx < nbox; ++bx)
                 tma_load_2d(smem_addr(stB + (size_t)bx * box_stride), bx == nbox - 1 ? &tmap_tail : &tmap_down,
-                            kBlockBytes * bcol, e * H + c_lo + bx * kBoxRows, fullB, pol);
+                            BB * bcol, e * H + c_lo + bx * kBoxRows, fullB, pol);
             s_lastB = 0;
             for (int j = first; j < nA; ++j)
                 if (!issueA(j)) break;
@@ -393,18 +397,25 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 ok = false;
             }
             const uint8_t *stage = stA + (size_t)st * stageA;
+            const int cnt = min(CH, n_rp - CH * j);  // row pairs of this stage: gate rows, then as many up rows
             float part[2 * kPairs];
 #pragma unroll
             for (int m = 0; m < kPairs; ++m) {
                 const int ql = (warp * RPW + g) * kPairs + m;  // row pair within the stage
                 part[2 * m] = part[2 * m + 1] = 0.f;
-                // a partly filled stage: skip the empty slots (warp-uniform when a warp holds one row)
-                if (ok && (RPW > 1 || CH * j + ql < n_rp)) {
-                    const uint8_t *grow = stage + ql * rowg + b * kBlockBytes;
-                    const uint8_t *urow = grow + CH * rowg;
-                    const uint4 hg = ld_s128(grow), qg0 = ld_s128(grow + 16 + 32 * i), qg1 = ld_s128(grow + 32 + 32 * i);
-                    const uint4 hu = ld_s128(urow), qu0 = ld_s128(urow + 16 + 32 * i), qu1 = ld_s128(urow + 32 + 32 * i);
-                    if (FP4) {
+                // a partly filled stage: skip the empty slots (per row group; the last stage
+                // holds only its own rows, so nothing may be read past them)
+                if (ok && CH * j + ql < n_rp) {
+                    const uint8_t *grow = stage + ql * rowg + b * BB;
+                    const uint8_t *urow = grow + cnt * rowg;
+                    const uint4 hg = ld_s128(grow), qg0 = ld_s128(grow + QO + 32 * i), qg1 = ld_s128(grow + QO + 16 + 32 * i);
+                    const uint4 hu = ld_s128(urow), qu0 = ld_s128(urow + QO + 32 * i), qu1 = ld_s128(urow + QO + 16 + 32 * i);
+                    if (Q5) {
+                        const uint4 hg0 = ld_s128(grow + kQ5QhOff), hg1 = ld_s128(grow + kQ5QhOff + 16);
+                        const uint4 hu0 = ld_s128(urow + kQ5QhOff), hu1 = ld_s128(urow + kQ5QhOff + 16);
+                        part[2 * m] = chunk_contrib_i(chunk_scales_i(hg, i), chunk_isums5(qg0, qg1, hg0, hg1, i, xwf), xs, Xa, Xb);
+                        part[2 * m + 1] = chunk_contrib_i(chunk_scales_i(hu, i), chunk_isums5(qu0, qu1, hu0, hu1, i, xwf), xs, Xa, Xb);
+                    } else if (FP4) {
                         part[2 * m] = tsg * chunk_contrib_nvfp4(hg, i, qg0, qg1, xwf, xs, XQ);
                         part[2 * m + 1] = tsu * chunk_contrib_nvfp4(hu, i, qu0, qu1, xwf, xs, XQ);
                     } else if (A8) {
@@ -522,9 +533,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const int lr = kBoxRows * m + 8 * warp + r8;
             float v = 0.f;
             if (lr < n_rows) {
-                const uint8_t *blk = stB + (size_t)m * box_stride + (size_t)(8 * warp + r8) * kBlockBytes;
-                const uint4 hd = ld_s128(blk), q0 = ld_s128(blk + 16 + 32 * i), q1 = ld_s128(blk + 32 + 32 * i);
-                v = FP4  ? chunk_contrib_nvfp4(hd, i, q0, q1, hwf, hs, HQ)
+                const uint8_t *blk = stB + (size_t)m * box_stride + (size_t)(8 * warp + r8) * BB;
+                const uint4 hd = ld_s128(blk), q0 = ld_s128(blk + QO + 32 * i), q1 = ld_s128(blk + QO + 16 + 32 * i);
+                uint4 qh0 = make_uint4(0, 0, 0, 0), qh1 = qh0;
+                if (Q5) qh0 = ld_s128(blk + kQ5QhOff), qh1 = ld_s128(blk + kQ5QhOff + 16);
+                v = Q5   ? chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums5(q0, q1, qh0, qh1, i, hwf), hs, Ha, Hb)
+                    : FP4 ? chunk_contrib_nvfp4(hd, i, q0, q1, hwf, hs, HQ)
                     : A8 ? chunk_contrib_i8(chunk_scales_i(hd, i), chunk_isums8(q0, q1, hwf), hs, hdb, Ha, Hb)
                          : chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums(q0, q1, hwf), hs, Ha, Hb);
             }
@@ -569,7 +583,8 @@ bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs
     if (nbh != 1 && nbh != 2 && nbh != 4 && nbh != 8) return false;
     if (C < 2 || C > 8) return false;
     const int CH = kCW * (32 / (4 * nbh)) * kPairs;
-    const int rowg = nbh * kBlockBytes;
+    const int BB = d.wtype == SI_WTYPE_Q5_K ? kQ5BlockBytes : kBlockBytes;
+    const int rowg = nbh * BB;
     const int stageA = 2 * CH * rowg;
     const int rp_max = (kQK + C - 1) / C;
     const int nA_max = (rp_max + CH - 1) / CH;
@@ -577,14 +592,16 @@ bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs
     if (rpc > kBoxRows * kMaxDownLanes) return false;
     const int nbox = (rpc + kBoxRows - 1) / kBoxRows;
     const int tail = rpc - (nbox - 1) * kBoxRows;  // 1..128 rows in the last box
-    const int box_stride = kBoxRows * kBlockBytes;  // 18432 = 144 * 128
+    const int box_stride = kBoxRows * BB;  // 18432 = 144 * 128 for Q4_K
     auto al = [](int v) { return (v + 127) / 128 * 128; };
     int NSA = nA_max < 3 ? nA_max : 3;
     int off = 0;
     a.cl_off_a = off;
-    off += NSA * stageA;
+    // without ring reuse the last stage holds only the rows that remain
+    off += nA_max <= NSA ? (NSA - 1) * stageA + 2 * (rp_max - (NSA - 1) * CH) * rowg : NSA * stageA;
+    off = al(off);
     a.cl_off_b = off;
-    off += (nbox - 1) * box_stride + al(tail * kBlockBytes);
+    off += (nbox - 1) * box_stride + al(tail * BB);
     a.cl_off_h = off;
     off += al(kQK * 4);
     a.cl_off_x = off;  // quantised x: [H/64][32] words + [H/64][7] (later: quantised h)
@@ -609,9 +626,10 @@ static bool make_down_tensor_map(const DecodeArgs &a, int rows, CUtensorMap *tm)
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const int nbi = a.I / kQK;
-    cuuint64_t dims[2] = {(cuuint64_t)nbi * kBlockBytes, (cuuint64_t)a.E * a.H};
-    cuuint64_t strides[1] = {(cuuint64_t)nbi * kBlockBytes};
-    cuuint32_t box[2] = {(cuuint32_t)kBlockBytes, (cuuint32_t)rows};
+    const int BB = a.wtype == SI_WTYPE_Q5_K ? kQ5BlockBytes : kBlockBytes;
+    cuuint64_t dims[2] = {(cuuint64_t)nbi * BB, (cuuint64_t)a.E * a.H};
+    cuuint64_t strides[1] = {(cuuint64_t)nbi * BB};
+    cuuint32_t box[2] = {(cuuint32_t)BB, (cuuint32_t)rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.wd), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -637,6 +655,7 @@ static cudaError_t launch_cluster_t(const DecodeArgs &a, const CUtensorMap &tm, 
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (a.wtype == SI_WTYPE_NVFP4) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 1>, tm, tt, a);
+    if (a.wtype == SI_WTYPE_Q5_K) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 3>, tm, tt, a);
     if (a.act8) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 2>, tm, tt, a);
     return a.norm_w ? cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, true, 0>, tm, tt, a)
                     : cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 0>, tm, tt, a);
@@ -657,16 +676,20 @@ cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s) {
 cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters) {
     *active_clusters = 0;
     if (!tensor_map_encoder()) return cudaErrorNotSupported;  // down blocks are fetched by a tensor map
-    const void *fs[4] = {nullptr, nullptr, nullptr, nullptr};  // plain and pre-normed Q4_K block, NVFP4, int8 activations
+    const void *fs[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};  // plain / pre-normed Q4_K, NVFP4, int8 act, Q5_K
     switch (nbh) {
         case 1: fs[0] = (const void *)k_expert_cluster<1, false, 0>, fs[1] = (const void *)k_expert_cluster<1, true, 0>,
-                fs[2] = (const void *)k_expert_cluster<1, false, 1>, fs[3] = (const void *)k_expert_cluster<1, false, 2>; break;
+                fs[2] = (const void *)k_expert_cluster<1, false, 1>, fs[3] = (const void *)k_expert_cluster<1, false, 2>,
+                fs[4] = (const void *)k_expert_cluster<1, false, 3>; break;
         case 2: fs[0] = (const void *)k_expert_cluster<2, false, 0>, fs[1] = (const void *)k_expert_cluster<2, true, 0>,
-                fs[2] = (const void *)k_expert_cluster<2, false, 1>, fs[3] = (const void *)k_expert_cluster<2, false, 2>; break;
+                fs[2] = (const void *)k_expert_cluster<2, false, 1>, fs[3] = (const void *)k_expert_cluster<2, false, 2>,
+                fs[4] = (const void *)k_expert_cluster<2, false, 3>; break;
         case 4: fs[0] = (const void *)k_expert_cluster<4, false, 0>, fs[1] = (const void *)k_expert_cluster<4, true, 0>,
-                fs[2] = (const void *)k_expert_cluster<4, false, 1>, fs[3] = (const void *)k_expert_cluster<4, false, 2>; break;
+                fs[2] = (const void *)k_expert_cluster<4, false, 1>, fs[3] = (const void *)k_expert_cluster<4, false, 2>,
+                fs[4] = (const void *)k_expert_cluster<4, false, 3>; break;
         default: fs[0] = (const void *)k_expert_cluster<8, false, 0>, fs[1] = (const void *)k_expert_cluster<8, true, 0>,
-                 fs[2] = (const void *)k_expert_cluster<8, false, 1>, fs[3] = (const void *)k_expert_cluster<8, false, 2>; break;
+                 fs[2] = (const void *)k_expert_cluster<8, false, 1>, fs[3] = (const void *)k_expert_cluster<8, false, 2>,
+                fs[4] = (const void *)k_expert_cluster<8, false, 3>; break;
     }
     int least = 1 << 30;
     for (const void *f : fs) {  // every variant must fit; the smallest resident count counts

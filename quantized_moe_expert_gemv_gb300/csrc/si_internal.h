@@ -163,6 +163,8 @@ cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *
 cudaError_t launch_debug_dequant(const uint8_t *blocks, int64_t n_blocks, float *out_f32,
                                  uint16_t *out_bf16, cudaStream_t s);
 cudaError_t launch_debug_nvfp4_f16(const uint8_t *blocks, int64_t n_blocks, float g, uint16_t *out, cudaStream_t s);
+cudaError_t launch_debug_q5k_f16(const uint8_t *blocks, int64_t n_blocks, const float *gamma, uint16_t *out,
+                                 cudaStream_t s);
 cudaError_t launch_debug_dequant_f16(const uint8_t *blocks, int64_t n_blocks, const float *gamma, uint16_t *out,
                                      cudaStream_t s);
 cudaError_t launch_debug_topk(const float *logits, int n, int E, int k, int32_t *ids, float *w,

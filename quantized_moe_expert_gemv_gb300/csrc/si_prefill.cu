@@ -427,7 +427,7 @@ constexpr int kNBuf = 2;                   // accumulator buffers of 256 tensor-
 constexpr int kBRows = 192;                // operand-B rows per CTA and stage
 constexpr int kATile = 128 * 128;          // 128 weight rows x 64 fp16
 constexpr int kBTile = kBRows * 128;       // 192 token rows x 64 fp16
-constexpr int kRaw = 128 * kBlockBytes;    // 128 weight rows x one Q4_K block
+constexpr int kRaw = 128 * kQ5BlockBytes;  // 128 weight rows x one block (room for the larger Q5_K block)
 constexpr int kOffB = kNS * kATile;
 constexpr int kOffRaw = kOffB + kNS * kBTile;
 constexpr int kStgBuf = 8192;              // MODE 0 epilogue staging buffer: 32 tokens x 64 fp16
@@ -529,6 +529,12 @@ __device__ __forceinline__ Pass make_pass(int e, int tile, int prow, int sc, int
 // Returns true when a weight of the sub-block (before the gain) lies beyond
 // fp16's finite range.  The GEMM's dequantization warps and the test export
 // si_debug_q4k_dequant_f16 both run this function.
+// -0 in place of every +0 of a pair of fp32 values.
+__device__ __forceinline__ f32x2 neg_zeros2(f32x2 r) {
+    const float2 v = unpack2(r);
+    return pack2(v.x == 0.f ? -0.f : v.x, v.y == 0.f ? -0.f : v.y);
+}
+
 struct Q4F16Lane {
     uint32_t m0, m8;           // nibble masks at p = 4*half and 4*half + 8
     float tp0, tp8, to0, to8;  // 2^-p and -2^(23-p) for both
@@ -557,6 +563,9 @@ __device__ __forceinline__ bool q4k_subblock_f16(const Q4F16Lane &c, const uint8
     const float dsc = dd * (float)sc, dm = dmin * (float)m;
     const bool bad = fmaxf(fabsf(fmaf(dsc, 15.f, -dm)), fabsf(dm)) > 65504.f;
     const f32x2 C = pack2(dsc * c.tp0, dsc * c.tp8), O = pack2(dsc * c.to0, dsc * c.to8), D = pack2(-dm, -dm);
+    // The fma above gives +0 for a zero code; the exact value d*sc*q - dmin*m is -0
+    // when d*sc is negative (or -0) and dmin*m is +0: those zeros get their sign back.
+    const bool negz = signbit(dsc) && __float_as_uint(dm) == 0u;
     const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
@@ -564,6 +573,54 @@ __device__ __forceinline__ bool q4k_subblock_f16(const Q4F16Lane &c, const uint8
         const f32x2 v01 = pack2(__uint_as_float((w & c.m0) | 0x4B000000u), __uint_as_float((w & c.m8) | 0x4B000000u));
         const f32x2 v23 = pack2(__uint_as_float((hi & c.m0) | 0x4B000000u), __uint_as_float((hi & c.m8) | 0x4B000000u));
         f32x2 r01 = add2(fma2(v01, C, O), D), r23 = add2(fma2(v23, C, O), D);
+        if (negz) r01 = neg_zeros2(r01), r23 = neg_zeros2(r23);
+        if (GAMMA) {
+            const float4 g4 = __ldg(reinterpret_cast<const float4 *>(gp) + t);
+            r01 = mul2(r01, pack2(g4.x, g4.y));
+            r23 = mul2(r23, pack2(g4.z, g4.w));
+        }
+        const float2 a01 = unpack2(r01), a23 = unpack2(r23);
+        o[2 * t] = f16x2_rn(a01.x, a01.y);
+        o[2 * t + 1] = f16x2_rn(a23.x, a23.y);
+    }
+    return bad;
+}
+
+// Q5_K -> fp16 operand conversion, one thread's share: sub-block 2j + half
+// (32 weights).  The 5-bit codes are first gathered one per byte (the four
+// low bits from qs, the fifth from bit 2j+half of qh), then formed as in
+// q4k_subblock_f16 (bytes 0, 1 of a word at p = 0, 8; bytes 2, 3 after a
+// 16-bit shift): w = d*sc*q - dmin*m exact in fp32, rounded once to fp16.
+// Returns true when a weight (before the gain) lies beyond fp16's range.
+template <bool GAMMA>
+__device__ __forceinline__ bool q5k_subblock_f16(const uint8_t *blk, int j, int half, const float *gp,
+                                                 uint32_t (&o)[16]) {
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 h0 = *reinterpret_cast<const uint4 *>(blk + kQ5QhOff);
+    const uint4 h1 = *reinterpret_cast<const uint4 *>(blk + kQ5QhOff + 16);
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(blk + kQ5QsOff + 32 * j);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(blk + kQ5QsOff + 16 + 32 * j);
+    int sc, m;
+    unpack_sc_m(hdr, 2 * j + half, sc, m);
+    const float dd = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffffu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+    const float dsc = dd * (float)sc, dm = dmin * (float)m;
+    const bool bad = fmaxf(fabsf(fmaf(dsc, 31.f, -dm)), fabsf(dm)) > 65504.f;
+    const Q4F16Lane c = q4f16_lane(0);  // 2^-p and -2^(23-p) for p = 0, 8
+    const f32x2 C = pack2(dsc * c.tp0, dsc * c.tp8), O = pack2(dsc * c.to0, dsc * c.to8), D = pack2(-dm, -dm);
+    // The fma above gives +0 for a zero code; the exact value d*sc*q - dmin*m is -0
+    // when d*sc is negative (or -0) and dmin*m is +0: those zeros get their sign back.
+    const bool negz = signbit(dsc) && __float_as_uint(dm) == 0u;
+    const uint32_t qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    constexpr uint32_t m0 = 31u, m8 = 31u << 8;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t w = half ? q5_codes_hi(qv[t], hv[t], j) : q5_codes_lo(qv[t], hv[t], j), hi = w >> 16;
+        const f32x2 v01 = pack2(__uint_as_float((w & m0) | 0x4B000000u), __uint_as_float((w & m8) | 0x4B000000u));
+        const f32x2 v23 = pack2(__uint_as_float((hi & m0) | 0x4B000000u), __uint_as_float((hi & m8) | 0x4B000000u));
+        f32x2 r01 = add2(fma2(v01, C, O), D), r23 = add2(fma2(v23, C, O), D);
+        if (negz) r01 = neg_zeros2(r01), r23 = neg_zeros2(r23);
         if (GAMMA) {
             const float4 g4 = __ldg(reinterpret_cast<const float4 *>(gp) + t);
             r01 = mul2(r01, pack2(g4.x, g4.y));
@@ -648,6 +705,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
                    const __grid_constant__ CUtensorMap tm_h, PrefillArgs a) {
     extern __shared__ uint8_t g_smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(g_smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int BB = WF == 3 ? kQ5BlockBytes : kBlockBytes;  // bytes per weight block (WF 3: Q5_K)
     __shared__ uint32_t s_taddr;
     __shared__ int s_err;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -743,13 +801,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
                         return;
                     }
                     const uint32_t dst = smem_addr(sm + kOffRaw + r * kRaw);
-                    mbar_arrive_expect_tx(raw_full + 8 * r, kRaw);
+                    mbar_arrive_expect_tx(raw_full + 8 * r, 128 * BB);
                     if (MODE == 0) {
                         const int y = ps.e * a.I + ps.tile * 128 + 64 * rank;
-                        tma_load_2d(dst, &tm_a0, kBlockBytes * blk, y, raw_full + 8 * r, pol);
-                        tma_load_2d(dst + 64 * kBlockBytes, &tm_a1, kBlockBytes * blk, y, raw_full + 8 * r, pol);
+                        tma_load_2d(dst, &tm_a0, BB * blk, y, raw_full + 8 * r, pol);
+                        tma_load_2d(dst + 64 * BB, &tm_a1, BB * blk, y, raw_full + 8 * r, pol);
                     } else {
-                        tma_load_2d(dst, &tm_a0, kBlockBytes * blk, ps.e * a.H + ps.tile * 256 + 128 * rank,
+                        tma_load_2d(dst, &tm_a0, BB * blk, ps.e * a.H + ps.tile * 256 + 128 * rank,
                                     raw_full + 8 * r, pol);
                     }
                 }
@@ -857,14 +915,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
                     fail();
                     return;
                 }
-                const uint8_t *blk = sm + kOffRaw + r * kRaw + raw_row * kBlockBytes;
+                const uint8_t *blk = sm + kOffRaw + r * kRaw + raw_row * BB;
                 uint32_t o[16];
                 // pre-normed block: the gate/up weights of hidden column c times gamma_c (the
                 // token's 1 / rms is applied to g and u in the epilogue), so x stays exact
                 const float *gp = (MODE == 0 && NORM) ? gam + 64 * ((kb + ps.rot) % nK) + 32 * half : nullptr;
-                if (WF) {
+                if (WF == 1) {
                     const float g = a.wscale[3 * ps.e + (MODE == 1 ? 2 : (raw_row >= 64 ? 1 : 0))];
                     if (nvfp4_half_f16(blk, j, half, g, o)) set_status(status, SI_ERR_RANGE);
+                } else if (WF == 3) {
+                    if (q5k_subblock_f16<MODE == 0 && NORM>(blk, j, half, gp, o)) set_status(status, SI_ERR_RANGE);
                 } else if (q4k_subblock_f16<MODE == 0 && NORM>(lc, blk, j, half, gp, o)) {
                     set_status(status, SI_ERR_RANGE);
                 }
@@ -1038,6 +1098,32 @@ __global__ void __launch_bounds__(256) k_debug_nvfp4_f16(const uint8_t *blocks, 
     for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
 }
 
+// Test export: the Q5_K operand conversion, as k_debug_dequant_f16.
+__global__ void __launch_bounds__(256) k_debug_q5k_f16(const uint8_t *blocks, int64_t n_blocks, const float *gamma,
+                                                       uint16_t *out) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= n_blocks * 8) return;
+    const int64_t b = t >> 3;
+    const int j = (int)(t & 7) >> 1, half = (int)(t & 1);
+    const uint8_t *blk = blocks + b * kQ5BlockBytes;
+    uint32_t o[16];
+    if (gamma)
+        q5k_subblock_f16<true>(blk, j, half, gamma + 256 * b + 64 * j + 32 * half, o);
+    else
+        q5k_subblock_f16<false>(blk, j, half, nullptr, o);
+    uint4 *dst = reinterpret_cast<uint4 *>(out + 256 * b + 64 * j + 32 * half);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+
+cudaError_t launch_debug_q5k_f16(const uint8_t *blocks, int64_t n_blocks, const float *gamma, uint16_t *out,
+                                 cudaStream_t s) {
+    if (n_blocks == 0) return cudaSuccess;
+    const int64_t threads = n_blocks * 8;
+    k_debug_q5k_f16<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(blocks, n_blocks, gamma, out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_debug_nvfp4_f16(const uint8_t *blocks, int64_t n_blocks, float g, uint16_t *out, cudaStream_t s) {
     if (n_blocks == 0) return cudaSuccess;
     const int64_t threads = n_blocks * 8;
@@ -1071,14 +1157,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return fn;
 }
 
-// Q4_K matrix of all experts as a 2-D byte tensor [rows][blocks_per_row * 144];
-// a box is one 144-byte block column of `box_rows` consecutive rows.
-static bool q4k_map(const uint8_t *base, int64_t rows, int blocks_per_row, int box_rows, CUtensorMap *tm) {
+// A block-quantised matrix of all experts as a 2-D byte tensor
+// [rows][blocks_per_row * bb] (bb = 144 for Q4_K and NVFP4, 176 for Q5_K); a box
+// is one bb-byte block column of `box_rows` consecutive rows.
+static bool q4k_map(const uint8_t *base, int64_t rows, int blocks_per_row, int box_rows, int bb, CUtensorMap *tm) {
     auto enc = encoder();
     if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)blocks_per_row * kBlockBytes, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)blocks_per_row * kBlockBytes};
-    cuuint32_t box[2] = {(cuuint32_t)kBlockBytes, (cuuint32_t)box_rows};
+    cuuint64_t dims[2] = {(cuuint64_t)blocks_per_row * bb, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)blocks_per_row * bb};
+    cuuint32_t box[2] = {(cuuint32_t)bb, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1106,11 +1193,12 @@ cudaError_t prefill_prepare(const Plan &p) {
     if (!encoder()) return cudaErrorNotSupported;
     cudaError_t err = cudaFuncSetAttribute(k_prefill_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
     if (err != cudaSuccess) return err;
-    const void *fs[5] = {(const void *)k_prefill_gemm<0, false, 0>, (const void *)k_prefill_gemm<0, true, 0>,
+    const void *fs[8] = {(const void *)k_prefill_gemm<0, false, 0>, (const void *)k_prefill_gemm<0, true, 0>,
                          (const void *)k_prefill_gemm<1, false, 0>, (const void *)k_prefill_gemm<0, false, 1>,
-                         (const void *)k_prefill_gemm<1, false, 1>};
+                         (const void *)k_prefill_gemm<1, false, 1>, (const void *)k_prefill_gemm<0, false, 3>,
+                         (const void *)k_prefill_gemm<1, false, 3>, nullptr};
     for (const void *f : fs)
-        if ((err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem)) != cudaSuccess)
+        if (f && (err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem)) != cudaSuccess)
             return err;
     return cudaSuccess;
 }
@@ -1149,23 +1237,30 @@ cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, 
 
     // operand B: token rows in boxes of 64 and of 16 rows (a CTA's half of a chunk is 64*a + 16*b rows)
     CUtensorMap tg, tu, td, txp64, txp16, th64, th16, ths;
-    if (!q4k_map(a.wg, (int64_t)a.E * a.I, a.H / kQK, 64, &tg) || !q4k_map(a.wu, (int64_t)a.E * a.I, a.H / kQK, 64, &tu) ||
-        !q4k_map(a.wd, (int64_t)a.E * a.H, a.I / kQK, 128, &td) ||
+    const int bb = a.wtype == SI_WTYPE_Q5_K ? kQ5BlockBytes : kBlockBytes;
+    if (!q4k_map(a.wg, (int64_t)a.E * a.I, a.H / kQK, 64, bb, &tg) ||
+        !q4k_map(a.wu, (int64_t)a.E * a.I, a.H / kQK, 64, bb, &tu) ||
+        !q4k_map(a.wd, (int64_t)a.E * a.H, a.I / kQK, 128, bb, &td) ||
         !mat_map(a.xp, a.rows, a.H, 2, 64, 64, true, &txp64) || !mat_map(a.xp, a.rows, a.H, 2, 64, 16, true, &txp16) ||
         !mat_map(a.h, a.rows, a.I, 2, 64, 64, true, &th64) || !mat_map(a.h, a.rows, a.I, 2, 64, 16, true, &th16) ||
         !mat_map(a.h, a.rows, a.I, 2, 64, 32, false, &ths))
         return cudaErrorInvalidValue;
     // one CTA pair (2-CTA cluster, declared on the kernel) per two SMs
     const int grid = 2 * (p.sm_count / 2);
+    const bool q5 = a.wtype == SI_WTYPE_Q5_K;  // (the API takes Q5_K in plain blocks only)
     if (a.norm_w)  // pre-normed block: gamma folded into the weights, 1 / rms into the epilogue
         k_prefill_gemm<0, true, 0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
+    else if (q5)
+        k_prefill_gemm<0, false, 3><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
     else if (a.wtype == SI_WTYPE_NVFP4)
         k_prefill_gemm<0, false, 1><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
     else
         k_prefill_gemm<0, false, 0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 2, s)) != cudaSuccess) return err;
-    if (a.wtype == SI_WTYPE_NVFP4)
+    if (q5)
+        k_prefill_gemm<1, false, 3><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
+    else if (a.wtype == SI_WTYPE_NVFP4)
         k_prefill_gemm<1, false, 1><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
     else
         k_prefill_gemm<1, false, 0><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
