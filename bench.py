@@ -19,7 +19,8 @@ region, the CPU oracle's throughput on a bounded sample, and (unless
 --no-extras) the 48-layer stack, the 4-token deduplicated workload, the
 headline workload as a pre-normed block, the 4096-token grouped prefill
 with its tensor-core roofline, the headline decode and the prefill with
-NVFP4 experts, and the headline decode in the int8-activation mode.
+NVFP4 experts, the headline decode in the int8-activation mode, and the
+headline decode and the prefill with Q5_K experts.
 
 --impl reference times the CPU oracle (the reference implementation of the
 method) on a bounded sample of the same workload on the host cores.
@@ -85,7 +86,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extras", action="store_true",
-                   help="skip the stack, dedup, pre-normed, prefill, NVFP4 and int8-activation workloads")
+                   help="skip the stack, dedup, pre-normed, prefill, NVFP4, int8-activation and Q5_K workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--tokens", type=int, default=0,
                    help="tokens per step of the headline layer (default 1024; small values for ncu)")
@@ -583,6 +584,35 @@ def bench_nvfp4(args, dist, binding, device, synth, torch, hbm_peak):
             "gpu_launches": {2: 2, 1: 2}.get(path, 3) * T * steps}
 
 
+def bench_q5k(args, dist, binding, device, synth, torch, hbm_peak):
+    """The headline decode workload (1024 sequential single-token calls in one
+    CUDA graph) with Q5_K experts (176 bytes per 256 weights)."""
+    wl = synth.WORKLOADS["layer"]
+    shape, seed, T = wl["shape"], wl["seed"], 1024
+    layer = synth.make_layer_q5k(shape, seed=seed)
+    dl = device.to_device(layer)
+    plan = binding.si_moe_plan(device.desc_for(shape, wtype=binding.SI_WTYPE_Q5_K), torch.cuda.current_device())
+    scratch = device.alloc_scratch(plan, binding.SI_MODE_DECODE, 1)
+    x = device.tokens_to_device(synth.make_tokens(shape, seed, T))
+    out = torch.empty((T, shape.hidden), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    g = build_layer_graph(binding, plan, dl.struct(), [x[t] for t in range(T)], [out[t] for t in range(T)],
+                          scratch, stream)
+    steps = max(1, args.steps // 2)
+    ms, clocks = time_graph(g, stream, steps, args.warmup, dist, ClockSampler(torch.cuda.current_device()))
+    st = binding.si_moe_read_status(plan, scratch, stream)
+    assert st == binding.SI_OK, binding.si_status_string(st)
+    tok_s = T * steps / (ms / 1e3)
+    expert_bytes = shape.top_k * 3 * shape.hidden * shape.intermediate // 256 * synth.Q5K_BLOCK_BYTES
+    gbs = expert_bytes * tok_s / 1e9
+    path = binding.si_debug_decode_fused(plan, 1)
+    del g
+    return {"workload": "qwen3-30b-a3b-moe-layer-decode-bs1 with Q5_K experts (176 B / 256 weights), 1024 tokens",
+            "tok_per_s": dist.sum(tok_s), "us_per_token": 1e6 / tok_s, "expert_bytes_per_token": expert_bytes,
+            "achieved_gbs": gbs, "frac_of_peak": gbs / hbm_peak, "clocks": clocks,
+            "gpu_launches": {2: 2, 1: 2}.get(path, 3) * T * steps}
+
+
 def bench_act8(args, dist, binding, device, synth, torch, hbm_peak):
     """The headline decode workload (1024 sequential single-token calls in one
     CUDA graph) in the int8-activation mode (SI_FLAG_ACT_INT8: x and h int8
@@ -628,15 +658,16 @@ def tensor_peak():
     return 1900.0, 1700.0, "fallback (1.9 PFLOP/s burst, 1.7 sustained)"
 
 
-def bench_prefill(args, dist, binding, device, synth, torch, nvfp4=False):
+def bench_prefill(args, dist, binding, device, synth, torch, nvfp4=False, q5k=False):
     """Grouped prefill of 4096 tokens through one layer of the Qwen3-30B-A3B
     shape: routing + two tensor-core GEMMs + combine, per call (Q4_K experts,
-    or NVFP4 experts with nvfp4=True)."""
+    NVFP4 experts with nvfp4=True, Q5_K experts with q5k=True)."""
     wl = synth.WORKLOADS["prefill"]
     shape, seed, T = wl["shape"], wl["seed"], wl["n_tokens"]
-    layer = synth.make_layer_nvfp4(shape, seed=seed) if nvfp4 else synth.make_layer(shape, seed=seed)
+    layer = (synth.make_layer_nvfp4(shape, seed=seed) if nvfp4 else
+             synth.make_layer_q5k(shape, seed=seed) if q5k else synth.make_layer(shape, seed=seed))
     dl = device.to_device(layer)
-    wtype = binding.SI_WTYPE_NVFP4 if nvfp4 else binding.SI_WTYPE_Q4_K
+    wtype = binding.SI_WTYPE_NVFP4 if nvfp4 else binding.SI_WTYPE_Q5_K if q5k else binding.SI_WTYPE_Q4_K
     plan = binding.si_moe_plan(device.desc_for(shape, max_tokens=T, wtype=wtype), torch.cuda.current_device())
     scratch = device.alloc_scratch(plan, binding.SI_MODE_PREFILL, T)
     x = device.tokens_to_device(synth.make_tokens(shape, seed, T))
@@ -683,7 +714,7 @@ def bench_prefill(args, dist, binding, device, synth, torch, nvfp4=False):
     tok_s = T / (ms * 1e-3)
     del scratch
     return {"workload": "grouped prefill, 4096 tokens x top-8 of 128 experts, one Qwen3-30B-A3B layer, seed 4" +
-                        (", NVFP4 experts" if nvfp4 else ""),
+                        (", NVFP4 experts" if nvfp4 else ", Q5_K experts" if q5k else ""),
             "tok_per_s": dist.sum(tok_s), "ms_per_call": ms,
             "kernels_ms": {"routing_counts_perm": parts[0], "gemm_gateup_swiglu": parts[1],
                            "gemm_down_weight": parts[2], "combine": parts[3]},
@@ -750,6 +781,12 @@ def run_ours(args, dist):
             line["act8"] = bench_act8(args, dist, binding, device, synth, torch, hbm_peak)
         except Exception as exc:
             line["act8"] = {"error": repr(exc)}
+        torch.cuda.empty_cache()
+        try:
+            line["q5k"] = bench_q5k(args, dist, binding, device, synth, torch, hbm_peak)
+            line["q5k"]["prefill"] = bench_prefill(args, dist, binding, device, synth, torch, q5k=True)
+        except Exception as exc:
+            line["q5k"] = {"error": repr(exc)}
     # two-sided guard: an achieved fraction of a measured peak above 1.0 means the timed
     # region did not do the work it is credited with
     fracs = {"roofline": line["roofline"].get("frac"), "chain": line.get("chain", {}).get("frac_of_peak")}
