@@ -427,21 +427,27 @@ constexpr int kNBuf = 2;                   // accumulator buffers of 256 tensor-
 constexpr int kBRows = 192;                // operand-B rows per CTA and stage
 constexpr int kATile = 128 * 128;          // 128 weight rows x 64 fp16
 constexpr int kBTile = kBRows * 128;       // 192 token rows x 64 fp16
-constexpr int kRaw = 128 * kQ5BlockBytes;  // 128 weight rows x one block (room for the larger Q5_K block)
+// 128 weight rows x one block; the regions after the raw stages depend on the
+// block size (144 bytes for Q4_K and NVFP4, 176 for Q5_K)
+__host__ __device__ constexpr int gemm_raw(int bb) { return 128 * bb; }
 constexpr int kOffB = kNS * kATile;
 constexpr int kOffRaw = kOffB + kNS * kBTile;
 constexpr int kStgBuf = 8192;              // MODE 0 epilogue staging buffer: 32 tokens x 64 fp16
-constexpr int kOffStg = kOffRaw + kNR * kRaw;
-constexpr int kOffBar = kOffStg + 2 * kStgBuf;
+__host__ __device__ constexpr int gemm_off_stg(int bb) { return kOffRaw + kNR * gemm_raw(bb); }
+__host__ __device__ constexpr int gemm_off_bar(int bb) { return gemm_off_stg(bb) + 2 * kStgBuf; }
 constexpr int kNBar = 2 * kNR + 2 * kNS + 2 * kNBuf + 2;
-constexpr int kOffTok = (kOffBar + kNBar * 8 + 15) & ~15;  // 16-byte readiness tokens [kNS][8], copied odd -> even CTA
-constexpr int kGemmSmem = kOffTok + 16 * 8 * kNS + 16 + 1024;  // + alignment slack
-static_assert(kGemmSmem + 64 <= 232448, "shared memory plan exceeds the per-CTA limit");
+// 16-byte readiness tokens [kNS][8], copied odd -> even CTA
+__host__ __device__ constexpr int gemm_off_tok(int bb) { return (gemm_off_bar(bb) + kNBar * 8 + 15) & ~15; }
+__host__ __device__ constexpr int gemm_smem(int bb) { return gemm_off_tok(bb) + 16 * 8 * kNS + 16 + 1024; }  // + alignment slack
+static_assert(gemm_smem(kQ5BlockBytes) + 64 <= 232448, "shared memory plan exceeds the per-CTA limit");
 static_assert(kATile % 1024 == 0 && kOffB % 1024 == 0 && kBTile % 1024 == 0 && (kChunkRows * 128) % 1024 == 0,
               "128-byte-swizzled operand tiles start on 1024-byte boundaries");
-static_assert(kOffRaw % 128 == 0 && kRaw % 128 == 0 && kOffStg % 128 == 0 && kStgBuf % 128 == 0,
+static_assert(kOffRaw % 128 == 0 && gemm_raw(kBlockBytes) % 128 == 0 && gemm_raw(kQ5BlockBytes) % 128 == 0 &&
+                  gemm_off_stg(kBlockBytes) % 128 == 0 && gemm_off_stg(kQ5BlockBytes) % 128 == 0 && kStgBuf % 128 == 0,
               "tensor-map copy destinations and sources are 128-byte aligned");
-static_assert(kOffBar % 8 == 0 && kOffTok % 16 == 0, "mbarriers 8-byte, bulk-copy tokens 16-byte aligned");
+static_assert(gemm_off_bar(kBlockBytes) % 8 == 0 && gemm_off_tok(kBlockBytes) % 16 == 0 &&
+                  gemm_off_bar(kQ5BlockBytes) % 8 == 0 && gemm_off_tok(kQ5BlockBytes) % 16 == 0,
+              "mbarriers 8-byte, bulk-copy tokens 16-byte aligned");
 constexpr long long kDrainG = 4000000000LL;
 constexpr uint16_t kPairMask = 3;          // both CTAs of the pair
 
@@ -529,12 +535,6 @@ __device__ __forceinline__ Pass make_pass(int e, int tile, int prow, int sc, int
 // Returns true when a weight of the sub-block (before the gain) lies beyond
 // fp16's finite range.  The GEMM's dequantization warps and the test export
 // si_debug_q4k_dequant_f16 both run this function.
-// -0 in place of every +0 of a pair of fp32 values.
-__device__ __forceinline__ f32x2 neg_zeros2(f32x2 r) {
-    const float2 v = unpack2(r);
-    return pack2(v.x == 0.f ? -0.f : v.x, v.y == 0.f ? -0.f : v.y);
-}
-
 struct Q4F16Lane {
     uint32_t m0, m8;           // nibble masks at p = 4*half and 4*half + 8
     float tp0, tp8, to0, to8;  // 2^-p and -2^(23-p) for both
@@ -550,6 +550,33 @@ __device__ __forceinline__ Q4F16Lane q4f16_lane(int half) {
     c.to8 = -__uint_as_float((142u - p0) << 23);
     return c;
 }
+// The 32 weights of one sub-block from its code words cw (a code at mask m0
+// of a word -- bit position p -- and at m8 -- p + 8 --, and likewise in the
+// word's upper half): 2^23 + q*2^p by or-ing in an exponent; with s = -1 when
+// d*sc is negative (or -0), else 1, fma(., s*d*sc*2^-p, -s*d*sc*2^(23-p)) =
+// s*d*sc*q exactly (+0 for q = 0), and fma(that, s, -dmin*m) rounds once to
+// the fp32 weight, with the sign of zero the exact expression d*sc*q - dmin*m
+// has; times the gain with GAMMA; rounded to fp16.
+template <bool GAMMA>
+__device__ __forceinline__ void codes_to_f16(const uint32_t (&cw)[8], uint32_t m0, uint32_t m8, f32x2 C, f32x2 O,
+                                             f32x2 S, f32x2 D, const float *gp, uint32_t (&o)[16]) {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t w = cw[t], hi = w >> 16;
+        const f32x2 v01 = pack2(__uint_as_float((w & m0) | 0x4B000000u), __uint_as_float((w & m8) | 0x4B000000u));
+        const f32x2 v23 = pack2(__uint_as_float((hi & m0) | 0x4B000000u), __uint_as_float((hi & m8) | 0x4B000000u));
+        f32x2 r01 = fma2(fma2(v01, C, O), S, D), r23 = fma2(fma2(v23, C, O), S, D);
+        if (GAMMA) {
+            const float4 g4 = __ldg(reinterpret_cast<const float4 *>(gp) + t);
+            r01 = mul2(r01, pack2(g4.x, g4.y));
+            r23 = mul2(r23, pack2(g4.z, g4.w));
+        }
+        const float2 a01 = unpack2(r01), a23 = unpack2(r23);
+        o[2 * t] = f16x2_rn(a01.x, a01.y);
+        o[2 * t + 1] = f16x2_rn(a23.x, a23.y);
+    }
+}
+
 template <bool GAMMA>
 __device__ __forceinline__ bool q4k_subblock_f16(const Q4F16Lane &c, const uint8_t *blk, int j, int half,
                                                  const float *gp, uint32_t (&o)[16]) {
@@ -562,27 +589,11 @@ __device__ __forceinline__ bool q4k_subblock_f16(const Q4F16Lane &c, const uint8
     const float dmin = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
     const float dsc = dd * (float)sc, dm = dmin * (float)m;
     const bool bad = fmaxf(fabsf(fmaf(dsc, 15.f, -dm)), fabsf(dm)) > 65504.f;
-    const f32x2 C = pack2(dsc * c.tp0, dsc * c.tp8), O = pack2(dsc * c.to0, dsc * c.to8), D = pack2(-dm, -dm);
-    // The fma above gives +0 for a zero code; the exact value d*sc*q - dmin*m is -0
-    // when d*sc is negative (or -0) and dmin*m is +0: those zeros get their sign back.
-    const bool negz = signbit(dsc) && __float_as_uint(dm) == 0u;
+    const float sg = signbit(dsc) ? -1.f : 1.f, sd = sg * dsc;
+    const f32x2 C = pack2(sd * c.tp0, sd * c.tp8), O = pack2(sd * c.to0, sd * c.to8), S = pack2(sg, sg),
+                D = pack2(-dm, -dm);
     const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        const uint32_t w = wv[t], hi = w >> 16;
-        const f32x2 v01 = pack2(__uint_as_float((w & c.m0) | 0x4B000000u), __uint_as_float((w & c.m8) | 0x4B000000u));
-        const f32x2 v23 = pack2(__uint_as_float((hi & c.m0) | 0x4B000000u), __uint_as_float((hi & c.m8) | 0x4B000000u));
-        f32x2 r01 = add2(fma2(v01, C, O), D), r23 = add2(fma2(v23, C, O), D);
-        if (negz) r01 = neg_zeros2(r01), r23 = neg_zeros2(r23);
-        if (GAMMA) {
-            const float4 g4 = __ldg(reinterpret_cast<const float4 *>(gp) + t);
-            r01 = mul2(r01, pack2(g4.x, g4.y));
-            r23 = mul2(r23, pack2(g4.z, g4.w));
-        }
-        const float2 a01 = unpack2(r01), a23 = unpack2(r23);
-        o[2 * t] = f16x2_rn(a01.x, a01.y);
-        o[2 * t + 1] = f16x2_rn(a23.x, a23.y);
-    }
+    codes_to_f16<GAMMA>(wv, c.m0, c.m8, C, O, S, D, gp, o);
     return bad;
 }
 
@@ -607,29 +618,15 @@ __device__ __forceinline__ bool q5k_subblock_f16(const uint8_t *blk, int j, int 
     const float dsc = dd * (float)sc, dm = dmin * (float)m;
     const bool bad = fmaxf(fabsf(fmaf(dsc, 31.f, -dm)), fabsf(dm)) > 65504.f;
     const Q4F16Lane c = q4f16_lane(0);  // 2^-p and -2^(23-p) for p = 0, 8
-    const f32x2 C = pack2(dsc * c.tp0, dsc * c.tp8), O = pack2(dsc * c.to0, dsc * c.to8), D = pack2(-dm, -dm);
-    // The fma above gives +0 for a zero code; the exact value d*sc*q - dmin*m is -0
-    // when d*sc is negative (or -0) and dmin*m is +0: those zeros get their sign back.
-    const bool negz = signbit(dsc) && __float_as_uint(dm) == 0u;
+    const float sg = signbit(dsc) ? -1.f : 1.f, sd = sg * dsc;
+    const f32x2 C = pack2(sd * c.tp0, sd * c.tp8), O = pack2(sd * c.to0, sd * c.to8), S = pack2(sg, sg),
+                D = pack2(-dm, -dm);
     const uint32_t qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
     const uint32_t hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-    constexpr uint32_t m0 = 31u, m8 = 31u << 8;
+    uint32_t cw[8];  // one 5-bit code per byte
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        const uint32_t w = half ? q5_codes_hi(qv[t], hv[t], j) : q5_codes_lo(qv[t], hv[t], j), hi = w >> 16;
-        const f32x2 v01 = pack2(__uint_as_float((w & m0) | 0x4B000000u), __uint_as_float((w & m8) | 0x4B000000u));
-        const f32x2 v23 = pack2(__uint_as_float((hi & m0) | 0x4B000000u), __uint_as_float((hi & m8) | 0x4B000000u));
-        f32x2 r01 = add2(fma2(v01, C, O), D), r23 = add2(fma2(v23, C, O), D);
-        if (negz) r01 = neg_zeros2(r01), r23 = neg_zeros2(r23);
-        if (GAMMA) {
-            const float4 g4 = __ldg(reinterpret_cast<const float4 *>(gp) + t);
-            r01 = mul2(r01, pack2(g4.x, g4.y));
-            r23 = mul2(r23, pack2(g4.z, g4.w));
-        }
-        const float2 a01 = unpack2(r01), a23 = unpack2(r23);
-        o[2 * t] = f16x2_rn(a01.x, a01.y);
-        o[2 * t + 1] = f16x2_rn(a23.x, a23.y);
-    }
+    for (int t = 0; t < 8; ++t) cw[t] = half ? q5_codes_hi(qv[t], hv[t], j) : q5_codes_lo(qv[t], hv[t], j);
+    codes_to_f16<GAMMA>(cw, 31u, 31u << 8, C, O, S, D, gp, o);
     return bad;
 }
 
@@ -706,6 +703,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGThreads, 1)
     extern __shared__ uint8_t g_smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(g_smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int BB = WF == 3 ? kQ5BlockBytes : kBlockBytes;  // bytes per weight block (WF 3: Q5_K)
+    constexpr int kRaw = gemm_raw(BB), kOffStg = gemm_off_stg(BB), kOffBar = gemm_off_bar(BB),
+                  kOffTok = gemm_off_tok(BB);
     __shared__ uint32_t s_taddr;
     __shared__ int s_err;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1198,7 +1197,9 @@ cudaError_t prefill_prepare(const Plan &p) {
                          (const void *)k_prefill_gemm<1, false, 1>, (const void *)k_prefill_gemm<0, false, 3>,
                          (const void *)k_prefill_gemm<1, false, 3>, nullptr};
     for (const void *f : fs)
-        if (f && (err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem)) != cudaSuccess)
+        if (f && (err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             gemm_smem(f == fs[5] || f == fs[6] ? kQ5BlockBytes : kBlockBytes))) !=
+                     cudaSuccess)
             return err;
     return cudaSuccess;
 }
@@ -1249,21 +1250,21 @@ cudaError_t launch_prefill(const Plan &p, const PrefillArgs &a, cudaStream_t s, 
     const int grid = 2 * (p.sm_count / 2);
     const bool q5 = a.wtype == SI_WTYPE_Q5_K;  // (the API takes Q5_K in plain blocks only)
     if (a.norm_w)  // pre-normed block: gamma folded into the weights, 1 / rms into the epilogue
-        k_prefill_gemm<0, true, 0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
+        k_prefill_gemm<0, true, 0><<<grid, kGThreads, gemm_smem(kBlockBytes), s>>>(tg, tu, txp64, txp16, ths, a);
     else if (q5)
-        k_prefill_gemm<0, false, 3><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
+        k_prefill_gemm<0, false, 3><<<grid, kGThreads, gemm_smem(kQ5BlockBytes), s>>>(tg, tu, txp64, txp16, ths, a);
     else if (a.wtype == SI_WTYPE_NVFP4)
-        k_prefill_gemm<0, false, 1><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
+        k_prefill_gemm<0, false, 1><<<grid, kGThreads, gemm_smem(kBlockBytes), s>>>(tg, tu, txp64, txp16, ths, a);
     else
-        k_prefill_gemm<0, false, 0><<<grid, kGThreads, kGemmSmem, s>>>(tg, tu, txp64, txp16, ths, a);
+        k_prefill_gemm<0, false, 0><<<grid, kGThreads, gemm_smem(kBlockBytes), s>>>(tg, tu, txp64, txp16, ths, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 2, s)) != cudaSuccess) return err;
     if (q5)
-        k_prefill_gemm<1, false, 3><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
+        k_prefill_gemm<1, false, 3><<<grid, kGThreads, gemm_smem(kQ5BlockBytes), s>>>(td, td, th64, th16, ths, a);
     else if (a.wtype == SI_WTYPE_NVFP4)
-        k_prefill_gemm<1, false, 1><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
+        k_prefill_gemm<1, false, 1><<<grid, kGThreads, gemm_smem(kBlockBytes), s>>>(td, td, th64, th16, ths, a);
     else
-        k_prefill_gemm<1, false, 0><<<grid, kGThreads, kGemmSmem, s>>>(td, td, th64, th16, ths, a);
+        k_prefill_gemm<1, false, 0><<<grid, kGThreads, gemm_smem(kBlockBytes), s>>>(td, td, th64, th16, ths, a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if ((err = mark(events, 3, s)) != cudaSuccess) return err;
     const size_t n4 = (size_t)a.T * (a.H / 4);
