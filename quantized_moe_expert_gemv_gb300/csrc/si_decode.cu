@@ -673,6 +673,10 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
     __syncthreads();
     cluster_arrive_relaxed();
     pdl_wait();  // x and the scratch are ready (previous kernels complete)
+    // the chunk of x this warp quantises for the expert kernel (at most one: H/64 <= 8*WPC), loaded
+    // together with the columns of the dot product
+    const int qc = blockIdx.x + C * warp;
+    const uint32_t qword = qc < H / 64 ? __ldg(reinterpret_cast<const uint32_t *>(xg_p) + 32 * qc + lane) : 0u;
     float xf[CPT];
     {
         const uint16_t *xp = xg_p + CPT * threadIdx.x;
@@ -727,12 +731,7 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
         if (lane == 0 && ologits_p) ologits_p[e] = z;
     }
     // x quantised per 64-column chunk for the expert kernel (as in k_router_topk)
-    {
-        const uint32_t *xw32 = reinterpret_cast<const uint32_t *>(xg_p);
-        const int NC = H / 64;
-        const bool act8 = pin_i32(a.act8) != 0;
-        for (int c = blockIdx.x + C * warp; c < NC; c += C * WPC) router_quant_chunk(xw32[32 * c + lane], c, NC, xq_p, lane, act8);
-    }
+    if (qc < H / 64) router_quant_chunk(qword, qc, H / 64, xq_p, lane, pin_i32(a.act8) != 0);
     if (!mbar_wait_warp_cluster(smem_addr(&s_zbar), 0, a.wait_budget)) set_status(a.ctrl + kCtrlStatus, SI_ERR_TIMEOUT);
     // warp q ranks expert e0 + q against all E logits (greater, or equal with a
     // lower index, beats it) and stores it at its rank if selected
