@@ -92,6 +92,9 @@ def parse_args():
                    help="tokens per step of the headline layer (default 1024; small values for ncu)")
     p.add_argument("--prefill-only", action="store_true",
                    help="time only the grouped prefill workload (for profiling its kernels)")
+    p.add_argument("--dedup-probe", type=int, default=0, metavar="S",
+                   help="run only S steps of the 4-token deduplicated workload as plain launches and print "
+                        "each step's distinct experts (for a per-launch DRAM capture of the expert kernel)")
     p.add_argument("--cpu-sample-tokens", type=int, default=0,
                    help="tokens of the CPU oracle sample (default: 16 per host core, at least 64)")
     return p.parse_args()
@@ -728,12 +731,44 @@ def bench_prefill(args, dist, binding, device, synth, torch, nvfp4=False, q5k=Fa
             "calls_timed": reps, "clocks": clocks, "gpu_launches": 6 * reps}
 
 
+def dedup_probe(args, binding, device, synth, torch):
+    """S steps of the dedup4 workload, launched one after another on a stream (no
+    graph), so that a profiler sees one expert-kernel launch per step; prints the
+    distinct experts of every step and the bytes each of them has."""
+    wl = synth.WORKLOADS["dedup4"]
+    shape, seed, n = wl["shape"], wl["seed"], wl["tokens_per_step"]
+    S = args.dedup_probe
+    bias = synth.dedup_router_bias(seed, synth.load_dedup_beta())
+    layer = synth.make_layer(shape, seed=seed, router_bias=bias)
+    dl = device.to_device(layer)
+    plan = binding.si_moe_plan(device.desc_for(shape), torch.cuda.current_device())
+    scratch = device.alloc_scratch(plan, binding.SI_MODE_DECODE, n)
+    x = device.tokens_to_device(synth.make_tokens(shape, seed, n * S)).view(S, n, shape.hidden)
+    out = torch.empty((S, n, shape.hidden), dtype=torch.float32, device="cuda")
+    counts = torch.zeros((S, shape.n_experts), dtype=torch.int32, device="cuda")
+    L = dl.struct()
+    for s in range(S):
+        binding.si_moe_forward_decode(plan, L, x[s], n, out[s], binding.route_struct(expert_counts=counts[s]),
+                                      scratch)
+    torch.cuda.synchronize()
+    st = binding.si_moe_read_status(plan, scratch)
+    assert st == binding.SI_OK, binding.si_status_string(st)
+    U = (counts > 0).sum(dim=1).tolist()
+    return {"dedup_probe_steps": S, "unique_experts_per_step": U, "bytes_per_expert": shape.expert_bytes,
+            "expert_kernel": "k_expert" if binding.si_debug_decode_fused(plan, n) >= 1 else "generic"}
+
+
 def run_ours(args, dist):
     import torch
     from quantized_moe_expert_gemv_gb300 import binding, build, device, synth
     build.build()
     binding.load_library()
     torch.cuda.set_device(dist.local)
+    if args.dedup_probe:
+        res = dedup_probe(args, binding, device, synth, torch)
+        if dist.rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     if args.prefill_only:
         res = bench_prefill(args, dist, binding, device, synth, torch)
         if dist.rank == 0:
