@@ -250,6 +250,8 @@ si_status si_moe_read_status_noalloc(si_stream_t stream);
 
 /* Test/bench export: which expert kernels decode of n_tokens tokens runs
  * after the router launch: 2 = the cluster kernel (one launch, n_tokens == 1),
+ * 3 = the cluster kernel over the distinct experts (one launch, 2..4 tokens of
+ * a block that is not pre-normed; a pre-normed block takes the next choice),
  * 1 = the grid-synchronised fused kernel (one launch), 0 = the generic
  * gate/up + down kernels (two launches); -1 on a bad argument. */
 int si_debug_decode_fused(si_moe_plan_t plan, int32_t n_tokens);

@@ -55,7 +55,7 @@ DecodeLayout decode_layout(const si_moe_desc &d, int n) {
     L.counts = take((size_t)d.n_experts * sizeof(int32_t));
     L.uniq = take(sizeof(UniqTable));
     L.h = take((size_t)n * d.top_k * d.intermediate * sizeof(float));
-    L.xq = take((size_t)(d.hidden / 64) * kXqWords * sizeof(uint32_t));
+    L.xq = take((size_t)n * (d.hidden / 64) * kXqWords * sizeof(uint32_t));
     L.total = o;
     return L;
 }
@@ -175,6 +175,22 @@ si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *o
                 p.cluster_ok = true;
                 p.cluster_size = C;
                 p.cluster_active = clusters;
+            }
+            cudaGetLastError();
+        }
+        // 2..4 plain Q4_K tokens: the same clusters over the distinct experts, in waves
+        p.cluster_mt_ok = false;
+        p.cluster_mt_active = 0;
+        si::DecodeArgs tmp{};
+        // (the int8-activation flag applies to single tokens only: batched tokens keep int16)
+        if (p.cluster_ok && desc->wtype == SI_WTYPE_Q4_K &&
+            si::expert_cluster_layout(*desc, p.cluster_size, p.smem_optin, tmp, SI_MAX_DECODE_TOKENS)) {
+            int clusters = 0;
+            if (si::expert_cluster_prepare(desc->hidden / 256, p.smem_optin, tmp.cl_smem, p.cluster_size, &clusters,
+                                           true) == cudaSuccess &&
+                clusters >= 1) {
+                p.cluster_mt_ok = true;
+                p.cluster_mt_active = clusters;
             }
             cudaGetLastError();
         }
@@ -423,6 +439,7 @@ int si_debug_plan_info(si_moe_plan_t plan, int32_t *info, int32_t n) {
 int si_debug_decode_fused(si_moe_plan_t plan, int32_t n_tokens) {
     if (!plan || n_tokens < 1 || n_tokens > SI_MAX_DECODE_TOKENS) return -1;
     if (n_tokens == 1 && plan->p.cluster_ok) return 2;
+    if (n_tokens > 1 && plan->p.cluster_mt_ok) return 3;
     return plan->p.fused_ok[n_tokens] ? 1 : 0;
 }
 

@@ -133,11 +133,12 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
     int32_t *const ocounts_p = pin_ptr(a.o_counts);
     uint32_t *const xq_p = pin_ptr(a.xq);
     const int n = pin_i32(a.n), H = pin_i32(a.H), E = pin_i32(a.E), k = pin_i32(a.k);
-    const int zero_out = pin_i32(a.zero_out), sel_logits = pin_i32(a.sel_logits);
-    // One plain token for the cluster expert kernel: that kernel's work before its
-    // own dependency wait reads nothing this call produces (x is quantised here),
-    // so it may be launched at once and be resident when this grid completes.
-    const bool early_dependents = !NORM && sel_logits;
+    const int zero_out = pin_i32(a.zero_out), sel_logits = pin_i32(a.sel_logits), mt = pin_i32(a.cl_mt);
+    // Plain tokens for a cluster expert kernel (one token, or 2..4 over the distinct
+    // experts): that kernel's work before its own dependency wait reads nothing this
+    // call produces (x is quantised here), so it may be launched at once and be
+    // resident when this grid completes.
+    const bool early_dependents = !NORM && (sel_logits || mt);
     if (early_dependents) pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wpc = blockDim.x >> 5;
@@ -266,16 +267,20 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
             }
         }
     }
-    // One plain token for the cluster expert kernel: quantise x per 64-column chunk
-    // into the scratch (int16 pairs, xq = rint(x / s), s = max|x| / 32767; the two
-    // 32-column sums; the four 16-column sums of xq), one warp per chunk, in the
-    // layout the expert kernel copies into its shared memory as it is.
+    // Plain tokens for a cluster expert kernel: quantise x per 64-column chunk into
+    // the scratch (int16 pairs, xq = rint(x / s), s = max|x| / 32767; the two
+    // 32-column sums; the four 16-column sums of xq), one warp per chunk, token t at
+    // word t * NC * kXqWords, in the layout the expert kernel copies into its shared
+    // memory as it is.
     if (early_dependents) {
         const uint32_t *xw32 = NJ > 0 ? reinterpret_cast<const uint32_t *>(s_x) : reinterpret_cast<const uint32_t *>(xg_p);
         const int NC = H / 64;
         const bool act8 = pin_i32(a.act8) != 0;
-        for (int c = blockIdx.x + gridDim.x * warp; c < NC; c += gridDim.x * wpc)
-            router_quant_chunk(xw32[32 * c + lane], c, NC, xq_p, lane, act8);
+        for (int c = blockIdx.x + gridDim.x * warp; c < n * NC; c += gridDim.x * wpc) {
+            const int t = c / NC, cc = c - t * NC;
+            router_quant_chunk(xw32[(size_t)t * (H / 2) + 32 * cc + lane], cc, NC, xq_p + (size_t)t * NC * kXqWords,
+                               lane, act8);
+        }
     }
     if (zsa) {
         if (e >= E) cluster_wait();  // warps without an expert still take the cluster barrier
@@ -809,7 +814,12 @@ cudaError_t launch_decode(const Plan &p, const DecodeArgs &a_in, cudaStream_t s,
     a.fault_wait = p.fault_wait ? 1 : 0;
     const bool cluster =
         a.n == 1 && p.cluster_ok && expert_cluster_layout(p.desc, p.cluster_size, p.smem_optin, a);
-    a.zero_out = cluster ? 1 : 0;
+    // 2..4 tokens of a plain block: the cluster kernel over the distinct experts
+    const bool mt = a.n > 1 && p.cluster_mt_ok && !a.norm_w &&
+                    expert_cluster_layout(p.desc, p.cluster_size, p.smem_optin, a, a.n);
+    a.cl_mt = mt ? 1 : 0;
+    a.cl_active = p.cluster_mt_active;
+    a.zero_out = cluster || mt ? 1 : 0;
     a.sel_logits = cluster ? 1 : 0;
     a.act8 = cluster && (p.desc.flags & SI_FLAG_ACT_INT8) ? 1 : 0;  // the other decode paths keep their precision
     cudaError_t err = mark(events, 0, s);
@@ -818,7 +828,7 @@ cudaError_t launch_decode(const Plan &p, const DecodeArgs &a_in, cudaStream_t s,
     if (err != cudaSuccess) return err;
     if ((err = mark(events, 1, s)) != cudaSuccess) return err;
 
-    if (cluster) {
+    if (cluster || mt) {
         err = launch_expert_cluster(a, s);
         if (err != cudaSuccess) return err;
         if ((err = mark(events, 2, s)) != cudaSuccess) return err;

@@ -35,6 +35,15 @@
 // wait (L2 evict-first).  The kernel lets the next kernel of the stream
 // launch at once: that kernel's own dependency wait still covers all of this
 // kernel's work.
+//
+// 2..4 tokens (MT): the same kernel over the router's table of distinct
+// experts (sparkinfer README, "Milestone 2": redundant weight reads removed).
+// A unit is (distinct expert s, block column b); its bytes are read once and
+// dotted with the x of every token that chose expert s (ntok[s] <= 4), and h,
+// the down partials and the combine are kept per token.  Units number U * I/256
+// (U known only on the device), so the grid covers the largest possible table
+// and clusters whose s >= U leave at once; the clusters run in waves, with no
+// grid-wide synchronisation.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -52,6 +61,7 @@ constexpr int kPairs = 2;                   // gate/up row pairs per warp per st
 constexpr long long kDrain = 4000000000LL;
 constexpr int kMaxDownLanes = 8;            // row groups per warp in the down phase: RPC <= 8*kCW*8
 constexpr int kBoxRows = 8 * kCW;           // down rows per tensor box = rows of one down iteration
+constexpr int kHqTok = 160;                 // words of one token's quantised h: [4][32] + [4][7] (+ pad)
 
 __device__ __forceinline__ uint4 ld_s128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
@@ -93,7 +103,7 @@ __device__ __forceinline__ float pair_sum(float g, float u, int li) {
 // the router) and h are int8 per 32 columns, dotted with dp4a.
 // WF = 3: Q5_K weights (176-byte super-blocks: the fifth code bit of every
 // weight in 32 qh bytes ahead of the Q4_K-style codes), int16 activations.
-template <int NBH, bool NORM, int WF>
+template <int NBH, bool NORM, int WF, bool MT>
 __global__ void __launch_bounds__(kClThreads, 1)
     k_expert_cluster(const __grid_constant__ CUtensorMap tmap_down, const __grid_constant__ CUtensorMap tmap_tail,
                      DecodeArgs a) {
@@ -110,7 +120,11 @@ __global__ void __launch_bounds__(kClThreads, 1)
     __shared__ float s_w;
     __shared__ int s_lastA[8];
     __shared__ int s_lastB;
-    pdl_launch_dependents();  // the next kernel's dependency wait still covers this whole grid
+    __shared__ int s_tok[SI_MAX_DECODE_TOKENS];    // MT: the unit's tokens
+    __shared__ float s_wt[SI_MAX_DECODE_TOKENS];   // MT: their routing weights for expert s
+    static_assert(!MT || (WF == 0 && !NORM), "the multi-token units take plain Q4_K blocks");
+    // the next kernel's dependency wait still covers this whole grid; MT: see below
+    if (!MT) pdl_launch_dependents();
 
     // parameters used after the dependency wait, read now
     const uint8_t *const wg = pin_ptr(a.wg), *const wu = pin_ptr(a.wu);
@@ -125,12 +139,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const int I = pin_i32(a.I), H = pin_i32(a.H);
     const float *const wsc = FP4 ? pin_ptr(a.wscale) : nullptr;  // NVFP4 tensor scales [E][3]
     const uint32_t *const xq_g = pin_ptr(a.xq);  // x quantised by the router (plain block)
+    const UniqTable *const uniq = MT ? pin_ptr(a.uniq) : nullptr;
+    const int cl_active = MT ? pin_i32(a.cl_active) : 0;
+    const int ystride = MT ? pin_i32(a.cl_ystride) : 0;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = (int)cluster_nctarank();
     const int rank = (int)cluster_ctarank();
     const int nbI = I / kQK;
     const int unit = blockIdx.x / C;
+    // slot: the top-k slot of the single token, or (MT) the index of the distinct expert
     const int slot = unit / nbI, bcol = unit - slot * nbI;
     const int r_lo = kQK * bcol + (kQK * rank) / C;
     const int n_rp = kQK * bcol + (kQK * (rank + 1)) / C - r_lo;
@@ -174,8 +192,10 @@ __global__ void __launch_bounds__(kClThreads, 1)
         // the bytes the box copies deliver: the last box is tail_rows high for every
         // CTA (the largest CTA's remainder), which may exceed this CTA's n_rows
         mbar_arrive_expect_tx(fullB, (uint32_t)(((nbox - 1) * kBoxRows + tail_rows) * BB));
-        mbar_arrive_expect_tx(hbar, (uint32_t)(kQK * 4));  // every h value of the unit, once
-        if (!NORM) mbar_arrive_expect_tx(xbar, xq_bytes);
+        if (!MT) {  // MT: the counts depend on the routing, posted by the producer after the wait
+            mbar_arrive_expect_tx(hbar, (uint32_t)(kQK * 4));  // every h value of the unit, once
+            if (!NORM) mbar_arrive_expect_tx(xbar, xq_bytes);
+        }
     }
     // A plain block reads x quantised by the router (after the dependency wait, in
     // the consumer warps), so this kernel may be launched before the router has
@@ -254,6 +274,23 @@ __global__ void __launch_bounds__(kClThreads, 1)
     // arrive now (thread 0's init fence is the release), wait before the first store
     cluster_arrive_relaxed();
     pdl_wait();  // routing of this token is complete
+    // MT: units past the table of distinct experts have nothing to do (the whole
+    // cluster leaves: no copy was issued, no peer stores into it).  The clusters of the
+    // last wave let the next kernel launch; the others count as having let it at exit.
+    // The table entries are read together with U (independent loads, one round trip;
+    // the table has room for every unit's slot).
+    int nt = 1, mt_e = 0;
+    int4 mt_tok = make_int4(0, 0, 0, 0);
+    if (MT) {
+        const int U = ctrl[kCtrlNumUnique];
+        const int ntv = uniq->ntok[slot];
+        mt_e = uniq->expert[slot];
+        mt_tok = *reinterpret_cast<const int4 *>(&uniq->tok[slot][0]);
+        if (slot >= U) return;
+        nt = ntv;
+        if (unit >= U * nbI - cl_active) pdl_launch_dependents();
+    }
+    auto unit_tok = [&mt_tok](int t) { return t == 0 ? mt_tok.x : t == 1 ? mt_tok.y : t == 2 ? mt_tok.z : mt_tok.w; };
     // The router left the k selected experts in rank order with their logits.
     // Only the producer thread needs this unit's expert id, to address its
     // copies: it reads it itself and issues them at once.  The renormalised
@@ -261,7 +298,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
     // largest), is needed only by the final reductions: warp 0 forms all k
     // meanwhile (CTA 0 reports them); the __syncthreads before the reductions
     // publishes it.
-    if (warp == 0) {
+    if (MT) {
+        if (warp == 0 && lane < nt) {
+            const int tk = unit_tok(lane);
+            s_tok[lane] = tk;
+            s_wt[lane] = zsel[tk * k + uniq->slot[slot][lane]];  // the router's renormalised weight
+        }
+    } else if (warp == 0) {
         const float zr = lane < k ? zsel[lane] : 0.f;
         const float z0 = __shfl_sync(0xffffffffu, zr, 0);
         const float ex = lane < k ? expf(zr - z0) : 0.f;
@@ -280,8 +323,16 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const uint64_t pol = l2_evict_first_policy();
             // the router's quantised x first (every consumer warp needs it for stage 0),
             // one copy into this CTA's shared memory
-            if (!NORM) bulk_g2s(smem_addr(xq_s), xq_g, xq_bytes, xbar, l2_evict_last_policy());
-            const int e = ids[slot];
+            if (MT) {  // x of each of the unit's tokens, in table order
+                mbar_arrive_expect_tx(hbar, (uint32_t)(nt * kQK * 4));
+                mbar_arrive_expect_tx(xbar, (uint32_t)nt * xq_bytes);
+                for (int t = 0; t < nt; ++t)
+                    bulk_g2s(smem_addr(xq_s) + t * xq_bytes, xq_g + (size_t)unit_tok(t) * (xq_bytes / 4), xq_bytes,
+                             xbar, l2_evict_last_policy());
+            } else if (!NORM) {
+                bulk_g2s(smem_addr(xq_s), xq_g, xq_bytes, xbar, l2_evict_last_policy());
+            }
+            const int e = MT ? mt_e : ids[slot];
             auto issueA = [&](int j) -> bool {
                 const int st = j % NSA;
                 const uint32_t bytes = stage_bytes(j);
@@ -353,12 +404,10 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const float4 f = reinterpret_cast<const float4 *>(xq_s + 16 * (H / 64))[chunk];
             xs = f.x, XQ[0] = __float_as_int(f.y), Xa = f.z, Xb = f.w;  // da, db (bits), the two sums
             XQ[1] = XQ[2] = XQ[3] = 0;
-        } else {  // quantised by the router, copied by the producer
-            if (!mbar_wait_warp(xbar, 0, budget)) {
-                set_status(status, SI_ERR_TIMEOUT);
-                *verr = 1;
-            }
-            const uint32_t *xq = xq_s;
+        }
+        // quantised by the router, copied by the producer (MT: token t of the unit at t * xq_bytes)
+        auto load_x = [&](int t) {
+            const uint32_t *xq = xq_s + (size_t)t * (xq_bytes / 4);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const uint4 v = reinterpret_cast<const uint4 *>(xq + 32 * chunk)[q ^ (chunk & 7)];
@@ -368,6 +417,13 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const uint4 f2 = reinterpret_cast<const uint4 *>(xq + H / 2 + 8 * chunk)[1];
             xs = __uint_as_float(f.x), Xa = __uint_as_float(f.y), Xb = __uint_as_float(f.z);
             XQ[0] = (int)f.w, XQ[1] = (int)f2.x, XQ[2] = (int)f2.y, XQ[3] = (int)f2.z;
+        };
+        if (!NORM && !A8) {
+            if (!mbar_wait_warp(xbar, 0, budget)) {
+                set_status(status, SI_ERR_TIMEOUT);
+                *verr = 1;
+            }
+            load_x(0);
         }
         auto xwf = [&xw](int p) { return xw[p]; };
         // NVFP4: this unit's expert's gate and up tensor scales
@@ -387,11 +443,14 @@ __global__ void __launch_bounds__(kClThreads, 1)
         cluster_wait();  // every CTA of the cluster has initialised its barriers
         // Every stage is visited and every h value is stored, also after an error
         // (zeros then), so that every CTA's h barrier completes and no CTA exits
-        // while a peer may still store into it.
+        // while a peer may still store into it.  MT: the stages stay resident (no
+        // ring reuse), and each of the unit's tokens passes over them in turn.
+        for (int t = 0; t < (MT ? nt : 1); ++t) {
+        if (MT && t > 0) load_x(t);
         for (int j = 0; j < nA; ++j) {
             const int st = j % NSA;
             bool ok = !__any_sync(0xffffffffu, *verr != 0);
-            if (ok && !mbar_wait_warp(fullA + 8 * st, (j / NSA) & 1, budget)) {
+            if (ok && (!MT || t == 0) && !mbar_wait_warp(fullA + 8 * st, (j / NSA) & 1, budget)) {
                 set_status(status, SI_ERR_TIMEOUT);
                 *verr = 1;
                 ok = false;
@@ -439,10 +498,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
                 const int q = CH * j + (warp * RPW + g) * kPairs + m;
                 if (q < n_rp)
                     for (int peer = li; peer < C; peer += GS)  // GS may be smaller than C
-                        st_async_cluster_u32(hslice + (r_lo + q - kQK * bcol), hbar, (uint32_t)peer, __float_as_uint(hm));
+                        st_async_cluster_u32(hslice + (kQK * t + r_lo + q - kQK * bcol), hbar, (uint32_t)peer,
+                                             __float_as_uint(hm));
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(emptyA + 8 * st);
+            if (lane == 0 && (!MT || t == nt - 1)) mbar_arrive(emptyA + 8 * st);
+        }
         }
     }
 
@@ -454,11 +515,14 @@ __global__ void __launch_bounds__(kClThreads, 1)
 
     // --------------------------------------------------------- down + combine
     const bool skip = __any_sync(0xffffffffu, *verr != 0);
-    uint32_t *hq = xq_s;  // reuse: [4][32] words (the same unit swizzle) + [4][7]
-    float *hqf = reinterpret_cast<float *>(hq + 128);
+    // reuse of the x region: per token [4][32] words (the same unit swizzle) + [4][7]
+    const int ntl = MT ? nt : 1;
     if (warp < kCW && !skip) {
+        uint32_t *hq = xq_s + (MT ? kHqTok * (warp >> 2) : 0);
+        float *hqf = reinterpret_cast<float *>(hq + 128);
+        const float *hsl = hslice + (MT ? kQK * (warp >> 2) : 0);
         if (A8 && warp < 4) {  // int8 per 32 columns, the layout of the router's x (kXq8Words)
-            const float2 v = reinterpret_cast<const float2 *>(hslice + 64 * warp)[lane];  // columns 2l, 2l+1
+            const float2 v = reinterpret_cast<const float2 *>(hsl + 64 * warp)[lane];  // columns 2l, 2l+1
             float d, sum;
             const uint32_t lo = quant_pair8(v.x, v.y, &d, &sum);
             const uint32_t hi = __shfl_down_sync(0xffffffffu, lo, 1);
@@ -470,8 +534,9 @@ __global__ void __launch_bounds__(kClThreads, 1)
             float *sc = reinterpret_cast<float *>(hq + 16 * 4) + 4 * warp;
             if (lane == 0) sc[0] = d, sc[2] = sum;
             if (lane == 16) sc[1] = d, sc[3] = sum;
-        } else if (warp < 4) {  // the unit's four 64-column chunks of h: warp c quantises chunk c
-            const float2 v = reinterpret_cast<const float2 *>(hslice + 64 * warp)[lane];  // columns 2l, 2l+1
+        } else if (warp < 4 * ntl) {  // the unit's four 64-column chunks of h: warp 4t+c quantises chunk c of token t
+            const int wc = MT ? (warp & 3) : warp;
+            const float2 v = reinterpret_cast<const float2 *>(hsl + 64 * wc)[lane];  // columns 2l, 2l+1
             float mx = fmaxf(fabsf(v.x), fabsf(v.y));
             float sum = v.x + v.y;  // lanes 0..15: sub-block a, 16..31: sub-block b
 #pragma unroll
@@ -479,47 +544,25 @@ __global__ void __launch_bounds__(kClThreads, 1)
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
             const float inv = mx > 0.f ? 32767.0f / mx : 0.f;
-            hq[32 * warp + 4 * ((lane >> 2) ^ warp) + (lane & 3)] = pack_q16(v.x, v.y, inv);
+            hq[32 * wc + 4 * ((lane >> 2) ^ wc) + (lane & 3)] = pack_q16(v.x, v.y, inv);
             if (lane == 0) {
-                hqf[7 * warp] = mx * (1.0f / 32767.0f);
-                hqf[7 * warp + 1] = sum;
+                hqf[7 * wc] = mx * (1.0f / 32767.0f);
+                hqf[7 * wc + 1] = sum;
             }
-            if (lane == 16) hqf[7 * warp + 2] = sum;
+            if (lane == 16) hqf[7 * wc + 2] = sum;
             if (FP4) {  // integer sums of the quantised h over 16-column blocks (8 lanes each)
                 const uint32_t wq2 = pack_q16(v.x, v.y, inv);
                 int s2 = (int)(int16_t)(wq2 & 0xffffu) + ((int)wq2 >> 16);
                 s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
                 s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
                 s2 += __shfl_xor_sync(0xffffffffu, s2, 4);
-                if ((lane & 7) == 0) reinterpret_cast<int *>(hqf)[7 * warp + 3 + (lane >> 3)] = s2;
+                if ((lane & 7) == 0) reinterpret_cast<int *>(hqf)[7 * wc + 3 + (lane >> 3)] = s2;
             }
         }
     }
     if (warp < kCW) asm volatile("bar.sync 1, %0;" ::"r"(kCW * 32) : "memory");  // consumer warps only
     if (warp < kCW && !skip) {
         const int r8 = lane >> 2, i = lane & 3;
-        uint32_t hw[32];
-        float hs, Ha, Hb, hdb = 0.f;
-        int HQ[4];
-        if (A8) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(hq) + xq8_unit_byte(i, q));
-                hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
-            }
-            const float4 f = reinterpret_cast<const float4 *>(hq + 16 * 4)[i];
-            hs = f.x, hdb = f.y, Ha = f.z, Hb = f.w;
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint4 v = reinterpret_cast<const uint4 *>(hq + 32 * i)[q ^ i];
-                hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
-            }
-            hs = hqf[7 * i], Ha = hqf[7 * i + 1], Hb = hqf[7 * i + 2];
-        }
-#pragma unroll
-        for (int b4 = 0; b4 < 4; ++b4) HQ[b4] = FP4 ? reinterpret_cast<const int *>(hqf)[7 * i + 3 + b4] : 0;
-        auto hwf = [&hw](int p) { return hw[p]; };
         // box m holds rows [128m, 128m + 128) = the rows of iteration m; every box
         // completes on one barrier (they land while gate/up is computed), rows past
         // n_rows are skipped
@@ -528,35 +571,72 @@ __global__ void __launch_bounds__(kClThreads, 1)
             set_status(status, SI_ERR_TIMEOUT);
             *verr = 1;
         }
-#pragma unroll 1
-        for (int m = 0; m < (landed ? nbox : 0); ++m) {
-            const int lr = kBoxRows * m + 8 * warp + r8;
-            float v = 0.f;
-            if (lr < n_rows) {
-                const uint8_t *blk = stB + (size_t)m * box_stride + (size_t)(8 * warp + r8) * BB;
-                const uint4 hd = ld_s128(blk), q0 = ld_s128(blk + QO + 32 * i), q1 = ld_s128(blk + QO + 16 + 32 * i);
-                uint4 qh0 = make_uint4(0, 0, 0, 0), qh1 = qh0;
-                if (Q5) qh0 = ld_s128(blk + kQ5QhOff), qh1 = ld_s128(blk + kQ5QhOff + 16);
-                v = Q5   ? chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums5(q0, q1, qh0, qh1, i, hwf), hs, Ha, Hb)
-                    : FP4 ? chunk_contrib_nvfp4(hd, i, q0, q1, hwf, hs, HQ)
-                    : A8 ? chunk_contrib_i8(chunk_scales_i(hd, i), chunk_isums8(q0, q1, hwf), hs, hdb, Ha, Hb)
-                         : chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums(q0, q1, hwf), hs, Ha, Hb);
+        for (int t = 0; t < (landed ? ntl : 0); ++t) {  // MT: each of the unit's tokens in turn
+            const uint32_t *hq = xq_s + (MT ? kHqTok * t : 0);
+            const float *hqf = reinterpret_cast<const float *>(hq + 128);
+            uint32_t hw[32];
+            float hs, Ha, Hb, hdb = 0.f;
+            int HQ[4];
+            if (A8) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(hq) + xq8_unit_byte(i, q));
+                    hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
+                }
+                const float4 f = reinterpret_cast<const float4 *>(hq + 16 * 4)[i];
+                hs = f.x, hdb = f.y, Ha = f.z, Hb = f.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 v = reinterpret_cast<const uint4 *>(hq + 32 * i)[q ^ i];
+                    hw[4 * q] = v.x, hw[4 * q + 1] = v.y, hw[4 * q + 2] = v.z, hw[4 * q + 3] = v.w;
+                }
+                hs = hqf[7 * i], Ha = hqf[7 * i + 1], Hb = hqf[7 * i + 2];
             }
-            v += __shfl_xor_sync(0xffffffffu, v, 1);
-            v += __shfl_xor_sync(0xffffffffu, v, 2);
-            if (i == 0 && lr < n_rows) ybuf[lr] = v;
+#pragma unroll
+            for (int b4 = 0; b4 < 4; ++b4) HQ[b4] = FP4 ? reinterpret_cast<const int *>(hqf)[7 * i + 3 + b4] : 0;
+            auto hwf = [&hw](int p) { return hw[p]; };
+            float *yb = ybuf + (MT ? ystride * t : 0);
+#pragma unroll 1
+            for (int m = 0; m < nbox; ++m) {
+                const int lr = kBoxRows * m + 8 * warp + r8;
+                float v = 0.f;
+                if (lr < n_rows) {
+                    const uint8_t *blk = stB + (size_t)m * box_stride + (size_t)(8 * warp + r8) * BB;
+                    const uint4 hd = ld_s128(blk), q0 = ld_s128(blk + QO + 32 * i), q1 = ld_s128(blk + QO + 16 + 32 * i);
+                    uint4 qh0 = make_uint4(0, 0, 0, 0), qh1 = qh0;
+                    if (Q5) qh0 = ld_s128(blk + kQ5QhOff), qh1 = ld_s128(blk + kQ5QhOff + 16);
+                    v = Q5   ? chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums5(q0, q1, qh0, qh1, i, hwf), hs, Ha, Hb)
+                        : FP4 ? chunk_contrib_nvfp4(hd, i, q0, q1, hwf, hs, HQ)
+                        : A8 ? chunk_contrib_i8(chunk_scales_i(hd, i), chunk_isums8(q0, q1, hwf), hs, hdb, Ha, Hb)
+                             : chunk_contrib_i(chunk_scales_i(hd, i), chunk_isums(q0, q1, hwf), hs, Ha, Hb);
+                }
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                if (i == 0 && lr < n_rows) yb[lr] = v;
+            }
         }
     }
     __syncthreads();
     if (!*verr) {
-        const float w = s_w;
-        float *out = out_g + c_lo;
-        for (int lr = threadIdx.x; lr < n_rows; lr += blockDim.x) red_add_f32(out + lr, w * ybuf[lr]);
+        if (MT) {  // each token's partials, weighted by its routing weight for this expert
+            for (int idx = threadIdx.x; idx < ntl * n_rows; idx += blockDim.x) {
+                const int t = idx / n_rows, lr = idx - t * n_rows;
+                red_add_f32(out_g + (size_t)s_tok[t] * H + c_lo + lr, s_wt[t] * ybuf[ystride * t + lr]);
+            }
+        } else {
+            const float w = s_w;
+            float *out = out_g + c_lo;
+            for (int lr = threadIdx.x; lr < n_rows; lr += blockDim.x) red_add_f32(out + lr, w * ybuf[lr]);
+        }
     } else if (threadIdx.x == 0) {  // no copy may still be writing this CTA's shared memory at exit
         for (int st = 0; st < NSA; ++st)
             if (s_lastA[st] >= 0) mbar_wait_bounded(fullA + 8 * st, s_lastA[st], kDrain);
         if (s_lastB >= 0) mbar_wait_bounded(fullB, 0, kDrain);
         if (!NORM) mbar_wait_bounded(xbar, 0, kDrain);  // issued by the producer in every case
+        // the peers store every h value, also after an error: let them all land here
+        // before this CTA's shared memory goes away
+        mbar_wait_bounded_cluster(hbar, 0, kDrain);
     }
 }
 
@@ -576,9 +656,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// Cluster size and shared-memory plan for n = 1; false if this shape needs
-// the other expert kernel.
-bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs &a) {
+// Cluster size and shared-memory plan for n = 1 (nt = 1), or for units of
+// up to nt tokens (the multi-token kernel: x, h and the down partials once
+// per token, and the gate/up stages without ring reuse); false if this shape
+// needs the other expert kernels.
+bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs &a, int nt) {
     const int nbh = d.hidden / kQK;
     if (nbh != 1 && nbh != 2 && nbh != 4 && nbh != 8) return false;
     if (C < 2 || C > 8) return false;
@@ -595,6 +677,7 @@ bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs
     const int box_stride = kBoxRows * BB;  // 18432 = 144 * 128 for Q4_K
     auto al = [](int v) { return (v + 127) / 128 * 128; };
     int NSA = nA_max < 3 ? nA_max : 3;
+    if (nt > 1 && nA_max > NSA) return false;  // the tokens pass over the resident stages in turn
     int off = 0;
     a.cl_off_a = off;
     // without ring reuse the last stage holds only the rows that remain
@@ -603,11 +686,13 @@ bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs
     a.cl_off_b = off;
     off += (nbox - 1) * box_stride + al(tail * BB);
     a.cl_off_h = off;
-    off += al(kQK * 4);
-    a.cl_off_x = off;  // quantised x: [H/64][32] words + [H/64][7] (later: quantised h)
-    off += al(d.hidden / 64 * kXqWords * 4);
+    off += nt * al(kQK * 4);
+    a.cl_off_x = off;  // quantised x per token: [H/64][32] words + [H/64][8] (later: quantised h)
+    off += nt * al(d.hidden / 64 * kXqWords * 4);
+    if (nt * kHqTok > nt * (d.hidden / 64) * kXqWords) return false;  // h per token fits where x was
     a.cl_off_y = off;
-    off += al(rpc * 4);
+    a.cl_ystride = al(rpc * 4) / 4;
+    off += nt * al(rpc * 4);
     a.cl_off_bar = off;
     off += 8 * (2 * NSA + 3) + 64;
     if (off + 1024 > smem_max) return false;  // + static shared memory
@@ -639,7 +724,8 @@ static bool make_down_tensor_map(const DecodeArgs &a, int rows, CUtensorMap *tm)
 template <int NBH>
 static cudaError_t launch_cluster_t(const DecodeArgs &a, const CUtensorMap &tm, const CUtensorMap &tt,
                                     cudaStream_t s) {
-    const int units = a.k * (a.I / kQK);
+    // MT: room for every distinct expert the call can have (at most n*k, at most E)
+    const int units = (a.cl_mt ? (a.n * a.k < a.E ? a.n * a.k : a.E) : a.k) * (a.I / kQK);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(units * a.cl_C);
     cfg.blockDim = dim3(kClThreads);
@@ -654,11 +740,12 @@ static cudaError_t launch_cluster_t(const DecodeArgs &a, const CUtensorMap &tm, 
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (a.wtype == SI_WTYPE_NVFP4) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 1>, tm, tt, a);
-    if (a.wtype == SI_WTYPE_Q5_K) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 3>, tm, tt, a);
-    if (a.act8) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 2>, tm, tt, a);
-    return a.norm_w ? cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, true, 0>, tm, tt, a)
-                    : cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 0>, tm, tt, a);
+    if (a.cl_mt) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 0, true>, tm, tt, a);
+    if (a.wtype == SI_WTYPE_NVFP4) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 1, false>, tm, tt, a);
+    if (a.wtype == SI_WTYPE_Q5_K) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 3, false>, tm, tt, a);
+    if (a.act8) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 2, false>, tm, tt, a);
+    return a.norm_w ? cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, true, 0, false>, tm, tt, a)
+                    : cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 0, false>, tm, tt, a);
 }
 
 cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s) {
@@ -673,26 +760,31 @@ cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s) {
     }
 }
 
-cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters) {
+cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters, bool mt) {
     *active_clusters = 0;
     if (!tensor_map_encoder()) return cudaErrorNotSupported;  // down blocks are fetched by a tensor map
-    const void *fs[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};  // plain / pre-normed Q4_K, NVFP4, int8 act, Q5_K
-    switch (nbh) {
-        case 1: fs[0] = (const void *)k_expert_cluster<1, false, 0>, fs[1] = (const void *)k_expert_cluster<1, true, 0>,
-                fs[2] = (const void *)k_expert_cluster<1, false, 1>, fs[3] = (const void *)k_expert_cluster<1, false, 2>,
-                fs[4] = (const void *)k_expert_cluster<1, false, 3>; break;
-        case 2: fs[0] = (const void *)k_expert_cluster<2, false, 0>, fs[1] = (const void *)k_expert_cluster<2, true, 0>,
-                fs[2] = (const void *)k_expert_cluster<2, false, 1>, fs[3] = (const void *)k_expert_cluster<2, false, 2>,
-                fs[4] = (const void *)k_expert_cluster<2, false, 3>; break;
-        case 4: fs[0] = (const void *)k_expert_cluster<4, false, 0>, fs[1] = (const void *)k_expert_cluster<4, true, 0>,
-                fs[2] = (const void *)k_expert_cluster<4, false, 1>, fs[3] = (const void *)k_expert_cluster<4, false, 2>,
-                fs[4] = (const void *)k_expert_cluster<4, false, 3>; break;
-        default: fs[0] = (const void *)k_expert_cluster<8, false, 0>, fs[1] = (const void *)k_expert_cluster<8, true, 0>,
-                 fs[2] = (const void *)k_expert_cluster<8, false, 1>, fs[3] = (const void *)k_expert_cluster<8, false, 2>,
-                fs[4] = (const void *)k_expert_cluster<8, false, 3>; break;
+    // single token: plain / pre-normed Q4_K, NVFP4, int8 act, Q5_K; mt: the multi-token kernel
+    const void *fs[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+#define SI_CL_VARIANTS(B)                                                                              \
+    if (mt) {                                                                                          \
+        fs[0] = (const void *)k_expert_cluster<B, false, 0, true>;                                     \
+    } else {                                                                                           \
+        fs[0] = (const void *)k_expert_cluster<B, false, 0, false>;                                    \
+        fs[1] = (const void *)k_expert_cluster<B, true, 0, false>;                                     \
+        fs[2] = (const void *)k_expert_cluster<B, false, 1, false>;                                    \
+        fs[3] = (const void *)k_expert_cluster<B, false, 2, false>;                                    \
+        fs[4] = (const void *)k_expert_cluster<B, false, 3, false>;                                    \
     }
+    switch (nbh) {
+        case 1: SI_CL_VARIANTS(1) break;
+        case 2: SI_CL_VARIANTS(2) break;
+        case 4: SI_CL_VARIANTS(4) break;
+        default: SI_CL_VARIANTS(8) break;
+    }
+#undef SI_CL_VARIANTS
     int least = 1 << 30;
     for (const void *f : fs) {  // every variant must fit; the smallest resident count counts
+        if (!f) continue;
         cudaFuncAttributes fa;
         cudaError_t err = cudaFuncGetAttributes(&fa, f);
         if (err != cudaSuccess) return err;

@@ -39,6 +39,8 @@ struct UniqTable {
     int32_t tok[kMaxSlots][SI_MAX_DECODE_TOKENS];     // which tokens
     int32_t slot[kMaxSlots][SI_MAX_DECODE_TOKENS];    // at which top-k slot
 };
+static_assert(offsetof(UniqTable, tok) % 16 == 0 && SI_MAX_DECODE_TOKENS == 4,
+              "a slot's tokens are read as one 16-byte word");
 
 struct DecodeLayout {
     size_t ctrl, logits, ids, wts, counts, uniq, h, xq, total;
@@ -54,6 +56,8 @@ struct Plan {
     bool fault_wait;        // test mode: expert kernels first wait on a flag nothing sets
     bool fused_ok[SI_MAX_DECODE_TOKENS + 1];  // fused expert kernel usable for n tokens
     bool cluster_ok;                          // cluster expert kernel usable for n = 1
+    bool cluster_mt_ok;                       // and for 2..4 tokens (units of distinct experts)
+    int cluster_mt_active;                    // resident clusters of the multi-token kernel
     bool prefill_ok;                          // tensor-core prefill kernels configured
     int cluster_size;                         // CTAs per cluster (all clusters co-resident)
     int cluster_active;                       // clusters of that size the device holds at once
@@ -85,7 +89,7 @@ struct DecodeArgs {
     int32_t *counts;
     UniqTable *uniq;
     float *h;  // [n][k][I]
-    uint32_t *xq;  // [H/64][kXqWords]: one token's x quantised per 64 columns by the router (cluster path)
+    uint32_t *xq;  // [n][H/64][kXqWords]: x quantised per 64 columns by the router (cluster paths)
     int32_t *o_ids;
     float *o_w;
     int32_t *o_counts;
@@ -98,6 +102,9 @@ struct DecodeArgs {
     // shared-memory plan of the cluster expert kernel (set by expert_cluster_layout)
     int cl_off_a, cl_off_b, cl_off_h, cl_off_x, cl_off_y, cl_off_bar;
     int cl_nsa, cl_C, cl_tail_rows, cl_nbox, cl_box_stride, cl_smem;
+    int cl_ystride;  // floats per token of the down partials
+    int cl_mt;       // 2..4 tokens on the cluster kernel: units (distinct expert, block column), in waves
+    int cl_active;   // clusters resident at once (MT: the last wave lets the next kernel launch)
     int zero_out;  // router sets out[n][H] to 0, or to x in a pre-normed block (the expert kernel accumulates into it)
     int act8;      // int8-activation mode (SI_FLAG_ACT_INT8) on the single-token cluster path
     int sel_logits;  // single token, cluster expert kernel: the router writes ids in rank order, the
@@ -157,9 +164,9 @@ cudaError_t launch_decode(const Plan &p, const DecodeArgs &a, cudaStream_t s,
 bool expert_fused_layout(const si_moe_desc &d, int n, int grid, int smem_max, DecodeArgs &a);
 cudaError_t launch_expert_fused(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t expert_fused_occupancy(int nbh, bool dedup, int smem, int smem_max, int *blocks_per_sm);
-bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs &a);
+bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs &a, int nt = 1);
 cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s);
-cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters);
+cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters, bool mt = false);
 cudaError_t launch_debug_dequant(const uint8_t *blocks, int64_t n_blocks, float *out_f32,
                                  uint16_t *out_bf16, cudaStream_t s);
 cudaError_t launch_debug_nvfp4_f16(const uint8_t *blocks, int64_t n_blocks, float g, uint16_t *out, cudaStream_t s);

@@ -86,14 +86,20 @@ def test_act8_single_token_decode_matches_the_emulation(shape, n_tok):
 
 @pytest.mark.parametrize("n", [2, 4])
 def test_act8_flag_leaves_batched_decode_unchanged(n):
+    """Batched decode keeps its int16 activations under the flag: the same
+    kernel and routing, outputs equal up to the order of the float reductions
+    of the top-k combine (they vary from run to run)."""
     shape = synth.QWEN3_30B_A3B
     layer = synth.make_layer(shape, seed=3)
     dl = device.to_device(layer)
     x = synth.make_tokens(shape, seed=8, n_tokens=n)
-    a = _decode(_plan(shape), dl, x, shape)
-    b = _decode(_plan(shape, flags=0), dl, x, shape)
-    for u, v in zip(a, b):
-        assert np.array_equal(u, v)
+    plan8, plan0 = _plan(shape), _plan(shape, flags=0)
+    assert binding.si_debug_decode_fused(plan8, n) == binding.si_debug_decode_fused(plan0, n)
+    a = _decode(plan8, dl, x, shape)
+    b = _decode(plan0, dl, x, shape)
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])   # routing: bit-exact
+    for t in range(n):
+        assert parity.rel_l2(a[0][t], b[0][t]) < 1e-6
 
 
 def test_act8_flag_leaves_prefill_unchanged():

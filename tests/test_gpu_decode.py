@@ -307,26 +307,30 @@ def test_fused_path_is_taken_for_the_qwen3_shape():
     assert info["cluster_ok"] == 1 and 2 <= info["cluster_size"] <= 8
     assert info["clusters_resident"] >= info["clusters_needed"] == 24   # one wave
     for n in range(2, binding.SI_MAX_DECODE_TOKENS + 1):
-        assert binding.si_debug_decode_fused(plan, n) == 1        # grid-synchronised kernel
+        assert binding.si_debug_decode_fused(plan, n) == 3        # cluster kernel over the distinct experts
     plan_h768 = binding.si_moe_plan(binding.make_desc(768, 512, 4, 4))
     assert binding.si_debug_decode_fused(plan_h768, 1) == 0
 
 
-@pytest.mark.parametrize("n", [1, 2])
-def test_bounded_wait_timeout_is_reported_and_the_context_survives(monkeypatch, n):
+@pytest.mark.parametrize("n,prenorm", [(1, False), (2, False), (2, True)])
+def test_bounded_wait_timeout_is_reported_and_the_context_survives(monkeypatch, n, prenorm):
     """A wait budget of 0 cycles makes every device-side wait of the expert
-    kernel (cluster kernel for n = 1, grid-synchronised kernel for n = 2) give
-    up at once: the kernel must record SI_ERR_TIMEOUT, let its copies land,
-    and return; the next call on a fresh scratch must be right."""
+    kernel (cluster kernel for n = 1, the cluster kernel over the distinct
+    experts for n = 2, the grid-synchronised kernel for n = 2 in a pre-normed
+    block) give up at once: the kernel must record SI_ERR_TIMEOUT, let its
+    copies land, and return; the next call on a fresh scratch must be right."""
     shape = synth.TINY
     layer = synth.make_layer(shape, seed=0)
+    if prenorm:
+        layer.norm_weight = synth.make_norm_weight(shape, seed=0)
+        layer.norm_eps = 1e-6
     dl = device.to_device(layer)
     x_bits = synth.make_tokens(shape, seed=0, n_tokens=n)
     x = device.tokens_to_device(x_bits)
     monkeypatch.setenv("SI_FAULT_WAIT_BUDGET", "0")
     plan0 = binding.si_moe_plan(device.desc_for(shape))
     monkeypatch.delenv("SI_FAULT_WAIT_BUDGET")
-    assert binding.si_debug_decode_fused(plan0, n) == (2 if n == 1 else 1)
+    assert binding.si_debug_decode_fused(plan0, n) == (2 if n == 1 else 3)  # pre-normed n > 1: grid kernel
     scratch = device.alloc_scratch(plan0, binding.SI_MODE_DECODE, n)
     out = torch.zeros((n, shape.hidden), dtype=torch.float32, device="cuda")
     binding.si_moe_forward_decode(plan0, dl.struct(), x, n, out, None, scratch)
@@ -338,7 +342,10 @@ def test_bounded_wait_timeout_is_reported_and_the_context_survives(monkeypatch, 
     binding.si_moe_forward_decode(plan, dl.struct(), x, n, out, None, scratch)
     assert binding.si_moe_read_status(plan, scratch) == binding.SI_OK
     for t in range(n):
-        ref = oracle.moe_token(layer, x_bits[t])
+        if prenorm:
+            ref = oracle.moe_token_prenorm(layer, x_bits[t], layer.norm_weight, layer.norm_eps)
+        else:
+            ref = oracle.moe_token(layer, x_bits[t])
         parity.assert_close(out.cpu().numpy()[t], ref.out64, "after timeout")
 
 
