@@ -183,7 +183,8 @@ si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *o
         p.cluster_mt_active = 0;
         si::DecodeArgs tmp{};
         // (the int8-activation flag applies to single tokens only: batched tokens keep int16)
-        if (p.cluster_ok && desc->wtype == SI_WTYPE_Q4_K &&
+        if (p.cluster_ok && desc->wtype == SI_WTYPE_Q4_K && si::router_one_shape(desc->n_experts, desc->hidden) &&
+            desc->top_k <= 8 &&
             si::expert_cluster_layout(*desc, p.cluster_size, p.smem_optin, tmp, SI_MAX_DECODE_TOKENS)) {
             int clusters = 0;
             if (si::expert_cluster_prepare(desc->hidden / 256, p.smem_optin, tmp.cl_smem, p.cluster_size, &clusters,

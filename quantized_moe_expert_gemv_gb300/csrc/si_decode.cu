@@ -618,22 +618,26 @@ static cudaError_t launch_router_t(const DecodeArgs &a, cudaStream_t s) {
                     : cudaLaunchKernelEx(&cfg, k_router_topk<NJ, false>, a);
 }
 
-// Router + top-k of ONE plain token for the cluster expert kernel, on an
+// Router + top-k of n <= 4 plain tokens for a cluster expert kernel, on an
 // 8-CTA cluster, WPC experts per CTA (E == 8*WPC) and CPT columns per thread
 // (H == 32*WPC*CPT).  Thread t of CTA c holds, in registers loaded before the
 // dependency wait, the router weights of the CTA's WPC experts at columns
 // CPT*t .. CPT*t+CPT-1, so that x is read once per CTA (CPT columns per
-// thread, no shared copy) instead of once per expert.  Each thread forms WPC
-// partial sums; a reduce-scatter across the warp's lanes (log2(WPC) halving
-// shuffle steps) leaves each expert's warp sum in 32/WPC lanes, and the warps'
-// sums are added in shared memory (fixed order).  Then, as in k_router_topk:
-// every CTA receives every logit by asynchronous stores, each warp ranks its
-// own expert and stores the selected ones at their rank; x is quantised for
-// the expert kernel, which is launched at once.
-template <int WPC, int CPT>
+// thread and token, no shared copy) instead of once per expert.  For each
+// token each thread forms WPC partial sums; a reduce-scatter across the warp's
+// lanes (log2(WPC) halving shuffle steps) leaves each expert's warp sum in
+// 32/WPC lanes, and the warps' sums are added in shared memory (fixed order).
+// Then every CTA receives every logit by asynchronous stores, and each warp
+// ranks its own expert for every token (descending logits, ties to the lower
+// index) and stores it at its rank, with its logit, where it is selected; the
+// expert kernel forms the renormalised weights (and, for several tokens, the
+// table of distinct experts) from these.  x is quantised for the expert
+// kernel, which is launched at once.
+template <int WPC, int CPT, int NT>
 __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
-    __shared__ float s_z[SI_MAX_EXPERTS];
-    __shared__ float s_part[WPC][WPC];  // [warp][local expert]
+    // NT: 1 (one token) or SI_MAX_DECODE_TOKENS (n = 2..NT tokens)
+    __shared__ float s_z[NT][SI_MAX_EXPERTS];
+    __shared__ float s_part[NT][WPC][WPC];  // [token][warp][local expert]
     __shared__ __align__(8) uint64_t s_zbar;
     const uint16_t *const xg_p = pin_ptr(a.x);
     float *const out_p = pin_ptr(a.out);
@@ -645,7 +649,7 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
     int32_t *const counts_p = pin_ptr(a.counts);
     int32_t *const ocounts_p = pin_ptr(a.o_counts);
     uint32_t *const xq_p = pin_ptr(a.xq);
-    const int H = pin_i32(a.H), E = pin_i32(a.E), k = pin_i32(a.k);
+    const int H = pin_i32(a.H), E = pin_i32(a.E), k = pin_i32(a.k), n = NT == 1 ? 1 : pin_i32(a.n);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = (int)gridDim.x;
     const int e0 = blockIdx.x * WPC;  // this CTA's experts
@@ -669,102 +673,129 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
     for (int q = 0; q < WPC; ++q)  // the weights are in registers before the wait, not fetched after it
 #pragma unroll
         for (int c = 0; c < CPT; ++c) asm volatile("" ::"f"(w[q][c]));
-    if (blockIdx.x == 0 && threadIdx.x < (H * 2) / 128) prefetch_l2(reinterpret_cast<const uint8_t *>(xg_p) + 128 * threadIdx.x);
+    if (blockIdx.x == 0 && threadIdx.x < (n * H * 2) / 128)
+        prefetch_l2(reinterpret_cast<const uint8_t *>(xg_p) + 128 * threadIdx.x);
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&s_zbar), 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(smem_addr(&s_zbar), (uint32_t)(E * 4));  // every logit, once
+        mbar_arrive_expect_tx(smem_addr(&s_zbar), (uint32_t)(n * E * 4));  // every logit, once
     }
     __syncthreads();
     cluster_arrive_relaxed();
     pdl_wait();  // x and the scratch are ready (previous kernels complete)
-    // the chunk of x this warp quantises for the expert kernel (at most one: H/64 <= 8*WPC), loaded
-    // together with the columns of the dot product
+    // the chunk of x this warp quantises for the expert kernel (at most one: n*H/64 <= 8*WPC), loaded
+    // together with the columns of the dot products
+    const int NC = H / 64;
     const int qc = blockIdx.x + C * warp;
-    const uint32_t qword = qc < H / 64 ? __ldg(reinterpret_cast<const uint32_t *>(xg_p) + 32 * qc + lane) : 0u;
-    float xf[CPT];
-    {
-        const uint16_t *xp = xg_p + CPT * threadIdx.x;
-        uint32_t xw[CPT / 2];
-        if (CPT == 2) xw[0] = __ldg(reinterpret_cast<const uint32_t *>(xp));
-        else if (CPT == 4) {
-            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(xp));
-            xw[0] = v.x, xw[1 % (CPT / 2)] = v.y;
-        } else {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xp));
-            xw[0] = v.x, xw[1 % (CPT / 2)] = v.y, xw[2 % (CPT / 2)] = v.z, xw[3 % (CPT / 2)] = v.w;
-        }
+    const uint32_t qword = qc < n * NC ? __ldg(reinterpret_cast<const uint32_t *>(xg_p) + 32 * qc + lane) : 0u;
+    uint32_t xw[NT][CPT / 2];
 #pragma unroll
-        for (int c = 0; c < CPT / 2; ++c) {
-            xf[2 * c] = __uint_as_float(xw[c] << 16);
-            xf[2 * c + 1] = __uint_as_float(xw[c] & 0xffff0000u);
+    for (int t = 0; t < NT; ++t) {
+        if (t < n) {
+            const uint16_t *xp = xg_p + (size_t)t * H + CPT * threadIdx.x;
+            if (CPT == 2) xw[t][0] = __ldg(reinterpret_cast<const uint32_t *>(xp));
+            else if (CPT == 4) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2 *>(xp));
+                xw[t][0] = v.x, xw[t][1 % (CPT / 2)] = v.y;
+            } else {
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xp));
+                xw[t][0] = v.x, xw[t][1 % (CPT / 2)] = v.y, xw[t][2 % (CPT / 2)] = v.z, xw[t][3 % (CPT / 2)] = v.w;
+            }
         }
     }
-    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < H; q += C * blockDim.x) out_p[q] = 0.f;  // the combine accumulates
-    float v[WPC];
-#pragma unroll
-    for (int q = 0; q < WPC; ++q) {
-        float acc = w[q][0] * xf[0];
-#pragma unroll
-        for (int c = 1; c < CPT; ++c) acc = fmaf(w[q][c], xf[c], acc);
-        v[q] = acc;
-    }
-    // reduce-scatter across the lanes: step s halves the experts a lane keeps
-#pragma unroll
-    for (int s = 0; (1 << s) < WPC; ++s) {
-        const int half = WPC >> (s + 1), mask = 16 >> s;
-        const bool up = (lane & mask) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float keep = up ? v[i + half] : v[i], send = up ? v[i] : v[i + half];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-        }
-    }
+    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < n * H; q += C * blockDim.x) out_p[q] = 0.f;  // the combine accumulates
     constexpr int kGroup = 32 / WPC;  // lanes that share one expert after the halving steps
 #pragma unroll
-    for (int m = kGroup / 2; m > 0; m >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
-    if (lane % kGroup == 0) s_part[warp][lane / kGroup] = v[0];
+    for (int t = 0; t < NT; ++t) {
+        if (t < n) {
+            float xf[CPT];
+#pragma unroll
+            for (int c = 0; c < CPT / 2; ++c) {
+                xf[2 * c] = __uint_as_float(xw[t][c] << 16);
+                xf[2 * c + 1] = __uint_as_float(xw[t][c] & 0xffff0000u);
+            }
+            float v[WPC];
+#pragma unroll
+            for (int q = 0; q < WPC; ++q) {
+                float acc = w[q][0] * xf[0];
+#pragma unroll
+                for (int c = 1; c < CPT; ++c) acc = fmaf(w[q][c], xf[c], acc);
+                v[q] = acc;
+            }
+            // reduce-scatter across the lanes: step s halves the experts a lane keeps
+#pragma unroll
+            for (int s = 0; (1 << s) < WPC; ++s) {
+                const int half = WPC >> (s + 1), mask = 16 >> s;
+                const bool up = (lane & mask) != 0;
+#pragma unroll
+                for (int i = 0; i < half; ++i) {
+                    const float keep = up ? v[i + half] : v[i], send = up ? v[i] : v[i + half];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+                }
+            }
+#pragma unroll
+            for (int m = kGroup / 2; m > 0; m >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+            if (lane % kGroup == 0) s_part[t][warp][lane / kGroup] = v[0];
+        }
+    }
     __syncthreads();
     cluster_wait();  // every CTA's mbarrier is initialised (all arrived long ago)
-    {  // warp q: the logit of expert e0 + q, the sum of the WPC warps' partials
-        float z = lane < WPC ? s_part[lane][warp] : 0.f;
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) z += __shfl_xor_sync(0xffffffffu, z, m);
-        const int e = e0 + warp;
-        if (bias_p) z += __ldg(bias_p + e);
-        if (lane < C) st_async_cluster_u32(&s_z[e], smem_addr(&s_zbar), (uint32_t)lane, __float_as_uint(z));
-        if (lane == 0 && ologits_p) ologits_p[e] = z;
-    }
-    // x quantised per 64-column chunk for the expert kernel (as in k_router_topk)
-    if (qc < H / 64) router_quant_chunk(qword, qc, H / 64, xq_p, lane, pin_i32(a.act8) != 0);
-    if (!mbar_wait_warp_cluster(smem_addr(&s_zbar), 0, a.wait_budget)) set_status(a.ctrl + kCtrlStatus, SI_ERR_TIMEOUT);
-    // warp q ranks expert e0 + q against all E logits (greater, or equal with a
-    // lower index, beats it) and stores it at its rank if selected
     const int e = e0 + warp;
-    const float ze = s_z[e];
-    int cnt = 0;
 #pragma unroll
-    for (int q = 0; q < SI_MAX_EXPERTS / 32; ++q) {
-        const int j = lane + 32 * q;
-        if (j < E) {
-            const float zj = s_z[j];
-            cnt += (zj > ze) | ((zj == ze) & (j < e));
+    for (int t = 0; t < NT; ++t) {  // warp q: the logits of expert e0 + q, the sums of the WPC warps' partials
+        if (t < n) {
+            float z = lane < WPC ? s_part[t][lane][warp] : 0.f;
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) z += __shfl_xor_sync(0xffffffffu, z, m);
+            if (bias_p) z += __ldg(bias_p + e);
+            if (lane < C) st_async_cluster_u32(&s_z[t][e], smem_addr(&s_zbar), (uint32_t)lane, __float_as_uint(z));
+            if (lane == 0 && ologits_p) ologits_p[t * E + e] = z;
         }
     }
-    const int r = __reduce_add_sync(0xffffffffu, cnt);
-    if (lane == 0) {
-        if (r < k) {
-            ids_p[r] = e;
-            wts_p[r] = ze;  // the expert kernel turns these into renormalised weights
-            if (oids_p) oids_p[r] = e;
+    // x quantised per 64-column chunk for the expert kernel (token t at word t * NC * kXqWords); the
+    // first chunk of each warp was loaded above, further ones (n*H/64 > 8*WPC) are loaded here
+    for (int c = qc; c < n * NC; c += C * WPC) {
+        const int t = c / NC, cc = c - t * NC;
+        const uint32_t wv = c == qc ? qword : __ldg(reinterpret_cast<const uint32_t *>(xg_p) + 32 * c + lane);
+        router_quant_chunk(wv, cc, NC, xq_p + (size_t)t * NC * kXqWords, lane, pin_i32(a.act8) != 0);
+    }
+    if (!mbar_wait_warp_cluster(smem_addr(&s_zbar), 0, a.wait_budget)) set_status(a.ctrl + kCtrlStatus, SI_ERR_TIMEOUT);
+    // warp q ranks expert e0 + q against all E logits of each token (greater, or equal
+    // with a lower index, beats it) and stores it at its rank where it is selected
+    int chosen = 0;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        if (t < n) {
+            const float ze = s_z[t][e];
+            int cnt = 0;
+#pragma unroll
+            for (int q = 0; q < SI_MAX_EXPERTS / 32; ++q) {
+                const int j = lane + 32 * q;
+                if (j < E) {
+                    const float zj = s_z[t][j];
+                    cnt += (zj > ze) | ((zj == ze) & (j < e));
+                }
+            }
+            const int r = __reduce_add_sync(0xffffffffu, cnt);
+            if (r < k) {
+                ++chosen;
+                if (lane == 0) {
+                    ids_p[t * k + r] = e;
+                    wts_p[t * k + r] = ze;  // the expert kernel turns these into renormalised weights
+                    if (oids_p) oids_p[t * k + r] = e;
+                }
+            }
         }
-        counts_p[e] = r < k ? 1 : 0;
-        if (ocounts_p) ocounts_p[e] = r < k ? 1 : 0;
+    }
+    if (lane == 0) {
+        counts_p[e] = chosen;
+        if (ocounts_p) ocounts_p[e] = chosen;
     }
 }
 
 template <int WPC, int CPT>
 static cudaError_t launch_router_one(const DecodeArgs &a, cudaStream_t s) {
+    auto kern = a.n == 1 ? k_router_one<WPC, CPT, 1> : k_router_one<WPC, CPT, SI_MAX_DECODE_TOKENS>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(8);
     cfg.blockDim = dim3(32 * WPC);
@@ -779,12 +810,17 @@ static cudaError_t launch_router_one(const DecodeArgs &a, cudaStream_t s) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_router_one<WPC, CPT>, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// Shapes the column-split router takes (E = 8 * WPC experts, H = 32 * WPC * CPT).
+bool router_one_shape(int E, int H) {
+    return (E == 128 && (H == 2048 || H == 1024)) || (E == 64 && (H == 2048 || H == 1024));
 }
 
 static cudaError_t launch_router(const DecodeArgs &a, cudaStream_t s) {
-    // one plain token for the cluster expert kernel: the column-split router
-    if (a.sel_logits && !a.norm_w && a.E % 8 == 0) {
+    // plain tokens for a cluster expert kernel: the column-split router
+    if ((a.sel_logits || a.cl_mt) && !a.norm_w && router_one_shape(a.E, a.H)) {
         const int wpc = a.E / 8;
         if (wpc == 16 && a.H == 512 * 4) return launch_router_one<16, 4>(a, s);
         if (wpc == 16 && a.H == 512 * 2) return launch_router_one<16, 2>(a, s);
@@ -815,7 +851,8 @@ cudaError_t launch_decode(const Plan &p, const DecodeArgs &a_in, cudaStream_t s,
     const bool cluster =
         a.n == 1 && p.cluster_ok && expert_cluster_layout(p.desc, p.cluster_size, p.smem_optin, a);
     // 2..4 tokens of a plain block: the cluster kernel over the distinct experts
-    const bool mt = a.n > 1 && p.cluster_mt_ok && !a.norm_w &&
+    // (its table of distinct experts is formed from the column-split router's ranked ids)
+    const bool mt = a.n > 1 && p.cluster_mt_ok && !a.norm_w && router_one_shape(a.E, a.H) && a.n * a.k <= 32 &&
                     expert_cluster_layout(p.desc, p.cluster_size, p.smem_optin, a, a.n);
     a.cl_mt = mt ? 1 : 0;
     a.cl_active = p.cluster_mt_active;

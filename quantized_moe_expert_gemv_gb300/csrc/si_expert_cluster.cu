@@ -36,14 +36,16 @@
 // launch at once: that kernel's own dependency wait still covers all of this
 // kernel's work.
 //
-// 2..4 tokens (MT): the same kernel over the router's table of distinct
-// experts (sparkinfer README, "Milestone 2": redundant weight reads removed).
-// A unit is (distinct expert s, block column b); its bytes are read once and
-// dotted with the x of every token that chose expert s (ntok[s] <= 4), and h,
-// the down partials and the combine are kept per token.  Units number U * I/256
-// (U known only on the device), so the grid covers the largest possible table
-// and clusters whose s >= U leave at once; the clusters run in waves, with no
-// grid-wide synchronisation.
+// 2..4 tokens (MT): the same kernel over the distinct experts the tokens
+// selected (sparkinfer README, "Milestone 2": redundant weight reads removed).
+// A unit is (distinct expert s, block column b), the distinct experts numbered
+// in ascending id order; its bytes are read once and dotted with the x of every
+// token that chose expert s (at most 4), and h, the down partials and the
+// combine are kept per token.  Each warp derives its unit's expert, tokens and
+// routing weights from the router's ranked ids and logits (mt_unit).  Units
+// number U * I/256 (U known only on the device), so the grid covers the largest
+// possible count and clusters whose s >= U leave at once; the clusters run in
+// waves, with no grid-wide synchronisation.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -80,6 +82,72 @@ __device__ __forceinline__ float quad_sum(float v0, float v1, float v2, float v3
 #pragma unroll
     for (int off = GS / 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     return v;
+}
+
+// One unit of the multi-token kernel, as a whole warp sees it (warp-uniform).
+struct MtUnit {
+    int U;          // distinct experts the n tokens selected
+    int e, nt;      // expert of distinct index s, tokens that chose it
+    int tok[SI_MAX_DECODE_TOKENS];
+    float w[SI_MAX_DECODE_TOKENS];  // their renormalised routing weights for e
+    float wp;       // this lane's pair weight (pair p = lane: token p / k, rank p % k)
+};
+
+// Whole warp, nk = n*k <= 32.  The router left token t's k selected experts at
+// ids[t*k + r] in rank order (descending logits) with their logits at
+// lg[t*k + r].  Pair p = lane: its expert, whether it is the lowest pair id of
+// that expert, and the number of distinct experts with a smaller id (from a
+// 256-bit presence mask); distinct index s is the first pair of the s-th
+// smallest expert, and the pairs that chose it are its tokens, ascending.
+// Weight of pair (t, r): exp(z_r - z_0) / sum_j exp(z_j - z_0) over the
+// token's k logits (z_0 its largest).
+__device__ __forceinline__ MtUnit mt_unit(const int32_t *ids, const float *lg, int nk, int k, int s, int lane,
+                                          bool want_w) {
+    MtUnit u;
+    const bool valid = lane < nk;
+    const int ex = valid ? ids[lane] : 0x7fffffff;
+    const float z = valid ? lg[lane] : 0.f;
+    const unsigned eq = __match_any_sync(0xffffffffu, ex);
+    const bool first = valid && (int)(__ffs(eq) - 1) == lane;
+    const unsigned firsts = __ballot_sync(0xffffffffu, first);
+    u.U = __popc(firsts);
+    int below = 0;
+    const int wsel = valid ? (ex >> 5) : 8, bsel = ex & 31;
+#pragma unroll
+    for (int q = 0; q < SI_MAX_EXPERTS / 32; ++q) {
+        const unsigned m = __reduce_or_sync(0xffffffffu, (first && (ex >> 5) == q) ? (1u << (ex & 31)) : 0u);
+        below += q < wsel ? __popc(m) : q == wsel ? __popc(m & ((1u << bsel) - 1u)) : 0;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, first && below == s);
+    const int src = hit ? (int)(__ffs(hit) - 1) : 0;
+    u.e = __shfl_sync(0xffffffffu, ex, src);
+    const unsigned mine = hit ? __shfl_sync(0xffffffffu, eq, src) : 0u;
+    u.nt = __popc(mine);
+    int pj[SI_MAX_DECODE_TOKENS];
+    unsigned rem = mine;
+#pragma unroll
+    for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {  // the pairs that chose e, ascending
+        pj[t] = rem ? (int)(__ffs(rem) - 1) : 0;
+        rem &= rem - 1u;
+        u.tok[t] = pj[t] / k;
+    }
+    u.wp = 0.f;
+    if (want_w) {  // this lane's pair weight, then the unit's tokens' weights
+        const int base = (lane / k) * k;
+        const float z0 = __shfl_sync(0xffffffffu, z, base);
+        const float ex = expf(z - z0);
+        float den = 0.f;
+        if ((k & (k - 1)) == 0) {  // k a power of two: the token's lanes form a butterfly group
+            den = ex;
+            for (int o = 1; o < k; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        } else {
+            for (int r = 0; r < k; ++r) den += __shfl_sync(0xffffffffu, ex, base + r);
+        }
+        u.wp = ex / den;
+#pragma unroll
+        for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) u.w[t] = __shfl_sync(0xffffffffu, u.wp, pj[t]);
+    }
+    return u;
 }
 
 // Sum of (g, u) over a group of GS lanes; lane 0 of the group gets the g total,
@@ -139,7 +207,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const int I = pin_i32(a.I), H = pin_i32(a.H);
     const float *const wsc = FP4 ? pin_ptr(a.wscale) : nullptr;  // NVFP4 tensor scales [E][3]
     const uint32_t *const xq_g = pin_ptr(a.xq);  // x quantised by the router (plain block)
-    const UniqTable *const uniq = MT ? pin_ptr(a.uniq) : nullptr;
+    const int n_tok = MT ? pin_i32(a.n) : 1;
     const int cl_active = MT ? pin_i32(a.cl_active) : 0;
     const int ystride = MT ? pin_i32(a.cl_ystride) : 0;
 
@@ -277,20 +345,17 @@ __global__ void __launch_bounds__(kClThreads, 1)
     // MT: units past the table of distinct experts have nothing to do (the whole
     // cluster leaves: no copy was issued, no peer stores into it).  The clusters of the
     // last wave let the next kernel launch; the others count as having let it at exit.
-    // The table entries are read together with U (independent loads, one round trip;
-    // the table has room for every unit's slot).
+    // Every warp forms its unit from the router's ranked ids (one round trip of loads).
     int nt = 1, mt_e = 0;
-    int4 mt_tok = make_int4(0, 0, 0, 0);
+    MtUnit mu{};
     if (MT) {
-        const int U = ctrl[kCtrlNumUnique];
-        const int ntv = uniq->ntok[slot];
-        mt_e = uniq->expert[slot];
-        mt_tok = *reinterpret_cast<const int4 *>(&uniq->tok[slot][0]);
-        if (slot >= U) return;
-        nt = ntv;
-        if (unit >= U * nbI - cl_active) pdl_launch_dependents();
+        mu = mt_unit(ids, zsel, n_tok * k, k, slot, lane, warp == 0);  // warp 0 reports the weights
+        if (slot >= mu.U) return;
+        nt = mu.nt;
+        mt_e = mu.e;
+        if (unit >= mu.U * nbI - cl_active) pdl_launch_dependents();
     }
-    auto unit_tok = [&mt_tok](int t) { return t == 0 ? mt_tok.x : t == 1 ? mt_tok.y : t == 2 ? mt_tok.z : mt_tok.w; };
+    auto unit_tok = [&mu](int t) { return t == 0 ? mu.tok[0] : t == 1 ? mu.tok[1] : t == 2 ? mu.tok[2] : mu.tok[3]; };
     // The router left the k selected experts in rank order with their logits.
     // Only the producer thread needs this unit's expert id, to address its
     // copies: it reads it itself and issues them at once.  The renormalised
@@ -299,10 +364,12 @@ __global__ void __launch_bounds__(kClThreads, 1)
     // meanwhile (CTA 0 reports them); the __syncthreads before the reductions
     // publishes it.
     if (MT) {
-        if (warp == 0 && lane < nt) {
-            const int tk = unit_tok(lane);
-            s_tok[lane] = tk;
-            s_wt[lane] = zsel[tk * k + uniq->slot[slot][lane]];  // the router's renormalised weight
+        if (warp == 0) {
+            if (lane < nt) {
+                s_tok[lane] = unit_tok(lane);
+                s_wt[lane] = lane == 0 ? mu.w[0] : lane == 1 ? mu.w[1] : lane == 2 ? mu.w[2] : mu.w[3];
+            }
+            if (blockIdx.x == 0 && o_w && lane < n_tok * k) o_w[lane] = mu.wp;
         }
     } else if (warp == 0) {
         const float zr = lane < k ? zsel[lane] : 0.f;

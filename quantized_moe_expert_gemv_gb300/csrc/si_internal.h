@@ -166,6 +166,7 @@ cudaError_t launch_expert_fused(const DecodeArgs &a, int grid, cudaStream_t s);
 cudaError_t expert_fused_occupancy(int nbh, bool dedup, int smem, int smem_max, int *blocks_per_sm);
 bool expert_cluster_layout(const si_moe_desc &d, int C, int smem_max, DecodeArgs &a, int nt = 1);
 cudaError_t launch_expert_cluster(const DecodeArgs &a, cudaStream_t s);
+bool router_one_shape(int E, int H);  // the column-split router takes this shape
 cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *active_clusters, bool mt = false);
 cudaError_t launch_debug_dequant(const uint8_t *blocks, int64_t n_blocks, float *out_f32,
                                  uint16_t *out_bf16, cudaStream_t s);

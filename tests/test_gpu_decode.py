@@ -224,6 +224,7 @@ def test_decode_dedup_batches_match_per_token_oracle(n):
 @pytest.mark.parametrize("H,I,E,k,n", [
     (256, 256, 8, 2, 1), (512, 768, 16, 4, 3), (768, 512, 4, 4, 2), (1024, 256, 32, 1, 4),
     (256, 1280, 6, 3, 1), (4096, 256, 8, 8, 2), (256, 256, 1, 1, 1), (2048, 768, 256, 16, 4),
+    (1024, 512, 64, 8, 4), (2048, 256, 128, 4, 3), (1024, 256, 64, 2, 2),
 ])
 def test_decode_shapes(H, I, E, k, n):
     shape = synth.MoeShape(H, I, E, k)
@@ -312,14 +313,14 @@ def test_fused_path_is_taken_for_the_qwen3_shape():
     assert binding.si_debug_decode_fused(plan_h768, 1) == 0
 
 
-@pytest.mark.parametrize("n,prenorm", [(1, False), (2, False), (2, True)])
-def test_bounded_wait_timeout_is_reported_and_the_context_survives(monkeypatch, n, prenorm):
+@pytest.mark.parametrize("n,prenorm,shape", [(1, False, synth.TINY), (2, False, synth.MoeShape(1024, 256, 64, 4)),
+                                             (2, True, synth.TINY)])
+def test_bounded_wait_timeout_is_reported_and_the_context_survives(monkeypatch, n, prenorm, shape):
     """A wait budget of 0 cycles makes every device-side wait of the expert
     kernel (cluster kernel for n = 1, the cluster kernel over the distinct
     experts for n = 2, the grid-synchronised kernel for n = 2 in a pre-normed
     block) give up at once: the kernel must record SI_ERR_TIMEOUT, let its
     copies land, and return; the next call on a fresh scratch must be right."""
-    shape = synth.TINY
     layer = synth.make_layer(shape, seed=0)
     if prenorm:
         layer.norm_weight = synth.make_norm_weight(shape, seed=0)
@@ -330,7 +331,7 @@ def test_bounded_wait_timeout_is_reported_and_the_context_survives(monkeypatch, 
     monkeypatch.setenv("SI_FAULT_WAIT_BUDGET", "0")
     plan0 = binding.si_moe_plan(device.desc_for(shape))
     monkeypatch.delenv("SI_FAULT_WAIT_BUDGET")
-    assert binding.si_debug_decode_fused(plan0, n) == (2 if n == 1 else 3)  # pre-normed n > 1: grid kernel
+    assert binding.si_debug_decode_fused(plan0, n) == (2 if n == 1 else 3 if not prenorm else 1)
     scratch = device.alloc_scratch(plan0, binding.SI_MODE_DECODE, n)
     out = torch.zeros((n, shape.hidden), dtype=torch.float32, device="cuda")
     binding.si_moe_forward_decode(plan0, dl.struct(), x, n, out, None, scratch)
