@@ -630,15 +630,21 @@ static cudaError_t launch_router_t(const DecodeArgs &a, cudaStream_t s) {
 // Then every CTA receives every logit by asynchronous stores, and each warp
 // ranks its own expert for every token (descending logits, ties to the lower
 // index) and stores it at its rank, with its logit, where it is selected; the
-// expert kernel forms the renormalised weights (and, for several tokens, the
-// table of distinct experts) from these.  x is quantised for the expert
-// kernel, which is launched at once.
+// expert kernel forms the renormalised weights from these.  Several tokens:
+// each CTA also sends its experts' selection bits to every CTA (a second
+// asynchronous exchange), so that each selected expert's warp knows its index
+// among the distinct experts (ascending id) and writes its entry of the table
+// (expert, tokens that chose it with their ranks); CTA 0 writes their number.
+// x is quantised for the expert kernel, which is launched at once.
 template <int WPC, int CPT, int NT>
 __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
     // NT: 1 (one token) or SI_MAX_DECODE_TOKENS (n = 2..NT tokens)
     __shared__ float s_z[NT][SI_MAX_EXPERTS];
     __shared__ float s_part[NT][WPC][WPC];  // [token][warp][local expert]
     __shared__ __align__(8) uint64_t s_zbar;
+    __shared__ __align__(8) uint64_t s_selbar;  // several tokens: every CTA's selection bits have arrived
+    __shared__ uint32_t s_sel[8];               // [CTA] bit w: expert 8*WPC... of warp w chosen by some token
+    __shared__ uint32_t s_mysel;
     const uint16_t *const xg_p = pin_ptr(a.x);
     float *const out_p = pin_ptr(a.out);
     const float *const bias_p = pin_ptr(a.router_bias);
@@ -677,8 +683,11 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
         prefetch_l2(reinterpret_cast<const uint8_t *>(xg_p) + 128 * threadIdx.x);
     if (threadIdx.x == 0) {
         mbar_init(smem_addr(&s_zbar), 1);
+        if (NT > 1) mbar_init(smem_addr(&s_selbar), 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(smem_addr(&s_zbar), (uint32_t)(n * E * 4));  // every logit, once
+        if (NT > 1) mbar_arrive_expect_tx(smem_addr(&s_selbar), (uint32_t)(C * 4));
+        s_mysel = 0;
     }
     __syncthreads();
     cluster_arrive_relaxed();
@@ -763,8 +772,10 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
     // warp q ranks expert e0 + q against all E logits of each token (greater, or equal
     // with a lower index, beats it) and stores it at its rank where it is selected
     int chosen = 0;
+    int rk[NT];  // this expert's rank for each token
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
+        rk[t] = k;
         if (t < n) {
             const float ze = s_z[t][e];
             int cnt = 0;
@@ -777,6 +788,7 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
                 }
             }
             const int r = __reduce_add_sync(0xffffffffu, cnt);
+            rk[t] = r;
             if (r < k) {
                 ++chosen;
                 if (lane == 0) {
@@ -790,6 +802,39 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
     if (lane == 0) {
         counts_p[e] = chosen;
         if (ocounts_p) ocounts_p[e] = chosen;
+    }
+    if (NT > 1) {  // the table of distinct experts
+        if (lane == 0 && chosen) atomicOr(&s_mysel, 1u << warp);
+        __syncthreads();
+        if (warp == 0 && lane < C)
+            st_async_cluster_u32(&s_sel[blockIdx.x], smem_addr(&s_selbar), (uint32_t)lane, s_mysel);
+        // every warp waits (the CTA may leave only once every peer's store has landed)
+        if (!mbar_wait_warp_cluster(smem_addr(&s_selbar), 0, a.wait_budget)) {
+            set_status(a.ctrl + kCtrlStatus, SI_ERR_TIMEOUT);
+            return;
+        }
+        int U = 0, below = 0;
+        for (int c = 0; c < C; ++c) {
+            const int pc = __popc(s_sel[c]);
+            U += pc;
+            below += c < (int)blockIdx.x ? pc : 0;
+        }
+        below += __popc(s_sel[blockIdx.x] & ((1u << warp) - 1u));
+        if (chosen && lane == 0) {
+            UniqTable *u = a.uniq;
+            u->expert[below] = e;
+            u->ntok[below] = chosen;
+            int j = 0;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                if (t < n && rk[t] < k) {
+                    u->tok[below][j] = t;
+                    u->slot[below][j] = rk[t];
+                    ++j;
+                }
+            }
+        }
+        if (blockIdx.x == 0 && threadIdx.x == 0) a.ctrl[kCtrlNumUnique] = U;
     }
 }
 

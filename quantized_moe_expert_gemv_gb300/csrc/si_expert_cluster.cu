@@ -41,11 +41,11 @@
 // A unit is (distinct expert s, block column b), the distinct experts numbered
 // in ascending id order; its bytes are read once and dotted with the x of every
 // token that chose expert s (at most 4), and h, the down partials and the
-// combine are kept per token.  Each warp derives its unit's expert, tokens and
-// routing weights from the router's ranked ids and logits (mt_unit).  Units
-// number U * I/256 (U known only on the device), so the grid covers the largest
-// possible count and clusters whose s >= U leave at once; the clusters run in
-// waves, with no grid-wide synchronisation.
+// combine are kept per token.  The router leaves the table of distinct experts
+// (expert, tokens, their ranks) and the ranked logits; warp 0 forms the
+// routing weights.  Units number U * I/256 (U known only on the device), so
+// the grid covers the largest possible count and clusters whose s >= U leave
+// at once; the clusters run in waves, with no grid-wide synchronisation.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -82,72 +82,6 @@ __device__ __forceinline__ float quad_sum(float v0, float v1, float v2, float v3
 #pragma unroll
     for (int off = GS / 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     return v;
-}
-
-// One unit of the multi-token kernel, as a whole warp sees it (warp-uniform).
-struct MtUnit {
-    int U;          // distinct experts the n tokens selected
-    int e, nt;      // expert of distinct index s, tokens that chose it
-    int tok[SI_MAX_DECODE_TOKENS];
-    float w[SI_MAX_DECODE_TOKENS];  // their renormalised routing weights for e
-    float wp;       // this lane's pair weight (pair p = lane: token p / k, rank p % k)
-};
-
-// Whole warp, nk = n*k <= 32.  The router left token t's k selected experts at
-// ids[t*k + r] in rank order (descending logits) with their logits at
-// lg[t*k + r].  Pair p = lane: its expert, whether it is the lowest pair id of
-// that expert, and the number of distinct experts with a smaller id (from a
-// 256-bit presence mask); distinct index s is the first pair of the s-th
-// smallest expert, and the pairs that chose it are its tokens, ascending.
-// Weight of pair (t, r): exp(z_r - z_0) / sum_j exp(z_j - z_0) over the
-// token's k logits (z_0 its largest).
-__device__ __forceinline__ MtUnit mt_unit(const int32_t *ids, const float *lg, int nk, int k, int s, int lane,
-                                          bool want_w) {
-    MtUnit u;
-    const bool valid = lane < nk;
-    const int ex = valid ? ids[lane] : 0x7fffffff;
-    const float z = valid ? lg[lane] : 0.f;
-    const unsigned eq = __match_any_sync(0xffffffffu, ex);
-    const bool first = valid && (int)(__ffs(eq) - 1) == lane;
-    const unsigned firsts = __ballot_sync(0xffffffffu, first);
-    u.U = __popc(firsts);
-    int below = 0;
-    const int wsel = valid ? (ex >> 5) : 8, bsel = ex & 31;
-#pragma unroll
-    for (int q = 0; q < SI_MAX_EXPERTS / 32; ++q) {
-        const unsigned m = __reduce_or_sync(0xffffffffu, (first && (ex >> 5) == q) ? (1u << (ex & 31)) : 0u);
-        below += q < wsel ? __popc(m) : q == wsel ? __popc(m & ((1u << bsel) - 1u)) : 0;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, first && below == s);
-    const int src = hit ? (int)(__ffs(hit) - 1) : 0;
-    u.e = __shfl_sync(0xffffffffu, ex, src);
-    const unsigned mine = hit ? __shfl_sync(0xffffffffu, eq, src) : 0u;
-    u.nt = __popc(mine);
-    int pj[SI_MAX_DECODE_TOKENS];
-    unsigned rem = mine;
-#pragma unroll
-    for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) {  // the pairs that chose e, ascending
-        pj[t] = rem ? (int)(__ffs(rem) - 1) : 0;
-        rem &= rem - 1u;
-        u.tok[t] = pj[t] / k;
-    }
-    u.wp = 0.f;
-    if (want_w) {  // this lane's pair weight, then the unit's tokens' weights
-        const int base = (lane / k) * k;
-        const float z0 = __shfl_sync(0xffffffffu, z, base);
-        const float ex = expf(z - z0);
-        float den = 0.f;
-        if ((k & (k - 1)) == 0) {  // k a power of two: the token's lanes form a butterfly group
-            den = ex;
-            for (int o = 1; o < k; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        } else {
-            for (int r = 0; r < k; ++r) den += __shfl_sync(0xffffffffu, ex, base + r);
-        }
-        u.wp = ex / den;
-#pragma unroll
-        for (int t = 0; t < SI_MAX_DECODE_TOKENS; ++t) u.w[t] = __shfl_sync(0xffffffffu, u.wp, pj[t]);
-    }
-    return u;
 }
 
 // Sum of (g, u) over a group of GS lanes; lane 0 of the group gets the g total,
@@ -208,6 +142,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     const float *const wsc = FP4 ? pin_ptr(a.wscale) : nullptr;  // NVFP4 tensor scales [E][3]
     const uint32_t *const xq_g = pin_ptr(a.xq);  // x quantised by the router (plain block)
     const int n_tok = MT ? pin_i32(a.n) : 1;
+    const UniqTable *const uniq = MT ? pin_ptr(a.uniq) : nullptr;
     const int cl_active = MT ? pin_i32(a.cl_active) : 0;
     const int ystride = MT ? pin_i32(a.cl_ystride) : 0;
 
@@ -345,17 +280,20 @@ __global__ void __launch_bounds__(kClThreads, 1)
     // MT: units past the table of distinct experts have nothing to do (the whole
     // cluster leaves: no copy was issued, no peer stores into it).  The clusters of the
     // last wave let the next kernel launch; the others count as having let it at exit.
-    // Every warp forms its unit from the router's ranked ids (one round trip of loads).
+    // The unit's table entry is read together with U (independent loads, one round
+    // trip; the table has room for every unit's slot).
     int nt = 1, mt_e = 0;
-    MtUnit mu{};
+    int4 mt_tok = make_int4(0, 0, 0, 0);
     if (MT) {
-        mu = mt_unit(ids, zsel, n_tok * k, k, slot, lane, warp == 0);  // warp 0 reports the weights
-        if (slot >= mu.U) return;
-        nt = mu.nt;
-        mt_e = mu.e;
-        if (unit >= mu.U * nbI - cl_active) pdl_launch_dependents();
+        const int U = ctrl[kCtrlNumUnique];
+        const int ntv = uniq->ntok[slot];
+        mt_e = uniq->expert[slot];
+        mt_tok = *reinterpret_cast<const int4 *>(&uniq->tok[slot][0]);
+        if (slot >= U) return;
+        nt = ntv;
+        if (unit >= U * nbI - cl_active) pdl_launch_dependents();
     }
-    auto unit_tok = [&mu](int t) { return t == 0 ? mu.tok[0] : t == 1 ? mu.tok[1] : t == 2 ? mu.tok[2] : mu.tok[3]; };
+    auto unit_tok = [&mt_tok](int t) { return t == 0 ? mt_tok.x : t == 1 ? mt_tok.y : t == 2 ? mt_tok.z : mt_tok.w; };
     // The router left the k selected experts in rank order with their logits.
     // Only the producer thread needs this unit's expert id, to address its
     // copies: it reads it itself and issues them at once.  The renormalised
@@ -365,11 +303,25 @@ __global__ void __launch_bounds__(kClThreads, 1)
     // publishes it.
     if (MT) {
         if (warp == 0) {
+            // pair p = lane (token p / k, rank p % k): exp(z_p - z_0) / sum over the token's k
+            // logits (z_0 its largest, at rank 0); then the weights of the unit's tokens
+            const int nk = n_tok * k;
+            const float z = lane < nk ? zsel[lane] : 0.f;
+            const int4 sl = *reinterpret_cast<const int4 *>(&uniq->slot[slot][0]);
+            const int base = (lane / k) * k;
+            const float ex = expf(z - __shfl_sync(0xffffffffu, z, base));
+            float den = 0.f;
+            for (int r = 0; r < k; ++r) den += __shfl_sync(0xffffffffu, ex, base + r);
+            const float wp = ex / den;
+            if (blockIdx.x == 0 && o_w && lane < nk) o_w[lane] = wp;
+            const int my_t = lane < nt ? lane : 0;
+            const int tk = unit_tok(my_t);
+            const int sr = my_t == 0 ? sl.x : my_t == 1 ? sl.y : my_t == 2 ? sl.z : sl.w;
+            const float wt = __shfl_sync(0xffffffffu, wp, tk * k + sr);
             if (lane < nt) {
-                s_tok[lane] = unit_tok(lane);
-                s_wt[lane] = lane == 0 ? mu.w[0] : lane == 1 ? mu.w[1] : lane == 2 ? mu.w[2] : mu.w[3];
+                s_tok[lane] = tk;
+                s_wt[lane] = wt;
             }
-            if (blockIdx.x == 0 && o_w && lane < n_tok * k) o_w[lane] = mu.wp;
         }
     } else if (warp == 0) {
         const float zr = lane < k ? zsel[lane] : 0.f;
