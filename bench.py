@@ -755,7 +755,8 @@ def dedup_probe(args, binding, device, synth, torch):
     assert st == binding.SI_OK, binding.si_status_string(st)
     U = (counts > 0).sum(dim=1).tolist()
     return {"dedup_probe_steps": S, "unique_experts_per_step": U, "bytes_per_expert": shape.expert_bytes,
-            "expert_kernel": "k_expert" if binding.si_debug_decode_fused(plan, n) >= 1 else "generic"}
+            "expert_kernel": {3: "k_expert_cluster (distinct-expert units)", 1: "k_expert"}.get(
+                binding.si_debug_decode_fused(plan, n), "generic")}
 
 
 def run_ours(args, dist):
