@@ -178,22 +178,28 @@ si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *o
             }
             cudaGetLastError();
         }
-        // 2..4 plain Q4_K tokens: the same clusters over the distinct experts, in waves
+        // 2..4 tokens of a plain block: clusters over the distinct experts, in waves.  The
+        // single-token cluster size if the per-token buffers fit beside its stages, else the
+        // smallest larger size that fits (one resident cluster is enough: the units run in
+        // waves).  The int8-activation flag applies to single tokens only: batched tokens
+        // keep int16 activations.
         p.cluster_mt_ok = false;
+        p.cluster_mt_size = 0;
         p.cluster_mt_active = 0;
-        si::DecodeArgs tmp{};
-        // (the int8-activation flag applies to single tokens only: batched tokens keep int16)
-        if (p.cluster_ok && desc->wtype == SI_WTYPE_Q4_K && si::router_one_shape(desc->n_experts, desc->hidden) &&
-            desc->top_k <= 8 &&
-            si::expert_cluster_layout(*desc, p.cluster_size, p.smem_optin, tmp, SI_MAX_DECODE_TOKENS)) {
-            int clusters = 0;
-            if (si::expert_cluster_prepare(desc->hidden / 256, p.smem_optin, tmp.cl_smem, p.cluster_size, &clusters,
-                                           true) == cudaSuccess &&
-                clusters >= 1) {
-                p.cluster_mt_ok = true;
-                p.cluster_mt_active = clusters;
+        if (p.cluster_ok && si::router_one_shape(desc->n_experts, desc->hidden) && desc->top_k <= 8) {
+            for (int C = p.cluster_size; C <= 8 && !p.cluster_mt_ok; ++C) {
+                si::DecodeArgs tmp{};
+                if (!si::expert_cluster_layout(*desc, C, p.smem_optin, tmp, SI_MAX_DECODE_TOKENS)) continue;
+                int clusters = 0;
+                if (si::expert_cluster_prepare(desc->hidden / 256, p.smem_optin, tmp.cl_smem, C, &clusters, true) ==
+                        cudaSuccess &&
+                    clusters >= 1) {
+                    p.cluster_mt_ok = true;
+                    p.cluster_mt_size = C;
+                    p.cluster_mt_active = clusters;
+                }
+                cudaGetLastError();
             }
-            cudaGetLastError();
         }
     }
     p.prefill_ok = si::prefill_prepare(p) == cudaSuccess;

@@ -898,7 +898,7 @@ cudaError_t launch_decode(const Plan &p, const DecodeArgs &a_in, cudaStream_t s,
     // 2..4 tokens of a plain block: the cluster kernel over the distinct experts
     // (its table of distinct experts is formed from the column-split router's ranked ids)
     const bool mt = a.n > 1 && p.cluster_mt_ok && !a.norm_w && router_one_shape(a.E, a.H) && a.n * a.k <= 32 &&
-                    expert_cluster_layout(p.desc, p.cluster_size, p.smem_optin, a, a.n);
+                    expert_cluster_layout(p.desc, p.cluster_mt_size, p.smem_optin, a, a.n);
     a.cl_mt = mt ? 1 : 0;
     a.cl_active = p.cluster_mt_active;
     a.zero_out = cluster || mt ? 1 : 0;

@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
     __shared__ int s_lastB;
     __shared__ int s_tok[SI_MAX_DECODE_TOKENS];    // MT: the unit's tokens
     __shared__ float s_wt[SI_MAX_DECODE_TOKENS];   // MT: their routing weights for expert s
-    static_assert(!MT || (WF == 0 && !NORM), "the multi-token units take plain Q4_K blocks");
+    static_assert(!MT || (WF != 2 && !NORM), "the multi-token units take plain Q4_K, NVFP4 or Q5_K blocks");
     // the next kernel's dependency wait still covers this whole grid; MT: see below
     if (!MT) pdl_launch_dependents();
 
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
             const float wt = __shfl_sync(0xffffffffu, wp, tk * k + sr);
             if (lane < nt) {
                 s_tok[lane] = tk;
-                s_wt[lane] = wt;
+                s_wt[lane] = FP4 ? wt * wsc[3 * mt_e + 2] : wt;  // NVFP4: times the down tensor scale
             }
         }
     } else if (warp == 0) {
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kClThreads, 1)
         // NVFP4: this unit's expert's gate and up tensor scales
         float tsg = 1.f, tsu = 1.f;
         if (FP4) {
-            const int eu = ids[slot];
+            const int eu = MT ? mt_e : ids[slot];
             tsg = wsc[3 * eu];
             tsu = wsc[3 * eu + 1];
         }
@@ -759,7 +759,11 @@ static cudaError_t launch_cluster_t(const DecodeArgs &a, const CUtensorMap &tm, 
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (a.cl_mt) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 0, true>, tm, tt, a);
+    if (a.cl_mt) {
+        if (a.wtype == SI_WTYPE_NVFP4) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 1, true>, tm, tt, a);
+        if (a.wtype == SI_WTYPE_Q5_K) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 3, true>, tm, tt, a);
+        return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 0, true>, tm, tt, a);
+    }
     if (a.wtype == SI_WTYPE_NVFP4) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 1, false>, tm, tt, a);
     if (a.wtype == SI_WTYPE_Q5_K) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 3, false>, tm, tt, a);
     if (a.act8) return cudaLaunchKernelEx(&cfg, k_expert_cluster<NBH, false, 2, false>, tm, tt, a);
@@ -787,6 +791,8 @@ cudaError_t expert_cluster_prepare(int nbh, int smem_max, int smem, int C, int *
 #define SI_CL_VARIANTS(B)                                                                              \
     if (mt) {                                                                                          \
         fs[0] = (const void *)k_expert_cluster<B, false, 0, true>;                                     \
+        fs[1] = (const void *)k_expert_cluster<B, false, 1, true>;                                     \
+        fs[2] = (const void *)k_expert_cluster<B, false, 3, true>;                                     \
     } else {                                                                                           \
         fs[0] = (const void *)k_expert_cluster<B, false, 0, false>;                                    \
         fs[1] = (const void *)k_expert_cluster<B, true, 0, false>;                                     \

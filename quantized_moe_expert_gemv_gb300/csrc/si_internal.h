@@ -57,6 +57,7 @@ struct Plan {
     bool fused_ok[SI_MAX_DECODE_TOKENS + 1];  // fused expert kernel usable for n tokens
     bool cluster_ok;                          // cluster expert kernel usable for n = 1
     bool cluster_mt_ok;                       // and for 2..4 tokens (units of distinct experts)
+    int cluster_mt_size;                      // CTAs per cluster of the multi-token kernel
     int cluster_mt_active;                    // resident clusters of the multi-token kernel
     bool prefill_ok;                          // tensor-core prefill kernels configured
     int cluster_size;                         // CTAs per cluster (all clusters co-resident)

@@ -110,7 +110,7 @@ def test_nvfp4_decode_small_batches(n):
     shape = synth.QWEN3_30B_A3B
     layer = synth.make_layer_nvfp4(shape, seed=2)
     plan = binding.si_moe_plan(_desc(shape))
-    assert binding.si_debug_decode_fused(plan, n) == 0  # the generic kernels serve NVFP4 batches
+    assert binding.si_debug_decode_fused(plan, n) == 3  # the cluster kernel over the distinct experts
     x = synth.make_tokens(shape, seed=10 + n, n_tokens=n)
     out, ids, w = _decode(layer, x, plan=plan)
     _check(layer, x, out, ids, w)

@@ -118,6 +118,7 @@ def test_q5k_decode_small_batches(n):
     shape = synth.QWEN3_30B_A3B
     layer = synth.make_layer_q5k(shape, seed=2)
     plan = binding.si_moe_plan(_desc(shape))
+    assert binding.si_debug_decode_fused(plan, n) == 3  # the cluster kernel over the distinct experts
     x = synth.make_tokens(shape, seed=20 + n, n_tokens=n)
     out, ids, w = _decode(plan, device.to_device(layer), x, shape)
     _check(layer, x, out, ids, w)
