@@ -631,10 +631,13 @@ static cudaError_t launch_router_t(const DecodeArgs &a, cudaStream_t s) {
 // ranks its own expert for every token (descending logits, ties to the lower
 // index) and stores it at its rank, with its logit, where it is selected; the
 // expert kernel forms the renormalised weights from these.  Several tokens:
-// each CTA also sends its experts' selection bits to every CTA (a second
-// asynchronous exchange), so that each selected expert's warp knows its index
-// among the distinct experts (ascending id) and writes its entry of the table
-// (expert, tokens that chose it with their ranks); CTA 0 writes their number.
+// each CTA also sends, for each token count c, the bits of its experts that c
+// tokens chose to every CTA (a second asynchronous exchange), so that each
+// selected expert's warp knows its index among the distinct experts and
+// writes its entry of the table (expert, tokens that chose it with their
+// ranks); CTA 0 writes their number.  The table lists the experts by token
+// count, descending, then by id: the expert kernel's units of the experts
+// several tokens chose take longest, and so start in its first wave.
 // x is quantised for the expert kernel, which is launched at once.
 template <int WPC, int CPT, int NT>
 __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
@@ -643,8 +646,8 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
     __shared__ float s_part[NT][WPC][WPC];  // [token][warp][local expert]
     __shared__ __align__(8) uint64_t s_zbar;
     __shared__ __align__(8) uint64_t s_selbar;  // several tokens: every CTA's selection bits have arrived
-    __shared__ uint32_t s_sel[8];               // [CTA] bit w: expert 8*WPC... of warp w chosen by some token
-    __shared__ uint32_t s_mysel;
+    __shared__ uint32_t s_sel[8][NT];           // [CTA][c-1] bit w: the CTA's expert w was chosen by c tokens
+    __shared__ uint32_t s_mysel[NT];
     const uint16_t *const xg_p = pin_ptr(a.x);
     float *const out_p = pin_ptr(a.out);
     const float *const bias_p = pin_ptr(a.router_bias);
@@ -686,8 +689,8 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
         if (NT > 1) mbar_init(smem_addr(&s_selbar), 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(smem_addr(&s_zbar), (uint32_t)(n * E * 4));  // every logit, once
-        if (NT > 1) mbar_arrive_expect_tx(smem_addr(&s_selbar), (uint32_t)(C * 4));
-        s_mysel = 0;
+        if (NT > 1) mbar_arrive_expect_tx(smem_addr(&s_selbar), (uint32_t)(C * NT * 4));
+        for (int c = 0; c < NT; ++c) s_mysel[c] = 0;
     }
     __syncthreads();
     cluster_arrive_relaxed();
@@ -804,22 +807,28 @@ __global__ void __launch_bounds__(32 * WPC) k_router_one(DecodeArgs a) {
         if (ocounts_p) ocounts_p[e] = chosen;
     }
     if (NT > 1) {  // the table of distinct experts
-        if (lane == 0 && chosen) atomicOr(&s_mysel, 1u << warp);
+        if (lane == 0 && chosen) atomicOr(&s_mysel[chosen - 1], 1u << warp);
         __syncthreads();
         if (warp == 0 && lane < C)
-            st_async_cluster_u32(&s_sel[blockIdx.x], smem_addr(&s_selbar), (uint32_t)lane, s_mysel);
+#pragma unroll
+            for (int c = 0; c < NT; ++c)
+                st_async_cluster_u32(&s_sel[blockIdx.x][c], smem_addr(&s_selbar), (uint32_t)lane, s_mysel[c]);
         // every warp waits (the CTA may leave only once every peer's store has landed)
         if (!mbar_wait_warp_cluster(smem_addr(&s_selbar), 0, a.wait_budget)) {
             set_status(a.ctrl + kCtrlStatus, SI_ERR_TIMEOUT);
             return;
         }
+        // index: experts chosen by more tokens, then those chosen as often with a smaller id
         int U = 0, below = 0;
-        for (int c = 0; c < C; ++c) {
-            const int pc = __popc(s_sel[c]);
-            U += pc;
-            below += c < (int)blockIdx.x ? pc : 0;
+        for (int cta = 0; cta < C; ++cta) {
+#pragma unroll
+            for (int c = 0; c < NT; ++c) {
+                const int pc = __popc(s_sel[cta][c]);
+                U += pc;
+                below += (c + 1 > chosen || (c + 1 == chosen && cta < (int)blockIdx.x)) ? pc : 0;
+            }
         }
-        below += __popc(s_sel[blockIdx.x] & ((1u << warp) - 1u));
+        if (chosen) below += __popc(s_sel[blockIdx.x][chosen - 1] & ((1u << warp) - 1u));
         if (chosen && lane == 0) {
             UniqTable *u = a.uniq;
             u->expert[below] = e;

@@ -43,7 +43,8 @@
 // 2..4 tokens (MT): the same kernel over the distinct experts the tokens
 // selected (sparkinfer README, "Milestone 2": redundant weight reads removed).
 // A unit is (distinct expert s, block column b), the distinct experts numbered
-// in ascending id order; its bytes are read once and dotted with the x of every
+// in the router's table order (token count descending, then id); its bytes are
+// read once and dotted with the x of every
 // token that chose expert s (at most 4), and h, the down partials and the
 // combine are kept per token.  The router leaves the table of distinct experts
 // (expert, tokens, their ranks) and the ranked logits; warp 0 forms the
