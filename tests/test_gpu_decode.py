@@ -221,6 +221,28 @@ def test_decode_dedup_batches_match_per_token_oracle(n):
             parity.assert_close(out[t], o1[0], "batched vs single")
 
 
+@pytest.mark.parametrize("shape,n", [(synth.QWEN3_30B_A3B, 4), (synth.QWEN3_30B_A3B, 2), (synth.MoeShape(1024, 512, 64, 8), 3)])
+def test_decode_batched_identical_tokens_reduce_to_one_token(shape, n):
+    """n copies of one token: every distinct expert is chosen by all n tokens, so
+    every unit of the multi-token kernel runs its full token loop (x, h and the
+    down partials per token).  Each output must match the oracle and the
+    single-token decode of the same token, with identical routing."""
+    layer = synth.make_layer(shape, seed=41 + n)
+    r = Runner(layer)
+    assert binding.si_debug_decode_fused(r.plan, n) == 3
+    x1 = synth.make_tokens(shape, seed=41 + n, n_tokens=1)
+    x = np.repeat(x1, n, axis=0)
+    out, ids, w, counts, _ = r.decode(x)
+    o1, i1, w1, _, _ = r.decode(x1)
+    assert np.array_equal(counts, np.bincount(ids.reshape(-1), minlength=shape.n_experts))
+    assert sorted(set(counts.tolist()) - {0}) == [n]
+    for t in range(n):
+        assert np.array_equal(ids[t], i1[0])
+        np.testing.assert_allclose(w[t], w1[0], rtol=0, atol=2e-6)
+        parity.assert_close(out[t], o1[0], "batched copy vs single")
+    check_tokens(layer, x, out, ids, w)
+
+
 @pytest.mark.parametrize("H,I,E,k,n", [
     (256, 256, 8, 2, 1), (512, 768, 16, 4, 3), (768, 512, 4, 4, 2), (1024, 256, 32, 1, 4),
     (256, 1280, 6, 3, 1), (4096, 256, 8, 8, 2), (256, 256, 1, 1, 1), (2048, 768, 256, 16, 4),

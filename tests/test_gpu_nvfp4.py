@@ -116,6 +116,24 @@ def test_nvfp4_decode_small_batches(n):
     _check(layer, x, out, ids, w)
 
 
+def test_nvfp4_decode_batched_identical_tokens():
+    """Four copies of one token: every unit of the multi-token kernel takes all four
+    tokens (NVFP4 tensor scales per unit, the down scale on each token's weight)."""
+    shape = synth.QWEN3_30B_A3B
+    layer = synth.make_layer_nvfp4(shape, seed=5)
+    plan = binding.si_moe_plan(_desc(shape))
+    assert binding.si_debug_decode_fused(plan, 4) == 3
+    x1 = synth.make_tokens(shape, seed=5, n_tokens=1)
+    x = np.repeat(x1, 4, axis=0)
+    dl = device.to_device(layer)
+    out, ids, w = _decode(layer, x, dl, plan)
+    o1, i1, w1 = _decode(layer, x1, dl, plan)
+    for t in range(4):
+        assert np.array_equal(ids[t], i1[0])
+        parity.assert_close(out[t], o1[0], "batched copy vs single")
+    _check(layer, x, out, ids, w)
+
+
 @pytest.mark.parametrize("H,I,E,k", [(512, 256, 16, 4), (1024, 768, 32, 8), (256, 512, 8, 1)])
 def test_nvfp4_decode_shapes(H, I, E, k):
     shape = synth.MoeShape(H, I, E, k)

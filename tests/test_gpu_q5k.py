@@ -124,6 +124,24 @@ def test_q5k_decode_small_batches(n):
     _check(layer, x, out, ids, w)
 
 
+def test_q5k_decode_batched_identical_tokens():
+    """Four copies of one token: every unit of the multi-token kernel (Q5_K blocks,
+    its own cluster size) takes all four tokens."""
+    shape = synth.QWEN3_30B_A3B
+    layer = synth.make_layer_q5k(shape, seed=6)
+    plan = binding.si_moe_plan(_desc(shape))
+    assert binding.si_debug_decode_fused(plan, 4) == 3
+    dl = device.to_device(layer)
+    x1 = synth.make_tokens(shape, seed=6, n_tokens=1)
+    x = np.repeat(x1, 4, axis=0)
+    out, ids, w = _decode(plan, dl, x, shape)
+    o1, i1, w1 = _decode(plan, dl, x1, shape)
+    for t in range(4):
+        assert np.array_equal(ids[t], i1[0])
+        parity.assert_close(out[t], o1[0], "batched copy vs single")
+    _check(layer, x, out, ids, w)
+
+
 def _prefill(layer, x_bits):
     s = layer.shape
     T = x_bits.shape[0]
