@@ -133,12 +133,12 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
     int32_t *const ocounts_p = pin_ptr(a.o_counts);
     uint32_t *const xq_p = pin_ptr(a.xq);
     const int n = pin_i32(a.n), H = pin_i32(a.H), E = pin_i32(a.E), k = pin_i32(a.k);
-    const int zero_out = pin_i32(a.zero_out), sel_logits = pin_i32(a.sel_logits), mt = pin_i32(a.cl_mt);
-    // Plain tokens for a cluster expert kernel (one token, or 2..4 over the distinct
-    // experts): that kernel's work before its own dependency wait reads nothing this
-    // call produces (x is quantised here), so it may be launched at once and be
-    // resident when this grid completes.
-    const bool early_dependents = !NORM && (sel_logits || mt);
+    const int zero_out = pin_i32(a.zero_out), sel_logits = pin_i32(a.sel_logits);
+    // One plain token for the cluster expert kernel (shapes the column-split router does
+    // not take): that kernel's work before its own dependency wait reads nothing this
+    // call produces (x is quantised here), so it may be launched at once and be resident
+    // when this grid completes.
+    const bool early_dependents = !NORM && sel_logits;
     if (early_dependents) pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wpc = blockDim.x >> 5;
@@ -267,11 +267,10 @@ __global__ void __launch_bounds__(NJ > 0 ? 512 : 1024) k_router_topk(DecodeArgs 
             }
         }
     }
-    // Plain tokens for a cluster expert kernel: quantise x per 64-column chunk into
-    // the scratch (int16 pairs, xq = rint(x / s), s = max|x| / 32767; the two
-    // 32-column sums; the four 16-column sums of xq), one warp per chunk, token t at
-    // word t * NC * kXqWords, in the layout the expert kernel copies into its shared
-    // memory as it is.
+    // One plain token for the cluster expert kernel: quantise x per 64-column chunk
+    // into the scratch (int16 pairs, xq = rint(x / s), s = max|x| / 32767; the two
+    // 32-column sums; the four 16-column sums of xq), one warp per chunk, in the
+    // layout the expert kernel copies into its shared memory as it is.
     if (early_dependents) {
         const uint32_t *xw32 = NJ > 0 ? reinterpret_cast<const uint32_t *>(s_x) : reinterpret_cast<const uint32_t *>(xg_p);
         const int NC = H / 64;
