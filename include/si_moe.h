@@ -70,7 +70,7 @@ typedef struct CUstream_st *si_stream_t;
 typedef enum si_status {
     SI_OK = 0,
     SI_ERR_INVALID_ARG = 1,       /* null pointer, bad size, bad mode */
-    SI_ERR_UNSUPPORTED = 2,       /* a shape this build has no kernel for */
+    SI_ERR_UNSUPPORTED = 2,       /* a shape the library has no kernel for */
     SI_ERR_MISALIGNED = 3,        /* a device pointer not 16-byte aligned */
     SI_ERR_SCRATCH_TOO_SMALL = 4, /* scratch_bytes below si_moe_scratch_bytes() */
     SI_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */

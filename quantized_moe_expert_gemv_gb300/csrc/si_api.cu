@@ -244,7 +244,7 @@ si_status si_moe_scratch_init(si_moe_plan_t plan, void *scratch, size_t scratch_
 
 }  // extern "C"
 
-// NVFP4 layers carry their tensor scales (and, in this build, no pre-norm);
+// NVFP4 layers carry their tensor scales (and have no pre-normed variant);
 // Q4_K layers carry none.
 static si_status check_weight_scales(const si_moe_desc &d, const si_moe_layer *layer) {
     if (d.wtype == SI_WTYPE_NVFP4) {
