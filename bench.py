@@ -385,9 +385,13 @@ def bench_layer(args, dist, binding, device, synth, torch, hbm_peak):
     # most this and its achieved bandwidth at least the figure below.  Events
     # recorded between the two kernels (kernels_ms_per_token_events) break that
     # overlap and serialise them; they only show how a token's time splits.
-    dom_name = (("k_router_topk + " + ("k_expert_cluster" if path == 2 else "k_expert") +
+    # The column-split router serves plain single tokens of the cluster kernel
+    # for E in {64, 128} and H in {1024, 2048}; other shapes take k_router_topk.
+    router = ("k_router_one" if path == 2 and shape.n_experts in (64, 128) and shape.hidden in (1024, 2048)
+              else "k_router_topk")
+    dom_name = ((router + " + " + ("k_expert_cluster" if path == 2 else "k_expert") +
                  " (router GEMV + top-k; fused gate/up dequant-GEMV + SwiGLU + down dequant-GEMV + combine)")
-                if fused else "k_router_topk + k_gateup_generic + k_down_generic")
+                if fused else router + " + k_gateup_generic + k_down_generic")
     dom_bytes, dom_ms = expert_bytes, ms_step / T
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic, traffic_note = profiled_traffic("k_expert_cluster") if path == 2 else \
