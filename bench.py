@@ -325,6 +325,38 @@ def time_graph(g, stream, steps, warmup, dist, sampler=None):
     return dist.max(ms), clocks
 
 
+def e2e_per_token(binding, plan, L, x_pin, scratch, stream, shape, dist, torch, n, warmup):
+    """A bs=1 caller without a graph: per token, its 4 KiB x from pinned host
+    memory, one decode call through the C ABI, its 8 KiB output back to pinned
+    host memory, and a wait for that output (the next token depends on it).
+    Host wall time over n tokens, so launch and synchronisation costs count."""
+    x_one = torch.empty((shape.hidden,), dtype=torch.int16, device="cuda")
+    out_one = torch.empty((shape.hidden,), dtype=torch.float32, device="cuda")
+    out_pin = torch.empty((n, shape.hidden), dtype=torch.float32).pin_memory()
+
+    def one(t):
+        with torch.cuda.stream(stream):
+            x_one.copy_(x_pin[t % x_pin.shape[0]], non_blocking=True)
+            binding.si_moe_forward_decode(plan, L, x_one, 1, out_one, None, scratch, stream=stream)
+            out_pin[t % n].copy_(out_one, non_blocking=True)
+        stream.synchronize()
+
+    for t in range(warmup):
+        one(t)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t0 = time.perf_counter()
+    for t in range(n):
+        one(t)
+    wall = dist.max(time.perf_counter() - t0)
+    st = binding.si_moe_read_status(plan, scratch, stream)
+    assert st == binding.SI_OK, binding.si_status_string(st)
+    return {"value": dist.sum(n / wall), "unit": "tok/s", "us_per_token": 1e6 * wall / n, "tokens": n,
+            "h2d_bytes_per_token": shape.hidden * 2, "d2h_bytes_per_token": shape.hidden * 4,
+            "timing": "host wall clock; one decode call (two kernel launches), one copy each way and one "
+                      "stream synchronisation per token, no CUDA graph"}
+
+
 def bench_layer(args, dist, binding, device, synth, torch, hbm_peak):
     wl = synth.WORKLOADS["layer"]
     shape, seed, T = wl["shape"], wl["seed"], (args.tokens or wl["n_tokens"])
@@ -419,6 +451,11 @@ def bench_layer(args, dist, binding, device, synth, torch, hbm_peak):
     e1.synchronize()
     e2e_ms = dist.max(e0.elapsed_time(e1))
     e2e_value = total_tokens / (e2e_ms / 1e3)
+    try:
+        e2e_tok = e2e_per_token(binding, plan, L, x_pin, scratch, stream, shape, dist, torch,
+                                n=min(T, 512), warmup=max(args.warmup, 16))
+    except Exception as exc:  # reported in the line; the headline figures above stand
+        e2e_tok = {"error": repr(exc)}
 
     tok_per_s_rank = T * args.steps / (ms / 1e3)
     chain_gbs = expert_bytes * tok_per_s_rank / 1e9
@@ -454,6 +491,7 @@ def bench_layer(args, dist, binding, device, synth, torch, hbm_peak):
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": T * shape.hidden * 2,
                 "d2h_bytes_per_step": T * shape.hidden * 4},
+        "e2e_per_token": e2e_tok,
         "gpu_launches": (2 if fused else 3) * T * args.steps,
     }
     del g, gi
@@ -787,7 +825,8 @@ def run_ours(args, dist):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "q4k-w x int16-act (per 64 columns) -> fp32 accumulate",
             "data": "synthetic (seeded Q4_K experts, bf16 N(0,1) tokens)"}
-    for k in ("config", "roofline", "kernels_ms_per_token_events", "chain", "clocks", "e2e", "gpu_launches"):
+    for k in ("config", "roofline", "kernels_ms_per_token_events", "chain", "clocks", "e2e", "e2e_per_token",
+              "gpu_launches"):
         line[k] = res[k]
     if not args.no_extras:
         torch.cuda.empty_cache()
