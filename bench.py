@@ -325,36 +325,52 @@ def time_graph(g, stream, steps, warmup, dist, sampler=None):
     return dist.max(ms), clocks
 
 
-def e2e_per_token(binding, plan, L, x_pin, scratch, stream, shape, dist, torch, n, warmup):
-    """A bs=1 caller without a graph: per token, its 4 KiB x from pinned host
-    memory, one decode call through the C ABI, its 8 KiB output back to pinned
-    host memory, and a wait for that output (the next token depends on it).
-    Host wall time over n tokens, so launch and synchronisation costs count."""
+def e2e_per_token(binding, device, plan, L, x_pin, scratch, stream, shape, dist, torch, n, warmup):
+    """A bs=1 caller without a graph, that needs each token's output on the
+    host: per token its 4 KiB x from pinned host memory in, one decode, its
+    8 KiB output back to pinned host memory, and a wait for it.  Timed two
+    ways by the host wall clock over n tokens: through the library's
+    host-buffer entry point (one C call per token: copies, launches, wait and
+    status read inside), and with torch's copies around the device entry
+    point (three Python-level calls and a stream wait per token)."""
     x_one = torch.empty((shape.hidden,), dtype=torch.int16, device="cuda")
     out_one = torch.empty((shape.hidden,), dtype=torch.float32, device="cuda")
     out_pin = torch.empty((n, shape.hidden), dtype=torch.float32).pin_memory()
+    host_scratch = device.alloc_scratch(plan, binding.SI_MODE_DECODE_HOST, 1)
+    rows = x_pin.shape[0]
 
-    def one(t):
+    def via_host_entry(t):
+        binding.si_moe_forward_decode_host(plan, L, x_pin[t % rows], 1, out_pin[t % n], None, host_scratch,
+                                           stream=stream)
+
+    def via_torch_copies(t):
         with torch.cuda.stream(stream):
-            x_one.copy_(x_pin[t % x_pin.shape[0]], non_blocking=True)
+            x_one.copy_(x_pin[t % rows], non_blocking=True)
             binding.si_moe_forward_decode(plan, L, x_one, 1, out_one, None, scratch, stream=stream)
             out_pin[t % n].copy_(out_one, non_blocking=True)
         stream.synchronize()
 
-    for t in range(warmup):
-        one(t)
-    torch.cuda.synchronize()
-    dist.barrier()
-    t0 = time.perf_counter()
-    for t in range(n):
-        one(t)
-    wall = dist.max(time.perf_counter() - t0)
+    def wall(one):
+        for t in range(warmup):
+            one(t)
+        torch.cuda.synchronize()
+        dist.barrier()
+        t0 = time.perf_counter()
+        for t in range(n):
+            one(t)
+        return dist.max(time.perf_counter() - t0)
+
+    w_host = wall(via_host_entry)
+    w_torch = wall(via_torch_copies)
     st = binding.si_moe_read_status(plan, scratch, stream)
     assert st == binding.SI_OK, binding.si_status_string(st)
-    return {"value": dist.sum(n / wall), "unit": "tok/s", "us_per_token": 1e6 * wall / n, "tokens": n,
+    return {"value": dist.sum(n / w_host), "unit": "tok/s", "us_per_token": 1e6 * w_host / n, "tokens": n,
             "h2d_bytes_per_token": shape.hidden * 2, "d2h_bytes_per_token": shape.hidden * 4,
-            "timing": "host wall clock; one decode call (two kernel launches), one copy each way and one "
-                      "stream synchronisation per token, no CUDA graph"}
+            "timing": "host wall clock; per token one si_moe_forward_decode_host call (copy in, two kernel "
+                      "launches, copy out, stream wait, status read), no CUDA graph",
+            "torch_copies": {"value": dist.sum(n / w_torch), "unit": "tok/s", "us_per_token": 1e6 * w_torch / n,
+                             "timing": "per token torch copy in, si_moe_forward_decode, torch copy out, "
+                                       "stream wait"}}
 
 
 def bench_layer(args, dist, binding, device, synth, torch, hbm_peak):
@@ -452,7 +468,7 @@ def bench_layer(args, dist, binding, device, synth, torch, hbm_peak):
     e2e_ms = dist.max(e0.elapsed_time(e1))
     e2e_value = total_tokens / (e2e_ms / 1e3)
     try:
-        e2e_tok = e2e_per_token(binding, plan, L, x_pin, scratch, stream, shape, dist, torch,
+        e2e_tok = e2e_per_token(binding, device, plan, L, x_pin, scratch, stream, shape, dist, torch,
                                 n=min(T, 512), warmup=max(args.warmup, 16))
     except Exception as exc:  # reported in the line; the headline figures above stand
         e2e_tok = {"error": repr(exc)}

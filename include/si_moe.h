@@ -97,6 +97,7 @@ typedef enum si_status {
 #define SI_FLAG_ACT_INT8 1u
 #define SI_MODE_DECODE 0
 #define SI_MODE_PREFILL 1
+#define SI_MODE_DECODE_HOST 2  /* si_moe_forward_decode_host: decode scratch + x and out staging */
 #define SI_MAX_EXPERTS 256
 #define SI_MAX_TOPK 16
 #define SI_MAX_DECODE_TOKENS 4
@@ -125,8 +126,9 @@ si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *o
 void si_moe_plan_destroy(si_moe_plan_t plan);
 
 /* Bytes of caller-allocated device scratch one forward call of `mode`
- * needs for n_tokens tokens (decode: 1..SI_MAX_DECODE_TOKENS; prefill:
- * 1..max_tokens).  A buffer sized for n tokens serves any smaller count. */
+ * needs for n_tokens tokens (SI_MODE_DECODE and SI_MODE_DECODE_HOST:
+ * 1..SI_MAX_DECODE_TOKENS; SI_MODE_PREFILL: 1..max_tokens).  A buffer sized
+ * for n tokens serves any smaller count. */
 si_status si_moe_scratch_bytes(si_moe_plan_t plan, int mode, int32_t n_tokens, size_t *bytes);
 
 /* Zero the scratch control block (status word and arrival counters),
@@ -183,6 +185,25 @@ typedef struct si_moe_route_out {
 si_status si_moe_forward_decode(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,
                                 int32_t n_tokens, float *out, si_moe_route_out *route_out,
                                 void *scratch, size_t scratch_bytes, si_stream_t stream);
+
+/* Decode with x and out in host memory, for a caller that keeps no device
+ * copy of them (a bs=1 generation loop that needs each output on the host
+ * before it forms the next token).  Copies x_bf16_host ([n][H] bf16) into the
+ * scratch, runs the decode of si_moe_forward_decode there, copies the [n][H]
+ * fp32 result into out_host, and waits for the stream: out_host holds the
+ * output when the call returns.  scratch holds
+ * si_moe_scratch_bytes(plan, SI_MODE_DECODE_HOST, n) bytes (the decode scratch
+ * followed by the staging of x and out) and was initialised with
+ * si_moe_scratch_init; route_out, if given, holds device pointers as for
+ * si_moe_forward_decode.  Page-locked host buffers (cudaHostAlloc) let the
+ * copies run asynchronously; pageable ones work, with staged copies.  Because
+ * it waits anyway, the call also reads the device status as
+ * si_moe_read_status does: SI_ERR_TIMEOUT or another device-side error is
+ * returned (and cleared) by the call that observes it.  Argument errors are
+ * returned before anything is queued.  Not usable inside stream capture. */
+si_status si_moe_forward_decode_host(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16_host,
+                                     int32_t n_tokens, float *out_host, si_moe_route_out *route_out,
+                                     void *scratch, size_t scratch_bytes, si_stream_t stream);
 
 /* Grouped prefill (SP⚡RKINFER README, "Benchmark · Qwen3.8-27B", prefill
  * paragraph: Q4_K dequantized into the GEMM operand; sparkinfer-k3 blog post,

@@ -33,6 +33,7 @@ SI_WTYPE_Q5_K = 13
 SI_FLAG_ACT_INT8 = 1
 SI_MODE_DECODE = 0
 SI_MODE_PREFILL = 1
+SI_MODE_DECODE_HOST = 2
 SI_MAX_EXPERTS = 256
 SI_MAX_TOPK = 16
 SI_MAX_DECODE_TOKENS = 4
@@ -92,7 +93,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.si_moe_scratch_bytes.argtypes = [vp, ctypes.c_int, i32, ctypes.POINTER(sz)]
     lib.si_moe_scratch_init.restype = ctypes.c_int
     lib.si_moe_scratch_init.argtypes = [vp, vp, sz, vp]
-    for name in ("si_moe_forward_decode", "si_moe_forward_prefill"):
+    for name in ("si_moe_forward_decode", "si_moe_forward_prefill", "si_moe_forward_decode_host"):
         f = getattr(lib, name)
         f.restype = ctypes.c_int
         f.argtypes = [vp, ctypes.POINTER(si_moe_layer), vp, i32, vp, ctypes.POINTER(si_moe_route_out),
@@ -146,6 +147,8 @@ def _ptr(t) -> Optional[int]:
         return None
     if isinstance(t, int):
         return t
+    if hasattr(t, "__array_interface__"):  # a numpy array in host memory
+        return t.__array_interface__["data"][0]
     return t.data_ptr()
 
 
@@ -247,6 +250,15 @@ def si_moe_forward_prefill(plan, layer: si_moe_layer, x, n_tokens, out, route_ou
                            stream=None, raw_status=False):
     return _forward("si_moe_forward_prefill", plan, layer, x, n_tokens, out, route_out, scratch, stream,
                     raw_status)
+
+
+def si_moe_forward_decode_host(plan, layer: si_moe_layer, x_host, n_tokens, out_host, route_out=None,
+                               scratch=None, stream=None, raw_status=False):
+    """Decode with x and out in host memory (numpy arrays or CPU tensors,
+    page-locked for asynchronous copies); returns once out_host holds the
+    result.  scratch: si_moe_scratch_bytes(plan, SI_MODE_DECODE_HOST, n)."""
+    return _forward("si_moe_forward_decode_host", plan, layer, x_host, n_tokens, out_host, route_out, scratch,
+                    stream, raw_status)
 
 
 def si_moe_forward_decode_noalloc(plan, layer: si_moe_layer, x, n_tokens, out, route_out=None,

@@ -214,12 +214,30 @@ si_status si_moe_plan(const si_moe_desc *desc, int cuda_device, si_moe_plan_t *o
 
 void si_moe_plan_destroy(si_moe_plan_t plan) { delete plan; }
 
+// Scratch of si_moe_forward_decode_host: the decode scratch, then the device
+// copies of x ([n][H] bf16) and of out ([n][H] fp32), each 256-byte aligned.
+struct HostStaging {
+    size_t x, out, total;
+};
+static HostStaging host_staging(const si_moe_desc &d, int n) {
+    HostStaging h{};
+    h.x = si::decode_layout(d, n).total;
+    h.out = align_up(h.x + (size_t)n * d.hidden * sizeof(uint16_t), 256);
+    h.total = align_up(h.out + (size_t)n * d.hidden * sizeof(float), 256);
+    return h;
+}
+
 si_status si_moe_scratch_bytes(si_moe_plan_t plan, int mode, int32_t n_tokens, size_t *bytes) {
     if (!plan || !bytes) return SI_ERR_INVALID_ARG;
     const si_moe_desc &d = plan->p.desc;
     if (mode == SI_MODE_DECODE) {
         if (n_tokens < 1 || n_tokens > SI_MAX_DECODE_TOKENS) return SI_ERR_INVALID_ARG;
         *bytes = si::decode_layout(d, n_tokens).total;
+        return SI_OK;
+    }
+    if (mode == SI_MODE_DECODE_HOST) {
+        if (n_tokens < 1 || n_tokens > SI_MAX_DECODE_TOKENS) return SI_ERR_INVALID_ARG;
+        *bytes = host_staging(d, n_tokens).total;
         return SI_OK;
     }
     if (mode == SI_MODE_PREFILL) {
@@ -337,6 +355,49 @@ si_status si_moe_forward_decode(si_moe_plan_t plan, const si_moe_layer *layer, c
                                 size_t scratch_bytes, si_stream_t stream) {
     return forward_decode_impl(plan, layer, x_bf16, n_tokens, out, ro, scratch, scratch_bytes,
                                nullptr, stream);
+}
+
+si_status si_moe_forward_decode_host(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16_host,
+                                     int32_t n_tokens, float *out_host, si_moe_route_out *ro, void *scratch,
+                                     size_t scratch_bytes, si_stream_t stream) {
+    if (!plan || !x_bf16_host || !out_host || !scratch) return SI_ERR_INVALID_ARG;
+    if (n_tokens < 1 || n_tokens > SI_MAX_DECODE_TOKENS) return SI_ERR_INVALID_ARG;
+    if (!aligned(scratch, 16)) return SI_ERR_MISALIGNED;
+    const si_moe_desc &d = plan->p.desc;
+    const HostStaging hs = host_staging(d, n_tokens);
+    if (scratch_bytes < hs.total) return SI_ERR_SCRATCH_TOO_SMALL;
+    uint8_t *sb = static_cast<uint8_t *>(scratch);
+    void *x_dev = sb + hs.x;
+    float *out_dev = reinterpret_cast<float *>(sb + hs.out);
+    // every argument error before anything is queued
+    const si_status chk = si::check_decode_args(plan, layer, x_dev, n_tokens, out_dev, ro);
+    if (chk != SI_OK) return chk;
+    const cudaStream_t s = (cudaStream_t)stream;
+    const size_t x_bytes = (size_t)n_tokens * d.hidden * sizeof(uint16_t);
+    const size_t out_bytes = (size_t)n_tokens * d.hidden * sizeof(float);
+    if (cudaMemcpyAsync(x_dev, x_bf16_host, x_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        return SI_ERR_CUDA;
+    }
+    const si_status st = forward_decode_impl(plan, layer, x_dev, n_tokens, out_dev, ro, scratch, hs.x,
+                                             nullptr, stream);
+    if (st != SI_OK) return st;
+    // The status word comes back with the output; both land before the wait returns.
+    int32_t word = 0;
+    if (cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return SI_ERR_CUDA;
+    }
+    if (word != 0) {
+        if (cudaMemset(scratch, 0, sizeof(word)) != cudaSuccess) {
+            cudaGetLastError();
+            return SI_ERR_CUDA;
+        }
+        return (si_status)word;
+    }
+    return SI_OK;
 }
 
 si_status si_debug_decode_events(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16,

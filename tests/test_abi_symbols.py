@@ -69,5 +69,7 @@ def test_null_plan_arguments_are_rejected(lib):
         binding.SI_ERR_INVALID_ARG
     assert lib.si_moe_forward_prefill(None, None, None, 1, None, None, None, 0, None) == \
         binding.SI_ERR_INVALID_ARG
+    assert lib.si_moe_forward_decode_host(None, None, None, 1, None, None, None, 0, None) == \
+        binding.SI_ERR_INVALID_ARG
     assert lib.si_debug_q4k_dequant(None, 1, None, None, None) == binding.SI_ERR_INVALID_ARG
     assert lib.si_debug_q4k_dequant(16, 1, 17, None, None) == binding.SI_ERR_MISALIGNED

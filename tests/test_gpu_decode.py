@@ -296,6 +296,66 @@ def test_decode_argument_errors():
     assert binding.si_moe_read_status(r.plan, r.scratch) == binding.SI_OK
 
 
+@pytest.mark.parametrize("workload,n", [("tiny", 1), ("layer", 1), ("dedup4", 4)])
+def test_decode_host_buffers_match_the_oracle(workload, n):
+    """si_moe_forward_decode_host: x from page-locked host memory, out back to
+    it, the stream wait and the status read inside the call; then the same
+    with pageable numpy buffers."""
+    wl = synth.WORKLOADS[workload]
+    shape, seed = wl["shape"], wl["seed"]
+    bias = synth.dedup_router_bias(seed, synth.load_dedup_beta()) if workload == "dedup4" else None
+    layer = synth.make_layer(shape, seed=seed, router_bias=bias)
+    x = synth.make_tokens(shape, seed, 3 * n)
+    dl = device.to_device(layer)
+    plan = binding.si_moe_plan(device.desc_for(shape))
+    scratch = device.alloc_scratch(plan, binding.SI_MODE_DECODE_HOST, n)
+    x_pin = torch.from_numpy(x.view(np.int16)).pin_memory()
+    out_pin = torch.empty((n, shape.hidden), dtype=torch.float32).pin_memory()
+    ids = torch.full((n, shape.top_k), -1, dtype=torch.int32, device="cuda")
+    w = torch.empty((n, shape.top_k), dtype=torch.float32, device="cuda")
+    ro = binding.route_struct(topk_ids=ids, topk_w=w)
+    for step in range(3):
+        out_pin.fill_(float("nan"))
+        st = binding.si_moe_forward_decode_host(plan, dl.struct(), x_pin[step * n:(step + 1) * n], n, out_pin,
+                                                ro, scratch)
+        assert st == binding.SI_OK
+        xs = x[step * n:(step + 1) * n]
+        near = check_tokens(layer, xs, out_pin.numpy().copy(), ids.cpu().numpy(), w.cpu().numpy())
+        assert near <= 1
+    out_np = np.full((1, shape.hidden), np.nan, dtype=np.float32)
+    x_np = np.ascontiguousarray(x[1:2])
+    assert binding.si_moe_forward_decode_host(plan, dl.struct(), x_np, 1, out_np, ro, scratch) == binding.SI_OK
+    check_tokens(layer, x_np, out_np, ids.cpu().numpy()[:1], w.cpu().numpy()[:1])
+
+
+def test_decode_host_buffers_argument_errors_and_timeout(monkeypatch):
+    shape = synth.TINY
+    layer = synth.make_layer(shape, seed=0)
+    dl = device.to_device(layer)
+    x = synth.make_tokens(shape, 0, 1)
+    out = np.full((1, shape.hidden), np.nan, dtype=np.float32)
+    plan = binding.si_moe_plan(device.desc_for(shape))
+    small = device.alloc_scratch(plan, binding.SI_MODE_DECODE, 1)  # no room for the staging of x and out
+    st = binding.si_moe_forward_decode_host(plan, dl.struct(), x, 1, out, None, small, raw_status=True)
+    assert st == binding.SI_ERR_SCRATCH_TOO_SMALL and np.isnan(out).all()
+    scratch = device.alloc_scratch(plan, binding.SI_MODE_DECODE_HOST, 1)
+    assert binding.si_moe_forward_decode_host(plan, dl.struct(), None, 1, out, None, scratch,
+                                              raw_status=True) == binding.SI_ERR_INVALID_ARG
+    assert binding.si_moe_forward_decode_host(plan, dl.struct(), x, 5, out, None, scratch,
+                                              raw_status=True) == binding.SI_ERR_INVALID_ARG
+    assert np.isnan(out).all()
+    # a wait that runs out is returned by the call itself, and cleared
+    monkeypatch.setenv("SI_FAULT_WAIT_BUDGET", "0")
+    plan0 = binding.si_moe_plan(device.desc_for(shape))
+    monkeypatch.delenv("SI_FAULT_WAIT_BUDGET")
+    assert binding.si_moe_forward_decode_host(plan0, dl.struct(), x, 1, out, None, scratch,
+                                              raw_status=True) == binding.SI_ERR_TIMEOUT
+    assert binding.si_moe_read_status(plan0, scratch) == binding.SI_OK
+    binding.si_moe_scratch_init(plan, scratch)
+    assert binding.si_moe_forward_decode_host(plan, dl.struct(), x, 1, out, None, scratch) == binding.SI_OK
+    parity.assert_close(out[0], oracle.moe_token(layer, x[0]).out64, "host buffers after a timeout")
+
+
 def test_decode_in_cuda_graph_matches_eager():
     wl = synth.WORKLOADS["layer"]
     shape = wl["shape"]
