@@ -1,6 +1,7 @@
 // si_api.cu -- the C ABI (include/si_moe.h): plans, validation, scratch
 // layout and stream-ordered launches.  Nothing here allocates device memory
-// or synchronises, except si_moe_read_status (which is documented to).
+// or synchronises, except si_moe_read_status and si_moe_forward_decode_host
+// (which are documented to).
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
