@@ -330,9 +330,10 @@ def e2e_per_token(binding, device, plan, L, x_pin, scratch, stream, shape, dist,
     host: per token its 4 KiB x from pinned host memory in, one decode, its
     8 KiB output back to pinned host memory, and a wait for it.  Timed two
     ways by the host wall clock over n tokens: through the library's
-    host-buffer entry point (one C call per token: copies, launches, wait and
-    status read inside), and with torch's copies around the device entry
-    point (three Python-level calls and a stream wait per token)."""
+    host-buffer entry point (one C call per token: one replay of a graph
+    holding the copies and the two kernels, the wait and the status read),
+    and with torch's copies around the device entry point (three
+    Python-level calls and a stream wait per token)."""
     x_one = torch.empty((shape.hidden,), dtype=torch.int16, device="cuda")
     out_one = torch.empty((shape.hidden,), dtype=torch.float32, device="cuda")
     out_pin = torch.empty((n, shape.hidden), dtype=torch.float32).pin_memory()
@@ -366,8 +367,8 @@ def e2e_per_token(binding, device, plan, L, x_pin, scratch, stream, shape, dist,
     assert st == binding.SI_OK, binding.si_status_string(st)
     return {"value": dist.sum(n / w_host), "unit": "tok/s", "us_per_token": 1e6 * w_host / n, "tokens": n,
             "h2d_bytes_per_token": shape.hidden * 2, "d2h_bytes_per_token": shape.hidden * 4,
-            "timing": "host wall clock; per token one si_moe_forward_decode_host call (copy in, two kernel "
-                      "launches, copy out, stream wait, status read), no CUDA graph",
+            "timing": "host wall clock; per token one si_moe_forward_decode_host call (one replay of its "
+                      "captured graph: copy in, two kernels, copy out; stream wait, status read)",
             "torch_copies": {"value": dist.sum(n / w_torch), "unit": "tok/s", "us_per_token": 1e6 * w_torch / n,
                              "timing": "per token torch copy in, si_moe_forward_decode, torch copy out, "
                                        "stream wait"}}

@@ -188,16 +188,19 @@ si_status si_moe_forward_decode(si_moe_plan_t plan, const si_moe_layer *layer, c
 
 /* Decode with x and out in host memory, for a caller that keeps no device
  * copy of them (a bs=1 generation loop that needs each output on the host
- * before it forms the next token).  Copies x_bf16_host ([n][H] bf16) into the
- * scratch, runs the decode of si_moe_forward_decode there, copies the [n][H]
- * fp32 result into out_host, and waits for the stream: out_host holds the
- * output when the call returns.  scratch holds
+ * before it forms the next token).  x_bf16_host: [n][H] bf16; out_host:
+ * [n][H] fp32; any host memory.  The call copies x into page-locked staging,
+ * launches one CUDA graph on `stream` (the copy into the scratch, the decode
+ * of si_moe_forward_decode, the copies of the result and of the device status
+ * back into staging), waits for it, and copies the result into out_host:
+ * out_host holds the output when the call returns.  The graph is captured on
+ * the first call for a given (layer, route_out, scratch, n) and kept with the
+ * plan (the four most recent; freed by si_moe_plan_destroy, with their
+ * page-locked staging); the plan serialises these calls.  scratch holds
  * si_moe_scratch_bytes(plan, SI_MODE_DECODE_HOST, n) bytes (the decode scratch
- * followed by the staging of x and out) and was initialised with
+ * followed by device copies of x and out) and was initialised with
  * si_moe_scratch_init; route_out, if given, holds device pointers as for
- * si_moe_forward_decode.  Page-locked host buffers (cudaHostAlloc) let the
- * copies run asynchronously; pageable ones work, with staged copies.  Because
- * it waits anyway, the call also reads the device status as
+ * si_moe_forward_decode.  The call reads the device status as
  * si_moe_read_status does: SI_ERR_TIMEOUT or another device-side error is
  * returned (and cleared) by the call that observes it.  Argument errors are
  * returned before anything is queued.  Not usable inside stream capture. */

@@ -254,9 +254,9 @@ def si_moe_forward_prefill(plan, layer: si_moe_layer, x, n_tokens, out, route_ou
 
 def si_moe_forward_decode_host(plan, layer: si_moe_layer, x_host, n_tokens, out_host, route_out=None,
                                scratch=None, stream=None, raw_status=False):
-    """Decode with x and out in host memory (numpy arrays or CPU tensors,
-    page-locked for asynchronous copies); returns once out_host holds the
-    result.  scratch: si_moe_scratch_bytes(plan, SI_MODE_DECODE_HOST, n)."""
+    """Decode with x and out in host memory (numpy arrays or CPU tensors);
+    returns once out_host holds the result.  scratch:
+    si_moe_scratch_bytes(plan, SI_MODE_DECODE_HOST, n)."""
     return _forward("si_moe_forward_decode_host", plan, layer, x_host, n_tokens, out_host, route_out, scratch,
                     stream, raw_status)
 

@@ -5,7 +5,9 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <vector>
 
 #include "si_internal.h"
 
@@ -13,8 +15,33 @@ using si::DecodeArgs;
 using si::DecodeLayout;
 using si::Plan;
 
+// One captured host-buffer decode (si_moe_forward_decode_host): the copy of x
+// from a page-locked staging buffer into the scratch, the decode's launches,
+// and the copies of out and of the status word back into page-locked staging.
+// Its key is everything the captured launches bake in.
+struct HostGraph {
+    si_moe_layer layer{};
+    si_moe_route_out ro{};
+    bool has_ro = false;
+    void *scratch = nullptr;
+    int n = 0;
+    cudaGraphExec_t exec = nullptr;
+    uint8_t *x_pin = nullptr;    // [n][H] bf16
+    uint8_t *out_pin = nullptr;  // [n][H] fp32, then the status word
+};
+
 struct si_moe_plan_s {
     Plan p;
+    std::mutex host_mu;                  // serialises the host-buffer calls on this plan
+    std::vector<HostGraph> host_graphs;  // least recently used first
+    ~si_moe_plan_s() {
+        for (HostGraph &g : host_graphs) {
+            if (g.exec) cudaGraphExecDestroy(g.exec);
+            if (g.x_pin) cudaFreeHost(g.x_pin);
+            if (g.out_pin) cudaFreeHost(g.out_pin);
+        }
+        cudaGetLastError();
+    }
 };
 
 namespace {
@@ -358,6 +385,64 @@ si_status si_moe_forward_decode(si_moe_plan_t plan, const si_moe_layer *layer, c
                                nullptr, stream);
 }
 
+constexpr size_t kHostGraphs = 4;  // captured host-buffer decodes kept per plan
+
+static bool same_host_key(const HostGraph &g, const si_moe_layer *layer, const si_moe_route_out *ro,
+                          void *scratch, int n) {
+    return g.n == n && g.scratch == scratch && std::memcmp(&g.layer, layer, sizeof(si_moe_layer)) == 0 &&
+           g.has_ro == (ro != nullptr) && (!ro || std::memcmp(&g.ro, ro, sizeof(si_moe_route_out)) == 0);
+}
+
+static void free_host_graph(HostGraph &g) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.x_pin) cudaFreeHost(g.x_pin);
+    if (g.out_pin) cudaFreeHost(g.out_pin);
+    g = HostGraph{};
+    cudaGetLastError();
+}
+
+// Capture one host-buffer decode on a private stream and instantiate it.
+static si_status build_host_graph(si_moe_plan_t plan, HostGraph &g) {
+    const si_moe_desc &d = plan->p.desc;
+    const HostStaging hs = host_staging(d, g.n);
+    const size_t x_bytes = (size_t)g.n * d.hidden * sizeof(uint16_t);
+    const size_t out_bytes = (size_t)g.n * d.hidden * sizeof(float);
+    uint8_t *sb = static_cast<uint8_t *>(g.scratch);
+    if (cudaHostAlloc(reinterpret_cast<void **>(&g.x_pin), x_bytes, cudaHostAllocDefault) != cudaSuccess ||
+        cudaHostAlloc(reinterpret_cast<void **>(&g.out_pin), out_bytes + sizeof(int32_t), cudaHostAllocDefault) !=
+            cudaSuccess) {
+        free_host_graph(g);
+        return SI_ERR_CUDA;
+    }
+    cudaStream_t cs = nullptr;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+        free_host_graph(g);
+        return SI_ERR_CUDA;
+    }
+    si_status st = SI_OK;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        st = SI_ERR_CUDA;
+    } else {
+        if (cudaMemcpyAsync(sb + hs.x, g.x_pin, x_bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess) st = SI_ERR_CUDA;
+        if (st == SI_OK)
+            st = forward_decode_impl(plan, &g.layer, sb + hs.x, g.n, reinterpret_cast<float *>(sb + hs.out),
+                                     g.has_ro ? &g.ro : nullptr, g.scratch, hs.x, nullptr, cs);
+        if (st == SI_OK &&
+            (cudaMemcpyAsync(g.out_pin, sb + hs.out, out_bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+             cudaMemcpyAsync(g.out_pin + out_bytes, g.scratch, sizeof(int32_t), cudaMemcpyDeviceToHost, cs) !=
+                 cudaSuccess))
+            st = SI_ERR_CUDA;
+        cudaGraph_t graph = nullptr;  // the capture is ended whatever happened inside it
+        if (cudaStreamEndCapture(cs, &graph) != cudaSuccess && st == SI_OK) st = SI_ERR_CUDA;
+        if (st == SI_OK && cudaGraphInstantiate(&g.exec, graph, 0) != cudaSuccess) st = SI_ERR_CUDA;
+        if (graph) cudaGraphDestroy(graph);
+    }
+    cudaStreamDestroy(cs);
+    if (st != SI_OK) free_host_graph(g);
+    cudaGetLastError();
+    return st;
+}
+
 si_status si_moe_forward_decode_host(si_moe_plan_t plan, const si_moe_layer *layer, const void *x_bf16_host,
                                      int32_t n_tokens, float *out_host, si_moe_route_out *ro, void *scratch,
                                      size_t scratch_bytes, si_stream_t stream) {
@@ -368,31 +453,51 @@ si_status si_moe_forward_decode_host(si_moe_plan_t plan, const si_moe_layer *lay
     const HostStaging hs = host_staging(d, n_tokens);
     if (scratch_bytes < hs.total) return SI_ERR_SCRATCH_TOO_SMALL;
     uint8_t *sb = static_cast<uint8_t *>(scratch);
-    void *x_dev = sb + hs.x;
-    float *out_dev = reinterpret_cast<float *>(sb + hs.out);
     // every argument error before anything is queued
-    const si_status chk = si::check_decode_args(plan, layer, x_dev, n_tokens, out_dev, ro);
+    const si_status chk = si::check_decode_args(plan, layer, sb + hs.x, n_tokens,
+                                                reinterpret_cast<const float *>(sb + hs.out), ro);
     if (chk != SI_OK) return chk;
-    const cudaStream_t s = (cudaStream_t)stream;
     const size_t x_bytes = (size_t)n_tokens * d.hidden * sizeof(uint16_t);
     const size_t out_bytes = (size_t)n_tokens * d.hidden * sizeof(float);
-    if (cudaMemcpyAsync(x_dev, x_bf16_host, x_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+
+    std::lock_guard<std::mutex> lock(plan->host_mu);
+    std::vector<HostGraph> &cache = plan->host_graphs;
+    size_t at = cache.size();
+    for (size_t i = 0; i < cache.size(); ++i)
+        if (same_host_key(cache[i], layer, ro, scratch, n_tokens)) at = i;
+    if (at == cache.size()) {  // first call with this layer, scratch and token count
+        HostGraph g{};
+        g.layer = *layer;
+        if (ro) g.ro = *ro;
+        g.has_ro = ro != nullptr;
+        g.scratch = scratch;
+        g.n = n_tokens;
+        const si_status st = build_host_graph(plan, g);
+        if (st != SI_OK) return st;
+        if (cache.size() == kHostGraphs) {
+            free_host_graph(cache.front());
+            cache.erase(cache.begin());
+        }
+        cache.push_back(g);
+        at = cache.size() - 1;
+    } else if (at + 1 != cache.size()) {  // most recently used last
+        const HostGraph g = cache[at];
+        cache.erase(cache.begin() + (long)at);
+        cache.push_back(g);
+        at = cache.size() - 1;
+    }
+    HostGraph &g = cache[at];
+    std::memcpy(g.x_pin, x_bf16_host, x_bytes);
+    if (cudaGraphLaunch(g.exec, (cudaStream_t)stream) != cudaSuccess ||
+        cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) {
         cudaGetLastError();
         return SI_ERR_CUDA;
     }
-    const si_status st = forward_decode_impl(plan, layer, x_dev, n_tokens, out_dev, ro, scratch, hs.x,
-                                             nullptr, stream);
-    if (st != SI_OK) return st;
-    // The status word comes back with the output; both land before the wait returns.
+    std::memcpy(out_host, g.out_pin, out_bytes);
     int32_t word = 0;
-    if (cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemcpyAsync(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess) {
-        cudaGetLastError();
-        return SI_ERR_CUDA;
-    }
-    if (word != 0) {
-        if (cudaMemset(scratch, 0, sizeof(word)) != cudaSuccess) {
+    std::memcpy(&word, g.out_pin + out_bytes, sizeof(word));
+    if (word != 0) {  // reported once, as si_moe_read_status does
+        if (cudaMemsetAsync(scratch, 0, sizeof(word), (cudaStream_t)stream) != cudaSuccess) {
             cudaGetLastError();
             return SI_ERR_CUDA;
         }

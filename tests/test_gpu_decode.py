@@ -328,6 +328,33 @@ def test_decode_host_buffers_match_the_oracle(workload, n):
     check_tokens(layer, x_np, out_np, ids.cpu().numpy()[:1], w.cpu().numpy()[:1])
 
 
+def test_decode_host_buffers_graph_cache_reuse_and_eviction():
+    """The host-buffer call keeps a captured graph per (layer, route_out,
+    scratch, n), at most four per plan: six scratch buffers in rotation make
+    every call after the fourth evict and capture again, and a repeated key
+    replays its graph with new host inputs."""
+    shape = synth.TINY
+    layer = synth.make_layer(shape, seed=0)
+    dl = device.to_device(layer)
+    x = synth.make_tokens(shape, 5, 12)
+    plan = binding.si_moe_plan(device.desc_for(shape))
+    scratches = [device.alloc_scratch(plan, binding.SI_MODE_DECODE_HOST, 2) for _ in range(6)]
+    refs = [oracle.moe_token(layer, x[t]).out64 for t in range(x.shape[0])]
+    for rep in range(2):
+        for i, sc in enumerate(scratches):
+            t = (2 * i + rep) % x.shape[0]
+            out = np.full((1, shape.hidden), np.nan, dtype=np.float32)
+            assert binding.si_moe_forward_decode_host(plan, dl.struct(), x[t:t + 1], 1, out, None, sc) == \
+                binding.SI_OK
+            parity.assert_close(out[0], refs[t], f"scratch {i}, token {t}")
+    sc = scratches[0]
+    for t in range(0, x.shape[0], 2):  # one key, new inputs every call, two tokens
+        out = np.full((2, shape.hidden), np.nan, dtype=np.float32)
+        assert binding.si_moe_forward_decode_host(plan, dl.struct(), x[t:t + 2], 2, out, None, sc) == binding.SI_OK
+        for j in range(2):
+            parity.assert_close(out[j], refs[t + j], f"token {t + j}")
+
+
 def test_decode_host_buffers_argument_errors_and_timeout(monkeypatch):
     shape = synth.TINY
     layer = synth.make_layer(shape, seed=0)
