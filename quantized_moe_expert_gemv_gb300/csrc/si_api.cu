@@ -387,10 +387,20 @@ si_status si_moe_forward_decode(si_moe_plan_t plan, const si_moe_layer *layer, c
 
 constexpr size_t kHostGraphs = 4;  // captured host-buffer decodes kept per plan
 
+// Field by field: a caller's struct may hold anything in its padding.
 static bool same_host_key(const HostGraph &g, const si_moe_layer *layer, const si_moe_route_out *ro,
                           void *scratch, int n) {
-    return g.n == n && g.scratch == scratch && std::memcmp(&g.layer, layer, sizeof(si_moe_layer)) == 0 &&
-           g.has_ro == (ro != nullptr) && (!ro || std::memcmp(&g.ro, ro, sizeof(si_moe_route_out)) == 0);
+    const si_moe_layer &a = g.layer;
+    const bool same_layer = a.w_gate == layer->w_gate && a.w_up == layer->w_up && a.w_down == layer->w_down &&
+                            a.router_w == layer->router_w && a.router_bias == layer->router_bias &&
+                            a.norm_weight == layer->norm_weight && a.w_scale == layer->w_scale &&
+                            (!a.norm_weight || std::memcmp(&a.norm_eps, &layer->norm_eps, sizeof(float)) == 0);
+    const bool same_ro = g.has_ro == (ro != nullptr) &&
+                         (!ro || (g.ro.topk_ids == ro->topk_ids && g.ro.topk_w == ro->topk_w &&
+                                  g.ro.expert_counts == ro->expert_counts &&
+                                  g.ro.expert_offsets == ro->expert_offsets && g.ro.perm == ro->perm &&
+                                  g.ro.logits == ro->logits));
+    return g.n == n && g.scratch == scratch && same_layer && same_ro;
 }
 
 static void free_host_graph(HostGraph &g) {
