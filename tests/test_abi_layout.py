@@ -48,3 +48,27 @@ def test_binding_structs_match_the_c_header(tmp_path):
         assert c[(name, "size")] == ctypes.sizeof(cls), name
         for field, _ in cls._fields_:
             assert c[(name, field)] == getattr(cls, field).offset, (name, field)
+
+
+def test_binding_constants_match_the_c_header(tmp_path):
+    """Every SI_* constant the header defines (status codes, weight types,
+    flags, modes, limits) has the same value in the binding: a small C program
+    built against include/si_moe.h prints them."""
+    import re
+    with open(os.path.join(ROOT, "include", "si_moe.h")) as f:
+        text = f.read()
+    names = sorted(set(re.findall(r"^#define (SI_[A-Z0-9_]+) ", text, flags=re.M)) |
+                   set(re.findall(r"^\s+(SI_(?:OK|ERR_[A-Z_]+)) =", text, flags=re.M)))
+    assert {"SI_OK", "SI_ERR_RANGE", "SI_MODE_DECODE_HOST", "SI_STATIC_SCRATCH_BYTES"} <= set(names)
+    lines = ['#include <stdio.h>', '#include "si_moe.h"', "int main(void) {"]
+    lines += [f'    printf("{n} %lld\\n", (long long)({n}));' for n in names]
+    lines += ["    return 0;", "}"]
+    src = tmp_path / "consts.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "consts"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    got = dict((k, int(v)) for k, v in (line.split() for line in out.splitlines()))
+    for n in names:
+        assert hasattr(binding, n), f"binding lacks {n}"
+        assert getattr(binding, n) == got[n], n
