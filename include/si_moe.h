@@ -23,7 +23,10 @@
  *  - Ownership: the caller owns every device buffer and the stream.  The
  *    library never allocates or frees device memory, never synchronises
  *    inside a forward call, and its forward calls can be captured in a CUDA
- *    graph.  A plan owns host memory only.
+ *    graph; the one exception is si_moe_forward_decode_host, which takes
+ *    host buffers and waits for its result.  A plan owns host memory only
+ *    (for si_moe_forward_decode_host also its captured graphs and their
+ *    page-locked staging).
  *  - Device pointers must be 16-byte aligned (SI_ERR_MISALIGNED otherwise).
  *  - Errors: no call throws.  Argument errors are reported before any
  *    launch.  A failed launch returns SI_ERR_CUDA.  Faults found on the
